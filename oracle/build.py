@@ -1,0 +1,34 @@
+"""Compile the CPU oracle (test infrastructure) into oracle/_build/libdt_oracle.so.
+
+Plain gcc, no vendor toolchain.  -ffp-contract=off keeps every fp32 multiply and
+add separately rounded on both x86-64 and aarch64 (gcc contracts a*b+c into an
+fma by default on aarch64), so the oracle's fp32 decisions are reproducible.
+"""
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "dt_oracle.c")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(OUT_DIR, "libdt_oracle.so")
+
+CFLAGS = ["-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off",
+          "-fno-fast-math", "-fexcess-precision=standard", "-Wall"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle if its library is missing or older than its source."""
+    if (not force and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+        return LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    tmp = LIB + ".tmp%d" % os.getpid()
+    cmd = ["gcc", *CFLAGS, "-o", tmp, SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv))

@@ -1,0 +1,777 @@
+/*
+ * dt_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU restatement of draft-tree build and tree
+ * verification for block (diffusion) drafters.  It exists to check the CUDA
+ * path and to serve as the timed CPU baseline; nothing in the product path may
+ * call it.  It shares no code, header, table or helper with the CUDA sources.
+ *
+ * Every function follows one passage of the pages it restates; the page is
+ * named by its title and the section, equation or algorithm it falls in:
+ *
+ *   [DARTree]  "DARTree: Speculative Diffusion Decoding With Autoregressive
+ *              Draft Trees" (papercache.org summary).
+ *   [TALON]    "TALON: Confidence-Aware Speculative Decoding with Adaptive
+ *              Token Trees" (papernotes.org notes).
+ *   [Unit11]   "Sampling, speculative decoding and multi-token prediction"
+ *              (formulas-to-systems course, unit 11).
+ *   [DDTree]   "DDTree algorithm: efficient inference-tree construction"
+ *              (CSDN explainer of DDTree).
+ *
+ * Precision.  The log-normaliser is accumulated in double and rounded once to
+ * fp32.  Every quantity that decides an integer result (a tree, an accepted
+ * path) is computed in fp32 in a fixed order, because the CUDA path takes those
+ * decisions in fp32 too: path scores are added left to right from the root's
+ * 0, the DARTree Markov term is a serial fmaf chain from 0.0f, and the T=1
+ * acceptance ratio and residual weights use exp_canon (below).  Build with
+ * -ffp-contract=off so that no multiply-add is fused behind our back.
+ *
+ * Parity status of each function is listed in its header comment.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_MAXL 32
+
+enum { OR_OK = 0, OR_EINVAL = -1, OR_ENOMEM = -2, OR_EBADTREE = -5 };
+
+/* ------------------------------------------------------------------------- */
+/* exp_canon: fp32 exponential by Cody and Waite's argument reduction          */
+/* (W. J. Cody, W. Waite, "Software Manual for the Elementary Functions",      */
+/* 1980): x = k ln2 + r with ln 2 split into a head whose product with k is    */
+/* exact and a tail, then e^r by its Taylor series to degree 7 in Horner form, */
+/* then scaling by 2^k.  Every step is one correctly rounded fp32 operation,   */
+/* so any IEEE machine with a true fma produces the same bits.                 */
+/* Range: returns 0 for x < -86 (results below 2^-124) and +inf for x > 88.5.  */
+/* Pinned: ulp error against double exp, monotonicity (tests).                 */
+/* ------------------------------------------------------------------------- */
+static float or_pow2i(int k) /* 2^k for -126 <= k <= 127, built from its bits */
+{
+    union { uint32_t u; float f; } v;
+    v.u = (uint32_t)(k + 127) << 23;
+    return v.f;
+}
+
+float or_exp_canon(float x)
+{
+    const float log2e = 1.44269504088896340736f;
+    const float ln2_hi = 0.693145751953125f;        /* 16 significant bits */
+    const float ln2_lo = 1.42860682030941723212e-6f; /* ln2 - ln2_hi */
+    if (x != x) return x;
+    if (x > 88.5f) return INFINITY;
+    if (x < -86.0f) return 0.0f;
+    float t = x * log2e;
+    float kf = rintf(t);
+    int k = (int)kf;
+    float r = fmaf(-kf, ln2_hi, x);
+    r = fmaf(-kf, ln2_lo, r);
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return p * or_pow2i(k);
+}
+
+void or_exp_canon_vec(const float* x, int64_t n, float* y)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = or_exp_canon(x[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Stage 1: per-position log-softmax and Top-Kc candidate list.                */
+/* [DARTree] Algorithm 1, line 4 (C_d = TopK(L_d^base, K)); [DDTree] section   */
+/* 3.3 (scores are log-probabilities of the per-position Top-K tokens).        */
+/* Rank order: logit descending, token id ascending on equal logits.           */
+/* lse = max + log(sum exp(x - max)) in double, rounded once to fp32;          */
+/* lp = x - lse in fp32.                                                       */
+/* Pinned: closed forms (uniform row, shift invariance), sum of exp(lp) = 1,   */
+/* brute-force sort in the tests.                                              */
+/* ------------------------------------------------------------------------- */
+typedef struct { float v; int32_t id; } or_vi;
+
+static int or_cmp_vi(const void* pa, const void* pb)
+{
+    const or_vi* a = (const or_vi*)pa;
+    const or_vi* b = (const or_vi*)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id);
+}
+
+int or_candidates(const float* x, int64_t rows, int32_t V, int32_t Kc,
+                  double* lse64, float* lse32, int32_t* ids, float* lps)
+{
+    if (V < 1 || Kc < 1 || Kc > V) return OR_EINVAL;
+    or_vi* buf = (or_vi*)malloc((size_t)V * sizeof(or_vi));
+    if (!buf) return OR_ENOMEM;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* row = x + r * (int64_t)V;
+        double m = -INFINITY;
+        for (int32_t v = 0; v < V; ++v)
+            if ((double)row[v] > m) m = (double)row[v];
+        double s = 0.0;
+        if (m != -INFINITY)
+            for (int32_t v = 0; v < V; ++v) s += exp((double)row[v] - m);
+        double l = (m == -INFINITY) ? m : m + log(s);
+        float l32 = (float)l;
+        if (lse64) lse64[r] = l;
+        lse32[r] = l32;
+        for (int32_t v = 0; v < V; ++v) { buf[v].v = row[v]; buf[v].id = v; }
+        qsort(buf, (size_t)V, sizeof(or_vi), or_cmp_vi);
+        for (int32_t k = 0; k < Kc; ++k) {
+            float lp = buf[k].v - l32;
+            ids[r * Kc + k] = buf[k].id;
+            lps[r * Kc + k] = lp;
+        }
+    }
+    free(buf);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Total order on tree nodes shared by all selections below: higher score      */
+/* first; on equal scores, the lexicographically smaller rank descriptor       */
+/* (0-based per-position ranks), a proper prefix before its extensions.        */
+/* [DARTree] Lemma 1 ("ancestors first on ties"); [DDTree] section 3.3 (heap   */
+/* of (-score, rho) tuples orders equal scores by the descriptor tuple).       */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    float s;               /* path score */
+    int32_t d;             /* depth (1-based position of the last token) */
+    int32_t r[OR_MAXL];    /* rank descriptor rho_1..rho_d, 0-based */
+    int32_t tok;           /* token of the last position */
+    int32_t parent;        /* index of the parent in the caller's node list */
+    int32_t self;          /* caller-side index */
+} or_node;
+
+static int or_lex_less(const int32_t* a, int da, const int32_t* b, int db)
+{
+    int n = da < db ? da : db;
+    for (int i = 0; i < n; ++i)
+        if (a[i] != b[i]) return a[i] < b[i];
+    return da < db;
+}
+
+static int or_before(const or_node* a, const or_node* b)
+{
+    if (a->s > b->s) return 1;
+    if (a->s < b->s) return 0;
+    return or_lex_less(a->r, a->d, b->r, b->d);
+}
+
+static int or_cmp_node(const void* pa, const void* pb)
+{
+    const or_node* a = (const or_node*)pa;
+    const or_node* b = (const or_node*)pb;
+    if (or_before(a, b)) return -1;
+    if (or_before(b, a)) return 1;
+    return 0;
+}
+
+/* A plain binary max-heap under or_before. */
+typedef struct { or_node* a; int n, cap; } or_heap;
+
+static int or_heap_push(or_heap* h, const or_node* x)
+{
+    if (h->n == h->cap) {
+        int nc = h->cap ? 2 * h->cap : 64;
+        or_node* na = (or_node*)realloc(h->a, (size_t)nc * sizeof(or_node));
+        if (!na) return OR_ENOMEM;
+        h->a = na; h->cap = nc;
+    }
+    int i = h->n++;
+    h->a[i] = *x;
+    while (i > 0) {
+        int p = (i - 1) / 2;
+        if (!or_before(&h->a[i], &h->a[p])) break;
+        or_node t = h->a[i]; h->a[i] = h->a[p]; h->a[p] = t;
+        i = p;
+    }
+    return OR_OK;
+}
+
+static or_node or_heap_pop(or_heap* h)
+{
+    or_node top = h->a[0];
+    h->a[0] = h->a[--h->n];
+    int i = 0;
+    for (;;) {
+        int l = 2 * i + 1, r = l + 1, b = i;
+        if (l < h->n && or_before(&h->a[l], &h->a[b])) b = l;
+        if (r < h->n && or_before(&h->a[r], &h->a[b])) b = r;
+        if (b == i) break;
+        or_node t = h->a[i]; h->a[i] = h->a[b]; h->a[b] = t;
+        i = b;
+    }
+    return top;
+}
+
+/* Tree output arrays, node 0 = root (token -1, parent -1, depth 0, rank -1,
+ * score 0). */
+typedef struct {
+    int32_t* tok; int32_t* parent; int32_t* depth; int32_t* rank; float* score;
+} or_tree_out;
+
+static void or_put_root(or_tree_out* o)
+{
+    o->tok[0] = -1; o->parent[0] = -1; o->depth[0] = 0; o->rank[0] = -1;
+    o->score[0] = 0.0f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* DDTree Top-B by the best-first heap over rank descriptors.                  */
+/* [DDTree] section 3.1 (Algorithm 1: start from (1), pop the best descriptor, */
+/* add it to the tree, push its first child and its next sibling, stop at B    */
+/* nodes), section 3.3 (log-domain scores, first child only below the depth    */
+/* cap, next sibling only while rho_d < K); [DARTree] "Tree verification and   */
+/* DDTree" (heap best-first, O(B log B)).                                      */
+/*                                                                             */
+/* The printed successor rule pushes the first child only when rho_d is the   */
+/* top rank, which leaves (2,1) unreachable, against the same section's claim  */
+/* that every prefix of S_K is reached through pred().  rule = 0 (the reading  */
+/* used everywhere) pushes the first child of every popped node; rule = 1      */
+/* keeps the printed condition and exists only so that a test can show the    */
+/* brute-force pin rejects it.                                                 */
+/* Score of (rho_1..rho_d) = lp_1[rho_1] + ... + lp_d[rho_d], fp32, left to    */
+/* right from 0.  B counts non-root nodes.                                     */
+/* Pinned: brute-force enumeration of S_K (tests), prefix closure, objective   */
+/* optimality on tiny vocabularies.                                            */
+/* ------------------------------------------------------------------------- */
+static float or_desc_score(const float* lp, int K, const int32_t* r, int d)
+{
+    float s = 0.0f;
+    for (int i = 0; i < d; ++i) s = s + lp[i * K + r[i]];
+    return s;
+}
+
+int or_ddtree(const float* lp, const int32_t* id, int L, int K, int B, int rule,
+              int Mmax, int32_t* tok, int32_t* parent, int32_t* depth,
+              int32_t* rank, float* score, int32_t* n_nodes)
+{
+    if (L < 1 || L > OR_MAXL || K < 1 || B < 1 || Mmax < 1) return OR_EINVAL;
+    or_tree_out o = { tok, parent, depth, rank, score };
+    or_put_root(&o);
+    or_node* popped = (or_node*)calloc((size_t)B + 1, sizeof(or_node));
+    or_heap h = { 0, 0, 0 };
+    if (!popped) return OR_ENOMEM;
+    or_node first;
+    memset(&first, 0, sizeof first);
+    first.d = 1; first.r[0] = 0; first.s = or_desc_score(lp, K, first.r, 1);
+    int rc = or_heap_push(&h, &first);
+    int n = 0;
+    while (rc == OR_OK && n < B && h.n > 0) {
+        or_node x = or_heap_pop(&h);
+        /* the parent is the popped node whose descriptor is x's minus its last rank */
+        int par = 0;
+        if (x.d > 1) {
+            par = -1;
+            for (int j = 0; j < n && par < 0; ++j)
+                if (popped[j].d == x.d - 1 &&
+                    memcmp(popped[j].r, x.r, sizeof(int32_t) * (size_t)(x.d - 1)) == 0)
+                    par = j + 1;
+            if (par < 0) { rc = OR_EINVAL; break; }
+        }
+        popped[n] = x;
+        ++n;
+        if (n >= Mmax) { rc = OR_EINVAL; break; }
+        tok[n] = id[(x.d - 1) * K + x.r[x.d - 1]];
+        parent[n] = par;
+        depth[n] = x.d;
+        rank[n] = x.r[x.d - 1];
+        score[n] = x.s;
+        int push_child = (x.d < L) && (rule == 0 || x.r[x.d - 1] == 0);
+        if (push_child) {
+            or_node c = x;
+            c.r[c.d] = 0; c.d += 1;
+            c.s = or_desc_score(lp, K, c.r, c.d);
+            rc = or_heap_push(&h, &c);
+        }
+        if (rc == OR_OK && x.r[x.d - 1] + 1 < K) {
+            or_node sib = x;
+            sib.r[sib.d - 1] += 1;
+            sib.s = or_desc_score(lp, K, sib.r, sib.d);
+            rc = or_heap_push(&h, &sib);
+        }
+    }
+    *n_nodes = n + 1;
+    free(popped);
+    free(h.a);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* DARTree depth-wise supertree and deferred pruning.                          */
+/* [DARTree] Algorithm 1 (lines 1-13) and the equation for s_beta in           */
+/* "Deferred best-first pruning"; Lemma 1 and its proof.                       */
+/*                                                                             */
+/* The correction head g is a parent-conditioned Markov term on the top-K      */
+/* candidates: log q~_d(c | u) = lp_d(c) + <U[tok(u)], Vt[c]>, the dot product */
+/* a serial fmaf chain over R terms from 0.0f; at depth 1 the parent is the    */
+/* root, whose token is root_tok (no term when root_tok < 0).                  */
+/* Score (line 8): s(child) = (s(parent) + log q~) + beta, in that order.      */
+/* Line 9 keeps the W best children of all parents by the shared node order.   */
+/* Line 12: T = TopB(S).  Lemma 1 proves TopB(S) equals the best-first heap    */
+/* over S when beta <= 0 and every log q~ <= 0.  This function returns the     */
+/* best-first heap result (always a prefix-closed tree) and reports through    */
+/* info whether it equals TopB(S) in content and order:                        */
+/*   info[0] = 1 if BestFirst_B(S) == TopB(S) (same nodes, same order)         */
+/*   info[1] = number of edges of S whose child outscores its parent           */
+/*   info[2] = |S| (non-root supertree nodes)                                  */
+/* Pinned: reduction to the DDTree heap for U = 0, beta = 0 and W wide enough  */
+/* to keep every prefix; Lemma 1 equality; a beta > 0 counterexample (tests).  */
+/* ------------------------------------------------------------------------- */
+static float or_markov(const float* U, const float* Vt, int R, int p, int c)
+{
+    float acc = 0.0f;
+    for (int k = 0; k < R; ++k)
+        acc = fmaf(U[(int64_t)p * R + k], Vt[(int64_t)c * R + k], acc);
+    return acc;
+}
+
+int or_dartree(const float* lp, const int32_t* id, int L, int K,
+               const float* U, const float* Vt, int R, int root_tok,
+               int W, float beta, int B, int Mmax,
+               int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
+               float* score, int32_t* n_nodes, int32_t* info,
+               int32_t* topb_out /* nullable [Mmax]: TopB(S) as supertree indices */)
+{
+    if (L < 1 || L > OR_MAXL || K < 1 || W < 1 || B < 1 || Mmax < 1) return OR_EINVAL;
+    if ((U == NULL) != (Vt == NULL)) return OR_EINVAL;
+    int cap = 1 + W * L;
+    or_node* S = (or_node*)calloc((size_t)cap, sizeof(or_node)); /* S[0] = root */
+    or_node* kids = (or_node*)calloc((size_t)W * K + K, sizeof(or_node));
+    if (!S || !kids) { free(S); free(kids); return OR_ENOMEM; }
+    S[0].s = 0.0f; S[0].d = 0; S[0].tok = root_tok; S[0].parent = -1; S[0].self = 0;
+    int nS = 1, prev_lo = 0, prev_hi = 1;
+    for (int d = 1; d <= L; ++d) {
+        int nk = 0;
+        for (int p = prev_lo; p < prev_hi; ++p) {
+            for (int j = 0; j < K; ++j) {
+                int c = id[(d - 1) * K + j];
+                float l = lp[(d - 1) * K + j];
+                float t;
+                int ptok = S[p].tok;
+                if (U != NULL && ptok >= 0) t = l + or_markov(U, Vt, R, ptok, c);
+                else t = l;
+                or_node* x = &kids[nk++];
+                *x = S[p];
+                x->r[d - 1] = j;
+                x->d = d;
+                x->s = (S[p].s + t) + beta;
+                x->tok = c;
+                x->parent = p;
+            }
+        }
+        qsort(kids, (size_t)nk, sizeof(or_node), or_cmp_node);
+        int keep = nk < W ? nk : W;
+        prev_lo = nS;
+        for (int i = 0; i < keep; ++i) { S[nS] = kids[i]; S[nS].self = nS; ++nS; }
+        prev_hi = nS;
+    }
+    int nsup = nS - 1;
+    int viol = 0;
+    for (int i = 1; i < nS; ++i)
+        if (S[i].s > S[S[i].parent].s) ++viol;
+
+    /* TopB(S), line 12 */
+    or_node* sorted = (or_node*)malloc((size_t)nsup * sizeof(or_node));
+    memcpy(sorted, S + 1, (size_t)nsup * sizeof(or_node));
+    qsort(sorted, (size_t)nsup, sizeof(or_node), or_cmp_node);
+    int nb = nsup < B ? nsup : B;
+
+    /* BestFirst_B(S): heap from the root's children, push the popped node's
+     * children in S, stop after B pops. */
+    or_heap h = { 0, 0, 0 };
+    int* out_of = (int*)malloc((size_t)nS * sizeof(int));
+    int32_t* order = (int32_t*)malloc((size_t)(nb + 1) * sizeof(int32_t));
+    int rc = OR_OK;
+    for (int i = 0; i < nS; ++i) out_of[i] = -1;
+    out_of[0] = 0;
+    for (int i = 1; i < nS && rc == OR_OK; ++i)
+        if (S[i].parent == 0) rc = or_heap_push(&h, &S[i]);
+    int n = 0;
+    while (rc == OR_OK && n < B && h.n > 0) {
+        or_node x = or_heap_pop(&h);
+        order[n++] = x.self;
+        out_of[x.self] = n;
+        for (int i = 1; i < nS && rc == OR_OK; ++i)
+            if (S[i].parent == x.self) rc = or_heap_push(&h, &S[i]);
+    }
+    if (n + 1 > Mmax) rc = OR_EINVAL;
+    if (rc == OR_OK) {
+        or_tree_out o = { tok, parent, depth, rank, score };
+        or_put_root(&o);
+        for (int i = 0; i < n; ++i) {
+            const or_node* x = &S[order[i]];
+            tok[i + 1] = x->tok;
+            parent[i + 1] = out_of[x->parent];
+            depth[i + 1] = x->d;
+            rank[i + 1] = x->r[x->d - 1];
+            score[i + 1] = x->s;
+        }
+        *n_nodes = n + 1;
+        int same = (n == nb);
+        for (int i = 0; same && i < n; ++i) same = (sorted[i].self == order[i]);
+        info[0] = same;
+        info[1] = viol;
+        info[2] = nsup;
+        if (topb_out)
+            for (int i = 0; i < nb && i + 1 < Mmax; ++i) topb_out[i] = sorted[i].self;
+    }
+    free(h.a); free(out_of); free(order); free(sorted); free(S); free(kids);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* TALON budgeted, confidence-gated expansion.                                 */
+/* [TALON] "Key designs" 1 (root layer keeps the Top-k children regardless of  */
+/* confidence, k = 10 by default) and 2 (pool = children of every node of the  */
+/* last layer, path probability p(u) = p(v) * P(w | x<=v), anchor m_d = max   */
+/* p(u) over the pool, keep p(u) >= mu * m_d; when the layer passing the gate  */
+/* exceeds the remaining budget N - |T|, keep its best N - |T| nodes and       */
+/* stop).                                                                      */
+/* Log domain: s(u) = s(v) + lp_d(w) in fp32; gate s(u) >= m_d + log_mu with   */
+/* log_mu = log(mu) rounded to fp32 by the caller.  For a block drafter        */
+/* P(w | x<=v) is the marginal at that position, so lp_d comes from the        */
+/* position's candidate list.  |T| excludes the root.  The list may be the     */
+/* full vocabulary (Kc = V) or the top min(N, V); both give the same tree.     */
+/* Pinned: hand-computed V=4 case (golden), invariants, full-list equality.    */
+/* ------------------------------------------------------------------------- */
+int or_talon(const float* lp, const int32_t* id, int L, int Kc, int talon_k,
+             float log_mu, int N, int Mmax,
+             int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
+             float* score, int32_t* n_nodes)
+{
+    if (L < 1 || L > OR_MAXL || Kc < 1 || talon_k < 1 || N < 1 || Mmax < N + 1) return OR_EINVAL;
+    or_node* T = (or_node*)calloc((size_t)N + 1, sizeof(or_node));
+    if (!T) return OR_ENOMEM;
+    int nT = 0;
+    int k1 = talon_k;
+    if (k1 > Kc) k1 = Kc;
+    if (k1 > N) k1 = N;
+    for (int r = 0; r < k1; ++r) {
+        or_node* x = &T[nT];
+        x->d = 1; x->r[0] = r; x->s = lp[r]; x->tok = id[r]; x->parent = -1;
+        x->self = nT;
+        ++nT;
+    }
+    int lay_lo = 0, lay_hi = nT;
+    or_node* pool = NULL;
+    int rc = OR_OK;
+    for (int d = 2; d <= L && nT < N; ++d) {
+        int np = (lay_hi - lay_lo) * Kc;
+        or_node* np_pool = (or_node*)realloc(pool, (size_t)np * sizeof(or_node));
+        if (!np_pool) { rc = OR_ENOMEM; break; }
+        pool = np_pool;
+        int k = 0;
+        float m_d = -INFINITY;
+        for (int v = lay_lo; v < lay_hi; ++v)
+            for (int w = 0; w < Kc; ++w) {
+                or_node* x = &pool[k++];
+                *x = T[v];
+                x->d = d;
+                x->r[d - 1] = w;
+                x->s = T[v].s + lp[(d - 1) * Kc + w];
+                x->tok = id[(d - 1) * Kc + w];
+                x->parent = v;
+                if (x->s > m_d) m_d = x->s;
+            }
+        float thr = m_d + log_mu;
+        int npass = 0;
+        for (int i = 0; i < k; ++i)
+            if (pool[i].s >= thr) pool[npass++] = pool[i];
+        int room = N - nT;
+        int stop = 0;
+        if (npass > room) {
+            qsort(pool, (size_t)npass, sizeof(or_node), or_cmp_node);
+            npass = room;
+            stop = 1;
+        }
+        lay_lo = nT;
+        for (int i = 0; i < npass; ++i) { T[nT] = pool[i]; T[nT].self = nT; ++nT; }
+        lay_hi = nT;
+        if (stop || npass == 0) break;
+    }
+    free(pool);
+    if (rc != OR_OK) { free(T); return rc; }
+    /* output: root, then T by the shared node order */
+    or_node* srt = (or_node*)malloc((size_t)nT * sizeof(or_node));
+    memcpy(srt, T, (size_t)nT * sizeof(or_node));
+    qsort(srt, (size_t)nT, sizeof(or_node), or_cmp_node);
+    int* out_of = (int*)malloc((size_t)(nT > 0 ? nT : 1) * sizeof(int));
+    for (int i = 0; i < nT; ++i) out_of[srt[i].self] = i + 1;
+    or_tree_out o = { tok, parent, depth, rank, score };
+    or_put_root(&o);
+    for (int i = 0; i < nT; ++i) {
+        const or_node* x = &srt[i];
+        tok[i + 1] = x->tok;
+        parent[i + 1] = x->parent < 0 ? 0 : out_of[x->parent];
+        depth[i + 1] = x->d;
+        rank[i + 1] = x->r[x->d - 1];
+        score[i + 1] = x->s;
+    }
+    *n_nodes = nT + 1;
+    free(srt); free(out_of); free(T);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Tree-attention mask and position ids.                                       */
+/* [DARTree] "Tree verification and DDTree" (each flattened node attends to    */
+/* the verified context and the tokens on its root-to-node path); [DDTree]     */
+/* section 4.2 (parent's global index per token, mask by path).                */
+/* mask[n][m] = 1 iff m is an ancestor of n or n itself, bit m%32 of word m/32 */
+/* of row n; row stride ceil(Mmax/32) words; pos[n] = depth(n) + pos_offset.   */
+/* Validation: parent[0] = -1, depth[0] = 0, and for n >= 1 the parent lies in */
+/* [0, M), differs from n, and depth(n) = depth(parent) + 1.                   */
+/* Pinned: hand-drawn depth-3 tree (golden), popcount and closure invariants.  */
+/* ------------------------------------------------------------------------- */
+static int or_tree_valid(const int32_t* parent, const int32_t* depth, int M, int L)
+{
+    if (M < 1) return 0;
+    if (parent[0] != -1 || depth[0] != 0) return 0;
+    for (int n = 1; n < M; ++n) {
+        int p = parent[n];
+        if (p < 0 || p >= M || p == n) return 0;
+        if (depth[n] != depth[p] + 1) return 0;
+        if (L > 0 && depth[n] > L) return 0;
+    }
+    return 1;
+}
+
+int or_tree_mask(const int32_t* parent, const int32_t* depth, int M, int Mmax,
+                 int L, int pos_offset, uint32_t* mask, int32_t* pos)
+{
+    if (M > Mmax) return OR_EINVAL;
+    if (!or_tree_valid(parent, depth, M, L)) return OR_EBADTREE;
+    int words = (Mmax + 31) / 32;
+    for (int n = 0; n < M; ++n) {
+        uint32_t* row = mask + (int64_t)n * words;
+        for (int w = 0; w < words; ++w) row[w] = 0u;
+        for (int a = n; a != -1; a = parent[a]) row[a / 32] |= 1u << (a % 32);
+        pos[n] = depth[n] + pos_offset;
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Greedy (T=0) tree verification.                                             */
+/* [DARTree] "Speculative sampling" (T=0 accepts draft tokens that match the   */
+/* target's greedy choice; at the first mismatch the target's choice is        */
+/* emitted); [Unit11] temperature section (greedy ties go to the smallest      */
+/* vocabulary index); [Unit11] bonus-token section (when the walk reaches a    */
+/* node with nothing left to verify, the target row of that node yields one    */
+/* more token).                                                                */
+/* Walk from the root: a = argmax of target row n; descend into the child of n */
+/* whose token is a, if any; otherwise stop.  Emits a.                         */
+/* acc_nodes[0] = 0 (root), acc_nodes[1..acc_len] the accepted nodes, the rest */
+/* -1.  visited rows only.                                                     */
+/* Pinned: chain tree = sequential greedy decoding; hash-defined target (the   */
+/* accepted path equals greedy decoding until it leaves the tree) (tests).     */
+/* ------------------------------------------------------------------------- */
+int or_verify_greedy(const int32_t* tok, const int32_t* parent, const int32_t* depth,
+                     int M, int L, const float* target, int V,
+                     int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok)
+{
+    if (!or_tree_valid(parent, depth, M, L)) return OR_EBADTREE;
+    for (int i = 0; i <= L; ++i) acc_nodes[i] = -1;
+    int n = 0, len = 0, a = -1;
+    acc_nodes[0] = 0;
+    for (;;) {
+        const float* row = target + (int64_t)n * V;
+        a = 0;
+        for (int v = 1; v < V; ++v)
+            if (row[v] > row[a]) a = v;
+        int child = -1;
+        for (int c = 1; c < M && child < 0; ++c)
+            if (parent[c] == n && tok[c] == a) child = c;
+        if (child < 0 || len >= L) break;
+        acc_nodes[++len] = child;
+        n = child;
+    }
+    *acc_len = len;
+    *next_tok = a;
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Stochastic (T=1) tree verification.                                         */
+/* [DARTree] "Speculative sampling" (accept y ~ q with min(1, p/q); on the     */
+/* first rejection draw one replacement from the normalised residual           */
+/* [p - q]_+); [Unit11] worked three-token example, probability tree and       */
+/* histogram proofs (R = 0 skips the residual; p(x) = 0 < q(x) always         */
+/* rejects); [Unit11] bonus-token section (a fully accepted path samples one   */
+/* more token from the target row).                                            */
+/* On a tree (the pages state the single-chain rule): at node n, test the      */
+/* children of n in rank order; child c is accepted iff                        */
+/*   u[0][c] < exp_canon((t_n[tok c] - lse_t) - (d_{pos c}[tok c] - lse_d)),   */
+/* and the walk descends into the first accepted child.  If n has children and */
+/* all are rejected, draw from w(v) = max(0, P(v) - Q(v)) with P, Q the        */
+/* fixed-point masses floor(exp_canon(.) * 2^32) of the target row of n and of */
+/* the drafter row of n's children's position; if that residual is empty draw  */
+/* from P.  A node without children draws its bonus token from P.  The draw:   */
+/* X = floor(u[1][n] * 2^24), target = floor(X * S / 2^24), emit the smallest  */
+/* v whose inclusive prefix sum of weights exceeds target.                     */
+/* lse_t of each visited row is computed here (double, rounded to fp32) unless */
+/* lse_in supplies it per step (to reproduce another implementation's          */
+/* normaliser bit for bit); lse_out receives the values used, per step.        */
+/* Pinned: worked example through a one-child chain, output frequencies equal  */
+/* p within 3 sigma, R = 0 and p = 0 edge cases (tests).                       */
+/* ------------------------------------------------------------------------- */
+static uint64_t or_fixed32(float p)
+{
+    float f = p * 4294967296.0f;
+    return (uint64_t)f;
+}
+
+static int or_draw(const uint64_t* w, int V, uint64_t S, float u)
+{
+    float xf = u * 16777216.0f;
+    uint64_t X = (uint64_t)xf;
+    if (X > 16777215u) X = 16777215u;
+    unsigned __int128 prod = (unsigned __int128)X * (unsigned __int128)S;
+    uint64_t target = (uint64_t)(prod >> 24);
+    uint64_t acc = 0;
+    int last = -1;
+    for (int v = 0; v < V; ++v) {
+        if (w[v] == 0) continue;
+        acc += w[v];
+        last = v;
+        if (acc > target) return v;
+    }
+    return last;
+}
+
+static float or_row_lse(const float* row, int V)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) if ((double)row[v] > m) m = (double)row[v];
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) s += exp((double)row[v] - m);
+    return (float)(m + log(s));
+}
+
+int or_verify_t1(const int32_t* tok, const int32_t* parent, const int32_t* depth,
+                 const int32_t* rank, int M, int L, int Mmax,
+                 const float* target, const float* draft, const float* draft_lse,
+                 int V, const float* u, const float* lse_in,
+                 int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                 float* lse_out)
+{
+    if (!or_tree_valid(parent, depth, M, L)) return OR_EBADTREE;
+    uint64_t* w = (uint64_t*)malloc((size_t)V * sizeof(uint64_t));
+    int* kids = (int*)malloc((size_t)M * sizeof(int));
+    if (!w || !kids) { free(w); free(kids); return OR_ENOMEM; }
+    for (int i = 0; i <= L; ++i) { acc_nodes[i] = -1; if (lse_out) lse_out[i] = 0.0f; }
+    int n = 0, len = 0, out = -1;
+    acc_nodes[0] = 0;
+    for (;;) {
+        const float* trow = target + (int64_t)n * V;
+        float lse_t = lse_in ? lse_in[len] : or_row_lse(trow, V);
+        if (lse_out) lse_out[len] = lse_t;
+        /* children of n in rank order (insertion sort; ranks are distinct) */
+        int nk = 0;
+        for (int c = 1; c < M; ++c)
+            if (parent[c] == n) {
+                int j = nk++;
+                while (j > 0 && rank[kids[j - 1]] > rank[c]) { kids[j] = kids[j - 1]; --j; }
+                kids[j] = c;
+            }
+        int acc = -1;
+        for (int i = 0; i < nk && acc < 0; ++i) {
+            int c = kids[i];
+            int pos = depth[c] - 1;
+            float lpt = trow[tok[c]] - lse_t;
+            float lpq = draft[(int64_t)pos * V + tok[c]] - draft_lse[pos];
+            float ratio = or_exp_canon(lpt - lpq);
+            if (u[c] < ratio) acc = c;
+        }
+        if (acc >= 0 && len < L) {
+            acc_nodes[++len] = acc;
+            n = acc;
+            continue;
+        }
+        uint64_t S = 0;
+        if (nk > 0) {
+            int pos = depth[n];
+            const float* drow = draft + (int64_t)pos * V;
+            float lsed = draft_lse[pos];
+            for (int v = 0; v < V; ++v) {
+                uint64_t P = or_fixed32(or_exp_canon(trow[v] - lse_t));
+                uint64_t Q = or_fixed32(or_exp_canon(drow[v] - lsed));
+                w[v] = P > Q ? P - Q : 0;
+                S += w[v];
+            }
+        }
+        if (S == 0) {
+            for (int v = 0; v < V; ++v) {
+                w[v] = or_fixed32(or_exp_canon(trow[v] - lse_t));
+                S += w[v];
+            }
+        }
+        out = or_draw(w, V, S, u[Mmax + n]);
+        break;
+    }
+    *acc_len = len;
+    *next_tok = out;
+    free(w); free(kids);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Single-position speculative sampling in double precision, the scalar rule   */
+/* the tree walk generalises.  [Unit11] worked three-token example and its     */
+/* probability-tree / histogram proofs; [DARTree] "Speculative sampling".      */
+/* Draw x ~ q by inverse CDF from u_draw; accept with a = min(1, p(x)/q(x))    */
+/* (a = 1 when q(x) = 0 is never needed: x ~ q has q(x) > 0); on rejection     */
+/* draw from r = (p - q)_+ / R by inverse CDF from u_res.  Outputs the accept  */
+/* probability of each token and the residual distribution (zeros if R = 0).  */
+/* Pinned: worked example values (golden), frequency test (tests).             */
+/* ------------------------------------------------------------------------- */
+int or_spec_scalar(const double* p, const double* q, int n, double u_draw,
+                   double u_acc, double u_res, double* accept_prob,
+                   double* residual, int32_t* drafted)
+{
+    double R = 0.0;
+    for (int i = 0; i < n; ++i) {
+        accept_prob[i] = q[i] > 0.0 ? (p[i] < q[i] ? p[i] / q[i] : 1.0) : 1.0;
+        double z = p[i] - q[i];
+        residual[i] = z > 0.0 ? z : 0.0;
+        R += residual[i];
+    }
+    for (int i = 0; i < n; ++i) residual[i] = R > 0.0 ? residual[i] / R : 0.0;
+    int x = n - 1;
+    double c = 0.0;
+    for (int i = 0; i < n; ++i) { c += q[i]; if (u_draw < c) { x = i; break; } }
+    if (drafted) *drafted = x;
+    if (u_acc < accept_prob[x]) return x;
+    if (R <= 0.0) return x; /* unreachable: R = 0 means p = q and a = 1 */
+    int y = n - 1;
+    c = 0.0;
+    for (int i = 0; i < n; ++i) { c += residual[i]; if (u_res < c) { y = i; break; } }
+    return y;
+}
+
+/* Many trials of or_spec_scalar from a caller-supplied stream of uniforms
+ * (three per trial), counting how often each token is emitted. */
+int or_spec_scalar_trials(const double* p, const double* q, int n,
+                          const double* uniforms, int64_t trials, int64_t* counts)
+{
+    double* a = (double*)malloc((size_t)n * sizeof(double));
+    double* r = (double*)malloc((size_t)n * sizeof(double));
+    if (!a || !r) { free(a); free(r); return OR_ENOMEM; }
+    for (int i = 0; i < n; ++i) counts[i] = 0;
+    for (int64_t t = 0; t < trials; ++t) {
+        int y = or_spec_scalar(p, q, n, uniforms[3 * t], uniforms[3 * t + 1],
+                               uniforms[3 * t + 2], a, r, NULL);
+        counts[y] += 1;
+    }
+    free(a); free(r);
+    return OR_OK;
+}
