@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Draft-tree build + verify throughput on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+stage-1 log-softmax/Top-K over the vocabulary, tree selection, tree mask and
+position ids, and the acceptance walk -- dt_build_tree, dt_tree_mask,
+dt_verify through the C ABI.  Default workload: a single request at the Qwen3
+vocabulary (batch 1, L=16, V=151936, bf16 logits with a +8 spike on one token
+per position with probability 0.7), DDTree with K=B=256, greedy verification
+against target rows whose spike matches the drafter's with probability 0.8.
+
+Timing: every step reads a different copy of the inputs (rotating copies
+whose drafter logits alone exceed twice the L2 size, so no step reads logits
+another step left in L2); each copy's step is captured once in a CUDA graph
+and replayed; CUDA events on the launching stream bracket exactly K steps,
+with a barrier and a device synchronise on both sides; max over ranks.
+
+Prints one JSON line.  --impl reference times the CPU oracle (the plain
+restatement the tests check the kernels against) on the host cores instead.
+"""
+import argparse
+import concurrent.futures
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft trees built+verified/sec and logit-read HBM GB/s (% of GB300 peak) at V=151936"
+L2_BYTES = 129 * 1024 * 1024
+
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the stage-1
+# kernel, keyed by the sha1 of the kernel source the capture was taken on; a
+# changed kernel reports null until it is captured again.
+KN1_TRAFFIC = {}
+
+
+def workloads():
+    from speculative_decoding_draft_bf16_gb300 import workloads as wk
+    return {
+        "single_request_B256": wk.single_request(256),
+        "single_request_B128": wk.single_request(128),
+        "single_request_B64": wk.single_request(64),
+        "stochastic_b1": wk.stochastic_batch(1),
+        "stochastic_b4": wk.stochastic_batch(4),
+        "stochastic_b16": wk.stochastic_batch(16),
+        "dartree_beta0": wk.dartree_supertree(0.0),
+        "dartree_beta-0.5": wk.dartree_supertree(-0.5),
+        "talon_N60": wk.talon_gated(60),
+        "talon_N1024": wk.talon_gated(1024),
+    }
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="single_request_B256")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def params_for(wl, U=None, Vt=None):
+    from speculative_decoding_draft_bf16_gb300 import dtree
+    return dtree.Params(mode=wl.mode, batch=wl.batch, L=wl.L, V=wl.V, dtype=wl.dtype, K=wl.K, B=wl.B, W=wl.W,
+                        beta=wl.beta, R=wl.R, U=U, Vt=Vt, talon_k=wl.talon_k, mu=wl.mu, N=wl.N)
+
+
+def max_nodes_of(wl):
+    if wl.mode == "dartree":
+        return min(wl.B, wl.W * wl.L) + 1
+    return wl.max_nodes
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, wl, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_draft_bf16_gb300 import dtree
+    from speculative_decoding_draft_bf16_gb300 import workloads as wk
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dtree.lib()
+    U = Vt = None
+    if wl.mode == "dartree":
+        U, Vt = wk.markov_tables(wl.V, wl.R, device=dev)
+    p = params_for(wl, U, Vt)
+    Mmax = max_nodes_of(wl)
+    esize = 2 if wl.dtype == "bf16" else 4
+    draft_bytes = wl.batch * wl.L * wl.V * esize
+    target_bytes = wl.batch * Mmax * wl.V * esize
+    R = max(2, math.ceil(2 * L2_BYTES / draft_bytes))
+    R = min(R, max(2, int(40e9 // max(target_bytes, 1))))
+    temperature = wl.temperature
+
+    # rotating copies: distinct requests per copy and per rank
+    copies = []
+    for r in range(R):
+        first = (rank * R + r) * wl.batch
+        x, spikes = wk.draft_logits(wl, device=dev, first_req=first)
+        tree = dtree.TreeBuffers(wl.batch, wl.L, p.Kc, Mmax, device=dev)
+        ws = dtree.make_workspace(p, device=dev)
+        dtree.build_tree(p, x, tree, workspace=ws)
+        torch.cuda.synchronize()
+        tgt = wk.target_logits(wl, tree.depth, tree.n_nodes, spikes, device=dev, first_req=first, rows=Mmax)
+        uni = wk.uniforms(wl, device=dev, first_req=first) if temperature == 1.0 else None
+        mask, pos = dtree.alloc_mask(tree, device=dev)
+        out = dtree.alloc_verify_out(tree, device=dev)
+        copies.append(dict(x=x, tree=tree, ws=ws, tgt=tgt, uni=uni, mask=mask, pos=pos, out=out))
+
+    def step(c, stages=("build", "mask", "verify")):
+        if "build" in stages:
+            dtree.build_tree(p, c["x"], c["tree"], workspace=c["ws"])
+        if "cand" in stages:
+            dtree.candidates(p, c["x"], c["tree"])
+        if "select" in stages:
+            dtree.select(p, c["tree"], workspace=c["ws"])
+        if "mask" in stages:
+            dtree.tree_mask(c["tree"], c["mask"], c["pos"])
+        if "verify" in stages:
+            dtree.verify(c["tree"], c["tgt"], temperature=temperature, draft=c["x"] if temperature else None,
+                         uniforms=c["uni"], out=c["out"])
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(stages):
+        graphs = []
+        for c in copies:
+            step(c, stages)  # eager warm call (sets kernel attributes)
+        torch.cuda.synchronize()
+        for c in copies:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(c, stages)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def timed(graphs, n, warm):
+        with torch.cuda.stream(stream):
+            for i in range(warm):
+                graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(n):
+                graphs[i % len(graphs)].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    full = capture(("build", "mask", "verify"))
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = timed(full, args.steps, args.warmup)
+    clk = clocks.stop()
+
+    # per-stage device time (same rotating inputs, graphs of one stage)
+    stage_us = {}
+    for name, stages in (("candidates", ("cand",)), ("select", ("select",)), ("mask", ("mask",)),
+                         ("verify", ("verify",))):
+        g = capture(stages)
+        n = max(args.steps, 2 * len(g))
+        stage_us[name] = timed(g, n, max(args.warmup, 3)) * 1000.0 / n
+        del g
+
+    # end to end: pinned host inputs copied in, results copied out, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        hx = [copies[i]["x"].cpu().pin_memory() for i in range(2)]
+        ht = [copies[i]["tgt"].cpu().pin_memory() for i in range(2)]
+        hu = [copies[i]["uni"].cpu().pin_memory() if copies[i]["uni"] is not None else None for i in range(2)]
+        c = copies[0]
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in c["out"]]
+        htok = torch.empty(c["tree"].node_tok.shape, dtype=torch.int32, pin_memory=True)
+        h2d = hx[0].numel() * hx[0].element_size() + ht[0].numel() * ht[0].element_size()
+        if hu[0] is not None:
+            h2d += hu[0].numel() * 4
+        d2h = sum(t.numel() * 4 for t in hout) + htok.numel() * 4
+
+        def e2e_step(i):
+            j = i % 2
+            c["x"].copy_(hx[j], non_blocking=True)
+            c["tgt"].copy_(ht[j], non_blocking=True)
+            if hu[j] is not None:
+                c["uni"].copy_(hu[j], non_blocking=True)
+            step(c)
+            for h, d in zip(hout, c["out"]):
+                h.copy_(d, non_blocking=True)
+            htok.copy_(c["tree"].node_tok, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                e2e_step(i)
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.e2e_steps):
+                e2e_step(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": args.e2e_steps * wl.batch * world / (ems / 1000.0), "unit": "trees/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    status = sum(int(c["tree"].status.abs().sum()) for c in copies)
+    launches_per_step = 4 + (1 if (wl.mode == "dartree" and wl.R > 0) else 0)
+    kn1_s = stage_us["candidates"] / 1e6
+    achieved = draft_bytes / kn1_s / 1e9
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    src = open(os.path.join(ROOT, "speculative_decoding_draft_bf16_gb300", "csrc", "kn1_candidates.cu"), "rb").read()
+    traffic = KN1_TRAFFIC.get(hashlib.sha1(src).hexdigest())
+    result = {
+        "metric": METRIC,
+        "value": args.steps * wl.batch * world / (ms / 1000.0),
+        "unit": "trees/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded Gaussian logits with confident-token spikes; Qwen3 vocabulary)",
+        "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch, "L": wl.L, "V": wl.V,
+                   "K": wl.K, "B": wl.B, "W": wl.W, "beta": wl.beta, "N": wl.N, "temperature": temperature,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "rotating %d input copies (drafter logits %.0f MB > 2x L2)" % (R, R * draft_bytes / 1e6)},
+        "roofline": {"bound": "hbm", "kernel": "kn1 log-softmax+Top-K", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic, "algorithmic_bytes_per_launch": draft_bytes},
+        "stages_us": stage_us,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "device_status_nonzero": status,
+    }
+    return result, copies
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: baseline leg and reference arm
+# ---------------------------------------------------------------------------
+def oracle_round(wl, x, tgt, uni, U, Vt):
+    """One tree through the oracle: stage 1, selection, mask, walk."""
+    import numpy as np
+    import oracle
+    _, l32, ids, lps = oracle.candidates(x, wl.Kc)
+    Mmax = max_nodes_of(wl)
+    if wl.mode == "ddtree":
+        t = oracle.ddtree(lps, ids, wl.B, Mmax=Mmax)
+    elif wl.mode == "dartree":
+        t, _, _ = oracle.dartree(lps, ids, U, Vt, -1, wl.W, wl.beta, wl.B, Mmax=Mmax)
+    else:
+        t = oracle.talon(lps, ids, wl.talon_k, wl.log_mu, wl.N, Mmax=Mmax)
+    oracle.tree_mask(t, Mmax, wl.L)
+    if tgt is None:
+        return t
+    if wl.temperature == 1.0:
+        oracle.verify_t1(t, tgt, x, l32, uni, wl.L, Mmax)
+    else:
+        oracle.verify_greedy(t, tgt, wl.L)
+    return t
+
+
+def oracle_inputs(wl, n_trees, seed_base=10_000):
+    """Host inputs for n_trees requests; targets follow the oracle's own trees."""
+    import numpy as np
+    import torch
+    from speculative_decoding_draft_bf16_gb300 import workloads as wk
+    U = Vt = None
+    if wl.mode == "dartree":
+        U, Vt = (t.numpy() for t in wk.markov_tables(wl.V, wl.R))
+    one = wl.with_(batch=1)
+    items = []
+    for i in range(n_trees):
+        x, spikes = wk.draft_logits(one, first_req=seed_base + i)
+        xf = x[0].float().numpy()
+        t = oracle_round(wl, xf, None, None, U, Vt)
+        Mmax = max_nodes_of(wl)
+        depth = np.zeros((1, Mmax), np.int32)
+        depth[0, :t.n] = t.depth[:t.n]
+        tgt = wk.target_logits(one, depth, [t.n], spikes, first_req=seed_base + i, rows=Mmax)[0].float().numpy()
+        uni = wk.uniforms(one, first_req=seed_base + i)[0].numpy() if wl.temperature == 1.0 else None
+        items.append((xf, tgt, uni))
+    return items, U, Vt
+
+
+def time_oracle(wl, items, U, Vt, threads):
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda it: oracle_round(wl, it[0], it[1], it[2], U, Vt), items))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, trees=None):
+    from oracle import build as ob
+    ob.build()
+    cores = os.cpu_count() or 1
+    trees = trees or max(2, min(2 * cores, 32))
+    items, U, Vt = oracle_inputs(wl, trees)
+    sec = time_oracle(wl, items, U, Vt, cores)
+    return {"value": trees / sec, "unit": "trees/s", "cores": cores, "kind": "oracle",
+            "sample": "%d single-request trees of the %s workload (stage 1, selection, mask, walk), "
+                      "one thread per tree over %d host cores" % (trees, wl.name, cores)}
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return None
+    from oracle import build as ob
+    ob.build()
+    cores = os.cpu_count() or 1
+    per_step = max(1, min(cores, 16))
+    items, U, Vt = oracle_inputs(wl, per_step)
+    for _ in range(args.warmup if args.warmup < 3 else 1):
+        time_oracle(wl, items[:1], U, Vt, 1)
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(wl, items, U, Vt, cores)
+    value = args.steps * per_step / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "trees/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded Gaussian logits with confident-token spikes; Qwen3 vocabulary)",
+        "config": {"workload": wl.name, "mode": wl.mode, "batch_per_step": per_step, "L": wl.L, "V": wl.V,
+                   "K": wl.K, "B": wl.B, "temperature": wl.temperature},
+        "cpu_baseline": {"value": value, "unit": "trees/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d single-request trees per step, one thread per tree" % per_step},
+        "e2e": {"value": value, "unit": "trees/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workloads()[args.workload]
+    if args.impl == "reference":
+        out = run_reference(args, wl, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    result, copies = run_ours(args, wl, rank, world, local)
+    del copies
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+/*
+ * dtree.h -- C ABI of the draft-tree build / tree-verify library for block
+ * (diffusion) drafters, GB300 (sm_103a).
+ *
+ * One speculative round on the pages: a block drafter scores all L future
+ * positions in one pass; per position the library keeps the Top-K tokens and
+ * their log-probabilities, selects a budget-B prefix tree (DDTree Top-B,
+ * DARTree supertree + deferred Top-B, or TALON gating), builds the tree
+ * attention mask and position ids, and, once the target model has scored every
+ * tree node, walks the longest accepted path.  Sources (by page title):
+ *   [DARTree] "DARTree: Speculative Diffusion Decoding With Autoregressive
+ *             Draft Trees" -- "Speculative sampling", "Tree verification and
+ *             DDTree", Algorithm 1, "Deferred best-first pruning", Lemma 1.
+ *   [TALON]   "TALON: Confidence-Aware Speculative Decoding with Adaptive
+ *             Token Trees" -- "Key designs" 1 and 2.
+ *   [Unit11]  "Sampling, speculative decoding and multi-token prediction"
+ *             (formulas-to-systems, unit 11) -- temperature and greedy ties,
+ *             the worked three-token example, the bonus token, the >= 1 token
+ *             per round argument.
+ *   [DDTree]  "DDTree algorithm: efficient inference-tree construction"
+ *             (CSDN explainer) -- Prop 1, Prop 2, Lemma (S_K), Algorithm 1
+ *             (heap over rank descriptors), section 4.2 (tree attention mask).
+ *
+ * Conventions for every call:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, never synchronises, and enqueues its kernels on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *  - Arrays are dense, row-major, without padding, laid out as the comment on
+ *    each argument says; b = request, L = block positions, V = vocabulary.
+ *  - Arguments the host can check (sizes, modes, NULL pointers, limits) are
+ *    checked before anything is enqueued: on failure the call returns a
+ *    negative dt_status and enqueues nothing.
+ *  - Conditions only the device can see (an invalid tree handed to the mask
+ *    or verify call, a wait that exceeded its bound) set bits in the caller's
+ *    per-request status word (dt_tree.status), readable after the stream
+ *    synchronises; see DT_DEV_*.
+ *  - A launch failure returns DT_ERR_CUDA (cudaGetLastError is consumed).
+ * Limits: L <= 32, V <= DT_MAX_V, candidate list Kc <= 1024, nodes per
+ * request (incl. the root) <= 1025.
+ */
+#ifndef DTREE_H
+#define DTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dt_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    DT_OK = 0,
+    DT_ERR_INVALID_ARG = -1, /* a size, mode, limit or pointer is invalid */
+    DT_ERR_UNSUPPORTED = -2, /* valid but outside this build's limits */
+    DT_ERR_CUDA = -4,        /* a CUDA launch or attribute call failed */
+} dt_status;
+
+enum { DT_MODE_DDTREE = 0, DT_MODE_DARTREE = 1, DT_MODE_TALON = 2 };
+enum { DT_BF16 = 0, DT_F32 = 1 };
+
+#define DT_MAX_L 32
+#define DT_MAX_KC 1024
+#define DT_MAX_NODES 1025
+#define DT_MAX_V (16 * 32768)
+
+/* Device status word bits (dt_tree.status[b]).  dt_build_tree stores a fresh
+ * value per request; dt_tree_mask and dt_verify OR their bits into it. */
+#define DT_DEV_BAD_TREE 0x1         /* mask/verify: parent/depth arrays invalid */
+#define DT_DEV_TIMEOUT 0x2          /* a bounded wait gave up; outputs undefined */
+#define DT_DEV_BESTFIRST 0x4        /* DARTree: TopB(S) was not a topologically
+                                       ordered tree; the best-first heap over S
+                                       was used (see dt_build_tree) */
+#define DT_DEV_VIOLATION_SHIFT 8    /* DARTree: number of supertree edges whose
+                                       child outscores its parent, saturating
+                                       at 2^23-1, in bits 8..30 */
+
+/* Build parameters.  [DARTree] Algorithm 1 inputs (logits, K, W, B, beta);
+ * [TALON] settings (root Top-k, mu, node budget N); [DDTree] Algorithm 1
+ * (K, budget B).  Budgets count non-root nodes. */
+typedef struct {
+    int32_t mode;       /* DT_MODE_* */
+    int32_t batch;      /* requests b >= 1 */
+    int32_t L;          /* block positions, 1..32 */
+    int32_t V;          /* vocabulary, >= 1 */
+    int32_t dtype;      /* drafter logits: DT_BF16 or DT_F32 */
+    int32_t K;          /* DDTree / DARTree: candidates per position, 1..min(V,1024)
+                           (DDTree: K = min(B, V) suffices, [DDTree] Lemma (S_K)) */
+    int32_t B;          /* DDTree / DARTree node budget, 1..1024 */
+    int32_t W;          /* DARTree layer width, 1..1024, W*K <= 4096 */
+    float beta;         /* DARTree depth bonus, must be <= 0 ([DARTree] Lemma 1) */
+    int32_t R;          /* DARTree Markov rank (columns of U and Vt), 0 = no term */
+    const float* U;     /* DARTree [V][R] fp32, parent-token embedding, or NULL */
+    const float* Vt;    /* DARTree [V][R] fp32, child-token embedding, or NULL */
+    const int32_t* root_tok; /* DARTree [batch] token of the verified prefix's
+                           last position (parent of depth-1 nodes), or NULL:
+                           no Markov term at depth 1 */
+    int32_t talon_k;    /* TALON root-layer Top-k, 1..N */
+    float log_mu;       /* TALON log(mu) rounded to fp32, mu in (0, 1] */
+    int32_t N;          /* TALON node budget, 1..1024 */
+} dt_build_params;
+
+/* Tree buffers (caller-owned device memory).  Node 0 of each request is the
+ * root (token -1, parent -1, depth 0, rank -1, score 0); nodes 1..n-1 follow
+ * in the shared node order: score descending, then rank descriptor ascending
+ * (a prefix before its extensions).  Rows n..max_nodes-1 are left untouched. */
+typedef struct {
+    int32_t max_nodes;  /* row capacity per request, >= budget + 1, <= 1025 */
+    int32_t Kc;         /* candidate-list length per position (DDTree/DARTree:
+                           K; TALON: min(N, V)) */
+    int32_t L;          /* positions (must equal the build's L) */
+    int32_t* node_tok;  /* [b][max_nodes] token of each node */
+    int32_t* parent;    /* [b][max_nodes] parent node index (root: -1) */
+    int32_t* depth;     /* [b][max_nodes] depth (root 0; position = depth) */
+    int32_t* rank;      /* [b][max_nodes] 0-based rank of the node's token in
+                           its position's candidate list (root -1) */
+    float* score;       /* [b][max_nodes] path score (fp32, see each mode) */
+    int32_t* n_nodes;   /* [b] nodes including the root */
+    float* lse;         /* [b][L] drafter log-normaliser per position */
+    int32_t* cand_id;   /* [b][L][Kc] Top-Kc token ids, logit desc, id asc */
+    float* cand_lp;     /* [b][L][Kc] their log-probabilities (logit - lse) */
+    int32_t* status;    /* [b] DT_DEV_* bits */
+} dt_tree;
+
+/* Bytes of caller-provided device workspace dt_build_tree / dt_select need
+ * for these parameters (0 for DDTree and TALON; DARTree: the per-request
+ * Markov table, batch*L*K*K*4 bytes).  Returns 0 and sets *ok = 0 on invalid
+ * parameters when ok != NULL. */
+size_t dt_workspace_size(const dt_build_params* p, int* ok);
+
+/* Stage 1: per-position log-softmax and Top-Kc over the full vocabulary.
+ * [DARTree] Algorithm 1 line 4; [DDTree] section 3.3 (log-domain scores of the
+ * per-position Top-K tokens).
+ *   draft_logits: [batch][L][V] in p->dtype (bf16 or fp32); finite values or
+ *   -inf (at least one finite value per row).
+ * Writes tree->lse [b][L] (fp32 accumulation of sum exp(x - max)),
+ * tree->cand_id / cand_lp [b][L][Kc] (rank order: logit descending, token id
+ * ascending on equal logits; lp = logit - lse in fp32).  Kc = tree->Kc must be
+ * K (DDTree/DARTree) or min(N, V) (TALON). */
+dt_status dt_candidates(const dt_build_params* p, const void* draft_logits,
+                        dt_tree* tree, dt_stream_t stream);
+
+/* Stages 2-3: tree selection from the candidate lists already in `tree`
+ * (written by dt_candidates, or by the caller), writing node_tok, parent,
+ * depth, rank, score, n_nodes and a fresh status word per request.
+ *  DDTree ([DDTree] Algorithm 1, Prop 2, Lemma (S_K); [DARTree] "Tree
+ *   verification and DDTree"): the B best prefixes of S_K under the node
+ *   order, score = sum of lp along the path, fp32, added from the root.
+ *  DARTree ([DARTree] Algorithm 1, "Deferred best-first pruning", Lemma 1):
+ *   per depth, all W*K children of the kept parents scored
+ *   s = (s_parent + (lp + <U[tok(parent)], Vt[tok(child)]>)) + beta (the dot
+ *   product a serial fp32 fma chain over R), keep the W best; then TopB over
+ *   the supertree S.  When TopB(S) is not a topologically ordered tree (only
+ *   possible when some edge raises the score), the result is the best-first
+ *   heap over S and DT_DEV_BESTFIRST is set.
+ *  TALON ([TALON] key designs 1-2): root layer = Top-talon_k of position 1;
+ *   then pool the children of the last layer, keep s >= max_pool + log_mu,
+ *   truncate to the best N - |T| and stop on overflow; at most L layers.
+ * workspace: device memory of dt_workspace_size(p) bytes (may be NULL when 0). */
+dt_status dt_select(const dt_build_params* p, dt_tree* tree, void* workspace,
+                    size_t workspace_bytes, dt_stream_t stream);
+
+/* dt_candidates followed by dt_select on the same stream. */
+dt_status dt_build_tree(const dt_build_params* p, const void* draft_logits,
+                        dt_tree* tree, void* workspace, size_t workspace_bytes,
+                        dt_stream_t stream);
+
+/* Tree-attention ancestor mask and position ids.  [DARTree] "Tree
+ * verification and DDTree" (a node attends to the verified context and its
+ * root-to-node path); [DDTree] section 4.2.
+ *   mask: [batch][max_nodes][ceil(max_nodes/32)] uint32; bit (m % 32) of word
+ *         m/32 of row n is 1 iff node m is node n or one of its ancestors;
+ *         rows >= n_nodes are not written.
+ *   pos:  [batch][max_nodes] int32, pos[n] = depth(n) + pos_offset.
+ * Reads tree->parent, depth, n_nodes; a request whose arrays are not a valid
+ * tree (root first, parents in range, depth = parent depth + 1 <= L) gets
+ * DT_DEV_BAD_TREE and no mask rows. */
+dt_status dt_tree_mask(const dt_tree* tree, int32_t batch, int32_t pos_offset,
+                       uint32_t* mask, int32_t* pos, dt_stream_t stream);
+
+/* Acceptance walk.  Row n of target_logits is the target model's next-token
+ * logits after the path root..n.
+ *  temperature 0 ([DARTree] "Speculative sampling"; [Unit11] greedy ties):
+ *   at node n take a = argmax of row n (smallest id on ties); descend into the
+ *   child of n whose token is a; stop when there is none; emit a.
+ *  temperature 1 ([DARTree] "Speculative sampling"; [Unit11] worked example,
+ *   bonus token): at node n, test n's children in rank order, child c accepted
+ *   iff uniforms[b][0][c] < exp_canon((t_n[c] - lse_t) - (d[c] - lse_d)),
+ *   descend into the first accepted one; if all are rejected draw from
+ *   max(0, P - Q) (P, Q = floor(2^32 * probability) of the target row of n and
+ *   of the drafter row of n's children's position), or from P when that is
+ *   empty or n has no children, by inverse CDF with uniforms[b][1][n].
+ *   exp_canon is an fp32 exponential by Cody-Waite reduction and a degree-7
+ *   Taylor polynomial (one rounding per step), so results are reproducible.
+ *   target_logits: [batch][max_nodes][V] (dtype); draft_logits [batch][L][V]
+ *   (dtype; T=1 only, else may be NULL); uniforms [batch][2][max_nodes] fp32
+ *   in [0,1) (T=1 only).
+ *   target_lse: NULL, or [batch][max_nodes] fp32 log-normalisers of the
+ *   target rows supplied by the caller (e.g. already computed by the target's
+ *   sampler); when NULL the walk computes them (fp32 accumulation) for the rows
+ *   it visits.  T=1 only.
+ * Outputs: acc_nodes [batch][L+1] (root, then accepted nodes, then -1),
+ *   acc_len [batch] (accepted draft tokens), next_tok [batch] (the emitted
+ *   correction / bonus token), visited_lse [batch][L+1] (T=1: fp32 target
+ *   log-normaliser of each visited row; may be NULL).
+ * Uses tree->lse at T=1. */
+dt_status dt_verify(const dt_tree* tree, int32_t batch, int32_t V, int32_t dtype,
+                    const void* target_logits, const float* target_lse,
+                    const void* draft_logits, float temperature, const float* uniforms,
+                    int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                    float* visited_lse, dt_stream_t stream);
+
+/* Static string for a dt_status value. */
+const char* dt_status_str(dt_status s);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int32_t dt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DTREE_H */

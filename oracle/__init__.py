@@ -207,8 +207,9 @@ def verify_greedy(tree, target, L):
 
 
 def verify_t1(tree, target, draft, draft_lse, uniforms, L, Mmax, lse_in=None):
-    """uniforms: [2, Mmax] (row 0: per-child acceptance, row 1: per-node draw).
-    Returns (acc_nodes, acc_len, next_tok, lse_used [L+1])."""
+    """uniforms: [2, Mmax] (row 0: per-child acceptance, row 1: per-node draw);
+    lse_in: optional per-node target normalisers [Mmax].
+    Returns (acc_nodes, acc_len, next_tok, lse_used per step [L+1])."""
     target = _f32(target)
     draft = _f32(draft)
     draft_lse = _f32(draft_lse)

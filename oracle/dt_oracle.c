@@ -619,8 +619,8 @@ int or_verify_greedy(const int32_t* tok, const int32_t* parent, const int32_t* d
 /* X = floor(u[1][n] * 2^24), target = floor(X * S / 2^24), emit the smallest  */
 /* v whose inclusive prefix sum of weights exceeds target.                     */
 /* lse_t of each visited row is computed here (double, rounded to fp32) unless */
-/* lse_in supplies it per step (to reproduce another implementation's          */
-/* normaliser bit for bit); lse_out receives the values used, per step.        */
+/* lse_in supplies it per node ([Mmax], row n's normaliser); lse_out receives  */
+/* the values used, per step of the walk.                                      */
 /* Pinned: worked example through a one-child chain, output frequencies equal  */
 /* p within 3 sigma, R = 0 and p = 0 edge cases (tests).                       */
 /* ------------------------------------------------------------------------- */
@@ -673,7 +673,7 @@ int or_verify_t1(const int32_t* tok, const int32_t* parent, const int32_t* depth
     acc_nodes[0] = 0;
     for (;;) {
         const float* trow = target + (int64_t)n * V;
-        float lse_t = lse_in ? lse_in[len] : or_row_lse(trow, V);
+        float lse_t = lse_in ? lse_in[n] : or_row_lse(trow, V);
         if (lse_out) lse_out[len] = lse_t;
         /* children of n in rank order (insertion sort; ranks are distinct) */
         int nk = 0;

@@ -1,0 +1,213 @@
+// dt_abi.cu -- the library's C ABI: argument checks, launch shapes, and the
+// entry points declared in include/dtree.h.
+#include <cuda_runtime.h>
+
+#include "dt_launch.h"
+#include "dtree.h"
+
+namespace {
+
+constexpr int kChunkMax = 32768;       // vocabulary elements per CTA (shared memory)
+constexpr int kCtaTarget = 2 * 152;    // aim for two CTAs per SM on a GB300
+constexpr size_t kSmemMax = 227 * 1024;
+
+int pow2_ceil(long long n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+int chunk_of(int V, int S, int dtype) {
+    const int g = dtype == DT_BF16 ? 8 : 4;  // elements per 16 bytes
+    long long per = ((long long)V + S - 1) / S;
+    return (int)(((per + g - 1) / g) * g);
+}
+
+// Cluster size for a row-parallel vocabulary pass over `rows` rows.
+int cluster_for(int V, long long rows, int dtype) {
+    int s_min = pow2_ceil(((long long)V + kChunkMax - 1) / kChunkMax);
+    int s_cap = pow2_ceil(((long long)V + 1023) / 1024);  // chunks of at least ~1K elements
+    int s = pow2_ceil((kCtaTarget + rows - 1) / rows);
+    if (s > s_cap) s = s_cap;
+    if (s < s_min) s = s_min;
+    if (s > 16) s = 16;
+    if (s < 1) s = 1;
+    (void)dtype;
+    return s;
+}
+
+dt_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DT_OK;
+    (void)cudaGetLastError();
+    return DT_ERR_CUDA;
+}
+
+int kc_of(const dt_build_params* p) {
+    if (p->mode == DT_MODE_TALON) return p->N < p->V ? p->N : p->V;
+    return p->K;
+}
+
+int budget_of(const dt_build_params* p) { return p->mode == DT_MODE_TALON ? p->N : p->B; }
+
+dt_status check_build(const dt_build_params* p, const dt_tree* t) {
+    if (!p || !t) return DT_ERR_INVALID_ARG;
+    if (p->mode < DT_MODE_DDTREE || p->mode > DT_MODE_TALON) return DT_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->L < 1 || p->L > DT_MAX_L || p->V < 1) return DT_ERR_INVALID_ARG;
+    if (p->V > DT_MAX_V) return DT_ERR_UNSUPPORTED;
+    if (p->dtype != DT_BF16 && p->dtype != DT_F32) return DT_ERR_INVALID_ARG;
+    if ((long long)p->batch * p->L > 65535) return DT_ERR_UNSUPPORTED;
+    if (p->mode == DT_MODE_TALON) {
+        if (p->N < 1 || p->N > DT_MAX_KC) return DT_ERR_INVALID_ARG;
+        if (p->talon_k < 1 || p->talon_k > p->N) return DT_ERR_INVALID_ARG;
+        if (!(p->log_mu <= 0.f) || p->log_mu != p->log_mu || p->log_mu == -__builtin_inff())
+            return DT_ERR_INVALID_ARG;
+    } else {
+        if (p->K < 1 || p->K > p->V || p->K > DT_MAX_KC) return DT_ERR_INVALID_ARG;
+        if (p->B < 1 || p->B > DT_MAX_NODES - 1) return DT_ERR_INVALID_ARG;
+    }
+    if (p->mode == DT_MODE_DARTREE) {
+        if (p->W < 1 || (long long)p->W * p->K > 4096 || (long long)p->W * p->L > 4096) return DT_ERR_INVALID_ARG;
+        if (!(p->beta <= 0.f)) return DT_ERR_INVALID_ARG;  // Lemma 1 needs beta <= 0
+        if (p->R < 0 || p->R > 1024) return DT_ERR_INVALID_ARG;
+        if (p->R > 0 && (!p->U || !p->Vt)) return DT_ERR_INVALID_ARG;
+        if (p->R > 0 && dt_kn3_table_smem_bytes(p->K, p->R) > kSmemMax) return DT_ERR_UNSUPPORTED;
+        if (dt_kn3_select_smem_bytes(p->L, p->K, p->W) > kSmemMax) return DT_ERR_UNSUPPORTED;
+    }
+    if (t->Kc != kc_of(p)) return DT_ERR_INVALID_ARG;
+    if (t->L != p->L) return DT_ERR_INVALID_ARG;
+    if (t->max_nodes < budget_of(p) + 1 || t->max_nodes > DT_MAX_NODES) {
+        // DARTree needs room for min(B, |S|) nodes; DDTree and TALON for their budget
+        if (!(p->mode == DT_MODE_DARTREE && t->max_nodes >= 1 + ((p->B < p->W * p->L) ? p->B : p->W * p->L) &&
+              t->max_nodes <= DT_MAX_NODES))
+            return DT_ERR_INVALID_ARG;
+    }
+    if (!t->node_tok || !t->parent || !t->depth || !t->rank || !t->score || !t->n_nodes || !t->lse ||
+        !t->cand_id || !t->cand_lp || !t->status)
+        return DT_ERR_INVALID_ARG;
+    return DT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dt_workspace_size(const dt_build_params* p, int* ok) {
+    if (ok) *ok = 1;
+    if (!p || p->batch < 1 || p->L < 1 || p->K < 0) {
+        if (ok) *ok = 0;
+        return 0;
+    }
+    if (p->mode == DT_MODE_DARTREE && p->R > 0 && p->U) return (size_t)p->batch * p->L * p->K * p->K * sizeof(float);
+    return 0;
+}
+
+dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_tree* t, dt_stream_t stream) {
+    dt_status s = check_build(p, t);
+    if (s != DT_OK) return s;
+    if (!draft_logits) return DT_ERR_INVALID_ARG;
+    const int Kc = kc_of(p);
+    const long long rows = (long long)p->batch * p->L;
+    const int S = cluster_for(p->V, rows, p->dtype);
+    const int chunk = chunk_of(p->V, S, p->dtype);
+    const int esize = p->dtype == DT_BF16 ? 2 : 4;
+    if (dt_kn1_smem_bytes(chunk, Kc, esize) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(t->status, 0, sizeof(int32_t) * (size_t)p->batch, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = dt_kn1_launch(draft_logits, p->dtype, (int)rows, p->L, p->V, Kc, S, chunk, t->lse, t->cand_id, t->cand_lp,
+                      t->status, st);
+    return cuda_status(e);
+}
+
+dt_status dt_select(const dt_build_params* p, dt_tree* t, void* workspace, size_t workspace_bytes,
+                    dt_stream_t stream) {
+    dt_status s = check_build(p, t);
+    if (s != DT_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    const int Mmax = t->max_nodes;
+    switch (p->mode) {
+        case DT_MODE_DDTREE:
+            if (dt_kn2_smem_bytes(p->K, p->B) > kSmemMax) return DT_ERR_UNSUPPORTED;
+            e = dt_kn2_launch(p->batch, p->L, p->K, p->B, Mmax, t->cand_lp, t->cand_id, t->node_tok, t->parent,
+                              t->depth, t->rank, t->score, t->n_nodes, st);
+            break;
+        case DT_MODE_DARTREE: {
+            const size_t need = dt_workspace_size(p, nullptr);
+            if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
+            const bool term = p->R > 0 && p->U;
+            e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt, p->root_tok,
+                              Mmax, t->cand_lp, t->cand_id, term ? (float*)workspace : nullptr, t->node_tok,
+                              t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, st);
+            break;
+        }
+        case DT_MODE_TALON:
+            if (dt_kn4_smem_bytes(kc_of(p), p->N) > kSmemMax) return DT_ERR_UNSUPPORTED;
+            e = dt_kn4_launch(p->batch, p->L, kc_of(p), p->talon_k, p->log_mu, p->N, Mmax, t->cand_lp, t->cand_id,
+                              t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, st);
+            break;
+    }
+    return cuda_status(e);
+}
+
+dt_status dt_build_tree(const dt_build_params* p, const void* draft_logits, dt_tree* t, void* workspace,
+                        size_t workspace_bytes, dt_stream_t stream) {
+    dt_status s = check_build(p, t);
+    if (s != DT_OK) return s;
+    if (p->mode == DT_MODE_DARTREE) {
+        const size_t need = dt_workspace_size(p, nullptr);
+        if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
+    }
+    s = dt_candidates(p, draft_logits, t, stream);
+    if (s != DT_OK) return s;
+    return dt_select(p, t, workspace, workspace_bytes, stream);
+}
+
+dt_status dt_tree_mask(const dt_tree* t, int32_t batch, int32_t pos_offset, uint32_t* mask, int32_t* pos,
+                       dt_stream_t stream) {
+    if (!t || !mask || !pos || batch < 1) return DT_ERR_INVALID_ARG;
+    if (t->max_nodes < 1 || t->max_nodes > DT_MAX_NODES || t->L < 1 || t->L > DT_MAX_L) return DT_ERR_INVALID_ARG;
+    if (!t->parent || !t->depth || !t->n_nodes || !t->status) return DT_ERR_INVALID_ARG;
+    cudaError_t e = dt_kn5_launch(batch, t->L, t->max_nodes, pos_offset, t->parent, t->depth, t->n_nodes, mask, pos,
+                                  t->status, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+dt_status dt_verify(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, const void* target_logits,
+                    const float* target_lse, const void* draft_logits, float temperature, const float* uniforms,
+                    int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
+                    dt_stream_t stream) {
+    if (!t || batch < 1 || V < 1 || !target_logits || !acc_nodes || !acc_len || !next_tok) return DT_ERR_INVALID_ARG;
+    if (V > DT_MAX_V) return DT_ERR_UNSUPPORTED;
+    if (dtype != DT_BF16 && dtype != DT_F32) return DT_ERR_INVALID_ARG;
+    if (t->max_nodes < 1 || t->max_nodes > DT_MAX_NODES || t->L < 1 || t->L > DT_MAX_L) return DT_ERR_INVALID_ARG;
+    if (!t->node_tok || !t->parent || !t->depth || !t->rank || !t->n_nodes || !t->status) return DT_ERR_INVALID_ARG;
+    const int t1 = (temperature == 1.0f);
+    if (!t1 && temperature != 0.0f) return DT_ERR_UNSUPPORTED;
+    if (t1 && (!draft_logits || !uniforms || !t->lse)) return DT_ERR_INVALID_ARG;
+    // the walk is sequential per request: spread each row over a full cluster
+    int s = 16;
+    while (s > 1 && chunk_of(V, s, dtype) < 1024) s >>= 1;
+    const int chunk = chunk_of(V, s, dtype);
+    const int esize = dtype == DT_BF16 ? 2 : 4;
+    if (chunk > kChunkMax || dt_kn6_smem_bytes(chunk, esize, t->max_nodes) + 1024 > kSmemMax) return DT_ERR_UNSUPPORTED;
+    cudaError_t e = dt_kn6_launch(batch, t->L, V, dtype, t->max_nodes, s, chunk, t1, t->node_tok, t->parent, t->depth,
+                                  t->rank, t->n_nodes, t->lse, target_logits, t1 ? target_lse : nullptr, draft_logits,
+                                  uniforms, acc_nodes,
+                                  acc_len, next_tok, visited_lse, t->status, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+const char* dt_status_str(dt_status s) {
+    switch (s) {
+        case DT_OK: return "ok";
+        case DT_ERR_INVALID_ARG: return "invalid argument";
+        case DT_ERR_UNSUPPORTED: return "unsupported (outside this build's limits)";
+        case DT_ERR_CUDA: return "CUDA launch or attribute call failed";
+    }
+    return "unknown status";
+}
+
+int32_t dt_version(void) { return 100; }
+
+}  // extern "C"

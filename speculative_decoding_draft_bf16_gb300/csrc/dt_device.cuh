@@ -1,0 +1,306 @@
+// dt_device.cuh -- device helpers shared by the draft-tree kernels (sm_103a).
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dtree.h"
+
+namespace cg = cooperative_groups;
+
+#define DT_DI __device__ __forceinline__
+
+// Bounded waits give up after this many SM clock cycles (~1 s at 2 GHz) and
+// report DT_DEV_TIMEOUT instead of spinning forever.
+#define DT_WAIT_BUDGET (1ll << 31)
+
+// ---------------------------------------------------------------------------
+// Element access and order-preserving keys.  A key is an unsigned integer
+// whose order equals the numeric order of the value; -0 is mapped onto +0 so
+// that equal values have equal keys.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct DtElem;
+
+template <>
+struct DtElem<uint16_t> {  // bf16 stored as raw bits
+    static constexpr int KB = 16;
+    static DT_DI float val(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+    static DT_DI uint32_t key(uint16_t h) {
+        if ((h & 0x7FFFu) == 0) h = 0;
+        return (h & 0x8000u) ? (~uint32_t(h) & 0xFFFFu) : (uint32_t(h) | 0x8000u);
+    }
+    static DT_DI float key_val(uint32_t k) {
+        uint32_t h = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+        return __uint_as_float(h << 16);
+    }
+};
+
+template <>
+struct DtElem<float> {
+    static constexpr int KB = 32;
+    static DT_DI float val(float x) { return x; }
+    static DT_DI uint32_t key(float x) {
+        uint32_t b = __float_as_uint(x);
+        if ((b & 0x7FFFFFFFu) == 0) b = 0;
+        return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    static DT_DI float key_val(uint32_t k) {
+        uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+        return __uint_as_float(b);
+    }
+};
+
+// Order key of an fp32 score (same mapping as DtElem<float>).
+DT_DI uint32_t dt_fkey(float x) { return DtElem<float>::key(x); }
+DT_DI float dt_fkey_val(uint32_t k) { return DtElem<float>::key_val(k); }
+
+// ---------------------------------------------------------------------------
+// exp_canon: fp32 exponential by Cody and Waite's argument reduction (W. J.
+// Cody, W. Waite, "Software Manual for the Elementary Functions", 1980) and
+// the Taylor series of e^r to degree 7 in Horner form.  Each step is one
+// correctly rounded fp32 operation (explicit _rn intrinsics, no contraction),
+// so the result is reproducible bit for bit on any IEEE machine with a fused
+// multiply-add.  x < -86 gives 0, x > 88.5 gives +inf.
+// ---------------------------------------------------------------------------
+DT_DI float dt_exp_canon(float x) {
+    if (x != x) return x;
+    if (x > 88.5f) return __int_as_float(0x7F800000);
+    if (x < -86.0f) return 0.0f;
+    const float log2e = 1.44269504088896340736f;
+    const float c_hi = 0.693145751953125f;          // ln 2 rounded to 16 bits
+    const float c_lo = 1.42860682030941723212e-6f;  // ln 2 - c_hi
+    float kf = rintf(__fmul_rn(x, log2e));
+    int k = (int)kf;
+    float r = __fmaf_rn(-kf, c_hi, x);
+    r = __fmaf_rn(-kf, c_lo, r);
+    float p = 1.0f / 5040.0f;
+    p = __fmaf_rn(p, r, 1.0f / 720.0f);
+    p = __fmaf_rn(p, r, 1.0f / 120.0f);
+    p = __fmaf_rn(p, r, 1.0f / 24.0f);
+    p = __fmaf_rn(p, r, 1.0f / 6.0f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __fmul_rn(p, __int_as_float((k + 127) << 23));
+}
+
+// floor(p * 2^32) for p in [0, 1] (exact scaling, then truncation).
+DT_DI uint64_t dt_fixed32(float p) { return (uint64_t)__fmul_rn(p, 4294967296.0f); }
+
+// ---------------------------------------------------------------------------
+// Warp / block reductions and scans.
+// ---------------------------------------------------------------------------
+DT_DI float dt_warp_max(float v) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+DT_DI uint32_t dt_warp_max_u32(uint32_t v) {
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+DT_DI float dt_warp_sum(float v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+DT_DI int dt_warp_sum_i(int v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+DT_DI unsigned long long dt_warp_sum_u64(unsigned long long v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+DT_DI int dt_warp_incl_scan(int v) {
+    const int lane = threadIdx.x & 31;
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// Exclusive prefix sum of one int per thread over the block; returns the
+// thread's exclusive prefix and writes the block total to *total.
+// `red` needs NT/32 ints of shared memory.  Contains two __syncthreads.
+template <int NT>
+DT_DI int dt_block_excl_scan(int v, int* red, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int inc = dt_warp_incl_scan(v);
+    if (lane == 31) red[w] = inc;
+    __syncthreads();
+    int wsum = (lane < NT / 32) ? red[lane] : 0;
+    int winc = dt_warp_incl_scan(wsum);
+    int before = __shfl_sync(0xffffffffu, winc, w) - __shfl_sync(0xffffffffu, wsum, w);
+    int tot = __shfl_sync(0xffffffffu, winc, NT / 32 - 1);
+    __syncthreads();
+    *total = tot;
+    return before + inc - v;
+}
+
+// Exclusive scan of an int array in shared memory (n entries, any n):
+// out[i] = sum of a[0..i), out[n] = total.  in and out may alias.
+template <int NT>
+DT_DI void dt_block_scan_array(const int* a, int* out, int n, int* red) {
+    int carry = 0;
+    for (int base = 0; base < n; base += NT) {
+        int i = base + threadIdx.x;
+        int v = (i < n) ? a[i] : 0;
+        int tot;
+        int ex = dt_block_excl_scan<NT>(v, red, &tot);
+        if (i < n) out[i] = carry + ex;
+        carry += tot;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[n] = carry;
+    __syncthreads();
+}
+
+// In-place bitonic sort of n (a power of two) 64-bit keys in shared memory,
+// descending when desc, else ascending.  Ends with __syncthreads.
+template <int NT>
+DT_DI void dt_bitonic_u64(unsigned long long* a, int n, bool desc) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += NT) {
+                int ixj = i ^ j;
+                if (ixj > i) {
+                    unsigned long long x = a[i], y = a[ixj];
+                    bool up = ((i & k) == 0) == desc;  // true: larger first
+                    if (up ? (x < y) : (x > y)) { a[i] = y; a[ixj] = x; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+DT_DI int dt_pow2_ceil(int n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk async copy (TMA, 1-D) helpers.
+// ---------------------------------------------------------------------------
+DT_DI uint32_t dt_smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+DT_DI void dt_mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(dt_smem_addr(bar)), "r"(count) : "memory");
+}
+DT_DI void dt_fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+DT_DI void dt_fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+DT_DI void dt_mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(dt_smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+// Bulk copy global -> own shared memory; dst, src 16-byte aligned, bytes a multiple of 16.
+DT_DI void dt_bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dt_smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(dt_smem_addr(bar))
+        : "memory");
+}
+// Wait for the phase with parity `phase` to complete; false if the budget ran out.
+DT_DI bool dt_mbar_wait(uint64_t* bar, uint32_t phase) {
+    const uint32_t a = dt_smem_addr(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(a), "r"(phase)
+            : "memory");
+        if (done) return true;
+        if (clock64() - t0 > DT_WAIT_BUDGET) return false;
+    }
+}
+
+// Stage elements [lo, hi) of a row into shared memory.  The shared buffer
+// `sbase` must be 16-byte aligned with room for (hi - lo) elements + 16 bytes;
+// the returned pointer is where element lo lands (sbase + (src address mod 16)).
+// The 16-byte-aligned interior moves with one bulk copy completing on `bar`
+// (one elected thread issues it); the ragged head and tail use plain loads by
+// all threads.  Returns the number of bytes the bulk copy will deliver (0 if
+// none) -- the caller waits on `bar` for that phase when it is non-zero.
+// Must be called by all threads of the block.
+template <typename T>
+DT_DI const T* dt_stage_row(const T* row, int lo, int hi, unsigned char* sbase, uint64_t* bar,
+                            uint32_t* bulk_bytes) {
+    const uintptr_t a_lo = (uintptr_t)(row + lo);
+    const uintptr_t a_hi = (uintptr_t)(row + hi);
+    T* s = (T*)(sbase + (a_lo & 15));
+    uintptr_t in_lo = (a_lo + 15) & ~(uintptr_t)15;
+    uintptr_t in_hi = a_hi & ~(uintptr_t)15;
+    uint32_t bytes = 0;
+    if (in_hi > in_lo) bytes = (uint32_t)(in_hi - in_lo);
+    else { in_lo = a_hi; in_hi = a_hi; }
+    const int e_in_lo = (int)((in_lo - a_lo) / sizeof(T));
+    const int e_in_hi = (int)((in_hi - a_lo) / sizeof(T));
+    const int n = hi - lo;
+    if (threadIdx.x == 0 && bytes) {
+        dt_mbar_arrive_expect_tx(bar, bytes);
+        dt_bulk_g2s(s + e_in_lo, (const void*)in_lo, bytes, bar);
+    }
+    for (int e = threadIdx.x; e < e_in_lo; e += blockDim.x) s[e] = row[lo + e];
+    for (int e = e_in_hi + threadIdx.x; e < n; e += blockDim.x) s[e] = row[lo + e];
+    *bulk_bytes = bytes;
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// Shared node order on explicit node arrays (score s, depth dep, parent par,
+// lex = (lexicographic rank of the parent among its depth << 16) | own rank):
+// does node y come before node x?  Higher score first; on equal scores the
+// lexicographically smaller rank descriptor, a prefix before its extensions.
+// Nodes of the same depth compare by lex; otherwise the deeper node is walked
+// up to the shallower one's depth.
+// ---------------------------------------------------------------------------
+DT_DI bool dt_node_before(int y, int x, const float* s, const int* dep, const int* par, const uint32_t* lex) {
+    const float sy = s[y], sx = s[x];
+    if (sy != sx) return sy > sx;
+    const int dy = dep[y], dx = dep[x];
+    if (dy == dx) return lex[y] < lex[x];
+    if (dy < dx) {
+        int a = x;
+        while (dep[a] > dy) a = par[a];
+        if (a == y) return true;
+        return lex[y] < lex[a];
+    }
+    int a = y;
+    while (dep[a] > dx) a = par[a];
+    if (a == x) return false;
+    return lex[a] < lex[x];
+}
+
+// Bitonic sort of n (a power of two) node indices by dt_node_before; entries
+// equal to -1 are padding and sort last.  Ends with __syncthreads.
+template <int NT>
+DT_DI void dt_bitonic_nodes(int* a, int n, const float* s, const int* dep, const int* par, const uint32_t* lex) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += NT) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const int x = a[i], y = a[ixj];
+                    // does y belong before x?
+                    bool y_first;
+                    if (x < 0) y_first = (y >= 0);
+                    else if (y < 0) y_first = false;
+                    else y_first = dt_node_before(y, x, s, dep, par, lex);
+                    const bool asc = ((i & k) == 0);
+                    if (asc ? y_first : (!y_first && x != y)) { a[i] = y; a[ixj] = x; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}

@@ -1,0 +1,45 @@
+// dt_launch.h -- host-side launchers of the draft-tree kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+// Stage 1 (kn1_candidates.cu).
+size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize);
+cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int L, int V, int Kc, int S, int chunk,
+                          float* lse, int32_t* cand_id, float* cand_lp, int32_t* status, cudaStream_t st);
+
+// DDTree selection (kn2_ddtree.cu).
+size_t dt_kn2_smem_bytes(int K, int B);
+cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
+                          int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
+                          int32_t* n_nodes, cudaStream_t st);
+
+// DARTree Markov table + selection (kn3_dartree.cu).
+size_t dt_kn3_table_smem_bytes(int K, int R);
+size_t dt_kn3_select_smem_bytes(int L, int K, int W);
+cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
+                          const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp, const int32_t* cand_id,
+                          float* table, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
+                          int32_t* n_nodes, int32_t* status, cudaStream_t st);
+
+// TALON selection (kn4_talon.cu).
+size_t dt_kn4_smem_bytes(int Kc, int N);
+cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
+                          const float* cand_lp, const int32_t* cand_id, int32_t* tok, int32_t* parent,
+                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, cudaStream_t st);
+
+// Tree mask (kn5_mask.cu).
+size_t dt_kn5_smem_bytes(int Mmax);
+cudaError_t dt_kn5_launch(int batch, int L, int Mmax, int pos_offset, const int32_t* parent, const int32_t* depth,
+                          const int32_t* n_nodes, uint32_t* mask, int32_t* pos, int32_t* status, cudaStream_t st);
+
+// Verification walk (kn6_verify.cu).
+size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax);
+cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int temperature_one,
+                          const int32_t* tok, const int32_t* parent, const int32_t* depth, const int32_t* rank,
+                          const int32_t* n_nodes, const float* draft_lse, const void* target,
+                          const float* target_lse, const void* draft,
+                          const float* uniforms, int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                          float* visited_lse, int32_t* status, cudaStream_t st);

@@ -1,0 +1,286 @@
+// kn2_ddtree.cu -- DDTree Top-B selection over the S_K prefix set.
+//
+// [DDTree] Prop 2 (a prefix is at least as likely as its extensions), Lemma
+// (S_K) and Algorithm 1 (best-first heap over rank descriptors); [DARTree]
+// "Tree verification and DDTree".  The heap pops the B best prefixes of S_K
+// under the node order (score descending, then rank descriptor ascending with
+// a prefix first); score = lp_1[rho_1] + ... + lp_d[rho_d] in fp32, added from
+// the root's 0.  Because a child never outscores its parent and a later
+// sibling never outscores an earlier one, that order places every prefix
+// after its predecessor, and the popped set is exactly the B smallest prefixes
+// in the order.
+//
+// GPU formulation (no heap): one CTA per request keeps C = the B best prefixes
+// of depth <= d, sorted.  C for depth d is the best B of C(d-1) plus the
+// children of C(d-1)'s depth-(d-1) nodes, since every depth-d member of the
+// answer has its parent there.  Per depth: list those parents in
+// lexicographic order, count per parent the children that can still enter
+// (binary search against the current B-th score; each parent's children are
+// sorted), materialise them as 64-bit keys (score, lexicographic position),
+// sort, and merge with C (merge path: one binary search per element).  Ties
+// across depths are resolved by walking the candidate's ancestors.  Stops at
+// the first depth that adds nothing.  Work per depth is O((|C| + m) log) plus
+// the sorts; everything lives in shared memory.
+#include "dt_device.cuh"
+#include "dt_launch.h"
+
+namespace {
+
+constexpr int NT = 512;
+constexpr int CAP = 2048;  // candidates materialised per merge
+
+struct Kn2Smem {
+    float* lp;       // [K]
+    float* cs;       // [2][B] scores (buffer `cur` at offset cur*B)
+    int* cpar;       // [2][B] parent C index (-1 = root)
+    int* crank;      // [2][B]
+    int* cdep;       // [2][B]
+    uint32_t* clex;  // [2][B] (lexrank of parent << 16) | rank
+    int* pidx;       // [B] parents in lexicographic order (C index or -1)
+    int* pn;         // [B + 1]
+    int* newpos;     // [B]
+    unsigned long long* cand;  // [CAP]
+};
+
+DT_DI Kn2Smem carve(unsigned char* s, int K, int B) {
+    Kn2Smem m;
+    m.cand = (unsigned long long*)s;
+    s += (size_t)CAP * 8;
+    m.lp = (float*)s;
+    s += (size_t)((K + 3) & ~3) * 4;
+    m.cs = (float*)s; s += (size_t)2 * B * 4;
+    m.cpar = (int*)s; s += (size_t)2 * B * 4;
+    m.crank = (int*)s; s += (size_t)2 * B * 4;
+    m.cdep = (int*)s; s += (size_t)2 * B * 4;
+    m.clex = (uint32_t*)s; s += (size_t)2 * B * 4;
+    m.pidx = (int*)s; s += (size_t)B * 4;
+    m.newpos = (int*)s; s += (size_t)B * 4;
+    m.pn = (int*)s;
+    return m;
+}
+
+// Does C node i precede the depth-d candidate with key y?
+DT_DI bool c_before_cand(int i, unsigned long long y, int d, const float* cs, const int* cdep, const int* cpar,
+                         const uint32_t* clex, const int* pidx) {
+    const float sy = dt_fkey_val((uint32_t)(y >> 32));
+    const float si = cs[i];
+    if (si != sy) return si > sy;
+    const uint32_t ly = 0xFFFFFFFFu - (uint32_t)y;
+    const int e = cdep[i];
+    if (e == d) return clex[i] < ly;
+    int a = pidx[ly >> 16];
+    while (cdep[a] > e) a = cpar[a];
+    if (a == i) return true;  // C node i is an ancestor of the candidate
+    return clex[i] < clex[a];
+}
+
+__global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_lp,
+                                                 const int32_t* __restrict__ cand_id, int L, int K, int B, int Mmax,
+                                                 int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
+                                                 int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
+                                                 float* __restrict__ o_score, int32_t* __restrict__ o_n) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int red[NT / 32];
+    __shared__ int sh_nP, sh_lrhi, sh_any;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    Kn2Smem S = carve(smem, K, B);
+    const float* lpb = cand_lp + (size_t)b * L * K;
+
+    // depth 1: the root's children are the first min(K, B) ranks, already in order
+    int nC = min(K, B);
+    int cur = 0;
+    for (int i = tid; i < nC; i += NT) {
+        S.cs[i] = lpb[i];
+        S.cpar[i] = -1;
+        S.crank[i] = i;
+        S.cdep[i] = 1;
+        S.clex[i] = (uint32_t)i;
+    }
+    __syncthreads();
+
+    for (int d = 2; d <= L; ++d) {
+        // ---- parents: depth-(d-1) members of C in lexicographic order ------
+        {
+            int cnt_local = 0;
+            for (int i = tid; i < nC; i += NT) cnt_local += ((S.cdep + cur * B)[i] == d - 1);
+            // compact with a scan over a per-thread strided layout
+            int tot;
+            int ex = dt_block_excl_scan<NT>(cnt_local, red, &tot);
+            int w = ex;
+            for (int i = tid; i < nC; i += NT)
+                if ((S.cdep + cur * B)[i] == d - 1)
+                    S.cand[w++] = ((unsigned long long)(S.clex + cur * B)[i] << 32) | (unsigned)i;
+            const int P2 = dt_pow2_ceil(tot);
+            for (int i = tot + tid; i < P2; i += NT) S.cand[i] = ~0ull;
+            if (tid == 0) sh_nP = tot;
+            __syncthreads();
+            dt_bitonic_u64<NT>(S.cand, P2, false);
+            for (int j = tid; j < tot; j += NT) S.pidx[j] = (int)(S.cand[j] & 0xFFFFFFFFull);
+            __syncthreads();
+        }
+        const int nP = sh_nP;
+        if (nP == 0) break;
+        for (int r = tid; r < K; r += NT) S.lp[r] = lpb[(size_t)(d - 1) * K + r];
+        __syncthreads();
+
+        int lr_lo = 0;
+        while (lr_lo < nP) {
+            const bool full = (nC == B);
+            const float tau = full ? (S.cs + cur * B)[B - 1] : 0.f;
+            // children of each remaining parent that can still enter
+            for (int j = tid; j < nP; j += NT) {
+                int cnt = 0;
+                const int p = S.pidx[j];
+                if (j >= lr_lo && p >= 0) {
+                    if (!full) {
+                        cnt = K;
+                    } else {
+                        const float sp = (S.cs + cur * B)[p];
+                        int lo = 0, hi = K;
+                        while (lo < hi) {
+                            int mid = (lo + hi) >> 1;
+                            if (__fadd_rn(sp, S.lp[mid]) >= tau) lo = mid + 1;
+                            else hi = mid;
+                        }
+                        cnt = lo;
+                    }
+                    cnt = min(cnt, B);
+                }
+                S.pn[j] = cnt;
+            }
+            __syncthreads();
+            dt_block_scan_array<NT>(S.pn, S.pn, nP, red);
+            if (tid == 0) sh_lrhi = lr_lo + 1;
+            __syncthreads();
+            for (int j = lr_lo + 1 + tid; j <= nP; j += NT)
+                if (S.pn[j] - S.pn[lr_lo] <= CAP) atomicMax(&sh_lrhi, j);
+            __syncthreads();
+            const int lr_hi = sh_lrhi;
+            const int base = S.pn[lr_lo];
+            const int m = S.pn[lr_hi] - base;
+            if (m > 0) {
+                // materialise candidates (key: score, then lexicographic position)
+                for (int idx = tid; idx < m; idx += NT) {
+                    const int g = base + idx;
+                    int lo = lr_lo, hi = lr_hi;  // find j with pn[j] <= g < pn[j+1]
+                    while (hi - lo > 1) {
+                        int mid = (lo + hi) >> 1;
+                        if (S.pn[mid] <= g) lo = mid;
+                        else hi = mid;
+                    }
+                    const int j = lo;
+                    const int r = g - S.pn[j];
+                    const float s = __fadd_rn((S.cs + cur * B)[S.pidx[j]], S.lp[r]);
+                    const uint32_t lex = ((uint32_t)j << 16) | (uint32_t)r;
+                    S.cand[idx] = ((unsigned long long)dt_fkey(s) << 32) | (unsigned long long)(0xFFFFFFFFu - lex);
+                }
+                const int P2 = dt_pow2_ceil(m);
+                for (int i = m + tid; i < P2; i += NT) S.cand[i] = 0ull;
+                __syncthreads();
+                dt_bitonic_u64<NT>(S.cand, P2, true);
+                const int mm = min(m, B);
+                // merge path: new position of every C member ...
+                for (int i = tid; i < nC; i += NT) {
+                    int lo = 0, hi = mm;
+                    while (lo < hi) {
+                        int mid = (lo + hi) >> 1;
+                        if (c_before_cand(i, S.cand[mid], d, (S.cs + cur * B), (S.cdep + cur * B), (S.cpar + cur * B), (S.clex + cur * B), S.pidx))
+                            hi = mid;
+                        else
+                            lo = mid + 1;
+                    }
+                    const int nr = i + lo;
+                    S.newpos[i] = nr < B ? nr : -1;
+                }
+                __syncthreads();
+                const int nx = cur ^ 1;
+                for (int i = tid; i < nC; i += NT) {
+                    const int np = S.newpos[i];
+                    if (np >= 0) {
+                        const int pp = (S.cpar + cur * B)[i];
+                        (S.cs + nx * B)[np] = (S.cs + cur * B)[i];
+                        (S.cpar + nx * B)[np] = pp < 0 ? -1 : S.newpos[pp];
+                        (S.crank + nx * B)[np] = (S.crank + cur * B)[i];
+                        (S.cdep + nx * B)[np] = (S.cdep + cur * B)[i];
+                        (S.clex + nx * B)[np] = (S.clex + cur * B)[i];
+                    }
+                }
+                // ... and of every candidate
+                for (int q = tid; q < mm; q += NT) {
+                    const unsigned long long y = S.cand[q];
+                    int lo = 0, hi = nC;
+                    while (lo < hi) {
+                        int mid = (lo + hi) >> 1;
+                        if (c_before_cand(mid, y, d, (S.cs + cur * B), (S.cdep + cur * B), (S.cpar + cur * B), (S.clex + cur * B), S.pidx))
+                            lo = mid + 1;
+                        else
+                            hi = mid;
+                    }
+                    const int nr = q + lo;
+                    if (nr < B) {
+                        const uint32_t lex = 0xFFFFFFFFu - (uint32_t)y;
+                        const int j = (int)(lex >> 16);
+                        (S.cs + nx * B)[nr] = dt_fkey_val((uint32_t)(y >> 32));
+                        (S.cpar + nx * B)[nr] = S.newpos[S.pidx[j]];
+                        (S.crank + nx * B)[nr] = (int)(lex & 0xFFFFu);
+                        (S.cdep + nx * B)[nr] = d;
+                        (S.clex + nx * B)[nr] = lex;
+                    }
+                }
+                __syncthreads();
+                for (int j = tid; j < nP; j += NT) {
+                    const int p = S.pidx[j];
+                    if (p >= 0) S.pidx[j] = S.newpos[p];
+                }
+                nC = min(B, nC + mm);
+                cur = nx;
+                __syncthreads();
+            }
+            lr_lo = lr_hi;
+        }
+        // stop once a depth adds nothing
+        if (tid == 0) sh_any = 0;
+        __syncthreads();
+        for (int i = tid; i < nC; i += NT)
+            if ((S.cdep + cur * B)[i] == d) sh_any = 1;
+        __syncthreads();
+        if (!sh_any) break;
+    }
+
+    // ---- output: root, then C in order -----------------------------------
+    const size_t ob = (size_t)b * Mmax;
+    for (int i = tid; i < nC; i += NT) {
+        const int dd = (S.cdep + cur * B)[i];
+        const int rr = (S.crank + cur * B)[i];
+        o_tok[ob + i + 1] = cand_id[((size_t)b * L + dd - 1) * K + rr];
+        o_par[ob + i + 1] = (S.cpar + cur * B)[i] + 1;
+        o_dep[ob + i + 1] = dd;
+        o_rank[ob + i + 1] = rr;
+        o_score[ob + i + 1] = (S.cs + cur * B)[i];
+    }
+    if (tid == 0) {
+        o_tok[ob] = -1;
+        o_par[ob] = -1;
+        o_dep[ob] = 0;
+        o_rank[ob] = -1;
+        o_score[ob] = 0.f;
+        o_n[b] = nC + 1;
+    }
+}
+
+}  // namespace
+
+size_t dt_kn2_smem_bytes(int K, int B) {
+    return (size_t)CAP * 8 + (size_t)((K + 3) & ~3) * 4 + (size_t)B * 4 * 10 + (size_t)B * 8 + (size_t)(B + 1) * 4 + 16;
+}
+
+cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
+                          int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
+                          int32_t* n_nodes, cudaStream_t st) {
+    const size_t smem = dt_kn2_smem_bytes(K, B);
+    cudaError_t e = cudaFuncSetAttribute(kn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kn2_kernel<<<batch, NT, smem, st>>>(cand_lp, cand_id, L, K, B, Mmax, tok, parent, depth, rank, score, n_nodes);
+    return cudaGetLastError();
+}

@@ -1,0 +1,250 @@
+// kn4_talon.cu -- TALON budgeted, confidence-gated tree expansion.
+//
+// [TALON] key design 1: the root layer keeps the Top-k tokens of the first
+// position regardless of confidence.  Key design 2: each later layer pools
+// every child of the last layer, scores it by its path probability
+// p(u) = p(v) * P(w) (log domain: s(u) = s(v) + lp(w), fp32), takes the anchor
+// m_d = max p(u) over the pool and keeps p(u) >= mu * m_d (s >= m_d + log mu);
+// if the layer passing the gate exceeds the remaining budget N - |T| it keeps
+// only the best N - |T| (shared node order) and growth stops.  At most L
+// layers.  For a block drafter P(w) is position d's marginal, so each
+// position's Top-min(N, V) list suffices: a kept child of rank r needs its r
+// better-ranked siblings kept as well.
+//
+// One CTA per request, everything in shared memory.  Layers are stored in
+// lexicographic order (children materialised parent by parent in rank
+// order), so a node's lexicographic key within its depth is
+// (index of its parent within the parent layer << 16) | rank.  Per layer the
+// passing children of each parent form a rank prefix found by binary search;
+// on overflow the best N - |T| are chosen in groups of parents (running
+// top list + group, bitonic sort), pruning later groups by the running cutoff.
+// The finished tree is sorted once in the shared node order.
+#include "dt_device.cuh"
+#include "dt_launch.h"
+
+namespace {
+
+constexpr int NT = 512;
+constexpr int CAP = 4096;
+
+struct Kn4Smem {
+    unsigned long long* cand;  // [CAP]
+    float* lp;                 // [Kc]
+    float* s;                  // [N]
+    int* dep;
+    int* par;
+    int* rank;
+    uint32_t* lex;
+    int* pn;                   // [N + 1]
+    int* ord;                  // [pow2(N)]
+};
+
+DT_DI Kn4Smem kn4_carve(unsigned char* p, int Kc, int N) {
+    Kn4Smem m;
+    m.cand = (unsigned long long*)p;
+    p += (size_t)CAP * 8;
+    m.lp = (float*)p; p += (size_t)((Kc + 3) & ~3) * 4;
+    m.s = (float*)p; p += (size_t)N * 4;
+    m.dep = (int*)p; p += (size_t)N * 4;
+    m.par = (int*)p; p += (size_t)N * 4;
+    m.rank = (int*)p; p += (size_t)N * 4;
+    m.lex = (uint32_t*)p; p += (size_t)N * 4;
+    m.pn = (int*)p; p += (size_t)(N + 1) * 4;
+    m.ord = (int*)p;
+    return m;
+}
+
+// Count of the first-ranked children w of a parent with score sp that satisfy
+// sp + lp[w] >= thr (monotone in w).
+DT_DI int count_pass(float sp, const float* lp, int Kc, float thr) {
+    int lo = 0, hi = Kc;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__fadd_rn(sp, lp[mid]) >= thr) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Locate j with pn[j] <= g < pn[j+1] within [lo, hi).
+DT_DI int find_parent(const int* pn, int lo, int hi, int g) {
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pn[mid] <= g) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
+                                                 const float* __restrict__ cand_lp,
+                                                 const int32_t* __restrict__ cand_id, int32_t* __restrict__ o_tok,
+                                                 int32_t* __restrict__ o_par, int32_t* __restrict__ o_dep,
+                                                 int32_t* __restrict__ o_rank, float* __restrict__ o_score,
+                                                 int32_t* __restrict__ o_n) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int red[NT / 32];
+    __shared__ float redf[NT / 32];
+    __shared__ int sh_jhi;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    Kn4Smem S = kn4_carve(smem, Kc, N);
+    const float* lpb = cand_lp + (size_t)b * L * Kc;
+
+    // root layer: Top-k of position 1
+    const int k1 = min(min(talon_k, Kc), N);
+    for (int i = tid; i < k1; i += NT) {
+        S.s[i] = lpb[i];
+        S.dep[i] = 1;
+        S.par[i] = -1;
+        S.rank[i] = i;
+        S.lex[i] = (uint32_t)i;
+    }
+    int nT = k1, lay_lo = 0, lay_hi = k1;
+    for (int d = 2; d <= L && nT < N; ++d) {
+        __syncthreads();
+        for (int w = tid; w < Kc; w += NT) S.lp[w] = lpb[(size_t)(d - 1) * Kc + w];
+        __syncthreads();
+        const int nP = lay_hi - lay_lo;
+        // anchor: best child score over the pool
+        float mx = -__int_as_float(0x7F800000);
+        for (int j = tid; j < nP; j += NT) mx = fmaxf(mx, __fadd_rn(S.s[lay_lo + j], S.lp[0]));
+        mx = dt_warp_max(mx);
+        if (lane == 0) redf[wid] = mx;
+        __syncthreads();
+        float m_d = redf[0];
+        for (int w = 1; w < NT / 32; ++w) m_d = fmaxf(m_d, redf[w]);
+        const float thr = __fadd_rn(m_d, log_mu);
+        for (int j = tid; j < nP; j += NT) S.pn[j] = count_pass(S.s[lay_lo + j], S.lp, Kc, thr);
+        __syncthreads();
+        dt_block_scan_array<NT>(S.pn, S.pn, nP, red);
+        const int m = S.pn[nP];
+        const int room = N - nT;
+        if (m <= room) {
+            // the whole passing pool becomes the next layer, in lexicographic order
+            for (int g = tid; g < m; g += NT) {
+                const int j = find_parent(S.pn, 0, nP, g);
+                const int w = g - S.pn[j];
+                const int x = nT + g;
+                S.s[x] = __fadd_rn(S.s[lay_lo + j], S.lp[w]);
+                S.dep[x] = d;
+                S.par[x] = lay_lo + j;
+                S.rank[x] = w;
+                S.lex[x] = ((uint32_t)j << 16) | (uint32_t)w;
+            }
+            lay_lo = nT;
+            lay_hi = nT + m;
+            nT += m;
+            continue;
+        }
+        // overflow: keep the best `room` of the pool, then stop
+        const int R = room;
+        int nR = 0;
+        int j_lo = 0;
+        while (j_lo < nP) {
+            __syncthreads();
+            // prune by the running cutoff once the running list is full
+            float thr2 = thr;
+            if (nR == R) thr2 = fmaxf(thr, dt_fkey_val((uint32_t)(S.cand[R - 1] >> 32)));
+            for (int j = tid; j < nP; j += NT)
+                S.pn[j] = (j < j_lo) ? 0 : count_pass(S.s[lay_lo + j], S.lp, Kc, thr2);
+            __syncthreads();
+            dt_block_scan_array<NT>(S.pn, S.pn, nP, red);
+            if (tid == 0) sh_jhi = j_lo + 1;
+            __syncthreads();
+            for (int j = j_lo + 1 + tid; j <= nP; j += NT)
+                if (S.pn[j] <= CAP - R) atomicMax(&sh_jhi, j);
+            __syncthreads();
+            const int j_hi = sh_jhi;
+            const int mg = S.pn[j_hi];
+            const int tot = nR + mg;
+            const int P2 = dt_pow2_ceil(R + mg);
+            for (int g = tid; g < mg; g += NT) {
+                const int j = find_parent(S.pn, j_lo, j_hi, g);
+                const int w = g - S.pn[j];
+                const float sc = __fadd_rn(S.s[lay_lo + j], S.lp[w]);
+                const uint32_t lx = ((uint32_t)j << 16) | (uint32_t)w;
+                S.cand[R + g] = ((unsigned long long)dt_fkey(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - lx);
+            }
+            for (int i = nR + tid; i < R; i += NT) S.cand[i] = 0ull;
+            for (int i = R + mg + tid; i < P2; i += NT) S.cand[i] = 0ull;
+            __syncthreads();
+            dt_bitonic_u64<NT>(S.cand, P2, true);
+            nR = min(R, tot);
+            j_lo = j_hi;
+        }
+        // selected keys -> lexicographic order -> nodes
+        __syncthreads();
+        const int Q2 = dt_pow2_ceil(nR);
+        for (int q = tid; q < Q2; q += NT) {
+            if (q < nR) {
+                const unsigned long long y = S.cand[q];
+                const uint32_t lx = 0xFFFFFFFFu - (uint32_t)y;
+                S.cand[q] = ((unsigned long long)lx << 32) | (y >> 32);
+            } else {
+                S.cand[q] = ~0ull;
+            }
+        }
+        __syncthreads();
+        dt_bitonic_u64<NT>(S.cand, Q2, false);
+        for (int q = tid; q < nR; q += NT) {
+            const unsigned long long y = S.cand[q];
+            const uint32_t lx = (uint32_t)(y >> 32);
+            const int j = (int)(lx >> 16), w = (int)(lx & 0xFFFFu);
+            const int x = nT + q;
+            S.s[x] = dt_fkey_val((uint32_t)(y & 0xFFFFFFFFull));
+            S.dep[x] = d;
+            S.par[x] = lay_lo + j;
+            S.rank[x] = w;
+            S.lex[x] = lx;
+        }
+        nT += nR;
+        break;
+    }
+    __syncthreads();
+
+    // final order: root, then the shared node order
+    const int Q2 = dt_pow2_ceil(nT);
+    for (int q = tid; q < Q2; q += NT) S.ord[q] = q < nT ? q : -1;
+    __syncthreads();
+    dt_bitonic_nodes<NT>(S.ord, Q2, S.s, S.dep, S.par, S.lex);
+    // output index of each node (reuse pn as the map)
+    for (int q = tid; q < nT; q += NT) S.pn[S.ord[q]] = q + 1;
+    __syncthreads();
+    const size_t ob = (size_t)b * Mmax;
+    for (int q = tid; q < nT; q += NT) {
+        const int x = S.ord[q];
+        const int dd = S.dep[x], rr = S.rank[x], p = S.par[x];
+        o_tok[ob + q + 1] = cand_id[((size_t)b * L + dd - 1) * Kc + rr];
+        o_par[ob + q + 1] = p < 0 ? 0 : S.pn[p];
+        o_dep[ob + q + 1] = dd;
+        o_rank[ob + q + 1] = rr;
+        o_score[ob + q + 1] = S.s[x];
+    }
+    if (tid == 0) {
+        o_tok[ob] = -1;
+        o_par[ob] = -1;
+        o_dep[ob] = 0;
+        o_rank[ob] = -1;
+        o_score[ob] = 0.f;
+        o_n[b] = nT + 1;
+    }
+}
+
+}  // namespace
+
+size_t dt_kn4_smem_bytes(int Kc, int N) {
+    int q2 = 1;
+    while (q2 < N) q2 <<= 1;
+    return (size_t)CAP * 8 + (size_t)((Kc + 3) & ~3) * 4 + (size_t)N * 20 + (size_t)(N + 1) * 4 + (size_t)q2 * 4 + 16;
+}
+
+cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
+                          const float* cand_lp, const int32_t* cand_id, int32_t* tok, int32_t* parent,
+                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, cudaStream_t st) {
+    const size_t smem = dt_kn4_smem_bytes(Kc, N);
+    cudaError_t e = cudaFuncSetAttribute(kn4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kn4_kernel<<<batch, NT, smem, st>>>(L, Kc, talon_k, log_mu, N, Mmax, cand_lp, cand_id, tok, parent, depth, rank,
+                                        score, n_nodes);
+    return cudaGetLastError();
+}

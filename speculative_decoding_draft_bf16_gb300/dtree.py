@@ -1,0 +1,251 @@
+"""Python binding of the draft-tree C ABI (include/dtree.h).
+
+Argument marshalling only: every step of build, mask and verify runs in the
+CUDA kernels of libdtree.so.  Tensors must be CUDA tensors, contiguous, of the
+documented dtype; the library writes into caller-owned buffers on the current
+torch stream (or the stream given).  A missing or unloadable library raises --
+there is no other code path.
+"""
+import ctypes
+import dataclasses
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+DT_MODE = {"ddtree": 0, "dartree": 1, "talon": 2}
+DT_BF16, DT_F32 = 0, 1
+DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_BESTFIRST = 0x1, 0x2, 0x4
+DT_DEV_VIOLATION_SHIFT = 8
+MAX_NODES = 1025
+MAX_KC = 1024
+
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+
+
+class BuildParams(ctypes.Structure):
+    _fields_ = [("mode", _i32), ("batch", _i32), ("L", _i32), ("V", _i32), ("dtype", _i32),
+                ("K", _i32), ("B", _i32), ("W", _i32), ("beta", ctypes.c_float), ("R", _i32),
+                ("U", _vp), ("Vt", _vp), ("root_tok", _vp), ("talon_k", _i32),
+                ("log_mu", ctypes.c_float), ("N", _i32)]
+
+
+class TreeStruct(ctypes.Structure):
+    _fields_ = [("max_nodes", _i32), ("Kc", _i32), ("L", _i32), ("node_tok", _vp), ("parent", _vp),
+                ("depth", _vp), ("rank", _vp), ("score", _vp), ("n_nodes", _vp), ("lse", _vp),
+                ("cand_id", _vp), ("cand_lp", _vp), ("status", _vp)]
+
+
+_LIB = None
+
+
+def lib():
+    """Load libdtree.so (compiling it first if it has never been built)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            path = _build.build()
+        L = ctypes.CDLL(path)
+        bp = ctypes.POINTER(BuildParams)
+        tp = ctypes.POINTER(TreeStruct)
+        L.dt_workspace_size.restype = ctypes.c_size_t
+        L.dt_workspace_size.argtypes = [bp, ctypes.POINTER(ctypes.c_int)]
+        L.dt_candidates.restype = _i32
+        L.dt_candidates.argtypes = [bp, _vp, tp, _vp]
+        L.dt_select.restype = _i32
+        L.dt_select.argtypes = [bp, tp, _vp, ctypes.c_size_t, _vp]
+        L.dt_build_tree.restype = _i32
+        L.dt_build_tree.argtypes = [bp, _vp, tp, _vp, ctypes.c_size_t, _vp]
+        L.dt_tree_mask.restype = _i32
+        L.dt_tree_mask.argtypes = [tp, _i32, _i32, _vp, _vp, _vp]
+        L.dt_verify.restype = _i32
+        L.dt_verify.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
+                                _vp]
+        L.dt_status_str.restype = ctypes.c_char_p
+        L.dt_status_str.argtypes = [_i32]
+        L.dt_version.restype = _i32
+        _LIB = L
+    return _LIB
+
+
+class DtError(RuntimeError):
+    pass
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise DtError("%s: %s (%d)" % (what, lib().dt_status_str(rc).decode(), rc))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return DT_BF16
+    if t.dtype == torch.float32:
+        return DT_F32
+    raise TypeError("logits must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _need(t, dtype=None, name="tensor"):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+@dataclasses.dataclass
+class Params:
+    """Build parameters; mirrors dt_build_params."""
+    mode: str
+    batch: int
+    L: int
+    V: int
+    dtype: str = "bf16"
+    K: int = 0
+    B: int = 0
+    W: int = 0
+    beta: float = 0.0
+    R: int = 0
+    U: torch.Tensor = None
+    Vt: torch.Tensor = None
+    root_tok: torch.Tensor = None
+    talon_k: int = 0
+    mu: float = 0.0
+    N: int = 0
+
+    @property
+    def Kc(self):
+        return min(self.N, self.V) if self.mode == "talon" else self.K
+
+    @property
+    def budget(self):
+        return self.N if self.mode == "talon" else self.B
+
+    def struct(self):
+        log_mu = 0.0
+        if self.mode == "talon":
+            log_mu = float(torch.tensor(math.log(self.mu), dtype=torch.float64).float())
+        return BuildParams(DT_MODE[self.mode], self.batch, self.L, self.V,
+                           DT_BF16 if self.dtype == "bf16" else DT_F32, self.K, self.B, self.W,
+                           self.beta, self.R if self.U is not None else 0, _ptr(self.U), _ptr(self.Vt),
+                           _ptr(self.root_tok), self.talon_k, log_mu, self.N)
+
+
+class TreeBuffers:
+    """Device buffers of a batch of trees (dt_tree)."""
+
+    def __init__(self, batch, L, Kc, max_nodes, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.batch, self.L, self.Kc, self.max_nodes = batch, L, Kc, max_nodes
+        self.node_tok = torch.full((batch, max_nodes), -1, **i32)
+        self.parent = torch.full((batch, max_nodes), -1, **i32)
+        self.depth = torch.zeros((batch, max_nodes), **i32)
+        self.rank = torch.full((batch, max_nodes), -1, **i32)
+        self.score = torch.zeros((batch, max_nodes), **f32)
+        self.n_nodes = torch.zeros((batch,), **i32)
+        self.lse = torch.zeros((batch, L), **f32)
+        self.cand_id = torch.zeros((batch, L, Kc), **i32)
+        self.cand_lp = torch.zeros((batch, L, Kc), **f32)
+        self.status = torch.zeros((batch,), **i32)
+
+    def struct(self):
+        return TreeStruct(self.max_nodes, self.Kc, self.L, *[
+            _ptr(getattr(self, f)) for f in ("node_tok", "parent", "depth", "rank", "score", "n_nodes",
+                                             "lse", "cand_id", "cand_lp", "status")])
+
+    @classmethod
+    def for_params(cls, p, max_nodes=None, device="cuda"):
+        return cls(p.batch, p.L, p.Kc, max_nodes or p.budget + 1, device)
+
+
+def workspace_size(p):
+    ok = ctypes.c_int(0)
+    n = lib().dt_workspace_size(ctypes.byref(p.struct()), ctypes.byref(ok))
+    if not ok.value:
+        raise DtError("invalid parameters for dt_workspace_size")
+    return int(n)
+
+
+def make_workspace(p, device="cuda"):
+    n = workspace_size(p)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device), n
+
+
+def candidates(p, draft_logits, tree, stream=None):
+    _need(draft_logits, name="draft_logits")
+    assert _dtype_code(draft_logits) == (DT_BF16 if p.dtype == "bf16" else DT_F32)
+    _check(lib().dt_candidates(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()),
+                               _stream(stream)), "dt_candidates")
+
+
+def select(p, tree, workspace=None, stream=None):
+    ws, n = (workspace if workspace is not None else (None, 0))
+    _check(lib().dt_select(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _ptr(ws), n, _stream(stream)),
+           "dt_select")
+
+
+def build_tree(p, draft_logits, tree, workspace=None, stream=None):
+    """Stage 1 + selection.  workspace: (tensor, bytes) from make_workspace (DARTree)."""
+    _need(draft_logits, name="draft_logits")
+    assert _dtype_code(draft_logits) == (DT_BF16 if p.dtype == "bf16" else DT_F32)
+    ws, n = (workspace if workspace is not None else (None, 0))
+    _check(lib().dt_build_tree(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()),
+                               _ptr(ws), n, _stream(stream)), "dt_build_tree")
+
+
+def tree_mask(tree, mask, pos, pos_offset=0, batch=None, stream=None):
+    _need(mask, torch.int32, "mask")
+    _need(pos, torch.int32, "pos")
+    _check(lib().dt_tree_mask(ctypes.byref(tree.struct()), batch or tree.batch, pos_offset, _ptr(mask), _ptr(pos),
+                              _stream(stream)), "dt_tree_mask")
+
+
+def alloc_mask(tree, device="cuda"):
+    words = (tree.max_nodes + 31) // 32
+    mask = torch.zeros((tree.batch, tree.max_nodes, words), dtype=torch.int32, device=device)
+    pos = torch.zeros((tree.batch, tree.max_nodes), dtype=torch.int32, device=device)
+    return mask, pos
+
+
+def verify(tree, target, temperature=0.0, draft=None, uniforms=None, out=None, visited_lse=None, batch=None,
+           target_lse=None, stream=None):
+    """Acceptance walk.  out = (acc_nodes [b, L+1], acc_len [b], next_tok [b]) int32 tensors;
+    target_lse: optional [b, max_nodes] fp32 normalisers of the target rows (T=1)."""
+    _need(target, name="target")
+    batch = batch or tree.batch
+    V = target.shape[-1]
+    if out is None:
+        out = alloc_verify_out(tree)
+    acc_nodes, acc_len, next_tok = out
+    if draft is not None:
+        _need(draft, name="draft")
+    if uniforms is not None:
+        _need(uniforms, torch.float32, "uniforms")
+    if target_lse is not None:
+        _need(target_lse, torch.float32, "target_lse")
+    _check(lib().dt_verify(ctypes.byref(tree.struct()), batch, V, _dtype_code(target), _ptr(target),
+                           _ptr(target_lse), _ptr(draft), float(temperature), _ptr(uniforms), _ptr(acc_nodes),
+                           _ptr(acc_len), _ptr(next_tok), _ptr(visited_lse), _stream(stream)), "dt_verify")
+    return out
+
+
+def alloc_verify_out(tree, device="cuda"):
+    return (torch.full((tree.batch, tree.L + 1), -1, dtype=torch.int32, device=device),
+            torch.zeros((tree.batch,), dtype=torch.int32, device=device),
+            torch.zeros((tree.batch,), dtype=torch.int32, device=device))

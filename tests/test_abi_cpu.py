@@ -1,0 +1,120 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every
+function include/dtree.h declares, and rejects invalid arguments on the host
+before anything touches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from speculative_decoding_draft_bf16_gb300 import dtree
+
+HEADER = os.path.join(ROOT, "include", "dtree.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dt_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("dt_candidates", "dt_select", "dt_build_tree", "dt_tree_mask", "dt_verify", "dt_workspace_size",
+              "dt_status_str", "dt_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = dtree.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_static_strings_and_version():
+    L = dtree.lib()
+    assert L.dt_version() >= 100
+    assert L.dt_status_str(0) == b"ok"
+    assert L.dt_status_str(-1) == b"invalid argument"
+    assert L.dt_status_str(-4).startswith(b"CUDA")
+
+
+def _params(**kw):
+    base = dict(mode="ddtree", batch=1, L=4, V=32, dtype="f32", K=4, B=8)
+    base.update(kw)
+    return dtree.Params(**base)
+
+
+class _FakeTree:
+    """A dt_tree with non-NULL fake device pointers: host validation never
+    dereferences them, and every case below fails validation first."""
+
+    def __init__(self, batch, L, Kc, max_nodes):
+        self.batch, self.L, self.Kc, self.max_nodes = batch, L, Kc, max_nodes
+
+    def struct(self):
+        p = [ctypes.c_void_p(0x1000 + 16 * i) for i in range(10)]
+        return dtree.TreeStruct(self.max_nodes, self.Kc, self.L, *p)
+
+
+def _call_build(p, tree, logits_ptr=0x2000):
+    return dtree.lib().dt_build_tree(ctypes.byref(p.struct()), ctypes.c_void_p(logits_ptr),
+                                     ctypes.byref(tree.struct()), None, 0, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(batch=0), dict(L=0), dict(L=33), dict(V=0), dict(K=0), dict(K=33), dict(B=0), dict(B=1025),
+    dict(mode="talon", N=0, talon_k=1, mu=0.5), dict(mode="talon", N=10, talon_k=11, mu=0.5),
+    dict(mode="dartree", W=0, K=4, B=8), dict(mode="dartree", W=4, K=4, B=8, beta=0.5),
+    dict(mode="dartree", W=2000, K=4, B=8),
+])
+def test_build_rejects_invalid_params(bad):
+    p = _params(**bad)
+    Kc = p.Kc if p.Kc > 0 else 1
+    tree = _FakeTree(max(p.batch, 1), max(p.L, 1), Kc, max(min(p.budget + 1, 1025), 1))
+    assert _call_build(p, tree) == -1
+
+
+def test_build_rejects_mismatched_tree_and_null_pointers():
+    p = _params()
+    assert _call_build(p, _FakeTree(1, 4, 5, 9)) == -1      # Kc != K
+    assert _call_build(p, _FakeTree(1, 3, 4, 9)) == -1      # L mismatch
+    assert _call_build(p, _FakeTree(1, 4, 4, 8)) == -1      # max_nodes < B + 1
+    assert _call_build(p, _FakeTree(1, 4, 4, 9), logits_ptr=0) == -1  # NULL logits
+    L = dtree.lib()
+    assert L.dt_build_tree(None, None, None, None, 0, None) == -1
+
+
+def test_unsupported_sizes():
+    p = _params(V=16 * 32768 + 1, K=4)
+    assert _call_build(p, _FakeTree(1, 4, 4, 9)) == -2
+
+
+def test_mask_and_verify_reject_invalid_arguments():
+    L = dtree.lib()
+    t = _FakeTree(1, 4, 4, 9).struct()
+    fake = ctypes.c_void_p(0x3000)
+    assert L.dt_tree_mask(ctypes.byref(t), 0, 0, fake, fake, None) == -1
+    assert L.dt_tree_mask(ctypes.byref(t), 1, 0, None, fake, None) == -1
+    t_big = _FakeTree(1, 4, 4, 1026).struct()
+    assert L.dt_tree_mask(ctypes.byref(t_big), 1, 0, fake, fake, None) == -1
+    # verify: temperature other than 0/1, NULL target, T=1 without uniforms
+    args = lambda temp, tgt, drf, uni: L.dt_verify(ctypes.byref(t), 1, 32, 1, tgt, None, drf, ctypes.c_float(temp),
+                                                   uni, fake, fake, fake, None, None)
+    assert args(0.5, fake, fake, fake) == -2
+    assert args(0.0, None, None, None) == -1
+    assert args(1.0, fake, None, fake) == -1
+    assert args(1.0, fake, fake, None) == -1
+
+
+def test_workspace_size():
+    assert dtree.workspace_size(_params()) == 0
+    assert dtree.workspace_size(_params(mode="talon", N=60, talon_k=10, mu=0.03)) == 0
+    # DARTree with a Markov term: batch * L * K * K * 4 bytes
+    import torch
+    U = torch.zeros((32, 8))
+    p = _params(mode="dartree", batch=3, L=4, K=4, W=4, B=8, R=8)
+    p.U = U
+    p.Vt = U
+    assert dtree.workspace_size(p) == 3 * 4 * 4 * 4 * 4
