@@ -11,9 +11,9 @@ against target rows whose spike matches the drafter's with probability 0.8.
 
 Timing: every step reads a different copy of the inputs (rotating copies
 whose drafter logits alone exceed twice the L2 size, so no step reads logits
-another step left in L2); each copy's step is captured once in a CUDA graph
-and replayed; CUDA events on the launching stream bracket exactly K steps,
-with a barrier and a device synchronise on both sides; max over ranks.
+another step left in L2); one CUDA graph holds the steps of a pass over all
+copies and is replayed; CUDA events on the launching stream bracket exactly K
+steps, with a barrier and a device synchronise on both sides; max over ranks.
 
 Prints one JSON line.  --impl reference times the CPU oracle (the plain
 restatement the tests check the kernels against) on the host cores instead.
@@ -58,11 +58,29 @@ def workloads():
     }
 
 
+def max_over_ranks(value, world, device="cpu"):
+    """Largest value over all ranks (replicas are timed independently; the job
+    takes as long as its slowest rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(steps, batch_per_rank, world, max_ms):
+    """Whole-job trees/s: every rank's trees over the slowest rank's time."""
+    return steps * batch_per_rank * world / (max_ms / 1000.0)
+
+
 def parse():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--copies", type=int, default=0, help="rotating input copies (0: enough to exceed 2x L2)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="single_request_B256")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -98,7 +116,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -156,6 +174,8 @@ def run_ours(args, wl, rank, world, local):
     target_bytes = wl.batch * Mmax * wl.V * esize
     R = max(2, math.ceil(2 * L2_BYTES / draft_bytes))
     R = min(R, max(2, int(40e9 // max(target_bytes, 1))))
+    if args.copies > 0:
+        R = args.copies
     temperature = wl.temperature
 
     # rotating copies: distinct requests per copy and per rank
@@ -188,27 +208,38 @@ def run_ours(args, wl, rank, world, local):
 
     stream = torch.cuda.Stream(device=dev)
 
-    def capture(stages):
-        graphs = []
-        for c in copies:
-            step(c, stages)  # eager warm call (sets kernel attributes)
-        torch.cuda.synchronize()
-        for c in copies:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
+    def capture(stages, n_copies):
+        """One CUDA graph running `stages` on copies 0..n_copies-1 in order."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in copies[:n_copies]:
                 step(c, stages)
-            graphs.append(g)
-        torch.cuda.synchronize()
-        return graphs
+        return g
 
     def barrier():
         if world > 1:
             dist.barrier()
 
-    def timed(graphs, n, warm):
+    def run_steps(stages, n, graphs):
+        """Enqueue exactly n steps: full passes over the copies, then a prefix."""
+        full, rem = divmod(n, R)
+        for _ in range(full):
+            graphs[R].replay()
+        if rem:
+            if rem not in graphs:
+                graphs[rem] = capture(stages, rem)
+            graphs[rem].replay()
+
+    def timed(stages, n, warm):
+        for c in copies:
+            step(c, stages)  # eager call first (kernel attributes are set outside capture)
+        torch.cuda.synchronize()
+        graphs = {R: capture(stages, R)}
+        for k in {n % R, warm % R} - {0}:
+            graphs[k] = capture(stages, k)
+        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            for i in range(warm):
-                graphs[i % len(graphs)].replay()
+            run_steps(stages, warm, graphs)
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
@@ -216,33 +247,32 @@ def run_ours(args, wl, rank, world, local):
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for i in range(n):
-                graphs[i % len(graphs)].replay()
+            run_steps(stages, n, graphs)
             e1.record(stream)
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        del graphs
         return ms
 
-    full = capture(("build", "mask", "verify"))
     clocks = ClockSampler(local)
+    full_stages = ("build", "mask", "verify")
+    # the clock sampler runs over the timed region only
+    for c in copies:
+        step(c, full_stages)
+    torch.cuda.synchronize()
     clocks.start()
-    ms = timed(full, args.steps, args.warmup)
+    time.sleep(0.3)  # let the sampler take its first reading
+    ms = timed(full_stages, args.steps, args.warmup)
     clk = clocks.stop()
 
     # per-stage device time (same rotating inputs, graphs of one stage)
     stage_us = {}
     for name, stages in (("candidates", ("cand",)), ("select", ("select",)), ("mask", ("mask",)),
                          ("verify", ("verify",))):
-        g = capture(stages)
-        n = max(args.steps, 2 * len(g))
-        stage_us[name] = timed(g, n, max(args.warmup, 3)) * 1000.0 / n
-        del g
+        n = max(R, (args.steps // R) * R)
+        stage_us[name] = timed(stages, n, R) * 1000.0 / n
 
     # end to end: pinned host inputs copied in, results copied out, every step
     e2e = None
@@ -282,12 +312,8 @@ def run_ours(args, wl, rank, world, local):
                 e2e_step(i)
             e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": args.e2e_steps * wl.batch * world / (ems / 1000.0), "unit": "trees/s",
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": job_throughput(args.e2e_steps, wl.batch, world, ems), "unit": "trees/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     status = sum(int(c["tree"].status.abs().sum()) for c in copies)
@@ -305,7 +331,7 @@ def run_ours(args, wl, rank, world, local):
     traffic = KN1_TRAFFIC.get(hashlib.sha1(src).hexdigest())
     result = {
         "metric": METRIC,
-        "value": args.steps * wl.batch * world / (ms / 1000.0),
+        "value": job_throughput(args.steps, wl.batch, world, ms),
         "unit": "trees/s",
         "n_gpus": world,
         "steps": args.steps,

@@ -65,10 +65,13 @@ enum { DT_BF16 = 0, DT_F32 = 1 };
 #define DT_MAX_NODES 1025
 #define DT_MAX_V (16 * 32768)
 
-/* Device status word bits (dt_tree.status[b]).  dt_build_tree stores a fresh
- * value per request; dt_tree_mask and dt_verify OR their bits into it. */
+/* Device status word bits (dt_tree.status[b]).  dt_select (and so
+ * dt_build_tree) stores a fresh value per request; dt_tree_mask and dt_verify
+ * OR their bits into it. */
 #define DT_DEV_BAD_TREE 0x1         /* mask/verify: parent/depth arrays invalid */
-#define DT_DEV_TIMEOUT 0x2          /* a bounded wait gave up; outputs undefined */
+#define DT_DEV_TIMEOUT 0x2          /* a bounded wait gave up; outputs undefined
+                                       (stage 1 marks such a row with a NaN lse,
+                                       which dt_select reports with this bit) */
 #define DT_DEV_BESTFIRST 0x4        /* DARTree: TopB(S) was not a topologically
                                        ordered tree; the best-first heap over S
                                        was used (see dt_build_tree) */
@@ -137,7 +140,8 @@ size_t dt_workspace_size(const dt_build_params* p, int* ok);
  * Writes tree->lse [b][L] (fp32 accumulation of sum exp(x - max)),
  * tree->cand_id / cand_lp [b][L][Kc] (rank order: logit descending, token id
  * ascending on equal logits; lp = logit - lse in fp32).  Kc = tree->Kc must be
- * K (DDTree/DARTree) or min(N, V) (TALON). */
+ * K (DDTree/DARTree) or min(N, V) (TALON).  Does not touch tree->status; a row
+ * whose staging wait exceeded its bound gets lse = NaN. */
 dt_status dt_candidates(const dt_build_params* p, const void* draft_logits,
                         dt_tree* tree, dt_stream_t stream);
 

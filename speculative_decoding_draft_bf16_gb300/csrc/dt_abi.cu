@@ -111,11 +111,8 @@ dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_t
     const int chunk = chunk_of(p->V, S, p->dtype);
     const int esize = p->dtype == DT_BF16 ? 2 : 4;
     if (dt_kn1_smem_bytes(chunk, Kc, esize) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
-    cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(t->status, 0, sizeof(int32_t) * (size_t)p->batch, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    e = dt_kn1_launch(draft_logits, p->dtype, (int)rows, p->L, p->V, Kc, S, chunk, t->lse, t->cand_id, t->cand_lp,
-                      t->status, st);
+    cudaError_t e = dt_kn1_launch(draft_logits, p->dtype, (int)rows, p->L, p->V, Kc, S, chunk, t->lse, t->cand_id,
+                                  t->cand_lp, (cudaStream_t)stream);
     return cuda_status(e);
 }
 
@@ -128,23 +125,24 @@ dt_status dt_select(const dt_build_params* p, dt_tree* t, void* workspace, size_
     const int Mmax = t->max_nodes;
     switch (p->mode) {
         case DT_MODE_DDTREE:
-            if (dt_kn2_smem_bytes(p->K, p->B) > kSmemMax) return DT_ERR_UNSUPPORTED;
-            e = dt_kn2_launch(p->batch, p->L, p->K, p->B, Mmax, t->cand_lp, t->cand_id, t->node_tok, t->parent,
-                              t->depth, t->rank, t->score, t->n_nodes, st);
+            if (dt_kn2_smem_bytes(p->L, p->K, p->B) > kSmemMax) return DT_ERR_UNSUPPORTED;
+            e = dt_kn2_launch(p->batch, p->L, p->K, p->B, Mmax, t->cand_lp, t->cand_id, t->lse, t->node_tok,
+                              t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, st);
             break;
         case DT_MODE_DARTREE: {
             const size_t need = dt_workspace_size(p, nullptr);
             if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
             const bool term = p->R > 0 && p->U;
             e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt, p->root_tok,
-                              Mmax, t->cand_lp, t->cand_id, term ? (float*)workspace : nullptr, t->node_tok,
+                              Mmax, t->cand_lp, t->cand_id, t->lse, term ? (float*)workspace : nullptr, t->node_tok,
                               t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, st);
             break;
         }
         case DT_MODE_TALON:
             if (dt_kn4_smem_bytes(kc_of(p), p->N) > kSmemMax) return DT_ERR_UNSUPPORTED;
             e = dt_kn4_launch(p->batch, p->L, kc_of(p), p->talon_k, p->log_mu, p->N, Mmax, t->cand_lp, t->cand_id,
-                              t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, st);
+                              t->lse, t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status,
+                              st);
             break;
     }
     return cuda_status(e);

@@ -176,6 +176,27 @@ DT_DI void dt_bitonic_u64(unsigned long long* a, int n, bool desc) {
     }
 }
 
+// Sort n <= 32 64-bit keys in shared memory with warp 0 only (shuffles, no
+// block barriers inside); descending when desc.  Ends with __syncthreads.
+DT_DI void dt_warp_sort_u64(unsigned long long* a, int n, bool desc) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        // pad: sorts after every real key
+        unsigned long long x = (lane < n) ? a[lane] : (desc ? 0ull : ~0ull);
+        for (int k = 2; k <= 32; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+                const bool lower = (lane & j) == 0;
+                const bool up = ((lane & k) == 0) == desc;  // larger first in this run
+                const bool take_max = (lower == up);
+                x = take_max ? (x > y ? x : y) : (x < y ? x : y);
+            }
+        }
+        if (lane < n) a[lane] = x;
+    }
+    __syncthreads();
+}
+
 DT_DI int dt_pow2_ceil(int n) {
     int p = 1;
     while (p < n) p <<= 1;
@@ -214,15 +235,26 @@ DT_DI bool dt_mbar_wait(uint64_t* bar, uint32_t phase) {
     const long long t0 = clock64();
     for (;;) {
         uint32_t done;
+        // the hint lets the hardware suspend the thread until the phase
+        // completes (up to ~10 ms) instead of returning at once, so waiting
+        // warps do not take issue slots from co-resident work
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
-            : "r"(a), "r"(phase)
+            : "r"(a), "r"(phase), "r"(10000000u)
             : "memory");
         if (done) return true;
         if (clock64() - t0 > DT_WAIT_BUDGET) return false;
     }
 }
+
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel in the stream is finishing.
+// dt_pdl_wait() blocks until all prerequisite grids have completed and their
+// memory is visible -- it must precede the first read of any input;
+// dt_pdl_trigger() lets the next kernel in the stream be scheduled.
+DT_DI void dt_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DT_DI void dt_pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Stage elements [lo, hi) of a row into shared memory.  The shared buffer
 // `sbase` must be 16-byte aligned with room for (hi - lo) elements + 16 bytes;

@@ -5,30 +5,60 @@
 #include <stddef.h>
 #include <stdint.h>
 
+// Launch configuration shared by every kernel: programmatic stream
+// serialisation (the kernel may start while its predecessor finishes; it
+// calls griddepcontrol.wait before reading inputs) and an optional cluster.
+struct DtLaunch {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    DtLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_x = 0) {
+        cfg = cudaLaunchConfig_t{};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        int n = 0;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+        if (cluster_x > 0) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = cluster_x;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = n;
+    }
+};
+
 // Stage 1 (kn1_candidates.cu).
 size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize);
 cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int L, int V, int Kc, int S, int chunk,
-                          float* lse, int32_t* cand_id, float* cand_lp, int32_t* status, cudaStream_t st);
+                          float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st);
 
 // DDTree selection (kn2_ddtree.cu).
-size_t dt_kn2_smem_bytes(int K, int B);
+size_t dt_kn2_smem_bytes(int L, int K, int B);
 cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
-                          int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
-                          int32_t* n_nodes, cudaStream_t st);
+                          const float* lse, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
+                          float* score, int32_t* n_nodes, int32_t* status, cudaStream_t st);
 
 // DARTree Markov table + selection (kn3_dartree.cu).
 size_t dt_kn3_table_smem_bytes(int K, int R);
 size_t dt_kn3_select_smem_bytes(int L, int K, int W);
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
-                          const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp, const int32_t* cand_id,
-                          float* table, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
-                          int32_t* n_nodes, int32_t* status, cudaStream_t st);
+                          const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
+                          const int32_t* cand_id, const float* lse, float* table, int32_t* tok, int32_t* parent,
+                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, int32_t* status,
+                          cudaStream_t st);
 
 // TALON selection (kn4_talon.cu).
 size_t dt_kn4_smem_bytes(int Kc, int N);
 cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
-                          const float* cand_lp, const int32_t* cand_id, int32_t* tok, int32_t* parent,
-                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, cudaStream_t st);
+                          const float* cand_lp, const int32_t* cand_id, const float* lse, int32_t* tok,
+                          int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
+                          int32_t* status, cudaStream_t st);
 
 // Tree mask (kn5_mask.cu).
 size_t dt_kn5_smem_bytes(int Mmax);

@@ -42,12 +42,16 @@ struct Kn2Smem {
     unsigned long long* cand;  // [CAP]
 };
 
-DT_DI Kn2Smem carve(unsigned char* s, int K, int B) {
+// All positions' lp rows are staged up front when they fit in this budget.
+constexpr int LP_ALL_BYTES = 64 * 1024;
+
+DT_DI Kn2Smem carve(unsigned char* s, int L, int K, int B) {
     Kn2Smem m;
     m.cand = (unsigned long long*)s;
     s += (size_t)CAP * 8;
     m.lp = (float*)s;
-    s += (size_t)((K + 3) & ~3) * 4;
+    const int rows = ((size_t)L * K * 4 <= LP_ALL_BYTES) ? L : 1;
+    s += (size_t)((rows * K + 3) & ~3) * 4;
     m.cs = (float*)s; s += (size_t)2 * B * 4;
     m.cpar = (int*)s; s += (size_t)2 * B * 4;
     m.crank = (int*)s; s += (size_t)2 * B * 4;
@@ -75,17 +79,35 @@ DT_DI bool c_before_cand(int i, unsigned long long y, int d, const float* cs, co
 }
 
 __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_lp,
-                                                 const int32_t* __restrict__ cand_id, int L, int K, int B, int Mmax,
+                                                 const int32_t* __restrict__ cand_id,
+                                                 const float* __restrict__ lse, int L, int K, int B, int Mmax,
                                                  int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
                                                  int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
-                                                 float* __restrict__ o_score, int32_t* __restrict__ o_n) {
+                                                 float* __restrict__ o_score, int32_t* __restrict__ o_n,
+                                                 int32_t* __restrict__ status) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int red[NT / 32];
     __shared__ int sh_nP, sh_lrhi, sh_any;
+    __shared__ float chain[DT_MAX_L + 1];  // score of the rank-0 chain to each depth
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
-    Kn2Smem S = carve(smem, K, B);
+    Kn2Smem S = carve(smem, L, K, B);
+    dt_pdl_trigger();
+    dt_pdl_wait();
     const float* lpb = cand_lp + (size_t)b * L * K;
+    const bool lp_all = (size_t)L * K * 4 <= LP_ALL_BYTES;
+    if (lp_all)
+        for (int i = tid; i < L * K; i += NT) S.lp[i] = lpb[i];
+    if (tid == 0) {
+        // every depth-d prefix scores at most the rank-0 chain (lp is sorted
+        // within a position and fp32 addition is monotone)
+        float u = 0.f;
+        chain[0] = 0.f;
+        for (int d = 1; d <= L; ++d) {
+            u = __fadd_rn(u, lpb[(size_t)(d - 1) * K]);
+            chain[d] = u;
+        }
+    }
 
     // depth 1: the root's children are the first min(K, B) ranks, already in order
     int nC = min(K, B);
@@ -100,29 +122,54 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
     __syncthreads();
 
     for (int d = 2; d <= L; ++d) {
-        // ---- parents: depth-(d-1) members of C in lexicographic order ------
+        const bool full0 = (nC == B);
+        const float tau0 = full0 ? (S.cs + cur * B)[B - 1] : 0.f;
+        // nothing at this depth or below can reach the current B-th score
+        if (full0 && chain[d] < tau0) break;
+        const float* lpd = S.lp;
+        if (lp_all) {
+            lpd = S.lp + (size_t)(d - 1) * K;
+        } else {
+            __syncthreads();
+            for (int r = tid; r < K; r += NT) S.lp[r] = lpb[(size_t)(d - 1) * K + r];
+            __syncthreads();
+        }
+        // ---- parents: depth-(d-1) members of C whose best child can still
+        // enter, in lexicographic order ----------------------------------------
         {
+            const float lp0 = lpd[0];
             int cnt_local = 0;
-            for (int i = tid; i < nC; i += NT) cnt_local += ((S.cdep + cur * B)[i] == d - 1);
+            for (int i = tid; i < nC; i += NT)
+                cnt_local += ((S.cdep + cur * B)[i] == d - 1) &&
+                             (!full0 || __fadd_rn((S.cs + cur * B)[i], lp0) >= tau0);
             // compact with a scan over a per-thread strided layout
             int tot;
             int ex = dt_block_excl_scan<NT>(cnt_local, red, &tot);
             int w = ex;
             for (int i = tid; i < nC; i += NT)
-                if ((S.cdep + cur * B)[i] == d - 1)
+                if ((S.cdep + cur * B)[i] == d - 1 && (!full0 || __fadd_rn((S.cs + cur * B)[i], lp0) >= tau0))
                     S.cand[w++] = ((unsigned long long)(S.clex + cur * B)[i] << 32) | (unsigned)i;
-            const int P2 = dt_pow2_ceil(tot);
-            for (int i = tot + tid; i < P2; i += NT) S.cand[i] = ~0ull;
-            if (tid == 0) sh_nP = tot;
+            if (tid == 0) { sh_nP = tot; sh_any = 0; }
             __syncthreads();
-            dt_bitonic_u64<NT>(S.cand, P2, false);
+            // already in lexicographic order (e.g. the depth-1 nodes)? then no sort
+            for (int i = tid; i + 1 < tot; i += NT)
+                if (S.cand[i] > S.cand[i + 1]) sh_any = 1;
+            __syncthreads();
+            if (sh_any) {
+                if (tot <= 32) {
+                    dt_warp_sort_u64(S.cand, tot, false);
+                } else {
+                    const int P2 = dt_pow2_ceil(tot);
+                    for (int i = tot + tid; i < P2; i += NT) S.cand[i] = ~0ull;
+                    __syncthreads();
+                    dt_bitonic_u64<NT>(S.cand, P2, false);
+                }
+            }
             for (int j = tid; j < tot; j += NT) S.pidx[j] = (int)(S.cand[j] & 0xFFFFFFFFull);
             __syncthreads();
         }
         const int nP = sh_nP;
         if (nP == 0) break;
-        for (int r = tid; r < K; r += NT) S.lp[r] = lpb[(size_t)(d - 1) * K + r];
-        __syncthreads();
 
         int lr_lo = 0;
         while (lr_lo < nP) {
@@ -140,7 +187,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                         int lo = 0, hi = K;
                         while (lo < hi) {
                             int mid = (lo + hi) >> 1;
-                            if (__fadd_rn(sp, S.lp[mid]) >= tau) lo = mid + 1;
+                            if (__fadd_rn(sp, lpd[mid]) >= tau) lo = mid + 1;
                             else hi = mid;
                         }
                         cnt = lo;
@@ -171,14 +218,19 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     }
                     const int j = lo;
                     const int r = g - S.pn[j];
-                    const float s = __fadd_rn((S.cs + cur * B)[S.pidx[j]], S.lp[r]);
+                    const float s = __fadd_rn((S.cs + cur * B)[S.pidx[j]], lpd[r]);
                     const uint32_t lex = ((uint32_t)j << 16) | (uint32_t)r;
                     S.cand[idx] = ((unsigned long long)dt_fkey(s) << 32) | (unsigned long long)(0xFFFFFFFFu - lex);
                 }
-                const int P2 = dt_pow2_ceil(m);
-                for (int i = m + tid; i < P2; i += NT) S.cand[i] = 0ull;
                 __syncthreads();
-                dt_bitonic_u64<NT>(S.cand, P2, true);
+                if (m <= 32) {
+                    dt_warp_sort_u64(S.cand, m, true);
+                } else {
+                    const int P2 = dt_pow2_ceil(m);
+                    for (int i = m + tid; i < P2; i += NT) S.cand[i] = 0ull;
+                    __syncthreads();
+                    dt_bitonic_u64<NT>(S.cand, P2, true);
+                }
                 const int mm = min(m, B);
                 // merge path: new position of every C member ...
                 for (int i = tid; i < nC; i += NT) {
@@ -266,21 +318,30 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
         o_rank[ob] = -1;
         o_score[ob] = 0.f;
         o_n[b] = nC + 1;
+        int bits = 0;
+        for (int l = 0; l < L; ++l) {
+            const float v = lse[(size_t)b * L + l];
+            if (v != v) bits |= DT_DEV_TIMEOUT;  // stage 1 flagged this row
+        }
+        status[b] = bits;
     }
 }
 
 }  // namespace
 
-size_t dt_kn2_smem_bytes(int K, int B) {
-    return (size_t)CAP * 8 + (size_t)((K + 3) & ~3) * 4 + (size_t)B * 4 * 10 + (size_t)B * 8 + (size_t)(B + 1) * 4 + 16;
+size_t dt_kn2_smem_bytes(int L, int K, int B) {
+    const int rows = ((size_t)L * K * 4 <= LP_ALL_BYTES) ? L : 1;
+    return (size_t)CAP * 8 + (size_t)((rows * K + 3) & ~3) * 4 + (size_t)B * 4 * 10 + (size_t)B * 8 +
+           (size_t)(B + 1) * 4 + 16;
 }
 
 cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
-                          int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
-                          int32_t* n_nodes, cudaStream_t st) {
-    const size_t smem = dt_kn2_smem_bytes(K, B);
+                          const float* lse, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
+                          float* score, int32_t* n_nodes, int32_t* status, cudaStream_t st) {
+    const size_t smem = dt_kn2_smem_bytes(L, K, B);
     cudaError_t e = cudaFuncSetAttribute(kn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kn2_kernel<<<batch, NT, smem, st>>>(cand_lp, cand_id, L, K, B, Mmax, tok, parent, depth, rank, score, n_nodes);
-    return cudaGetLastError();
+    DtLaunch lc(dim3(batch), dim3(NT), smem, st);
+    return cudaLaunchKernelEx(&lc.cfg, kn2_kernel, cand_lp, cand_id, lse, L, K, B, Mmax, tok, parent, depth, rank,
+                              score, n_nodes, status);
 }

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(NT_TAB) kn3_table_kernel(int L, int K, int R, 
     extern __shared__ __align__(128) unsigned char smem[];
     const int d = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int Rp = R | 1;  // odd row stride: conflict-free column reads
+    dt_pdl_trigger();
+    dt_pdl_wait();
     float* Us = (float*)smem;
     float* Vs = Us + (size_t)K * Rp;
     int np;
@@ -110,6 +112,7 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
                                                         const int32_t* __restrict__ root_tok, int V,
                                                         int Mmax, const float* __restrict__ cand_lp,
                                                         const int32_t* __restrict__ cand_id,
+                                                        const float* __restrict__ lse,
                                                         const float* __restrict__ table,
                                                         int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
                                                         int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
@@ -120,6 +123,8 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
     __shared__ int sh_bad, sh_viol;
     const int b = blockIdx.x, tid = threadIdx.x;
     Kn3Smem S = kn3_carve(smem, L, K, W);
+    dt_pdl_trigger();
+    dt_pdl_wait();
     const float* lpb = cand_lp + (size_t)b * L * K;
     const int rt = root_tok ? root_tok[b] : -1;
     const bool term1 = use_table && rt >= 0 && rt < V;
@@ -289,7 +294,11 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
         int bits = sh_bad ? DT_DEV_BESTFIRST : 0;
         const int v = sh_viol < (1 << 23) - 1 ? sh_viol : (1 << 23) - 1;
         bits |= v << DT_DEV_VIOLATION_SHIFT;
-        if (bits) atomicOr(&status[b], bits);
+        for (int l = 0; l < L; ++l) {
+            const float x = lse[(size_t)b * L + l];
+            if (x != x) bits |= DT_DEV_TIMEOUT;  // stage 1 flagged this row
+        }
+        status[b] = bits;
     }
 }
 
@@ -305,9 +314,10 @@ size_t dt_kn3_select_smem_bytes(int L, int K, int W) {
 }
 
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
-                          const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp, const int32_t* cand_id,
-                          float* table, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
-                          int32_t* n_nodes, int32_t* status, cudaStream_t st) {
+                          const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
+                          const int32_t* cand_id, const float* lse, float* table, int32_t* tok, int32_t* parent,
+                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, int32_t* status,
+                          cudaStream_t st) {
     cudaError_t e;
     const int use_table = (R > 0 && table != nullptr) ? 1 : 0;
     if (use_table) {
@@ -315,14 +325,16 @@ cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float be
         if ((e = cudaFuncSetAttribute(kn3_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) !=
             cudaSuccess)
             return e;
-        kn3_table_kernel<<<dim3(L, batch), NT_TAB, sm, st>>>(L, K, R, V, U, Vt, root_tok, cand_id, table);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        DtLaunch lt(dim3(L, batch), dim3(NT_TAB), sm, st);
+        if ((e = cudaLaunchKernelEx(&lt.cfg, kn3_table_kernel, L, K, R, V, U, Vt, root_tok, cand_id, table)) !=
+            cudaSuccess)
+            return e;
     }
     const size_t sm = dt_kn3_select_smem_bytes(L, K, W);
     if ((e = cudaFuncSetAttribute(kn3_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) !=
         cudaSuccess)
         return e;
-    kn3_select_kernel<<<batch, NT, sm, st>>>(L, K, W, B, beta, use_table, root_tok, V, Mmax, cand_lp,
-                                             cand_id, table, tok, parent, depth, rank, score, n_nodes, status);
-    return cudaGetLastError();
+    DtLaunch ls(dim3(batch), dim3(NT), sm, st);
+    return cudaLaunchKernelEx(&ls.cfg, kn3_select_kernel, L, K, W, B, beta, use_table, root_tok, V, Mmax, cand_lp,
+                              cand_id, lse, (const float*)table, tok, parent, depth, rank, score, n_nodes, status);
 }

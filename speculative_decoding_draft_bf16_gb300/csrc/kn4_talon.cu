@@ -78,16 +78,19 @@ DT_DI int find_parent(const int* pn, int lo, int hi, int g) {
 
 __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
                                                  const float* __restrict__ cand_lp,
-                                                 const int32_t* __restrict__ cand_id, int32_t* __restrict__ o_tok,
-                                                 int32_t* __restrict__ o_par, int32_t* __restrict__ o_dep,
-                                                 int32_t* __restrict__ o_rank, float* __restrict__ o_score,
-                                                 int32_t* __restrict__ o_n) {
+                                                 const int32_t* __restrict__ cand_id, const float* __restrict__ lse,
+                                                 int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
+                                                 int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
+                                                 float* __restrict__ o_score, int32_t* __restrict__ o_n,
+                                                 int32_t* __restrict__ status) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int red[NT / 32];
     __shared__ float redf[NT / 32];
     __shared__ int sh_jhi;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     Kn4Smem S = kn4_carve(smem, Kc, N);
+    dt_pdl_trigger();
+    dt_pdl_wait();
     const float* lpb = cand_lp + (size_t)b * L * Kc;
 
     // root layer: Top-k of position 1
@@ -227,6 +230,12 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
         o_rank[ob] = -1;
         o_score[ob] = 0.f;
         o_n[b] = nT + 1;
+        int bits = 0;
+        for (int l = 0; l < L; ++l) {
+            const float x = lse[(size_t)b * L + l];
+            if (x != x) bits |= DT_DEV_TIMEOUT;  // stage 1 flagged this row
+        }
+        status[b] = bits;
     }
 }
 
@@ -239,12 +248,13 @@ size_t dt_kn4_smem_bytes(int Kc, int N) {
 }
 
 cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
-                          const float* cand_lp, const int32_t* cand_id, int32_t* tok, int32_t* parent,
-                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, cudaStream_t st) {
+                          const float* cand_lp, const int32_t* cand_id, const float* lse, int32_t* tok,
+                          int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
+                          int32_t* status, cudaStream_t st) {
     const size_t smem = dt_kn4_smem_bytes(Kc, N);
     cudaError_t e = cudaFuncSetAttribute(kn4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kn4_kernel<<<batch, NT, smem, st>>>(L, Kc, talon_k, log_mu, N, Mmax, cand_lp, cand_id, tok, parent, depth, rank,
-                                        score, n_nodes);
-    return cudaGetLastError();
+    DtLaunch lc(dim3(batch), dim3(NT), smem, st);
+    return cudaLaunchKernelEx(&lc.cfg, kn4_kernel, L, Kc, talon_k, log_mu, N, Mmax, cand_lp, cand_id, lse, tok,
+                              parent, depth, rank, score, n_nodes, status);
 }

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(NT) kn5_kernel(int L, int Mmax, int pos_offset
     int* dep = par + Mmax;
     int* order = dep + Mmax;
     uint32_t* rows = (uint32_t*)(order + Mmax);
+    dt_pdl_trigger();
+    dt_pdl_wait();
     const int M = n_nodes[b];
     if (tid == 0) bad = (M < 1 || M > Mmax) ? 1 : 0;
     if (tid < DT_MAX_L + 2) dcount[tid] = 0;
@@ -98,6 +100,6 @@ cudaError_t dt_kn5_launch(int batch, int L, int Mmax, int pos_offset, const int3
     const size_t smem = dt_kn5_smem_bytes(Mmax);
     cudaError_t e = cudaFuncSetAttribute(kn5_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kn5_kernel<<<batch, NT, smem, st>>>(L, Mmax, pos_offset, parent, depth, n_nodes, mask, pos, status);
-    return cudaGetLastError();
+    DtLaunch lc(dim3(batch), dim3(NT), smem, st);
+    return cudaLaunchKernelEx(&lc.cfg, kn5_kernel, L, Mmax, pos_offset, parent, depth, n_nodes, mask, pos, status);
 }

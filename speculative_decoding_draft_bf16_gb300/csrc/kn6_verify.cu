@@ -28,6 +28,7 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int NW = NT / 32;
+constexpr int SMAX = 16;
 
 struct Pub {
     float m, s;
@@ -86,13 +87,15 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
     int* s_rank = s_dep + Mmax;
     unsigned char* dbuf = smem + 1024 + (size_t)(((Mmax * 16) + 127) & ~127);
 
-    const int M = g_n[b];
     if (tid == 0) {
         dt_mbar_init(&misc->bar, 1);
         dt_fence_mbar_init();
         misc->timeout = 0;
-        misc->bad = (M < 1 || M > Mmax) ? 1 : 0;
     }
+    dt_pdl_trigger();
+    dt_pdl_wait();  // the tree and the target rows come from earlier kernels
+    const int M = g_n[b];
+    if (tid == 0) misc->bad = (M < 1 || M > Mmax) ? 1 : 0;
     __syncthreads();
     const size_t tb = (size_t)b * Mmax;
     if (!misc->bad) {
@@ -139,7 +142,11 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
         dt_fence_proxy_async();
         const T* x = dt_stage_row<T>(trow, lo, hi, dbuf, &misc->bar, &bytes);
         if (bytes) {
-            if (!dt_mbar_wait(&misc->bar, phase)) { misc->timeout = 1; dt_mbar_wait(&misc->bar, phase); }
+            // one thread waits on the copy; the others block in the barrier
+            if (tid == 0 && !dt_mbar_wait(&misc->bar, phase)) {
+                misc->timeout = 1;
+                dt_mbar_wait(&misc->bar, phase);
+            }
             phase ^= 1;
         }
         __syncthreads();
@@ -164,11 +171,12 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             }
             __syncthreads();
             cluster.sync();
+            unsigned long long part[SMAX];
+#pragma unroll
+            for (int j = 0; j < SMAX; ++j) part[j] = (j < S) ? cluster.map_shared_rank(misc, j)->pub[k & 1].u : 0ull;
             unsigned long long g = 0;
-            for (int j = 0; j < S; ++j) {
-                unsigned long long v = cluster.map_shared_rank(misc, j)->pub[k & 1].u;
-                g = v > g ? v : g;
-            }
+#pragma unroll
+            for (int j = 0; j < SMAX; ++j) g = part[j] > g ? part[j] : g;
             ++k;
             const int a = (int)(0xFFFFFFFFu - (uint32_t)(g & 0xFFFFFFFFull));
             out_tok = a;
@@ -205,13 +213,24 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             }
             __syncthreads();
             cluster.sync();
-            float M_ = -__int_as_float(0x7F800000);
-            for (int j = 0; j < S; ++j) M_ = fmaxf(M_, cluster.map_shared_rank(misc, j)->pub[k & 1].m);
-            float ssum = 0.f;
-            for (int j = 0; j < S; ++j) {
-                const Pub* r = &cluster.map_shared_rank(misc, j)->pub[k & 1];
-                if (r->m != -__int_as_float(0x7F800000)) ssum += r->s * __expf(r->m - M_);
+            float pm[SMAX], ps[SMAX];
+#pragma unroll
+            for (int j = 0; j < SMAX; ++j) {
+                pm[j] = -__int_as_float(0x7F800000);
+                ps[j] = 0.f;
+                if (j < S) {
+                    const Pub* r = &cluster.map_shared_rank(misc, j)->pub[k & 1];
+                    pm[j] = r->m;
+                    ps[j] = r->s;
+                }
             }
+            float M_ = -__int_as_float(0x7F800000);
+#pragma unroll
+            for (int j = 0; j < SMAX; ++j) M_ = fmaxf(M_, pm[j]);
+            float ssum = 0.f;
+#pragma unroll
+            for (int j = 0; j < SMAX; ++j)
+                if (j < S && pm[j] != -__int_as_float(0x7F800000)) ssum += ps[j] * __expf(pm[j] - M_);
             ++k;
             lse_t = M_ + logf(ssum);
         }
@@ -257,7 +276,10 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             uint32_t by = 0;
             y = dt_stage_row<T>(drow, lo, hi, dbuf2, &misc->bar, &by);
             if (by) {
-                if (!dt_mbar_wait(&misc->bar, phase)) { misc->timeout = 1; dt_mbar_wait(&misc->bar, phase); }
+                if (tid == 0 && !dt_mbar_wait(&misc->bar, phase)) {
+                    misc->timeout = 1;
+                    dt_mbar_wait(&misc->bar, phase);
+                }
                 phase ^= 1;
             }
             lse_d = draft_lse[(size_t)b * L + dpos];
@@ -285,12 +307,15 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             }
             __syncthreads();
             cluster.sync();
+            unsigned long long sums[SMAX];
+#pragma unroll
+            for (int j = 0; j < SMAX; ++j) sums[j] = (j < S) ? cluster.map_shared_rank(misc, j)->pub[k & 1].u : 0ull;
             unsigned long long tot = 0, before = 0, mine = 0;
-            for (int j = 0; j < S; ++j) {
-                unsigned long long v = cluster.map_shared_rank(misc, j)->pub[k & 1].u;
-                if (j < c) before += v;
-                if (j == c) mine = v;
-                tot += v;
+#pragma unroll
+            for (int j = 0; j < SMAX; ++j) {
+                if (j < c) before += sums[j];
+                if (j == c) mine = sums[j];
+                tot += sums[j];
             }
             ++k;
             if (tot == 0) continue;  // empty residual: draw from P instead
@@ -371,22 +396,13 @@ size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax) {
 cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int temperature_one,
                           const int32_t* tok, const int32_t* parent, const int32_t* depth, const int32_t* rank,
                           const int32_t* n_nodes, const float* draft_lse, const void* target,
-                          const float* target_lse, const void* draft, const float* uniforms, int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
-                          float* visited_lse, int32_t* status, cudaStream_t st) {
+                          const float* target_lse, const void* draft, const float* uniforms, int32_t* acc_nodes,
+                          int32_t* acc_len, int32_t* next_tok, float* visited_lse, int32_t* status,
+                          cudaStream_t st) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
     const size_t smem = dt_kn6_smem_bytes(chunk, esize, Mmax);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S, batch, 1);
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = S;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    DtLaunch lc(dim3(S, batch, 1), dim3(NT, 1, 1), smem, st, S);
+    cudaLaunchConfig_t& cfg = lc.cfg;
     cudaError_t e;
     if (dtype == DT_BF16) {
         auto k = kn6_kernel<uint16_t>;
