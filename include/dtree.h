@@ -215,6 +215,31 @@ dt_status dt_verify(const dt_tree* tree, int32_t batch, int32_t V, int32_t dtype
                     int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
                     float* visited_lse, dt_stream_t stream);
 
+/* Allocation-free DARTree selection.  The pages have no counterpart: this is
+ * a service to callers that cannot allocate device memory -- e.g. a serving
+ * process whose framework has reserved the whole device budget and lets no
+ * library allocate, or a latency-critical path where cudaMalloc/cudaFree are
+ * banned because they can synchronise the device.
+ * Same result as dt_select with p->mode == DT_MODE_DARTREE, but the Markov
+ * table that dt_select keeps in the caller's workspace lives in a fixed array
+ * inside the library (DT_NOALLOC_TABLE_BYTES, resident on every GPU that
+ * loads the library until the process exits).  The caller still owns and
+ * passes the tree buffers.  Nothing is allocated, by the library or by CUDA on
+ * its behalf.
+ *   - Returns DT_ERR_UNSUPPORTED when batch * L * K * K * 4 exceeds
+ *     DT_NOALLOC_TABLE_BYTES, DT_ERR_INVALID_ARG for a mode other than
+ *     DT_MODE_DARTREE, and the usual errors otherwise.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; each call writes every entry it reads, so none needs clearing.
+ *     Calls whose kernels overlap on the GPU (different streams, or
+ *     concurrent host threads on one device) race on the array: serialise
+ *     them. */
+#define DT_NOALLOC_TABLE_BYTES (4u << 20)
+dt_status dt_select_dartree_noalloc(const dt_build_params* p, dt_tree* tree, dt_stream_t stream);
+
 /* Static string for a dt_status value. */
 const char* dt_status_str(dt_status s);
 

@@ -209,3 +209,68 @@ const char* dt_status_str(dt_status s) {
 int32_t dt_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free DARTree selection (dt_select_dartree_noalloc).
+//
+// Some callers cannot hand the library a device workspace: a serving process
+// whose framework reserves the whole device memory budget up front (for
+// weights and KV cache) and does not let libraries allocate more, or code on a
+// latency-critical path where cudaMalloc/cudaFree are not allowed because they
+// can synchronise the device.  For them the DARTree Markov table lives in a
+// fixed file-scope device array instead of caller memory.  Limits: at most
+// DT_NOALLOC_TABLE_BYTES of table (batch * L * K * K floats); the array is
+// resident on every GPU that loads this library, for the life of the process.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoallocTableFloats = DT_NOALLOC_TABLE_BYTES / sizeof(float);
+
+// Shared by every call on a device; it keeps the last call's contents.  Each
+// call writes every table entry it later reads, so nothing needs clearing.
+static __device__ __align__(256) float g_noalloc_table[kNoallocTableFloats];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_addr[kNoallocMaxDevices];  // device address of the array, per device
+
+// Device address of g_noalloc_table on the current device, looked up once per
+// device (with that device current) and cached.
+dt_status noalloc_table(float** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kNoallocMaxDevices) return DT_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_table);
+        if (e != cudaSuccess || !ptr) return cuda_status(e == cudaSuccess ? cudaErrorInvalidSymbol : e);
+        g_noalloc_addr[dev] = (float*)ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return DT_OK;
+}
+
+}  // namespace
+
+extern "C" dt_status dt_select_dartree_noalloc(const dt_build_params* p, dt_tree* t, dt_stream_t stream) {
+    dt_status s = check_build(p, t);
+    if (s != DT_OK) return s;
+    if (p->mode != DT_MODE_DARTREE) return DT_ERR_INVALID_ARG;
+    const bool term = p->R > 0 && p->U;
+    float* table = nullptr;
+    if (term) {
+        const size_t need = (size_t)p->batch * p->L * p->K * p->K;
+        if (need > kNoallocTableFloats) return DT_ERR_UNSUPPORTED;
+        s = noalloc_table(&table);
+        if (s != DT_OK) return s;
+    }
+    cudaError_t e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt,
+                                  p->root_tok, t->max_nodes, t->cand_lp, t->cand_id, t->lse, table, t->node_tok,
+                                  t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status,
+                                  (cudaStream_t)stream);
+    return cuda_status(e);
+}

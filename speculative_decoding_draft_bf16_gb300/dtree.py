@@ -65,6 +65,8 @@ def lib():
         L.dt_verify.restype = _i32
         L.dt_verify.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
                                 _vp]
+        L.dt_select_dartree_noalloc.restype = _i32
+        L.dt_select_dartree_noalloc.argtypes = [bp, tp, _vp]
         L.dt_status_str.restype = ctypes.c_char_p
         L.dt_status_str.argtypes = [_i32]
         L.dt_version.restype = _i32
@@ -198,6 +200,13 @@ def select(p, tree, workspace=None, stream=None):
     ws, n = (workspace if workspace is not None else (None, 0))
     _check(lib().dt_select(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _ptr(ws), n, _stream(stream)),
            "dt_select")
+
+
+def select_dartree_noalloc(p, tree, stream=None):
+    """DARTree selection with the library's own fixed table (no workspace);
+    see dt_select_dartree_noalloc in include/dtree.h."""
+    _check(lib().dt_select_dartree_noalloc(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _stream(stream)),
+           "dt_select_dartree_noalloc")
 
 
 def build_tree(p, draft_logits, tree, workspace=None, stream=None):
