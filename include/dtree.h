@@ -133,7 +133,7 @@ typedef struct {
 size_t dt_workspace_size(const dt_build_params* p, int* ok);
 
 /* Stage 1: per-position log-softmax and Top-Kc over the full vocabulary.
- * [DARTree] Algorithm 1 line 4; [DDTree] section 3.3 (log-domain scores of the
+ * [DARTree] Algorithm 1 (per-position Top-K); [DDTree] section 3.3 (log-domain scores of the
  * per-position Top-K tokens).
  *   draft_logits: [batch][L][V] in p->dtype (bf16 or fp32); finite values or
  *   -inf (at least one finite value per row).

@@ -85,8 +85,8 @@ void or_exp_canon_vec(const float* x, int64_t n, float* y)
 
 /* ------------------------------------------------------------------------- */
 /* Stage 1: per-position log-softmax and Top-Kc candidate list.                */
-/* [DARTree] Algorithm 1, line 4 (C_d = TopK(L_d^base, K)); [DDTree] section   */
-/* 3.3 (scores are log-probabilities of the per-position Top-K tokens).        */
+/* [DARTree] Algorithm 1, its per-position Top-K candidate step; [DDTree]      */
+/* section 3.3 (scores are log-probabilities of the per-position Top-K tokens).*/
 /* Rank order: logit descending, token id ascending on equal logits.           */
 /* lse = max + log(sum exp(x - max)) in double, rounded once to fp32;          */
 /* lp = x - lse in fp32.                                                       */
@@ -307,18 +307,18 @@ int or_ddtree(const float* lp, const int32_t* id, int L, int K, int B, int rule,
 
 /* ------------------------------------------------------------------------- */
 /* DARTree depth-wise supertree and deferred pruning.                          */
-/* [DARTree] Algorithm 1 (lines 1-13) and the equation for s_beta in           */
-/* "Deferred best-first pruning"; Lemma 1 and its proof.                       */
+/* [DARTree] Algorithm 1 (depth-wise construction, then pruning) and the       */
+/* equation for s_beta in "Deferred best-first pruning"; Lemma 1 and proof.    */
 /*                                                                             */
 /* The correction head g is a parent-conditioned Markov term on the top-K      */
 /* candidates: log q~_d(c | u) = lp_d(c) + <U[tok(u)], Vt[c]>, the dot product */
 /* a serial fmaf chain over R terms from 0.0f; at depth 1 the parent is the    */
 /* root, whose token is root_tok (no term when root_tok < 0).                  */
-/* Score (line 8): s(child) = (s(parent) + log q~) + beta, in that order.      */
-/* Line 9 keeps the W best children of all parents by the shared node order.   */
-/* Line 12: T = TopB(S).  Lemma 1 proves TopB(S) equals the best-first heap    */
-/* over S when beta <= 0 and every log q~ <= 0.  This function returns the     */
-/* best-first heap result (always a prefix-closed tree) and reports through    */
+/* Child score, in the algorithm's order: (s(parent) + log q~) + beta.         */
+/* Each depth keeps the W best children of all parents (shared node order).   */
+/* The final pruning takes T = TopB(S).  Lemma 1 proves TopB(S) equals the     */
+/* best-first heap over S when beta <= 0 and every log q~ <= 0.  This returns  */
+/* the best-first heap result (always a prefix-closed tree) and reports via    */
 /* info whether it equals TopB(S) in content and order:                        */
 /*   info[0] = 1 if BestFirst_B(S) == TopB(S) (same nodes, same order)         */
 /*   info[1] = number of edges of S whose child outscores its parent           */
@@ -379,7 +379,7 @@ int or_dartree(const float* lp, const int32_t* id, int L, int K,
     for (int i = 1; i < nS; ++i)
         if (S[i].s > S[S[i].parent].s) ++viol;
 
-    /* TopB(S), line 12 */
+    /* TopB(S), the deferred pruning */
     or_node* sorted = (or_node*)malloc((size_t)nsup * sizeof(or_node));
     memcpy(sorted, S + 1, (size_t)nsup * sizeof(or_node));
     qsort(sorted, (size_t)nsup, sizeof(or_node), or_cmp_node);

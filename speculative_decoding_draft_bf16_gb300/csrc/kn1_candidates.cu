@@ -1,6 +1,6 @@
 // kn1_candidates.cu -- stage 1: per-position log-softmax and exact Top-Kc.
 //
-// [DARTree] Algorithm 1 line 4 (C_d = TopK(L_d^base, K)); [DDTree] section 3.3
+// [DARTree] Algorithm 1, its per-position Top-K candidate step; [DDTree] section 3.3
 // (log-domain scores of each position's Top-K tokens).
 //
 // One thread-block cluster of S CTAs per row (request b, position l); CTA c

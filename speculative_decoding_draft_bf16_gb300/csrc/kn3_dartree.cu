@@ -1,10 +1,10 @@
 // kn3_dartree.cu -- DARTree depth-wise supertree and deferred Top-B pruning.
 //
-// [DARTree] Algorithm 1 (lines 1-13): per depth d, score every child (one of
-// the position's Top-K tokens) of every kept parent with the causal
-// correction, s(child) = (s(parent) + log q~_d) + beta (line 8), keep the W
-// best children of all parents (line 9), accumulate them into the supertree
-// S (line 10); finally T = TopB(S) (line 12).  "Deferred best-first pruning":
+// [DARTree] Algorithm 1: per depth d, score every child (one of the
+// position's Top-K tokens) of every kept parent with the causal correction,
+// s(child) = (s(parent) + log q~_d) + beta, keep the W best children of all
+// parents, accumulate them into the supertree S; finally T = TopB(S).
+// "Deferred best-first pruning":
 // s_beta = sum log q~ + beta*d; Lemma 1: with beta <= 0 and every log q~ <= 0,
 // TopB(S) equals the best-first heap over S.
 //
