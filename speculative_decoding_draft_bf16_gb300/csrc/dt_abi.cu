@@ -2,6 +2,8 @@
 // entry points declared in include/dtree.h.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "dt_launch.h"
 #include "dtree.h"
 
@@ -23,17 +25,63 @@ int chunk_of(int V, int S, int dtype) {
     return (int)(((per + g - 1) / g) * g);
 }
 
-// Cluster size for a row-parallel vocabulary pass over `rows` rows.
-int cluster_for(int V, long long rows, int dtype) {
+// Clusters of S CTAs that the device holds at once for stage 1 (kind 1) or
+// the verification walk (kind 6) with these sizes; cached per device.
+int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
+    struct Fit {
+        int dev, kind, dtype, S, chunk, extra, n;
+    };
+    static std::mutex mu;
+    static Fit fits[128];
+    static int nfit = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < nfit; ++i) {
+        const Fit& f = fits[i];
+        if (f.dev == dev && f.kind == kind && f.dtype == dtype && f.S == S && f.chunk == chunk && f.extra == extra)
+            return f.n;
+    }
+    const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra) : dt_kn6_max_clusters(dtype, S, chunk, extra);
+    if (n > 0 && nfit < 128) fits[nfit++] = Fit{dev, kind, dtype, S, chunk, extra, n};
+    return n;
+}
+
+// Per-CTA cost of a row pass that does not scale with its chunk (staging
+// latency, cluster barriers, exchanges), in element-equivalents.
+constexpr long long kFixedElems = 12288;
+
+// Cluster size for a row-parallel vocabulary pass over `rows` rows (one
+// cluster per row): the power of two in [s_min, 16] -- chunks of at most
+// kChunkMax elements, and of at least ~1K unless that is s_min -- that
+// minimises the estimated time, waves x (chunk + kFixedElems), where a wave is
+// as many clusters as the device holds at once.  smem_ok(S) says whether a
+// cluster size fits in shared memory; fits(S) gives the resident clusters.
+template <typename SmemOk, typename Fits>
+int cluster_for(int V, long long rows, int dtype, SmemOk smem_ok, Fits fits) {
     int s_min = pow2_ceil(((long long)V + kChunkMax - 1) / kChunkMax);
     int s_cap = pow2_ceil(((long long)V + 1023) / 1024);  // chunks of at least ~1K elements
-    int s = pow2_ceil((kCtaTarget + rows - 1) / rows);
-    if (s > s_cap) s = s_cap;
-    if (s < s_min) s = s_min;
-    if (s > 16) s = 16;
-    if (s < 1) s = 1;
-    (void)dtype;
-    return s;
+    if (s_cap > 16) s_cap = 16;
+    if (s_min < 1) s_min = 1;
+    if (s_cap < s_min) s_cap = s_min;
+    int best = s_min;
+    long long best_cost = -1;
+    for (int s = s_min; s <= s_cap; s <<= 1) {
+        if (!smem_ok(s)) continue;
+        const int chunk = chunk_of(V, s, dtype);
+        int n = fits(s, chunk);
+        if (n < 1) n = (int)((kCtaTarget + s - 1) / s);  // unknown: assume two CTAs per SM
+        const long long waves = (rows + n - 1) / n;
+        const long long cost = waves * (chunk + kFixedElems);
+        if (best_cost < 0 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 dt_status cuda_status(cudaError_t e) {
@@ -107,9 +155,13 @@ dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_t
     if (!draft_logits) return DT_ERR_INVALID_ARG;
     const int Kc = kc_of(p);
     const long long rows = (long long)p->batch * p->L;
-    const int S = cluster_for(p->V, rows, p->dtype);
-    const int chunk = chunk_of(p->V, S, p->dtype);
     const int esize = p->dtype == DT_BF16 ? 2 : 4;
+    const int V = p->V, dtype = p->dtype;
+    const int S = cluster_for(
+        V, rows, dtype,
+        [&](int s) { return dt_kn1_smem_bytes(chunk_of(V, s, dtype), Kc, esize) + 4096 <= kSmemMax; },
+        [&](int s, int chunk) { return max_clusters(1, dtype, s, chunk, Kc); });
+    const int chunk = chunk_of(V, S, dtype);
     if (dt_kn1_smem_bytes(chunk, Kc, esize) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
     cudaError_t e = dt_kn1_launch(draft_logits, p->dtype, (int)rows, p->L, p->V, Kc, S, chunk, t->lse, t->cand_id,
                                   t->cand_lp, (cudaStream_t)stream);
@@ -183,12 +235,16 @@ dt_status dt_verify(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, c
     const int t1 = (temperature == 1.0f);
     if (!t1 && temperature != 0.0f) return DT_ERR_UNSUPPORTED;
     if (t1 && (!draft_logits || !uniforms || !t->lse)) return DT_ERR_INVALID_ARG;
-    // the walk is sequential per request: spread each row over a full cluster
-    int s = 16;
-    while (s > 1 && chunk_of(V, s, dtype) < 1024) s >>= 1;
-    const int chunk = chunk_of(V, s, dtype);
+    // the walk is sequential per request: spread each row over a cluster as
+    // wide as the batch lets the device hold at once
     const int esize = dtype == DT_BF16 ? 2 : 4;
-    if (chunk > kChunkMax || dt_kn6_smem_bytes(chunk, esize, t->max_nodes) + 1024 > kSmemMax) return DT_ERR_UNSUPPORTED;
+    const int Mmax = t->max_nodes;
+    const int s = cluster_for(
+        V, batch, dtype,
+        [&](int q) { return dt_kn6_smem_bytes(chunk_of(V, q, dtype), esize, Mmax) + 1024 <= kSmemMax; },
+        [&](int q, int chunk) { return max_clusters(6, dtype, q, chunk, Mmax); });
+    const int chunk = chunk_of(V, s, dtype);
+    if (chunk > kChunkMax || dt_kn6_smem_bytes(chunk, esize, Mmax) + 1024 > kSmemMax) return DT_ERR_UNSUPPORTED;
     cudaError_t e = dt_kn6_launch(batch, t->L, V, dtype, t->max_nodes, s, chunk, t1, t->node_tok, t->parent, t->depth,
                                   t->rank, t->n_nodes, t->lse, target_logits, t1 ? target_lse : nullptr, draft_logits,
                                   uniforms, acc_nodes,
@@ -222,7 +278,6 @@ int32_t dt_version(void) { return 100; }
 // DT_NOALLOC_TABLE_BYTES of table (batch * L * K * K floats); the array is
 // resident on every GPU that loads this library, for the life of the process.
 // ---------------------------------------------------------------------------
-#include <mutex>
 
 namespace {
 

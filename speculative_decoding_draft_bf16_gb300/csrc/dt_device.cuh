@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -255,6 +256,109 @@ DT_DI bool dt_mbar_wait(uint64_t* bar, uint32_t phase) {
 // dt_pdl_trigger() lets the next kernel in the stream be scheduled.
 DT_DI void dt_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 DT_DI void dt_pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Split cluster barrier: arrive (releasing this thread's prior shared-memory
+// accesses) now, wait (acquiring every cluster thread's) later, so that local
+// work can run in between.  Every thread of every CTA must execute both.
+DT_DI void dt_cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+DT_DI void dt_cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// Packed fp32 pairs (one 64-bit register pair) for the two-lane f32x2
+// instructions; every operation is rounded to nearest on its own.
+DT_DI unsigned long long dt_f2_pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+DT_DI void dt_f2_unpack(unsigned long long r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+DT_DI unsigned long long dt_f2_sub(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+DT_DI unsigned long long dt_f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+DT_DI unsigned long long dt_f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of staged row elements (8 bf16 or 4 fp32).
+// ---------------------------------------------------------------------------
+// Hardware base-2 exponential (approximate, ~2 ulp); used only for
+// log-normaliser sums, whose tolerance is 1e-5.
+DT_DI float dt_ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The element type's bits of a value that came from that type (exact).
+template <typename T> DT_DI T dt_to_elem(float x);
+template <> DT_DI uint16_t dt_to_elem<uint16_t>(float x) { return (uint16_t)(__float_as_uint(x) >> 16); }
+template <> DT_DI float dt_to_elem<float>(float x) { return x; }
+
+// Values of the elements of a 16-byte vector, as fp32.
+template <typename T> DT_DI void dt_vec_vals(const uint4& q, float (&x)[16 / sizeof(T)]);
+template <> DT_DI void dt_vec_vals<uint16_t>(const uint4& q, float (&x)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+template <> DT_DI void dt_vec_vals<float>(const uint4& q, float (&x)[4]) {
+    x[0] = __uint_as_float(q.x);
+    x[1] = __uint_as_float(q.y);
+    x[2] = __uint_as_float(q.z);
+    x[3] = __uint_as_float(q.w);
+}
+
+// Largest value of a full 16-byte vector (bf16: packed two-way compares).
+template <typename T> DT_DI float dt_vec_max(const uint4& q);
+template <> DT_DI float dt_vec_max<uint16_t>(const uint4& q) {
+    const __nv_bfloat162 a = __hmax2(*(const __nv_bfloat162*)&q.x, *(const __nv_bfloat162*)&q.y);
+    const __nv_bfloat162 b = __hmax2(*(const __nv_bfloat162*)&q.z, *(const __nv_bfloat162*)&q.w);
+    const __nv_bfloat162 c = __hmax2(a, b);
+    return fmaxf(__low2float(c), __high2float(c));
+}
+template <> DT_DI float dt_vec_max<float>(const uint4& q) {
+    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+}
+
+// acc + (exp2((x0 - m) * log2e), exp2((x1 - m) * log2e)), two lanes at once;
+// m2 and l2 hold (m, m) and (log2e, log2e).  The difference is rounded before
+// the product, so x = m gives exactly 1 at any magnitude.
+DT_DI unsigned long long dt_pair_exp(float x0, float x1, unsigned long long m2, unsigned long long l2,
+                                     unsigned long long acc) {
+    float d0, d1;
+    dt_f2_unpack(dt_f2_mul(dt_f2_sub(dt_f2_pack(x0, x1), m2), l2), d0, d1);
+    return dt_f2_add(acc, dt_f2_pack(dt_ex2_approx(d0), dt_ex2_approx(d1)));
+}
+// acc + the pairwise exp sums of every element of a full vector.
+template <typename T> DT_DI unsigned long long dt_vec_expsum(const uint4& q, unsigned long long m2,
+                                                           unsigned long long l2, unsigned long long acc);
+template <> DT_DI unsigned long long dt_vec_expsum<uint16_t>(const uint4& q, unsigned long long m2,
+                                                           unsigned long long l2, unsigned long long acc) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        acc = dt_pair_exp(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u), m2, l2, acc);
+    return acc;
+}
+template <> DT_DI unsigned long long dt_vec_expsum<float>(const uint4& q, unsigned long long m2,
+                                                        unsigned long long l2, unsigned long long acc) {
+    acc = dt_pair_exp(__uint_as_float(q.x), __uint_as_float(q.y), m2, l2, acc);
+    return dt_pair_exp(__uint_as_float(q.z), __uint_as_float(q.w), m2, l2, acc);
+}
 
 // Stage elements [lo, hi) of a row into shared memory.  The shared buffer
 // `sbase` must be 16-byte aligned with room for (hi - lo) elements + 16 bytes;

@@ -33,7 +33,32 @@ struct DtLaunch {
     }
 };
 
+// Clusters of cluster_x CTAs of `kernel` (block threads, smem dynamic shared
+// bytes; its attributes already set) that the device holds at once; 0 when the
+// query fails.
+template <typename K>
+inline int dt_max_active_clusters(K kernel, int cluster_x, int block, size_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    cfg.gridDim = dim3(cluster_x, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cluster_x;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // Stage 1 (kn1_candidates.cu).
+int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc);
 size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize);
 cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int L, int V, int Kc, int S, int chunk,
                           float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st);
@@ -66,6 +91,7 @@ cudaError_t dt_kn5_launch(int batch, int L, int Mmax, int pos_offset, const int3
                           const int32_t* n_nodes, uint32_t* mask, int32_t* pos, int32_t* status, cudaStream_t st);
 
 // Verification walk (kn6_verify.cu).
+int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax);
 size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax);
 cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int temperature_one,
                           const int32_t* tok, const int32_t* parent, const int32_t* depth, const int32_t* rank,

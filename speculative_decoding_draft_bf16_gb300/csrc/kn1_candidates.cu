@@ -4,27 +4,36 @@
 // (log-domain scores of each position's Top-K tokens).
 //
 // One thread-block cluster of S CTAs per row (request b, position l); CTA c
-// owns a contiguous vocabulary chunk.  Each CTA streams its chunk once from
-// HBM into shared memory with a 1-D bulk async copy, then, reading shared
-// memory 16 bytes per lane at a time:
-//   pass 1  chunk max (order key);
-//   pass 2  sum exp(x - max) and a 256-bin histogram of the keys within 256
-//           key steps below the chunk max (one histogram per warp, warp w
-//           owning a contiguous slice of the chunk);
-//   cluster exchange (DSMEM) -> row log-normaliser and the exact Kc-th key;
-//   (fp32 logits: two more 8-bit radix rounds on the low key bits; rows where
-//    the 256-step window holds fewer than Kc keys: full radix from the top);
-//   emit the CTA's keys above the threshold, plus threshold ties taken in
-//   token-id order (per-warp tie counts come from the histograms, the order
-//   inside a warp from a warp scan);
-//   gather the Kc selected (key, id) pairs of all CTAs (one warp per partner)
-//   and write each own entry at its rank (one warp per entry).
-// Every element of the row is read from HBM exactly once; nothing goes to
-// global memory except the outputs.  A row whose staging wait ran out of its
+// owns a contiguous vocabulary chunk, staged once from HBM into shared memory
+// by a 1-D bulk async copy and then read 16 bytes per lane at a time.
+//
+// Fast path (no per-element atomics):
+//   pass 1   each lane's maximum over its elements (packed compares) and the
+//            chunk maximum; the lane maxima (one per thread) go into a 256-bin
+//            histogram of order keys below the chunk maximum;
+//   exchange every lane maximum is a distinct element of the row, so the
+//            Kc-th largest lane maximum of the row is a lower bound for its
+//            Kc-th largest logit.  The CTAs merge their histograms in the
+//            frame of the row maximum through DSMEM (entries that fall outside
+//            the frame are dropped, which can only lower the bound) and read
+//            the bound off the top;
+//   pass 2   sum exp(x - max) for the normaliser (packed f32x2 arithmetic) and
+//            collect every element at or above the bound as a candidate
+//            (a vector is looked into only when its maximum reaches the bound);
+//   exchange normaliser and candidate counts; every CTA gathers the row's
+//            candidates and ranks its own (logit descending, token id
+//            ascending), writing those of rank < Kc.
+// The candidates hold the true Top-Kc and everything ranked above any of its
+// members, so their ranks among themselves are the exact ranks.
+// Rows whose candidates overflow the buffers (a row of many equal logits, a
+// tiny vocabulary) take the fallback, the same for the whole cluster: a 256-bin
+// window histogram of all keys below the chunk maximum, the exact threshold
+// found across the cluster (fp32: two more radix rounds; a window holding
+// fewer than Kc keys: full radix from the top), threshold ties taken in
+// token-id order.
+// Every logit is read from HBM once.  A row whose staging wait ran out of its
 // bound gets a NaN normaliser (the selection kernels turn that into
 // DT_DEV_TIMEOUT).
-#include <cuda_bf16.h>
-
 #include "dt_device.cuh"
 #include "dt_launch.h"
 
@@ -33,34 +42,43 @@ namespace {
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int SMAX = 16;
+constexpr int CCAP = 1024;  // candidates one CTA keeps (>= the largest Kc)
+constexpr int ACAP = 2048;  // candidates of one row
 
 struct Kn1Misc {
     uint64_t bar;
     float m;           // chunk max value
     float s;           // chunk sum exp(x - m)
     uint32_t mk16;     // chunk max key, top 16 bits
-    int nsel;          // selected entries in this CTA
+    int ncand;         // candidates found in this CTA (may exceed CCAP)
+    int nsel;          // fallback: selected entries in this CTA
     int timeout;
     float cm[SMAX];    // partners' values, copied through DSMEM
     float cs[SMAX];
     uint32_t cmk[SMAX];
+    int cnc[SMAX];
     int ceq[SMAX];
     int cnsel[SMAX];
     int cto[SMAX];
     float lse;
     int round_digit;
     int round_need;
-    int weq[NW];       // threshold ties per warp slice
+    int weq[NW];       // fallback: threshold ties per warp slice
     float red_f[NW];   // per-warp maxima
     float red_s[NW];   // per-warp sums
     int wsum[8];
 };
 
-// Dynamic shared memory: [misc 1 KB][per-warp histograms NW*1 KB][chist 2 KB]
-// [sel Kc*8][all Kc*8][chunk data + 16]
-DT_DI uint32_t* whist_of(unsigned char* s) { return (uint32_t*)(s + 1024); }
-DT_DI uint32_t* chist_of(unsigned char* s) { return (uint32_t*)(s + 1024 + NW * 1024); }
-DT_DI unsigned long long* sel_of(unsigned char* s) { return (unsigned long long*)(s + 1024 + NW * 1024 + 2048); }
+// Dynamic shared memory: [misc 1 KB][chist 2 KB][cand CCAP*8][all ACAP*8]
+// [chunk data + 32].  The fallback's per-warp histograms (NW*1 KB) live in
+// `all`, which it fills only after its last histogram read.
+constexpr size_t OFF_CHIST = 1024;
+constexpr size_t OFF_CAND = OFF_CHIST + 2048;
+constexpr size_t OFF_ALL = OFF_CAND + (size_t)CCAP * 8;
+constexpr size_t OFF_DATA = OFF_ALL + (size_t)ACAP * 8;
+static_assert((size_t)ACAP * 8 >= (size_t)NW * 1024, "per-warp histograms must fit in the gather buffer");
+static_assert(sizeof(Kn1Misc) <= OFF_CHIST, "misc block overflows its slot");
+static_assert(OFF_DATA % 128 == 0, "chunk data must stay 128-byte aligned");
 
 // Vector access to the staged chunk: vector j (16 bytes) holds elements
 // j*EPV - h .. j*EPV - h + EPV - 1, where h is the head misalignment.
@@ -71,7 +89,6 @@ struct Chunk {
     int h;           // elements of vector 0 that precede the chunk
     int n;           // elements in the chunk
     int nv;          // vectors covering the chunk
-    int lo;          // token id of element 0
     DT_DI void unpack(const uint4& q, T (&e)[EPV]) const {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         if constexpr (sizeof(T) == 2) {
@@ -86,48 +103,6 @@ struct Chunk {
         }
     }
 };
-
-// Hardware base-2 exponential (approximate, ~2 ulp), used only for the
-// fp32 normaliser sum whose tolerance is 1e-5.
-DT_DI float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// The element type's bits of a value that came from that type (exact).
-template <typename T> DT_DI T to_elem(float x);
-template <> DT_DI uint16_t to_elem<uint16_t>(float x) { return (uint16_t)(__float_as_uint(x) >> 16); }
-template <> DT_DI float to_elem<float>(float x) { return x; }
-
-// Values of the EPV elements of a 16-byte vector, as fp32.
-template <typename T> DT_DI void vec_vals(const uint4& q, float (&x)[16 / sizeof(T)]);
-template <> DT_DI void vec_vals<uint16_t>(const uint4& q, float (&x)[8]) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        x[2 * k] = __uint_as_float(w[k] << 16);
-        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
-}
-template <> DT_DI void vec_vals<float>(const uint4& q, float (&x)[4]) {
-    x[0] = __uint_as_float(q.x);
-    x[1] = __uint_as_float(q.y);
-    x[2] = __uint_as_float(q.z);
-    x[3] = __uint_as_float(q.w);
-}
-
-// Largest value in a full 16-byte vector (bf16: packed two-way compares).
-template <typename T> DT_DI float vec_max(const uint4& q);
-template <> DT_DI float vec_max<uint16_t>(const uint4& q) {
-    const __nv_bfloat162 a = __hmax2(*(const __nv_bfloat162*)&q.x, *(const __nv_bfloat162*)&q.y);
-    const __nv_bfloat162 b = __hmax2(*(const __nv_bfloat162*)&q.z, *(const __nv_bfloat162*)&q.w);
-    const __nv_bfloat162 c = __hmax2(a, b);
-    return fmaxf(__low2float(c), __high2float(c));
-}
-template <> DT_DI float vec_max<float>(const uint4& q) {
-    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
-}
 
 // Warp w owns vectors [w*vseg, min(nv, (w+1)*vseg)).
 DT_DI void warp_vectors(int nv, int* v0, int* v1) {
@@ -162,6 +137,64 @@ DT_DI void find_bin(const uint32_t* g, int need, Kn1Misc* misc) {
     __syncthreads();
 }
 
+// g[t] = sum over the cluster's CTAs j of their 256-bin histogram `h` (each
+// in its own frame: bin i counts keys with top bits refs[j] - i), re-framed
+// at `top` (bin t counts keys with top bits top - t).  Entries outside the new
+// frame are dropped.  Ends with __syncthreads.
+DT_DI void merge_framed(cg::cluster_group& cluster, const uint32_t* h, int S, const uint32_t* refs, uint32_t top,
+                        uint32_t* g) {
+    const int t = threadIdx.x;
+    if (t < 256) {
+        uint32_t part[SMAX];
+#pragma unroll
+        for (int j = 0; j < SMAX; ++j) {
+            part[j] = 0;
+            const int wj = t - (int)(top - refs[j < S ? j : 0]);
+            if (j < S && wj >= 0 && wj < 256) part[j] = cluster.map_shared_rank(h, j)[wj];
+        }
+        uint32_t a = 0;
+#pragma unroll
+        for (int j = 0; j < SMAX; ++j) a += part[j];
+        g[t] = a;
+    }
+    __syncthreads();
+}
+
+// Sum over the cluster of bin-aligned histograms (buffer `h` of every CTA).
+DT_DI void merge_plain(cg::cluster_group& cluster, const uint32_t* h, int S, uint32_t* g) {
+    const int t = threadIdx.x;
+    if (t < 256) {
+        uint32_t part[SMAX];
+#pragma unroll
+        for (int j = 0; j < SMAX; ++j) part[j] = (j < S) ? cluster.map_shared_rank(h, j)[t] : 0u;
+        uint32_t a = 0;
+#pragma unroll
+        for (int j = 0; j < SMAX; ++j) a += part[j];
+        g[t] = a;
+    }
+    __syncthreads();
+}
+
+// Rank each of this CTA's `mine` entries `own` among the `total` entries
+// `all` of the row (larger key first; keys are distinct) and write those of
+// rank < Kc.  One warp per entry.
+template <typename T>
+DT_DI void rank_and_write(const unsigned long long* own, int mine, const unsigned long long* all, int total, int Kc,
+                          float lse, int row, int32_t* cand_id, float* cand_lp) {
+    using E = DtElem<T>;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = wid; i < mine; i += NW) {
+        const unsigned long long key = own[i];
+        int rank = 0;
+        for (int q = lane; q < total; q += 32) rank += (all[q] > key);
+        rank = dt_warp_sum_i(rank);
+        if (lane == 0 && rank < Kc) {
+            cand_id[(size_t)row * Kc + rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+            cand_lp[(size_t)row * Kc + rank] = __fsub_rn(E::key_val((uint32_t)(key >> 32)), lse);
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, int V, int chunk, int Kc,
                                                  int L, float* __restrict__ lse_out,
@@ -169,6 +202,7 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
                                                  float* __restrict__ cand_lp) {
     using E = DtElem<T>;
     constexpr int EPV = Chunk<T>::EPV;
+    const float NEG_INF = -__int_as_float(0x7F800000);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t g[256];
     cg::cluster_group cluster = cg::this_cluster();
@@ -179,19 +213,19 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
     const int lo = min(V, c * chunk), hi = min(V, lo + chunk);
 
     Kn1Misc* misc = (Kn1Misc*)smem;
-    uint32_t* whist = whist_of(smem);
-    uint32_t* chist = chist_of(smem);
-    unsigned long long* sel = sel_of(smem);
-    unsigned long long* all = sel + Kc;
-    unsigned char* dbase = (unsigned char*)(all + Kc);
+    uint32_t* chist = (uint32_t*)(smem + OFF_CHIST);
+    unsigned long long* cand = (unsigned long long*)(smem + OFF_CAND);
+    unsigned long long* all = (unsigned long long*)(smem + OFF_ALL);
+    unsigned char* dbase = smem + OFF_DATA;
 
     if (tid == 0) {
         dt_mbar_init(&misc->bar, 1);
         dt_fence_mbar_init();
+        misc->ncand = 0;
         misc->nsel = 0;
         misc->timeout = 0;
     }
-    for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
+    if (tid < 256) chist[tid] = 0;
     dt_pdl_trigger();
     __syncthreads();
     dt_pdl_wait();  // the logits may come from the kernel just before us
@@ -214,135 +248,257 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
     ch.v = (const uint4*)dbase;
     ch.n = hi - lo;
     ch.nv = (ch.h + ch.n + EPV - 1) / EPV;
-    ch.lo = lo;
     int v0, v1;
     warp_vectors(ch.nv, &v0, &v1);
-
-    // ---- pass 1: chunk max (packed compares on whole vectors) -------------
     // vectors 0 and nv-1 may be partial (misaligned head, ragged tail); they
     // take the element-wise path
     const int full_lo = (ch.h > 0) ? 1 : 0;
     const int full_hi = ((ch.h + ch.n) % EPV == 0) ? ch.nv : ch.nv - 1;
-    float mx = -__int_as_float(0x7F800000);
+
+    // ---- pass 1: lane maxima and the chunk maximum --------------------------
+    float lmax = NEG_INF;
     for (int j = v0 + lane; j < v1; j += 32) {
         const uint4 q = ch.v[j];
         if (j >= full_lo && j < full_hi) {
-            mx = fmaxf(mx, vec_max<T>(q));
+            lmax = fmaxf(lmax, dt_vec_max<T>(q));
         } else {
             T e[EPV];
             ch.unpack(q, e);
 #pragma unroll
             for (int s = 0; s < EPV; ++s) {
                 const int idx = j * EPV + s - ch.h;
-                if (idx >= 0 && idx < ch.n) mx = fmaxf(mx, E::val(e[s]));
+                if (idx >= 0 && idx < ch.n) lmax = fmaxf(lmax, E::val(e[s]));
             }
         }
     }
-    mx = dt_warp_max(mx);
-    if (lane == 0) misc->red_f[wid] = mx;
+    const bool has = v0 + lane < v1;  // every vector holds at least one element
+    const float wmax = dt_warp_max(lmax);
+    if (lane == 0) misc->red_f[wid] = wmax;
     __syncthreads();
-    float m_c = -__int_as_float(0x7F800000);
+    float m_c = NEG_INF;
 #pragma unroll
     for (int w = 0; w < NW; ++w) m_c = fmaxf(m_c, misc->red_f[w]);
     const bool any = ch.n > 0;
-    const uint32_t mk16 = any ? (E::key(to_elem<T>(m_c)) >> (E::KB - 16)) : 0u;
-    const bool finite_max = (m_c != -__int_as_float(0x7F800000));
-    // the window holds keys mk16-255 .. mk16 (top 16 bits); as a value bound
-    const uint32_t klo = mk16 >= 255u ? mk16 - 255u : 0u;
-    const float x_lo = (klo <= 127u) ? -__int_as_float(0x7F800000) : E::key_val(klo << (E::KB - 16));
-
-    // ---- pass 2: sum exp(x - max) and the windowed key histogram ---------
-    const float log2e = 1.44269504088896340736f;
-    float sum = 0.f;
-    uint32_t* myh = whist + wid * 256;
-    for (int j = v0 + lane; j < v1; j += 32) {
-        const uint4 q = ch.v[j];
-        float x[EPV];
-        vec_vals<T>(q, x);
-        const bool full = (j >= full_lo && j < full_hi);
-#pragma unroll
-        for (int s = 0; s < EPV; ++s) {
-            const int idx = j * EPV + s - ch.h;
-            if (full || (idx >= 0 && idx < ch.n)) {
-                // x - max is exact for the max itself (e^0 = 1 at any magnitude)
-                if (finite_max) sum += ex2_approx(__fmul_rn(__fsub_rn(x[s], m_c), log2e));
-                if (x[s] >= x_lo) atomicAdd(&myh[mk16 - (E::key(to_elem<T>(x[s])) >> (E::KB - 16))], 1u);
-            }
-        }
-    }
-    sum = dt_warp_sum(sum);
-    if (lane == 0) misc->red_s[wid] = sum;
-    __syncthreads();
-    if (tid < 256) {
-        uint32_t a = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
-        chist[tid] = a;
+    const uint32_t mk16 = any ? (E::key(dt_to_elem<T>(m_c)) >> (E::KB - 16)) : 0u;
+    const bool finite_max = (m_c != NEG_INF);
+    if (has) {
+        const uint32_t b = mk16 - (E::key(dt_to_elem<T>(lmax)) >> (E::KB - 16));
+        if (b < 256u) atomicAdd(&chist[b], 1u);
     }
     if (tid == 0) {
-        float a = 0.f;
-        for (int i = 0; i < NW; ++i) a += misc->red_s[i];
-        misc->s = a;
         misc->m = m_c;
         misc->mk16 = mk16;
     }
     __syncthreads();
     cluster.sync();
 
-    // ---- exchange: normaliser and window histogram ------------------------
+    // ---- exchange 1: a lower bound for the Kc-th logit from the lane maxima -
     if (tid < S) {
         const Kn1Misc* r = cluster.map_shared_rank(misc, tid);
         misc->cm[tid] = r->m;
-        misc->cs[tid] = r->s;
         misc->cmk[tid] = r->mk16;
-        misc->cto[tid] = r->timeout;
     }
     __syncthreads();
     uint32_t Mk16 = 0;
     for (int j = 0; j < S; ++j) Mk16 = max(Mk16, misc->cmk[j]);
+    merge_framed(cluster, chist, S, misc->cmk, Mk16, g);
+    find_bin<false>(g, Kc, misc);
+    float bound = NEG_INF;
+    if (misc->round_digit >= 0) {
+        const uint32_t b16 = Mk16 - (uint32_t)misc->round_digit;
+        // smallest value whose key has these top bits (keys <= 127 are -inf or NaN)
+        if (b16 > 127u) bound = E::key_val(b16 << (E::KB - 16));
+    }
+
+    // ---- pass 2: sum exp(x - max); candidates at or above the bound --------
+    const float log2e = 1.44269504088896340736f;
+    const unsigned long long m2 = dt_f2_pack(m_c, m_c), l2 = dt_f2_pack(log2e, log2e);
+    unsigned long long acc = dt_f2_pack(0.f, 0.f);
+    float sum = 0.f;
+    for (int j = v0 + lane; j < v1; j += 32) {
+        const uint4 q = ch.v[j];
+        float x[EPV];
+        if (j >= full_lo && j < full_hi) {
+            if (finite_max) acc = dt_vec_expsum<T>(q, m2, l2, acc);
+            if (dt_vec_max<T>(q) >= bound) {
+                dt_vec_vals<T>(q, x);
+#pragma unroll
+                for (int s = 0; s < EPV; ++s) {
+                    if (x[s] >= bound) {
+                        const int slot = atomicAdd(&misc->ncand, 1);
+                        if (slot < CCAP)
+                            cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + j * EPV + s - ch.h));
+                    }
+                }
+            }
+        } else {
+            dt_vec_vals<T>(q, x);
+#pragma unroll
+            for (int s = 0; s < EPV; ++s) {
+                const int idx = j * EPV + s - ch.h;
+                if (idx >= 0 && idx < ch.n) {
+                    if (finite_max) sum += dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], m_c), log2e));
+                    if (x[s] >= bound) {
+                        const int slot = atomicAdd(&misc->ncand, 1);
+                        if (slot < CCAP)
+                            cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
+                    }
+                }
+            }
+        }
+    }
+    {
+        float a0, a1;
+        dt_f2_unpack(acc, a0, a1);
+        sum += a0 + a1;
+    }
+    sum = dt_warp_sum(sum);
+    if (lane == 0) misc->red_s[wid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        float a = 0.f;
+        for (int i = 0; i < NW; ++i) a += misc->red_s[i];
+        misc->s = a;
+    }
+    __syncthreads();
+    cluster.sync();
+
+    // ---- exchange 2: normaliser and candidate counts ------------------------
+    if (tid < S) {
+        const Kn1Misc* r = cluster.map_shared_rank(misc, tid);
+        misc->cs[tid] = r->s;
+        misc->cnc[tid] = r->ncand;
+        misc->cto[tid] = r->timeout;
+    }
+    __syncthreads();
     if (tid == 0) {
         float M = misc->cm[0];
         for (int j = 1; j < S; ++j) M = fmaxf(M, misc->cm[j]);
         float ssum = 0.f;
         for (int j = 0; j < S; ++j)
-            if (misc->cm[j] != -__int_as_float(0x7F800000)) ssum += misc->cs[j] * __expf(misc->cm[j] - M);
+            if (misc->cm[j] != NEG_INF) ssum += misc->cs[j] * __expf(misc->cm[j] - M);
         misc->lse = M + logf(ssum);
     }
-    // global window histogram: bin t counts keys whose top 16 bits equal Mk16 - t
-    if (tid < 256) {
-        uint32_t part[SMAX];
-#pragma unroll
-        for (int j = 0; j < SMAX; ++j) {
-            part[j] = 0;
-            const int wj = tid - (int)(Mk16 - misc->cmk[j < S ? j : 0]);
-            if (j < S && wj >= 0 && wj < 256) part[j] = cluster.map_shared_rank(chist, j)[wj];
-        }
-        uint32_t a = 0;
-#pragma unroll
-        for (int j = 0; j < SMAX; ++j) a += part[j];
-        g[tid] = a;
+    // every CTA sees the same counts, so the branch below is uniform across
+    // the cluster (it holds cluster barriers)
+    int total = 0;
+    bool overflow = false;
+    for (int j = 0; j < S; ++j) {
+        total += misc->cnc[j];
+        overflow |= misc->cnc[j] > CCAP;
     }
+    overflow |= total > ACAP;
     __syncthreads();
-    find_bin<false>(g, Kc, misc);
+    const float lse = misc->lse;
 
-    uint32_t T_key;
-    int need;
-    int cur = 0;        // chist buffer of the last round
-    int last_bin = -1;  // per-warp histogram bin holding the threshold ties
-    if (misc->round_digit >= 0) {
-        const uint32_t t16 = Mk16 - (uint32_t)misc->round_digit;
-        need = misc->round_need;
-        if (tid < S) {
-            const int wj = (int)(misc->cmk[tid] - t16);
-            misc->ceq[tid] = (wj >= 0 && wj < 256) ? (int)cluster.map_shared_rank(chist, tid)[wj] : 0;
+    if (!overflow) {
+        // ---- gather every CTA's candidates (one warp per partner) -----------
+        for (int j = wid; j < S; j += NW) {
+            int off = 0;
+            for (int q = 0; q < j; ++q) off += misc->cnc[q];
+            const unsigned long long* rs = cluster.map_shared_rank(cand, j);
+            const int cnt = misc->cnc[j];
+            for (int i = lane; i < cnt; i += 32) all[off + i] = rs[i];
         }
-        last_bin = (int)(mk16 - t16);  // may be outside [0,256) when this CTA has no ties
-        T_key = t16 << (E::KB - 16);
-        if constexpr (E::KB == 32) {
-            // two radix rounds over the low 16 bits among keys with top bits t16
-            for (int rd = 0; rd < 2; ++rd) {
-                const int shift = 8 - 8 * rd;
-                const uint32_t pre = T_key >> (shift + 8);
+        // partners may exit once everyone has gathered; ranking is local
+        dt_cluster_arrive();
+        __syncthreads();
+        rank_and_write<T>(cand, misc->cnc[c], all, total, Kc, lse, row, cand_id, cand_lp);
+        dt_cluster_wait();
+    } else {
+        // ---- fallback: window histogram over all keys, exact radix select ---
+        uint32_t* whist = (uint32_t*)all;  // per-warp histograms
+        uint32_t* myh = whist + wid * 256;
+        for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
+        __syncthreads();
+        const uint32_t klo = mk16 >= 255u ? mk16 - 255u : 0u;
+        const float x_lo = (klo <= 127u) ? NEG_INF : E::key_val(klo << (E::KB - 16));
+        for (int j = v0 + lane; j < v1; j += 32) {
+            float x[EPV];
+            dt_vec_vals<T>(ch.v[j], x);
+            const bool full = (j >= full_lo && j < full_hi);
+#pragma unroll
+            for (int s = 0; s < EPV; ++s) {
+                const int idx = j * EPV + s - ch.h;
+                if ((full || (idx >= 0 && idx < ch.n)) && x[s] >= x_lo)
+                    atomicAdd(&myh[mk16 - (E::key(dt_to_elem<T>(x[s])) >> (E::KB - 16))], 1u);
+            }
+        }
+        __syncthreads();
+        // partners last read chist (the lane-maximum histogram) before the
+        // previous cluster barrier, so it can be overwritten
+        if (tid < 256) {
+            uint32_t a = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
+            chist[tid] = a;
+        }
+        __syncthreads();
+        cluster.sync();
+        merge_framed(cluster, chist, S, misc->cmk, Mk16, g);
+        find_bin<false>(g, Kc, misc);
+
+        uint32_t T_key;
+        int need;
+        int cur = 0;        // chist buffer of the last round
+        int last_bin = -1;  // per-warp histogram bin holding the threshold ties
+        if (misc->round_digit >= 0) {
+            const uint32_t t16 = Mk16 - (uint32_t)misc->round_digit;
+            need = misc->round_need;
+            if (tid < S) {
+                const int wj = (int)(misc->cmk[tid] - t16);
+                misc->ceq[tid] = (wj >= 0 && wj < 256) ? (int)cluster.map_shared_rank(chist, tid)[wj] : 0;
+            }
+            last_bin = (int)(mk16 - t16);  // outside [0,256) when this CTA has no ties
+            T_key = t16 << (E::KB - 16);
+            if constexpr (E::KB == 32) {
+                // two radix rounds over the low 16 bits among keys with top bits t16
+                for (int rd = 0; rd < 2; ++rd) {
+                    const int shift = 8 - 8 * rd;
+                    const uint32_t pre = T_key >> (shift + 8);
+                    __syncthreads();
+                    for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
+                    __syncthreads();
+                    for (int j = v0 + lane; j < v1; j += 32) {
+                        T e[EPV];
+                        ch.unpack(ch.v[j], e);
+#pragma unroll
+                        for (int s = 0; s < EPV; ++s) {
+                            const int idx = j * EPV + s - ch.h;
+                            const uint32_t k = E::key(e[s]);
+                            if (idx >= 0 && idx < ch.n && (k >> (shift + 8)) == pre)
+                                atomicAdd(&myh[(k >> shift) & 255u], 1u);
+                        }
+                    }
+                    __syncthreads();
+                    cur ^= 1;
+                    if (tid < 256) {
+                        uint32_t a = 0;
+#pragma unroll
+                        for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
+                        chist[cur * 256 + tid] = a;
+                    }
+                    __syncthreads();
+                    cluster.sync();
+                    merge_plain(cluster, chist + cur * 256, S, g);
+                    find_bin<true>(g, need, misc);
+                    const uint32_t dg = (uint32_t)misc->round_digit;
+                    need = misc->round_need;
+                    T_key |= dg << shift;
+                    last_bin = (int)dg;
+                    if (tid < S) misc->ceq[tid] = (int)cluster.map_shared_rank(chist, tid)[cur * 256 + dg];
+                    __syncthreads();
+                }
+            }
+        } else {
+            // the window holds fewer than Kc keys: full radix over the whole key
+            need = Kc;
+            T_key = 0;
+            for (int rd = 0; rd < E::KB / 8; ++rd) {
+                const int shift = E::KB - 8 - 8 * rd;
+                const uint32_t pre = rd ? (T_key >> (shift + 8)) : 0u;
                 __syncthreads();
                 for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
                 __syncthreads();
@@ -353,7 +509,7 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
                     for (int s = 0; s < EPV; ++s) {
                         const int idx = j * EPV + s - ch.h;
                         const uint32_t k = E::key(e[s]);
-                        if (idx >= 0 && idx < ch.n && (k >> (shift + 8)) == pre)
+                        if (idx >= 0 && idx < ch.n && (rd == 0 || (k >> (shift + 8)) == pre))
                             atomicAdd(&myh[(k >> shift) & 255u], 1u);
                     }
                 }
@@ -367,17 +523,7 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
                 }
                 __syncthreads();
                 cluster.sync();
-                if (tid < 256) {
-                    uint32_t part[SMAX];
-#pragma unroll
-                    for (int j = 0; j < SMAX; ++j)
-                        part[j] = (j < S) ? cluster.map_shared_rank(chist, j)[cur * 256 + tid] : 0u;
-                    uint32_t a = 0;
-#pragma unroll
-                    for (int j = 0; j < SMAX; ++j) a += part[j];
-                    g[tid] = a;
-                }
-                __syncthreads();
+                merge_plain(cluster, chist + cur * 256, S, g);
                 find_bin<true>(g, need, misc);
                 const uint32_t dg = (uint32_t)misc->round_digit;
                 need = misc->round_need;
@@ -387,138 +533,75 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
                 __syncthreads();
             }
         }
-    } else {
-        // fallback: full radix select over the whole key, 8 bits per round
-        need = Kc;
-        T_key = 0;
-        for (int rd = 0; rd < E::KB / 8; ++rd) {
-            const int shift = E::KB - 8 - 8 * rd;
-            const uint32_t pre = rd ? (T_key >> (shift + 8)) : 0u;
-            __syncthreads();
-            for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
-            __syncthreads();
-            for (int j = v0 + lane; j < v1; j += 32) {
-                T e[EPV];
-                ch.unpack(ch.v[j], e);
+        // threshold ties per warp slice, straight from the last round's histograms
+        if (tid < NW) misc->weq[tid] = (last_bin >= 0 && last_bin < 256) ? (int)whist[tid * 256 + last_bin] : 0;
+        __syncthreads();
+
+        // emit keys above T, plus the first `need` ties by token id, into sel
+        unsigned long long* sel = cand;
+        int eqbase = 0;
+        for (int j = 0; j < c; ++j) eqbase += misc->ceq[j];
+        for (int w = 0; w < wid; ++w) eqbase += misc->weq[w];
+        const float Tv = E::key_val(T_key);
+        int running = 0;
+        for (int base = v0; base < v1; base += 32) {
+            const int j = base + lane;
+            float x[EPV];
+            int neq = 0;
+            bool ok[EPV];
+            if (j < v1) {
+                dt_vec_vals<T>(ch.v[j], x);
+                const bool full = (j >= full_lo && j < full_hi);
 #pragma unroll
                 for (int s = 0; s < EPV; ++s) {
                     const int idx = j * EPV + s - ch.h;
-                    const uint32_t k = E::key(e[s]);
-                    if (idx >= 0 && idx < ch.n && (rd == 0 || (k >> (shift + 8)) == pre))
-                        atomicAdd(&myh[(k >> shift) & 255u], 1u);
+                    ok[s] = full || (idx >= 0 && idx < ch.n);
+                    neq += (ok[s] && x[s] == Tv);
                 }
             }
-            __syncthreads();
-            cur ^= 1;
-            if (tid < 256) {
-                uint32_t a = 0;
+            const int inc = dt_warp_incl_scan(neq);
+            int r = running + inc - neq;  // ties before this lane's vector in this warp slice
+            running += __shfl_sync(0xffffffffu, inc, 31);
+            if (j < v1) {
 #pragma unroll
-                for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
-                chist[cur * 256 + tid] = a;
-            }
-            __syncthreads();
-            cluster.sync();
-            if (tid < 256) {
-                uint32_t part[SMAX];
-#pragma unroll
-                for (int j = 0; j < SMAX; ++j)
-                    part[j] = (j < S) ? cluster.map_shared_rank(chist, j)[cur * 256 + tid] : 0u;
-                uint32_t a = 0;
-#pragma unroll
-                for (int j = 0; j < SMAX; ++j) a += part[j];
-                g[tid] = a;
-            }
-            __syncthreads();
-            find_bin<true>(g, need, misc);
-            const uint32_t dg = (uint32_t)misc->round_digit;
-            need = misc->round_need;
-            T_key |= dg << shift;
-            last_bin = (int)dg;
-            if (tid < S) misc->ceq[tid] = (int)cluster.map_shared_rank(chist, tid)[cur * 256 + dg];
-            __syncthreads();
-        }
-    }
-    // threshold ties per warp slice, straight from the last round's histograms
-    if (tid < NW) misc->weq[tid] = (last_bin >= 0 && last_bin < 256) ? (int)whist[tid * 256 + last_bin] : 0;
-    __syncthreads();
-
-    // ---- emit: keys above T, plus the first `need` ties by token id -------
-    int eqbase = 0;
-    for (int j = 0; j < c; ++j) eqbase += misc->ceq[j];
-    for (int w = 0; w < wid; ++w) eqbase += misc->weq[w];
-    const float Tv = E::key_val(T_key);
-    int running = 0;
-    for (int base = v0; base < v1; base += 32) {
-        const int j = base + lane;
-        float x[EPV];
-        int neq = 0;
-        bool ok[EPV];
-        if (j < v1) {
-            vec_vals<T>(ch.v[j], x);
-            const bool full = (j >= full_lo && j < full_hi);
-#pragma unroll
-            for (int s = 0; s < EPV; ++s) {
-                const int idx = j * EPV + s - ch.h;
-                ok[s] = full || (idx >= 0 && idx < ch.n);
-                neq += (ok[s] && x[s] == Tv);
-            }
-        }
-        const int inc = dt_warp_incl_scan(neq);
-        int r = running + inc - neq;  // ties before this lane's vector in this warp slice
-        running += __shfl_sync(0xffffffffu, inc, 31);
-        if (j < v1) {
-#pragma unroll
-            for (int s = 0; s < EPV; ++s) {
-                if (!ok[s] || !(x[s] >= Tv)) continue;
-                bool take = true;
-                if (x[s] == Tv) {
-                    take = (eqbase + r < need);
-                    ++r;
-                }
-                if (take) {
-                    const int idx = j * EPV + s - ch.h;
-                    const int slot = atomicAdd(&misc->nsel, 1);
-                    if (slot < Kc)
-                        sel[slot] = ((unsigned long long)E::key(to_elem<T>(x[s])) << 32) |
-                                    (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
+                for (int s = 0; s < EPV; ++s) {
+                    if (!ok[s] || !(x[s] >= Tv)) continue;
+                    bool take = true;
+                    if (x[s] == Tv) {
+                        take = (eqbase + r < need);
+                        ++r;
+                    }
+                    if (take) {
+                        const int idx = j * EPV + s - ch.h;
+                        const int slot = atomicAdd(&misc->nsel, 1);
+                        if (slot < Kc)
+                            sel[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                        (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
+                    }
                 }
             }
         }
-    }
-    __syncthreads();
-    cluster.sync();
-
-    // ---- gather every CTA's selection (one warp per partner) -------------
-    if (tid < S) misc->cnsel[tid] = min(Kc, cluster.map_shared_rank(misc, tid)->nsel);
-    __syncthreads();
-    for (int j = wid; j < S; j += NW) {
-        int off = 0;
-        for (int q = 0; q < j; ++q) off += misc->cnsel[q];
-        const unsigned long long* rs = cluster.map_shared_rank(sel, j);
-        const int cnt = misc->cnsel[j];
-        for (int i = lane; i < cnt; i += 32)
-            if (off + i < Kc) all[off + i] = rs[i];
-    }
-    int total = 0;
-    for (int q = 0; q < S; ++q) total += misc->cnsel[q];
-    total = min(total, Kc);
-    __syncthreads();
-    cluster.sync();  // partners' selections are no longer read after this point
-
-    // ---- rank each own entry (one warp per entry) and write it -----------
-    const float lse = misc->lse;
-    const int mine = misc->cnsel[c];
-    for (int i = wid; i < mine; i += NW) {
-        const unsigned long long key = sel[i];
-        int rank = 0;
-        for (int q = lane; q < total; q += 32) rank += (all[q] > key);
-        rank = dt_warp_sum_i(rank);
-        if (lane == 0 && rank < Kc) {
-            const uint32_t id = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
-            const float v = E::key_val((uint32_t)(key >> 32));
-            cand_id[(size_t)row * Kc + rank] = (int32_t)id;
-            cand_lp[(size_t)row * Kc + rank] = __fsub_rn(v, lse);
+        __syncthreads();
+        cluster.sync();
+        // gather every CTA's selection (one warp per partner); this overwrites
+        // the per-warp histograms, whose last read was before the barrier
+        if (tid < S) misc->cnsel[tid] = min(Kc, cluster.map_shared_rank(misc, tid)->nsel);
+        __syncthreads();
+        for (int j = wid; j < S; j += NW) {
+            int off = 0;
+            for (int q = 0; q < j; ++q) off += misc->cnsel[q];
+            const unsigned long long* rs = cluster.map_shared_rank(sel, j);
+            const int cnt = misc->cnsel[j];
+            for (int i = lane; i < cnt; i += 32)
+                if (off + i < Kc) all[off + i] = rs[i];
         }
+        int tot = 0;
+        for (int q = 0; q < S; ++q) tot += misc->cnsel[q];
+        tot = min(tot, Kc);
+        dt_cluster_arrive();
+        __syncthreads();
+        rank_and_write<T>(sel, misc->cnsel[c], all, tot, Kc, lse, row, cand_id, cand_lp);
+        dt_cluster_wait();
     }
     if (c == 0 && tid == 0) {
         int to = 0;
@@ -530,7 +613,27 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
 }  // namespace
 
 size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize) {
-    return 1024 + (size_t)NW * 1024 + 2048 + (size_t)Kc * 16 + (size_t)chunk * esize + 32;
+    (void)Kc;  // the fixed candidate buffers also hold the fallback's Kc <= 1024 selections
+    return OFF_DATA + (size_t)chunk * esize + 32;
+}
+
+// Sets the kernel's shared-memory and cluster-size attributes for a launch.
+template <typename T>
+cudaError_t kn1_prepare(int S, size_t smem) {
+    cudaError_t e = cudaFuncSetAttribute(kn1_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && S > 8) e = cudaFuncSetAttribute(kn1_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc) {
+    const int esize = dtype == DT_BF16 ? 2 : 4;
+    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize);
+    if (dtype == DT_BF16) {
+        if (kn1_prepare<uint16_t>(S, smem) != cudaSuccess) return 0;
+        return dt_max_active_clusters(kn1_kernel<uint16_t>, S, NT, smem);
+    }
+    if (kn1_prepare<float>(S, smem) != cudaSuccess) return 0;
+    return dt_max_active_clusters(kn1_kernel<float>, S, NT, smem);
 }
 
 cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int L, int V, int Kc, int S, int chunk,
@@ -540,18 +643,11 @@ cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int L, int V,
     DtLaunch lc(dim3(S, rows, 1), dim3(NT, 1, 1), smem, st, S);
     cudaError_t e;
     if (dtype == DT_BF16) {
-        auto k = kn1_kernel<uint16_t>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-            return e;
-        if (S > 8 && (e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-            return e;
-        return cudaLaunchKernelEx(&lc.cfg, k, (const uint16_t*)logits, V, chunk, Kc, L, lse, cand_id, cand_lp);
-    } else {
-        auto k = kn1_kernel<float>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-            return e;
-        if (S > 8 && (e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-            return e;
-        return cudaLaunchKernelEx(&lc.cfg, k, (const float*)logits, V, chunk, Kc, L, lse, cand_id, cand_lp);
+        if ((e = kn1_prepare<uint16_t>(S, smem)) != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<uint16_t>, (const uint16_t*)logits, V, chunk, Kc, L, lse,
+                                  cand_id, cand_lp);
     }
+    if ((e = kn1_prepare<float>(S, smem)) != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<float>, (const float*)logits, V, chunk, Kc, L, lse, cand_id,
+                              cand_lp);
 }

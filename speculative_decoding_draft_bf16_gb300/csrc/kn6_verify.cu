@@ -17,36 +17,45 @@
 // and the draw is an exact integer inverse CDF, so results are reproducible.
 //
 // One thread-block cluster of S CTAs per request; CTA c owns a vocabulary
-// chunk.  Per visited node each CTA bulk-copies its chunk of the target row
-// into shared memory (the only HBM traffic: visited rows, plus one drafter
-// row on a T=1 rejection); partial argmax / (max, sum exp) / residual sums are
-// combined across the cluster through distributed shared memory.
+// chunk.  Rows are bulk-copied chunk-wise into shared memory: the target row
+// of each visited node (at T=1 with caller-supplied normalisers only the last
+// one) and, at T=1, the drafter row of the children's position of each
+// visited inner node (for the residual).  While node n is processed, the
+// target row of n's rank-0 child (the drafter's favourite, the likeliest next
+// node) is already on its way into a second buffer, so an accepted favourite
+// costs no copy latency.  Partial argmax / (max, sum exp) / residual sums are
+// combined across the cluster through distributed shared memory.  The
+// residual draw computes each thread's run of masses once; the CTA holding the
+// draw scans the run sums, and one warp re-walks the single run that holds it.
 #include "dt_device.cuh"
 #include "dt_launch.h"
 
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int SMAX = 16;
+constexpr int NBMAX = 3;  // row buffers: up to two target rows, one drafter row
 
 struct Pub {
     float m, s;
-    unsigned long long u;
+    unsigned long long u, w;
 };
 
 struct Kn6Misc {
-    uint64_t bar;
+    uint64_t bar[NBMAX];
     int timeout;
     int bad;
     Pub pub[2];
     unsigned long long red_u[NW];
+    unsigned long long red_w[NW];
     float red_f[NW];
-    int red_i[NW];
-    unsigned long long scan_u[NW];
     int child;
-    int nkids;
-    int found_v;
+    unsigned long long best_kid;
+    float xm[SMAX];               // partners' published values, copied through DSMEM
+    float xs[SMAX];
+    unsigned long long xu[SMAX];
+    unsigned long long xw[SMAX];
 };
 
 DT_DI unsigned long long warp_max_u64(unsigned long long v) {
@@ -57,8 +66,80 @@ DT_DI unsigned long long warp_max_u64(unsigned long long v) {
     return v;
 }
 
+DT_DI unsigned long long warp_incl_scan_u64(unsigned long long v) {
+    const int lane = threadIdx.x & 31;
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// 2^32 fixed-point probability mass exp(v - lse) of one element, or of the
+// residual max(0, P - Q) when resid.
+DT_DI unsigned long long mass(float xv, float lse_t, bool resid, float yv, float lse_d) {
+    unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(xv, lse_t)));
+    if (resid) {
+        const unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(yv, lse_d)));
+        P = P > Q ? P - Q : 0ull;
+    }
+    return P;
+}
+
+// Row buffers of one CTA.  Every thread keeps an identical copy of this state
+// (named scalars and bit masks rather than arrays, so it stays in registers).
 template <typename T>
-__global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chunk, int t1,
+struct Rows {
+    unsigned char* base;  // buffer 0; buffer i at base + i * stride
+    int stride;
+    uint64_t* bar;
+    int h0, h1, h2;       // head misalignment (elements) of the chunk staged in each buffer
+    int t0, t1, t2;       // which row (target: node, drafter: position) a buffer holds; -1 none
+    uint32_t pend;        // bit i: a bulk copy into buffer i has not been waited for
+    uint32_t ph;          // bit i: mbarrier phase parity of buffer i
+
+    DT_DI void init(unsigned char* b, int s, uint64_t* bars) {
+        base = b;
+        stride = s;
+        bar = bars;
+        h0 = h1 = h2 = 0;
+        t0 = t1 = t2 = -1;
+        pend = ph = 0;
+    }
+    DT_DI int holds(int i) const { return i == 0 ? t0 : (i == 1 ? t1 : t2); }
+    DT_DI int head(int i) const { return i == 0 ? h0 : (i == 1 ? h1 : h2); }
+    DT_DI const uint4* vec(int i) const { return (const uint4*)(base + (size_t)i * stride); }
+    DT_DI const T* elems(int i) const { return (const T*)(base + (size_t)i * stride) + head(i); }
+    // Waits (one thread) for buffer i's copy; the caller syncs the block before reading.
+    DT_DI void wait(int i, int* timeout) {
+        if (!((pend >> i) & 1u)) return;
+        if (threadIdx.x == 0 && !dt_mbar_wait(&bar[i], (ph >> i) & 1u)) {
+            *timeout = 1;
+            dt_mbar_wait(&bar[i], (ph >> i) & 1u);
+        }
+        ph ^= 1u << i;
+        pend &= ~(1u << i);
+    }
+    // Starts copying chunk [lo, hi) of `row` into buffer i (all threads).  Any
+    // earlier copy into it is waited for first, and all earlier reads of it
+    // are ordered before the new writes.
+    DT_DI void stage(int i, const T* row, int tag, int lo, int hi, int* timeout) {
+        wait(i, timeout);
+        __syncthreads();
+        dt_fence_proxy_async();
+        uint32_t bytes = 0;
+        unsigned char* dst = base + (size_t)i * stride;
+        const T* x = dt_stage_row<T>(row, lo, hi, dst, &bar[i], &bytes);
+        const int hd = (int)(((const unsigned char*)x - dst) / sizeof(T));
+        if (bytes) pend |= 1u << i;
+        if (i == 0) { h0 = hd; t0 = tag; }
+        else if (i == 1) { h1 = hd; t1 = tag; }
+        else { h2 = hd; t2 = tag; }
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int chunk, int nbt, int t1,
                                                  const int32_t* __restrict__ g_tok,
                                                  const int32_t* __restrict__ g_par,
                                                  const int32_t* __restrict__ g_dep,
@@ -71,6 +152,8 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
                                                  int32_t* __restrict__ next_tok, float* __restrict__ visited_lse,
                                                  int32_t* __restrict__ status) {
     using E = DtElem<T>;
+    constexpr int EPV = 16 / sizeof(T);
+    const float NEG_INF = -__int_as_float(0x7F800000);
     extern __shared__ __align__(128) unsigned char smem[];
     cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)cluster.num_blocks();
@@ -85,10 +168,16 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
     int* s_par = s_tok + Mmax;
     int* s_dep = s_par + Mmax;
     int* s_rank = s_dep + Mmax;
-    unsigned char* dbuf = smem + 1024 + (size_t)(((Mmax * 16) + 127) & ~127);
+    int* s_nk = s_rank + Mmax;    // children per node
+    int* s_pred = s_nk + Mmax;    // rank-0 child (smallest index), INT_MAX if none
+    const size_t tree_bytes = ((size_t)Mmax * 24 + 127) & ~(size_t)127;
+    const int DB = nbt;           // index of the drafter buffer
+
+    Rows<T> rows;
+    rows.init(smem + 1024 + tree_bytes, (int)(((size_t)chunk * sizeof(T) + 16 + 127) & ~(size_t)127), misc->bar);
 
     if (tid == 0) {
-        dt_mbar_init(&misc->bar, 1);
+        for (int i = 0; i < NBMAX; ++i) dt_mbar_init(&misc->bar[i], 1);
         dt_fence_mbar_init();
         misc->timeout = 0;
     }
@@ -104,6 +193,8 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             s_par[i] = g_par[tb + i];
             s_dep[i] = g_dep[tb + i];
             s_rank[i] = g_rank[tb + i];
+            s_nk[i] = 0;
+            s_pred[i] = 0x7FFFFFFF;
         }
         __syncthreads();
         for (int i = tid; i < M; i += NT) {
@@ -113,6 +204,10 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             else ok = (p >= 0 && p < M && p != i && d >= 1 && d <= L && d == s_dep[p] + 1 && s_tok[i] >= 0 &&
                        s_tok[i] < V);
             if (!ok) misc->bad = 1;
+            else if (i > 0) {
+                atomicAdd(&s_nk[p], 1);
+                if (s_rank[i] == 0) atomicMin(&s_pred[p], i);
+            }
         }
     }
     __syncthreads();
@@ -128,38 +223,70 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
     }
 
     int n = 0, len = 0;
-    uint32_t phase = 0;
-    int k = 0;  // cluster exchanges so far (selects the Pub slot)
+    int cur = 0;  // target buffer holding row n
+    int k = 0;    // cluster exchanges so far (selects the Pub slot)
     int out_tok = -1;
     const float* u0 = uniforms ? uniforms + (size_t)b * 2 * Mmax : nullptr;
     const float* u1 = u0 ? u0 + Mmax : nullptr;
+    // per-node target rows: argmax (T=0) or the normaliser (T=1 without target_lse)
+    const bool rows_needed = !t1 || !target_lse;
+    auto trow_of = [&](int node) { return target + (tb + node) * (size_t)V; };
+    auto drow_of = [&](int pos) { return draft + ((size_t)b * L + pos) * V; };
+    if (rows_needed) rows.stage(cur, trow_of(0), 0, lo, hi, &misc->timeout);
 
     for (;;) {
-        // ---- stage this CTA's chunk of target row n -----------------------
-        const T* trow = target + (tb + n) * (size_t)V;
-        uint32_t bytes = 0;
-        __syncthreads();
-        dt_fence_proxy_async();
-        const T* x = dt_stage_row<T>(trow, lo, hi, dbuf, &misc->bar, &bytes);
-        if (bytes) {
-            // one thread waits on the copy; the others block in the barrier
-            if (tid == 0 && !dt_mbar_wait(&misc->bar, phase)) {
-                misc->timeout = 1;
-                dt_mbar_wait(&misc->bar, phase);
-            }
-            phase ^= 1;
-        }
-        __syncthreads();
+        // ---- copies for what may come next -----------------------------------
+        const int pred = s_pred[n];
+        if (rows_needed && nbt == 2 && pred != 0x7FFFFFFF && len < L && rows.holds(cur ^ 1) != pred)
+            rows.stage(cur ^ 1, trow_of(pred), pred, lo, hi, &misc->timeout);
+        if (t1 && s_nk[n] > 0 && rows.holds(DB) != s_dep[n])
+            rows.stage(DB, drow_of(s_dep[n]), s_dep[n], lo, hi, &misc->timeout);
 
         int child = -1;
         float lse_t = 0.f;
+        const uint4* xv = rows.vec(cur);
+        const int h = rows.head(cur);
+        const int nv = (h + nch + EPV - 1) / EPV;
+        const int full_lo = (h > 0) ? 1 : 0;
+        const int full_hi = ((h + nch) % EPV == 0) ? nv : nv - 1;
+        if (rows_needed) {
+            rows.wait(cur, &misc->timeout);
+            __syncthreads();
+        }
         if (!t1) {
-            // argmax, smallest id on ties: max of (key << 32 | ~id)
+            // argmax, smallest id on ties: each thread keeps the first of its
+            // vectors holding its largest value, then the first such element
+            float lb = NEG_INF;
+            int lj = -1;
+            for (int j = tid; j < nv; j += NT) {
+                const uint4 q = xv[j];
+                float vm;
+                if (j >= full_lo && j < full_hi) {
+                    vm = dt_vec_max<T>(q);
+                } else {
+                    float xe[EPV];
+                    dt_vec_vals<T>(q, xe);
+                    vm = NEG_INF;
+#pragma unroll
+                    for (int s = 0; s < EPV; ++s) {
+                        const int idx = j * EPV + s - h;
+                        if (idx >= 0 && idx < nch) vm = fmaxf(vm, xe[s]);
+                    }
+                }
+                if (vm > lb || lj < 0) { lb = vm; lj = j; }
+            }
             unsigned long long best = 0;
-            for (int e = tid; e < nch; e += NT) {
-                unsigned long long key = ((unsigned long long)E::key(x[e]) << 32) |
-                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + e));
-                best = key > best ? key : best;
+            if (lj >= 0) {
+                float xe[EPV];
+                dt_vec_vals<T>(xv[lj], xe);
+                int id = -1;
+#pragma unroll
+                for (int s = EPV - 1; s >= 0; --s) {
+                    const int idx = lj * EPV + s - h;
+                    if (idx >= 0 && idx < nch && xe[s] == lb) id = lo + idx;
+                }
+                best = ((unsigned long long)E::key(dt_to_elem<T>(lb)) << 32) |
+                       (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
             }
             best = warp_max_u64(best);
             if (lane == 0) misc->red_u[wid] = best;
@@ -168,41 +295,72 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
                 unsigned long long a = 0;
                 for (int w = 0; w < NW; ++w) a = misc->red_u[w] > a ? misc->red_u[w] : a;
                 misc->pub[k & 1].u = a;
+                misc->child = 0x7FFFFFFF;
             }
             __syncthreads();
             cluster.sync();
-            unsigned long long part[SMAX];
-#pragma unroll
-            for (int j = 0; j < SMAX; ++j) part[j] = (j < S) ? cluster.map_shared_rank(misc, j)->pub[k & 1].u : 0ull;
+            if (tid < S) misc->xu[tid] = cluster.map_shared_rank(misc, tid)->pub[k & 1].u;
+            __syncthreads();
             unsigned long long g = 0;
-#pragma unroll
-            for (int j = 0; j < SMAX; ++j) g = part[j] > g ? part[j] : g;
+            for (int j = 0; j < S; ++j) g = misc->xu[j] > g ? misc->xu[j] : g;
             ++k;
             const int a = (int)(0xFFFFFFFFu - (uint32_t)(g & 0xFFFFFFFFull));
             out_tok = a;
-            if (tid == 0) misc->child = 0x7FFFFFFF;
-            __syncthreads();
-            for (int i = 1 + tid; i < M; i += NT)
-                if (s_par[i] == n && s_tok[i] == a) atomicMin(&misc->child, i);
+            if (s_nk[n] > 0)
+                for (int i = 1 + tid; i < M; i += NT)
+                    if (s_par[i] == n && s_tok[i] == a) atomicMin(&misc->child, i);
             __syncthreads();
             child = (misc->child == 0x7FFFFFFF) ? -1 : misc->child;
         } else if (target_lse) {
             lse_t = target_lse[tb + n];
-        }
-        if (t1 && !target_lse) {
-            // target log-normaliser of row n
-            float mx = -__int_as_float(0x7F800000);
-            for (int e = tid; e < nch; e += NT) mx = fmaxf(mx, E::val(x[e]));
-            mx = dt_warp_max(mx);
-            if (lane == 0) misc->red_f[wid] = mx;
+        } else {
+            // target log-normaliser of row n: chunk max, then sum exp(x - max)
+            float lm = NEG_INF;
+            for (int j = tid; j < nv; j += NT) {
+                const uint4 q = xv[j];
+                if (j >= full_lo && j < full_hi) {
+                    lm = fmaxf(lm, dt_vec_max<T>(q));
+                } else {
+                    float xe[EPV];
+                    dt_vec_vals<T>(q, xe);
+#pragma unroll
+                    for (int s = 0; s < EPV; ++s) {
+                        const int idx = j * EPV + s - h;
+                        if (idx >= 0 && idx < nch) lm = fmaxf(lm, xe[s]);
+                    }
+                }
+            }
+            lm = dt_warp_max(lm);
+            if (lane == 0) misc->red_f[wid] = lm;
             __syncthreads();
-            float m_c = misc->red_f[0];
-            for (int w = 1; w < NW; ++w) m_c = fmaxf(m_c, misc->red_f[w]);
-            __syncthreads();
+            float m_c = NEG_INF;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) m_c = fmaxf(m_c, misc->red_f[w]);
+            const float log2e = 1.44269504088896340736f;
             float sm = 0.f;
-            if (m_c != -__int_as_float(0x7F800000))
-                for (int e = tid; e < nch; e += NT) sm += __expf(E::val(x[e]) - m_c);
+            if (m_c != NEG_INF) {
+                const unsigned long long m2 = dt_f2_pack(m_c, m_c), l2 = dt_f2_pack(log2e, log2e);
+                unsigned long long acc = dt_f2_pack(0.f, 0.f);
+                for (int j = tid; j < nv; j += NT) {
+                    const uint4 q = xv[j];
+                    if (j >= full_lo && j < full_hi) {
+                        acc = dt_vec_expsum<T>(q, m2, l2, acc);
+                    } else {
+                        float xe[EPV];
+                        dt_vec_vals<T>(q, xe);
+#pragma unroll
+                        for (int s = 0; s < EPV; ++s) {
+                            const int idx = j * EPV + s - h;
+                            if (idx >= 0 && idx < nch) sm += dt_ex2_approx(__fmul_rn(__fsub_rn(xe[s], m_c), log2e));
+                        }
+                    }
+                }
+                float a0, a1;
+                dt_f2_unpack(acc, a0, a1);
+                sm += a0 + a1;
+            }
             sm = dt_warp_sum(sm);
+            __syncthreads();  // every thread has read red_f
             if (lane == 0) misc->red_f[wid] = sm;
             __syncthreads();
             if (tid == 0) {
@@ -213,112 +371,116 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             }
             __syncthreads();
             cluster.sync();
-            float pm[SMAX], ps[SMAX];
-#pragma unroll
-            for (int j = 0; j < SMAX; ++j) {
-                pm[j] = -__int_as_float(0x7F800000);
-                ps[j] = 0.f;
-                if (j < S) {
-                    const Pub* r = &cluster.map_shared_rank(misc, j)->pub[k & 1];
-                    pm[j] = r->m;
-                    ps[j] = r->s;
-                }
+            if (tid < S) {
+                const Pub* r = &cluster.map_shared_rank(misc, tid)->pub[k & 1];
+                misc->xm[tid] = r->m;
+                misc->xs[tid] = r->s;
             }
-            float M_ = -__int_as_float(0x7F800000);
-#pragma unroll
-            for (int j = 0; j < SMAX; ++j) M_ = fmaxf(M_, pm[j]);
+            __syncthreads();
+            float M_ = NEG_INF;
+            for (int j = 0; j < S; ++j) M_ = fmaxf(M_, misc->xm[j]);
             float ssum = 0.f;
-#pragma unroll
-            for (int j = 0; j < SMAX; ++j)
-                if (j < S && pm[j] != -__int_as_float(0x7F800000)) ssum += ps[j] * __expf(pm[j] - M_);
+            for (int j = 0; j < S; ++j)
+                if (misc->xm[j] != NEG_INF) ssum += misc->xs[j] * __expf(misc->xm[j] - M_);
             ++k;
             lse_t = M_ + logf(ssum);
         }
         if (t1) {
             if (c == 0 && tid == 0 && visited_lse) visited_lse[(size_t)b * (L + 1) + len] = lse_t;
-            // ratio tests of n's children; the first accepted in rank order wins
-            if (tid == 0) { misc->child = 0x7FFFFFFF; misc->nkids = 0; }
+            // ratio tests of n's children; the first accepted in (rank, index) order wins
+            if (tid == 0) misc->best_kid = ~0ull;
             __syncthreads();
-            for (int i = 1 + tid; i < M; i += NT) {
-                if (s_par[i] != n) continue;
-                atomicAdd(&misc->nkids, 1);
-                const int tk = s_tok[i];
-                const int pos = s_dep[i] - 1;
-                const float tv = E::val(trow[tk]);
-                const float dv = E::val(draft[((size_t)b * L + pos) * V + tk]);
-                const float lpt = __fsub_rn(tv, lse_t);
-                const float lpq = __fsub_rn(dv, draft_lse[(size_t)b * L + pos]);
-                const float ratio = dt_exp_canon(__fsub_rn(lpt, lpq));
-                if (u0[i] < ratio) atomicMin(&misc->child, s_rank[i] * 2048 + i);
+            if (s_nk[n] > 0) {
+                const T* trow = trow_of(n);
+                for (int i = 1 + tid; i < M; i += NT) {
+                    if (s_par[i] != n) continue;
+                    const int tk = s_tok[i];
+                    const int pos = s_dep[i] - 1;
+                    const float tv = E::val(trow[tk]);
+                    const float dv = E::val(draft[((size_t)b * L + pos) * V + tk]);
+                    const float lpt = __fsub_rn(tv, lse_t);
+                    const float lpq = __fsub_rn(dv, draft_lse[(size_t)b * L + pos]);
+                    const float ratio = dt_exp_canon(__fsub_rn(lpt, lpq));
+                    if (u0[i] < ratio)
+                        atomicMin(&misc->best_kid,
+                                  ((unsigned long long)((uint32_t)s_rank[i] ^ 0x80000000u) << 32) | (uint32_t)i);
+                }
             }
             __syncthreads();
-            child = (misc->child == 0x7FFFFFFF) ? -1 : (misc->child & 2047);
+            child = (misc->best_kid == ~0ull) ? -1 : (int)(misc->best_kid & 0xFFFFFFFFull);
         }
 
         if (child >= 0 && len < L) {
             ++len;
             if (c == 0 && tid == 0) acc_nodes[(size_t)b * (L + 1) + len] = child;
             n = child;
+            if (rows_needed) {
+                if (nbt == 2 && rows.holds(cur ^ 1) == child) cur ^= 1;
+                else rows.stage(cur, trow_of(child), child, lo, hi, &misc->timeout);
+            }
             continue;
         }
         if (!t1) break;
 
         // ---- T=1: draw the replacement / bonus token ------------------------
-        const bool has_kids = misc->nkids > 0;
-        const int dpos = s_dep[n];  // drafter row of n's children's position
-        const T* y = nullptr;
+        const bool has_kids = s_nk[n] > 0;
+        if (rows.holds(cur) != n) rows.stage(cur, trow_of(n), n, lo, hi, &misc->timeout);
+        rows.wait(cur, &misc->timeout);
         float lse_d = 0.f;
         if (has_kids) {
-            __syncthreads();
-            dt_fence_proxy_async();
-            unsigned char* dbuf2 = dbuf + (((size_t)chunk * sizeof(T) + 16 + 127) & ~(size_t)127);
-            const T* drow = draft + ((size_t)b * L + dpos) * V;
-            uint32_t by = 0;
-            y = dt_stage_row<T>(drow, lo, hi, dbuf2, &misc->bar, &by);
-            if (by) {
-                if (tid == 0 && !dt_mbar_wait(&misc->bar, phase)) {
-                    misc->timeout = 1;
-                    dt_mbar_wait(&misc->bar, phase);
-                }
-                phase ^= 1;
-            }
-            lse_d = draft_lse[(size_t)b * L + dpos];
-            __syncthreads();
+            rows.wait(DB, &misc->timeout);
+            lse_d = draft_lse[(size_t)b * L + s_dep[n]];
         }
-        // two attempts at most: the residual, then P if the residual is empty
-        for (int attempt = has_kids ? 0 : 1; attempt < 2; ++attempt) {
-            const bool resid = (attempt == 0);
-            unsigned long long part = 0;
-            for (int e = tid; e < nch; e += NT) {
-                unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
-                if (resid) {
-                    unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(y[e]), lse_d)));
-                    P = P > Q ? P - Q : 0ull;
-                }
-                part += P;
+        __syncthreads();
+        const T* x = rows.elems(cur);
+        const T* y = rows.elems(DB);
+        // masses of a contiguous run of elements per thread (odd length, so
+        // that the lanes' 2- or 4-byte reads spread over the banks)
+        const int run = ((nch + NT - 1) / NT) | 1;
+        const int e0 = min(nch, tid * run), e1 = min(nch, e0 + run);
+        unsigned long long rR = 0, rP = 0;
+        for (int e = e0; e < e1; ++e) {
+            const float xe = E::val(x[e]);
+            const unsigned long long P = mass(xe, lse_t, false, 0.f, 0.f);
+            rP += P;
+            if (has_kids) {
+                const unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(y[e]), lse_d)));
+                rR += P > Q ? P - Q : 0ull;
             }
-            part = dt_warp_sum_u64(part);
-            if (lane == 0) misc->red_u[wid] = part;
-            __syncthreads();
-            if (tid == 0) {
-                unsigned long long a = 0;
-                for (int w = 0; w < NW; ++w) a += misc->red_u[w];
-                misc->pub[k & 1].u = a;
-            }
-            __syncthreads();
-            cluster.sync();
-            unsigned long long sums[SMAX];
-#pragma unroll
-            for (int j = 0; j < SMAX; ++j) sums[j] = (j < S) ? cluster.map_shared_rank(misc, j)->pub[k & 1].u : 0ull;
-            unsigned long long tot = 0, before = 0, mine = 0;
-#pragma unroll
-            for (int j = 0; j < SMAX; ++j) {
-                if (j < c) before += sums[j];
-                if (j == c) mine = sums[j];
-                tot += sums[j];
-            }
-            ++k;
-            if (tot == 0) continue;  // empty residual: draw from P instead
+        }
+        {
+            const unsigned long long sR = dt_warp_sum_u64(rR), sP = dt_warp_sum_u64(rP);
+            if (lane == 0) { misc->red_u[wid] = sR; misc->red_w[wid] = sP; }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long aR = 0, aP = 0;
+            for (int w = 0; w < NW; ++w) { aR += misc->red_u[w]; aP += misc->red_w[w]; }
+            misc->pub[k & 1].u = aR;
+            misc->pub[k & 1].w = aP;
+        }
+        __syncthreads();
+        cluster.sync();
+        if (tid < S) {
+            const Pub* r = &cluster.map_shared_rank(misc, tid)->pub[k & 1];
+            misc->xu[tid] = r->u;
+            misc->xw[tid] = r->w;
+        }
+        __syncthreads();
+        ++k;
+        unsigned long long totR = 0;
+        for (int j = 0; j < S; ++j) totR += misc->xu[j];
+        // the residual, or P where the residual is empty (or the node has no children)
+        const bool resid = has_kids && totR > 0;
+        const unsigned long long* sums = resid ? misc->xu : misc->xw;
+        unsigned long long tot = 0, before = 0, mine = 0;
+        for (int j = 0; j < S; ++j) {
+            const unsigned long long v = sums[j];
+            if (j < c) before += v;
+            if (j == c) mine = v;
+            tot += v;
+        }
+        if (tot > 0) {
             float uf = __fmul_rn(u1[n], 16777216.0f);
             unsigned long long X = (unsigned long long)uf;
             if (X > 16777215ull) X = 16777215ull;
@@ -326,45 +488,37 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
             const unsigned long long hi64 = __umul64hi(X, tot);
             const unsigned long long tgt = (lo64 >> 24) | (hi64 << 40);
             if (tgt >= before && tgt < before + mine) {
-                // this CTA holds the draw: scan its chunk in vocabulary order
-                const unsigned long long local = tgt - before;
-                const int run = (nch + NT - 1) / NT;
-                const int e0 = min(nch, tid * run), e1 = min(nch, e0 + run);
-                unsigned long long rs = 0;
-                for (int e = e0; e < e1; ++e) {
-                    unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
-                    if (resid) {
-                        unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(y[e]), lse_d)));
-                        P = P > Q ? P - Q : 0ull;
-                    }
-                    rs += P;
-                }
-                // exclusive scan of run sums over the block
-                unsigned long long inc = rs;
-                for (int o = 1; o < 32; o <<= 1) {
-                    unsigned long long t = __shfl_up_sync(0xffffffffu, inc, o);
-                    if (lane >= o) inc += t;
-                }
-                if (lane == 31) misc->scan_u[wid] = inc;
+                // this CTA holds the draw: exclusive scan of the run sums
+                const unsigned long long rs = resid ? rR : rP;
+                const unsigned long long inc = warp_incl_scan_u64(rs);
+                __syncthreads();  // red_u was read by tid 0 above
+                if (lane == 31) misc->red_u[wid] = inc;
                 __syncthreads();
                 unsigned long long wb = 0;
-                for (int w = 0; w < wid; ++w) wb += misc->scan_u[w];
+                for (int w = 0; w < wid; ++w) wb += misc->red_u[w];
                 const unsigned long long ex = wb + inc - rs;
-                if (rs > 0 && local >= ex && local < ex + rs) {
-                    unsigned long long acc = ex;
-                    for (int e = e0; e < e1; ++e) {
-                        unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
-                        if (resid) {
-                            unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(y[e]), lse_d)));
-                            P = P > Q ? P - Q : 0ull;
+                const unsigned long long local = tgt - before;
+                const bool hit = rs > 0 && local >= ex && local < ex + rs;
+                const unsigned hm = __ballot_sync(0xffffffffu, hit);
+                if (hm) {
+                    // one warp re-walks the run that holds the draw, 32 elements at a time
+                    const int src = __ffs(hm) - 1;
+                    const int a0 = __shfl_sync(0xffffffffu, e0, src), a1 = __shfl_sync(0xffffffffu, e1, src);
+                    unsigned long long base = __shfl_sync(0xffffffffu, ex, src);
+                    for (int g0 = a0; g0 < a1; g0 += 32) {
+                        const int e = g0 + lane;
+                        unsigned long long P = 0;
+                        if (e < a1) P = mass(E::val(x[e]), lse_t, resid, resid ? E::val(y[e]) : 0.f, lse_d);
+                        const unsigned long long ci = warp_incl_scan_u64(P);
+                        const unsigned found = __ballot_sync(0xffffffffu, P > 0 && base + ci > local);
+                        if (found) {
+                            if (lane == __ffs(found) - 1) next_tok[b] = lo + e;
+                            break;
                         }
-                        if (P == 0) continue;
-                        acc += P;
-                        if (acc > local) { next_tok[b] = lo + e; break; }
+                        base += __shfl_sync(0xffffffffu, ci, 31);
                     }
                 }
             }
-            break;
         }
         break;
     }
@@ -380,17 +534,46 @@ __global__ void __launch_bounds__(NT) kn6_kernel(int L, int V, int Mmax, int chu
         if (visited_lse)
             for (int i = (t1 ? len + 1 : 0); i <= L; ++i) visited_lse[(size_t)b * (L + 1) + i] = 0.f;
     }
-    if (tid == 0 && misc->timeout) atomicOr(&status[b], DT_DEV_TIMEOUT);
+    // no copy may still be landing in shared memory when the CTA exits
+#pragma unroll
+    for (int i = 0; i < NBMAX; ++i) rows.wait(i, &misc->timeout);
     __syncthreads();
+    if (tid == 0 && misc->timeout) atomicOr(&status[b], DT_DEV_TIMEOUT);
     cluster.sync();  // keep shared memory alive until every CTA finished its remote reads
+}
+
+// Target-row buffers: two (prefetch of the favourite child) when they fit.
+int kn6_target_buffers(int chunk, int esize, int Mmax) {
+    const size_t tree = (((size_t)Mmax * 24) + 127) & ~(size_t)127;
+    const size_t buf = (((size_t)chunk * esize + 16 + 127) & ~(size_t)127);
+    return (1024 + tree + 3 * buf + 1024 <= (size_t)227 * 1024) ? 2 : 1;
 }
 
 }  // namespace
 
 size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax) {
-    const size_t tree = (((size_t)Mmax * 16) + 127) & ~(size_t)127;
+    const size_t tree = (((size_t)Mmax * 24) + 127) & ~(size_t)127;
     const size_t buf = (((size_t)chunk * esize + 16 + 127) & ~(size_t)127);
-    return 1024 + tree + 2 * buf;
+    return 1024 + tree + (size_t)(kn6_target_buffers(chunk, esize, Mmax) + 1) * buf;
+}
+
+// Sets the kernel's shared-memory and cluster-size attributes for a launch.
+template <typename T>
+cudaError_t kn6_prepare(int S, size_t smem) {
+    cudaError_t e = cudaFuncSetAttribute(kn6_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && S > 8) e = cudaFuncSetAttribute(kn6_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax) {
+    const int esize = dtype == DT_BF16 ? 2 : 4;
+    const size_t smem = dt_kn6_smem_bytes(chunk, esize, Mmax);
+    if (dtype == DT_BF16) {
+        if (kn6_prepare<uint16_t>(S, smem) != cudaSuccess) return 0;
+        return dt_max_active_clusters(kn6_kernel<uint16_t>, S, NT, smem);
+    }
+    if (kn6_prepare<float>(S, smem) != cudaSuccess) return 0;
+    return dt_max_active_clusters(kn6_kernel<float>, S, NT, smem);
 }
 
 cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int temperature_one,
@@ -401,28 +584,18 @@ cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, i
                           cudaStream_t st) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
     const size_t smem = dt_kn6_smem_bytes(chunk, esize, Mmax);
+    const int nbt = kn6_target_buffers(chunk, esize, Mmax);
     DtLaunch lc(dim3(S, batch, 1), dim3(NT, 1, 1), smem, st, S);
-    cudaLaunchConfig_t& cfg = lc.cfg;
     cudaError_t e;
     if (dtype == DT_BF16) {
-        auto k = kn6_kernel<uint16_t>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-            return e;
-        if (S > 8 && (e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-            return e;
-        return cudaLaunchKernelEx(&cfg, k, L, V, Mmax, chunk, temperature_one, tok, parent, depth, rank, n_nodes,
-                                  draft_lse, (const uint16_t*)target, target_lse, (const uint16_t*)draft, uniforms,
-                                  acc_nodes,
-                                  acc_len, next_tok, visited_lse, status);
-    } else {
-        auto k = kn6_kernel<float>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-            return e;
-        if (S > 8 && (e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-            return e;
-        return cudaLaunchKernelEx(&cfg, k, L, V, Mmax, chunk, temperature_one, tok, parent, depth, rank, n_nodes,
-                                  draft_lse, (const float*)target, target_lse, (const float*)draft, uniforms,
-                                  acc_nodes, acc_len,
-                                  next_tok, visited_lse, status);
+        if ((e = kn6_prepare<uint16_t>(S, smem)) != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<uint16_t>, L, V, Mmax, chunk, nbt, temperature_one, tok, parent,
+                                  depth, rank, n_nodes, draft_lse, (const uint16_t*)target, target_lse,
+                                  (const uint16_t*)draft, uniforms, acc_nodes, acc_len, next_tok, visited_lse,
+                                  status);
     }
+    if ((e = kn6_prepare<float>(S, smem)) != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<float>, L, V, Mmax, chunk, nbt, temperature_one, tok, parent, depth,
+                              rank, n_nodes, draft_lse, (const float*)target, target_lse, (const float*)draft,
+                              uniforms, acc_nodes, acc_len, next_tok, visited_lse, status);
 }
