@@ -25,8 +25,9 @@ int chunk_of(int V, int S, int dtype) {
     return (int)(((per + g - 1) / g) * g);
 }
 
-// Clusters of S CTAs that the device holds at once for stage 1 (kind 1) or
-// the verification walk (kind 6) with these sizes; cached per device.
+// Clusters of S CTAs that the device holds at once for stage 1 (kind 1,
+// extra = 4 * Kc + chunk buffers) or the verification walk (kind 6, extra =
+// max_nodes) with these sizes; cached per device.
 int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
     struct Fit {
         int dev, kind, dtype, S, chunk, extra, n;
@@ -45,10 +46,22 @@ int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
         if (f.dev == dev && f.kind == kind && f.dtype == dtype && f.S == S && f.chunk == chunk && f.extra == extra)
             return f.n;
     }
-    const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra) : dt_kn6_max_clusters(dtype, S, chunk, extra);
+    const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra >> 2, extra & 3)
+                            : dt_kn6_max_clusters(dtype, S, chunk, extra);
     if (n > 0 && nfit < 128) fits[nfit++] = Fit{dev, kind, dtype, S, chunk, extra, n};
     return n;
 }
+
+// Stage 1 gives each row a CTA of its own (kn1b_rows.cu) instead of spreading
+// it over a cluster (kn1_candidates.cu) from this many rows on, or for
+// candidate lists longer than kRowsPerCtaKc at any row count (measured on a
+// GB300 at V = 151936: both take ~21-25 us at 64 rows; at 16 rows the cluster
+// kernel is faster for Kc <= 256, the row kernel for Kc = 1024).
+#ifndef DT_KN1B_MIN_ROWS
+#define DT_KN1B_MIN_ROWS 64
+#endif
+constexpr long long kRowsPerCtaMin = DT_KN1B_MIN_ROWS;
+constexpr int kRowsPerCtaKc = 512;
 
 // Per-CTA cost of a row pass that does not scale with its chunk (staging
 // latency, cluster barriers, exchanges), in element-equivalents.
@@ -157,14 +170,33 @@ dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_t
     const long long rows = (long long)p->batch * p->L;
     const int esize = p->dtype == DT_BF16 ? 2 : 4;
     const int V = p->V, dtype = p->dtype;
+    // enough rows to fill the GPU with whole rows, or long candidate lists:
+    // one CTA per row, no cluster
+    if (rows >= kRowsPerCtaMin || Kc > kRowsPerCtaKc) {
+        cudaError_t e = dt_kn1b_launch(draft_logits, dtype, (int)rows, V, Kc, t->lse, t->cand_id, t->cand_lp,
+                                       (cudaStream_t)stream);
+        return cuda_status(e);
+    }
     const int S = cluster_for(
         V, rows, dtype,
-        [&](int s) { return dt_kn1_smem_bytes(chunk_of(V, s, dtype), Kc, esize) + 4096 <= kSmemMax; },
-        [&](int s, int chunk) { return max_clusters(1, dtype, s, chunk, Kc); });
+        [&](int s) { return dt_kn1_smem_bytes(chunk_of(V, s, dtype), Kc, esize, 1) + 4096 <= kSmemMax; },
+        [&](int s, int chunk) { return max_clusters(1, dtype, s, chunk, 4 * Kc + 1); });
     const int chunk = chunk_of(V, S, dtype);
-    if (dt_kn1_smem_bytes(chunk, Kc, esize) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
-    cudaError_t e = dt_kn1_launch(draft_logits, p->dtype, (int)rows, p->L, p->V, Kc, S, chunk, t->lse, t->cand_id,
-                                  t->cand_lp, (cudaStream_t)stream);
+    if (dt_kn1_smem_bytes(chunk, Kc, esize, 1) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
+    // more rows than the device holds clusters at once: persistent clusters,
+    // each prefetching its next row's chunk while it works on the current one
+    int nbuf = 1;
+    long long grid_rows = rows;
+    const int held = max_clusters(1, dtype, S, chunk, 4 * Kc + 1);
+    if (held > 0 && rows > held && dt_kn1_smem_bytes(chunk, Kc, esize, 2) + 4096 <= kSmemMax) {
+        const int held2 = max_clusters(1, dtype, S, chunk, 4 * Kc + 2);
+        if (held2 > 0) {
+            nbuf = 2;
+            grid_rows = held2 < rows ? held2 : rows;
+        }
+    }
+    cudaError_t e = dt_kn1_launch(draft_logits, dtype, (int)rows, (int)grid_rows, V, Kc, S, chunk, nbuf, t->lse,
+                                  t->cand_id, t->cand_lp, (cudaStream_t)stream);
     return cuda_status(e);
 }
 

@@ -392,6 +392,55 @@ DT_DI const T* dt_stage_row(const T* row, int lo, int hi, unsigned char* sbase, 
     return s;
 }
 
+// Chunk staging in two steps, for prefetching.  start(): one thread issues the
+// bulk copy of the 16-byte-aligned interior of elements [lo, hi) of `row`
+// (completing on `bar`), and the ragged head and tail elements (fewer than 16
+// of each) are loaded into registers of threads 0-15 and 16-31; it returns the
+// bulk bytes (0: nothing to wait for on `bar`).  finish(): those threads store
+// their element into the buffer; the caller syncs the block before reading.
+// The load latency of the ragged elements thus overlaps whatever runs between
+// the two calls.  Element lo lands at sbase + (address of row + lo) mod 16, as
+// with dt_stage_row.  Both must be called by all threads of the block.
+template <typename T>
+struct DtStager {
+    T held;
+    int held_off;  // byte offset of the held element in the buffer; -1: none
+
+    DT_DI uint32_t start(const T* row, int lo, int hi, unsigned char* sbase, uint64_t* bar) {
+        const uintptr_t a_lo = (uintptr_t)(row + lo);
+        const uintptr_t a_hi = (uintptr_t)(row + hi);
+        const int off0 = (int)(a_lo & 15);
+        uintptr_t in_lo = (a_lo + 15) & ~(uintptr_t)15;
+        uintptr_t in_hi = a_hi & ~(uintptr_t)15;
+        uint32_t bytes = 0;
+        if (in_hi > in_lo) bytes = (uint32_t)(in_hi - in_lo);
+        else { in_lo = a_hi; in_hi = a_hi; }  // no aligned interior: fewer than 32 bytes in all
+        const int e_in_lo = (int)((in_lo - a_lo) / sizeof(T));
+        const int e_in_hi = (int)((in_hi - a_lo) / sizeof(T));
+        const int n = hi - lo;
+        if (threadIdx.x == 0 && bytes) {
+            dt_mbar_arrive_expect_tx(bar, bytes);
+            dt_bulk_g2s(sbase + off0 + (size_t)e_in_lo * sizeof(T), (const void*)in_lo, bytes, bar);
+        }
+        const int t = threadIdx.x;
+        int e = -1;
+        if (t < 16) {
+            if (t < e_in_lo) e = t;
+        } else if (t < 32) {
+            if (e_in_hi + (t - 16) < n) e = e_in_hi + (t - 16);
+        }
+        held_off = -1;
+        if (e >= 0) {
+            held = row[lo + e];
+            held_off = off0 + e * (int)sizeof(T);
+        }
+        return bytes;
+    }
+    DT_DI void finish(unsigned char* sbase) const {
+        if (held_off >= 0) *(T*)(sbase + held_off) = held;
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Shared node order on explicit node arrays (score s, depth dep, parent par,
 // lex = (lexicographic rank of the parent among its depth << 16) | own rank):

@@ -34,8 +34,8 @@
 // Every logit is read from HBM once.  A row whose staging wait ran out of its
 // bound gets a NaN normaliser (the selection kernels turn that into
 // DT_DEV_TIMEOUT).
-#include "dt_device.cuh"
 #include "dt_launch.h"
+#include "kn1_common.cuh"
 
 namespace {
 
@@ -45,14 +45,21 @@ constexpr int SMAX = 16;
 constexpr int CCAP = 1024;  // candidates one CTA keeps (>= the largest Kc)
 constexpr int ACAP = 2048;  // candidates of one row
 
+// Per-row values that partners read after the row's second cluster barrier,
+// kept per row parity: a CTA may start its next row while a partner still
+// reads them.
+struct RowPub {
+    float s;      // chunk sum exp(x - m)
+    int ncand;    // candidates found in this CTA (may exceed CCAP)
+    int nsel;     // fallback: selected entries in this CTA
+    int timeout;  // the chunk's staging wait ran out
+};
+
 struct Kn1Misc {
-    uint64_t bar;
-    float m;           // chunk max value
-    float s;           // chunk sum exp(x - m)
-    uint32_t mk16;     // chunk max key, top 16 bits
-    int ncand;         // candidates found in this CTA (may exceed CCAP)
-    int nsel;          // fallback: selected entries in this CTA
-    int timeout;
+    uint64_t bar[2];   // one per chunk buffer
+    float m;           // this row: chunk max value
+    uint32_t mk16;     // this row: chunk max key, top 16 bits
+    RowPub pub[2];
     float cm[SMAX];    // partners' values, copied through DSMEM
     float cs[SMAX];
     uint32_t cmk[SMAX];
@@ -61,16 +68,14 @@ struct Kn1Misc {
     int cnsel[SMAX];
     int cto[SMAX];
     float lse;
-    int round_digit;
-    int round_need;
+    DtBinSearch bs;
     int weq[NW];       // fallback: threshold ties per warp slice
     float red_f[NW];   // per-warp maxima
     float red_s[NW];   // per-warp sums
-    int wsum[8];
 };
 
 // Dynamic shared memory: [misc 1 KB][chist 2 KB][cand CCAP*8][all ACAP*8]
-// [chunk data + 32].  The fallback's per-warp histograms (NW*1 KB) live in
+// [chunk buffer 0][chunk buffer 1 when prefetching].  The fallback's per-warp histograms (NW*1 KB) live in
 // `all`, which it fills only after its last histogram read.
 constexpr size_t OFF_CHIST = 1024;
 constexpr size_t OFF_CAND = OFF_CHIST + 2048;
@@ -112,31 +117,6 @@ DT_DI void warp_vectors(int nv, int* v0, int* v1) {
     *v1 = min(nv, *v0 + vseg);
 }
 
-// Block-wide: global histogram g[256]; when TOP_IS_HIGH a higher bin index is
-// a larger key, else bin 0 is the largest.  Finds the bin holding the
-// need-th largest key: misc->round_digit (-1 if the bins hold fewer than
-// `need` keys) and misc->round_need (keys still needed inside that bin).
-template <bool TOP_IS_HIGH>
-DT_DI void find_bin(const uint32_t* g, int need, Kn1Misc* misc) {
-    const int t = threadIdx.x;
-    int v = 0;
-    if (t < 256) v = (int)g[TOP_IS_HIGH ? 255 - t : t];
-    const int inc = dt_warp_incl_scan(v);
-    if (t < 256 && (t & 31) == 31) misc->wsum[t >> 5] = inc;
-    if (t == 0) { misc->round_digit = -1; misc->round_need = need; }
-    __syncthreads();
-    if (t < 256) {
-        int before = 0;
-        for (int i = 0; i < (t >> 5); ++i) before += misc->wsum[i];
-        const int cum = before + inc;
-        if (cum >= need && cum - v < need) {
-            misc->round_digit = TOP_IS_HIGH ? 255 - t : t;
-            misc->round_need = need - (cum - v);
-        }
-    }
-    __syncthreads();
-}
-
 // g[t] = sum over the cluster's CTAs j of their 256-bin histogram `h` (each
 // in its own frame: bin i counts keys with top bits refs[j] - i), re-framed
 // at `top` (bin t counts keys with top bits top - t).  Entries outside the new
@@ -175,29 +155,9 @@ DT_DI void merge_plain(cg::cluster_group& cluster, const uint32_t* h, int S, uin
     __syncthreads();
 }
 
-// Rank each of this CTA's `mine` entries `own` among the `total` entries
-// `all` of the row (larger key first; keys are distinct) and write those of
-// rank < Kc.  One warp per entry.
 template <typename T>
-DT_DI void rank_and_write(const unsigned long long* own, int mine, const unsigned long long* all, int total, int Kc,
-                          float lse, int row, int32_t* cand_id, float* cand_lp) {
-    using E = DtElem<T>;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = wid; i < mine; i += NW) {
-        const unsigned long long key = own[i];
-        int rank = 0;
-        for (int q = lane; q < total; q += 32) rank += (all[q] > key);
-        rank = dt_warp_sum_i(rank);
-        if (lane == 0 && rank < Kc) {
-            cand_id[(size_t)row * Kc + rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-            cand_lp[(size_t)row * Kc + rank] = __fsub_rn(E::key_val((uint32_t)(key >> 32)), lse);
-        }
-    }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, int V, int chunk, int Kc,
-                                                 int L, float* __restrict__ lse_out,
+__global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits, int V, int chunk, int Kc, int rows,
+                                                 int nbuf, float* __restrict__ lse_out,
                                                  int32_t* __restrict__ cand_id,
                                                  float* __restrict__ cand_lp) {
     using E = DtElem<T>;
@@ -208,256 +168,322 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
     cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)cluster.num_blocks();
     const int c = (int)cluster.block_rank();
-    const int row = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int lo = min(V, c * chunk), hi = min(V, lo + chunk);
+    const int G = gridDim.y;  // clusters; cluster q takes rows q, q + G, q + 2G, ...
 
     Kn1Misc* misc = (Kn1Misc*)smem;
     uint32_t* chist = (uint32_t*)(smem + OFF_CHIST);
     unsigned long long* cand = (unsigned long long*)(smem + OFF_CAND);
     unsigned long long* all = (unsigned long long*)(smem + OFF_ALL);
-    unsigned char* dbase = smem + OFF_DATA;
+    const size_t dstride = ((size_t)chunk * sizeof(T) + 32 + 127) & ~(size_t)127;
 
     if (tid == 0) {
-        dt_mbar_init(&misc->bar, 1);
+        dt_mbar_init(&misc->bar[0], 1);
+        dt_mbar_init(&misc->bar[1], 1);
         dt_fence_mbar_init();
-        misc->ncand = 0;
-        misc->nsel = 0;
-        misc->timeout = 0;
     }
-    if (tid < 256) chist[tid] = 0;
     dt_pdl_trigger();
     __syncthreads();
     dt_pdl_wait();  // the logits may come from the kernel just before us
 
-    // ---- stage the chunk (one HBM read) --------------------------------
-    uint32_t bulk = 0;
-    const T* rowp = logits + (size_t)row * (size_t)V;
-    const T* xs = dt_stage_row<T>(rowp, lo, hi, dbase, &misc->bar, &bulk);
-    // one thread waits on the copy; the others block in the barrier below
-    // (blocked warps take no issue slots)
-    if (bulk && tid == 0) {
-        if (!dt_mbar_wait(&misc->bar, 0)) {
-            misc->timeout = 1;
-            dt_mbar_wait(&misc->bar, 0);
-        }
-    }
-    __syncthreads();
-    Chunk<T> ch;
-    ch.h = (int)(((uintptr_t)xs - (uintptr_t)dbase) / sizeof(T));
-    ch.v = (const uint4*)dbase;
-    ch.n = hi - lo;
-    ch.nv = (ch.h + ch.n + EPV - 1) / EPV;
-    int v0, v1;
-    warp_vectors(ch.nv, &v0, &v1);
-    // vectors 0 and nv-1 may be partial (misaligned head, ragged tail); they
-    // take the element-wise path
-    const int full_lo = (ch.h > 0) ? 1 : 0;
-    const int full_hi = ((ch.h + ch.n) % EPV == 0) ? ch.nv : ch.nv - 1;
+    // chunk buffers (bit i of a mask: buffer i): a bulk copy not yet waited
+    // for, and the parity of the buffer's next mbarrier completion
+    uint32_t pend = 0, phase = 0;
+    DtStager<T> stg;  // ragged chunk ends of the latest copy, held in registers
+    auto issue = [&](int b, int r) {
+        if (stg.start(logits + (size_t)r * (size_t)V, lo, hi, smem + OFF_DATA + b * dstride, &misc->bar[b]))
+            pend |= 1u << b;
+    };
+    int row = blockIdx.y;
+    int buf = 0;
+    if (row < rows) issue(0, row);
 
-    // ---- pass 1: lane maxima and the chunk maximum --------------------------
-    float lmax = NEG_INF;
-    for (int j = v0 + lane; j < v1; j += 32) {
-        const uint4 q = ch.v[j];
-        if (j >= full_lo && j < full_hi) {
-            lmax = fmaxf(lmax, dt_vec_max<T>(q));
-        } else {
-            T e[EPV];
-            ch.unpack(q, e);
-#pragma unroll
-            for (int s = 0; s < EPV; ++s) {
-                const int idx = j * EPV + s - ch.h;
-                if (idx >= 0 && idx < ch.n) lmax = fmaxf(lmax, E::val(e[s]));
+    for (int it = 0; row < rows; ++it, row += G) {
+        const int par = it & 1;
+        const int nxt = row + G;
+        RowPub* mp = &misc->pub[par];
+        if (tid == 0) {
+            mp->ncand = 0;
+            mp->nsel = 0;
+            mp->timeout = 0;
+        }
+        if (tid < 256) chist[tid] = 0;
+        stg.finish(smem + OFF_DATA + buf * dstride);  // this row's ragged ends
+        // start the next row's copy into the other buffer (its last reads were
+        // the previous row's, all before the barriers since)
+        if (nbuf == 2 && nxt < rows) {
+            __syncthreads();
+            dt_fence_proxy_async();
+            issue(buf ^ 1, nxt);
+        }
+        // one thread waits on this row's copy; the others block in the barrier
+        // below (blocked warps take no issue slots)
+        if ((pend >> buf) & 1u) {
+            if (tid == 0 && !dt_mbar_wait(&misc->bar[buf], (phase >> buf) & 1u)) {
+                mp->timeout = 1;
+                dt_mbar_wait(&misc->bar[buf], (phase >> buf) & 1u);
             }
+            phase ^= 1u << buf;
+            pend &= ~(1u << buf);
         }
-    }
-    const bool has = v0 + lane < v1;  // every vector holds at least one element
-    const float wmax = dt_warp_max(lmax);
-    if (lane == 0) misc->red_f[wid] = wmax;
-    __syncthreads();
-    float m_c = NEG_INF;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) m_c = fmaxf(m_c, misc->red_f[w]);
-    const bool any = ch.n > 0;
-    const uint32_t mk16 = any ? (E::key(dt_to_elem<T>(m_c)) >> (E::KB - 16)) : 0u;
-    const bool finite_max = (m_c != NEG_INF);
-    if (has) {
-        const uint32_t b = mk16 - (E::key(dt_to_elem<T>(lmax)) >> (E::KB - 16));
-        if (b < 256u) atomicAdd(&chist[b], 1u);
-    }
-    if (tid == 0) {
-        misc->m = m_c;
-        misc->mk16 = mk16;
-    }
-    __syncthreads();
-    cluster.sync();
+        __syncthreads();
+        unsigned char* dbase = smem + OFF_DATA + buf * dstride;
+        Chunk<T> ch;
+        // element lo sits at the source address's offset within 16 bytes
+        ch.h = (int)(((uintptr_t)(logits + (size_t)row * (size_t)V + lo) & 15u) / sizeof(T));
+        ch.v = (const uint4*)dbase;
+        ch.n = hi - lo;
+        ch.nv = (ch.h + ch.n + EPV - 1) / EPV;
+        int v0, v1;
+        warp_vectors(ch.nv, &v0, &v1);
+        // vectors 0 and nv-1 may be partial (misaligned head, ragged tail);
+        // they take the element-wise path
+        const int full_lo = (ch.h > 0) ? 1 : 0;
+        const int full_hi = ((ch.h + ch.n) % EPV == 0) ? ch.nv : ch.nv - 1;
 
-    // ---- exchange 1: a lower bound for the Kc-th logit from the lane maxima -
-    if (tid < S) {
-        const Kn1Misc* r = cluster.map_shared_rank(misc, tid);
-        misc->cm[tid] = r->m;
-        misc->cmk[tid] = r->mk16;
-    }
-    __syncthreads();
-    uint32_t Mk16 = 0;
-    for (int j = 0; j < S; ++j) Mk16 = max(Mk16, misc->cmk[j]);
-    merge_framed(cluster, chist, S, misc->cmk, Mk16, g);
-    find_bin<false>(g, Kc, misc);
-    float bound = NEG_INF;
-    if (misc->round_digit >= 0) {
-        const uint32_t b16 = Mk16 - (uint32_t)misc->round_digit;
-        // smallest value whose key has these top bits (keys <= 127 are -inf or NaN)
-        if (b16 > 127u) bound = E::key_val(b16 << (E::KB - 16));
-    }
-
-    // ---- pass 2: sum exp(x - max); candidates at or above the bound --------
-    const float log2e = 1.44269504088896340736f;
-    const unsigned long long m2 = dt_f2_pack(m_c, m_c), l2 = dt_f2_pack(log2e, log2e);
-    unsigned long long acc = dt_f2_pack(0.f, 0.f);
-    float sum = 0.f;
-    for (int j = v0 + lane; j < v1; j += 32) {
-        const uint4 q = ch.v[j];
-        float x[EPV];
-        if (j >= full_lo && j < full_hi) {
-            if (finite_max) acc = dt_vec_expsum<T>(q, m2, l2, acc);
-            if (dt_vec_max<T>(q) >= bound) {
-                dt_vec_vals<T>(q, x);
+        // ---- pass 1: lane maxima and the chunk maximum ----------------------
+        float lmax = NEG_INF;
+        for (int j = v0 + lane; j < v1; j += 32) {
+            const uint4 q = ch.v[j];
+            if (j >= full_lo && j < full_hi) {
+                lmax = fmaxf(lmax, dt_vec_max<T>(q));
+            } else {
+                T e[EPV];
+                ch.unpack(q, e);
 #pragma unroll
                 for (int s = 0; s < EPV; ++s) {
-                    if (x[s] >= bound) {
-                        const int slot = atomicAdd(&misc->ncand, 1);
-                        if (slot < CCAP)
-                            cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
-                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + j * EPV + s - ch.h));
-                    }
-                }
-            }
-        } else {
-            dt_vec_vals<T>(q, x);
-#pragma unroll
-            for (int s = 0; s < EPV; ++s) {
-                const int idx = j * EPV + s - ch.h;
-                if (idx >= 0 && idx < ch.n) {
-                    if (finite_max) sum += dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], m_c), log2e));
-                    if (x[s] >= bound) {
-                        const int slot = atomicAdd(&misc->ncand, 1);
-                        if (slot < CCAP)
-                            cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
-                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
-                    }
+                    const int idx = j * EPV + s - ch.h;
+                    if (idx >= 0 && idx < ch.n) lmax = fmaxf(lmax, E::val(e[s]));
                 }
             }
         }
-    }
-    {
-        float a0, a1;
-        dt_f2_unpack(acc, a0, a1);
-        sum += a0 + a1;
-    }
-    sum = dt_warp_sum(sum);
-    if (lane == 0) misc->red_s[wid] = sum;
-    __syncthreads();
-    if (tid == 0) {
-        float a = 0.f;
-        for (int i = 0; i < NW; ++i) a += misc->red_s[i];
-        misc->s = a;
-    }
-    __syncthreads();
-    cluster.sync();
-
-    // ---- exchange 2: normaliser and candidate counts ------------------------
-    if (tid < S) {
-        const Kn1Misc* r = cluster.map_shared_rank(misc, tid);
-        misc->cs[tid] = r->s;
-        misc->cnc[tid] = r->ncand;
-        misc->cto[tid] = r->timeout;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float M = misc->cm[0];
-        for (int j = 1; j < S; ++j) M = fmaxf(M, misc->cm[j]);
-        float ssum = 0.f;
-        for (int j = 0; j < S; ++j)
-            if (misc->cm[j] != NEG_INF) ssum += misc->cs[j] * __expf(misc->cm[j] - M);
-        misc->lse = M + logf(ssum);
-    }
-    // every CTA sees the same counts, so the branch below is uniform across
-    // the cluster (it holds cluster barriers)
-    int total = 0;
-    bool overflow = false;
-    for (int j = 0; j < S; ++j) {
-        total += misc->cnc[j];
-        overflow |= misc->cnc[j] > CCAP;
-    }
-    overflow |= total > ACAP;
-    __syncthreads();
-    const float lse = misc->lse;
-
-    if (!overflow) {
-        // ---- gather every CTA's candidates (one warp per partner) -----------
-        for (int j = wid; j < S; j += NW) {
-            int off = 0;
-            for (int q = 0; q < j; ++q) off += misc->cnc[q];
-            const unsigned long long* rs = cluster.map_shared_rank(cand, j);
-            const int cnt = misc->cnc[j];
-            for (int i = lane; i < cnt; i += 32) all[off + i] = rs[i];
-        }
-        // partners may exit once everyone has gathered; ranking is local
-        dt_cluster_arrive();
+        const bool has = v0 + lane < v1;  // every vector holds at least one element
+        const float wmax = dt_warp_max(lmax);
+        if (lane == 0) misc->red_f[wid] = wmax;
         __syncthreads();
-        rank_and_write<T>(cand, misc->cnc[c], all, total, Kc, lse, row, cand_id, cand_lp);
-        dt_cluster_wait();
-    } else {
-        // ---- fallback: window histogram over all keys, exact radix select ---
-        uint32_t* whist = (uint32_t*)all;  // per-warp histograms
-        uint32_t* myh = whist + wid * 256;
-        for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
-        __syncthreads();
-        const uint32_t klo = mk16 >= 255u ? mk16 - 255u : 0u;
-        const float x_lo = (klo <= 127u) ? NEG_INF : E::key_val(klo << (E::KB - 16));
-        for (int j = v0 + lane; j < v1; j += 32) {
-            float x[EPV];
-            dt_vec_vals<T>(ch.v[j], x);
-            const bool full = (j >= full_lo && j < full_hi);
+        float m_c = NEG_INF;
 #pragma unroll
-            for (int s = 0; s < EPV; ++s) {
-                const int idx = j * EPV + s - ch.h;
-                if ((full || (idx >= 0 && idx < ch.n)) && x[s] >= x_lo)
-                    atomicAdd(&myh[mk16 - (E::key(dt_to_elem<T>(x[s])) >> (E::KB - 16))], 1u);
-            }
+        for (int w = 0; w < NW; ++w) m_c = fmaxf(m_c, misc->red_f[w]);
+        const bool any = ch.n > 0;
+        const uint32_t mk16 = any ? (E::key(dt_to_elem<T>(m_c)) >> (E::KB - 16)) : 0u;
+        const bool finite_max = (m_c != NEG_INF);
+        if (has) {
+            const uint32_t bn = mk16 - (E::key(dt_to_elem<T>(lmax)) >> (E::KB - 16));
+            if (bn < 256u) atomicAdd(&chist[bn], 1u);
         }
-        __syncthreads();
-        // partners last read chist (the lane-maximum histogram) before the
-        // previous cluster barrier, so it can be overwritten
-        if (tid < 256) {
-            uint32_t a = 0;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
-            chist[tid] = a;
+        if (tid == 0) {
+            misc->m = m_c;
+            misc->mk16 = mk16;
         }
         __syncthreads();
         cluster.sync();
-        merge_framed(cluster, chist, S, misc->cmk, Mk16, g);
-        find_bin<false>(g, Kc, misc);
 
-        uint32_t T_key;
-        int need;
-        int cur = 0;        // chist buffer of the last round
-        int last_bin = -1;  // per-warp histogram bin holding the threshold ties
-        if (misc->round_digit >= 0) {
-            const uint32_t t16 = Mk16 - (uint32_t)misc->round_digit;
-            need = misc->round_need;
-            if (tid < S) {
-                const int wj = (int)(misc->cmk[tid] - t16);
-                misc->ceq[tid] = (wj >= 0 && wj < 256) ? (int)cluster.map_shared_rank(chist, tid)[wj] : 0;
+        // ---- exchange 1: a lower bound for the Kc-th logit from the lane maxima
+        if (tid < S) {
+            const Kn1Misc* r = cluster.map_shared_rank(misc, tid);
+            misc->cm[tid] = r->m;
+            misc->cmk[tid] = r->mk16;
+        }
+        __syncthreads();
+        uint32_t Mk16 = 0;
+        for (int j = 0; j < S; ++j) Mk16 = max(Mk16, misc->cmk[j]);
+        merge_framed(cluster, chist, S, misc->cmk, Mk16, g);
+        dt_find_bin<false>(g, Kc, &misc->bs);
+        float bound = NEG_INF;
+        if (misc->bs.digit >= 0) {
+            const uint32_t b16 = Mk16 - (uint32_t)misc->bs.digit;
+            // smallest value whose key has these top bits (keys <= 127 are -inf or NaN)
+            if (b16 > 127u) bound = E::key_val(b16 << (E::KB - 16));
+        }
+
+        // ---- pass 2: sum exp(x - max); candidates at or above the bound ----
+        const float log2e = 1.44269504088896340736f;
+        const unsigned long long m2 = dt_f2_pack(m_c, m_c), l2 = dt_f2_pack(log2e, log2e);
+        unsigned long long acc = dt_f2_pack(0.f, 0.f);
+        float sum = 0.f;
+        for (int j = v0 + lane; j < v1; j += 32) {
+            const uint4 q = ch.v[j];
+            float x[EPV];
+            if (j >= full_lo && j < full_hi) {
+                if (finite_max) acc = dt_vec_expsum<T>(q, m2, l2, acc);
+                if (dt_vec_max<T>(q) >= bound) {
+                    dt_vec_vals<T>(q, x);
+#pragma unroll
+                    for (int s = 0; s < EPV; ++s) {
+                        if (x[s] >= bound) {
+                            const int slot = atomicAdd(&mp->ncand, 1);
+                            if (slot < CCAP)
+                                cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                             (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + j * EPV + s - ch.h));
+                        }
+                    }
+                }
+            } else {
+                dt_vec_vals<T>(q, x);
+#pragma unroll
+                for (int s = 0; s < EPV; ++s) {
+                    const int idx = j * EPV + s - ch.h;
+                    if (idx >= 0 && idx < ch.n) {
+                        if (finite_max) sum += dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], m_c), log2e));
+                        if (x[s] >= bound) {
+                            const int slot = atomicAdd(&mp->ncand, 1);
+                            if (slot < CCAP)
+                                cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                             (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
+                        }
+                    }
+                }
             }
-            last_bin = (int)(mk16 - t16);  // outside [0,256) when this CTA has no ties
-            T_key = t16 << (E::KB - 16);
-            if constexpr (E::KB == 32) {
-                // two radix rounds over the low 16 bits among keys with top bits t16
-                for (int rd = 0; rd < 2; ++rd) {
-                    const int shift = 8 - 8 * rd;
-                    const uint32_t pre = T_key >> (shift + 8);
+        }
+        {
+            float a0, a1;
+            dt_f2_unpack(acc, a0, a1);
+            sum += a0 + a1;
+        }
+        sum = dt_warp_sum(sum);
+        if (lane == 0) misc->red_s[wid] = sum;
+        __syncthreads();
+        if (tid == 0) {
+            float a = 0.f;
+            for (int i = 0; i < NW; ++i) a += misc->red_s[i];
+            mp->s = a;
+        }
+        __syncthreads();
+        cluster.sync();
+
+        // ---- exchange 2: normaliser and candidate counts --------------------
+        if (tid < S) {
+            const RowPub* r = &cluster.map_shared_rank(misc, tid)->pub[par];
+            misc->cs[tid] = r->s;
+            misc->cnc[tid] = r->ncand;
+            misc->cto[tid] = r->timeout;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float M = misc->cm[0];
+            for (int j = 1; j < S; ++j) M = fmaxf(M, misc->cm[j]);
+            float ssum = 0.f;
+            for (int j = 0; j < S; ++j)
+                if (misc->cm[j] != NEG_INF) ssum += misc->cs[j] * __expf(misc->cm[j] - M);
+            misc->lse = M + logf(ssum);
+        }
+        // every CTA sees the same counts, so the branch below is uniform across
+        // the cluster (it holds cluster barriers)
+        int total = 0;
+        bool overflow = false;
+        for (int j = 0; j < S; ++j) {
+            total += misc->cnc[j];
+            overflow |= misc->cnc[j] > CCAP;
+        }
+        overflow |= total > ACAP;
+        __syncthreads();
+        const float lse = misc->lse;
+
+        if (!overflow) {
+            // ---- gather every CTA's candidates (one warp per partner) -------
+            for (int j = wid; j < S; j += NW) {
+                int off = 0;
+                for (int q = 0; q < j; ++q) off += misc->cnc[q];
+                const unsigned long long* rs = cluster.map_shared_rank(cand, j);
+                const int cnt = misc->cnc[j];
+                for (int i = lane; i < cnt; i += 32) all[off + i] = rs[i];
+            }
+            __syncthreads();
+            if (total > DT_SORT_MIN) dt_sort_and_write<T, NT>(all, total, Kc, c, S, lse, row, cand_id, cand_lp);
+            else dt_rank_and_write<T, NT>(cand, misc->cnc[c], all, total, Kc, lse, row, cand_id, cand_lp);
+        } else {
+            // ---- fallback: window histogram over all keys, exact radix select
+            uint32_t* whist = (uint32_t*)all;  // per-warp histograms
+            uint32_t* myh = whist + wid * 256;
+            for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
+            __syncthreads();
+            const uint32_t klo = mk16 >= 255u ? mk16 - 255u : 0u;
+            const float x_lo = (klo <= 127u) ? NEG_INF : E::key_val(klo << (E::KB - 16));
+            for (int j = v0 + lane; j < v1; j += 32) {
+                float x[EPV];
+                dt_vec_vals<T>(ch.v[j], x);
+                const bool full = (j >= full_lo && j < full_hi);
+#pragma unroll
+                for (int s = 0; s < EPV; ++s) {
+                    const int idx = j * EPV + s - ch.h;
+                    if ((full || (idx >= 0 && idx < ch.n)) && x[s] >= x_lo)
+                        atomicAdd(&myh[mk16 - (E::key(dt_to_elem<T>(x[s])) >> (E::KB - 16))], 1u);
+                }
+            }
+            __syncthreads();
+            // partners last read chist (the lane-maximum histogram) before the
+            // previous cluster barrier, so it can be overwritten
+            if (tid < 256) {
+                uint32_t a = 0;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
+                chist[tid] = a;
+            }
+            __syncthreads();
+            cluster.sync();
+            merge_framed(cluster, chist, S, misc->cmk, Mk16, g);
+            dt_find_bin<false>(g, Kc, &misc->bs);
+
+            uint32_t T_key;
+            int need;
+            int cur = 0;        // chist buffer of the last round
+            int last_bin = -1;  // per-warp histogram bin holding the threshold ties
+            if (misc->bs.digit >= 0) {
+                const uint32_t t16 = Mk16 - (uint32_t)misc->bs.digit;
+                need = misc->bs.need;
+                if (tid < S) {
+                    const int wj = (int)(misc->cmk[tid] - t16);
+                    misc->ceq[tid] = (wj >= 0 && wj < 256) ? (int)cluster.map_shared_rank(chist, tid)[wj] : 0;
+                }
+                last_bin = (int)(mk16 - t16);  // outside [0,256) when this CTA has no ties
+                T_key = t16 << (E::KB - 16);
+                if constexpr (E::KB == 32) {
+                    // two radix rounds over the low 16 bits among keys with top bits t16
+                    for (int rd = 0; rd < 2; ++rd) {
+                        const int shift = 8 - 8 * rd;
+                        const uint32_t pre = T_key >> (shift + 8);
+                        __syncthreads();
+                        for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
+                        __syncthreads();
+                        for (int j = v0 + lane; j < v1; j += 32) {
+                            T e[EPV];
+                            ch.unpack(ch.v[j], e);
+#pragma unroll
+                            for (int s = 0; s < EPV; ++s) {
+                                const int idx = j * EPV + s - ch.h;
+                                const uint32_t k = E::key(e[s]);
+                                if (idx >= 0 && idx < ch.n && (k >> (shift + 8)) == pre)
+                                    atomicAdd(&myh[(k >> shift) & 255u], 1u);
+                            }
+                        }
+                        __syncthreads();
+                        cur ^= 1;
+                        if (tid < 256) {
+                            uint32_t a = 0;
+#pragma unroll
+                            for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
+                            chist[cur * 256 + tid] = a;
+                        }
+                        __syncthreads();
+                        cluster.sync();
+                        merge_plain(cluster, chist + cur * 256, S, g);
+                        dt_find_bin<true>(g, need, &misc->bs);
+                        const uint32_t dg = (uint32_t)misc->bs.digit;
+                        need = misc->bs.need;
+                        T_key |= dg << shift;
+                        last_bin = (int)dg;
+                        if (tid < S) misc->ceq[tid] = (int)cluster.map_shared_rank(chist, tid)[cur * 256 + dg];
+                        __syncthreads();
+                    }
+                }
+            } else {
+                // the window holds fewer than Kc keys: full radix over the whole key
+                need = Kc;
+                T_key = 0;
+                for (int rd = 0; rd < E::KB / 8; ++rd) {
+                    const int shift = E::KB - 8 - 8 * rd;
+                    const uint32_t pre = rd ? (T_key >> (shift + 8)) : 0u;
                     __syncthreads();
                     for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
                     __syncthreads();
@@ -468,7 +494,7 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
                         for (int s = 0; s < EPV; ++s) {
                             const int idx = j * EPV + s - ch.h;
                             const uint32_t k = E::key(e[s]);
-                            if (idx >= 0 && idx < ch.n && (k >> (shift + 8)) == pre)
+                            if (idx >= 0 && idx < ch.n && (rd == 0 || (k >> (shift + 8)) == pre))
                                 atomicAdd(&myh[(k >> shift) & 255u], 1u);
                         }
                     }
@@ -483,138 +509,108 @@ __global__ void __launch_bounds__(NT) kn1_kernel(const T* __restrict__ logits, i
                     __syncthreads();
                     cluster.sync();
                     merge_plain(cluster, chist + cur * 256, S, g);
-                    find_bin<true>(g, need, misc);
-                    const uint32_t dg = (uint32_t)misc->round_digit;
-                    need = misc->round_need;
+                    dt_find_bin<true>(g, need, &misc->bs);
+                    const uint32_t dg = (uint32_t)misc->bs.digit;
+                    need = misc->bs.need;
                     T_key |= dg << shift;
                     last_bin = (int)dg;
                     if (tid < S) misc->ceq[tid] = (int)cluster.map_shared_rank(chist, tid)[cur * 256 + dg];
                     __syncthreads();
                 }
             }
-        } else {
-            // the window holds fewer than Kc keys: full radix over the whole key
-            need = Kc;
-            T_key = 0;
-            for (int rd = 0; rd < E::KB / 8; ++rd) {
-                const int shift = E::KB - 8 - 8 * rd;
-                const uint32_t pre = rd ? (T_key >> (shift + 8)) : 0u;
-                __syncthreads();
-                for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
-                __syncthreads();
-                for (int j = v0 + lane; j < v1; j += 32) {
-                    T e[EPV];
-                    ch.unpack(ch.v[j], e);
+            // threshold ties per warp slice, straight from the last round's histograms
+            if (tid < NW) misc->weq[tid] = (last_bin >= 0 && last_bin < 256) ? (int)whist[tid * 256 + last_bin] : 0;
+            __syncthreads();
+
+            // emit keys above T, plus the first `need` ties by token id, into sel
+            unsigned long long* sel = cand;
+            int eqbase = 0;
+            for (int j = 0; j < c; ++j) eqbase += misc->ceq[j];
+            for (int w = 0; w < wid; ++w) eqbase += misc->weq[w];
+            const float Tv = E::key_val(T_key);
+            int running = 0;
+            for (int base = v0; base < v1; base += 32) {
+                const int j = base + lane;
+                float x[EPV];
+                int neq = 0;
+                bool ok[EPV];
+                if (j < v1) {
+                    dt_vec_vals<T>(ch.v[j], x);
+                    const bool full = (j >= full_lo && j < full_hi);
 #pragma unroll
                     for (int s = 0; s < EPV; ++s) {
                         const int idx = j * EPV + s - ch.h;
-                        const uint32_t k = E::key(e[s]);
-                        if (idx >= 0 && idx < ch.n && (rd == 0 || (k >> (shift + 8)) == pre))
-                            atomicAdd(&myh[(k >> shift) & 255u], 1u);
+                        ok[s] = full || (idx >= 0 && idx < ch.n);
+                        neq += (ok[s] && x[s] == Tv);
                     }
                 }
-                __syncthreads();
-                cur ^= 1;
-                if (tid < 256) {
-                    uint32_t a = 0;
+                const int inc = dt_warp_incl_scan(neq);
+                int r = running + inc - neq;  // ties before this lane's vector in this warp slice
+                running += __shfl_sync(0xffffffffu, inc, 31);
+                if (j < v1) {
 #pragma unroll
-                    for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
-                    chist[cur * 256 + tid] = a;
-                }
-                __syncthreads();
-                cluster.sync();
-                merge_plain(cluster, chist + cur * 256, S, g);
-                find_bin<true>(g, need, misc);
-                const uint32_t dg = (uint32_t)misc->round_digit;
-                need = misc->round_need;
-                T_key |= dg << shift;
-                last_bin = (int)dg;
-                if (tid < S) misc->ceq[tid] = (int)cluster.map_shared_rank(chist, tid)[cur * 256 + dg];
-                __syncthreads();
-            }
-        }
-        // threshold ties per warp slice, straight from the last round's histograms
-        if (tid < NW) misc->weq[tid] = (last_bin >= 0 && last_bin < 256) ? (int)whist[tid * 256 + last_bin] : 0;
-        __syncthreads();
-
-        // emit keys above T, plus the first `need` ties by token id, into sel
-        unsigned long long* sel = cand;
-        int eqbase = 0;
-        for (int j = 0; j < c; ++j) eqbase += misc->ceq[j];
-        for (int w = 0; w < wid; ++w) eqbase += misc->weq[w];
-        const float Tv = E::key_val(T_key);
-        int running = 0;
-        for (int base = v0; base < v1; base += 32) {
-            const int j = base + lane;
-            float x[EPV];
-            int neq = 0;
-            bool ok[EPV];
-            if (j < v1) {
-                dt_vec_vals<T>(ch.v[j], x);
-                const bool full = (j >= full_lo && j < full_hi);
-#pragma unroll
-                for (int s = 0; s < EPV; ++s) {
-                    const int idx = j * EPV + s - ch.h;
-                    ok[s] = full || (idx >= 0 && idx < ch.n);
-                    neq += (ok[s] && x[s] == Tv);
-                }
-            }
-            const int inc = dt_warp_incl_scan(neq);
-            int r = running + inc - neq;  // ties before this lane's vector in this warp slice
-            running += __shfl_sync(0xffffffffu, inc, 31);
-            if (j < v1) {
-#pragma unroll
-                for (int s = 0; s < EPV; ++s) {
-                    if (!ok[s] || !(x[s] >= Tv)) continue;
-                    bool take = true;
-                    if (x[s] == Tv) {
-                        take = (eqbase + r < need);
-                        ++r;
-                    }
-                    if (take) {
-                        const int idx = j * EPV + s - ch.h;
-                        const int slot = atomicAdd(&misc->nsel, 1);
-                        if (slot < Kc)
-                            sel[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
-                                        (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
+                    for (int s = 0; s < EPV; ++s) {
+                        if (!ok[s] || !(x[s] >= Tv)) continue;
+                        bool take = true;
+                        if (x[s] == Tv) {
+                            take = (eqbase + r < need);
+                            ++r;
+                        }
+                        if (take) {
+                            const int idx = j * EPV + s - ch.h;
+                            const int slot = atomicAdd(&mp->nsel, 1);
+                            if (slot < Kc)
+                                sel[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                            (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
+                        }
                     }
                 }
             }
+            __syncthreads();
+            cluster.sync();
+            // gather every CTA's selection (one warp per partner); this
+            // overwrites the per-warp histograms, whose last read was before
+            // the barrier
+            if (tid < S) misc->cnsel[tid] = min(Kc, cluster.map_shared_rank(misc, tid)->pub[par].nsel);
+            __syncthreads();
+            for (int j = wid; j < S; j += NW) {
+                int off = 0;
+                for (int q = 0; q < j; ++q) off += misc->cnsel[q];
+                const unsigned long long* rs = cluster.map_shared_rank(sel, j);
+                const int cnt = misc->cnsel[j];
+                for (int i = lane; i < cnt; i += 32)
+                    if (off + i < Kc) all[off + i] = rs[i];
+            }
+            int tot = 0;
+            for (int q = 0; q < S; ++q) tot += misc->cnsel[q];
+            tot = min(tot, Kc);
+            __syncthreads();
+            if (tot > DT_SORT_MIN) dt_sort_and_write<T, NT>(all, tot, Kc, c, S, lse, row, cand_id, cand_lp);
+            else dt_rank_and_write<T, NT>(sel, misc->cnsel[c], all, tot, Kc, lse, row, cand_id, cand_lp);
         }
-        __syncthreads();
-        cluster.sync();
-        // gather every CTA's selection (one warp per partner); this overwrites
-        // the per-warp histograms, whose last read was before the barrier
-        if (tid < S) misc->cnsel[tid] = min(Kc, cluster.map_shared_rank(misc, tid)->nsel);
-        __syncthreads();
-        for (int j = wid; j < S; j += NW) {
-            int off = 0;
-            for (int q = 0; q < j; ++q) off += misc->cnsel[q];
-            const unsigned long long* rs = cluster.map_shared_rank(sel, j);
-            const int cnt = misc->cnsel[j];
-            for (int i = lane; i < cnt; i += 32)
-                if (off + i < Kc) all[off + i] = rs[i];
+        if (c == 0 && tid == 0) {
+            int to = 0;
+            for (int j = 0; j < S; ++j) to |= misc->cto[j];
+            lse_out[row] = to ? __int_as_float(0x7FC00000) : lse;
         }
-        int tot = 0;
-        for (int q = 0; q < S; ++q) tot += misc->cnsel[q];
-        tot = min(tot, Kc);
-        dt_cluster_arrive();
-        __syncthreads();
-        rank_and_write<T>(sel, misc->cnsel[c], all, tot, Kc, lse, row, cand_id, cand_lp);
-        dt_cluster_wait();
+        // without a second buffer the next row's copy starts only now
+        if (nbuf == 1 && nxt < rows) {
+            __syncthreads();
+            dt_fence_proxy_async();
+            issue(0, nxt);
+        }
+        if (nbuf == 2) buf ^= 1;
     }
-    if (c == 0 && tid == 0) {
-        int to = 0;
-        for (int j = 0; j < S; ++j) to |= misc->cto[j];
-        lse_out[row] = to ? __int_as_float(0x7FC00000) : lse;
-    }
+    // partners may still be gathering from this CTA's shared memory
+    __syncthreads();
+    cluster.sync();
 }
 
 }  // namespace
 
-size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize) {
+size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize, int nbuf) {
     (void)Kc;  // the fixed candidate buffers also hold the fallback's Kc <= 1024 selections
-    return OFF_DATA + (size_t)chunk * esize + 32;
+    return OFF_DATA + (size_t)nbuf * ((((size_t)chunk * esize + 32) + 127) & ~(size_t)127);
 }
 
 // Sets the kernel's shared-memory and cluster-size attributes for a launch.
@@ -625,9 +621,9 @@ cudaError_t kn1_prepare(int S, size_t smem) {
     return e;
 }
 
-int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc) {
+int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc, int nbuf) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
-    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize);
+    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize, nbuf);
     if (dtype == DT_BF16) {
         if (kn1_prepare<uint16_t>(S, smem) != cudaSuccess) return 0;
         return dt_max_active_clusters(kn1_kernel<uint16_t>, S, NT, smem);
@@ -636,18 +632,18 @@ int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc) {
     return dt_max_active_clusters(kn1_kernel<float>, S, NT, smem);
 }
 
-cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int L, int V, int Kc, int S, int chunk,
-                          float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st) {
+cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int grid_rows, int V, int Kc, int S, int chunk,
+                          int nbuf, float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
-    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize);
-    DtLaunch lc(dim3(S, rows, 1), dim3(NT, 1, 1), smem, st, S);
+    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize, nbuf);
+    DtLaunch lc(dim3(S, grid_rows, 1), dim3(NT, 1, 1), smem, st, S);
     cudaError_t e;
     if (dtype == DT_BF16) {
         if ((e = kn1_prepare<uint16_t>(S, smem)) != cudaSuccess) return e;
-        return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<uint16_t>, (const uint16_t*)logits, V, chunk, Kc, L, lse,
-                                  cand_id, cand_lp);
+        return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<uint16_t>, (const uint16_t*)logits, V, chunk, Kc, rows, nbuf,
+                                  lse, cand_id, cand_lp);
     }
     if ((e = kn1_prepare<float>(S, smem)) != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<float>, (const float*)logits, V, chunk, Kc, L, lse, cand_id,
-                              cand_lp);
+    return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<float>, (const float*)logits, V, chunk, Kc, rows, nbuf, lse,
+                              cand_id, cand_lp);
 }

@@ -1,0 +1,407 @@
+// kn1b_rows.cu -- stage 1 for batches of many rows: one CTA per row.
+//
+// [DARTree] Algorithm 1, its per-position Top-K candidate step; [DDTree] section 3.3
+// (log-domain scores of each position's Top-K tokens).
+//
+// With enough rows (request b, position l) to fill the GPU, a whole row per
+// CTA needs no cross-CTA exchange at all:
+//   pass 1  streams the row from HBM with 16-byte loads, four in flight per
+//           thread; each thread keeps a running maximum and sum exp(x - max)
+//           (rescaled whenever the maximum grows) and, per load slot u, the
+//           maximum of the vectors it loaded in that slot: 4 x 512 = 2048
+//           maxima of distinct elements;
+//   the CTA merges the (max, sum) pairs into the row's log-normaliser and
+//   takes the Kc-th largest slot maximum (256-bin histogram of order keys
+//   below the row maximum) as a lower bound for the row's Kc-th largest logit;
+//   pass 2  re-reads, cooperatively, only the vectors of slots whose maximum
+//           reaches the bound (a slot below it holds no candidate), keeping
+//           every element at or above the bound;
+//   the candidates are ranked exactly (logit descending, token id ascending)
+//   and the top Kc written.
+// A row whose candidates overflow the buffer (many equal logits) takes the
+// exact fallback: 8-bit radix rounds over the whole key with per-warp
+// histograms over contiguous warp slices, then an emit pass taking threshold
+// ties in token-id order.
+#include "dt_launch.h"
+#include "kn1_common.cuh"
+
+namespace {
+
+constexpr int NT = 512;
+constexpr int NW = NT / 32;
+constexpr int UNR = 4;      // 16-byte loads in flight per thread, and its maximum slots
+constexpr int CAP = 2048;   // candidates of a row
+
+struct Kn1bMisc {
+    float wm[NW];  // per-warp running maximum and sum
+    float ws[NW];
+    float m;       // row maximum
+    float lse;
+    int ncand;
+    int nsel;
+    int nslot;     // slots whose maximum reaches the bound
+    int weq[NW];   // fallback: threshold ties per warp slice
+    DtBinSearch bs;
+};
+
+// Dynamic shared memory: [misc 1 KB][hist 1 KB][rank scratch 4 KB][cand CAP*8]
+// [work CAP*8].  `work` holds, in turn, the list of slots to re-read (pass 2),
+// the fallback's per-warp histograms (NW KB), and the rank buckets.
+constexpr size_t OFF_HIST = 1024;
+constexpr size_t OFF_RS = OFF_HIST + 1024;
+constexpr size_t OFF_CAND = OFF_RS + 4096;
+constexpr size_t OFF_WORK = OFF_CAND + (size_t)CAP * 8;
+constexpr size_t SMEM = OFF_WORK + (size_t)CAP * 8;
+static_assert(sizeof(Kn1bMisc) <= OFF_HIST, "misc block overflows its slot");
+static_assert(sizeof(DtRankScratch) <= 4096, "rank scratch overflows its slot");
+static_assert((size_t)CAP * 8 >= (size_t)NW * 1024, "per-warp histograms must fit the work area");
+static_assert(NT * UNR <= CAP * 2, "the slot list must fit the work area");
+
+template <typename T>
+DT_DI uint4 ldv(const T* row, int v) {
+    return __ldg(reinterpret_cast<const uint4*>(row) + v);
+}
+
+// Folds a vector (values x, maximum vm) into a running (max M, sum S of
+// exp(x - M)).  x - M is rounded before the product with log2(e), so an
+// element equal to M adds exactly 1 at any magnitude.
+template <int EPV>
+DT_DI void online_add(const float (&x)[EPV], float vm, float& M, float& S) {
+    const float NEG_INF = -__int_as_float(0x7F800000);
+    const float log2e = 1.44269504088896340736f;
+    if (vm > M) {
+        S = (M == NEG_INF) ? 0.f : __fmul_rn(S, dt_ex2_approx(__fmul_rn(__fsub_rn(M, vm), log2e)));
+        M = vm;
+    }
+    if (M == NEG_INF) return;  // every element so far is -inf
+    float e[EPV];
+#pragma unroll
+    for (int s = 0; s < EPV; ++s) e[s] = dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], M), log2e));
+#pragma unroll
+    for (int w = EPV / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int s = 0; s < w; ++s) e[s] = __fadd_rn(e[s], e[s + w]);
+    S = __fadd_rn(S, e[0]);
+}
+
+// (M, S) <- the merge of two running (max, sum) pairs.
+DT_DI void merge_pair(float& M, float& S, float M2, float S2) {
+    const float NEG_INF = -__int_as_float(0x7F800000);
+    const float log2e = 1.44269504088896340736f;
+    const float Mn = fmaxf(M, M2);
+    const float a = (M == NEG_INF) ? 0.f : __fmul_rn(S, dt_ex2_approx(__fmul_rn(__fsub_rn(M, Mn), log2e)));
+    const float b = (M2 == NEG_INF) ? 0.f : __fmul_rn(S2, dt_ex2_approx(__fmul_rn(__fsub_rn(M2, Mn), log2e)));
+    M = Mn;
+    S = __fadd_rn(a, b);
+}
+
+// Exact fallback for a row whose candidates overflowed the buffer: 8-bit radix
+// rounds over the whole key, per-warp histograms over contiguous warp slices,
+// then an emit pass that takes threshold ties in token-id order; the Kc
+// selected are ranked and written.  Kept out of line so that its registers do
+// not weigh on the common path.
+template <typename T>
+__device__ __noinline__ void fallback_row(const T* __restrict__ rp, int V, int nfull, int nvec, int Kc, float lse,
+                                          uint32_t mk16, int row, Kn1bMisc* misc, uint32_t* hist, DtRankScratch* rs,
+                                          unsigned long long* cand, unsigned char* work,
+                                          int32_t* __restrict__ cand_id, float* __restrict__ cand_lp) {
+    using E = DtElem<T>;
+    constexpr int EPV = 16 / sizeof(T);
+    const float NEG_INF = -__int_as_float(0x7F800000);
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t* whist = (uint32_t*)work;
+    unsigned long long* bucket = (unsigned long long*)work;
+    // ---- fallback: exact radix select over the whole key --------------
+    const int vseg = (nvec + NW - 1) / NW;
+    const int v0 = min(nvec, wid * vseg), v1 = min(nvec, v0 + vseg);
+    uint32_t* myh = whist + wid * 256;
+    auto get = [&](int v, float (&x)[EPV]) {  // values, -inf past the row
+        if (v < nfull) {
+            dt_vec_vals<T>(ldv(rp, v), x);
+        } else {
+#pragma unroll
+            for (int s = 0; s < EPV; ++s) x[s] = v * EPV + s < V ? E::val(rp[v * EPV + s]) : NEG_INF;
+        }
+    };
+    uint32_t T_key = 0;
+    int need = Kc, last_bin = 0;
+    for (int rd = 0; rd < E::KB / 8; ++rd) {
+        const int shift = E::KB - 8 - 8 * rd;
+        const uint32_t pre = rd ? (T_key >> (shift + 8)) : 0u;
+        __syncthreads();
+        for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
+        __syncthreads();
+        for (int v = v0 + lane; v < v1; v += 32) {
+            float x[EPV];
+            get(v, x);
+#pragma unroll
+            for (int s = 0; s < EPV; ++s) {
+                const uint32_t k = E::key(dt_to_elem<T>(x[s]));
+                if (v * EPV + s < V && (rd == 0 || (k >> (shift + 8)) == pre))
+                    atomicAdd(&myh[(k >> shift) & 255u], 1u);
+            }
+        }
+        __syncthreads();
+        if (tid < 256) {
+            uint32_t a = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) a += whist[w * 256 + tid];
+            hist[tid] = a;
+        }
+        __syncthreads();
+        dt_find_bin<true>(hist, need, &misc->bs);
+        const uint32_t dg = (uint32_t)misc->bs.digit;
+        need = misc->bs.need;
+        T_key |= dg << shift;
+        last_bin = (int)dg;
+    }
+    // threshold ties per warp slice, from the last round's histograms
+    if (tid < NW) misc->weq[tid] = (int)whist[tid * 256 + last_bin];
+    __syncthreads();
+    int eqbase = 0;
+    for (int w = 0; w < wid; ++w) eqbase += misc->weq[w];
+    const float Tv = E::key_val(T_key);
+    int running = 0;
+    for (int base = v0; base < v1; base += 32) {
+        const int v = base + lane;
+        float x[EPV];
+        int neq = 0;
+        if (v < v1) {
+            get(v, x);
+#pragma unroll
+            for (int s = 0; s < EPV; ++s) neq += (v * EPV + s < V && x[s] == Tv);
+        }
+        const int inc = dt_warp_incl_scan(neq);
+        int r = running + inc - neq;  // ties before this lane's vector in this warp slice
+        running += __shfl_sync(0xffffffffu, inc, 31);
+        if (v < v1) {
+#pragma unroll
+            for (int s = 0; s < EPV; ++s) {
+                if (v * EPV + s >= V || !(x[s] >= Tv)) continue;
+                bool take = true;
+                if (x[s] == Tv) {
+                    take = (eqbase + r < need);
+                    ++r;
+                }
+                if (take) {
+                    const int slot = atomicAdd(&misc->nsel, 1);
+                    if (slot < Kc)
+                        cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                     (unsigned long long)(0xFFFFFFFFu - (uint32_t)(v * EPV + s));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int tot = min(misc->nsel, Kc);
+    // the per-warp histograms are no longer read: `work` becomes the buckets
+    if (tot <= 64 ||
+        !dt_bucket_rank_and_write<T, NT>(cand, tot, 0, tot, mk16, Kc, lse, row, cand_id, cand_lp, rs,
+                                         bucket)) {
+        if (tot <= 64) dt_rank_and_write<T, NT>(cand, tot, cand, tot, Kc, lse, row, cand_id, cand_lp);
+        else dt_sort_and_write<T, NT>(cand, tot, Kc, 0, 1, lse, row, cand_id, cand_lp);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 2) kn1b_kernel(const T* __restrict__ logits, int V, int Kc, int rows,
+                                                     float* __restrict__ lse_out, int32_t* __restrict__ cand_id,
+                                                     float* __restrict__ cand_lp) {
+    using E = DtElem<T>;
+    constexpr int EPV = 16 / sizeof(T);
+    const float NEG_INF = -__int_as_float(0x7F800000);
+    extern __shared__ __align__(128) unsigned char smem[];
+    Kn1bMisc* misc = (Kn1bMisc*)smem;
+    uint32_t* hist = (uint32_t*)(smem + OFF_HIST);
+    DtRankScratch* rs = (DtRankScratch*)(smem + OFF_RS);
+    unsigned long long* cand = (unsigned long long*)(smem + OFF_CAND);
+    int* slots = (int*)(smem + OFF_WORK);
+    unsigned long long* bucket = (unsigned long long*)(smem + OFF_WORK);
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+    dt_pdl_trigger();
+    dt_pdl_wait();  // the logits may come from the kernel just before us
+
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+        const T* rp = logits + (size_t)row * (size_t)V;
+        const bool aligned = ((uintptr_t)rp & 15u) == 0;
+        const int nfull = aligned ? V / EPV : 0;  // vectors read with 16-byte loads
+        const int nvec = (V + EPV - 1) / EPV;
+        if (tid < 256) hist[tid] = 0;
+        if (tid == 0) {
+            misc->ncand = 0;
+            misc->nsel = 0;
+            misc->nslot = 0;
+        }
+
+        // ---- pass 1: running (max, sum exp) and slot maxima ------------------
+        float M = NEG_INF, S = 0.f;
+        float gm[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) gm[u] = NEG_INF;
+        uint32_t gv = 0;  // bit u: slot u holds at least one element
+        for (int v0 = tid; v0 < nfull; v0 += UNR * NT) {
+            uint4 q[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u)
+                if (v0 + u * NT < nfull) q[u] = ldv(rp, v0 + u * NT);
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                if (v0 + u * NT < nfull) {
+                    const float vm = dt_vec_max<T>(q[u]);
+                    gm[u] = fmaxf(gm[u], vm);
+                    gv |= 1u << u;
+                    float x[EPV];
+                    dt_vec_vals<T>(q[u], x);
+                    online_add<EPV>(x, vm, M, S);
+                }
+            }
+        }
+        // the rest -- a ragged last vector, or every vector of a row that is not
+        // 16-byte aligned -- with element loads (-inf fill adds nothing)
+        for (int v = nfull + tid; v < nvec; v += NT) {
+            float x[EPV];
+            float vm = NEG_INF;
+#pragma unroll
+            for (int s = 0; s < EPV; ++s) {
+                const int idx = v * EPV + s;
+                x[s] = idx < V ? E::val(rp[idx]) : NEG_INF;
+                vm = fmaxf(vm, x[s]);
+            }
+            gm[0] = fmaxf(gm[0], vm);
+            gv |= 1u;
+            online_add<EPV>(x, vm, M, S);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
+            const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+            merge_pair(M, S, M2, S2);
+        }
+        if (lane == 0) {
+            misc->wm[wid] = M;
+            misc->ws[wid] = S;
+        }
+        __syncthreads();
+        if (wid == 0) {
+            float m2 = lane < NW ? misc->wm[lane] : NEG_INF;
+            float s2 = lane < NW ? misc->ws[lane] : 0.f;
+            for (int o = 16; o > 0; o >>= 1) {
+                const float M2 = __shfl_xor_sync(0xffffffffu, m2, o);
+                const float S2 = __shfl_xor_sync(0xffffffffu, s2, o);
+                merge_pair(m2, s2, M2, S2);
+            }
+            if (lane == 0) {
+                misc->m = m2;
+                misc->lse = m2 + logf(s2);
+            }
+        }
+        __syncthreads();
+        const float mrow = misc->m;
+        const float lse = misc->lse;
+
+        // ---- the bound: Kc-th largest slot maximum ---------------------------
+        const uint32_t mk16 = E::key(dt_to_elem<T>(mrow)) >> (E::KB - 16);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            if ((gv >> u) & 1u) {
+                const uint32_t b = mk16 - (E::key(dt_to_elem<T>(gm[u])) >> (E::KB - 16));
+                if (b < 256u) atomicAdd(&hist[b], 1u);
+            }
+        }
+        __syncthreads();
+        dt_find_bin<false>(hist, Kc, &misc->bs);
+        float bound = NEG_INF;
+        if (misc->bs.digit >= 0) {
+            const uint32_t b16 = mk16 - (uint32_t)misc->bs.digit;
+            // smallest value whose key has these top bits (keys <= 127 are -inf or NaN)
+            if (b16 > 127u) bound = E::key_val(b16 << (E::KB - 16));
+        }
+
+        // ---- pass 2: re-read the slots that reach the bound ------------------
+        auto keep = [&](float xv, int idx) {
+            const int slot = atomicAdd(&misc->ncand, 1);
+            if (slot < CAP)
+                cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(xv)) << 32) |
+                             (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+        };
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+            if (((gv >> u) & 1u) && gm[u] >= bound && tid + u * NT < nfull)
+                slots[atomicAdd(&misc->nslot, 1)] = tid + u * NT;  // first vector of the slot
+        __syncthreads();
+        {
+            // item i: vector k of listed slot j (slot vectors are UNR * NT apart)
+            const int per = (nfull + UNR * NT - 1) / (UNR * NT);
+            const int items = misc->nslot * per;
+            for (int i0 = tid; i0 < items; i0 += UNR * NT) {
+                uint4 q[UNR];
+                int vv[UNR];
+#pragma unroll
+                for (int u = 0; u < UNR; ++u) {
+                    const int i = i0 + u * NT;
+                    vv[u] = i < items ? slots[i / per] + (i % per) * (UNR * NT) : nfull;
+                    if (vv[u] < nfull) q[u] = ldv(rp, vv[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < UNR; ++u) {
+                    if (vv[u] < nfull && dt_vec_max<T>(q[u]) >= bound) {
+                        float x[EPV];
+                        dt_vec_vals<T>(q[u], x);
+#pragma unroll
+                        for (int s = 0; s < EPV; ++s)
+                            if (x[s] >= bound) keep(x[s], vv[u] * EPV + s);
+                    }
+                }
+            }
+        }
+        if (((gv & 1u) && gm[0] >= bound) || bound == NEG_INF) {
+            for (int v = nfull + tid; v < nvec; v += NT) {
+#pragma unroll
+                for (int s = 0; s < EPV; ++s) {
+                    const int idx = v * EPV + s;
+                    if (idx < V) {
+                        const float xv = E::val(rp[idx]);
+                        if (xv >= bound) keep(xv, idx);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        const int total = misc->ncand;
+
+        if (total <= CAP) {
+            if (total <= 64 ||
+                !dt_bucket_rank_and_write<T, NT>(cand, total, 0, total, mk16, Kc, lse, row, cand_id, cand_lp, rs,
+                                                 bucket)) {
+                if (total <= 64) dt_rank_and_write<T, NT>(cand, total, cand, total, Kc, lse, row, cand_id, cand_lp);
+                else dt_sort_and_write<T, NT>(cand, total, Kc, 0, 1, lse, row, cand_id, cand_lp);
+            }
+        } else {
+            fallback_row<T>(rp, V, nfull, nvec, Kc, lse, mk16, row, misc, hist, rs, cand, smem + OFF_WORK, cand_id,
+                            cand_lp);
+        }
+        if (tid == 0) lse_out[row] = lse;
+        __syncthreads();  // the next row reuses every buffer
+    }
+}
+
+}  // namespace
+
+size_t dt_kn1b_smem_bytes() { return SMEM; }
+
+cudaError_t dt_kn1b_launch(const void* logits, int dtype, int rows, int V, int Kc, float* lse, int32_t* cand_id,
+                           float* cand_lp, cudaStream_t st) {
+    DtLaunch lc(dim3(rows, 1, 1), dim3(NT, 1, 1), SMEM, st);
+    cudaError_t e;
+    if (dtype == DT_BF16) {
+        if ((e = cudaFuncSetAttribute(kn1b_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
+            cudaSuccess)
+            return e;
+        return cudaLaunchKernelEx(&lc.cfg, kn1b_kernel<uint16_t>, (const uint16_t*)logits, V, Kc, rows, lse, cand_id,
+                                  cand_lp);
+    }
+    if ((e = cudaFuncSetAttribute(kn1b_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
+        cudaSuccess)
+        return e;
+    return cudaLaunchKernelEx(&lc.cfg, kn1b_kernel<float>, (const float*)logits, V, Kc, rows, lse, cand_id, cand_lp);
+}

@@ -97,6 +97,7 @@ struct Rows {
     int t0, t1, t2;       // which row (target: node, drafter: position) a buffer holds; -1 none
     uint32_t pend;        // bit i: a bulk copy into buffer i has not been waited for
     uint32_t ph;          // bit i: mbarrier phase parity of buffer i
+    DtStager<T> s0, s1, s2;  // ragged chunk ends of each buffer's latest copy, in registers
 
     DT_DI void init(unsigned char* b, int s, uint64_t* bars) {
         base = b;
@@ -105,13 +106,22 @@ struct Rows {
         h0 = h1 = h2 = 0;
         t0 = t1 = t2 = -1;
         pend = ph = 0;
+        s0.held_off = s1.held_off = s2.held_off = -1;
     }
     DT_DI int holds(int i) const { return i == 0 ? t0 : (i == 1 ? t1 : t2); }
     DT_DI int head(int i) const { return i == 0 ? h0 : (i == 1 ? h1 : h2); }
     DT_DI const uint4* vec(int i) const { return (const uint4*)(base + (size_t)i * stride); }
     DT_DI const T* elems(int i) const { return (const T*)(base + (size_t)i * stride) + head(i); }
-    // Waits (one thread) for buffer i's copy; the caller syncs the block before reading.
+    // Completes buffer i: stores its ragged ends, then one thread waits for
+    // its bulk copy.  The caller syncs the block before reading.
     DT_DI void wait(int i, int* timeout) {
+        unsigned char* dst = base + (size_t)i * stride;
+        if (i == 0) s0.finish(dst);
+        else if (i == 1) s1.finish(dst);
+        else s2.finish(dst);
+        if (i == 0) s0.held_off = -1;
+        else if (i == 1) s1.held_off = -1;
+        else s2.held_off = -1;
         if (!((pend >> i) & 1u)) return;
         if (threadIdx.x == 0 && !dt_mbar_wait(&bar[i], (ph >> i) & 1u)) {
             *timeout = 1;
@@ -127,10 +137,10 @@ struct Rows {
         wait(i, timeout);
         __syncthreads();
         dt_fence_proxy_async();
-        uint32_t bytes = 0;
         unsigned char* dst = base + (size_t)i * stride;
-        const T* x = dt_stage_row<T>(row, lo, hi, dst, &bar[i], &bytes);
-        const int hd = (int)(((const unsigned char*)x - dst) / sizeof(T));
+        const uint32_t bytes = i == 0 ? s0.start(row, lo, hi, dst, &bar[i])
+                                      : (i == 1 ? s1.start(row, lo, hi, dst, &bar[i]) : s2.start(row, lo, hi, dst, &bar[i]));
+        const int hd = (int)(((uintptr_t)(row + lo) & 15u) / sizeof(T));
         if (bytes) pend |= 1u << i;
         if (i == 0) { h0 = hd; t0 = tag; }
         else if (i == 1) { h1 = hd; t1 = tag; }

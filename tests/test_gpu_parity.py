@@ -123,7 +123,9 @@ CAND_CASES = [
     (1, 16, 151936, "bf16", 256, 3.0, 0.7),  # single request at Qwen3 vocabulary (16-CTA clusters)
     (2, 4, 151936, "bf16", 1024, 3.0, 0.7),  # largest candidate list
     (1, 2, 151936, "f32", 64, 3.0, 0.7),
-    (20, 16, 151936, "bf16", 60, 3.0, 0.5),  # many rows: 8-CTA clusters
+    (20, 16, 151936, "bf16", 60, 3.0, 0.5),  # many rows: persistent clusters prefetching their next row
+    (8, 16, 151936, "bf16", 1024, 3.0, 0.7),  # many rows, largest list: sorted ranking
+    (6, 16, 151936, "f32", 256, 3.0, 0.7),    # many fp32 rows
 ]
 
 
@@ -172,6 +174,45 @@ def test_candidates_edge_rows():
         assert np.max(np.abs(tree.lse[0].cpu().numpy() - lse64)) < TOL
         assert tree.cand_id[0, 3, :2].cpu().tolist() == [7, 19999]
         assert abs(float(tree.lse[0, 3]) - math.log(2.0)) < TOL
+
+
+@pytest.mark.parametrize("batch", [6, 16])
+def test_candidates_edge_rows_among_many(batch):
+    # many rows, so that CTAs or clusters run through several rows in turn;
+    # edge rows (equal logits, an outlier, -inf runs) between Gaussian rows
+    # switch between the candidate path and the exact fallback from one row to
+    # the next
+    L, V, Kc = 16, 20000, 40
+    g = torch.Generator().manual_seed(99)
+    x = torch.randn((batch * L, V), generator=g) * 2
+    for r in range(0, batch * L, 5):
+        kind = (r // 5) % 4
+        if kind == 0:
+            x[r] = 0.75
+        elif kind == 1:
+            x[r, (r * 37) % V] = 1e30
+        elif kind == 2:
+            x[r, r % 3::3] = -float("inf")
+        else:
+            x[r] = -float("inf")
+            x[r, r % V] = 1.0
+    for dtype in ("bf16", "f32"):
+        xx = x.to(torch.bfloat16) if dtype == "bf16" else x.clone()
+        p = dtree.Params(mode="ddtree", batch=batch, L=L, V=V, dtype=dtype, K=Kc, B=Kc)
+        tree = dtree.TreeBuffers.for_params(p)
+        dtree.candidates(p, xx.reshape(batch, L, V).contiguous().cuda(), tree)
+        torch.cuda.synchronize()
+        xs = f32(xx)
+        lse64, _, ids, lps = oracle.candidates(xs, Kc)
+        g_ids = tree.cand_id.cpu().numpy().reshape(batch * L, Kc)
+        g_lse = tree.lse.cpu().numpy().reshape(batch * L)
+        assert np.array_equal(g_ids, ids), dtype  # -inf ties too: smallest ids first
+        assert np.max(np.abs(g_lse - lse64)) < TOL, dtype
+        g_lp = tree.cand_lp.cpu().numpy().reshape(batch * L, Kc)
+        finite = np.isfinite(lps)
+        assert np.array_equal(g_lp[~finite], lps[~finite]), dtype
+        assert np.max(np.abs(g_lp[finite] - lps[finite])) < TOL, dtype
+        assert int(tree.status.abs().sum()) == 0
 
 
 # ---------------------------------------------------------------------------
