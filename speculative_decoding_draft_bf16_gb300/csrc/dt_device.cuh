@@ -283,6 +283,11 @@ DT_DI unsigned long long dt_f2_mul(unsigned long long a, unsigned long long b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+DT_DI unsigned long long dt_f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
 DT_DI unsigned long long dt_f2_add(unsigned long long a, unsigned long long b) {
     unsigned long long r;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -390,6 +395,18 @@ DT_DI const T* dt_stage_row(const T* row, int lo, int hi, unsigned char* sbase, 
     for (int e = e_in_hi + threadIdx.x; e < n; e += blockDim.x) s[e] = row[lo + e];
     *bulk_bytes = bytes;
     return s;
+}
+
+// Per-thread asynchronous 16-byte copies global -> shared (L2 only, not L1),
+// grouped: commit closes a group; wait<N> returns once at most N of this
+// thread's groups are still in flight.
+DT_DI void dt_cp_async16(void* sdst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dt_smem_addr(sdst)), "l"(gsrc) : "memory");
+}
+DT_DI void dt_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+DT_DI void dt_cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Chunk staging in two steps, for prefetching.  start(): one thread issues the

@@ -5,11 +5,12 @@
 //
 // With enough rows (request b, position l) to fill the GPU, a whole row per
 // CTA needs no cross-CTA exchange at all:
-//   pass 1  streams the row from HBM with 16-byte loads, four in flight per
-//           thread; each thread keeps a running maximum and sum exp(x - max)
-//           (rescaled whenever the maximum grows) and, per load slot u, the
-//           maximum of the vectors it loaded in that slot: 4 x 512 = 2048
-//           maxima of distinct elements;
+//   pass 1  streams the row from HBM: each thread copies its 16-byte
+//           vectors (every NT-th) asynchronously into its own ring of RING
+//           shared-memory slots, RING - 1 copies in flight, and keeps a running
+//           maximum and sum exp(x - max) (rescaled whenever the maximum grows)
+//           and the maximum of its vectors m = u (mod 4) for u = 0..3 -- 4 x 512
+//           = 2048 maxima of distinct elements;
 //   the CTA merges the (max, sum) pairs into the row's log-normaliser and
 //   takes the Kc-th largest slot maximum (256-bin histogram of order keys
 //   below the row maximum) as a lower bound for the row's Kc-th largest logit;
@@ -29,7 +30,8 @@ namespace {
 
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
-constexpr int UNR = 4;      // 16-byte loads in flight per thread, and its maximum slots
+constexpr int UNR = 4;      // maximum slots per thread; loads in flight per thread in pass 2
+constexpr int RING = 8;     // per-thread ring of 16-byte vectors in pass 1
 constexpr int CAP = 2048;   // candidates of a row
 
 struct Kn1bMisc {
@@ -45,13 +47,16 @@ struct Kn1bMisc {
 };
 
 // Dynamic shared memory: [misc 1 KB][hist 1 KB][rank scratch 4 KB][cand CAP*8]
-// [work CAP*8].  `work` holds, in turn, the list of slots to re-read (pass 2),
-// the fallback's per-warp histograms (NW KB), and the rank buckets.
+// [work CAP*8][ring RING*NT*16].  `work` holds, in turn, the list of slots to
+// re-read (pass 2), the fallback's per-warp histograms (NW KB), and the rank
+// buckets.  Ring slot k of thread t sits at (k * NT + t) * 16 bytes, so a
+// warp's 16-byte reads of one slot are conflict-free.
 constexpr size_t OFF_HIST = 1024;
 constexpr size_t OFF_RS = OFF_HIST + 1024;
 constexpr size_t OFF_CAND = OFF_RS + 4096;
 constexpr size_t OFF_WORK = OFF_CAND + (size_t)CAP * 8;
-constexpr size_t SMEM = OFF_WORK + (size_t)CAP * 8;
+constexpr size_t OFF_RING = OFF_WORK + (size_t)CAP * 8;
+constexpr size_t SMEM = OFF_RING + (size_t)RING * NT * 16;
 static_assert(sizeof(Kn1bMisc) <= OFF_HIST, "misc block overflows its slot");
 static_assert(sizeof(DtRankScratch) <= 4096, "rank scratch overflows its slot");
 static_assert((size_t)CAP * 8 >= (size_t)NW * 1024, "per-warp histograms must fit the work area");
@@ -63,8 +68,11 @@ DT_DI uint4 ldv(const T* row, int v) {
 }
 
 // Folds a vector (values x, maximum vm) into a running (max M, sum S of
-// exp(x - M)).  x - M is rounded before the product with log2(e), so an
-// element equal to M adds exactly 1 at any magnitude.
+// exp(x - M)).  For |M| < 64 each term is exp2(x * log2e - c) with c = M *
+// log2e rounded, one fused multiply-add: c's rounding error (<= 2^-18) is a
+// factor common to all terms, shifting the log-normaliser by < 3e-6.  Larger
+// maxima round x - M first, so that an element equal to M adds exactly 1 at
+// any magnitude.
 template <int EPV>
 DT_DI void online_add(const float (&x)[EPV], float vm, float& M, float& S) {
     const float NEG_INF = -__int_as_float(0x7F800000);
@@ -74,6 +82,22 @@ DT_DI void online_add(const float (&x)[EPV], float vm, float& M, float& S) {
         M = vm;
     }
     if (M == NEG_INF) return;  // every element so far is -inf
+    if (fabsf(M) < 64.f) {
+        // two lanes per packed f32x2 instruction
+        const float c = __fmul_rn(M, log2e);
+        const unsigned long long l2 = dt_f2_pack(log2e, log2e), c2 = dt_f2_pack(-c, -c);
+        unsigned long long acc = dt_f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < EPV; s += 2) {
+            float d0, d1;
+            dt_f2_unpack(dt_f2_fma(dt_f2_pack(x[s], x[s + 1]), l2, c2), d0, d1);
+            acc = dt_f2_add(acc, dt_f2_pack(dt_ex2_approx(d0), dt_ex2_approx(d1)));
+        }
+        float a0, a1;
+        dt_f2_unpack(acc, a0, a1);
+        S = __fadd_rn(S, __fadd_rn(a0, a1));
+        return;
+    }
     float e[EPV];
 #pragma unroll
     for (int s = 0; s < EPV; ++s) e[s] = dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], M), log2e));
@@ -239,23 +263,47 @@ __global__ void __launch_bounds__(NT, 2) kn1b_kernel(const T* __restrict__ logit
         float gm[UNR];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) gm[u] = NEG_INF;
-        uint32_t gv = 0;  // bit u: slot u holds at least one element
-        for (int v0 = tid; v0 < nfull; v0 += UNR * NT) {
-            uint4 q[UNR];
+        // this thread's 16-byte vectors: m-th at vector index tid + m * NT
+        const int nmine = nfull > tid ? (nfull - tid + NT - 1) / NT : 0;
+        uint32_t gv = nmine >= UNR ? (1u << UNR) - 1 : (1u << nmine) - 1;  // bit u: slot u holds an element
+        {
+            // copies go in groups of two vectors, PRE groups ahead of use
+            constexpr int G = 2, PRE = RING / G - 1;
+            uint4* ring = (uint4*)(smem + OFF_RING) + tid;  // slot k at ring[k * NT]
+            const uint4* src = reinterpret_cast<const uint4*>(rp) + tid;
 #pragma unroll
-            for (int u = 0; u < UNR; ++u)
-                if (v0 + u * NT < nfull) q[u] = ldv(rp, v0 + u * NT);
+            for (int k = 0; k < PRE * G; ++k) {
+                if (k < nmine) dt_cp_async16(ring + k * NT, src + (size_t)k * NT);
+                if (k % G == G - 1) dt_cp_commit();
+            }
+            for (int m0 = 0; m0 < nmine; m0 += UNR) {
+                const int rbase = m0 % RING;  // 0 or UNR
 #pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                if (v0 + u * NT < nfull) {
-                    const float vm = dt_vec_max<T>(q[u]);
-                    gm[u] = fmaxf(gm[u], vm);
-                    gv |= 1u << u;
-                    float x[EPV];
-                    dt_vec_vals<T>(q[u], x);
-                    online_add<EPV>(x, vm, M, S);
+                for (int h = 0; h < UNR / G; ++h) {
+                    if (m0 + h * G < nmine) {
+                        const int mi = m0 + (h + PRE) * G;  // first vector of the group to start
+#pragma unroll
+                        for (int j = 0; j < G; ++j)
+                            if (mi + j < nmine)
+                                dt_cp_async16(ring + ((rbase + (h + PRE) * G + j) % RING) * NT, src + (size_t)(mi + j) * NT);
+                        dt_cp_commit();
+                        dt_cp_wait<PRE>();  // this group has landed
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            const int u = h * G + j;
+                            if (m0 + u < nmine) {
+                                const uint4 q = ring[(rbase + u) * NT];
+                                const float vm = dt_vec_max<T>(q);
+                                gm[u] = fmaxf(gm[u], vm);
+                                float x[EPV];
+                                dt_vec_vals<T>(q, x);
+                                online_add<EPV>(x, vm, M, S);
+                            }
+                        }
+                    }
                 }
             }
+            dt_cp_wait<0>();
         }
         // the rest -- a ragged last vector, or every vector of a row that is not
         // 16-byte aligned -- with element loads (-inf fill adds nothing)
@@ -330,26 +378,33 @@ __global__ void __launch_bounds__(NT, 2) kn1b_kernel(const T* __restrict__ logit
                 slots[atomicAdd(&misc->nslot, 1)] = tid + u * NT;  // first vector of the slot
         __syncthreads();
         {
-            // item i: vector k of listed slot j (slot vectors are UNR * NT apart)
+            // a slot's vectors are UNR * NT apart, per of them; a warp takes spw
+            // listed slots at a time, lane = (slot dj, vector kc + k), kl
+            // vectors of a slot per pass
             const int per = (nfull + UNR * NT - 1) / (UNR * NT);
-            const int items = misc->nslot * per;
-            for (int i0 = tid; i0 < items; i0 += UNR * NT) {
-                uint4 q[UNR];
-                int vv[UNR];
+            const int kl = per < 32 ? per : 32;
+            const int spw = kl > 0 ? 32 / kl : 1;
+            const int dj = kl > 0 ? lane / kl : 0, k = kl > 0 ? lane % kl : 0;
+            const int nslot = misc->nslot;
+            for (int kc = 0; kc < per; kc += kl) {
+                for (int j0 = wid * spw; j0 < nslot; j0 += 2 * NW * spw) {
+                    uint4 q[2];
+                    int vv[2];
 #pragma unroll
-                for (int u = 0; u < UNR; ++u) {
-                    const int i = i0 + u * NT;
-                    vv[u] = i < items ? slots[i / per] + (i % per) * (UNR * NT) : nfull;
-                    if (vv[u] < nfull) q[u] = ldv(rp, vv[u]);
-                }
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = j0 + h * NW * spw + dj;
+                        vv[h] = (dj < spw && j < nslot && kc + k < per) ? slots[j] + (kc + k) * (UNR * NT) : nfull;
+                        if (vv[h] < nfull) q[h] = ldv(rp, vv[h]);
+                    }
 #pragma unroll
-                for (int u = 0; u < UNR; ++u) {
-                    if (vv[u] < nfull && dt_vec_max<T>(q[u]) >= bound) {
-                        float x[EPV];
-                        dt_vec_vals<T>(q[u], x);
+                    for (int h = 0; h < 2; ++h) {
+                        if (vv[h] < nfull && dt_vec_max<T>(q[h]) >= bound) {
+                            float x[EPV];
+                            dt_vec_vals<T>(q[h], x);
 #pragma unroll
-                        for (int s = 0; s < EPV; ++s)
-                            if (x[s] >= bound) keep(x[s], vv[u] * EPV + s);
+                            for (int s = 0; s < EPV; ++s)
+                                if (x[s] >= bound) keep(x[s], vv[h] * EPV + s);
+                        }
                     }
                 }
             }

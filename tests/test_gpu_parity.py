@@ -126,6 +126,8 @@ CAND_CASES = [
     (20, 16, 151936, "bf16", 60, 3.0, 0.5),  # many rows: persistent clusters prefetching their next row
     (8, 16, 151936, "bf16", 1024, 3.0, 0.7),  # many rows, largest list: sorted ranking
     (6, 16, 151936, "f32", 256, 3.0, 0.7),    # many fp32 rows
+    (4, 16, 300000, "f32", 64, 3.0, 0.7),     # long fp32 rows: > 32 vectors per maximum slot
+    (4, 16, 10001, "bf16", 32, 3.0, 0.7),     # many rows, odd V: rows not 16-byte aligned
 ]
 
 
