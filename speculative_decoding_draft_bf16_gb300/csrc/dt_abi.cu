@@ -132,7 +132,7 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
         if (p->R < 0 || p->R > 1024) return DT_ERR_INVALID_ARG;
         if (p->R > 0 && (!p->U || !p->Vt)) return DT_ERR_INVALID_ARG;
         if (p->R > 0 && dt_kn3_table_smem_bytes(p->K, p->R) > kSmemMax) return DT_ERR_UNSUPPORTED;
-        if (dt_kn3_select_smem_bytes(p->L, p->K, p->W) > kSmemMax) return DT_ERR_UNSUPPORTED;
+        if (dt_kn3_select_smem_bytes(p->L, p->K, p->W, p->R > 0 && p->U) > kSmemMax) return DT_ERR_UNSUPPORTED;
     }
     if (t->Kc != kc_of(p)) return DT_ERR_INVALID_ARG;
     if (t->L != p->L) return DT_ERR_INVALID_ARG;

@@ -198,6 +198,64 @@ DT_DI void dt_warp_sort_u64(unsigned long long* a, int n, bool desc) {
     __syncthreads();
 }
 
+// Register-level warp sorts of one 64-bit key per lane (bitonic network on
+// shuffles, no block barrier).  dt_warp_sort_reg: any order in, sorted out
+// (descending when desc); dt_warp_merge_reg: a bitonic sequence in, sorted out.
+DT_DI unsigned long long dt_warp_sort_reg(unsigned long long x, bool desc) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+            const bool take_max = (((lane & j) == 0) == (((lane & k) == 0) == desc));
+            x = take_max ? (x > y ? x : y) : (x < y ? x : y);
+        }
+    }
+    return x;
+}
+DT_DI unsigned long long dt_warp_merge_reg(unsigned long long x, bool desc) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+        const bool take_max = (((lane & j) == 0) == desc);
+        x = take_max ? (x > y ? x : y) : (x < y ? x : y);
+    }
+    return x;
+}
+// a, b: descending warp lists (one key per lane).  Returns the 32 largest of
+// their union, descending: the lane-wise maximum of a and reversed b is a
+// bitonic sequence holding exactly those.
+DT_DI unsigned long long dt_warp_top32_merge(unsigned long long a, unsigned long long b) {
+    const unsigned long long r = __shfl_sync(0xffffffffu, b, 31 - (threadIdx.x & 31));
+    return dt_warp_merge_reg(a > r ? a : r, true);
+}
+
+// The 32 largest of m keys key_of(0..m-1) (all nonzero), descending, one per
+// lane of warp 0 (0 past the m-th); other warps get no result.  Each warp
+// keeps a running top-32 over chunks of 32 keys, then the warps' lists merge
+// pairwise in a tree through `scratch` (NT 64-bit words).  Must be called by
+// all threads; contains log2(NT/32) __syncthreads and ends with one.
+template <int NT, typename KeyFn>
+DT_DI unsigned long long dt_block_top32(int m, KeyFn key_of, unsigned long long* scratch) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    constexpr int NW = NT / 32;
+    unsigned long long R = 0ull;
+    for (int base = wid * 32; base < m; base += NT) {
+        const unsigned long long x = (base + lane < m) ? key_of(base + lane) : 0ull;
+        R = dt_warp_top32_merge(R, dt_warp_sort_reg(x, true));
+    }
+#pragma unroll
+    for (int lev = 1; lev < NW; lev <<= 1) {
+        if ((wid & (2 * lev - 1)) == lev) scratch[wid * 32 + lane] = R;
+        __syncthreads();
+        if ((wid & (2 * lev - 1)) == 0 && wid + lev < NW) R = dt_warp_top32_merge(R, scratch[(wid + lev) * 32 + lane]);
+    }
+    __syncthreads();
+    return R;
+}
+
 DT_DI int dt_pow2_ceil(int n) {
     int p = 1;
     while (p < n) p <<= 1;

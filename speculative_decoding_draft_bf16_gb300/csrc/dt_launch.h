@@ -78,7 +78,7 @@ cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float*
 
 // DARTree Markov table + selection (kn3_dartree.cu).
 size_t dt_kn3_table_smem_bytes(int K, int R);
-size_t dt_kn3_select_smem_bytes(int L, int K, int W);
+size_t dt_kn3_select_smem_bytes(int L, int K, int W, int use_table);
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* lse, float* table, int32_t* tok, int32_t* parent,

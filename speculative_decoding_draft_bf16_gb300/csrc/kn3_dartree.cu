@@ -85,13 +85,28 @@ struct Kn3Smem {
     int* order;   // [W*L] output order / heap
     int* cstart;  // [W*L + 1] children CSR (fallback)
     int* clist;   // [W*L]
+    unsigned long long* scratch;  // [NT] warp-list merges (W <= 32)
+    float* lps;   // [L*K] the request's candidate log-probs
+    float* tabs;  // [L*K*K] the request's Markov table, when it fits (else nullptr)
 };
+
+// Markov table entries staged in shared memory per request, at most.
+constexpr int kTabStage = 16384;
 
 DT_DI size_t kn3_cap(int W, int K) { return (size_t)dt_pow2_ceil(W * K > W ? W * K : W); }
 
-DT_DI Kn3Smem kn3_carve(unsigned char* p, int L, int K, int W) {
+DT_DI Kn3Smem kn3_carve(unsigned char* p, int L, int K, int W, bool stage_tab) {
     Kn3Smem m;
     const int NS = W * L;
+    m.scratch = (unsigned long long*)p;
+    p += (size_t)NT * 8;
+    m.lps = (float*)p;
+    p += (size_t)((L * K + 3) & ~3) * 4;
+    m.tabs = nullptr;
+    if (stage_tab) {
+        m.tabs = (float*)p;
+        p += (size_t)L * K * K * 4;
+    }
     m.cand = (unsigned long long*)p;
     p += kn3_cap(W, K) * 8;
     m.lp = (float*)p; p += (size_t)((K + 3) & ~3) * 4;
@@ -122,60 +137,94 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
     __shared__ int lay_start[DT_MAX_L + 2];
     __shared__ int sh_bad, sh_viol;
     const int b = blockIdx.x, tid = threadIdx.x;
-    Kn3Smem S = kn3_carve(smem, L, K, W);
+    const bool stage_tab = use_table && L * K * K <= kTabStage;
+    Kn3Smem S = kn3_carve(smem, L, K, W, stage_tab);
     dt_pdl_trigger();
     dt_pdl_wait();
-    const float* lpb = cand_lp + (size_t)b * L * K;
     const int rt = root_tok ? root_tok[b] : -1;
     const bool term1 = use_table && rt >= 0 && rt < V;
+    // the request's log-probs (and Markov table, when small) into shared memory
+    for (int i = tid; i < L * K; i += NT) S.lps[i] = cand_lp[(size_t)b * L * K + i];
+    if (stage_tab) {
+        const float* tb = table + (size_t)b * L * K * K;
+        const int n = L * K * K;
+        const int n4 = (((uintptr_t)tb & 15u) == 0) ? n / 4 : 0;  // 16-byte loads where aligned
+        for (int i = tid; i < n4; i += NT) ((float4*)S.tabs)[i] = ((const float4*)tb)[i];
+        for (int i = n4 * 4 + tid; i < n; i += NT) S.tabs[i] = tb[i];
+    }
+    __syncthreads();
 
     int nS = 0;      // supertree nodes so far
     int nprev = 1;   // size of the previous layer (the root)
     if (tid == 0) { lay_start[0] = 0; sh_bad = 0; sh_viol = 0; }
     for (int d = 1; d <= L; ++d) {
-        __syncthreads();
-        for (int r = tid; r < K; r += NT) S.lp[r] = lpb[(size_t)(d - 1) * K + r];
-        __syncthreads();
+        const float* lpd = S.lps + (size_t)(d - 1) * K;
         const bool term = use_table && (d > 1 || term1);
-        const float* tab = table ? table + ((size_t)b * L + d - 1) * K * K : nullptr;
+        const float* tab = !term ? nullptr
+                                 : (stage_tab ? S.tabs + (size_t)(d - 1) * K * K
+                                              : table + ((size_t)b * L + d - 1) * K * K);
         const int m = nprev * K;
-        const int P2 = dt_pow2_ceil(m);
-        for (int idx = tid; idx < P2; idx += NT) {
-            unsigned long long key = 0ull;
-            if (idx < m) {
-                const int j = idx / K, r = idx % K;
-                const int p = (d == 1) ? -1 : S.lexl[j];
-                const float sp = (d == 1) ? 0.f : S.s[p];
-                float t = S.lp[r];
-                if (term) t = __fadd_rn(t, tab[(size_t)((d == 1) ? 0 : S.rank[p]) * K + r]);
-                const float sc = __fadd_rn(__fadd_rn(sp, t), beta);
-                const uint32_t lx = ((uint32_t)j << 16) | (uint32_t)r;
-                key = ((unsigned long long)dt_fkey(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - lx);
-            }
-            S.cand[idx] = key;
-        }
-        __syncthreads();
-        dt_bitonic_u64<NT>(S.cand, P2, true);
+        // key of candidate idx = (parent j in lexicographic order, child rank r)
+        auto key_of = [&](int idx) {
+            const int j = idx / K, r = idx % K;
+            const int p = (d == 1) ? -1 : S.lexl[j];
+            const float sp = (d == 1) ? 0.f : S.s[p];
+            float t = lpd[r];
+            if (term) t = __fadd_rn(t, tab[(size_t)((d == 1) ? 0 : S.rank[p]) * K + r]);
+            const float sc = __fadd_rn(__fadd_rn(sp, t), beta);
+            const uint32_t lx = ((uint32_t)j << 16) | (uint32_t)r;
+            return ((unsigned long long)dt_fkey(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - lx);
+        };
         const int keep = min(W, m);
-        for (int q = tid; q < keep; q += NT) {
-            const unsigned long long y = S.cand[q];
-            const uint32_t lx = 0xFFFFFFFFu - (uint32_t)y;
-            const int j = (int)(lx >> 16), r = (int)(lx & 0xFFFFu);
-            const int x = nS + q;
-            S.s[x] = dt_fkey_val((uint32_t)(y >> 32));
-            S.dep[x] = d;
-            S.par[x] = (d == 1) ? -1 : S.lexl[j];
-            S.rank[x] = r;
-            S.lex[x] = lx;
+        if (W <= 32) {
+            // top-W: warp sorts merged in a tree; the layer's lexicographic
+            // order by warp 0 alone
+            const unsigned long long y = dt_block_top32<NT>(m, key_of, S.scratch);
+            if (tid < 32) {
+                uint32_t lx = 0;
+                int par = -1;
+                if (tid < keep) {
+                    lx = 0xFFFFFFFFu - (uint32_t)y;
+                    const int j = (int)(lx >> 16), r = (int)(lx & 0xFFFFu);
+                    const int x = nS + tid;
+                    par = (d == 1) ? -1 : S.lexl[j];
+                    S.s[x] = dt_fkey_val((uint32_t)(y >> 32));
+                    S.dep[x] = d;
+                    S.par[x] = par;
+                    S.rank[x] = r;
+                    S.lex[x] = lx;
+                }
+                __syncwarp();  // every lane has read lexl before it is rewritten
+                const unsigned long long k2 =
+                    dt_warp_sort_reg(tid < keep ? (((unsigned long long)lx << 32) | (unsigned)(nS + tid)) : ~0ull, false);
+                if (tid < keep) S.lexl[tid] = (int)(k2 & 0xFFFFFFFFull);
+            }
+        } else {
+            const int P2 = dt_pow2_ceil(m);
+            for (int idx = tid; idx < P2; idx += NT) S.cand[idx] = idx < m ? key_of(idx) : 0ull;
+            __syncthreads();
+            dt_bitonic_u64<NT>(S.cand, P2, true);
+            for (int q = tid; q < keep; q += NT) {
+                const unsigned long long y = S.cand[q];
+                const uint32_t lx = 0xFFFFFFFFu - (uint32_t)y;
+                const int j = (int)(lx >> 16), r = (int)(lx & 0xFFFFu);
+                const int x = nS + q;
+                S.s[x] = dt_fkey_val((uint32_t)(y >> 32));
+                S.dep[x] = d;
+                S.par[x] = (d == 1) ? -1 : S.lexl[j];
+                S.rank[x] = r;
+                S.lex[x] = lx;
+            }
+            __syncthreads();
+            // previous-layer order for the next depth: this layer by lexicographic key
+            const int Q2 = dt_pow2_ceil(keep);
+            for (int q = tid; q < Q2; q += NT)
+                S.cand[q] = (q < keep) ? (((unsigned long long)S.lex[nS + q] << 32) | (unsigned)(nS + q)) : ~0ull;
+            __syncthreads();
+            dt_bitonic_u64<NT>(S.cand, Q2, false);
+            for (int q = tid; q < keep; q += NT) S.lexl[q] = (int)(S.cand[q] & 0xFFFFFFFFull);
         }
         __syncthreads();
-        // previous-layer order for the next depth: this layer by lexicographic key
-        const int Q2 = dt_pow2_ceil(keep);
-        for (int q = tid; q < Q2; q += NT)
-            S.cand[q] = (q < keep) ? (((unsigned long long)S.lex[nS + q] << 32) | (unsigned)(nS + q)) : ~0ull;
-        __syncthreads();
-        dt_bitonic_u64<NT>(S.cand, Q2, false);
-        for (int q = tid; q < keep; q += NT) S.lexl[q] = (int)(S.cand[q] & 0xFFFFFFFFull);
         nS += keep;
         nprev = keep;
         if (tid == 0) lay_start[d] = nS;
@@ -306,11 +355,13 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
 
 size_t dt_kn3_table_smem_bytes(int K, int R) { return (size_t)2 * K * (R | 1) * 4 + 16; }
 
-size_t dt_kn3_select_smem_bytes(int L, int K, int W) {
+size_t dt_kn3_select_smem_bytes(int L, int K, int W, int use_table) {
     int cap = 1;
     while (cap < W * K || cap < W) cap <<= 1;
     const size_t NS = (size_t)W * L;
-    return (size_t)cap * 8 + (size_t)((K + 3) & ~3) * 4 + NS * 4 * 8 + (NS + 1) * 4 + (size_t)W * 4 + 16;
+    const bool stage_tab = use_table && L * K * K <= kTabStage;
+    return (size_t)NT * 8 + (size_t)((L * K + 3) & ~3) * 4 + (stage_tab ? (size_t)L * K * K * 4 : 0) +
+           (size_t)cap * 8 + (size_t)((K + 3) & ~3) * 4 + NS * 4 * 8 + (NS + 1) * 4 + (size_t)W * 4 + 16;
 }
 
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
@@ -330,7 +381,7 @@ cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float be
             cudaSuccess)
             return e;
     }
-    const size_t sm = dt_kn3_select_smem_bytes(L, K, W);
+    const size_t sm = dt_kn3_select_smem_bytes(L, K, W, use_table);
     if ((e = cudaFuncSetAttribute(kn3_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) !=
         cudaSuccess)
         return e;

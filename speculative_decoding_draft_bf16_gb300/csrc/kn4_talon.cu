@@ -25,10 +25,8 @@
 namespace {
 
 constexpr int NT = 512;
-constexpr int CAP = 4096;
 
 struct Kn4Smem {
-    unsigned long long* cand;  // [CAP]
     float* lp;                 // [Kc]
     float* s;                  // [N]
     int* dep;
@@ -41,8 +39,6 @@ struct Kn4Smem {
 
 DT_DI Kn4Smem kn4_carve(unsigned char* p, int Kc, int N) {
     Kn4Smem m;
-    m.cand = (unsigned long long*)p;
-    p += (size_t)CAP * 8;
     m.lp = (float*)p; p += (size_t)((Kc + 3) & ~3) * 4;
     m.s = (float*)p; p += (size_t)N * 4;
     m.dep = (int*)p; p += (size_t)N * 4;
@@ -86,7 +82,6 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int red[NT / 32];
     __shared__ float redf[NT / 32];
-    __shared__ int sh_jhi;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     Kn4Smem S = kn4_carve(smem, Kc, N);
     dt_pdl_trigger();
@@ -139,66 +134,71 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
             nT += m;
             continue;
         }
-        // overflow: keep the best `room` of the pool, then stop
+        // overflow: keep the best `room` of the pool, then stop.  Every
+        // parent's passing children are a rank prefix, so the number of pool
+        // members scoring >= t is a sum of per-parent binary searches; a
+        // binary search over the order keys of t in [thr, m_d] finds the
+        // R-th best score t*.  The layer takes every member above t* and the
+        // first ties at t* in lexicographic order (parent, then rank).
         const int R = room;
-        int nR = 0;
-        int j_lo = 0;
-        while (j_lo < nP) {
+        auto count_all = [&](float t) {
+            int c = 0;
+            for (int j = tid; j < nP; j += NT) c += count_pass(S.s[lay_lo + j], S.lp, Kc, t);
+            c = dt_warp_sum_i(c);
+            if (lane == 0) red[wid] = c;
             __syncthreads();
-            // prune by the running cutoff once the running list is full
-            float thr2 = thr;
-            if (nR == R) thr2 = fmaxf(thr, dt_fkey_val((uint32_t)(S.cand[R - 1] >> 32)));
-            for (int j = tid; j < nP; j += NT)
-                S.pn[j] = (j < j_lo) ? 0 : count_pass(S.s[lay_lo + j], S.lp, Kc, thr2);
+            int tot = 0;
+#pragma unroll
+            for (int w = 0; w < NT / 32; ++w) tot += red[w];
             __syncthreads();
-            dt_block_scan_array<NT>(S.pn, S.pn, nP, red);
-            if (tid == 0) sh_jhi = j_lo + 1;
-            __syncthreads();
-            for (int j = j_lo + 1 + tid; j <= nP; j += NT)
-                if (S.pn[j] <= CAP - R) atomicMax(&sh_jhi, j);
-            __syncthreads();
-            const int j_hi = sh_jhi;
-            const int mg = S.pn[j_hi];
-            const int tot = nR + mg;
-            const int P2 = dt_pow2_ceil(R + mg);
-            for (int g = tid; g < mg; g += NT) {
-                const int j = find_parent(S.pn, j_lo, j_hi, g);
-                const int w = g - S.pn[j];
-                const float sc = __fadd_rn(S.s[lay_lo + j], S.lp[w]);
-                const uint32_t lx = ((uint32_t)j << 16) | (uint32_t)w;
-                S.cand[R + g] = ((unsigned long long)dt_fkey(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - lx);
-            }
-            for (int i = nR + tid; i < R; i += NT) S.cand[i] = 0ull;
-            for (int i = R + mg + tid; i < P2; i += NT) S.cand[i] = 0ull;
-            __syncthreads();
-            dt_bitonic_u64<NT>(S.cand, P2, true);
-            nR = min(R, tot);
-            j_lo = j_hi;
+            return tot;
+        };
+        uint32_t klo = dt_fkey(thr), khi = dt_fkey(m_d) + 1u;  // count(klo) >= R > count(khi)
+        while (khi - klo > 1u) {
+            const uint32_t mid = klo + ((khi - klo) >> 1);
+            if (count_all(dt_fkey_val(mid)) >= R) klo = mid;
+            else khi = mid;
         }
-        // selected keys -> lexicographic order -> nodes
-        __syncthreads();
-        const int Q2 = dt_pow2_ceil(nR);
-        for (int q = tid; q < Q2; q += NT) {
-            if (q < nR) {
-                const unsigned long long y = S.cand[q];
-                const uint32_t lx = 0xFFFFFFFFu - (uint32_t)y;
-                S.cand[q] = ((unsigned long long)lx << 32) | (y >> 32);
-            } else {
-                S.cand[q] = ~0ull;
-            }
+        const float t_eq = dt_fkey_val(klo), t_gt = dt_fkey_val(klo + 1u);
+        // per parent: a = children above t*, ties = children at t*
+        for (int j = tid; j < nP; j += NT) {
+            const int a_j = count_pass(S.s[lay_lo + j], S.lp, Kc, t_gt);
+            S.pn[j] = count_pass(S.s[lay_lo + j], S.lp, Kc, t_eq) - a_j;
+            S.ord[j] = a_j;
         }
         __syncthreads();
-        dt_bitonic_u64<NT>(S.cand, Q2, false);
-        for (int q = tid; q < nR; q += NT) {
-            const unsigned long long y = S.cand[q];
-            const uint32_t lx = (uint32_t)(y >> 32);
-            const int j = (int)(lx >> 16), w = (int)(lx & 0xFFFFu);
-            const int x = nT + q;
-            S.s[x] = dt_fkey_val((uint32_t)(y & 0xFFFFFFFFull));
+        dt_block_scan_array<NT>(S.pn, S.pn, nP, red);  // exclusive prefix of the ties
+        {
+            // ties still needed after every member above t*
+            int c = 0;
+            for (int j = tid; j < nP; j += NT) c += S.ord[j];
+            c = dt_warp_sum_i(c);
+            if (lane == 0) red[wid] = c;
+            __syncthreads();
+            int above = 0;
+#pragma unroll
+            for (int w = 0; w < NT / 32; ++w) above += red[w];
+            const int need = R - above;
+            __syncthreads();
+            // parent j takes its a_j children above t* plus its share of ties
+            for (int j = tid; j < nP; j += NT) {
+                const int t0 = S.pn[j], tj = S.pn[j + 1] - t0;
+                const int take_t = max(0, min(tj, need - t0));
+                S.ord[j] += take_t;
+            }
+            __syncthreads();
+        }
+        dt_block_scan_array<NT>(S.ord, S.pn, nP, red);  // prefix of the per-parent takes
+        const int nR = S.pn[nP];
+        for (int g = tid; g < nR; g += NT) {
+            const int j = find_parent(S.pn, 0, nP, g);
+            const int w = g - S.pn[j];
+            const int x = nT + g;
+            S.s[x] = __fadd_rn(S.s[lay_lo + j], S.lp[w]);
             S.dep[x] = d;
             S.par[x] = lay_lo + j;
             S.rank[x] = w;
-            S.lex[x] = lx;
+            S.lex[x] = ((uint32_t)j << 16) | (uint32_t)w;
         }
         nT += nR;
         break;
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
 size_t dt_kn4_smem_bytes(int Kc, int N) {
     int q2 = 1;
     while (q2 < N) q2 <<= 1;
-    return (size_t)CAP * 8 + (size_t)((Kc + 3) & ~3) * 4 + (size_t)N * 20 + (size_t)(N + 1) * 4 + (size_t)q2 * 4 + 16;
+    return (size_t)((Kc + 3) & ~3) * 4 + (size_t)N * 20 + (size_t)(N + 1) * 4 + (size_t)q2 * 4 + 16;
 }
 
 cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,

@@ -583,6 +583,15 @@ def test_talon_parity_small(N, mu, scale):
     talon_case(x, N, mu)
 
 
+@pytest.mark.parametrize("N", [30, 257])
+def test_talon_layer_overflow_all_ties(N):
+    # equal logits: every child of a layer scores the same, so the budget cut
+    # falls inside one run of ties, broken by the lexicographic order
+    x = torch.full((2, 6, 500), 0.5).to(torch.bfloat16)
+    x[1, :, 7] = 1.0  # second request: one favoured token per position
+    talon_case(x, N, 0.5, talon_k=4)
+
+
 @pytest.mark.parametrize("N", [60, 1024])
 def test_talon_full_size(N):
     wl = wk.talon_gated(N)
