@@ -37,9 +37,27 @@ METRIC = "draft trees built+verified/sec and logit-read HBM GB/s (% of GB300 pea
 L2_BYTES = 129 * 1024 * 1024
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the stage-1
-# kernel, keyed by the sha1 of the kernel source the capture was taken on; a
-# changed kernel reports null until it is captured again.
-KN1_TRAFFIC = {}
+# kernel, keyed by (kernel, workload, sha1 of the kernel's sources when the
+# capture was taken); a changed kernel reports null until it is captured again.
+KN1_TRAFFIC = {
+    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', 'e191525f2920d993c087cc777a01718198052a7c'): 4932000,
+    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 38962500,
+    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 78785500,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 315424500,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 346304500,
+}
+STAGE1_SOURCES = {
+    "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),
+    "kn1b_kernel": ("kn1b_rows.cu", "kn1_common.cuh", "dt_device.cuh"),
+}
+
+
+def stage1_source_hash(kernel):
+    h = hashlib.sha1()
+    for f in STAGE1_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "speculative_decoding_draft_bf16_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def workloads():
@@ -327,8 +345,11 @@ def run_ours(args, wl, rank, world, local):
     except OSError:
         pass
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    src = open(os.path.join(ROOT, "speculative_decoding_draft_bf16_gb300", "csrc", "kn1_candidates.cu"), "rb").read()
-    traffic = KN1_TRAFFIC.get(hashlib.sha1(src).hexdigest())
+    plan_kind, plan_cluster = dtree.stage1_plan(p)
+    kn1_name = "kn1_kernel" if plan_kind == "cluster" else "kn1b_kernel"
+    kn1_desc = ("%s (log-softmax + Top-K, a cluster of %d CTAs per row)" % (kn1_name, plan_cluster)
+                if plan_kind == "cluster" else "%s (log-softmax + Top-K, one CTA per row)" % kn1_name)
+    traffic = KN1_TRAFFIC.get((kn1_name, wl.name, stage1_source_hash(kn1_name)))
     result = {
         "metric": METRIC,
         "value": job_throughput(args.steps, wl.batch, world, ms),
@@ -346,7 +367,7 @@ def run_ours(args, wl, rank, world, local):
                    "K": wl.K, "B": wl.B, "W": wl.W, "beta": wl.beta, "N": wl.N, "temperature": temperature,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d input copies (drafter logits %.0f MB > 2x L2)" % (R, R * draft_bytes / 1e6)},
-        "roofline": {"bound": "hbm", "kernel": "kn1 log-softmax+Top-K", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": kn1_desc, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "algorithmic_bytes_per_launch": draft_bytes},
         "stages_us": stage_us,

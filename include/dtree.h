@@ -145,6 +145,17 @@ size_t dt_workspace_size(const dt_build_params* p, int* ok);
 dt_status dt_candidates(const dt_build_params* p, const void* draft_logits,
                         dt_tree* tree, dt_stream_t stream);
 
+/* Which stage-1 kernel dt_candidates launches for these parameters, without
+ * launching anything (a query of the current device's cluster residency may
+ * run on the first call).  *kernel = DT_STAGE1_CLUSTER: each row is split over
+ * a thread-block cluster of *cluster CTAs (few rows: latency);
+ * DT_STAGE1_ROWS: one CTA per row, *cluster = 1 (many rows, or candidate lists
+ * longer than 512: throughput).  Returns DT_ERR_INVALID_ARG for parameters
+ * dt_candidates would reject on shape (batch, L, V, dtype, Kc). */
+#define DT_STAGE1_CLUSTER 1
+#define DT_STAGE1_ROWS 2
+dt_status dt_stage1_plan(const dt_build_params* p, int32_t* kernel, int32_t* cluster);
+
 /* Stages 2-3: tree selection from the candidate lists already in `tree`
  * (written by dt_candidates, or by the caller), writing node_tok, parent,
  * depth, rank, score, n_nodes and a fresh status word per request.

@@ -26,8 +26,8 @@ int chunk_of(int V, int S, int dtype) {
 }
 
 // Clusters of S CTAs that the device holds at once for stage 1 (kind 1,
-// extra = 4 * Kc + chunk buffers) or the verification walk (kind 6, extra =
-// max_nodes) with these sizes; cached per device.
+// extra = Kc) or the verification walk (kind 6, extra = max_nodes) with these
+// sizes; cached per device.
 int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
     struct Fit {
         int dev, kind, dtype, S, chunk, extra, n;
@@ -46,8 +46,7 @@ int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
         if (f.dev == dev && f.kind == kind && f.dtype == dtype && f.S == S && f.chunk == chunk && f.extra == extra)
             return f.n;
     }
-    const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra >> 2, extra & 3)
-                            : dt_kn6_max_clusters(dtype, S, chunk, extra);
+    const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra) : dt_kn6_max_clusters(dtype, S, chunk, extra);
     if (n > 0 && nfit < 128) fits[nfit++] = Fit{dev, kind, dtype, S, chunk, extra, n};
     return n;
 }
@@ -148,6 +147,32 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
     return DT_OK;
 }
 
+// Stage-1 launch shape: kernel DT_STAGE1_ROWS (one CTA per row) or
+// DT_STAGE1_CLUSTER (a cluster of S CTAs, chunk elements each, per row).
+struct Stage1Plan {
+    int kernel, S, chunk;
+};
+
+dt_status plan_stage1(const dt_build_params* p, Stage1Plan* plan) {
+    const int Kc = kc_of(p);
+    const long long rows = (long long)p->batch * p->L;
+    const int esize = p->dtype == DT_BF16 ? 2 : 4;
+    const int V = p->V, dtype = p->dtype;
+    // enough rows to fill the GPU with whole rows, or long candidate lists:
+    // one CTA per row, no cluster
+    if (rows >= kRowsPerCtaMin || Kc > kRowsPerCtaKc) {
+        *plan = Stage1Plan{DT_STAGE1_ROWS, 1, V};
+        return DT_OK;
+    }
+    const int S = cluster_for(
+        V, rows, dtype, [&](int q) { return dt_kn1_smem_bytes(chunk_of(V, q, dtype), Kc, esize) + 4096 <= kSmemMax; },
+        [&](int q, int chunk) { return max_clusters(1, dtype, q, chunk, Kc); });
+    const int chunk = chunk_of(V, S, dtype);
+    if (dt_kn1_smem_bytes(chunk, Kc, esize) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
+    *plan = Stage1Plan{DT_STAGE1_CLUSTER, S, chunk};
+    return DT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -162,41 +187,34 @@ size_t dt_workspace_size(const dt_build_params* p, int* ok) {
     return 0;
 }
 
+dt_status dt_stage1_plan(const dt_build_params* p, int32_t* kernel, int32_t* cluster) {
+    if (!p || !kernel || !cluster) return DT_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->L < 1 || p->L > DT_MAX_L || p->V < 1 || p->V > DT_MAX_V) return DT_ERR_INVALID_ARG;
+    if (p->dtype != DT_BF16 && p->dtype != DT_F32) return DT_ERR_INVALID_ARG;
+    const int Kc = kc_of(p);
+    if (Kc < 1 || Kc > DT_MAX_KC || Kc > p->V) return DT_ERR_INVALID_ARG;
+    Stage1Plan plan;
+    const dt_status s = plan_stage1(p, &plan);
+    if (s != DT_OK) return s;
+    *kernel = plan.kernel;
+    *cluster = plan.S;
+    return DT_OK;
+}
+
 dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_tree* t, dt_stream_t stream) {
     dt_status s = check_build(p, t);
     if (s != DT_OK) return s;
     if (!draft_logits) return DT_ERR_INVALID_ARG;
-    const int Kc = kc_of(p);
-    const long long rows = (long long)p->batch * p->L;
-    const int esize = p->dtype == DT_BF16 ? 2 : 4;
-    const int V = p->V, dtype = p->dtype;
-    // enough rows to fill the GPU with whole rows, or long candidate lists:
-    // one CTA per row, no cluster
-    if (rows >= kRowsPerCtaMin || Kc > kRowsPerCtaKc) {
-        cudaError_t e = dt_kn1b_launch(draft_logits, dtype, (int)rows, V, Kc, t->lse, t->cand_id, t->cand_lp,
-                                       (cudaStream_t)stream);
-        return cuda_status(e);
-    }
-    const int S = cluster_for(
-        V, rows, dtype,
-        [&](int s) { return dt_kn1_smem_bytes(chunk_of(V, s, dtype), Kc, esize, 1) + 4096 <= kSmemMax; },
-        [&](int s, int chunk) { return max_clusters(1, dtype, s, chunk, 4 * Kc + 1); });
-    const int chunk = chunk_of(V, S, dtype);
-    if (dt_kn1_smem_bytes(chunk, Kc, esize, 1) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
-    // more rows than the device holds clusters at once: persistent clusters,
-    // each prefetching its next row's chunk while it works on the current one
-    int nbuf = 1;
-    long long grid_rows = rows;
-    const int held = max_clusters(1, dtype, S, chunk, 4 * Kc + 1);
-    if (held > 0 && rows > held && dt_kn1_smem_bytes(chunk, Kc, esize, 2) + 4096 <= kSmemMax) {
-        const int held2 = max_clusters(1, dtype, S, chunk, 4 * Kc + 2);
-        if (held2 > 0) {
-            nbuf = 2;
-            grid_rows = held2 < rows ? held2 : rows;
-        }
-    }
-    cudaError_t e = dt_kn1_launch(draft_logits, dtype, (int)rows, (int)grid_rows, V, Kc, S, chunk, nbuf, t->lse,
-                                  t->cand_id, t->cand_lp, (cudaStream_t)stream);
+    Stage1Plan plan;
+    if ((s = plan_stage1(p, &plan)) != DT_OK) return s;
+    const int rows = p->batch * p->L;
+    cudaError_t e;
+    if (plan.kernel == DT_STAGE1_ROWS)
+        e = dt_kn1b_launch(draft_logits, p->dtype, rows, p->V, kc_of(p), t->lse, t->cand_id, t->cand_lp,
+                           (cudaStream_t)stream);
+    else
+        e = dt_kn1_launch(draft_logits, p->dtype, rows, rows, p->V, kc_of(p), plan.S, plan.chunk, t->lse,
+                          t->cand_id, t->cand_lp, (cudaStream_t)stream);
     return cuda_status(e);
 }
 

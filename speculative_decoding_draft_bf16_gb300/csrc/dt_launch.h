@@ -58,12 +58,11 @@ inline int dt_max_active_clusters(K kernel, int cluster_x, int block, size_t sme
 }
 
 // Stage 1 (kn1_candidates.cu).
-// nbuf chunk buffers per CTA (2: each cluster prefetches its next row);
 // grid_rows clusters share the rows round-robin.
-int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc, int nbuf);
-size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize, int nbuf);
+int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc);
+size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize);
 cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int grid_rows, int V, int Kc, int S, int chunk,
-                          int nbuf, float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st);
+                          float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st);
 
 // Stage 1 for many rows, one CTA per row (kn1b_rows.cu).
 size_t dt_kn1b_smem_bytes();

@@ -56,7 +56,7 @@ struct RowPub {
 };
 
 struct Kn1Misc {
-    uint64_t bar[2];   // one per chunk buffer
+    uint64_t bar;      // the chunk copy
     float m;           // this row: chunk max value
     uint32_t mk16;     // this row: chunk max key, top 16 bits
     RowPub pub[2];
@@ -75,7 +75,7 @@ struct Kn1Misc {
 };
 
 // Dynamic shared memory: [misc 1 KB][chist 2 KB][cand CCAP*8][all ACAP*8]
-// [chunk buffer 0][chunk buffer 1 when prefetching].  The fallback's per-warp histograms (NW*1 KB) live in
+// [chunk data + 32].  The fallback's per-warp histograms (NW*1 KB) live in
 // `all`, which it fills only after its last histogram read.
 constexpr size_t OFF_CHIST = 1024;
 constexpr size_t OFF_CAND = OFF_CHIST + 2048;
@@ -157,7 +157,7 @@ DT_DI void merge_plain(cg::cluster_group& cluster, const uint32_t* h, int S, uin
 
 template <typename T>
 __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits, int V, int chunk, int Kc, int rows,
-                                                 int nbuf, float* __restrict__ lse_out,
+                                                 float* __restrict__ lse_out,
                                                  int32_t* __restrict__ cand_id,
                                                  float* __restrict__ cand_lp) {
     using E = DtElem<T>;
@@ -176,11 +176,9 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
     uint32_t* chist = (uint32_t*)(smem + OFF_CHIST);
     unsigned long long* cand = (unsigned long long*)(smem + OFF_CAND);
     unsigned long long* all = (unsigned long long*)(smem + OFF_ALL);
-    const size_t dstride = ((size_t)chunk * sizeof(T) + 32 + 127) & ~(size_t)127;
 
     if (tid == 0) {
-        dt_mbar_init(&misc->bar[0], 1);
-        dt_mbar_init(&misc->bar[1], 1);
+        dt_mbar_init(&misc->bar, 1);
         dt_fence_mbar_init();
     }
     dt_pdl_trigger();
@@ -189,15 +187,15 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
 
     // chunk buffers (bit i of a mask: buffer i): a bulk copy not yet waited
     // for, and the parity of the buffer's next mbarrier completion
-    uint32_t pend = 0, phase = 0;
-    DtStager<T> stg;  // ragged chunk ends of the latest copy, held in registers
-    auto issue = [&](int b, int r) {
-        if (stg.start(logits + (size_t)r * (size_t)V, lo, hi, smem + OFF_DATA + b * dstride, &misc->bar[b]))
-            pend |= 1u << b;
+    // the chunk copy: pending (issued, not waited for) and its mbarrier phase
+    bool pend = false;
+    uint32_t phase = 0;
+    DtStager<T> stg;  // ragged chunk ends of the copy, held in registers
+    auto issue = [&](int r) {
+        pend = stg.start(logits + (size_t)r * (size_t)V, lo, hi, smem + OFF_DATA, &misc->bar) != 0;
     };
     int row = blockIdx.y;
-    int buf = 0;
-    if (row < rows) issue(0, row);
+    if (row < rows) issue(row);
 
     for (int it = 0; row < rows; ++it, row += G) {
         const int par = it & 1;
@@ -209,26 +207,19 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
             mp->timeout = 0;
         }
         if (tid < 256) chist[tid] = 0;
-        stg.finish(smem + OFF_DATA + buf * dstride);  // this row's ragged ends
-        // start the next row's copy into the other buffer (its last reads were
-        // the previous row's, all before the barriers since)
-        if (nbuf == 2 && nxt < rows) {
-            __syncthreads();
-            dt_fence_proxy_async();
-            issue(buf ^ 1, nxt);
-        }
+        stg.finish(smem + OFF_DATA);  // this row's ragged ends
         // one thread waits on this row's copy; the others block in the barrier
         // below (blocked warps take no issue slots)
-        if ((pend >> buf) & 1u) {
-            if (tid == 0 && !dt_mbar_wait(&misc->bar[buf], (phase >> buf) & 1u)) {
+        if (pend) {
+            if (tid == 0 && !dt_mbar_wait(&misc->bar, phase)) {
                 mp->timeout = 1;
-                dt_mbar_wait(&misc->bar[buf], (phase >> buf) & 1u);
+                dt_mbar_wait(&misc->bar, phase);
             }
-            phase ^= 1u << buf;
-            pend &= ~(1u << buf);
+            phase ^= 1u;
+            pend = false;
         }
         __syncthreads();
-        unsigned char* dbase = smem + OFF_DATA + buf * dstride;
+        unsigned char* dbase = smem + OFF_DATA;
         Chunk<T> ch;
         // element lo sits at the source address's offset within 16 bytes
         ch.h = (int)(((uintptr_t)(logits + (size_t)row * (size_t)V + lo) & 15u) / sizeof(T));
@@ -593,13 +584,12 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
             for (int j = 0; j < S; ++j) to |= misc->cto[j];
             lse_out[row] = to ? __int_as_float(0x7FC00000) : lse;
         }
-        // without a second buffer the next row's copy starts only now
-        if (nbuf == 1 && nxt < rows) {
+        // the next row's copy starts once every read of this one is done
+        if (nxt < rows) {
             __syncthreads();
             dt_fence_proxy_async();
-            issue(0, nxt);
+            issue(nxt);
         }
-        if (nbuf == 2) buf ^= 1;
     }
     // partners may still be gathering from this CTA's shared memory
     __syncthreads();
@@ -608,9 +598,9 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
 
 }  // namespace
 
-size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize, int nbuf) {
+size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize) {
     (void)Kc;  // the fixed candidate buffers also hold the fallback's Kc <= 1024 selections
-    return OFF_DATA + (size_t)nbuf * ((((size_t)chunk * esize + 32) + 127) & ~(size_t)127);
+    return OFF_DATA + (size_t)chunk * esize + 32;
 }
 
 // Sets the kernel's shared-memory and cluster-size attributes for a launch.
@@ -621,9 +611,9 @@ cudaError_t kn1_prepare(int S, size_t smem) {
     return e;
 }
 
-int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc, int nbuf) {
+int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
-    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize, nbuf);
+    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize);
     if (dtype == DT_BF16) {
         if (kn1_prepare<uint16_t>(S, smem) != cudaSuccess) return 0;
         return dt_max_active_clusters(kn1_kernel<uint16_t>, S, NT, smem);
@@ -633,17 +623,17 @@ int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc, int nbuf) {
 }
 
 cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int grid_rows, int V, int Kc, int S, int chunk,
-                          int nbuf, float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st) {
+                          float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
-    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize, nbuf);
+    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize);
     DtLaunch lc(dim3(S, grid_rows, 1), dim3(NT, 1, 1), smem, st, S);
     cudaError_t e;
     if (dtype == DT_BF16) {
         if ((e = kn1_prepare<uint16_t>(S, smem)) != cudaSuccess) return e;
-        return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<uint16_t>, (const uint16_t*)logits, V, chunk, Kc, rows, nbuf,
+        return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<uint16_t>, (const uint16_t*)logits, V, chunk, Kc, rows,
                                   lse, cand_id, cand_lp);
     }
     if ((e = kn1_prepare<float>(S, smem)) != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<float>, (const float*)logits, V, chunk, Kc, rows, nbuf, lse,
+    return cudaLaunchKernelEx(&lc.cfg, kn1_kernel<float>, (const float*)logits, V, chunk, Kc, rows, lse,
                               cand_id, cand_lp);
 }

@@ -19,6 +19,7 @@ DT_MODE = {"ddtree": 0, "dartree": 1, "talon": 2}
 DT_BF16, DT_F32 = 0, 1
 DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_BESTFIRST = 0x1, 0x2, 0x4
 DT_DEV_VIOLATION_SHIFT = 8
+DT_STAGE1_CLUSTER, DT_STAGE1_ROWS = 1, 2
 MAX_NODES = 1025
 MAX_KC = 1024
 
@@ -56,6 +57,8 @@ def lib():
         L.dt_workspace_size.argtypes = [bp, ctypes.POINTER(ctypes.c_int)]
         L.dt_candidates.restype = _i32
         L.dt_candidates.argtypes = [bp, _vp, tp, _vp]
+        L.dt_stage1_plan.restype = _i32
+        L.dt_stage1_plan.argtypes = [bp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
         L.dt_select.restype = _i32
         L.dt_select.argtypes = [bp, tp, _vp, ctypes.c_size_t, _vp]
         L.dt_build_tree.restype = _i32
@@ -195,6 +198,14 @@ def candidates(p, draft_logits, tree, stream=None):
     _check(lib().dt_candidates(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()),
                                _stream(stream)), "dt_candidates")
 
+
+
+def stage1_plan(p):
+    """(kernel, cluster) that candidates() launches for Params p: kernel is
+    "cluster" (each row over a cluster of `cluster` CTAs) or "rows" (a CTA per row)."""
+    k, c = _i32(0), _i32(0)
+    _check(lib().dt_stage1_plan(ctypes.byref(p.struct()), ctypes.byref(k), ctypes.byref(c)), "dt_stage1_plan")
+    return ({DT_STAGE1_CLUSTER: "cluster", DT_STAGE1_ROWS: "rows"}[k.value], c.value)
 
 def select(p, tree, workspace=None, stream=None):
     ws, n = (workspace if workspace is not None else (None, 0))

@@ -118,3 +118,20 @@ def test_workspace_size():
     p.U = U
     p.Vt = U
     assert dtree.workspace_size(p) == 3 * 4 * 4 * 4 * 4
+
+
+def test_stage1_plan_picks_the_kernel_by_rows_and_list_length():
+    # many rows, or long candidate lists: a CTA per row (no device query needed)
+    p = dtree.Params(mode="ddtree", batch=64, L=16, V=151936, dtype="bf16", K=60, B=60)
+    assert dtree.stage1_plan(p) == ("rows", 1)
+    p = dtree.Params(mode="talon", batch=1, L=16, V=151936, dtype="bf16", talon_k=10, mu=0.03, N=1024)
+    assert dtree.stage1_plan(p) == ("rows", 1)
+    # one request: each row over a cluster (a power of two, chunks of at most 32768 elements)
+    p = dtree.Params(mode="ddtree", batch=1, L=16, V=151936, dtype="bf16", K=256, B=256)
+    kind, s = dtree.stage1_plan(p)
+    assert kind == "cluster" and s in (8, 16)
+    with pytest.raises(dtree.DtError):
+        dtree.stage1_plan(dtree.Params(mode="ddtree", batch=1, L=16, V=100, dtype="bf16", K=101, B=4))
+    L = dtree.lib()
+    k = ctypes.c_int32()
+    assert L.dt_stage1_plan(None, ctypes.byref(k), ctypes.byref(k)) == -1
