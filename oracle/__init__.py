@@ -34,9 +34,11 @@ def lib():
                                     _f64p, _f32p, _i32p, _f32p]
         L.or_ddtree.argtypes = [_f32p, _i32p] + [ctypes.c_int] * 5 + [_i32p] * 4 + [_f32p, _i32p]
         L.or_dartree.argtypes = ([_f32p, _i32p, ctypes.c_int, ctypes.c_int, _f32p, _f32p,
-                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                  ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_int, ctypes.c_float,
                                   ctypes.c_int, ctypes.c_int] + [_i32p] * 4 +
                                  [_f32p, _i32p, _i32p, _i32p])
+        L.or_markov_norm.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _f32p, _f32p,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p]
         L.or_talon.argtypes = ([_f32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_float, ctypes.c_int, ctypes.c_int] + [_i32p] * 4 +
                                [_f32p, _i32p])
@@ -136,9 +138,11 @@ def ddtree(cand_lp, cand_id, B, Mmax=None, rule=0):
     return t
 
 
-def dartree(cand_lp, cand_id, U, Vt, root_tok, W, beta, B, Mmax=None):
+def dartree(cand_lp, cand_id, U, Vt, root_tok, W, beta, B, Mmax=None, znorm=None):
     """DARTree supertree + deferred pruning.  Returns (tree, info, topb) with
-    info = dict(topb_equals_bestfirst, violations, supertree_size)."""
+    info = dict(topb_equals_bestfirst, violations, supertree_size).  znorm
+    ([L, K] fp32 log-normalisers from markov_norm) selects the full-vocabulary
+    normalised correction."""
     lp = _f32(cand_lp)
     ids = _i32(cand_id)
     L, K = lp.shape
@@ -150,18 +154,39 @@ def dartree(cand_lp, cand_id, U, Vt, root_tok, W, beta, B, Mmax=None):
         Vt = _f32(Vt)
         R = U.shape[1]
         Up, Vp = _p(U, ctypes.c_float), _p(Vt, ctypes.c_float)
+    zp = None
+    if znorm is not None:
+        znorm = _f32(znorm).reshape(L, K)
+        zp = _p(znorm, ctypes.c_float)
     Mmax = Mmax or B + 1
     t = _new_tree(Mmax)
     n = np.zeros(1, np.int32)
     info = np.zeros(3, np.int32)
     topb = np.full(Mmax, -1, np.int32)
     _check(lib().or_dartree(_p(lp, ctypes.c_float), _p(ids, ctypes.c_int32), L, K, Up, Vp, R,
-                            int(root_tok), W, ctypes.c_float(beta), B, Mmax, *_tree_args(t),
+                            int(root_tok), zp, W, ctypes.c_float(beta), B, Mmax, *_tree_args(t),
                             _p(n, ctypes.c_int32), _p(info, ctypes.c_int32),
                             _p(topb, ctypes.c_int32)), "dartree")
     t.n = int(n[0])
     return t, dict(topb_equals_bestfirst=bool(info[0]), violations=int(info[1]),
                    supertree_size=int(info[2])), topb
+
+
+def markov_norm(x, cand_id, U, Vt, root_tok, only_row=-1, out=None):
+    """[L, K] fp32 log-normalisers log Z of the full-vocabulary corrected
+    distribution (double inside) for raw logits x [L, V] (fp32 values) and the
+    candidate ids [L, K]; only_row >= 0 computes that flat row alone."""
+    x = _f32(x)
+    ids = _i32(cand_id)
+    L, V = x.shape
+    K = ids.shape[1]
+    U = _f32(U)
+    Vt = _f32(Vt)
+    z = np.zeros((L, K), np.float32) if out is None else out
+    _check(lib().or_markov_norm(_p(x, ctypes.c_float), L, V, _p(ids, ctypes.c_int32), K, _p(U, ctypes.c_float),
+                                _p(Vt, ctypes.c_float), U.shape[1], int(root_tok), int(only_row),
+                                _p(z, ctypes.c_float)), "markov_norm")
+    return z
 
 
 def talon(cand_lp, cand_id, talon_k, log_mu, N, Mmax=None):

@@ -323,6 +323,8 @@ int or_ddtree(const float* lp, const int32_t* id, int L, int K, int B, int rule,
 /*   info[0] = 1 if BestFirst_B(S) == TopB(S) (same nodes, same order)         */
 /*   info[1] = number of edges of S whose child outscores its parent           */
 /*   info[2] = |S| (non-root supertree nodes)                                  */
+/* With znorm (the full-vocabulary normalised correction, or_markov_norm):     */
+/* log q~ = (lp + <U, Vt>) - log Z, every term rounded to fp32 in that order.   */
 /* Pinned: reduction to the DDTree heap for U = 0, beta = 0 and W wide enough  */
 /* to keep every prefix; Lemma 1 equality; a beta > 0 counterexample (tests).  */
 /* ------------------------------------------------------------------------- */
@@ -336,6 +338,7 @@ static float or_markov(const float* U, const float* Vt, int R, int p, int c)
 
 int or_dartree(const float* lp, const int32_t* id, int L, int K,
                const float* U, const float* Vt, int R, int root_tok,
+               const float* znorm /* nullable [L][K]: log-normalisers, see or_markov_norm */,
                int W, float beta, int B, int Mmax,
                int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
                float* score, int32_t* n_nodes, int32_t* info,
@@ -357,8 +360,15 @@ int or_dartree(const float* lp, const int32_t* id, int L, int K,
                 float l = lp[(d - 1) * K + j];
                 float t;
                 int ptok = S[p].tok;
-                if (U != NULL && ptok >= 0) t = l + or_markov(U, Vt, R, ptok, c);
-                else t = l;
+                if (U != NULL && ptok >= 0) {
+                    t = l + or_markov(U, Vt, R, ptok, c);
+                    /* normalised correction: minus log Z of the parent's row,
+                     * row (position d-1, parent's rank at position d-2), or
+                     * row (0, 0) for the root */
+                    if (znorm != NULL) t = t - znorm[(d - 1) * K + (d == 1 ? 0 : S[p].r[d - 2])];
+                } else {
+                    t = l;
+                }
                 or_node* x = &kids[nk++];
                 *x = S[p];
                 x->r[d - 1] = j;
@@ -426,6 +436,60 @@ int or_dartree(const float* lp, const int32_t* id, int L, int K,
     }
     free(h.a); free(out_of); free(order); free(sorted); free(S); free(kids);
     return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Full-vocabulary normaliser of the corrected drafter distribution.           */
+/* [DARTree] "Causal correction": q~ is a probability over the vocabulary, so  */
+/* q~_d(v | u) = exp(lp_d(v) + <U[u], Vt[v]>) / Z_d(u) with                      */
+/* Z_d(u) = sum over every v of exp(lp_d(v) + <U[u], Vt[v]>).                     */
+/* Row (d, i) of z (0-based position d, i < K) holds log Z_d(u) for the parent  */
+/* token u of depth-(d+1) children: the i-th candidate of position d-1, or the  */
+/* root token at d = 0 (row (0, 0) only; the other rows of position 0, and all */
+/* of them when root_tok < 0, have no term and hold 0).                         */
+/* In double: lse_d = log sum_v exp x_d(v); lp_d(v) = x_d(v) - lse_d; the dot    */
+/* product; log Z = a_max + log sum_v exp(a_v - a_max).  Rounded once to fp32.  */
+/* only_row >= 0 computes that flat row (d * K + i) alone and leaves the rest. */
+/* Test infrastructure.                                                        */
+/* Pinned: U = 0 gives 0; one token gives its own term; hand-computed V = 3    */
+/* golden case; a constant added to every term shifts it; the normalised      */
+/* terms sum to 1; bounds max a <= log Z <= max a + log V (tests).             */
+/* ------------------------------------------------------------------------- */
+int or_markov_norm(const float* x /* [L][V] */, int L, int V, const int32_t* id /* [L][K] */, int K,
+                   const float* U, const float* Vt, int R, int root_tok, int only_row,
+                   float* z /* [L][K] */)
+{
+    if (L < 1 || L > OR_MAXL || V < 1 || K < 1 || R < 0 || !x || !id || !U || !Vt || !z) return OR_EINVAL;
+    double* a = (double*)malloc((size_t)V * sizeof(double));
+    if (!a) return OR_ENOMEM;
+    for (int d = 0; d < L; ++d) {
+        const float* xd = x + (int64_t)d * V;
+        int need = 0;
+        for (int i = 0; i < K; ++i) need |= (only_row < 0 || only_row == d * K + i);
+        if (!need) continue;
+        double mx = -INFINITY;
+        for (int v = 0; v < V; ++v) if ((double)xd[v] > mx) mx = (double)xd[v];
+        double sx = 0.0;
+        for (int v = 0; v < V; ++v) sx += exp((double)xd[v] - mx);
+        const double lse = mx + log(sx);
+        for (int i = 0; i < K; ++i) {
+            if (only_row >= 0 && only_row != d * K + i) continue;
+            const int u = (d == 0) ? (i == 0 ? root_tok : -1) : id[(d - 1) * K + i];
+            if (u < 0) { z[d * K + i] = 0.0f; continue; }
+            double am = -INFINITY;
+            for (int v = 0; v < V; ++v) {
+                double m = 0.0;
+                for (int k = 0; k < R; ++k) m += (double)U[(int64_t)u * R + k] * (double)Vt[(int64_t)v * R + k];
+                a[v] = ((double)xd[v] - lse) + m;
+                if (a[v] > am) am = a[v];
+            }
+            double sa = 0.0;
+            for (int v = 0; v < V; ++v) sa += exp(a[v] - am);
+            z[d * K + i] = (float)(am + log(sa));
+        }
+    }
+    free(a);
+    return OR_OK;
 }
 
 /* ------------------------------------------------------------------------- */
