@@ -102,6 +102,12 @@ typedef struct {
     int32_t talon_k;    /* TALON root-layer Top-k, 1..N */
     float log_mu;       /* TALON log(mu) rounded to fp32, mu in (0, 1] */
     int32_t N;          /* TALON node budget, 1..1024 */
+    int32_t markov_norm; /* DARTree with R > 0: 1 = normalise the corrected
+                           distribution over the full vocabulary ([DARTree]
+                           "Causal correction": q~ is a probability), i.e.
+                           log q~ = (lp + <U, Vt>) - log Z_d(parent token),
+                           see dt_markov_norm; needs R = 64 and 16-byte
+                           aligned U, Vt.  0 = the unnormalised term. */
 } dt_build_params;
 
 /* Tree buffers (caller-owned device memory).  Node 0 of each request is the
@@ -127,8 +133,11 @@ typedef struct {
 } dt_tree;
 
 /* Bytes of caller-provided device workspace dt_build_tree / dt_select need
- * for these parameters (0 for DDTree and TALON; DARTree: the per-request
- * Markov table, batch*L*K*K*4 bytes).  Returns 0 and sets *ok = 0 on invalid
+ * for these parameters (0 for DDTree and TALON; DARTree with R > 0: the
+ * per-request Markov table, batch*L*K*K*4 bytes, rounded up to 256; with
+ * markov_norm also the log-normaliser table, batch*L*K*4 bytes rounded up to
+ * 256, at byte offset DT_ZNORM_OFFSET(p) = the rounded Markov table size,
+ * then scratch for dt_markov_norm).  Returns 0 and sets *ok = 0 on invalid
  * parameters when ok != NULL. */
 size_t dt_workspace_size(const dt_build_params* p, int* ok);
 
@@ -165,7 +174,9 @@ dt_status dt_stage1_plan(const dt_build_params* p, int32_t* kernel, int32_t* clu
  *  DARTree ([DARTree] Algorithm 1, "Deferred best-first pruning", Lemma 1):
  *   per depth, all W*K children of the kept parents scored
  *   s = (s_parent + (lp + <U[tok(parent)], Vt[tok(child)]>)) + beta (the dot
- *   product a serial fp32 fma chain over R), keep the W best; then TopB over
+ *   product a serial fp32 fma chain over R; with markov_norm the term is
+ *   (lp + <U, Vt>) - log Z from the workspace table that dt_markov_norm, or
+ *   the caller, wrote), keep the W best; then TopB over
  *   the supertree S.  When TopB(S) is not a topologically ordered tree (only
  *   possible when some edge raises the score), the result is the best-first
  *   heap over S and DT_DEV_BESTFIRST is set.
@@ -176,7 +187,24 @@ dt_status dt_stage1_plan(const dt_build_params* p, int32_t* kernel, int32_t* clu
 dt_status dt_select(const dt_build_params* p, dt_tree* tree, void* workspace,
                     size_t workspace_bytes, dt_stream_t stream);
 
-/* dt_candidates followed by dt_select on the same stream. */
+/* Full-vocabulary log-normalisers of the corrected DARTree distribution
+ * ([DARTree] "Causal correction"), for p->markov_norm = 1.  For every request
+ * b, position d and candidate i of position d-1 (the possible parent tokens
+ * of depth-(d+1) nodes; at d = 0 the root token, row i = 0 only):
+ *   log Z = log sum over every v of exp(lp_d(v) + <U[u], Vt[v]>)
+ * written as fp32 to the workspace at DT_ZNORM_OFFSET(p), [b][L][K] (rows
+ * without a parent token get 0).  The [b*L*K x 64] x [64 x V] contraction
+ * runs on the tensor cores with U and Vt rounded to bf16 (fp32
+ * accumulation), so each value differs from the exact one by at most about
+ * 2^-8 * max_v sum_k |U[u][k] * Vt[v][k]| plus 1e-5.  Reads draft_logits and
+ * tree->cand_id, tree->lse (from dt_candidates).  A row whose bounded wait
+ * ran out gets NaN, which dt_select reports as DT_DEV_TIMEOUT. */
+#define DT_ZNORM_OFFSET(p) ((((size_t)(p)->batch * (p)->L * (p)->K * (p)->K * 4) + 255) & ~(size_t)255)
+dt_status dt_markov_norm(const dt_build_params* p, const void* draft_logits, dt_tree* tree, void* workspace,
+                         size_t workspace_bytes, dt_stream_t stream);
+
+/* dt_candidates, then dt_markov_norm when p->markov_norm, then dt_select, on
+ * the same stream. */
 dt_status dt_build_tree(const dt_build_params* p, const void* draft_logits,
                         dt_tree* tree, void* workspace, size_t workspace_bytes,
                         dt_stream_t stream);
@@ -238,7 +266,8 @@ dt_status dt_verify(const dt_tree* tree, int32_t batch, int32_t V, int32_t dtype
  * passes the tree buffers.  Nothing is allocated, by the library or by CUDA on
  * its behalf.
  *   - Returns DT_ERR_UNSUPPORTED when batch * L * K * K * 4 exceeds
- *     DT_NOALLOC_TABLE_BYTES, DT_ERR_INVALID_ARG for a mode other than
+ *     DT_NOALLOC_TABLE_BYTES or p->markov_norm is set (its normaliser table
+ *     needs caller workspace), DT_ERR_INVALID_ARG for a mode other than
  *     DT_MODE_DARTREE, and the usual errors otherwise.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any

@@ -131,6 +131,10 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
         if (p->R < 0 || p->R > 1024) return DT_ERR_INVALID_ARG;
         if (p->R > 0 && (!p->U || !p->Vt)) return DT_ERR_INVALID_ARG;
         if (p->R > 0 && dt_kn3_table_smem_bytes(p->K, p->R) > kSmemMax) return DT_ERR_UNSUPPORTED;
+        if (p->markov_norm != 0 && p->markov_norm != 1) return DT_ERR_INVALID_ARG;
+        if (p->markov_norm && (p->R == 0 || !p->U)) return DT_ERR_INVALID_ARG;  // nothing to normalise
+        if (p->markov_norm && p->R != 64) return DT_ERR_UNSUPPORTED;           // tensor-core tile: R = 64
+        if (p->markov_norm && ((((uintptr_t)p->U) | ((uintptr_t)p->Vt)) & 15u)) return DT_ERR_INVALID_ARG;
         if (dt_kn3_select_smem_bytes(p->L, p->K, p->W, p->R > 0 && p->U) > kSmemMax) return DT_ERR_UNSUPPORTED;
     }
     if (t->Kc != kc_of(p)) return DT_ERR_INVALID_ARG;
@@ -146,6 +150,9 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
         return DT_ERR_INVALID_ARG;
     return DT_OK;
 }
+
+// Bytes of the DARTree log-normaliser table (rounded up to 256).
+size_t znorm_bytes(const dt_build_params* p) { return (((size_t)p->batch * p->L * p->K * 4) + 255) & ~(size_t)255; }
 
 // Stage-1 launch shape: kernel DT_STAGE1_ROWS (one CTA per row) or
 // DT_STAGE1_CLUSTER (a cluster of S CTAs, chunk elements each, per row).
@@ -183,7 +190,11 @@ size_t dt_workspace_size(const dt_build_params* p, int* ok) {
         if (ok) *ok = 0;
         return 0;
     }
-    if (p->mode == DT_MODE_DARTREE && p->R > 0 && p->U) return (size_t)p->batch * p->L * p->K * p->K * sizeof(float);
+    if (p->mode == DT_MODE_DARTREE && p->R > 0 && p->U) {
+        size_t n = DT_ZNORM_OFFSET(p);
+        if (p->markov_norm) n += znorm_bytes(p) + dt_kn3n_part_bytes(p->batch * p->L * p->K);
+        return n;
+    }
     return 0;
 }
 
@@ -235,9 +246,11 @@ dt_status dt_select(const dt_build_params* p, dt_tree* t, void* workspace, size_
             const size_t need = dt_workspace_size(p, nullptr);
             if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
             const bool term = p->R > 0 && p->U;
+            const float* znorm =
+                (term && p->markov_norm) ? (const float*)((const unsigned char*)workspace + DT_ZNORM_OFFSET(p)) : nullptr;
             e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt, p->root_tok,
-                              Mmax, t->cand_lp, t->cand_id, t->lse, term ? (float*)workspace : nullptr, t->node_tok,
-                              t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, st);
+                              Mmax, t->cand_lp, t->cand_id, t->lse, term ? (float*)workspace : nullptr, znorm,
+                              t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, st);
             break;
         }
         case DT_MODE_TALON:
@@ -247,6 +260,20 @@ dt_status dt_select(const dt_build_params* p, dt_tree* t, void* workspace, size_
                               st);
             break;
     }
+    return cuda_status(e);
+}
+
+dt_status dt_markov_norm(const dt_build_params* p, const void* draft_logits, dt_tree* t, void* workspace,
+                         size_t workspace_bytes, dt_stream_t stream) {
+    dt_status s = check_build(p, t);
+    if (s != DT_OK) return s;
+    if (p->mode != DT_MODE_DARTREE || !p->markov_norm || !draft_logits) return DT_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < dt_workspace_size(p, nullptr)) return DT_ERR_INVALID_ARG;
+    unsigned char* ws = (unsigned char*)workspace;
+    float* z = (float*)(ws + DT_ZNORM_OFFSET(p));
+    float2* part = (float2*)(ws + DT_ZNORM_OFFSET(p) + znorm_bytes(p));
+    cudaError_t e = dt_kn3n_launch(draft_logits, p->dtype, p->batch, p->L, p->K, p->V, p->root_tok, t->cand_id, t->lse,
+                                   p->U, p->Vt, part, z, (cudaStream_t)stream);
     return cuda_status(e);
 }
 
@@ -260,6 +287,10 @@ dt_status dt_build_tree(const dt_build_params* p, const void* draft_logits, dt_t
     }
     s = dt_candidates(p, draft_logits, t, stream);
     if (s != DT_OK) return s;
+    if (p->mode == DT_MODE_DARTREE && p->markov_norm) {
+        s = dt_markov_norm(p, draft_logits, t, workspace, workspace_bytes, stream);
+        if (s != DT_OK) return s;
+    }
     return dt_select(p, t, workspace, workspace_bytes, stream);
 }
 
@@ -365,6 +396,7 @@ extern "C" dt_status dt_select_dartree_noalloc(const dt_build_params* p, dt_tree
     dt_status s = check_build(p, t);
     if (s != DT_OK) return s;
     if (p->mode != DT_MODE_DARTREE) return DT_ERR_INVALID_ARG;
+    if (p->markov_norm) return DT_ERR_UNSUPPORTED;  // the normaliser table needs caller workspace
     const bool term = p->R > 0 && p->U;
     float* table = nullptr;
     if (term) {
@@ -374,7 +406,7 @@ extern "C" dt_status dt_select_dartree_noalloc(const dt_build_params* p, dt_tree
         if (s != DT_OK) return s;
     }
     cudaError_t e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt,
-                                  p->root_tok, t->max_nodes, t->cand_lp, t->cand_id, t->lse, table, t->node_tok,
+                                  p->root_tok, t->max_nodes, t->cand_lp, t->cand_id, t->lse, table, nullptr, t->node_tok,
                                   t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status,
                                   (cudaStream_t)stream);
     return cuda_status(e);

@@ -80,9 +80,9 @@ size_t dt_kn3_table_smem_bytes(int K, int R);
 size_t dt_kn3_select_smem_bytes(int L, int K, int W, int use_table);
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
-                          const int32_t* cand_id, const float* lse, float* table, int32_t* tok, int32_t* parent,
-                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, int32_t* status,
-                          cudaStream_t st);
+                          const int32_t* cand_id, const float* lse, float* table, const float* znorm, int32_t* tok,
+                          int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
+                          int32_t* status, cudaStream_t st);
 
 // TALON selection (kn4_talon.cu).
 size_t dt_kn4_smem_bytes(int Kc, int N);
@@ -90,6 +90,14 @@ cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, i
                           const float* cand_lp, const int32_t* cand_id, const float* lse, int32_t* tok,
                           int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
                           int32_t* status, cudaStream_t st);
+
+// Full-vocabulary DARTree log-normalisers on the tensor cores (kn3n_norm.cu):
+// z [batch][L][K]; part: scratch of dt_kn3n_part_bytes(batch * L * K) bytes.
+#define DT_KN3N_MAX_SPLIT 256
+size_t dt_kn3n_part_bytes(int rows);
+cudaError_t dt_kn3n_launch(const void* x, int dtype, int batch, int L, int K, int V, const int32_t* root_tok,
+                           const int32_t* cand_id, const float* lse, const float* U, const float* Vt, float2* part,
+                           float* z, cudaStream_t st);
 
 // Tree mask (kn5_mask.cu).
 size_t dt_kn5_smem_bytes(int Mmax);

@@ -88,6 +88,7 @@ struct Kn3Smem {
     unsigned long long* scratch;  // [NT] warp-list merges (W <= 32)
     float* lps;   // [L*K] the request's candidate log-probs
     float* tabs;  // [L*K*K] the request's Markov table, when it fits (else nullptr)
+    float* zs;    // [L*K] the request's log-normalisers (normalised correction)
 };
 
 // Markov table entries staged in shared memory per request, at most.
@@ -101,6 +102,8 @@ DT_DI Kn3Smem kn3_carve(unsigned char* p, int L, int K, int W, bool stage_tab) {
     m.scratch = (unsigned long long*)p;
     p += (size_t)NT * 8;
     m.lps = (float*)p;
+    p += (size_t)((L * K + 3) & ~3) * 4;
+    m.zs = (float*)p;
     p += (size_t)((L * K + 3) & ~3) * 4;
     m.tabs = nullptr;
     if (stage_tab) {
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
                                                         const int32_t* __restrict__ cand_id,
                                                         const float* __restrict__ lse,
                                                         const float* __restrict__ table,
+                                                        const float* __restrict__ znorm,
                                                         int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
                                                         int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
                                                         float* __restrict__ o_score, int32_t* __restrict__ o_n,
@@ -144,7 +148,10 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
     const int rt = root_tok ? root_tok[b] : -1;
     const bool term1 = use_table && rt >= 0 && rt < V;
     // the request's log-probs (and Markov table, when small) into shared memory
-    for (int i = tid; i < L * K; i += NT) S.lps[i] = cand_lp[(size_t)b * L * K + i];
+    for (int i = tid; i < L * K; i += NT) {
+        S.lps[i] = cand_lp[(size_t)b * L * K + i];
+        S.zs[i] = znorm ? znorm[(size_t)b * L * K + i] : 0.f;
+    }
     if (stage_tab) {
         const float* tb = table + (size_t)b * L * K * K;
         const int n = L * K * K;
@@ -170,7 +177,11 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
             const int p = (d == 1) ? -1 : S.lexl[j];
             const float sp = (d == 1) ? 0.f : S.s[p];
             float t = lpd[r];
-            if (term) t = __fadd_rn(t, tab[(size_t)((d == 1) ? 0 : S.rank[p]) * K + r]);
+            if (term) {
+                const int pr = (d == 1) ? 0 : S.rank[p];  // parent's candidate index (root: row 0)
+                t = __fadd_rn(t, tab[(size_t)pr * K + r]);
+                if (znorm) t = __fsub_rn(t, S.zs[(size_t)(d - 1) * K + pr]);  // normalised: minus log Z
+            }
             const float sc = __fadd_rn(__fadd_rn(sp, t), beta);
             const uint32_t lx = ((uint32_t)j << 16) | (uint32_t)r;
             return ((unsigned long long)dt_fkey(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - lx);
@@ -347,6 +358,9 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
             const float x = lse[(size_t)b * L + l];
             if (x != x) bits |= DT_DEV_TIMEOUT;  // stage 1 flagged this row
         }
+        if (znorm)
+            for (int i = 0; i < L * K; ++i)
+                if (S.zs[i] != S.zs[i]) bits |= DT_DEV_TIMEOUT;  // the normaliser kernel flagged this row
         status[b] = bits;
     }
 }
@@ -360,13 +374,14 @@ size_t dt_kn3_select_smem_bytes(int L, int K, int W, int use_table) {
     while (cap < W * K || cap < W) cap <<= 1;
     const size_t NS = (size_t)W * L;
     const bool stage_tab = use_table && L * K * K <= kTabStage;
-    return (size_t)NT * 8 + (size_t)((L * K + 3) & ~3) * 4 + (stage_tab ? (size_t)L * K * K * 4 : 0) +
+    return (size_t)NT * 8 + (size_t)((L * K + 3) & ~3) * 8 + (stage_tab ? (size_t)L * K * K * 4 : 0) +
            (size_t)cap * 8 + (size_t)((K + 3) & ~3) * 4 + NS * 4 * 8 + (NS + 1) * 4 + (size_t)W * 4 + 16;
 }
 
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
-                          const int32_t* cand_id, const float* lse, float* table, int32_t* tok, int32_t* parent,
+                          const int32_t* cand_id, const float* lse, float* table, const float* znorm, int32_t* tok,
+                          int32_t* parent,
                           int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, int32_t* status,
                           cudaStream_t st) {
     cudaError_t e;
@@ -387,5 +402,6 @@ cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float be
         return e;
     DtLaunch ls(dim3(batch), dim3(NT), sm, st);
     return cudaLaunchKernelEx(&ls.cfg, kn3_select_kernel, L, K, W, B, beta, use_table, root_tok, V, Mmax, cand_lp,
-                              cand_id, lse, (const float*)table, tok, parent, depth, rank, score, n_nodes, status);
+                              cand_id, lse, (const float*)table, znorm, tok, parent, depth, rank, score, n_nodes,
+                              status);
 }

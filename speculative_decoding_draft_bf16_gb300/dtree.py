@@ -31,7 +31,7 @@ class BuildParams(ctypes.Structure):
     _fields_ = [("mode", _i32), ("batch", _i32), ("L", _i32), ("V", _i32), ("dtype", _i32),
                 ("K", _i32), ("B", _i32), ("W", _i32), ("beta", ctypes.c_float), ("R", _i32),
                 ("U", _vp), ("Vt", _vp), ("root_tok", _vp), ("talon_k", _i32),
-                ("log_mu", ctypes.c_float), ("N", _i32)]
+                ("log_mu", ctypes.c_float), ("N", _i32), ("markov_norm", _i32)]
 
 
 class TreeStruct(ctypes.Structure):
@@ -57,6 +57,8 @@ def lib():
         L.dt_workspace_size.argtypes = [bp, ctypes.POINTER(ctypes.c_int)]
         L.dt_candidates.restype = _i32
         L.dt_candidates.argtypes = [bp, _vp, tp, _vp]
+        L.dt_markov_norm.restype = _i32
+        L.dt_markov_norm.argtypes = [bp, _vp, tp, _vp, ctypes.c_size_t, _vp]
         L.dt_stage1_plan.restype = _i32
         L.dt_stage1_plan.argtypes = [bp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
         L.dt_select.restype = _i32
@@ -132,6 +134,7 @@ class Params:
     talon_k: int = 0
     mu: float = 0.0
     N: int = 0
+    markov_norm: bool = False  # DARTree: full-vocabulary normalised correction
 
     @property
     def Kc(self):
@@ -148,7 +151,7 @@ class Params:
         return BuildParams(DT_MODE[self.mode], self.batch, self.L, self.V,
                            DT_BF16 if self.dtype == "bf16" else DT_F32, self.K, self.B, self.W,
                            self.beta, self.R if self.U is not None else 0, _ptr(self.U), _ptr(self.Vt),
-                           _ptr(self.root_tok), self.talon_k, log_mu, self.N)
+                           _ptr(self.root_tok), self.talon_k, log_mu, self.N, int(bool(self.markov_norm)))
 
 
 class TreeBuffers:
@@ -206,6 +209,21 @@ def stage1_plan(p):
     k, c = _i32(0), _i32(0)
     _check(lib().dt_stage1_plan(ctypes.byref(p.struct()), ctypes.byref(k), ctypes.byref(c)), "dt_stage1_plan")
     return ({DT_STAGE1_CLUSTER: "cluster", DT_STAGE1_ROWS: "rows"}[k.value], c.value)
+
+def markov_norm(p, draft_logits, tree, workspace, stream=None):
+    """Full-vocabulary DARTree log-normalisers into the workspace (dt_markov_norm)."""
+    ws, n = workspace
+    _check(lib().dt_markov_norm(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()), _ptr(ws),
+                                n, _stream(stream)), "dt_markov_norm")
+
+
+def znorm_view(p, workspace):
+    """The [batch, L, K] fp32 log-normaliser table inside a DARTree workspace."""
+    ws, _ = workspace
+    off = (p.batch * p.L * p.K * p.K * 4 + 255) & ~255
+    n = p.batch * p.L * p.K
+    return ws[off:off + 4 * n].view(torch.float32).view(p.batch, p.L, p.K)
+
 
 def select(p, tree, workspace=None, stream=None):
     ws, n = (workspace if workspace is not None else (None, 0))
