@@ -71,6 +71,7 @@ def workloads():
         "stochastic_b16": wk.stochastic_batch(16),
         "dartree_beta0": wk.dartree_supertree(0.0),
         "dartree_beta-0.5": wk.dartree_supertree(-0.5),
+        "dartree_norm_beta0": wk.dartree_normalised(0.0),
         "talon_N60": wk.talon_gated(60),
         "talon_N1024": wk.talon_gated(1024),
     }
@@ -109,7 +110,8 @@ def parse():
 def params_for(wl, U=None, Vt=None):
     from speculative_decoding_draft_bf16_gb300 import dtree
     return dtree.Params(mode=wl.mode, batch=wl.batch, L=wl.L, V=wl.V, dtype=wl.dtype, K=wl.K, B=wl.B, W=wl.W,
-                        beta=wl.beta, R=wl.R, U=U, Vt=Vt, talon_k=wl.talon_k, mu=wl.mu, N=wl.N)
+                        beta=wl.beta, R=wl.R, U=U, Vt=Vt, talon_k=wl.talon_k, mu=wl.mu, N=wl.N,
+                        markov_norm=wl.markov_norm)
 
 
 def max_nodes_of(wl):
@@ -216,6 +218,8 @@ def run_ours(args, wl, rank, world, local):
             dtree.build_tree(p, c["x"], c["tree"], workspace=c["ws"])
         if "cand" in stages:
             dtree.candidates(p, c["x"], c["tree"])
+        if "norm" in stages:
+            dtree.markov_norm(p, c["x"], c["tree"], c["ws"])
         if "select" in stages:
             dtree.select(p, c["tree"], workspace=c["ws"])
         if "mask" in stages:
@@ -287,8 +291,10 @@ def run_ours(args, wl, rank, world, local):
 
     # per-stage device time (same rotating inputs, graphs of one stage)
     stage_us = {}
-    for name, stages in (("candidates", ("cand",)), ("select", ("select",)), ("mask", ("mask",)),
-                         ("verify", ("verify",))):
+    stage_list = [("candidates", ("cand",)), ("select", ("select",)), ("mask", ("mask",)), ("verify", ("verify",))]
+    if wl.markov_norm:
+        stage_list.insert(1, ("normalise", ("norm",)))
+    for name, stages in stage_list:
         n = max(R, (args.steps // R) * R)
         stage_us[name] = timed(stages, n, R) * 1000.0 / n
 
@@ -335,7 +341,7 @@ def run_ours(args, wl, rank, world, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     status = sum(int(c["tree"].status.abs().sum()) for c in copies)
-    launches_per_step = 4 + (1 if (wl.mode == "dartree" and wl.R > 0) else 0)
+    launches_per_step = 4 + (1 if (wl.mode == "dartree" and wl.R > 0) else 0) + (2 if wl.markov_norm else 0)
     kn1_s = stage_us["candidates"] / 1e6
     achieved = draft_bytes / kn1_s / 1e9
     peaks = {}
@@ -391,7 +397,8 @@ def oracle_round(wl, x, tgt, uni, U, Vt):
     if wl.mode == "ddtree":
         t = oracle.ddtree(lps, ids, wl.B, Mmax=Mmax)
     elif wl.mode == "dartree":
-        t, _, _ = oracle.dartree(lps, ids, U, Vt, -1, wl.W, wl.beta, wl.B, Mmax=Mmax)
+        z = oracle.markov_norm(x, ids, U, Vt, -1) if wl.markov_norm else None
+        t, _, _ = oracle.dartree(lps, ids, U, Vt, -1, wl.W, wl.beta, wl.B, Mmax=Mmax, znorm=z)
     else:
         t = oracle.talon(lps, ids, wl.talon_k, wl.log_mu, wl.N, Mmax=Mmax)
     oracle.tree_mask(t, Mmax, wl.L)

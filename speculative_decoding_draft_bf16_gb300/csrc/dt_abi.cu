@@ -192,7 +192,7 @@ size_t dt_workspace_size(const dt_build_params* p, int* ok) {
     }
     if (p->mode == DT_MODE_DARTREE && p->R > 0 && p->U) {
         size_t n = DT_ZNORM_OFFSET(p);
-        if (p->markov_norm) n += znorm_bytes(p) + dt_kn3n_part_bytes(p->batch * p->L * p->K);
+        if (p->markov_norm) n += znorm_bytes(p) + dt_kn3n_scratch_bytes(p->batch * p->L * p->K, p->V);
         return n;
     }
     return 0;
@@ -271,9 +271,9 @@ dt_status dt_markov_norm(const dt_build_params* p, const void* draft_logits, dt_
     if (!workspace || workspace_bytes < dt_workspace_size(p, nullptr)) return DT_ERR_INVALID_ARG;
     unsigned char* ws = (unsigned char*)workspace;
     float* z = (float*)(ws + DT_ZNORM_OFFSET(p));
-    float2* part = (float2*)(ws + DT_ZNORM_OFFSET(p) + znorm_bytes(p));
+    void* scratch = ws + DT_ZNORM_OFFSET(p) + znorm_bytes(p);
     cudaError_t e = dt_kn3n_launch(draft_logits, p->dtype, p->batch, p->L, p->K, p->V, p->root_tok, t->cand_id, t->lse,
-                                   p->U, p->Vt, part, z, (cudaStream_t)stream);
+                                   p->U, p->Vt, scratch, z, (cudaStream_t)stream);
     return cuda_status(e);
 }
 

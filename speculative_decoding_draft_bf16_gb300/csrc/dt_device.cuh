@@ -462,6 +462,20 @@ DT_DI void dt_cp_async16(void* sdst, const void* gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dt_smem_addr(sdst)), "l"(gsrc) : "memory");
 }
 DT_DI void dt_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Copies the first src_bytes (0..16) of 16 bytes and zero-fills the rest.
+DT_DI void dt_cp_async16_zfill(void* sdst, const void* gsrc, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dt_smem_addr(sdst)), "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+// Arrives on the mbarrier once all of this thread's earlier cp.async copies
+// have landed (the arrival is counted in the barrier's expected count).
+DT_DI void dt_cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dt_smem_addr(bar)) : "memory");
+}
+// Plain mbarrier arrival by this thread.
+DT_DI void dt_mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(dt_smem_addr(bar)) : "memory");
+}
 template <int N>
 DT_DI void dt_cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");

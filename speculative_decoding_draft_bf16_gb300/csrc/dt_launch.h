@@ -92,11 +92,12 @@ cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, i
                           int32_t* status, cudaStream_t st);
 
 // Full-vocabulary DARTree log-normalisers on the tensor cores (kn3n_norm.cu):
-// z [batch][L][K]; part: scratch of dt_kn3n_part_bytes(batch * L * K) bytes.
+// z [batch][L][K]; scratch: 256-byte aligned, dt_kn3n_scratch_bytes(batch * L * K, V)
+// bytes (per-slice partial sums, then the child-token table in bf16).
 #define DT_KN3N_MAX_SPLIT 256
-size_t dt_kn3n_part_bytes(int rows);
+size_t dt_kn3n_scratch_bytes(int rows, int V);
 cudaError_t dt_kn3n_launch(const void* x, int dtype, int batch, int L, int K, int V, const int32_t* root_tok,
-                           const int32_t* cand_id, const float* lse, const float* U, const float* Vt, float2* part,
+                           const int32_t* cand_id, const float* lse, const float* U, const float* Vt, void* scratch,
                            float* z, cudaStream_t st);
 
 // Tree mask (kn5_mask.cu).

@@ -25,14 +25,32 @@
 
 namespace {
 
-constexpr int NT = 128;       // four warps: TMEM lanes 0..127, one row each
+constexpr int NT = 320;       // warps 0-7: epilogue; warp 8: copies; warp 9: MMA issue
+constexpr int NEPI = 256;     // epilogue threads: TMEM lane quarter (warp % 4) x column half (warp / 4)
+constexpr int STAGES = 3;     // ring of Vt / logit tiles
 constexpr int TM = 128;       // rows per tile
 constexpr int TN = 128;       // tokens per MMA step
 constexpr int RK = 64;        // contraction length R (64 bf16 = one 128-byte row)
+constexpr int XG = 16;        // (request, position) logit rows staged per step, at most
 constexpr uint32_t IDESC = dt_idesc_bf16_f32(TM, TN);
-// alignment slack, A and B tiles, barrier; padded so that at most four CTAs
-// share an SM, whose 512 TMEM columns then always cover their allocations
-constexpr size_t SMEM = 56 * 1024;
+constexpr size_t A_BYTES = 16384, B_BYTES = 16384, X_BYTES = (size_t)XG * TN * 4;
+constexpr size_t OFF_B = A_BYTES;
+constexpr size_t OFF_X = OFF_B + STAGES * B_BYTES;
+constexpr size_t OFF_BAR = OFF_X + STAGES * X_BYTES;
+
+struct Kn3nShared {
+    uint64_t full[STAGES];   // tile landed (32 copy-thread arrivals)
+    uint64_t empty[STAGES];  // tile consumed (MMA commit + NEPI logit readers)
+    uint64_t accf[2];        // accumulator written (MMA commit)
+    uint64_t acce[2];        // accumulator read (NEPI arrivals)
+    uint32_t tmem;
+    int fail;
+    float pm[TM], ps[TM];    // second column half's partial (max, sum) per row
+};
+// A tile, three B tiles and three logit tiles from a 1024-byte aligned base; at
+// most two CTAs fit an SM, so their 2 x 256 TMEM columns always fit its 512
+constexpr size_t SMEM = 1024 + OFF_BAR + sizeof(Kn3nShared);
+static_assert(2 * (SMEM + 1024) <= 233472 && 3 * (SMEM + 1024) > 233472, "two CTAs per SM, not three");
 
 // Parent token of row r (-1: the row has no term).
 DT_DI int row_parent(int r, int L, int K, int V, const int32_t* root_tok, const int32_t* cand_id, int* b, int* d) {
@@ -45,10 +63,11 @@ DT_DI int row_parent(int r, int L, int K, int V, const int32_t* root_tok, const 
     return (u >= 0 && u < V) ? u : -1;
 }
 
-// Row `row` of an fp32 [*, 64] table into an swizzled bf16 tile row (zeros when src is null).
-DT_DI void stage_row_bf16(unsigned char* tile, int row, const float* src) {
+// Columns [k0, k0 + 32) of an fp32 [*, 64] table row into a swizzled bf16
+// tile row (zeros when src is null).
+DT_DI void stage_half_row_bf16(unsigned char* tile, int row, int k0, const float* src) {
 #pragma unroll
-    for (int k = 0; k < RK; k += 4) {
+    for (int k = k0; k < k0 + 32; k += 4) {
         float4 f = src ? *(const float4*)(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
         const __nv_bfloat162 lo = __floats2bfloat162_rn(f.x, f.y);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(f.z, f.w);
@@ -59,126 +78,254 @@ DT_DI void stage_row_bf16(unsigned char* tile, int row, const float* src) {
     }
 }
 
-// 32 drafter logits x[v0 .. v0+31] as fp32 (-inf from vend on).
-template <typename T>
-DT_DI void load_x32(const T* xrow, int v0, int vend, float (&o)[32]) {
-    using E = DtElem<T>;
+// Bounded wait; records a timeout in *fail (outputs then become NaN).
+DT_DI void wait_or_fail(uint64_t* bar, uint32_t parity, int* fail) {
+    if (!dt_mbar_wait(bar, parity)) *fail = 1;
+}
+
+// Fp32 table -> bf16 table (round to nearest), 8 values per thread step.
+__global__ void __launch_bounds__(256) kn3n_convert_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
+                                                           size_t n8) {
+    dt_pdl_trigger();
+    dt_pdl_wait();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = ((const float4*)src)[2 * i], c = ((const float4*)src)[2 * i + 1];
+        const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+        const __nv_bfloat162 p2 = __floats2bfloat162_rn(c.x, c.y), p3 = __floats2bfloat162_rn(c.z, c.w);
+        uint4 w;
+        w.x = *(const uint32_t*)&p0;
+        w.y = *(const uint32_t*)&p1;
+        w.z = *(const uint32_t*)&p2;
+        w.w = *(const uint32_t*)&p3;
+        ((uint4*)dst)[i] = w;
+    }
+}
+
+// The 32 logits of this thread's chunk from the staged tile, as fp32.
+DT_DI void tile_x32(const uint16_t* xt, float (&o)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float t[8];
+        dt_vec_vals<uint16_t>(*(const uint4*)(xt + 8 * q), t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[8 * q + i] = t[i];
+    }
+}
+DT_DI void tile_x32(const float* xt, float (&o)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float t[4];
+        dt_vec_vals<float>(*(const uint4*)(xt + 4 * q), t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[4 * q + i] = t[i];
+    }
+}
+
+// Folds v[0..31] (entries from nvalid on excluded) into a running (max M,
+// sum S of exp(v - M)).  For |M| < 64 each term is exp2(v * log2e - c) with
+// c = M * log2e rounded, one fused multiply-add on two lanes at a time: c's
+// rounding error (<= 2^-18) is common to every term of the row and shifts
+// log Z by < 3e-6.  Larger maxima round v - M first.
+DT_DI void fold32(float (&v)[32], int nvalid, float& M, float& S) {
     const float NEG_INF = -__int_as_float(0x7F800000);
-    const T* p = xrow + v0;
-    if (v0 + 32 <= vend && (((uintptr_t)p) & 15u) == 0) {
-        constexpr int EPV = 16 / sizeof(T);
+    const float log2e = 1.44269504088896340736f;
+    if (nvalid < 32) {
 #pragma unroll
-        for (int q = 0; q < 32 / EPV; ++q) {
-            float t[EPV];
-            dt_vec_vals<T>(*(const uint4*)(p + q * EPV), t);
+        for (int i = 0; i < 32; ++i)
+            if (i >= nvalid) v[i] = NEG_INF;
+    }
+    float cm = v[0];
 #pragma unroll
-            for (int s = 0; s < EPV; ++s) o[q * EPV + s] = t[s];
+    for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
+    if (cm > M) {
+        S = (M == NEG_INF) ? 0.f : __fmul_rn(S, dt_ex2_approx(__fmul_rn(__fsub_rn(M, cm), log2e)));
+        M = cm;
+    }
+    if (M == NEG_INF) return;
+    if (fabsf(M) < 64.f) {
+        const float c = __fmul_rn(M, log2e);
+        const unsigned long long l2 = dt_f2_pack(log2e, log2e), c2 = dt_f2_pack(-c, -c);
+        unsigned long long acc = dt_f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            float d0, d1;
+            dt_f2_unpack(dt_f2_fma(dt_f2_pack(v[i], v[i + 1]), l2, c2), d0, d1);
+            acc = dt_f2_add(acc, dt_f2_pack(dt_ex2_approx(d0), dt_ex2_approx(d1)));
         }
+        float a0, a1;
+        dt_f2_unpack(acc, a0, a1);
+        S = __fadd_rn(S, __fadd_rn(a0, a1));
     } else {
+        float p = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = (v0 + j < vend) ? E::val(p[j]) : NEG_INF;
+        for (int i = 0; i < 32; ++i) p = __fadd_rn(p, dt_ex2_approx(__fmul_rn(__fsub_rn(v[i], M), log2e)));
+        S = __fadd_rn(S, p);
     }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(NT) kn3n_kernel(const T* __restrict__ x, int V, int L, int K, int rows,
-                                                  const int32_t* __restrict__ root_tok,
-                                                  const int32_t* __restrict__ cand_id, const float* __restrict__ U,
-                                                  const float* __restrict__ Vt, int vs, float2* __restrict__ part) {
+__global__ void __launch_bounds__(NT, 2) kn3n_kernel(const T* __restrict__ x, int V, int L, int K, int rows,
+                                                     const int32_t* __restrict__ root_tok,
+                                                     const int32_t* __restrict__ cand_id,
+                                                     const float* __restrict__ U, const uint16_t* __restrict__ Vt16,
+                                                     int vs, float2* __restrict__ part) {
+    using E = DtElem<T>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* As = smem;
-    unsigned char* Bs = smem + 16384;
-    uint64_t* bar = (uint64_t*)(smem + 32768);
-    uint32_t* tslot = (uint32_t*)(smem + 32768 + 8);
-    int* fail = (int*)(smem + 32768 + 16);
-    const int tid = threadIdx.x, wid = tid >> 5;
+    unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    Kn3nShared* sh = (Kn3nShared*)(sm + OFF_BAR);
+    const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, tile = blockIdx.y;
-    const int r = tile * TM + tid;
+    const int vbeg = split * vs, vend = min(V, vbeg + vs);
+    const int nsteps = (vend - vbeg + TN - 1) / TN;
     const float NEG_INF = -__int_as_float(0x7F800000);
     const float log2e = 1.44269504088896340736f;
+    // logit rows of this tile: flat (request, position) indices g0 .. g0 + ng - 1
+    const int g0 = (tile * TM) / K;
+    const int ng = (min(rows, tile * TM + TM) - 1) / K - g0 + 1;
+    const bool xs = ng <= XG && (((uintptr_t)x) & 15u) == 0 && ((size_t)V * sizeof(T)) % 16 == 0;
 
-    if (wid == 0) dt_tmem_alloc(tslot, TN);
+    if (wid == 0) dt_tmem_alloc(&sh->tmem, 2 * TN);
     if (tid == 0) {
-        dt_mbar_init(bar, 1);
+        for (int i = 0; i < STAGES; ++i) {
+            dt_mbar_init(&sh->full[i], 32);
+            dt_mbar_init(&sh->empty[i], 1 + NEPI);
+        }
+        for (int i = 0; i < 2; ++i) {
+            dt_mbar_init(&sh->accf[i], 1);
+            dt_mbar_init(&sh->acce[i], NEPI);
+        }
         dt_fence_mbar_init();
-        *fail = 0;
+        sh->fail = 0;
     }
     dt_pdl_trigger();
-    dt_pdl_wait();  // candidate ids and logits come from earlier kernels
+    dt_pdl_wait();  // candidate ids, logits and the bf16 table come from earlier kernels
 
-    int b = 0, d = 0, u = -1;
-    if (r < rows) u = row_parent(r, L, K, V, root_tok, cand_id, &b, &d);
-    stage_row_bf16(As, tid, u >= 0 ? U + (size_t)u * RK : nullptr);
-    const T* xrow = x + ((size_t)b * L + d) * V;
-    const int vbeg = split * vs, vend = min(V, vbeg + vs);
-    const uint32_t a_base = dt_smem_addr(As), b_base = dt_smem_addr(Bs);
-
+    if (tid < NEPI) {  // A tile: the rows' U vectors, two threads per row
+        const int row = tid & (TM - 1), r = tile * TM + row;
+        int b, d;
+        const int u = r < rows ? row_parent(r, L, K, V, root_tok, cand_id, &b, &d) : -1;
+        stage_half_row_bf16(sm, row, 32 * (tid >> 7), u >= 0 ? U + (size_t)u * RK : nullptr);
+    }
     dt_fence_proxy_async_smem();
     dt_tc_fence_before();
     __syncthreads();
     dt_tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t tlane = tmem + ((uint32_t)(wid * 32) << 16);
+    const uint32_t tmem = sh->tmem;
 
-    float m_run = NEG_INF, s_run = 0.f;
-    uint32_t phase = 0;
-    // *fail is read only after a block barrier, so every thread leaves together
-    for (int v0 = vbeg; v0 < vend && !*fail; v0 += TN) {
-        // B tile: token v0 + tid's Vt vector (zeros past the slice)
-        const int v = v0 + tid;
-        stage_row_bf16(Bs, tid, v < vend ? Vt + (size_t)v * RK : nullptr);
-        dt_fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            dt_tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < RK / 16; ++kk)
-                dt_mma_bf16(tmem, dt_desc_kmajor_sw128(a_base + 32 * kk), dt_desc_kmajor_sw128(b_base + 32 * kk),
-                            IDESC, kk > 0);
-            dt_mma_commit(bar);
-        }
-        if (!dt_mbar_wait(bar, phase)) {
-            *fail = 1;
-            dt_mbar_wait(bar, phase);
-        }
-        phase ^= 1u;
-        dt_tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < TN; c += 32) {
-            float acc[32];
-            dt_tmem_ld32(tlane + c, acc);
-            if (u >= 0 && v0 + c < vend) {
-                float xv[32];
-                load_x32<T>(xrow, v0 + c, vend, xv);
-                float cm = NEG_INF;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc[j] = __fadd_rn(acc[j], xv[j]);  // -inf past the slice
-                    cm = fmaxf(cm, acc[j]);
-                }
-                if (cm > m_run) {
-                    s_run = (m_run == NEG_INF) ? 0.f : __fmul_rn(s_run, dt_ex2_approx(__fmul_rn(__fsub_rn(m_run, cm), log2e)));
-                    m_run = cm;
-                }
-                if (m_run != NEG_INF) {
-                    float p = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) p = __fadd_rn(p, dt_ex2_approx(__fmul_rn(__fsub_rn(acc[j], m_run), log2e)));
-                    s_run = __fadd_rn(s_run, p);
+    if (wid == 8) {
+        // ---- copies: Vt rows (swizzled) and logit rows of each step ---------
+        for (int j = 0; j < nsteps; ++j) {
+            const int s = j % STAGES;
+            if (j >= STAGES) wait_or_fail(&sh->empty[s], ((j / STAGES) - 1) & 1, &sh->fail);
+            const int v0 = vbeg + j * TN;
+            unsigned char* bt = sm + OFF_B + s * B_BYTES;
+            for (int q = lane; q < TN * 8; q += 32) {
+                const int row = q >> 3, c = q & 7, v = v0 + row;
+                const bool ok = v < vend;
+                dt_cp_async16_zfill(bt + row * 128 + ((c ^ (row & 7)) << 4), Vt16 + (size_t)(ok ? v : 0) * RK + c * 8,
+                                    ok ? 16u : 0u);
+            }
+            if (xs) {
+                constexpr int EPC = 16 / sizeof(T);   // elements per 16-byte chunk
+                constexpr int CPR = TN / EPC;         // chunks per logit row
+                unsigned char* xt = sm + OFF_X + s * X_BYTES;
+                for (int q = lane; q < ng * CPR; q += 32) {
+                    const int g = q / CPR, c = q % CPR, e0 = v0 + c * EPC;
+                    const int nb = max(0, min(16, (vend - e0) * (int)sizeof(T)));
+                    const T* src = x + (size_t)(g0 + g) * V + e0;
+                    dt_cp_async16_zfill(xt + (size_t)g * TN * sizeof(T) + c * 16, nb > 0 ? (const void*)src : (const void*)x,
+                                        (uint32_t)nb);
                 }
             }
+            dt_cp_async_arrive(&sh->full[s]);
         }
-        dt_tc_fence_before();
-        __syncthreads();  // accumulator read and B tile consumed before the next step
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (wid == 9) {
+        // ---- MMA issue: 128 x 128 x 64 per step into alternating accumulators
+        if (lane == 0) {
+            const uint32_t ab = dt_smem_addr(sm);
+            for (int j = 0; j < nsteps; ++j) {
+                const int s = j % STAGES, a = j & 1;
+                wait_or_fail(&sh->full[s], (j / STAGES) & 1, &sh->fail);
+                if (j >= 2) wait_or_fail(&sh->acce[a], ((j >> 1) - 1) & 1, &sh->fail);
+                dt_tc_fence_after();
+                dt_fence_proxy_async_smem();
+                const uint32_t bb = dt_smem_addr(sm + OFF_B + s * B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < RK / 16; ++kk)
+                    dt_mma_bf16(tmem + a * TN, dt_desc_kmajor_sw128(ab + 32 * kk), dt_desc_kmajor_sw128(bb + 32 * kk),
+                                IDESC, kk > 0);
+                dt_mma_commit(&sh->empty[s]);
+                dt_mma_commit(&sh->accf[a]);
+            }
+        }
     }
+    float m_run = NEG_INF, s_run = 0.f;
+    const int q4 = wid & 3, h = wid >> 2;     // epilogue: lane quarter, column half
+    const int row = q4 * 32 + lane, r = tile * TM + row;
+    if (wid < 8) {
+        // ---- epilogue: accumulator + logit, folded into a running (max, sum)
+        int b = 0, d = 0;
+        const int u = r < rows ? row_parent(r, L, K, V, root_tok, cand_id, &b, &d) : -1;
+        const int g = u >= 0 ? (b * L + d) - g0 : 0;  // logit row within the staged tile
+        const T* xrow = x + ((size_t)b * L + d) * V;
+        for (int j = 0; j < nsteps; ++j) {
+            const int s = j % STAGES, a = j & 1;
+            const int c0 = vbeg + j * TN + h * 64;  // first token of this thread's columns
+            const T* xt = (const T*)(sm + OFF_X + s * X_BYTES) + (size_t)g * TN + h * 64;
+            wait_or_fail(&sh->accf[a], (j >> 1) & 1, &sh->fail);
+            if (xs) wait_or_fail(&sh->full[s], (j / STAGES) & 1, &sh->fail);  // the logit tile has landed
+            dt_tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(q4 * 32) << 16) + a * TN + h * 64;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float v[32];
+                dt_tmem_ld32(ta + 32 * half, v);
+                const int cb = c0 + 32 * half;             // token of v[0]
+                const int nvalid = u >= 0 ? max(0, min(32, vend - cb)) : 0;
+                if (nvalid > 0) {
+                    float xv[32];
+                    if (xs) {
+                        tile_x32(xt + 32 * half, xv);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) xv[i] = (i < nvalid) ? E::val(xrow[cb + i]) : 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float a0, a1;
+                        dt_f2_unpack(dt_f2_add(dt_f2_pack(v[i], v[i + 1]), dt_f2_pack(xv[i], xv[i + 1])), a0, a1);
+                        v[i] = a0;
+                        v[i + 1] = a1;
+                    }
+                }
+                if (half == 1) {
+                    dt_tc_fence_before();
+                    dt_mbar_arrive(&sh->acce[a]);   // accumulator free for step j + 2
+                    dt_mbar_arrive(&sh->empty[s]);  // logit tile read
+                }
+                if (nvalid > 0) fold32(v, nvalid, m_run, s_run);
+            }
+        }
+        if (h == 1) {
+            sh->pm[row] = m_run;
+            sh->ps[row] = s_run;
+        }
+    }
+    dt_tc_fence_before();
     __syncthreads();
-    // a wait that ran out of its bound leaves the slice's sums undefined: NaN
-    if (r < rows) part[(size_t)r * gridDim.x + split] = *fail ? make_float2(__int_as_float(0x7FC00000), 0.f)
-                                                              : make_float2(m_run, s_run);
+    if (wid < 4 && r < rows) {
+        // merge the two column halves; a bounded wait that ran out leaves NaN
+        const float m2 = sh->pm[row], s2 = sh->ps[row];
+        const float M = fmaxf(m_run, m2);
+        float S = 0.f;
+        if (m_run != NEG_INF) S = __fmul_rn(s_run, dt_ex2_approx(__fmul_rn(__fsub_rn(m_run, M), log2e)));
+        if (m2 != NEG_INF) S = __fadd_rn(S, __fmul_rn(s2, dt_ex2_approx(__fmul_rn(__fsub_rn(m2, M), log2e))));
+        part[(size_t)r * gridDim.x + split] = sh->fail ? make_float2(__int_as_float(0x7FC00000), 0.f) : make_float2(M, S);
+    }
     if (wid == 0) {
         dt_tc_fence_after();
-        dt_tmem_dealloc(tmem, TN);
+        dt_tmem_dealloc(tmem, 2 * TN);
     }
 }
 
@@ -220,38 +367,50 @@ __global__ void __launch_bounds__(256) kn3n_reduce_kernel(const float2* __restri
 
 }  // namespace
 
-size_t dt_kn3n_part_bytes(int rows) { return (size_t)rows * DT_KN3N_MAX_SPLIT * sizeof(float2); }
+size_t dt_kn3n_scratch_bytes(int rows, int V) {
+    const size_t part = (((size_t)rows * DT_KN3N_MAX_SPLIT * sizeof(float2)) + 255) & ~(size_t)255;
+    return part + (size_t)V * RK * sizeof(uint16_t);
+}
 
 cudaError_t dt_kn3n_launch(const void* x, int dtype, int batch, int L, int K, int V, const int32_t* root_tok,
-                           const int32_t* cand_id, const float* lse, const float* U, const float* Vt, float2* part,
+                           const int32_t* cand_id, const float* lse, const float* U, const float* Vt, void* scratch,
                            float* z, cudaStream_t st) {
     const int rows = batch * L * K;
     const int mtiles = (rows + TM - 1) / TM;
+    float2* part = (float2*)scratch;
+    uint16_t* Vt16 = (uint16_t*)((unsigned char*)scratch +
+                                 ((((size_t)rows * DT_KN3N_MAX_SPLIT * sizeof(float2)) + 255) & ~(size_t)255));
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess || sms < 1) {
         (void)cudaGetLastError();
         sms = 148;
     }
-    // about two CTAs per SM, vocabulary slices of whole 128-token steps
+    cudaError_t e;
+    // the child-token table in bf16, once per call
+    const size_t n8 = (size_t)V * RK / 8;
+    size_t cblocks = (n8 + 255) / 256;
+    if (cblocks > (size_t)sms * 8) cblocks = (size_t)sms * 8;
+    DtLaunch lcv(dim3((unsigned)cblocks), dim3(256), 0, st);
+    if ((e = cudaLaunchKernelEx(&lcv.cfg, kn3n_convert_kernel, Vt, Vt16, n8)) != cudaSuccess) return e;
+    // two CTAs per SM, vocabulary slices of whole 128-token steps
     int nsplit = (2 * sms + mtiles - 1) / mtiles;
     const int steps = (V + TN - 1) / TN;
     nsplit = max(1, min(min(nsplit, DT_KN3N_MAX_SPLIT), steps));
     const int vs = ((steps + nsplit - 1) / nsplit) * TN;
     nsplit = (V + vs - 1) / vs;
-    cudaError_t e;
     DtLaunch lc(dim3(nsplit, mtiles, 1), dim3(NT, 1, 1), SMEM, st);
     if (dtype == DT_BF16) {
         if ((e = cudaFuncSetAttribute(kn3n_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
             cudaSuccess)
             return e;
         e = cudaLaunchKernelEx(&lc.cfg, kn3n_kernel<uint16_t>, (const uint16_t*)x, V, L, K, rows, root_tok, cand_id, U,
-                               Vt, vs, part);
+                               (const uint16_t*)Vt16, vs, part);
     } else {
         if ((e = cudaFuncSetAttribute(kn3n_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
             cudaSuccess)
             return e;
-        e = cudaLaunchKernelEx(&lc.cfg, kn3n_kernel<float>, (const float*)x, V, L, K, rows, root_tok, cand_id, U, Vt,
-                               vs, part);
+        e = cudaLaunchKernelEx(&lc.cfg, kn3n_kernel<float>, (const float*)x, V, L, K, rows, root_tok, cand_id, U,
+                               (const uint16_t*)Vt16, vs, part);
     }
     if (e != cudaSuccess) return e;
     DtLaunch lr(dim3((rows + 255) / 256), dim3(256), 0, st);

@@ -48,6 +48,7 @@ class Workload:
     mu: float = 0.0
     N: int = 0           # TALON node budget
     cfg: int = 0         # workload family number (seed base)
+    markov_norm: bool = False  # DARTree: full-vocabulary normalised correction
 
     @property
     def Kc(self):
@@ -89,6 +90,12 @@ def dartree_supertree(beta):
     """Batch 8, L=16, V=151936, W=32, K=16, R=64, beta in {0, -0.5}, B=512, greedy."""
     return Workload("dartree_b8_L16_V151936_W32_K16_B512_beta%g" % beta, "dartree", 8, 16,
                     V_QWEN3, "bf16", 3.0, 0.7, 0.0, K=16, B=512, W=32, beta=beta, R=64, cfg=3)
+
+
+def dartree_normalised(beta):
+    """The DARTree workload with the full-vocabulary normalised correction."""
+    return dataclasses.replace(dartree_supertree(beta), markov_norm=True,
+                               name="dartree_norm_b8_L16_V151936_W32_K16_B512_beta%g" % beta)
 
 
 def talon_gated(N):
