@@ -107,6 +107,23 @@ def parse():
     return ap.parse_args()
 
 
+def normaliser_roofline(wl, stage_us, peaks):
+    """The tensor-core normaliser's roofline (the dominant kernel of the
+    normalised DARTree workload): 2 * rows * V * R flops of the contraction per
+    launch over its measured stage time, against the sustained bf16 peak (it
+    runs inside a long step)."""
+    rows = wl.batch * wl.L * wl.K
+    flops = 2.0 * rows * wl.V * wl.R
+    tflops = flops / (stage_us["normalise"] * 1e-6) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    return {"roofline_normaliser": {
+        "bound": "tensor", "kernel": "kn3n_kernel (tcgen05 [rows x 64] x [64 x V] + log-sum-exp)",
+        "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+        "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops_sustained)", "traffic": None,
+        "algorithmic_flops_per_launch": flops,
+        "note": "one exp per (row, token) in the epilogue: %.0f M per launch" % (rows * wl.V / 1e6)}}
+
+
 def params_for(wl, U=None, Vt=None):
     from speculative_decoding_draft_bf16_gb300 import dtree
     return dtree.Params(mode=wl.mode, batch=wl.batch, L=wl.L, V=wl.V, dtype=wl.dtype, K=wl.K, B=wl.B, W=wl.W,
@@ -377,6 +394,7 @@ def run_ours(args, wl, rank, world, local):
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "algorithmic_bytes_per_launch": draft_bytes},
         "stages_us": stage_us,
+        **(normaliser_roofline(wl, stage_us, peaks) if wl.markov_norm else {}),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
