@@ -230,7 +230,9 @@ def run_ours(args, wl, rank, world, local):
         out = dtree.alloc_verify_out(tree, device=dev)
         copies.append(dict(x=x, tree=tree, ws=ws, tgt=tgt, uni=uni, mask=mask, pos=pos, out=out))
 
-    def step(c, stages=("build", "mask", "verify")):
+    def step(c, stages=("buildmask", "verify")):
+        if "buildmask" in stages:  # stage 1, selection, and the mask written by the selection kernel
+            dtree.build_tree_mask(p, c["x"], c["tree"], c["mask"], c["pos"], workspace=c["ws"])
         if "build" in stages:
             dtree.build_tree(p, c["x"], c["tree"], workspace=c["ws"])
         if "cand" in stages:
@@ -239,6 +241,8 @@ def run_ours(args, wl, rank, world, local):
             dtree.markov_norm(p, c["x"], c["tree"], c["ws"])
         if "select" in stages:
             dtree.select(p, c["tree"], workspace=c["ws"])
+        if "selmask" in stages:
+            dtree.select_mask(p, c["tree"], c["mask"], c["pos"], workspace=c["ws"])
         if "mask" in stages:
             dtree.tree_mask(c["tree"], c["mask"], c["pos"])
         if "verify" in stages:
@@ -296,7 +300,7 @@ def run_ours(args, wl, rank, world, local):
         return ms
 
     clocks = ClockSampler(local)
-    full_stages = ("build", "mask", "verify")
+    full_stages = ("buildmask", "verify")
     # the clock sampler runs over the timed region only
     for c in copies:
         step(c, full_stages)
@@ -308,7 +312,8 @@ def run_ours(args, wl, rank, world, local):
 
     # per-stage device time (same rotating inputs, graphs of one stage)
     stage_us = {}
-    stage_list = [("candidates", ("cand",)), ("select", ("select",)), ("mask", ("mask",)), ("verify", ("verify",))]
+    stage_list = [("candidates", ("cand",)), ("select+mask", ("selmask",)), ("select", ("select",)),
+                  ("mask", ("mask",)), ("verify", ("verify",))]
     if wl.markov_norm:
         stage_list.insert(1, ("normalise", ("norm",)))
     for name, stages in stage_list:
@@ -358,7 +363,9 @@ def run_ours(args, wl, rank, world, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     status = sum(int(c["tree"].status.abs().sum()) for c in copies)
-    launches_per_step = 4 + (1 if (wl.mode == "dartree" and wl.R > 0) else 0) + (2 if wl.markov_norm else 0)
+    # stage 1, selection (writing the mask), walk; DARTree's Markov table; the normalised correction's
+    # table conversion, normaliser and merge
+    launches_per_step = 3 + (1 if (wl.mode == "dartree" and wl.R > 0) else 0) + (3 if wl.markov_norm else 0)
     kn1_s = stage_us["candidates"] / 1e6
     achieved = draft_bytes / kn1_s / 1e9
     peaks = {}

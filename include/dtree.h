@@ -209,6 +209,20 @@ dt_status dt_build_tree(const dt_build_params* p, const void* draft_logits,
                         dt_tree* tree, void* workspace, size_t workspace_bytes,
                         dt_stream_t stream);
 
+/* dt_select followed by dt_tree_mask: same outputs as the two calls.  For
+ * trees of at most 512 rows (max_nodes) the selection kernel writes the mask
+ * and positions itself (one kernel launch fewer; its trees have every parent
+ * before its children); larger trees get the mask kernel after it.
+ * mask/pos as in dt_tree_mask. */
+dt_status dt_select_mask(const dt_build_params* p, dt_tree* tree, void* workspace, size_t workspace_bytes,
+                         int32_t pos_offset, uint32_t* mask, int32_t* pos, dt_stream_t stream);
+
+/* dt_build_tree followed by dt_tree_mask: dt_candidates, dt_markov_norm when
+ * p->markov_norm, then dt_select_mask. */
+dt_status dt_build_tree_mask(const dt_build_params* p, const void* draft_logits, dt_tree* tree, void* workspace,
+                             size_t workspace_bytes, int32_t pos_offset, uint32_t* mask, int32_t* pos,
+                             dt_stream_t stream);
+
 /* Tree-attention ancestor mask and position ids.  [DARTree] "Tree
  * verification and DDTree" (a node attends to the verified context and its
  * root-to-node path); [DDTree] section 4.2.

@@ -229,18 +229,26 @@ dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_t
     return cuda_status(e);
 }
 
-dt_status dt_select(const dt_build_params* p, dt_tree* t, void* workspace, size_t workspace_bytes,
-                    dt_stream_t stream) {
+// Largest tree (rows) whose mask the selection kernel writes itself; larger
+// trees get the level-by-level mask kernel after the selection (measured on a
+// GB300: fused is faster for 61, 257 and 497 rows, slower for 1025).
+constexpr int kFusedMaskMaxNodes = 512;
+
+// Selection kernels, optionally also writing the tree mask and positions.
+static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspace, size_t workspace_bytes,
+                             uint32_t* mask_out, int32_t* pos_out, int pos_offset, cudaStream_t st) {
     dt_status s = check_build(p, t);
     if (s != DT_OK) return s;
-    cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
     const int Mmax = t->max_nodes;
+    const bool fuse = mask_out && Mmax <= kFusedMaskMaxNodes;
+    uint32_t* mask = fuse ? mask_out : nullptr;
+    int32_t* pos = fuse ? pos_out : nullptr;
     switch (p->mode) {
         case DT_MODE_DDTREE:
             if (dt_kn2_smem_bytes(p->L, p->K, p->B) > kSmemMax) return DT_ERR_UNSUPPORTED;
             e = dt_kn2_launch(p->batch, p->L, p->K, p->B, Mmax, t->cand_lp, t->cand_id, t->lse, t->node_tok,
-                              t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, st);
+                              t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, mask, pos, pos_offset, st);
             break;
         case DT_MODE_DARTREE: {
             const size_t need = dt_workspace_size(p, nullptr);
@@ -250,17 +258,51 @@ dt_status dt_select(const dt_build_params* p, dt_tree* t, void* workspace, size_
                 (term && p->markov_norm) ? (const float*)((const unsigned char*)workspace + DT_ZNORM_OFFSET(p)) : nullptr;
             e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt, p->root_tok,
                               Mmax, t->cand_lp, t->cand_id, t->lse, term ? (float*)workspace : nullptr, znorm,
-                              t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, st);
+                              t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, mask, pos,
+                              pos_offset, st);
             break;
         }
         case DT_MODE_TALON:
             if (dt_kn4_smem_bytes(kc_of(p), p->N) > kSmemMax) return DT_ERR_UNSUPPORTED;
             e = dt_kn4_launch(p->batch, p->L, kc_of(p), p->talon_k, p->log_mu, p->N, Mmax, t->cand_lp, t->cand_id,
                               t->lse, t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status,
-                              st);
+                              mask, pos, pos_offset, st);
             break;
     }
+    if (e == cudaSuccess && mask_out && !fuse)
+        e = dt_kn5_launch(p->batch, t->L, Mmax, pos_offset, t->parent, t->depth, t->n_nodes, mask_out, pos_out,
+                          t->status, st);
     return cuda_status(e);
+}
+
+dt_status dt_select(const dt_build_params* p, dt_tree* t, void* workspace, size_t workspace_bytes,
+                    dt_stream_t stream) {
+    return select_impl(p, t, workspace, workspace_bytes, nullptr, nullptr, 0, (cudaStream_t)stream);
+}
+
+dt_status dt_select_mask(const dt_build_params* p, dt_tree* t, void* workspace, size_t workspace_bytes,
+                         int32_t pos_offset, uint32_t* mask, int32_t* pos, dt_stream_t stream) {
+    if (!mask || !pos) return DT_ERR_INVALID_ARG;
+    return select_impl(p, t, workspace, workspace_bytes, mask, pos, pos_offset, (cudaStream_t)stream);
+}
+
+dt_status dt_build_tree_mask(const dt_build_params* p, const void* draft_logits, dt_tree* t, void* workspace,
+                             size_t workspace_bytes, int32_t pos_offset, uint32_t* mask, int32_t* pos,
+                             dt_stream_t stream) {
+    dt_status s = check_build(p, t);
+    if (s != DT_OK) return s;
+    if (!mask || !pos) return DT_ERR_INVALID_ARG;
+    if (p->mode == DT_MODE_DARTREE) {
+        const size_t need = dt_workspace_size(p, nullptr);
+        if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
+    }
+    s = dt_candidates(p, draft_logits, t, stream);
+    if (s != DT_OK) return s;
+    if (p->mode == DT_MODE_DARTREE && p->markov_norm) {
+        s = dt_markov_norm(p, draft_logits, t, workspace, workspace_bytes, stream);
+        if (s != DT_OK) return s;
+    }
+    return select_impl(p, t, workspace, workspace_bytes, mask, pos, pos_offset, (cudaStream_t)stream);
 }
 
 dt_status dt_markov_norm(const dt_build_params* p, const void* draft_logits, dt_tree* t, void* workspace,
@@ -407,7 +449,7 @@ extern "C" dt_status dt_select_dartree_noalloc(const dt_build_params* p, dt_tree
     }
     cudaError_t e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt,
                                   p->root_tok, t->max_nodes, t->cand_lp, t->cand_id, t->lse, table, nullptr, t->node_tok,
-                                  t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status,
+                                  t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, nullptr, nullptr, 0,
                                   (cudaStream_t)stream);
     return cuda_status(e);
 }

@@ -73,7 +73,8 @@ cudaError_t dt_kn1b_launch(const void* logits, int dtype, int rows, int V, int K
 size_t dt_kn2_smem_bytes(int L, int K, int B);
 cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
                           const float* lse, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
-                          float* score, int32_t* n_nodes, int32_t* status, cudaStream_t st);
+                          float* score, int32_t* n_nodes, int32_t* status, uint32_t* mask, int32_t* pos,
+                          int pos_offset, cudaStream_t st);
 
 // DARTree Markov table + selection (kn3_dartree.cu).
 size_t dt_kn3_table_smem_bytes(int K, int R);
@@ -82,14 +83,14 @@ cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float be
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* lse, float* table, const float* znorm, int32_t* tok,
                           int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
-                          int32_t* status, cudaStream_t st);
+                          int32_t* status, uint32_t* mask, int32_t* pos, int pos_offset, cudaStream_t st);
 
 // TALON selection (kn4_talon.cu).
 size_t dt_kn4_smem_bytes(int Kc, int N);
 cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
                           const float* cand_lp, const int32_t* cand_id, const float* lse, int32_t* tok,
                           int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
-                          int32_t* status, cudaStream_t st);
+                          int32_t* status, uint32_t* mask, int32_t* pos, int pos_offset, cudaStream_t st);
 
 // Full-vocabulary DARTree log-normalisers on the tensor cores (kn3n_norm.cu):
 // z [batch][L][K]; scratch: 256-byte aligned, dt_kn3n_scratch_bytes(batch * L * K, V)

@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                                                  int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
                                                  int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
                                                  float* __restrict__ o_score, int32_t* __restrict__ o_n,
-                                                 int32_t* __restrict__ status) {
+                                                 int32_t* __restrict__ status, uint32_t* __restrict__ o_mask,
+                                                 int32_t* __restrict__ o_pos, int pos_offset) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int red[NT / 32];
     __shared__ int sh_nP, sh_lrhi, sh_any;
@@ -325,6 +326,11 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
         }
         status[b] = bits;
     }
+    if (o_mask) {  // fused tree mask and positions
+        __syncthreads();
+        dt_write_mask_rows<NT>(nC + 1, Mmax, o_par + ob, o_dep + ob, pos_offset,
+                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5), o_pos + ob);
+    }
 }
 
 }  // namespace
@@ -337,11 +343,12 @@ size_t dt_kn2_smem_bytes(int L, int K, int B) {
 
 cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
                           const float* lse, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
-                          float* score, int32_t* n_nodes, int32_t* status, cudaStream_t st) {
+                          float* score, int32_t* n_nodes, int32_t* status, uint32_t* mask, int32_t* pos,
+                          int pos_offset, cudaStream_t st) {
     const size_t smem = dt_kn2_smem_bytes(L, K, B);
     cudaError_t e = cudaFuncSetAttribute(kn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     DtLaunch lc(dim3(batch), dim3(NT), smem, st);
     return cudaLaunchKernelEx(&lc.cfg, kn2_kernel, cand_lp, cand_id, lse, L, K, B, Mmax, tok, parent, depth, rank,
-                              score, n_nodes, status);
+                              score, n_nodes, status, mask, pos, pos_offset);
 }

@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
                                                         int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
                                                         int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
                                                         float* __restrict__ o_score, int32_t* __restrict__ o_n,
-                                                        int32_t* __restrict__ status) {
+                                                        int32_t* __restrict__ status, uint32_t* __restrict__ o_mask,
+                                                        int32_t* __restrict__ o_pos, int pos_offset) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int lay_start[DT_MAX_L + 2];
     __shared__ int sh_bad, sh_viol;
@@ -363,6 +364,11 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
                 if (S.zs[i] != S.zs[i]) bits |= DT_DEV_TIMEOUT;  // the normaliser kernel flagged this row
         status[b] = bits;
     }
+    if (o_mask) {  // fused tree mask and positions
+        __syncthreads();
+        dt_write_mask_rows<NT>(nOut + 1, Mmax, o_par + ob, o_dep + ob, pos_offset,
+                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5), o_pos + ob);
+    }
 }
 
 }  // namespace
@@ -381,9 +387,8 @@ size_t dt_kn3_select_smem_bytes(int L, int K, int W, int use_table) {
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* lse, float* table, const float* znorm, int32_t* tok,
-                          int32_t* parent,
-                          int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes, int32_t* status,
-                          cudaStream_t st) {
+                          int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
+                          int32_t* status, uint32_t* mask, int32_t* pos, int pos_offset, cudaStream_t st) {
     cudaError_t e;
     const int use_table = (R > 0 && table != nullptr) ? 1 : 0;
     if (use_table) {
@@ -403,5 +408,5 @@ cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float be
     DtLaunch ls(dim3(batch), dim3(NT), sm, st);
     return cudaLaunchKernelEx(&ls.cfg, kn3_select_kernel, L, K, W, B, beta, use_table, root_tok, V, Mmax, cand_lp,
                               cand_id, lse, (const float*)table, znorm, tok, parent, depth, rank, score, n_nodes,
-                              status);
+                              status, mask, pos, pos_offset);
 }

@@ -78,7 +78,8 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
                                                  int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
                                                  int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
                                                  float* __restrict__ o_score, int32_t* __restrict__ o_n,
-                                                 int32_t* __restrict__ status) {
+                                                 int32_t* __restrict__ status, uint32_t* __restrict__ o_mask,
+                                                 int32_t* __restrict__ o_pos, int pos_offset) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int red[NT / 32];
     __shared__ float redf[NT / 32];
@@ -237,6 +238,11 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
         }
         status[b] = bits;
     }
+    if (o_mask) {  // fused tree mask and positions
+        __syncthreads();
+        dt_write_mask_rows<NT>(nT + 1, Mmax, o_par + ob, o_dep + ob, pos_offset,
+                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5), o_pos + ob);
+    }
 }
 
 }  // namespace
@@ -250,11 +256,11 @@ size_t dt_kn4_smem_bytes(int Kc, int N) {
 cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
                           const float* cand_lp, const int32_t* cand_id, const float* lse, int32_t* tok,
                           int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
-                          int32_t* status, cudaStream_t st) {
+                          int32_t* status, uint32_t* mask, int32_t* pos, int pos_offset, cudaStream_t st) {
     const size_t smem = dt_kn4_smem_bytes(Kc, N);
     cudaError_t e = cudaFuncSetAttribute(kn4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     DtLaunch lc(dim3(batch), dim3(NT), smem, st);
     return cudaLaunchKernelEx(&lc.cfg, kn4_kernel, L, Kc, talon_k, log_mu, N, Mmax, cand_lp, cand_id, lse, tok,
-                              parent, depth, rank, score, n_nodes, status);
+                              parent, depth, rank, score, n_nodes, status, mask, pos, pos_offset);
 }

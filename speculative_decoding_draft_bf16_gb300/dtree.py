@@ -247,6 +247,28 @@ def build_tree(p, draft_logits, tree, workspace=None, stream=None):
                                _ptr(ws), n, _stream(stream)), "dt_build_tree")
 
 
+
+def select_mask(p, tree, mask, pos, workspace=None, pos_offset=0, stream=None):
+    """select + tree_mask with the mask written by the selection kernel (dt_select_mask)."""
+    _need(mask, torch.int32, "mask")
+    _need(pos, torch.int32, "pos")
+    ws, n = (workspace if workspace is not None else (None, 0))
+    _check(lib().dt_select_mask(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _ptr(ws), n, int(pos_offset),
+                                _ptr(mask), _ptr(pos), _stream(stream)), "dt_select_mask")
+
+
+def build_tree_mask(p, draft_logits, tree, mask, pos, workspace=None, pos_offset=0, stream=None):
+    """build_tree + tree_mask with the mask written by the selection kernel
+    (dt_build_tree_mask); mask, pos from alloc_mask(tree)."""
+    _need(draft_logits, name="draft_logits")
+    assert _dtype_code(draft_logits) == (DT_BF16 if p.dtype == "bf16" else DT_F32)
+    _need(mask, torch.int32, "mask")
+    _need(pos, torch.int32, "pos")
+    ws, n = (workspace if workspace is not None else (None, 0))
+    _check(lib().dt_build_tree_mask(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()),
+                                    _ptr(ws), n, int(pos_offset), _ptr(mask), _ptr(pos), _stream(stream)),
+           "dt_build_tree_mask")
+
 def tree_mask(tree, mask, pos, pos_offset=0, batch=None, stream=None):
     _need(mask, torch.int32, "mask")
     _need(pos, torch.int32, "pos")

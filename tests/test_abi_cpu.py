@@ -135,3 +135,42 @@ def test_stage1_plan_picks_the_kernel_by_rows_and_list_length():
     L = dtree.lib()
     k = ctypes.c_int32()
     assert L.dt_stage1_plan(None, ctypes.byref(k), ctypes.byref(k)) == -1
+
+
+def test_fused_entry_points_and_normalisation_reject_invalid_arguments():
+    L = dtree.lib()
+    fake = ctypes.c_void_p(0x3000)
+    good = dtree.Params(mode="ddtree", batch=1, L=4, V=32, dtype="bf16", K=4, B=8)
+    bad = dtree.Params(mode="ddtree", batch=0, L=4, V=32, dtype="bf16", K=4, B=8)
+    t = _FakeTree(1, 4, 4, 9).struct()
+    # null mask / positions, invalid parameters: rejected on the host
+    assert L.dt_select_mask(ctypes.byref(good.struct()), ctypes.byref(t), None, 0, 0, None, fake, None) == -1
+    assert L.dt_select_mask(ctypes.byref(bad.struct()), ctypes.byref(t), None, 0, 0, fake, fake, None) == -1
+    assert L.dt_build_tree_mask(ctypes.byref(bad.struct()), fake, ctypes.byref(t), None, 0, 0, fake, fake,
+                                None) == -1
+    assert L.dt_build_tree_mask(ctypes.byref(good.struct()), fake, ctypes.byref(t), None, 0, 0, fake, None,
+                                None) == -1
+    # the normalised DARTree correction: needs a Markov table of rank 64 and 16-byte aligned tables
+    def dart(**kw):
+        q = dict(mode="dartree", batch=1, L=4, V=32, dtype="bf16", K=4, W=4, B=8, R=64, markov_norm=True)
+        q.update(kw)
+        return dtree.Params(**q)
+    U = ctypes.c_void_p(0x10000)
+
+    def with_tables(q, u=U, r=None):
+        st = q.struct()
+        st.U, st.Vt = u, U
+        st.R = q.R if r is None else r
+        return st
+    s = with_tables(dart())
+    td = _FakeTree(1, 4, 4, 9).struct()
+    w = ctypes.c_int(0)
+    assert L.dt_workspace_size(ctypes.byref(s), ctypes.byref(w)) > 0 and w.value == 1
+    s32 = with_tables(dart(R=32))
+    assert L.dt_markov_norm(ctypes.byref(s32), fake, ctypes.byref(td), fake, 1 << 30, None) == -2
+    s_unaligned = with_tables(dart(), u=ctypes.c_void_p(0x10004))
+    assert L.dt_markov_norm(ctypes.byref(s_unaligned), fake, ctypes.byref(td), fake, 1 << 30, None) == -1
+    s_noterm = dart(R=0).struct()
+    assert L.dt_markov_norm(ctypes.byref(s_noterm), fake, ctypes.byref(td), fake, 1 << 30, None) == -1
+    # the allocation-free selection does not take the normalised correction
+    assert L.dt_select_dartree_noalloc(ctypes.byref(s), ctypes.byref(td), None) == -2

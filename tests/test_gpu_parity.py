@@ -623,3 +623,61 @@ def test_talon_full_size(N):
     torch.cuda.synchronize()
     for b in sample:
         near_tie_diff(gpu_tree(t3, b), want[b])
+
+
+# ---------------------------------------------------------------------------
+# Mask written by the selection kernel itself (dt_build_tree_mask)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", ["ddtree", "dartree", "talon", "talon_large"])
+def test_fused_mask_equals_mask_kernel(mode):
+    batch, L, V = 3, 8, 5000
+    x = gen_logits(batch, L, V, "bf16", 3.0, 0.7, seed=77).cuda()
+    if mode == "ddtree":
+        p = dtree.Params(mode="ddtree", batch=batch, L=L, V=V, dtype="bf16", K=40, B=40)
+    elif mode == "dartree":
+        g = torch.Generator().manual_seed(78)
+        U = (torch.randn((V, 64), generator=g) * 0.1).cuda()
+        Vt = (torch.randn((V, 64), generator=g) * 0.1).cuda()
+        p = dtree.Params(mode="dartree", batch=batch, L=L, V=V, dtype="bf16", K=8, W=16, B=60, beta=-0.25, R=64,
+                         U=U, Vt=Vt)
+    elif mode == "talon":
+        p = dtree.Params(mode="talon", batch=batch, L=L, V=V, dtype="bf16", talon_k=6, mu=0.05, N=90)
+    else:  # more than 512 rows: the mask kernel runs after the selection
+        p = dtree.Params(mode="talon", batch=batch, L=L, V=V, dtype="bf16", talon_k=10, mu=0.01, N=700)
+    max_nodes = min(p.B, p.W * L) + 1 if mode == "dartree" else p.budget + 1
+    ws = dtree.make_workspace(p)
+    t1 = dtree.TreeBuffers.for_params(p, max_nodes=max_nodes)
+    t2 = dtree.TreeBuffers.for_params(p, max_nodes=max_nodes)
+    m1, p1 = dtree.alloc_mask(t1)
+    m2, p2 = dtree.alloc_mask(t2)
+    dtree.build_tree(p, x, t1, workspace=ws)
+    dtree.tree_mask(t1, m1, p1, pos_offset=11)
+    dtree.build_tree_mask(p, x, t2, m2, p2, workspace=ws, pos_offset=11)
+    torch.cuda.synchronize()
+    for f in ("node_tok", "parent", "depth", "rank", "n_nodes", "status"):
+        assert torch.equal(getattr(t1, f), getattr(t2, f)), (mode, f)
+    for b in range(batch):
+        n = int(t1.n_nodes[b])
+        assert torch.equal(m1[b, :n], m2[b, :n]), (mode, b)
+        assert torch.equal(p1[b, :n], p2[b, :n]), (mode, b)
+
+
+def test_fused_mask_single_request_against_oracle():
+    wl = wk.single_request(256)
+    x, _ = wk.draft_logits(wl)
+    p = dtree.Params(mode="ddtree", batch=1, L=16, V=wl.V, dtype="bf16", K=256, B=256)
+    # the oracle side: its own stage 1, tree and mask
+    _, _, ids, lps = oracle.candidates(f32(x[0]), 256)
+    ot = oracle.ddtree(lps, ids, 256, Mmax=257)
+    rc, omask, opos = oracle.tree_mask(ot, 257, 16, pos_offset=5)
+    assert rc == 0
+    # the GPU side: stage 1, selection and the fused mask from the same logits
+    t = dtree.TreeBuffers.for_params(p)
+    m, pp = dtree.alloc_mask(t)
+    dtree.build_tree_mask(p, x.cuda(), t, m, pp, pos_offset=5)
+    torch.cuda.synchronize()
+    g = gpu_tree(t, 0)
+    if near_tie_diff(g, ot.trimmed()) == 0 and np.array_equal(g.parent[:g.n], ot.trimmed().parent[:g.n]):
+        n = g.n
+        assert np.array_equal(m[0, :n].cpu().numpy().view(np.uint32), omask[:n])
+        assert np.array_equal(pp[0, :n].cpu().numpy(), opos[:n])
