@@ -48,6 +48,9 @@ def lib():
         L.or_verify_t1.argtypes = ([_i32p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, _f32p, _f32p, _f32p, ctypes.c_int, _f32p,
                                     _f32p, _i32p, _i32p, _i32p, _f32p])
+        L.or_verify_iter_residual.argtypes = L.or_verify_t1.argtypes
+        L.or_verify_target_match.argtypes = ([_i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              _f32p, ctypes.c_int, _f32p, _f32p, _i32p, _i32p, _i32p, _f32p])
         L.or_spec_scalar.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_double,
                                      ctypes.c_double, ctypes.c_double, _f64p, _f64p, _i32p]
         L.or_spec_scalar_trials.argtypes = [_f64p, _f64p, ctypes.c_int, _f64p,
@@ -231,10 +234,15 @@ def verify_greedy(tree, target, L):
     return acc, int(alen[0]), int(nxt[0])
 
 
-def verify_t1(tree, target, draft, draft_lse, uniforms, L, Mmax, lse_in=None):
+def verify_t1(tree, target, draft, draft_lse, uniforms, L, Mmax, lse_in=None, rule="ratio"):
     """uniforms: [2, Mmax] (row 0: per-child acceptance, row 1: per-node draw);
-    lse_in: optional per-node target normalisers [Mmax].
+    lse_in: optional per-node target normalisers [Mmax];
+    rule: "ratio" (every child against p), "iter_residual" (one residual per
+    rejected sibling) or "target_match" (draw from the target, match a child;
+    draft and draft_lse unused).
     Returns (acc_nodes, acc_len, next_tok, lse_used per step [L+1])."""
+    if rule == "target_match":
+        return verify_target_match(tree, target, uniforms, L, Mmax, lse_in)
     target = _f32(target)
     draft = _f32(draft)
     draft_lse = _f32(draft_lse)
@@ -250,13 +258,38 @@ def verify_t1(tree, target, draft, draft_lse, uniforms, L, Mmax, lse_in=None):
     if lse_in is not None:
         lse_in = _f32(lse_in)
         lin = _p(lse_in, ctypes.c_float)
-    rc = lib().or_verify_t1(_p(tok, ctypes.c_int32), _p(par, ctypes.c_int32),
+    fn = {"ratio": lib().or_verify_t1, "iter_residual": lib().or_verify_iter_residual}[rule]
+    rc = fn(_p(tok, ctypes.c_int32), _p(par, ctypes.c_int32),
                             _p(dep, ctypes.c_int32), _p(rnk, ctypes.c_int32), tree.n, L, Mmax,
                             _p(target, ctypes.c_float), _p(draft, ctypes.c_float),
                             _p(draft_lse, ctypes.c_float), V, _p(u, ctypes.c_float), lin,
                             _p(acc, ctypes.c_int32), _p(alen, ctypes.c_int32),
                             _p(nxt, ctypes.c_int32), _p(lse_out, ctypes.c_float))
-    _check(rc, "verify_t1")
+    _check(rc, "verify_t1 " + rule)
+    return acc, int(alen[0]), int(nxt[0]), lse_out
+
+
+def verify_target_match(tree, target, uniforms, L, Mmax, lse_in=None):
+    """Exact target-sample matching; uniforms [2, Mmax] (row 1 used).
+    Returns (acc_nodes, acc_len, next_tok, lse_used per step [L+1])."""
+    target = _f32(target)
+    u = _f32(uniforms)
+    assert u.shape == (2, Mmax)
+    V = target.shape[-1]
+    acc = np.empty(L + 1, np.int32)
+    alen = np.zeros(1, np.int32)
+    nxt = np.zeros(1, np.int32)
+    lse_out = np.zeros(L + 1, np.float32)
+    tok, par, dep = _i32(tree.tok), _i32(tree.parent), _i32(tree.depth)
+    lin = None
+    if lse_in is not None:
+        lse_in = _f32(lse_in)
+        lin = _p(lse_in, ctypes.c_float)
+    rc = lib().or_verify_target_match(_p(tok, ctypes.c_int32), _p(par, ctypes.c_int32), _p(dep, ctypes.c_int32),
+                                      tree.n, L, Mmax, _p(target, ctypes.c_float), V, _p(u, ctypes.c_float), lin,
+                                      _p(acc, ctypes.c_int32), _p(alen, ctypes.c_int32), _p(nxt, ctypes.c_int32),
+                                      _p(lse_out, ctypes.c_float))
+    _check(rc, "verify_target_match")
     return acc, int(alen[0]), int(nxt[0]), lse_out
 
 

@@ -789,6 +789,173 @@ int or_verify_t1(const int32_t* tok, const int32_t* parent, const int32_t* depth
 }
 
 /* ------------------------------------------------------------------------- */
+/* Tree verification at T=1 with one residual per rejected sibling.            */
+/* [Unit11] residual formula: after drafting y ~ q is rejected, the output is   */
+/* drawn from r = [p - q]_+ / sum [p - q]_+; [DARTree] "Speculative sampling"  */
+/* (the same rule).  The pages state it for one drafted token per position;    */
+/* with several children at a node the plain extension applies it once per     */
+/* rejected child: child c_1 is tested against p, child c_i (i >= 2) against   */
+/* the residual r_{i-1} left by the rejections of c_1 .. c_{i-1}, where         */
+/*   r_0 = p,   r_i = [r_{i-1} - q]_+ / sum [r_{i-1} - q]_+,                    */
+/* and the replacement is drawn from r_k after all k children are rejected.    */
+/* Exact integer form: with P, Q the 2^32 fixed-point masses (as in            */
+/* or_verify_t1), r_i is proportional to                                       */
+/*   W_i(v) = max(0, P(v) - floor(Q(v) * T_i / 2^32)),                          */
+/*   T_1 = 2^32 (the nominal mass of P),  T_{i+1} = T_i + S_i,  S_i = sum W_i,  */
+/* since subtracting S_i * q from [P - T_i q]_+ and clamping at zero equals     */
+/* [P - (T_i + S_i) q]_+.  Child c_1 takes or_verify_t1's test; child c_i       */
+/* (i >= 2) is accepted iff floor(u * 2^24) * Q(c) * S_{i-1}                    */
+/*   < W_{i-1}(c) * 2^56, i.e. u < r_{i-1}(c) / q(c) in exact integers.         */
+/* When a residual is empty (S_i = 0) the remaining children are not tested    */
+/* and the draw is from P, as in or_verify_t1.  With one child per node this   */
+/* is or_verify_t1 exactly.  The draw uses or_draw with uniforms[1][n].        */
+/* Pinned: equals or_verify_t1 on single-child trees; with the children's      */
+/* tokens drawn i.i.d. from q the emitted first token follows p (frequency     */
+/* test), the losslessness of the iterated rule for sampled candidates (tests). */
+/* ------------------------------------------------------------------------- */
+static uint64_t or_qscale(uint64_t Q, uint64_t T)
+{
+    return (uint64_t)(((unsigned __int128)Q * (unsigned __int128)T) >> 32);
+}
+
+static uint64_t or_resid_w(uint64_t P, uint64_t Q, uint64_t T)
+{
+    uint64_t s = or_qscale(Q, T);
+    return P > s ? P - s : 0;
+}
+
+static int or_accept_resid(float u, uint64_t Q, uint64_t S, uint64_t W)
+{
+    float xf = u * 16777216.0f;
+    uint64_t X = (uint64_t)xf;
+    if (X > 16777215u) X = 16777215u;
+    unsigned __int128 lhs = (unsigned __int128)(X * Q) * (unsigned __int128)S;
+    unsigned __int128 rhs = (unsigned __int128)W << 56;
+    return lhs < rhs;
+}
+
+int or_verify_iter_residual(const int32_t* tok, const int32_t* parent, const int32_t* depth,
+                            const int32_t* rank, int M, int L, int Mmax,
+                            const float* target, const float* draft, const float* draft_lse,
+                            int V, const float* u, const float* lse_in,
+                            int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                            float* lse_out)
+{
+    if (!or_tree_valid(parent, depth, M, L)) return OR_EBADTREE;
+    uint64_t* w = (uint64_t*)malloc((size_t)V * sizeof(uint64_t));
+    uint64_t* P = (uint64_t*)malloc((size_t)V * sizeof(uint64_t));
+    uint64_t* Q = (uint64_t*)malloc((size_t)V * sizeof(uint64_t));
+    int* kids = (int*)malloc((size_t)M * sizeof(int));
+    if (!w || !P || !Q || !kids) { free(w); free(P); free(Q); free(kids); return OR_ENOMEM; }
+    for (int i = 0; i <= L; ++i) { acc_nodes[i] = -1; if (lse_out) lse_out[i] = 0.0f; }
+    int n = 0, len = 0, out = -1;
+    acc_nodes[0] = 0;
+    for (;;) {
+        const float* trow = target + (int64_t)n * V;
+        float lse_t = lse_in ? lse_in[n] : or_row_lse(trow, V);
+        if (lse_out) lse_out[len] = lse_t;
+        int nk = 0;
+        for (int c = 1; c < M; ++c)
+            if (parent[c] == n) {
+                int j = nk++;
+                while (j > 0 && rank[kids[j - 1]] > rank[c]) { kids[j] = kids[j - 1]; --j; }
+                kids[j] = c;
+            }
+        int acc = -1;
+        uint64_t S = 0;
+        if (nk > 0) {
+            int pos = depth[n]; /* the children's position */
+            const float* drow = draft + (int64_t)pos * V;
+            float lsed = draft_lse[pos];
+            for (int v = 0; v < V; ++v) {
+                P[v] = or_fixed32(or_exp_canon(trow[v] - lse_t));
+                Q[v] = or_fixed32(or_exp_canon(drow[v] - lsed));
+            }
+            /* c_1 against p */
+            int c = kids[0];
+            float lpt = trow[tok[c]] - lse_t;
+            float lpq = drow[tok[c]] - lsed;
+            if (u[c] < or_exp_canon(lpt - lpq)) acc = c;
+            /* c_2 .. c_k against the residuals */
+            uint64_t T = (uint64_t)1 << 32;
+            for (int i = 1; acc < 0; ++i) {
+                S = 0;
+                for (int v = 0; v < V; ++v) { w[v] = or_resid_w(P[v], Q[v], T); S += w[v]; }
+                if (i == nk || S == 0) break;
+                c = kids[i];
+                if (or_accept_resid(u[c], Q[tok[c]], S, w[tok[c]])) acc = c;
+                else T += S;
+            }
+        }
+        if (acc >= 0 && len < L) {
+            acc_nodes[++len] = acc;
+            n = acc;
+            continue;
+        }
+        if (S == 0) {
+            for (int v = 0; v < V; ++v) {
+                w[v] = or_fixed32(or_exp_canon(trow[v] - lse_t));
+                S += w[v];
+            }
+        }
+        out = or_draw(w, V, S, u[Mmax + n]);
+        break;
+    }
+    *acc_len = len;
+    *next_tok = out;
+    free(w); free(P); free(Q); free(kids);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Tree verification at T=1 by exact target-sample matching.                   */
+/* [DARTree] "Speculative sampling": some systems (DFlash) do not run the       */
+/* rejection procedure and instead match a sample of the target against the    */
+/* draft.  On a tree: at node n draw y from the target row of n (P, the 2^32    */
+/* fixed-point masses, or_draw with uniforms[1][n]); if a child of n carries    */
+/* token y, accept it and continue from it; otherwise emit y.  A node without   */
+/* children emits its draw as the bonus token.  Every emitted token is a       */
+/* target sample given the accepted prefix, so the output follows the target   */
+/* distribution whatever the tree.  The drafter rows are not used.              */
+/* Pinned: the emitted first token follows p (frequency test); with one-hot     */
+/* target rows it is the greedy walk (tests).                                   */
+/* ------------------------------------------------------------------------- */
+int or_verify_target_match(const int32_t* tok, const int32_t* parent, const int32_t* depth,
+                           int M, int L, int Mmax, const float* target, int V,
+                           const float* u, const float* lse_in,
+                           int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                           float* lse_out)
+{
+    if (!or_tree_valid(parent, depth, M, L)) return OR_EBADTREE;
+    uint64_t* w = (uint64_t*)malloc((size_t)V * sizeof(uint64_t));
+    if (!w) return OR_ENOMEM;
+    for (int i = 0; i <= L; ++i) { acc_nodes[i] = -1; if (lse_out) lse_out[i] = 0.0f; }
+    int n = 0, len = 0, y = -1;
+    acc_nodes[0] = 0;
+    for (;;) {
+        const float* trow = target + (int64_t)n * V;
+        float lse_t = lse_in ? lse_in[n] : or_row_lse(trow, V);
+        if (lse_out) lse_out[len] = lse_t;
+        uint64_t S = 0;
+        for (int v = 0; v < V; ++v) {
+            w[v] = or_fixed32(or_exp_canon(trow[v] - lse_t));
+            S += w[v];
+        }
+        y = or_draw(w, V, S, u[Mmax + n]);
+        int child = -1;
+        for (int c = 1; c < M && child < 0; ++c)
+            if (parent[c] == n && tok[c] == y) child = c;
+        if (child < 0 || len >= L) break;
+        acc_nodes[++len] = child;
+        n = child;
+    }
+    *acc_len = len;
+    *next_tok = y;
+    free(w);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Single-position speculative sampling in double precision, the scalar rule   */
 /* the tree walk generalises.  [Unit11] worked three-token example and its     */
 /* probability-tree / histogram proofs; [DARTree] "Speculative sampling".      */
