@@ -39,6 +39,12 @@ def lib():
                                  [_f32p, _i32p, _i32p, _i32p])
         L.or_markov_norm.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _f32p, _f32p,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p]
+        L.or_markov_table.argtypes = [_i32p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, ctypes.c_int,
+                                      ctypes.c_int, _f32p]
+        L.or_tdes_table.argtypes = [_i32p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, _f32p, _f32p, ctypes.c_int,
+                                    ctypes.c_float, ctypes.c_float, ctypes.c_int, _f32p]
+        L.or_heap_select.argtypes = ([_f32p, _i32p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, ctypes.c_int,
+                                      ctypes.c_int] + [_i32p] * 4 + [_f32p, _i32p])
         L.or_talon.argtypes = ([_f32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_float, ctypes.c_int, ctypes.c_int] + [_i32p] * 4 +
                                [_f32p, _i32p])
@@ -173,6 +179,54 @@ def dartree(cand_lp, cand_id, U, Vt, root_tok, W, beta, B, Mmax=None, znorm=None
     t.n = int(n[0])
     return t, dict(topb_equals_bestfirst=bool(info[0]), violations=int(info[1]),
                    supertree_size=int(info[2])), topb
+
+
+def markov_table(cand_id, U, Vt, root_tok):
+    """[L, K, K] Markov edge terms <U[parent], Vt[child]> on the candidate lattice
+    (row 0 of position 0: the root token; zeros when root_tok < 0)."""
+    ids = _i32(cand_id)
+    L, K = ids.shape
+    U, Vt = _f32(U), _f32(Vt)
+    E = np.empty((L, K, K), np.float32)
+    _check(lib().or_markov_table(_p(ids, ctypes.c_int32), L, K, _p(U, ctypes.c_float), _p(Vt, ctypes.c_float),
+                                 U.shape[1], int(root_tok), _p(E, ctypes.c_float)), "markov_table")
+    return E
+
+
+def tdes_table(cand_id, Ap, Ac, Dd, w, b0, s, root_tok):
+    """[L, K, K] TDES edge terms s * f(parent, child, depth) on the candidate lattice.
+    Ap, Ac: [V, H] per-token first-layer rows; Dd: [L, H] depth rows (bias included); w: [H]."""
+    ids = _i32(cand_id)
+    L, K = ids.shape
+    Ap, Ac, Dd, w = _f32(Ap), _f32(Ac), _f32(Dd), _f32(w)
+    H = w.shape[0]
+    E = np.empty((L, K, K), np.float32)
+    _check(lib().or_tdes_table(_p(ids, ctypes.c_int32), L, K, _p(Ap, ctypes.c_float), _p(Ac, ctypes.c_float),
+                               _p(Dd, ctypes.c_float), _p(w, ctypes.c_float), H, ctypes.c_float(b0),
+                               ctypes.c_float(s), int(root_tok), _p(E, ctypes.c_float)), "tdes_table")
+    return E
+
+
+def heap_select(cand_lp, cand_id, B, E=None, znorm=None, Mmax=None):
+    """Best-first heap with parent-conditioned edge scores lp + E (- znorm);
+    E: [L, K, K] from markov_table / tdes_table, or None (DDTree)."""
+    lp = _f32(cand_lp)
+    ids = _i32(cand_id)
+    L, K = lp.shape
+    Ep = zp = None
+    if E is not None:
+        E = _f32(E).reshape(L, K, K)
+        Ep = _p(E, ctypes.c_float)
+    if znorm is not None:
+        znorm = _f32(znorm).reshape(L, K)
+        zp = _p(znorm, ctypes.c_float)
+    Mmax = Mmax or B + 1
+    t = _new_tree(Mmax)
+    n = np.zeros(1, np.int32)
+    _check(lib().or_heap_select(_p(lp, ctypes.c_float), _p(ids, ctypes.c_int32), L, K, Ep, zp, B, Mmax,
+                                *_tree_args(t), _p(n, ctypes.c_int32)), "heap_select")
+    t.n = int(n[0])
+    return t
 
 
 def markov_norm(x, cand_id, U, Vt, root_tok, only_row=-1, out=None):

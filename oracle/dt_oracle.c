@@ -493,6 +493,171 @@ int or_markov_norm(const float* x /* [L][V] */, int L, int V, const int32_t* id 
 }
 
 /* ------------------------------------------------------------------------- */
+/* Parent-conditioned edge terms on the candidate lattice.                     */
+/* E[d][i][j] is the term of the edge from candidate i of position d-1 (the    */
+/* parent's token) to candidate j of position d; row 0 of position 0 belongs   */
+/* to the root, whose token is root_tok (all zeros when root_tok < 0: no term). */
+/* or_markov_table: [DARTree] "Causal correction" (Markov head <U[p], Vt[c]>), */
+/* the serial fmaf chain of or_markov.                                         */
+/* or_tdes_table: [GRAFT] "Target-distilled edge scoring", the edge scorer     */
+/* f(p, c, d) = w . ReLU(W [g_p(e_p); g_c(e_c); e_d] + b) + b0 with its        */
+/* learned scale s.  The projections depend on the token only ("computed once  */
+/* and reused"), and so does the first layer's product with them, so the       */
+/* inputs are the per-token rows Ap[v] = W_p g_p(e_v), Ac[v] = W_c g_c(e_v)    */
+/* ([V][H]) and the per-depth row Dd[d-1] = W_d e_d + b ([L][H]).  In fp32:     */
+/* a = (Ap[p][h] + Ac[c][h]) + Dd[d-1][h], r = max(a, 0), acc = fmaf(w[h], r,  */
+/* acc) from 0 over h, E = s * (acc + b0).  The edge score of the tree builder */
+/* is then lp + E (the page's training target softmax(log q + f) and its      */
+/* inference path score, a sum of edge scores).                               */
+/* Pinned: hand-computed two-unit edges, the ReLU cut, a float64 restatement   */
+/* within rounding (tests).                                                    */
+/* ------------------------------------------------------------------------- */
+int or_markov_table(const int32_t* id, int L, int K, const float* U, const float* Vt, int R, int root_tok,
+                    float* E /* [L][K][K] */)
+{
+    if (L < 1 || L > OR_MAXL || K < 1 || R < 1 || !U || !Vt || !E) return OR_EINVAL;
+    memset(E, 0, sizeof(float) * (size_t)L * K * K);
+    for (int d = 0; d < L; ++d) {
+        int np = d == 0 ? (root_tok >= 0 ? 1 : 0) : K;
+        for (int i = 0; i < np; ++i) {
+            int ptok = d == 0 ? root_tok : id[(d - 1) * K + i];
+            for (int j = 0; j < K; ++j)
+                E[((int64_t)d * K + i) * K + j] = or_markov(U, Vt, R, ptok, id[d * K + j]);
+        }
+    }
+    return OR_OK;
+}
+
+int or_tdes_table(const int32_t* id, int L, int K, const float* Ap, const float* Ac, const float* Dd,
+                  const float* w, int H, float b0, float s, int root_tok, float* E /* [L][K][K] */)
+{
+    if (L < 1 || L > OR_MAXL || K < 1 || H < 1 || !Ap || !Ac || !Dd || !w || !E) return OR_EINVAL;
+    memset(E, 0, sizeof(float) * (size_t)L * K * K);
+    for (int d = 0; d < L; ++d) {
+        int np = d == 0 ? (root_tok >= 0 ? 1 : 0) : K;
+        for (int i = 0; i < np; ++i) {
+            int ptok = d == 0 ? root_tok : id[(d - 1) * K + i];
+            for (int j = 0; j < K; ++j) {
+                int ctok = id[d * K + j];
+                float acc = 0.0f;
+                for (int h = 0; h < H; ++h) {
+                    float a = Ap[(int64_t)ptok * H + h] + Ac[(int64_t)ctok * H + h];
+                    a = a + Dd[(int64_t)d * H + h];
+                    float r = a > 0.0f ? a : 0.0f;
+                    acc = fmaf(w[h], r, acc);
+                }
+                E[((int64_t)d * K + i) * K + j] = s * (acc + b0);
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Best-first heap with parent-conditioned edge scores.                        */
+/* [DARTree] tree-construction ablation (Table 2): "sequential correction with */
+/* heap" alternates the correction of a popped node's children with heap      */
+/* updates; [GRAFT] "Inference": prefixes ordered in a max-heap by the sum of  */
+/* their edge scores, the best one added to the tree until the budget is met. */
+/* Edge score of child j (position d) under parent u (candidate i of position  */
+/* d-1, or the root at d = 1): t = lp_d[j] + E[d-1][i][j], then minus           */
+/* znorm[d-1][i] when given (the normalised DARTree correction), in fp32; the   */
+/* path score adds t to the parent's score.  The children of u in the order    */
+/* (t desc, j asc) play the part of DDTree's ranks: each pop adds the node,    */
+/* pushes its first child (below depth L) and its next sibling in its parent's */
+/* order.  Heap order: score desc, then the descriptor of order positions      */
+/* lexicographically (a prefix first), as in or_ddtree.  Nodes are output in   */
+/* pop order (parents before children); rank = the node's candidate rank.     */
+/* B counts non-root nodes.  With E = NULL (and no znorm) this is or_ddtree.   */
+/* Pinned: reduction to or_ddtree, brute force over every prefix of tiny       */
+/* lattices with non-positive edge scores, the best-first invariant with       */
+/* arbitrary signs, and DARTree without width pruning (tests).                 */
+/* ------------------------------------------------------------------------- */
+static const float* or_hs_lp;
+static const float* or_hs_E;
+static const float* or_hs_z;
+static int or_hs_K, or_hs_i, or_hs_d;
+
+static float or_hs_edge(int d, int i, int j) /* d: 1-based position of the child */
+{
+    int K = or_hs_K;
+    float t = or_hs_lp[(d - 1) * K + j];
+    if (or_hs_E) t = t + or_hs_E[((int64_t)(d - 1) * K + i) * K + j];
+    if (or_hs_z) t = t - or_hs_z[(d - 1) * K + i];
+    return t;
+}
+
+static int or_hs_cmp(const void* pa, const void* pb)
+{
+    int a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+    float ta = or_hs_edge(or_hs_d, or_hs_i, a), tb = or_hs_edge(or_hs_d, or_hs_i, b);
+    if (ta > tb) return -1;
+    if (ta < tb) return 1;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+/* the children of candidate i of position d-1 (i = 0 for the root at d = 1) in edge order */
+static void or_hs_order(int d, int i, int K, int32_t* ord)
+{
+    for (int j = 0; j < K; ++j) ord[j] = j;
+    or_hs_d = d; or_hs_i = i; or_hs_K = K;
+    qsort(ord, (size_t)K, sizeof(int32_t), or_hs_cmp);
+}
+
+int or_heap_select(const float* lp, const int32_t* id, int L, int K,
+                   const float* E /* nullable [L][K][K] */, const float* znorm /* nullable [L][K] */,
+                   int B, int Mmax, int32_t* tok, int32_t* parent, int32_t* depth,
+                   int32_t* rank, float* score, int32_t* n_nodes)
+{
+    if (L < 1 || L > OR_MAXL || K < 1 || B < 1 || Mmax < 1) return OR_EINVAL;
+    or_tree_out o = { tok, parent, depth, rank, score };
+    or_put_root(&o);
+    or_hs_lp = lp; or_hs_E = E; or_hs_z = znorm; or_hs_K = K;
+    /* child order of each emitted node (row of its node index), K entries */
+    int32_t* ord = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B + 1) * K);
+    int32_t* crank = (int32_t*)calloc((size_t)B + 1, sizeof(int32_t)); /* candidate rank per node */
+    or_heap h = { 0, 0, 0 };
+    if (!ord || !crank) { free(ord); free(crank); return OR_ENOMEM; }
+    crank[0] = 0; /* the root's edge row */
+    or_hs_order(1, 0, K, ord);
+    or_node first;
+    memset(&first, 0, sizeof first);
+    first.d = 1; first.r[0] = 0; first.parent = 0;
+    first.s = 0.0f + or_hs_edge(1, 0, ord[0]);
+    int rc = or_heap_push(&h, &first);
+    int n = 0;
+    while (rc == OR_OK && n < B && h.n > 0) {
+        or_node x = or_heap_pop(&h);
+        int p = x.parent, jpos = x.r[x.d - 1];
+        int c = ord[(size_t)p * K + jpos]; /* candidate rank at position x.d */
+        ++n;
+        if (n >= Mmax) { rc = OR_EINVAL; break; }
+        tok[n] = id[(x.d - 1) * K + c];
+        parent[n] = p;
+        depth[n] = x.d;
+        rank[n] = c;
+        score[n] = x.s;
+        crank[n] = c;
+        if (x.d < L) {
+            or_hs_order(x.d + 1, c, K, ord + (size_t)n * K);
+            or_node ch = x;
+            ch.d = x.d + 1; ch.r[x.d] = 0; ch.parent = n;
+            ch.s = x.s + or_hs_edge(ch.d, c, ord[(size_t)n * K]);
+            rc = or_heap_push(&h, &ch);
+        }
+        if (rc == OR_OK && jpos + 1 < K) {
+            or_node sib = x;
+            sib.r[x.d - 1] = jpos + 1;
+            sib.s = score[p] + or_hs_edge(x.d, crank[p], ord[(size_t)p * K + jpos + 1]);
+            rc = or_heap_push(&h, &sib);
+        }
+    }
+    *n_nodes = n + 1;
+    free(ord); free(crank); free(h.a);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
 /* TALON budgeted, confidence-gated expansion.                                 */
 /* [TALON] "Key designs" 1 (root layer keeps the Top-k children regardless of  */
 /* confidence, k = 10 by default) and 2 (pool = children of every node of the  */
