@@ -69,6 +69,8 @@ def workloads():
         "stochastic_b1": wk.stochastic_batch(1),
         "stochastic_b4": wk.stochastic_batch(4),
         "stochastic_b16": wk.stochastic_batch(16),
+        "stochastic_iter_residual_b16": wk.stochastic_rule(16, "iter_residual"),
+        "stochastic_target_match_b16": wk.stochastic_rule(16, "target_match"),
         "dartree_beta0": wk.dartree_supertree(0.0),
         "dartree_beta-0.5": wk.dartree_supertree(-0.5),
         "dartree_norm_beta0": wk.dartree_normalised(0.0),
@@ -246,8 +248,9 @@ def run_ours(args, wl, rank, world, local):
         if "mask" in stages:
             dtree.tree_mask(c["tree"], c["mask"], c["pos"])
         if "verify" in stages:
-            dtree.verify(c["tree"], c["tgt"], temperature=temperature, draft=c["x"] if temperature else None,
-                         uniforms=c["uni"], out=c["out"])
+            dtree.verify(c["tree"], c["tgt"], temperature=temperature,
+                         draft=c["x"] if temperature and wl.verify_rule != "target_match" else None,
+                         uniforms=c["uni"], out=c["out"], rule=wl.verify_rule or None)
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -395,6 +398,7 @@ def run_ours(args, wl, rank, world, local):
         "data": "synthetic (seeded Gaussian logits with confident-token spikes; Qwen3 vocabulary)",
         "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch, "L": wl.L, "V": wl.V,
                    "K": wl.K, "B": wl.B, "W": wl.W, "beta": wl.beta, "N": wl.N, "temperature": temperature,
+                   "verify_rule": wl.verify_rule or ("ratio" if temperature else "greedy"),
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d input copies (drafter logits %.0f MB > 2x L2)" % (R, R * draft_bytes / 1e6)},
         "roofline": {"bound": "hbm", "kernel": kn1_desc, "achieved": achieved, "peak": peak,
@@ -430,7 +434,7 @@ def oracle_round(wl, x, tgt, uni, U, Vt):
     if tgt is None:
         return t
     if wl.temperature == 1.0:
-        oracle.verify_t1(t, tgt, x, l32, uni, wl.L, Mmax)
+        oracle.verify_t1(t, tgt, x, l32, uni, wl.L, Mmax, rule=wl.verify_rule or "ratio")
     else:
         oracle.verify_greedy(t, tgt, wl.L)
     return t

@@ -57,7 +57,25 @@ typedef enum {
     DT_ERR_CUDA = -4,        /* a CUDA launch or attribute call failed */
 } dt_status;
 
-enum { DT_MODE_DDTREE = 0, DT_MODE_DARTREE = 1, DT_MODE_TALON = 2 };
+enum { DT_MODE_DDTREE = 0, DT_MODE_DARTREE = 1, DT_MODE_TALON = 2, DT_MODE_HEAP = 3 };
+
+/* TDES edge scorer ([GRAFT] "Target-distilled edge scoring"):
+ *   f(p, c, d) = w . ReLU(W [g_p(e_p); g_c(e_c); e_d] + b) + b0,  term = s * f.
+ * The token projections are fixed per token ("computed once and reused"), so
+ * the scorer is given by the first layer's per-token and per-depth parts:
+ *   Ap[v] = W_p g_p(e_v), Ac[v] = W_c g_c(e_v)  ([V][H] fp32),
+ *   Dd[d-1] = W_d e_d + b                         ([L][H] fp32),
+ * and per edge, in fp32: a = (Ap[p][h] + Ac[c][h]) + Dd[d-1][h],
+ * r = max(a, 0), acc = fma(w[h], r, acc) from 0 over h, term = s * (acc + b0). */
+typedef struct {
+    int32_t H;          /* hidden units, 1..4096 */
+    const float* Ap;    /* [V][H] parent-token rows */
+    const float* Ac;    /* [V][H] child-token rows */
+    const float* Dd;    /* [L][H] depth rows (bias included) */
+    const float* w;     /* [H] output weights */
+    float b0;           /* output bias */
+    float s;            /* scale */
+} dt_tdes;
 enum { DT_BF16 = 0, DT_F32 = 1 };
 
 #define DT_MAX_L 32
@@ -102,12 +120,15 @@ typedef struct {
     int32_t talon_k;    /* TALON root-layer Top-k, 1..N */
     float log_mu;       /* TALON log(mu) rounded to fp32, mu in (0, 1] */
     int32_t N;          /* TALON node budget, 1..1024 */
-    int32_t markov_norm; /* DARTree with R > 0: 1 = normalise the corrected
+    int32_t markov_norm; /* DARTree (or HEAP with the Markov term) with R > 0:
+                           1 = normalise the corrected
                            distribution over the full vocabulary ([DARTree]
                            "Causal correction": q~ is a probability), i.e.
                            log q~ = (lp + <U, Vt>) - log Z_d(parent token),
                            see dt_markov_norm; needs R = 64 and 16-byte
                            aligned U, Vt.  0 = the unnormalised term. */
+    const dt_tdes* tdes; /* DT_MODE_HEAP: TDES edge scorer, or NULL (then the
+                           Markov term when R > 0, else no edge term) */
 } dt_build_params;
 
 /* Tree buffers (caller-owned device memory).  Node 0 of each request is the
@@ -133,8 +154,9 @@ typedef struct {
 } dt_tree;
 
 /* Bytes of caller-provided device workspace dt_build_tree / dt_select need
- * for these parameters (0 for DDTree and TALON; DARTree with R > 0: the
- * per-request Markov table, batch*L*K*K*4 bytes, rounded up to 256; with
+ * for these parameters (0 for DDTree and TALON; DARTree with R > 0, and HEAP
+ * with an edge term: the per-request edge table, batch*L*K*K*4 bytes,
+ * rounded up to 256; with
  * markov_norm also the log-normaliser table, batch*L*K*4 bytes rounded up to
  * 256, at byte offset DT_ZNORM_OFFSET(p) = the rounded Markov table size,
  * then scratch for dt_markov_norm).  Returns 0 and sets *ok = 0 on invalid
@@ -183,6 +205,18 @@ dt_status dt_stage1_plan(const dt_build_params* p, int32_t* kernel, int32_t* clu
  *  TALON ([TALON] key designs 1-2): root layer = Top-talon_k of position 1;
  *   then pool the children of the last layer, keep s >= max_pool + log_mu,
  *   truncate to the best N - |T| and stop on overflow; at most L layers.
+ *  HEAP ([DARTree] tree-construction ablation, "sequential correction with
+ *   heap"; [GRAFT] "Inference", TDES path scores in a max-heap): best-first
+ *   over prefixes with a parent-conditioned edge score
+ *   t = lp + E(parent token, child token, depth) (minus log Z with
+ *   markov_norm), E the Markov term <U, Vt> (R > 0, tdes NULL), the TDES term
+ *   (tdes), or none (then the DDTree result); the children of a parent are
+ *   taken in (t desc, rank asc) order, each pop adds the best prefix (score
+ *   desc, then its descriptor of order positions) and pushes its first child
+ *   and next sibling; B pops.  Nodes are in pop order, parents first; a child
+ *   may outscore its parent.  No width limit, unlike DARTree.  Needs K <= 256
+ *   and the order tables within shared memory (else DT_ERR_UNSUPPORTED);
+ *   dt_select_mask writes the mask with the mask kernel afterwards.
  * workspace: device memory of dt_workspace_size(p) bytes (may be NULL when 0). */
 dt_status dt_select(const dt_build_params* p, dt_tree* tree, void* workspace,
                     size_t workspace_bytes, dt_stream_t stream);
@@ -267,6 +301,42 @@ dt_status dt_verify(const dt_tree* tree, int32_t batch, int32_t V, int32_t dtype
                     const void* draft_logits, float temperature, const float* uniforms,
                     int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
                     float* visited_lse, dt_stream_t stream);
+
+/* Acceptance walk with an explicit rule.  dt_verify(temperature 0) is
+ * DT_VERIFY_GREEDY and dt_verify(temperature 1) is DT_VERIFY_RATIO; the pages
+ * state the T=1 rule for one drafted token per position and leave several
+ * children per node open, so two more readings are offered:
+ *  DT_VERIFY_ITER_RESIDUAL ([Unit11] residual formula applied once per
+ *   rejected sibling; [DARTree] "Speculative sampling"): child c_1 of n is
+ *   tested as in DT_VERIFY_RATIO; child c_i (i >= 2, rank order) against the
+ *   residual r_{i-1} left by rejecting c_1 .. c_{i-1}, r_i = [r_{i-1} - q]_+
+ *   normalised, held exactly as the integer weights
+ *   W_i = max(0, P - floor(Q * T_i / 2^32)), T_1 = 2^32,
+ *   T_{i+1} = T_i + sum_v W_i(v); c_i is accepted iff
+ *   floor(u * 2^24) * Q(c_i) * S_{i-1} < W_{i-1}(c_i) * 2^56 (S = sum W).  After
+ *   all children are rejected the replacement is drawn from the last residual
+ *   (from P when a residual is empty, and then no further child is tested).
+ *   With one child per node this is DT_VERIFY_RATIO.  With children drawn
+ *   i.i.d. from q it preserves the target distribution; with deterministic
+ *   Top-K children neither this nor DT_VERIFY_RATIO is claimed to.  Cost: one
+ *   pass over the row per rejected child after the first.
+ *  DT_VERIFY_TARGET_MATCH ([DARTree] "Speculative sampling": DFlash's exact
+ *   target-sample matching): at each visited node n draw y from P (row n) by
+ *   inverse CDF with uniforms[b][1][n]; if a child of n has token y descend
+ *   into it, else emit y.  Distribution-preserving for any tree.
+ *   draft_logits, tree->lse and uniforms[b][0][*] are not read (draft_logits
+ *   may be NULL).
+ * Other arguments and outputs as for dt_verify; target_lse and uniforms apply
+ * to every T=1 rule.  Returns DT_ERR_INVALID_ARG for an unknown rule. */
+#define DT_VERIFY_GREEDY 0
+#define DT_VERIFY_RATIO 1
+#define DT_VERIFY_ITER_RESIDUAL 2
+#define DT_VERIFY_TARGET_MATCH 3
+dt_status dt_verify_rule(const dt_tree* tree, int32_t batch, int32_t V, int32_t dtype,
+                         const void* target_logits, const float* target_lse,
+                         const void* draft_logits, int32_t rule, const float* uniforms,
+                         int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                         float* visited_lse, dt_stream_t stream);
 
 /* Allocation-free DARTree selection.  The pages have no counterpart: this is
  * a service to callers that cannot allocate device memory -- e.g. a serving

@@ -26,8 +26,8 @@ int chunk_of(int V, int S, int dtype) {
 }
 
 // Clusters of S CTAs that the device holds at once for stage 1 (kind 1,
-// extra = Kc) or the verification walk (kind 6, extra = max_nodes) with these
-// sizes; cached per device.
+// extra = Kc) or the verification walk (kind 6, extra = 4 * max_nodes + rule)
+// with these sizes; cached per device.
 int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
     struct Fit {
         int dev, kind, dtype, S, chunk, extra, n;
@@ -46,7 +46,8 @@ int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
         if (f.dev == dev && f.kind == kind && f.dtype == dtype && f.S == S && f.chunk == chunk && f.extra == extra)
             return f.n;
     }
-    const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra) : dt_kn6_max_clusters(dtype, S, chunk, extra);
+    const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra)
+                            : dt_kn6_max_clusters(dtype, S, chunk, extra >> 2, extra & 3);
     if (n > 0 && nfit < 128) fits[nfit++] = Fit{dev, kind, dtype, S, chunk, extra, n};
     return n;
 }
@@ -109,9 +110,17 @@ int kc_of(const dt_build_params* p) {
 
 int budget_of(const dt_build_params* p) { return p->mode == DT_MODE_TALON ? p->N : p->B; }
 
+// The Markov term <U, Vt> is on: DARTree, or the heap without a TDES scorer.
+bool markov_on(const dt_build_params* p) {
+    return (p->mode == DT_MODE_DARTREE || (p->mode == DT_MODE_HEAP && !p->tdes)) && p->R > 0 && p->U;
+}
+
+// A per-request edge table lives in the workspace.
+bool table_on(const dt_build_params* p) { return markov_on(p) || (p->mode == DT_MODE_HEAP && p->tdes); }
+
 dt_status check_build(const dt_build_params* p, const dt_tree* t) {
     if (!p || !t) return DT_ERR_INVALID_ARG;
-    if (p->mode < DT_MODE_DDTREE || p->mode > DT_MODE_TALON) return DT_ERR_INVALID_ARG;
+    if (p->mode < DT_MODE_DDTREE || p->mode > DT_MODE_HEAP) return DT_ERR_INVALID_ARG;
     if (p->batch < 1 || p->L < 1 || p->L > DT_MAX_L || p->V < 1) return DT_ERR_INVALID_ARG;
     if (p->V > DT_MAX_V) return DT_ERR_UNSUPPORTED;
     if (p->dtype != DT_BF16 && p->dtype != DT_F32) return DT_ERR_INVALID_ARG;
@@ -136,6 +145,23 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
         if (p->markov_norm && p->R != 64) return DT_ERR_UNSUPPORTED;           // tensor-core tile: R = 64
         if (p->markov_norm && ((((uintptr_t)p->U) | ((uintptr_t)p->Vt)) & 15u)) return DT_ERR_INVALID_ARG;
         if (dt_kn3_select_smem_bytes(p->L, p->K, p->W, p->R > 0 && p->U) > kSmemMax) return DT_ERR_UNSUPPORTED;
+    }
+    if (p->mode == DT_MODE_HEAP) {
+        if (p->K > 256) return DT_ERR_UNSUPPORTED;
+        if (p->markov_norm != 0 && p->markov_norm != 1) return DT_ERR_INVALID_ARG;
+        if (p->tdes) {
+            const dt_tdes* q = p->tdes;
+            if (q->H < 1 || q->H > 4096 || !q->Ap || !q->Ac || !q->Dd || !q->w) return DT_ERR_INVALID_ARG;
+            if (p->markov_norm) return DT_ERR_INVALID_ARG;  // the normaliser is the Markov term's
+            if (dt_kn8_smem_bytes(p->K, q->H) > kSmemMax) return DT_ERR_UNSUPPORTED;
+        } else {
+            if (p->R < 0 || p->R > 1024) return DT_ERR_INVALID_ARG;
+            if (p->R > 0 && (!p->U || !p->Vt)) return DT_ERR_INVALID_ARG;
+            if (p->R > 0 && dt_kn3_table_smem_bytes(p->K, p->R) > kSmemMax) return DT_ERR_UNSUPPORTED;
+            if (p->markov_norm && (p->R == 0 || !p->U)) return DT_ERR_INVALID_ARG;
+            if (p->markov_norm && p->R != 64) return DT_ERR_UNSUPPORTED;
+            if (p->markov_norm && ((((uintptr_t)p->U) | ((uintptr_t)p->Vt)) & 15u)) return DT_ERR_INVALID_ARG;
+        }
     }
     if (t->Kc != kc_of(p)) return DT_ERR_INVALID_ARG;
     if (t->L != p->L) return DT_ERR_INVALID_ARG;
@@ -190,9 +216,10 @@ size_t dt_workspace_size(const dt_build_params* p, int* ok) {
         if (ok) *ok = 0;
         return 0;
     }
-    if (p->mode == DT_MODE_DARTREE && p->R > 0 && p->U) {
+    if (table_on(p)) {
         size_t n = DT_ZNORM_OFFSET(p);
-        if (p->markov_norm) n += znorm_bytes(p) + dt_kn3n_scratch_bytes(p->batch * p->L * p->K, p->V);
+        if (markov_on(p) && p->markov_norm)
+            n += znorm_bytes(p) + dt_kn3n_scratch_bytes(p->batch * p->L * p->K, p->V);
         return n;
     }
     return 0;
@@ -241,7 +268,7 @@ static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspa
     if (s != DT_OK) return s;
     cudaError_t e = cudaSuccess;
     const int Mmax = t->max_nodes;
-    const bool fuse = mask_out && Mmax <= kFusedMaskMaxNodes;
+    const bool fuse = mask_out && Mmax <= kFusedMaskMaxNodes && p->mode != DT_MODE_HEAP;
     uint32_t* mask = fuse ? mask_out : nullptr;
     int32_t* pos = fuse ? pos_out : nullptr;
     switch (p->mode) {
@@ -260,6 +287,28 @@ static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspa
                               Mmax, t->cand_lp, t->cand_id, t->lse, term ? (float*)workspace : nullptr, znorm,
                               t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, mask, pos,
                               pos_offset, st);
+            break;
+        }
+        case DT_MODE_HEAP: {
+            const size_t need = dt_workspace_size(p, nullptr);
+            if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
+            if (dt_kn7_smem_bytes(p->L, p->K, p->B, Mmax) > kSmemMax) return DT_ERR_UNSUPPORTED;
+            float* table = table_on(p) ? (float*)workspace : nullptr;
+            if (p->tdes) {
+                const dt_tdes* q = p->tdes;
+                e = dt_kn8_launch(p->batch, p->L, p->V, p->K, q->H, q->Ap, q->Ac, q->Dd, q->w, q->b0, q->s,
+                                  p->root_tok, t->cand_id, table, st);
+            } else if (table) {
+                e = dt_kn3_table_launch(p->batch, p->L, p->V, p->K, p->R, p->U, p->Vt, p->root_tok, t->cand_id,
+                                        table, st);
+            }
+            const float* znorm = (markov_on(p) && p->markov_norm)
+                                     ? (const float*)((const unsigned char*)workspace + DT_ZNORM_OFFSET(p))
+                                     : nullptr;
+            if (e == cudaSuccess)
+                e = dt_kn7_launch(p->batch, p->L, p->V, p->K, p->B, Mmax, t->cand_lp, t->cand_id, table, p->root_tok,
+                                  znorm, t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status,
+                                  st);
             break;
         }
         case DT_MODE_TALON:
@@ -292,13 +341,13 @@ dt_status dt_build_tree_mask(const dt_build_params* p, const void* draft_logits,
     dt_status s = check_build(p, t);
     if (s != DT_OK) return s;
     if (!mask || !pos) return DT_ERR_INVALID_ARG;
-    if (p->mode == DT_MODE_DARTREE) {
+    {
         const size_t need = dt_workspace_size(p, nullptr);
         if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
     }
     s = dt_candidates(p, draft_logits, t, stream);
     if (s != DT_OK) return s;
-    if (p->mode == DT_MODE_DARTREE && p->markov_norm) {
+    if (markov_on(p) && p->markov_norm) {
         s = dt_markov_norm(p, draft_logits, t, workspace, workspace_bytes, stream);
         if (s != DT_OK) return s;
     }
@@ -309,7 +358,7 @@ dt_status dt_markov_norm(const dt_build_params* p, const void* draft_logits, dt_
                          size_t workspace_bytes, dt_stream_t stream) {
     dt_status s = check_build(p, t);
     if (s != DT_OK) return s;
-    if (p->mode != DT_MODE_DARTREE || !p->markov_norm || !draft_logits) return DT_ERR_INVALID_ARG;
+    if (!markov_on(p) || !p->markov_norm || !draft_logits) return DT_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < dt_workspace_size(p, nullptr)) return DT_ERR_INVALID_ARG;
     unsigned char* ws = (unsigned char*)workspace;
     float* z = (float*)(ws + DT_ZNORM_OFFSET(p));
@@ -323,13 +372,13 @@ dt_status dt_build_tree(const dt_build_params* p, const void* draft_logits, dt_t
                         size_t workspace_bytes, dt_stream_t stream) {
     dt_status s = check_build(p, t);
     if (s != DT_OK) return s;
-    if (p->mode == DT_MODE_DARTREE) {
+    {
         const size_t need = dt_workspace_size(p, nullptr);
         if (need > 0 && (!workspace || workspace_bytes < need)) return DT_ERR_INVALID_ARG;
     }
     s = dt_candidates(p, draft_logits, t, stream);
     if (s != DT_OK) return s;
-    if (p->mode == DT_MODE_DARTREE && p->markov_norm) {
+    if (markov_on(p) && p->markov_norm) {
         s = dt_markov_norm(p, draft_logits, t, workspace, workspace_bytes, stream);
         if (s != DT_OK) return s;
     }
@@ -350,26 +399,44 @@ dt_status dt_verify(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, c
                     const float* target_lse, const void* draft_logits, float temperature, const float* uniforms,
                     int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
                     dt_stream_t stream) {
+    if (temperature != 0.0f && temperature != 1.0f) return DT_ERR_UNSUPPORTED;
+    return dt_verify_rule(t, batch, V, dtype, target_logits, target_lse, draft_logits,
+                          temperature == 1.0f ? DT_VERIFY_RATIO : DT_VERIFY_GREEDY, uniforms, acc_nodes, acc_len,
+                          next_tok, visited_lse, stream);
+}
+
+dt_status dt_verify_rule(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, const void* target_logits,
+                         const float* target_lse, const void* draft_logits, int32_t rule, const float* uniforms,
+                         int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
+                         dt_stream_t stream) {
     if (!t || batch < 1 || V < 1 || !target_logits || !acc_nodes || !acc_len || !next_tok) return DT_ERR_INVALID_ARG;
     if (V > DT_MAX_V) return DT_ERR_UNSUPPORTED;
     if (dtype != DT_BF16 && dtype != DT_F32) return DT_ERR_INVALID_ARG;
     if (t->max_nodes < 1 || t->max_nodes > DT_MAX_NODES || t->L < 1 || t->L > DT_MAX_L) return DT_ERR_INVALID_ARG;
     if (!t->node_tok || !t->parent || !t->depth || !t->rank || !t->n_nodes || !t->status) return DT_ERR_INVALID_ARG;
-    const int t1 = (temperature == 1.0f);
-    if (!t1 && temperature != 0.0f) return DT_ERR_UNSUPPORTED;
-    if (t1 && (!draft_logits || !uniforms || !t->lse)) return DT_ERR_INVALID_ARG;
+    if (rule < DT_VERIFY_GREEDY || rule > DT_VERIFY_TARGET_MATCH) return DT_ERR_INVALID_ARG;
+    const bool t1 = rule != DT_VERIFY_GREEDY;
+    const bool uses_q = rule == DT_VERIFY_RATIO || rule == DT_VERIFY_ITER_RESIDUAL;
+    if (t1 && !uniforms) return DT_ERR_INVALID_ARG;
+    if (uses_q && (!draft_logits || !t->lse)) return DT_ERR_INVALID_ARG;
     // the walk is sequential per request: spread each row over a cluster as
     // wide as the batch lets the device hold at once
     const int esize = dtype == DT_BF16 ? 2 : 4;
     const int Mmax = t->max_nodes;
     const int s = cluster_for(
         V, batch, dtype,
-        [&](int q) { return dt_kn6_smem_bytes(chunk_of(V, q, dtype), esize, Mmax) + 1024 <= kSmemMax; },
-        [&](int q, int chunk) { return max_clusters(6, dtype, q, chunk, Mmax); });
+        [&](int q) {
+            // the residual-per-sibling rule wants clusters whose chunks leave room for its cache
+            const int chunk = chunk_of(V, q, dtype);
+            return dt_kn6_smem_bytes(chunk, esize, Mmax, rule) + 1024 <= kSmemMax &&
+                   (rule != DT_VERIFY_ITER_RESIDUAL || dt_kn6_pq_cache(chunk, esize, Mmax, rule));
+        },
+        [&](int q, int chunk) { return max_clusters(6, dtype, q, chunk, Mmax * 4 + rule); });
     const int chunk = chunk_of(V, s, dtype);
-    if (chunk > kChunkMax || dt_kn6_smem_bytes(chunk, esize, Mmax) + 1024 > kSmemMax) return DT_ERR_UNSUPPORTED;
-    cudaError_t e = dt_kn6_launch(batch, t->L, V, dtype, t->max_nodes, s, chunk, t1, t->node_tok, t->parent, t->depth,
-                                  t->rank, t->n_nodes, t->lse, target_logits, t1 ? target_lse : nullptr, draft_logits,
+    if (chunk > kChunkMax || dt_kn6_smem_bytes(chunk, esize, Mmax, rule) + 1024 > kSmemMax) return DT_ERR_UNSUPPORTED;
+    cudaError_t e = dt_kn6_launch(batch, t->L, V, dtype, t->max_nodes, s, chunk, rule, t->node_tok, t->parent,
+                                  t->depth, t->rank, t->n_nodes, t->lse, target_logits, t1 ? target_lse : nullptr,
+                                  uses_q ? draft_logits : nullptr,
                                   uniforms, acc_nodes,
                                   acc_len, next_tok, visited_lse, t->status, (cudaStream_t)stream);
     return cuda_status(e);

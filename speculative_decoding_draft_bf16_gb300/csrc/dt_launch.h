@@ -85,6 +85,27 @@ cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float be
                           int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
                           int32_t* status, uint32_t* mask, int32_t* pos, int pos_offset, cudaStream_t st);
 
+// The Markov edge table alone, [batch][L][K][K] (row 0 of position 0: the
+// root token, left unwritten without one).
+cudaError_t dt_kn3_table_launch(int batch, int L, int V, int K, int R, const float* U, const float* Vt,
+                                const int32_t* root_tok, const int32_t* cand_id, float* table, cudaStream_t st);
+
+// Best-first heap with parent-conditioned edge scores (kn7_heap.cu): edge
+// terms from `table` ([batch][L][K][K], or NULL: none), minus znorm when given;
+// the depth-1 term only when root_tok names a token.  Returns
+// cudaErrorInvalidValue when the shapes do not fit shared memory.
+size_t dt_kn7_smem_bytes(int L, int K, int B, int Mmax);
+cudaError_t dt_kn7_launch(int batch, int L, int V, int K, int B, int Mmax, const float* cand_lp,
+                          const int32_t* cand_id, const float* table, const int32_t* root_tok, const float* znorm,
+                          int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
+                          int32_t* n_nodes, int32_t* status, cudaStream_t st);
+
+// TDES edge table (kn7_heap.cu): [batch][L][K][K] = s * f(parent, child, depth).
+size_t dt_kn8_smem_bytes(int K, int H);
+cudaError_t dt_kn8_launch(int batch, int L, int V, int K, int H, const float* Ap, const float* Ac, const float* Dd,
+                          const float* w, float b0, float s, const int32_t* root_tok, const int32_t* cand_id,
+                          float* table, cudaStream_t st);
+
 // TALON selection (kn4_talon.cu).
 size_t dt_kn4_smem_bytes(int Kc, int N);
 cudaError_t dt_kn4_launch(int batch, int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
@@ -106,10 +127,11 @@ size_t dt_kn5_smem_bytes(int Mmax);
 cudaError_t dt_kn5_launch(int batch, int L, int Mmax, int pos_offset, const int32_t* parent, const int32_t* depth,
                           const int32_t* n_nodes, uint32_t* mask, int32_t* pos, int32_t* status, cudaStream_t st);
 
-// Verification walk (kn6_verify.cu).
-int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax);
-size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax);
-cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int temperature_one,
+// Verification walk (kn6_verify.cu); rule: DT_VERIFY_*.
+int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax, int rule);
+size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax, int rule);
+int dt_kn6_pq_cache(int chunk, int esize, int Mmax, int rule);  // 1: the residual passes cache (P, Q)
+cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int rule,
                           const int32_t* tok, const int32_t* parent, const int32_t* depth, const int32_t* rank,
                           const int32_t* n_nodes, const float* draft_lse, const void* target,
                           const float* target_lse, const void* draft,

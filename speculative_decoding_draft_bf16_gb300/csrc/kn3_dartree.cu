@@ -384,6 +384,15 @@ size_t dt_kn3_select_smem_bytes(int L, int K, int W, int use_table) {
            (size_t)cap * 8 + (size_t)((K + 3) & ~3) * 4 + NS * 4 * 8 + (NS + 1) * 4 + (size_t)W * 4 + 16;
 }
 
+cudaError_t dt_kn3_table_launch(int batch, int L, int V, int K, int R, const float* U, const float* Vt,
+                                const int32_t* root_tok, const int32_t* cand_id, float* table, cudaStream_t st) {
+    const size_t sm = dt_kn3_table_smem_bytes(K, R);
+    cudaError_t e = cudaFuncSetAttribute(kn3_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    DtLaunch lt(dim3(L, batch), dim3(NT_TAB), sm, st);
+    return cudaLaunchKernelEx(&lt.cfg, kn3_table_kernel, L, K, R, V, U, Vt, root_tok, cand_id, table);
+}
+
 cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* lse, float* table, const float* znorm, int32_t* tok,

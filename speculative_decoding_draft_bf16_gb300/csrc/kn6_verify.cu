@@ -8,13 +8,24 @@
 // rejects), bonus-token section (a node with nothing left to verify samples
 // one more token from its target row), greedy ties (smallest id).
 //
-// On a tree (the pages give the single-chain rule): at node n the children of
-// n are tested in rank order and the walk descends into the first accepted
-// one; if all are rejected the replacement comes from max(0, P - Q) with P, Q
-// the 2^32 fixed-point masses of the target row of n and the drafter row of
-// n's children's position (P when the residual is empty); a node without
-// children draws its bonus token from P.  Ratios and masses use dt_exp_canon,
-// and the draw is an exact integer inverse CDF, so results are reproducible.
+// On a tree (the pages give the single-chain rule), three rules at T=1:
+//  - ratio (DT_VERIFY_RATIO): at node n the children of n are tested in rank
+//    order against p and the walk descends into the first accepted one; if
+//    all are rejected the replacement comes from max(0, P - Q) with P, Q the
+//    2^32 fixed-point masses of the target row of n and the drafter row of n's
+//    children's position (P when the residual is empty); a node without
+//    children draws its bonus token from P.
+//  - one residual per rejected sibling (DT_VERIFY_ITER_RESIDUAL): child c_1 as
+//    above; child c_i (i >= 2) against the residual left by c_1 .. c_{i-1},
+//    r_i = [r_{i-1} - q]_+ normalised, held exactly as the integer weights
+//    W_i = max(0, P - floor(Q * T_i / 2^32)), T_1 = 2^32, T_{i+1} = T_i + sum W_i
+//    (one pass over the row per rejected child); the replacement comes from
+//    the last residual.
+//  - exact target-sample matching (DT_VERIFY_TARGET_MATCH, as DFlash does per
+//    [DARTree] "Speculative sampling"): at every node draw from P and descend
+//    while the draw is a child's token; the drafter rows are not read.
+// Ratios and masses use dt_exp_canon, and the draws are exact integer inverse
+// CDFs, so results are reproducible.
 //
 // One thread-block cluster of S CTAs per request; CTA c owns a vocabulary
 // chunk.  Rows are bulk-copied chunk-wise into shared memory: the target row
@@ -51,6 +62,7 @@ struct Kn6Misc {
     unsigned long long red_w[NW];
     float red_f[NW];
     int child;
+    int drawn[2];                 // matching: the token drawn by the CTA holding the draw
     unsigned long long best_kid;
     float xm[SMAX];               // partners' published values, copied through DSMEM
     float xs[SMAX];
@@ -75,15 +87,29 @@ DT_DI unsigned long long warp_incl_scan_u64(unsigned long long v) {
     return v;
 }
 
-// 2^32 fixed-point probability mass exp(v - lse) of one element, or of the
-// residual max(0, P - Q) when resid.
-DT_DI unsigned long long mass(float xv, float lse_t, bool resid, float yv, float lse_d) {
-    unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(xv, lse_t)));
-    if (resid) {
-        const unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(yv, lse_d)));
-        P = P > Q ? P - Q : 0ull;
-    }
-    return P;
+// Residual weight max(0, P - floor(Q * T / 2^32)) (Q <= 2^32, T < 2^44).
+DT_DI unsigned long long resid_w(unsigned long long P, unsigned long long Q, unsigned long long T) {
+    const unsigned long long s = ((Q * T) >> 32) | (__umul64hi(Q, T) << 32);
+    return P > s ? P - s : 0ull;
+}
+
+// Test of a child against the residual with weights W (sum S):
+// floor(u * 2^24) * Q * S < W * 2^56, in 128-bit integers.
+DT_DI bool resid_accepts(float u, unsigned long long Q, unsigned long long S, unsigned long long W) {
+    unsigned long long X = (unsigned long long)__fmul_rn(u, 16777216.0f);
+    if (X > 16777215ull) X = 16777215ull;
+    const unsigned long long a = X * Q;
+    const unsigned long long lhi = __umul64hi(a, S), llo = a * S;
+    const unsigned long long rhi = W >> 8, rlo = W << 56;
+    return lhi < rhi || (lhi == rhi && llo < rlo);
+}
+
+// 2^32 fixed-point probability mass exp(v - lse) of one element, or its
+// residual weight resid_w(P, Q, T) when resid.
+DT_DI unsigned long long mass(float xv, float lse_t, bool resid, float yv, float lse_d, unsigned long long T) {
+    const unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(xv, lse_t)));
+    if (!resid) return P;
+    return resid_w(P, dt_fixed32(dt_exp_canon(__fsub_rn(yv, lse_d))), T);
 }
 
 // Row buffers of one CTA.  Every thread keeps an identical copy of this state
@@ -148,8 +174,10 @@ struct Rows {
     }
 };
 
-template <typename T>
-__global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int chunk, int nbt, int t1,
+// One instantiation per acceptance rule (RULE = DT_VERIFY_*), so that each
+// walk carries only its own code.
+template <typename T, int RULE>
+__global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int chunk, int nbt, int pq_on,
                                                  const int32_t* __restrict__ g_tok,
                                                  const int32_t* __restrict__ g_par,
                                                  const int32_t* __restrict__ g_dep,
@@ -236,12 +264,31 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
     int cur = 0;  // target buffer holding row n
     int k = 0;    // cluster exchanges so far (selects the Pub slot)
     int out_tok = -1;
+    constexpr int rule = RULE;
+    constexpr bool greedy = rule == DT_VERIFY_GREEDY;
+    constexpr bool match = rule == DT_VERIFY_TARGET_MATCH;
+    constexpr bool uses_q = rule == DT_VERIFY_RATIO || rule == DT_VERIFY_ITER_RESIDUAL;
     const float* u0 = uniforms ? uniforms + (size_t)b * 2 * Mmax : nullptr;
     const float* u1 = u0 ? u0 + Mmax : nullptr;
-    // per-node target rows: argmax (T=0) or the normaliser (T=1 without target_lse)
-    const bool rows_needed = !t1 || !target_lse;
+    // per-node target rows: argmax (T=0), a draw at every node (matching), or
+    // the normaliser (T=1 without target_lse)
+    const bool rows_needed = greedy || match || !target_lse;
     auto trow_of = [&](int node) { return target + (tb + node) * (size_t)V; };
     auto drow_of = [&](int pos) { return draft + ((size_t)b * L + pos) * V; };
+    // children are tested in (rank, index) order
+    auto kid_key = [&](int i) {
+        return ((unsigned long long)((uint32_t)s_rank[i] ^ 0x80000000u) << 32) | (uint32_t)i;
+    };
+    // accept `ch` as the next path node
+    auto descend = [&](int ch) {
+        ++len;
+        if (c == 0 && tid == 0) acc_nodes[(size_t)b * (L + 1) + len] = ch;
+        n = ch;
+        if (rows_needed) {
+            if (nbt == 2 && rows.holds(cur ^ 1) == ch) cur ^= 1;
+            else rows.stage(cur, trow_of(ch), ch, lo, hi, &misc->timeout);
+        }
+    };
     if (rows_needed) rows.stage(cur, trow_of(0), 0, lo, hi, &misc->timeout);
 
     for (;;) {
@@ -249,7 +296,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
         const int pred = s_pred[n];
         if (rows_needed && nbt == 2 && pred != 0x7FFFFFFF && len < L && rows.holds(cur ^ 1) != pred)
             rows.stage(cur ^ 1, trow_of(pred), pred, lo, hi, &misc->timeout);
-        if (t1 && s_nk[n] > 0 && rows.holds(DB) != s_dep[n])
+        if (uses_q && s_nk[n] > 0 && rows.holds(DB) != s_dep[n])
             rows.stage(DB, drow_of(s_dep[n]), s_dep[n], lo, hi, &misc->timeout);
 
         int child = -1;
@@ -263,7 +310,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
             rows.wait(cur, &misc->timeout);
             __syncthreads();
         }
-        if (!t1) {
+        if (greedy) {
             // argmax, smallest id on ties: each thread keeps the first of its
             // vectors holding its largest value, then the first such element
             float lb = NEG_INF;
@@ -395,49 +442,54 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
             ++k;
             lse_t = M_ + logf(ssum);
         }
-        if (t1) {
+        // single-residual test of child i against p (fp32, exp_canon ratio)
+        auto ratio_accepts = [&](int i) {
+            const int tk = s_tok[i];
+            const int pos = s_dep[i] - 1;
+            const float tv = E::val(trow_of(n)[tk]);
+            const float dv = E::val(drow_of(pos)[tk]);
+            const float lpt = __fsub_rn(tv, lse_t);
+            const float lpq = __fsub_rn(dv, draft_lse[(size_t)b * L + pos]);
+            return u0[i] < dt_exp_canon(__fsub_rn(lpt, lpq));
+        };
+        unsigned long long prev_key = 0;  // one residual per sibling: the last child tested
+        if (!greedy) {
             if (c == 0 && tid == 0 && visited_lse) visited_lse[(size_t)b * (L + 1) + len] = lse_t;
-            // ratio tests of n's children; the first accepted in (rank, index) order wins
-            if (tid == 0) misc->best_kid = ~0ull;
-            __syncthreads();
-            if (s_nk[n] > 0) {
-                const T* trow = trow_of(n);
-                for (int i = 1 + tid; i < M; i += NT) {
-                    if (s_par[i] != n) continue;
-                    const int tk = s_tok[i];
-                    const int pos = s_dep[i] - 1;
-                    const float tv = E::val(trow[tk]);
-                    const float dv = E::val(draft[((size_t)b * L + pos) * V + tk]);
-                    const float lpt = __fsub_rn(tv, lse_t);
-                    const float lpq = __fsub_rn(dv, draft_lse[(size_t)b * L + pos]);
-                    const float ratio = dt_exp_canon(__fsub_rn(lpt, lpq));
-                    if (u0[i] < ratio)
-                        atomicMin(&misc->best_kid,
-                                  ((unsigned long long)((uint32_t)s_rank[i] ^ 0x80000000u) << 32) | (uint32_t)i);
+            if (uses_q) {
+                // ratio rule: every child against p, the first accepted in (rank, index)
+                // order wins; residual rule: find the first child and test it alone
+                if (tid == 0) misc->best_kid = ~0ull;
+                __syncthreads();
+                if (s_nk[n] > 0) {
+                    for (int i = 1 + tid; i < M; i += NT) {
+                        if (s_par[i] != n) continue;
+                        if (rule != DT_VERIFY_RATIO || ratio_accepts(i)) atomicMin(&misc->best_kid, kid_key(i));
+                    }
+                }
+                __syncthreads();
+                const unsigned long long bk = misc->best_kid;
+                if (rule == DT_VERIFY_RATIO) {
+                    child = (bk == ~0ull) ? -1 : (int)(bk & 0xFFFFFFFFull);
+                } else if (bk != ~0ull) {
+                    prev_key = bk;
+                    if (ratio_accepts((int)(bk & 0xFFFFFFFFull))) child = (int)(bk & 0xFFFFFFFFull);
                 }
             }
-            __syncthreads();
-            child = (misc->best_kid == ~0ull) ? -1 : (int)(misc->best_kid & 0xFFFFFFFFull);
         }
 
         if (child >= 0 && len < L) {
-            ++len;
-            if (c == 0 && tid == 0) acc_nodes[(size_t)b * (L + 1) + len] = child;
-            n = child;
-            if (rows_needed) {
-                if (nbt == 2 && rows.holds(cur ^ 1) == child) cur ^= 1;
-                else rows.stage(cur, trow_of(child), child, lo, hi, &misc->timeout);
-            }
+            descend(child);
             continue;
         }
-        if (!t1) break;
+        if (greedy) break;
 
-        // ---- T=1: draw the replacement / bonus token ------------------------
+        // ---- T=1: residuals and the draw -------------------------------------
         const bool has_kids = s_nk[n] > 0;
+        const bool resid = uses_q && has_kids;
         if (rows.holds(cur) != n) rows.stage(cur, trow_of(n), n, lo, hi, &misc->timeout);
         rows.wait(cur, &misc->timeout);
         float lse_d = 0.f;
-        if (has_kids) {
+        if (resid) {
             rows.wait(DB, &misc->timeout);
             lse_d = draft_lse[(size_t)b * L + s_dep[n]];
         }
@@ -448,41 +500,100 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
         // that the lanes' 2- or 4-byte reads spread over the banks)
         const int run = ((nch + NT - 1) / NT) | 1;
         const int e0 = min(nch, tid * run), e1 = min(nch, e0 + run);
-        unsigned long long rR = 0, rP = 0;
+        unsigned long long Tq = 1ull << 32;  // residual weights max(0, P - floor(Q * Tq / 2^32))
+        unsigned long long rR = 0, rP = 0, totR = 0;
+        // one residual per sibling: the run's (P, Q) are kept in shared memory
+        // (32 bits each; a 2^32 mass -- a one-hot row -- sends the CTA back to
+        // recomputing them) and a bit mask marks the elements whose weight is
+        // still positive, which is all a later pass visits (weights only fall)
+        const bool cache = pq_on && rule == DT_VERIFY_ITER_RESIDUAL && resid && run <= 64;
+        uint2* pq = (uint2*)(smem + 1024 + tree_bytes + (size_t)(nbt + 1) * rows.stride);
+        unsigned long long alive = 0;
+        bool sat = false;
         for (int e = e0; e < e1; ++e) {
-            const float xe = E::val(x[e]);
-            const unsigned long long P = mass(xe, lse_t, false, 0.f, 0.f);
+            const unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
             rP += P;
-            if (has_kids) {
+            if (resid) {
                 const unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(y[e]), lse_d)));
-                rR += P > Q ? P - Q : 0ull;
+                const unsigned long long w = P > Q ? P - Q : 0ull;
+                rR += w;
+                if (cache) {
+                    pq[e] = make_uint2((uint32_t)P, (uint32_t)Q);
+                    sat |= ((P | Q) >> 32) != 0;
+                    if (w) alive |= 1ull << (e - e0);
+                }
             }
         }
-        {
-            const unsigned long long sR = dt_warp_sum_u64(rR), sP = dt_warp_sum_u64(rP);
-            if (lane == 0) { misc->red_u[wid] = sR; misc->red_w[wid] = sP; }
+        const bool use_pq = cache && !__syncthreads_or(sat);
+        child = -1;
+        for (bool first = true;; first = false) {
+            if (!first) {  // a later residual: T has grown
+                rR = 0;
+                if (use_pq) {
+                    for (unsigned long long m = alive; m; m &= m - 1) {
+                        const int j = __ffsll((long long)m) - 1;
+                        const uint2 v = pq[e0 + j];
+                        const unsigned long long w = resid_w(v.x, v.y, Tq);
+                        rR += w;
+                        if (!w) alive &= ~(1ull << j);
+                    }
+                } else {
+                    for (int e = e0; e < e1; ++e)
+                        rR += mass(E::val(x[e]), lse_t, true, E::val(y[e]), lse_d, Tq);
+                }
+            }
+            {
+                const unsigned long long sR = dt_warp_sum_u64(rR), sP = dt_warp_sum_u64(rP);
+                if (lane == 0) { misc->red_u[wid] = sR; misc->red_w[wid] = sP; }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                unsigned long long aR = 0, aP = 0;
+                for (int w = 0; w < NW; ++w) { aR += misc->red_u[w]; aP += misc->red_w[w]; }
+                misc->pub[k & 1].u = aR;
+                misc->pub[k & 1].w = aP;
+            }
+            __syncthreads();
+            cluster.sync();
+            if (tid < S) {
+                const Pub* r = &cluster.map_shared_rank(misc, tid)->pub[k & 1];
+                misc->xu[tid] = r->u;
+                misc->xw[tid] = r->w;
+            }
+            __syncthreads();
+            ++k;
+            totR = 0;
+            for (int j = 0; j < S; ++j) totR += misc->xu[j];
+            if (rule != DT_VERIFY_ITER_RESIDUAL || !resid || totR == 0) break;
+            // the next child in test order, against the residual just summed
+            if (tid == 0) misc->best_kid = ~0ull;
+            __syncthreads();
+            for (int i = 1 + tid; i < M; i += NT)
+                if (s_par[i] == n && kid_key(i) > prev_key) atomicMin(&misc->best_kid, kid_key(i));
+            __syncthreads();
+            const unsigned long long bk = misc->best_kid;
+            if (bk == ~0ull) break;  // every child rejected: draw from this residual
+            prev_key = bk;
+            const int ci = (int)(bk & 0xFFFFFFFFull);
+            const int tk = s_tok[ci];
+            const unsigned long long Pc = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(trow_of(n)[tk]), lse_t)));
+            const unsigned long long Qc = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(drow_of(s_dep[n])[tk]), lse_d)));
+            if (resid_accepts(u0[ci], Qc, totR, resid_w(Pc, Qc, Tq))) {
+                child = ci;
+                break;
+            }
+            Tq += totR;
+            __syncthreads();  // every thread has read best_kid and xu
         }
-        __syncthreads();
-        if (tid == 0) {
-            unsigned long long aR = 0, aP = 0;
-            for (int w = 0; w < NW; ++w) { aR += misc->red_u[w]; aP += misc->red_w[w]; }
-            misc->pub[k & 1].u = aR;
-            misc->pub[k & 1].w = aP;
+        if (child >= 0) {
+            descend(child);
+            continue;
         }
-        __syncthreads();
-        cluster.sync();
-        if (tid < S) {
-            const Pub* r = &cluster.map_shared_rank(misc, tid)->pub[k & 1];
-            misc->xu[tid] = r->u;
-            misc->xw[tid] = r->w;
-        }
-        __syncthreads();
-        ++k;
-        unsigned long long totR = 0;
-        for (int j = 0; j < S; ++j) totR += misc->xu[j];
-        // the residual, or P where the residual is empty (or the node has no children)
-        const bool resid = has_kids && totR > 0;
-        const unsigned long long* sums = resid ? misc->xu : misc->xw;
+
+        // the residual, or P where the residual is empty (or the node has no
+        // children, or the rule draws from the target)
+        const bool use_r = resid && totR > 0;
+        const unsigned long long* sums = use_r ? misc->xu : misc->xw;
         unsigned long long tot = 0, before = 0, mine = 0;
         for (int j = 0; j < S; ++j) {
             const unsigned long long v = sums[j];
@@ -490,6 +601,11 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
             if (j == c) mine = v;
             tot += v;
         }
+        // matching at an inner node: the draw decides the next node, so every
+        // CTA needs it; elsewhere it is the emitted token
+        const bool bcast = match && has_kids && len < L;
+        if (tid == 0) misc->drawn[k & 1] = -1;  // ordered before the holder's write by its barriers
+        int holder = -1;
         if (tot > 0) {
             float uf = __fmul_rn(u1[n], 16777216.0f);
             unsigned long long X = (unsigned long long)uf;
@@ -497,9 +613,14 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
             const unsigned long long lo64 = X * tot;
             const unsigned long long hi64 = __umul64hi(X, tot);
             const unsigned long long tgt = (lo64 >> 24) | (hi64 << 40);
-            if (tgt >= before && tgt < before + mine) {
+            unsigned long long cum = 0;
+            for (int j = 0; j < S; ++j) {
+                if (holder < 0 && tgt >= cum && tgt < cum + sums[j]) holder = j;
+                cum += sums[j];
+            }
+            if (holder == c) {
                 // this CTA holds the draw: exclusive scan of the run sums
-                const unsigned long long rs = resid ? rR : rP;
+                const unsigned long long rs = use_r ? rR : rP;
                 const unsigned long long inc = warp_incl_scan_u64(rs);
                 __syncthreads();  // red_u was read by tid 0 above
                 if (lane == 31) misc->red_u[wid] = inc;
@@ -518,31 +639,56 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
                     for (int g0 = a0; g0 < a1; g0 += 32) {
                         const int e = g0 + lane;
                         unsigned long long P = 0;
-                        if (e < a1) P = mass(E::val(x[e]), lse_t, resid, resid ? E::val(y[e]) : 0.f, lse_d);
+                        if (e < a1) P = mass(E::val(x[e]), lse_t, use_r, use_r ? E::val(y[e]) : 0.f, lse_d, Tq);
                         const unsigned long long ci = warp_incl_scan_u64(P);
                         const unsigned found = __ballot_sync(0xffffffffu, P > 0 && base + ci > local);
                         if (found) {
-                            if (lane == __ffs(found) - 1) next_tok[b] = lo + e;
+                            if (lane == __ffs(found) - 1) {
+                                if (bcast) misc->drawn[k & 1] = lo + e;
+                                else next_tok[b] = lo + e;
+                            }
                             break;
                         }
                         base += __shfl_sync(0xffffffffu, ci, 31);
                     }
                 }
             }
+        } else if (c == 0 && tid == 0) {
+            next_tok[b] = -1;  // no mass to draw from
+        }
+        if (bcast && tot > 0) {
+            __syncthreads();
+            cluster.sync();
+            if (tid == 0) misc->child = cluster.map_shared_rank(misc, holder)->drawn[k & 1];
+            __syncthreads();
+            const int yt = misc->child;
+            ++k;
+            __syncthreads();  // every thread has read misc->child
+            if (tid == 0) misc->child = 0x7FFFFFFF;
+            __syncthreads();
+            for (int i = 1 + tid; i < M; i += NT)
+                if (s_par[i] == n && s_tok[i] == yt) atomicMin(&misc->child, i);
+            __syncthreads();
+            const int ch = misc->child;
+            if (ch != 0x7FFFFFFF) {
+                descend(ch);
+                continue;
+            }
+            if (c == 0 && tid == 0) next_tok[b] = yt;
         }
         break;
     }
 
     if (c == 0 && tid == 0) {
         acc_len[b] = len;
-        if (!t1) next_tok[b] = out_tok;
+        if (greedy) next_tok[b] = out_tok;
     }
     if (c == 0)
         for (int i = len + 1 + tid; i <= L; i += NT) acc_nodes[(size_t)b * (L + 1) + i] = -1;
     if (c == 0 && tid == 0) {
         acc_nodes[(size_t)b * (L + 1)] = 0;
         if (visited_lse)
-            for (int i = (t1 ? len + 1 : 0); i <= L; ++i) visited_lse[(size_t)b * (L + 1) + i] = 0.f;
+            for (int i = (greedy ? 0 : len + 1); i <= L; ++i) visited_lse[(size_t)b * (L + 1) + i] = 0.f;
     }
     // no copy may still be landing in shared memory when the CTA exits
 #pragma unroll
@@ -552,60 +698,107 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
     cluster.sync();  // keep shared memory alive until every CTA finished its remote reads
 }
 
-// Target-row buffers: two (prefetch of the favourite child) when they fit.
-int kn6_target_buffers(int chunk, int esize, int Mmax) {
+// Shared-memory layout: misc (1 KB), tree, nbt target-row buffers and one
+// drafter-row buffer, and for the residual-per-sibling rule the (P, Q) cache
+// (8 bytes per chunk element) when it fits.  Two target buffers (prefetch of
+// the favourite child) when they fit, but the cache comes first.
+struct Kn6Layout {
+    int nbt;
+    size_t pq, total;
+};
+Kn6Layout kn6_layout(int chunk, int esize, int Mmax, int rule) {
     const size_t tree = (((size_t)Mmax * 24) + 127) & ~(size_t)127;
     const size_t buf = (((size_t)chunk * esize + 16 + 127) & ~(size_t)127);
-    return (1024 + tree + 3 * buf + 1024 <= (size_t)227 * 1024) ? 2 : 1;
+    const size_t pq = rule == DT_VERIFY_ITER_RESIDUAL ? (((size_t)chunk * 8 + 127) & ~(size_t)127) : 0;
+    const size_t cap = (size_t)226 * 1024;
+    auto total = [&](int nbt, size_t p) { return 1024 + tree + (size_t)(nbt + 1) * buf + p; };
+    if (pq && total(2, pq) <= cap) return Kn6Layout{2, pq, total(2, pq)};
+    if (pq && total(1, pq) <= cap) return Kn6Layout{1, pq, total(1, pq)};
+    const int nbt = total(2, 0) <= cap ? 2 : 1;
+    return Kn6Layout{nbt, 0, total(nbt, 0)};
 }
 
 }  // namespace
 
-size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax) {
-    const size_t tree = (((size_t)Mmax * 24) + 127) & ~(size_t)127;
-    const size_t buf = (((size_t)chunk * esize + 16 + 127) & ~(size_t)127);
-    return 1024 + tree + (size_t)(kn6_target_buffers(chunk, esize, Mmax) + 1) * buf;
+size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax, int rule) {
+    return kn6_layout(chunk, esize, Mmax, rule).total;
+}
+
+int dt_kn6_pq_cache(int chunk, int esize, int Mmax, int rule) {
+    return kn6_layout(chunk, esize, Mmax, rule).pq > 0;
 }
 
 // Sets the kernel's shared-memory and cluster-size attributes for a launch.
-template <typename T>
+template <typename T, int RULE>
 cudaError_t kn6_prepare(int S, size_t smem) {
-    cudaError_t e = cudaFuncSetAttribute(kn6_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess && S > 8) e = cudaFuncSetAttribute(kn6_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaError_t e = cudaFuncSetAttribute(kn6_kernel<T, RULE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && S > 8)
+        e = cudaFuncSetAttribute(kn6_kernel<T, RULE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
 
-int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax) {
-    const int esize = dtype == DT_BF16 ? 2 : 4;
-    const size_t smem = dt_kn6_smem_bytes(chunk, esize, Mmax);
-    if (dtype == DT_BF16) {
-        if (kn6_prepare<uint16_t>(S, smem) != cudaSuccess) return 0;
-        return dt_max_active_clusters(kn6_kernel<uint16_t>, S, NT, smem);
-    }
-    if (kn6_prepare<float>(S, smem) != cudaSuccess) return 0;
-    return dt_max_active_clusters(kn6_kernel<float>, S, NT, smem);
+template <typename T, int RULE>
+int kn6_max_clusters(int S, size_t smem) {
+    if (kn6_prepare<T, RULE>(S, smem) != cudaSuccess) return 0;
+    return dt_max_active_clusters(kn6_kernel<T, RULE>, S, NT, smem);
 }
 
-cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int temperature_one,
+template <typename T>
+int kn6_max_clusters_rule(int rule, int S, size_t smem) {
+    switch (rule) {
+        case DT_VERIFY_GREEDY: return kn6_max_clusters<T, DT_VERIFY_GREEDY>(S, smem);
+        case DT_VERIFY_RATIO: return kn6_max_clusters<T, DT_VERIFY_RATIO>(S, smem);
+        case DT_VERIFY_ITER_RESIDUAL: return kn6_max_clusters<T, DT_VERIFY_ITER_RESIDUAL>(S, smem);
+        default: return kn6_max_clusters<T, DT_VERIFY_TARGET_MATCH>(S, smem);
+    }
+}
+
+template <typename T, int RULE>
+cudaError_t kn6_launch_t(const DtLaunch& lc, size_t smem, int S, int L, int V, int Mmax, int chunk, int nbt,
+                         int pq_on, const int32_t* tok, const int32_t* parent, const int32_t* depth,
+                         const int32_t* rank, const int32_t* n_nodes, const float* draft_lse, const void* target,
+                         const float* target_lse, const void* draft, const float* uniforms, int32_t* acc_nodes,
+                         int32_t* acc_len, int32_t* next_tok, float* visited_lse, int32_t* status) {
+    cudaError_t e = kn6_prepare<T, RULE>(S, smem);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<T, RULE>, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank,
+                              n_nodes, draft_lse, (const T*)target, target_lse, (const T*)draft, uniforms, acc_nodes,
+                              acc_len, next_tok, visited_lse, status);
+}
+
+int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax, int rule) {
+    const int esize = dtype == DT_BF16 ? 2 : 4;
+    const size_t smem = dt_kn6_smem_bytes(chunk, esize, Mmax, rule);
+    return dtype == DT_BF16 ? kn6_max_clusters_rule<uint16_t>(rule, S, smem)
+                            : kn6_max_clusters_rule<float>(rule, S, smem);
+}
+
+cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, int chunk, int rule,
                           const int32_t* tok, const int32_t* parent, const int32_t* depth, const int32_t* rank,
                           const int32_t* n_nodes, const float* draft_lse, const void* target,
                           const float* target_lse, const void* draft, const float* uniforms, int32_t* acc_nodes,
                           int32_t* acc_len, int32_t* next_tok, float* visited_lse, int32_t* status,
                           cudaStream_t st) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
-    const size_t smem = dt_kn6_smem_bytes(chunk, esize, Mmax);
-    const int nbt = kn6_target_buffers(chunk, esize, Mmax);
+    const Kn6Layout lay = kn6_layout(chunk, esize, Mmax, rule);
+    const size_t smem = lay.total;
+    const int nbt = lay.nbt, pq_on = lay.pq > 0;
     DtLaunch lc(dim3(S, batch, 1), dim3(NT, 1, 1), smem, st, S);
-    cudaError_t e;
+#define DT_KN6_ARGS lc, smem, S, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank, n_nodes, draft_lse, target, \
+                    target_lse, draft, uniforms, acc_nodes, acc_len, next_tok, visited_lse, status
     if (dtype == DT_BF16) {
-        if ((e = kn6_prepare<uint16_t>(S, smem)) != cudaSuccess) return e;
-        return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<uint16_t>, L, V, Mmax, chunk, nbt, temperature_one, tok, parent,
-                                  depth, rank, n_nodes, draft_lse, (const uint16_t*)target, target_lse,
-                                  (const uint16_t*)draft, uniforms, acc_nodes, acc_len, next_tok, visited_lse,
-                                  status);
+        switch (rule) {
+            case DT_VERIFY_GREEDY: return kn6_launch_t<uint16_t, DT_VERIFY_GREEDY>(DT_KN6_ARGS);
+            case DT_VERIFY_RATIO: return kn6_launch_t<uint16_t, DT_VERIFY_RATIO>(DT_KN6_ARGS);
+            case DT_VERIFY_ITER_RESIDUAL: return kn6_launch_t<uint16_t, DT_VERIFY_ITER_RESIDUAL>(DT_KN6_ARGS);
+            default: return kn6_launch_t<uint16_t, DT_VERIFY_TARGET_MATCH>(DT_KN6_ARGS);
+        }
     }
-    if ((e = kn6_prepare<float>(S, smem)) != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<float>, L, V, Mmax, chunk, nbt, temperature_one, tok, parent, depth,
-                              rank, n_nodes, draft_lse, (const float*)target, target_lse, (const float*)draft,
-                              uniforms, acc_nodes, acc_len, next_tok, visited_lse, status);
+    switch (rule) {
+        case DT_VERIFY_GREEDY: return kn6_launch_t<float, DT_VERIFY_GREEDY>(DT_KN6_ARGS);
+        case DT_VERIFY_RATIO: return kn6_launch_t<float, DT_VERIFY_RATIO>(DT_KN6_ARGS);
+        case DT_VERIFY_ITER_RESIDUAL: return kn6_launch_t<float, DT_VERIFY_ITER_RESIDUAL>(DT_KN6_ARGS);
+        default: return kn6_launch_t<float, DT_VERIFY_TARGET_MATCH>(DT_KN6_ARGS);
+    }
+#undef DT_KN6_ARGS
 }

@@ -15,11 +15,13 @@ import torch
 
 from . import build as _build
 
-DT_MODE = {"ddtree": 0, "dartree": 1, "talon": 2}
+DT_MODE = {"ddtree": 0, "dartree": 1, "talon": 2, "heap": 3}
 DT_BF16, DT_F32 = 0, 1
 DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_BESTFIRST = 0x1, 0x2, 0x4
 DT_DEV_VIOLATION_SHIFT = 8
 DT_STAGE1_CLUSTER, DT_STAGE1_ROWS = 1, 2
+# acceptance rules of dt_verify_rule
+VERIFY_RULES = {"greedy": 0, "ratio": 1, "iter_residual": 2, "target_match": 3}
 MAX_NODES = 1025
 MAX_KC = 1024
 
@@ -27,11 +29,17 @@ _i32 = ctypes.c_int32
 _vp = ctypes.c_void_p
 
 
+class TdesStruct(ctypes.Structure):
+    _fields_ = [("H", _i32), ("Ap", _vp), ("Ac", _vp), ("Dd", _vp), ("w", _vp), ("b0", ctypes.c_float),
+                ("s", ctypes.c_float)]
+
+
 class BuildParams(ctypes.Structure):
     _fields_ = [("mode", _i32), ("batch", _i32), ("L", _i32), ("V", _i32), ("dtype", _i32),
                 ("K", _i32), ("B", _i32), ("W", _i32), ("beta", ctypes.c_float), ("R", _i32),
                 ("U", _vp), ("Vt", _vp), ("root_tok", _vp), ("talon_k", _i32),
-                ("log_mu", ctypes.c_float), ("N", _i32), ("markov_norm", _i32)]
+                ("log_mu", ctypes.c_float), ("N", _i32), ("markov_norm", _i32),
+                ("tdes", ctypes.POINTER(TdesStruct))]
 
 
 class TreeStruct(ctypes.Structure):
@@ -68,6 +76,8 @@ def lib():
         L.dt_tree_mask.restype = _i32
         L.dt_tree_mask.argtypes = [tp, _i32, _i32, _vp, _vp, _vp]
         L.dt_verify.restype = _i32
+        L.dt_verify_rule.restype = _i32
+        L.dt_verify_rule.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
         L.dt_verify.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
                                 _vp]
         L.dt_select_dartree_noalloc.restype = _i32
@@ -135,6 +145,7 @@ class Params:
     mu: float = 0.0
     N: int = 0
     markov_norm: bool = False  # DARTree: full-vocabulary normalised correction
+    tdes: "Tdes" = None        # heap mode: TDES edge scorer
 
     @property
     def Kc(self):
@@ -148,10 +159,32 @@ class Params:
         log_mu = 0.0
         if self.mode == "talon":
             log_mu = float(torch.tensor(math.log(self.mu), dtype=torch.float64).float())
-        return BuildParams(DT_MODE[self.mode], self.batch, self.L, self.V,
-                           DT_BF16 if self.dtype == "bf16" else DT_F32, self.K, self.B, self.W,
-                           self.beta, self.R if self.U is not None else 0, _ptr(self.U), _ptr(self.Vt),
-                           _ptr(self.root_tok), self.talon_k, log_mu, self.N, int(bool(self.markov_norm)))
+        bp = BuildParams(DT_MODE[self.mode], self.batch, self.L, self.V,
+                         DT_BF16 if self.dtype == "bf16" else DT_F32, self.K, self.B, self.W,
+                         self.beta, self.R if self.U is not None else 0, _ptr(self.U), _ptr(self.Vt),
+                         _ptr(self.root_tok), self.talon_k, log_mu, self.N, int(bool(self.markov_norm)))
+        if self.tdes is not None:
+            bp._tdes = self.tdes.struct()  # kept alive with the parameter block
+            bp.tdes = ctypes.pointer(bp._tdes)
+        return bp
+
+
+@dataclasses.dataclass
+class Tdes:
+    """TDES edge scorer (dt_tdes): per-token first-layer rows Ap, Ac [V, H], depth rows
+    Dd [L, H] (bias included), output weights w [H], bias b0, scale s; fp32 device tensors."""
+    Ap: torch.Tensor
+    Ac: torch.Tensor
+    Dd: torch.Tensor
+    w: torch.Tensor
+    b0: float = 0.0
+    s: float = 1.0
+
+    def struct(self):
+        for name in ("Ap", "Ac", "Dd", "w"):
+            _need(getattr(self, name), torch.float32, name)
+        return TdesStruct(int(self.w.shape[0]), _ptr(self.Ap), _ptr(self.Ac), _ptr(self.Dd), _ptr(self.w),
+                          float(self.b0), float(self.s))
 
 
 class TreeBuffers:
@@ -284,9 +317,10 @@ def alloc_mask(tree, device="cuda"):
 
 
 def verify(tree, target, temperature=0.0, draft=None, uniforms=None, out=None, visited_lse=None, batch=None,
-           target_lse=None, stream=None):
+           target_lse=None, stream=None, rule=None):
     """Acceptance walk.  out = (acc_nodes [b, L+1], acc_len [b], next_tok [b]) int32 tensors;
-    target_lse: optional [b, max_nodes] fp32 normalisers of the target rows (T=1)."""
+    target_lse: optional [b, max_nodes] fp32 normalisers of the target rows (T=1);
+    rule: None (greedy at temperature 0, "ratio" at 1) or one of VERIFY_RULES."""
     _need(target, name="target")
     batch = batch or tree.batch
     V = target.shape[-1]
@@ -299,6 +333,12 @@ def verify(tree, target, temperature=0.0, draft=None, uniforms=None, out=None, v
         _need(uniforms, torch.float32, "uniforms")
     if target_lse is not None:
         _need(target_lse, torch.float32, "target_lse")
+    if rule is not None:
+        _check(lib().dt_verify_rule(ctypes.byref(tree.struct()), batch, V, _dtype_code(target), _ptr(target),
+                                    _ptr(target_lse), _ptr(draft), VERIFY_RULES[rule], _ptr(uniforms),
+                                    _ptr(acc_nodes), _ptr(acc_len), _ptr(next_tok), _ptr(visited_lse),
+                                    _stream(stream)), "dt_verify_rule")
+        return out
     _check(lib().dt_verify(ctypes.byref(tree.struct()), batch, V, _dtype_code(target), _ptr(target),
                            _ptr(target_lse), _ptr(draft), float(temperature), _ptr(uniforms), _ptr(acc_nodes),
                            _ptr(acc_len), _ptr(next_tok), _ptr(visited_lse), _stream(stream)), "dt_verify")

@@ -49,6 +49,7 @@ class Workload:
     N: int = 0           # TALON node budget
     cfg: int = 0         # workload family number (seed base)
     markov_norm: bool = False  # DARTree: full-vocabulary normalised correction
+    verify_rule: str = ""      # acceptance rule at T=1 ("" = "ratio"; "iter_residual", "target_match")
 
     @property
     def Kc(self):
@@ -84,6 +85,12 @@ def stochastic_batch(batch):
     """Batch in {1, 4, 16}, L=16, V=151936, bf16, B=K=256, T=1."""
     return Workload("ddtree_t1_b%d_L16_V151936_K256_B256" % batch, "ddtree", batch, 16, V_QWEN3,
                     "bf16", 3.0, 0.7, 1.0, K=256, B=256, cfg=2)
+
+
+def stochastic_rule(batch, rule):
+    """The T=1 workload verified with another acceptance rule."""
+    return dataclasses.replace(stochastic_batch(batch), verify_rule=rule,
+                               name="ddtree_t1_%s_b%d_L16_V151936_K256_B256" % (rule, batch))
 
 
 def dartree_supertree(beta):

@@ -106,6 +106,16 @@ def test_mask_and_verify_reject_invalid_arguments():
     assert args(0.0, None, None, None) == -1
     assert args(1.0, fake, None, fake) == -1
     assert args(1.0, fake, fake, None) == -1
+    # verify with an explicit rule: unknown rules; the drafter rows are needed by
+    # the ratio and residual rules, uniforms by every T=1 rule
+    rule = lambda r, tgt, drf, uni: L.dt_verify_rule(ctypes.byref(t), 1, 32, 1, tgt, None, drf, r, uni, fake, fake,
+                                                     fake, None, None)
+    assert rule(-1, fake, fake, fake) == -1 and rule(4, fake, fake, fake) == -1
+    for r in (dtree.VERIFY_RULES["ratio"], dtree.VERIFY_RULES["iter_residual"]):
+        assert rule(r, fake, None, fake) == -1
+        assert rule(r, fake, fake, None) == -1
+    assert rule(dtree.VERIFY_RULES["target_match"], fake, fake, None) == -1
+    assert rule(dtree.VERIFY_RULES["greedy"], None, None, None) == -1
 
 
 def test_workspace_size():
