@@ -74,6 +74,9 @@ def workloads():
         "dartree_beta0": wk.dartree_supertree(0.0),
         "dartree_beta-0.5": wk.dartree_supertree(-0.5),
         "dartree_norm_beta0": wk.dartree_normalised(0.0),
+        "heap_markov": wk.heap_markov(False),
+        "heap_markov_norm": wk.heap_markov(True),
+        "heap_tdes": wk.heap_tdes(256),
         "talon_N60": wk.talon_gated(60),
         "talon_N1024": wk.talon_gated(1024),
     }
@@ -126,11 +129,15 @@ def normaliser_roofline(wl, stage_us, peaks):
         "note": "one exp per (row, token) in the epilogue: %.0f M per launch" % (rows * wl.V / 1e6)}}
 
 
-def params_for(wl, U=None, Vt=None):
+def params_for(wl, U=None, Vt=None, tdes=None):
     from speculative_decoding_draft_bf16_gb300 import dtree
+    td = None
+    if tdes is not None:
+        Ap, Ac, Dd, w, b0, s = tdes
+        td = dtree.Tdes(Ap, Ac, Dd, w, b0=b0, s=s)
     return dtree.Params(mode=wl.mode, batch=wl.batch, L=wl.L, V=wl.V, dtype=wl.dtype, K=wl.K, B=wl.B, W=wl.W,
                         beta=wl.beta, R=wl.R, U=U, Vt=Vt, talon_k=wl.talon_k, mu=wl.mu, N=wl.N,
-                        markov_norm=wl.markov_norm)
+                        markov_norm=wl.markov_norm, tdes=td)
 
 
 def max_nodes_of(wl):
@@ -203,10 +210,12 @@ def run_ours(args, wl, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dtree.lib()
-    U = Vt = None
-    if wl.mode == "dartree":
+    U = Vt = tdes = None
+    if wl.R > 0 and wl.mode in ("dartree", "heap"):
         U, Vt = wk.markov_tables(wl.V, wl.R, device=dev)
-    p = params_for(wl, U, Vt)
+    if wl.H > 0:
+        tdes = wk.tdes_weights(wl.V, wl.L, wl.H, device=dev)
+    p = params_for(wl, U, Vt, tdes)
     Mmax = max_nodes_of(wl)
     esize = 2 if wl.dtype == "bf16" else 4
     draft_bytes = wl.batch * wl.L * wl.V * esize
@@ -366,9 +375,11 @@ def run_ours(args, wl, rank, world, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     status = sum(int(c["tree"].status.abs().sum()) for c in copies)
-    # stage 1, selection (writing the mask), walk; DARTree's Markov table; the normalised correction's
-    # table conversion, normaliser and merge
-    launches_per_step = 3 + (1 if (wl.mode == "dartree" and wl.R > 0) else 0) + (3 if wl.markov_norm else 0)
+    # stage 1, selection (writing the mask), walk; the heap's separate mask kernel; the Markov or TDES
+    # edge table; the normalised correction's table conversion, normaliser and merge
+    edge_table = wl.mode in ("dartree", "heap") and (wl.R > 0 or wl.H > 0)
+    launches_per_step = (3 + (1 if wl.mode == "heap" else 0) + (1 if edge_table else 0) +
+                         (3 if wl.markov_norm else 0))
     kn1_s = stage_us["candidates"] / 1e6
     achieved = draft_bytes / kn1_s / 1e9
     peaks = {}
@@ -397,7 +408,8 @@ def run_ours(args, wl, rank, world, local):
         "dtype": wl.dtype,
         "data": "synthetic (seeded Gaussian logits with confident-token spikes; Qwen3 vocabulary)",
         "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch, "L": wl.L, "V": wl.V,
-                   "K": wl.K, "B": wl.B, "W": wl.W, "beta": wl.beta, "N": wl.N, "temperature": temperature,
+                   "K": wl.K, "B": wl.B, "W": wl.W, "beta": wl.beta, "N": wl.N, "R": wl.R, "H": wl.H,
+                   "markov_norm": wl.markov_norm, "temperature": temperature,
                    "verify_rule": wl.verify_rule or ("ratio" if temperature else "greedy"),
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d input copies (drafter logits %.0f MB > 2x L2)" % (R, R * draft_bytes / 1e6)},
@@ -417,17 +429,28 @@ def run_ours(args, wl, rank, world, local):
 # ---------------------------------------------------------------------------
 # CPU oracle: baseline leg and reference arm
 # ---------------------------------------------------------------------------
-def oracle_round(wl, x, tgt, uni, U, Vt):
-    """One tree through the oracle: stage 1, selection, mask, walk."""
+def oracle_round(wl, x, tgt, uni, M):
+    """One tree through the oracle: stage 1, selection, mask, walk.  M: the
+    edge-term weights (U, Vt: Markov; tdes: TDES) as host arrays."""
     import numpy as np
     import oracle
     _, l32, ids, lps = oracle.candidates(x, wl.Kc)
     Mmax = max_nodes_of(wl)
+    U, Vt = M["U"], M["Vt"]
     if wl.mode == "ddtree":
         t = oracle.ddtree(lps, ids, wl.B, Mmax=Mmax)
     elif wl.mode == "dartree":
         z = oracle.markov_norm(x, ids, U, Vt, -1) if wl.markov_norm else None
         t, _, _ = oracle.dartree(lps, ids, U, Vt, -1, wl.W, wl.beta, wl.B, Mmax=Mmax, znorm=z)
+    elif wl.mode == "heap":
+        z = E = None
+        if M["tdes"] is not None:
+            Ap, Ac, Dd, w, b0, s = M["tdes"]
+            E = oracle.tdes_table(ids, Ap, Ac, Dd, w, b0, s, -1)
+        elif U is not None:
+            E = oracle.markov_table(ids, U, Vt, -1)
+            z = oracle.markov_norm(x, ids, U, Vt, -1) if wl.markov_norm else None
+        t = oracle.heap_select(lps, ids, wl.B, E=E, znorm=z, Mmax=Mmax)
     else:
         t = oracle.talon(lps, ids, wl.talon_k, wl.log_mu, wl.N, Mmax=Mmax)
     oracle.tree_mask(t, Mmax, wl.L)
@@ -445,28 +468,30 @@ def oracle_inputs(wl, n_trees, seed_base=10_000):
     import numpy as np
     import torch
     from speculative_decoding_draft_bf16_gb300 import workloads as wk
-    U = Vt = None
-    if wl.mode == "dartree":
-        U, Vt = (t.numpy() for t in wk.markov_tables(wl.V, wl.R))
+    M = {"U": None, "Vt": None, "tdes": None}
+    if wl.R > 0 and wl.mode in ("dartree", "heap"):
+        M["U"], M["Vt"] = (t.numpy() for t in wk.markov_tables(wl.V, wl.R))
+    if wl.H > 0:
+        M["tdes"] = tuple(v.numpy() if hasattr(v, "numpy") else v for v in wk.tdes_weights(wl.V, wl.L, wl.H))
     one = wl.with_(batch=1)
     items = []
     for i in range(n_trees):
         x, spikes = wk.draft_logits(one, first_req=seed_base + i)
         xf = x[0].float().numpy()
-        t = oracle_round(wl, xf, None, None, U, Vt)
+        t = oracle_round(wl, xf, None, None, M)
         Mmax = max_nodes_of(wl)
         depth = np.zeros((1, Mmax), np.int32)
         depth[0, :t.n] = t.depth[:t.n]
         tgt = wk.target_logits(one, depth, [t.n], spikes, first_req=seed_base + i, rows=Mmax)[0].float().numpy()
         uni = wk.uniforms(one, first_req=seed_base + i)[0].numpy() if wl.temperature == 1.0 else None
         items.append((xf, tgt, uni))
-    return items, U, Vt
+    return items, M
 
 
-def time_oracle(wl, items, U, Vt, threads):
+def time_oracle(wl, items, M, threads):
     t0 = time.perf_counter()
     with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(lambda it: oracle_round(wl, it[0], it[1], it[2], U, Vt), items))
+        list(ex.map(lambda it: oracle_round(wl, it[0], it[1], it[2], M), items))
     return time.perf_counter() - t0
 
 
@@ -476,11 +501,11 @@ def cpu_baseline(wl, cpu_seconds=20.0):
     from oracle import build as ob
     ob.build()
     cores = os.cpu_count() or 1
-    probe, U, Vt = oracle_inputs(wl, 1, seed_base=20_000)
-    t1 = time_oracle(wl, probe, U, Vt, 1)
+    probe, M = oracle_inputs(wl, 1, seed_base=20_000)
+    t1 = time_oracle(wl, probe, M, 1)
     trees = int(max(cores, min(4 * cores, cpu_seconds / max(t1, 1e-3))))
-    items, U, Vt = oracle_inputs(wl, trees)
-    sec = time_oracle(wl, items, U, Vt, cores)
+    items, M = oracle_inputs(wl, trees)
+    sec = time_oracle(wl, items, M, cores)
     return {"value": trees / sec, "unit": "trees/s", "cores": cores, "kind": "oracle",
             "sample": "%d single-request trees of the %s workload (stage 1, selection, mask, walk; "
                       "%.2f s per tree on one core), one thread per tree over %d host cores"
@@ -497,12 +522,12 @@ def run_reference(args, wl, rank, world, budget_s=150.0):
     ob.build()
     cores = os.cpu_count() or 1
     per_step = cores
-    items, U, Vt = oracle_inputs(wl, per_step)
-    warm = time_oracle(wl, items, U, Vt, cores)  # one untimed warm-up step
+    items, M = oracle_inputs(wl, per_step)
+    warm = time_oracle(wl, items, M, cores)  # one untimed warm-up step
     steps = max(1, min(args.steps, int(budget_s / max(warm, 1e-3))))
     total = 0.0
     for _ in range(steps):
-        total += time_oracle(wl, items, U, Vt, cores)
+        total += time_oracle(wl, items, M, cores)
     value = steps * per_step / total
     sample = "%d single-request trees per step (one per host core), %d of %d requested steps timed" % (
         per_step, steps, args.steps)

@@ -21,10 +21,11 @@
 //
 // One CTA per request.  All warps first compute the order rows that fit in
 // shared memory (all of them for the usual sizes); warp 0 then runs the B pops
-// alone: the frontier (at most B + 1 entries) lives in shared memory and each
-// pop is a warp-wide arg-max over it, ties on the score going to the smaller
-// descriptor found by walking both parent chains.  Rows that did not fit are
-// computed by warp 0 when a node needing them is popped.
+// alone: the frontier (at most B + 1 entries) lives in shared memory, cut into
+// blocks of 32 slots whose maxima the lanes keep in registers, so a pop is a
+// warp max and one ballot; ties on the score go to the smaller descriptor,
+// found by walking both parent chains.  Rows that did not fit are computed by
+// warp 0 when a node needing them is popped.
 //
 // TDES table (kn8): the projections depend only on the token, so the inputs
 // are the per-token first-layer rows Ap = W_p g_p(e), Ac = W_c g_c(e) and the
@@ -203,23 +204,49 @@ __global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, in
             S.fj[0] = 0;
         }
         __syncwarp();
+        // Block maxima: the frontier is cut into blocks of 32 slots; lane l keeps
+        // the largest score key of blocks l and l + 32 (0: empty).  A pop is a
+        // warp max over them and one ballot inside the winning block; only the
+        // blocks a pop changes are refreshed.  Equal best scores (rare outside
+        // coarse logits) go to the full comparison with descriptors.
+        uint32_t bk0 = 0, bk1 = 0;
+        auto skey = [&](int x) { return ordf(__fadd_rn(S.fs[x], 0.f)); };  // -0 and +0 alike
+        auto refresh = [&](int blk, int nfr) {
+            const int x = blk * 32 + lane;
+            const uint32_t m = __reduce_max_sync(0xffffffffu, x < nfr ? skey(x) : 0u);
+            if (lane == (blk & 31)) {
+                if (blk < 32) bk0 = m;
+                else bk1 = m;
+            }
+        };
         int nf = 1, n = 0;
+        refresh(0, nf);
         while (n < B && nf > 0) {
-            // arg-max of the frontier under (score desc, descriptor asc)
-            int best = -1;
-            float bs = 0.f;
-            for (int x = lane; x < nf; x += 32) {
-                const float s = S.fs[x];
-                if (best < 0 || entry_before(S, x, s, best, bs)) { best = x; bs = s; }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const int ob = __shfl_xor_sync(0xffffffffu, best, o);
-                const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-                if (ob >= 0 && (best < 0 || entry_before(S, ob, os, best, bs))) { best = ob; bs = os; }
-            }
             if (n + 1 >= Mmax) break;  // the host checks max_nodes > B; never taken
+            const uint32_t g = __reduce_max_sync(0xffffffffu, bk0 > bk1 ? bk0 : bk1);
+            const unsigned h0 = __ballot_sync(0xffffffffu, bk0 == g), h1 = __ballot_sync(0xffffffffu, bk1 == g);
+            int best = -1;
+            if (__popc(h0) + __popc(h1) == 1) {
+                const int blk = h0 ? __ffs(h0) - 1 : 32 + __ffs(h1) - 1;
+                const int xl = blk * 32 + lane;
+                const unsigned hit = __ballot_sync(0xffffffffu, xl < nf && skey(xl) == g);
+                if (__popc(hit) == 1) best = blk * 32 + __ffs(hit) - 1;
+            }
+            if (best < 0) {  // several entries share the best score: descriptor order decides
+                float bs = 0.f;
+                for (int x = lane; x < nf; x += 32) {
+                    const float sx = S.fs[x];
+                    if (best < 0 || entry_before(S, x, sx, best, bs)) { best = x; bs = sx; }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const int ob = __shfl_xor_sync(0xffffffffu, best, o);
+                    const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+                    if (ob >= 0 && (best < 0 || entry_before(S, ob, os, best, bs))) { best = ob; bs = os; }
+                }
+            }
             const int x = best, p = S.fp[x], j = S.fj[x];
+            const float bs = S.fs[x];
             const int d = S.ndep[p] + 1, rowp = S.nrow[p];
             const int c = S.ord[(size_t)rowp * K + j];
             const int m = ++n;
@@ -255,6 +282,11 @@ __global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, in
             }
             if (r >= 0) ++nf;
             __syncwarp();
+            // blocks touched: the popped slot's, the old last slot's, the new last slot's
+            const int bx = x >> 5, bl = last >> 5, bn = nf > 0 ? (nf - 1) >> 5 : bl;
+            refresh(bx, nf);
+            if (bl != bx) refresh(bl, nf);
+            if (bn != bx && bn != bl) refresh(bn, nf);
         }
         if (lane == 0) S.misc[0] = n;
     }

@@ -50,6 +50,7 @@ class Workload:
     cfg: int = 0         # workload family number (seed base)
     markov_norm: bool = False  # DARTree: full-vocabulary normalised correction
     verify_rule: str = ""      # acceptance rule at T=1 ("" = "ratio"; "iter_residual", "target_match")
+    H: int = 0                 # heap mode: TDES hidden units (0: the Markov term when R > 0)
 
     @property
     def Kc(self):
@@ -103,6 +104,29 @@ def dartree_normalised(beta):
     """The DARTree workload with the full-vocabulary normalised correction."""
     return dataclasses.replace(dartree_supertree(beta), markov_norm=True,
                                name="dartree_norm_b8_L16_V151936_W32_K16_B512_beta%g" % beta)
+
+
+def heap_markov(norm=False):
+    """The DARTree workload's shapes (b=8, L=16, K=16, B=512, R=64) built by the exact
+    best-first heap with the Markov correction (no width limit), optionally normalised."""
+    return Workload("heap_markov%s_b8_L16_V151936_K16_B512" % ("_norm" if norm else ""), "heap", 8, 16, V_QWEN3,
+                    "bf16", 3.0, 0.7, 0.0, K=16, B=512, R=64, markov_norm=norm, cfg=3)
+
+
+def heap_tdes(H=256):
+    """The same shapes with TDES edge scores (H hidden units, synthetic weights)."""
+    return Workload("heap_tdes_H%d_b8_L16_V151936_K16_B512" % H, "heap", 8, 16, V_QWEN3, "bf16", 3.0, 0.7, 0.0,
+                    K=16, B=512, H=H, cfg=3)
+
+
+def tdes_weights(V, L, H, device="cpu"):
+    """TDES first-layer rows Ap, Ac [V, H], depth rows Dd [L, H]: 0.3 N(0, 1); output
+    weights w [H]: N(0, 1/H); b0 = -0.1, s = 0.8; seeds 11-14."""
+    Ap = torch.randn((V, H), generator=_gen(11, device), device=device) * 0.3
+    Ac = torch.randn((V, H), generator=_gen(12, device), device=device) * 0.3
+    Dd = torch.randn((L, H), generator=_gen(13, device), device=device) * 0.3
+    w = torch.randn((H,), generator=_gen(14, device), device=device) * (1.0 / math.sqrt(H))
+    return Ap, Ac, Dd, w, -0.1, 0.8
 
 
 def talon_gated(N):

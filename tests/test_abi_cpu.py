@@ -184,3 +184,32 @@ def test_fused_entry_points_and_normalisation_reject_invalid_arguments():
     assert L.dt_markov_norm(ctypes.byref(s_noterm), fake, ctypes.byref(td), fake, 1 << 30, None) == -1
     # the allocation-free selection does not take the normalised correction
     assert L.dt_select_dartree_noalloc(ctypes.byref(s), ctypes.byref(td), None) == -2
+
+
+def test_heap_mode_rejects_invalid_arguments():
+    L = dtree.lib()
+    t = _FakeTree(1, 4, 4, 9).struct()
+    fake = ctypes.c_void_p(0x3000)
+    heap = dtree.Params(mode="heap", batch=1, L=4, V=32, dtype="bf16", K=4, B=8)
+    # no edge term: no workspace
+    w = ctypes.c_int(0)
+    assert L.dt_workspace_size(ctypes.byref(heap.struct()), ctypes.byref(w)) == 0 and w.value == 1
+    # a TDES scorer: an edge table of batch * L * K * K floats, rounded to 256 bytes
+    st = heap.struct()
+    tds = dtree.TdesStruct(8, fake, fake, fake, fake, 0.0, 1.0)
+    st.tdes = ctypes.pointer(tds)
+    assert L.dt_workspace_size(ctypes.byref(st), ctypes.byref(w)) == 256 and w.value == 1
+    assert L.dt_select(ctypes.byref(st), ctypes.byref(t), None, 0, None) == -1  # workspace missing
+    for bad in (dtree.TdesStruct(0, fake, fake, fake, fake, 0.0, 1.0),
+                dtree.TdesStruct(8, None, fake, fake, fake, 0.0, 1.0),
+                dtree.TdesStruct(8, fake, fake, fake, None, 0.0, 1.0)):
+        st.tdes = ctypes.pointer(bad)
+        assert L.dt_select(ctypes.byref(st), ctypes.byref(t), fake, 1 << 20, None) == -1
+    # the normaliser belongs to the Markov term, not to TDES
+    st.tdes = ctypes.pointer(tds)
+    st.markov_norm = 1
+    assert L.dt_select(ctypes.byref(st), ctypes.byref(t), fake, 1 << 20, None) == -1
+    # candidate lists longer than 256
+    big = dtree.Params(mode="heap", batch=1, L=4, V=1000, dtype="bf16", K=300, B=8)
+    assert L.dt_select(ctypes.byref(big.struct()), ctypes.byref(_FakeTree(1, 4, 300, 9).struct()), None, 0,
+                       None) == -2

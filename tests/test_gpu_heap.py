@@ -78,9 +78,8 @@ def _run(batch, L, V, K, B, seed, term=None, root=True, dtype="bf16", norm=False
         elif term == "tdes":
             E = oracle.tdes_table(ids, Ap.numpy(), Ac.numpy(), Dd.numpy(), w.numpy(), -0.1, 0.8, r)
             Eg = ws[0][:batch * L * K * K * 4].view(torch.float32).view(batch, L, K, K)[b].cpu().numpy()
-            rows = slice(None) if root else slice(1, None)  # without a root token row 0 is not written
             assert np.array_equal(Eg[1:], E[1:]), "TDES table"
-            if root:
+            if root:  # without a root token the depth-1 row is not written
                 assert np.array_equal(Eg[0, 0], E[0, 0]), "TDES root row"
         want = oracle.heap_select(lps, ids, B, E=E, znorm=zs.get(b))
         _same(gpu_tree(tree, b), want, (term, b))
