@@ -34,9 +34,12 @@ def lib():
                                     _f64p, _f32p, _i32p, _f32p]
         L.or_ddtree.argtypes = [_f32p, _i32p] + [ctypes.c_int] * 5 + [_i32p] * 4 + [_f32p, _i32p]
         L.or_dartree.argtypes = ([_f32p, _i32p, ctypes.c_int, ctypes.c_int, _f32p, _f32p,
-                                  ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_int, ctypes.c_float,
+                                  ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_int, _i32p, ctypes.c_float,
                                   ctypes.c_int, ctypes.c_int] + [_i32p] * 4 +
                                  [_f32p, _i32p, _i32p, _i32p])
+        L.or_uniform_widths.argtypes = [ctypes.c_int, ctypes.c_int, _i32p]
+        L.or_saba.argtypes = [_f32p, ctypes.c_int, _f32p, ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int, _f32p, _i32p]
         L.or_markov_norm.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _f32p, _f32p,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p]
         L.or_markov_table.argtypes = [_i32p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, ctypes.c_int,
@@ -147,7 +150,42 @@ def ddtree(cand_lp, cand_id, B, Mmax=None, rule=0):
     return t
 
 
-def dartree(cand_lp, cand_id, U, Vt, root_tok, W, beta, B, Mmax=None, znorm=None):
+def uniform_widths(B, L):
+    """DARTree (fixed): per-depth widths spreading B over L depths."""
+    w = np.zeros(L, np.int32)
+    _check(lib().or_uniform_widths(B, L, _p(w, ctypes.c_int32)), "uniform_widths")
+    return w
+
+
+class SabaState:
+    """One request's SABA history: a ring of the last w accepted lengths and a count."""
+
+    def __init__(self, w):
+        self.w = w
+        self.ring = np.zeros(w, np.int32)
+        self.count = np.zeros(1, np.int32)
+
+
+def saba(top_lp, hidden, st, prev_len, c_verify, c_fixed, B_min, B_max):
+    """SABA budget for one request: top_lp [D] (lp of each position's top candidate),
+    hidden [D, Hd] or None, st a SabaState (updated), prev_len the last round's
+    accepted length or -1.  Returns (budget, state [conf, degen, hist, a])."""
+    lp = _f32(top_lp)
+    D = lp.shape[0]
+    hp, Hd = None, 0
+    if hidden is not None:
+        hidden = _f32(hidden)
+        hp, Hd = _p(hidden, ctypes.c_float), hidden.shape[1]
+    state = np.zeros(4, np.float32)
+    b = np.zeros(1, np.int32)
+    _check(lib().or_saba(_p(lp, ctypes.c_float), D, hp, Hd, _p(st.ring, ctypes.c_int32),
+                         _p(st.count, ctypes.c_int32), st.w, int(prev_len), ctypes.c_float(c_verify),
+                         ctypes.c_float(c_fixed), B_min, B_max, _p(state, ctypes.c_float), _p(b, ctypes.c_int32)),
+           "saba")
+    return int(b[0]), state
+
+
+def dartree(cand_lp, cand_id, U, Vt, root_tok, W, beta, B, Mmax=None, znorm=None, widths=None):
     """DARTree supertree + deferred pruning.  Returns (tree, info, topb) with
     info = dict(topb_equals_bestfirst, violations, supertree_size).  znorm
     ([L, K] fp32 log-normalisers from markov_norm) selects the full-vocabulary
@@ -172,8 +210,12 @@ def dartree(cand_lp, cand_id, U, Vt, root_tok, W, beta, B, Mmax=None, znorm=None
     n = np.zeros(1, np.int32)
     info = np.zeros(3, np.int32)
     topb = np.full(Mmax, -1, np.int32)
+    wp = None
+    if widths is not None:
+        widths = _i32(widths)
+        wp = _p(widths, ctypes.c_int32)
     _check(lib().or_dartree(_p(lp, ctypes.c_float), _p(ids, ctypes.c_int32), L, K, Up, Vp, R,
-                            int(root_tok), zp, W, ctypes.c_float(beta), B, Mmax, *_tree_args(t),
+                            int(root_tok), zp, W, wp, ctypes.c_float(beta), B, Mmax, *_tree_args(t),
                             _p(n, ctypes.c_int32), _p(info, ctypes.c_int32),
                             _p(topb, ctypes.c_int32)), "dartree")
     t.n = int(n[0])

@@ -315,6 +315,8 @@ int or_ddtree(const float* lp, const int32_t* id, int L, int K, int B, int rule,
 /* a serial fmaf chain over R terms from 0.0f; at depth 1 the parent is the    */
 /* root, whose token is root_tok (no term when root_tok < 0).                  */
 /* Child score, in the algorithm's order: (s(parent) + log q~) + beta.         */
+/* widths (optional) gives each depth its own width, e.g. DARTree (fixed)'s    */
+/* uniform per-depth budget (or_uniform_widths).                               */
 /* Each depth keeps the W best children of all parents (shared node order).   */
 /* The final pruning takes T = TopB(S).  Lemma 1 proves TopB(S) equals the     */
 /* best-first heap over S when beta <= 0 and every log q~ <= 0.  This returns  */
@@ -339,12 +341,16 @@ static float or_markov(const float* U, const float* Vt, int R, int p, int c)
 int or_dartree(const float* lp, const int32_t* id, int L, int K,
                const float* U, const float* Vt, int R, int root_tok,
                const float* znorm /* nullable [L][K]: log-normalisers, see or_markov_norm */,
-               int W, float beta, int B, int Mmax,
+               int W, const int32_t* widths /* nullable [L]: width of each depth (<= W) */,
+               float beta, int B, int Mmax,
                int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
                float* score, int32_t* n_nodes, int32_t* info,
                int32_t* topb_out /* nullable [Mmax]: TopB(S) as supertree indices */)
 {
     if (L < 1 || L > OR_MAXL || K < 1 || W < 1 || B < 1 || Mmax < 1) return OR_EINVAL;
+    if (widths)
+        for (int d = 0; d < L; ++d)
+            if (widths[d] < 1 || widths[d] > W) return OR_EINVAL;
     if ((U == NULL) != (Vt == NULL)) return OR_EINVAL;
     int cap = 1 + W * L;
     or_node* S = (or_node*)calloc((size_t)cap, sizeof(or_node)); /* S[0] = root */
@@ -379,7 +385,8 @@ int or_dartree(const float* lp, const int32_t* id, int L, int K,
             }
         }
         qsort(kids, (size_t)nk, sizeof(or_node), or_cmp_node);
-        int keep = nk < W ? nk : W;
+        int Wd = widths ? widths[d - 1] : W;
+        int keep = nk < Wd ? nk : Wd;
         prev_lo = nS;
         for (int i = 0; i < keep; ++i) { S[nS] = kids[i]; S[nS].self = nS; ++nS; }
         prev_hi = nS;
@@ -436,6 +443,87 @@ int or_dartree(const float* lp, const int32_t* id, int L, int K,
     }
     free(h.a); free(out_of); free(order); free(sorted); free(S); free(kids);
     return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* DARTree (fixed): the node budget spread uniformly over the depths.          */
+/* [DARTree] experimental setup: the fixed variant allots the budget evenly to */
+/* the 16 depths (4 nodes per layer for B = 64).  When L does not divide B the */
+/* remainder goes one node each to the shallowest depths (nearest the root,    */
+/* the likeliest to be accepted).  The widths feed or_dartree; their sum is B, */
+/* so the deferred pruning keeps the whole supertree.                          */
+/* Pinned: B = 64, L = 16 gives 4 per layer (the page's figure); sums and      */
+/* spreads of every (B, L) (tests).                                            */
+/* ------------------------------------------------------------------------- */
+int or_uniform_widths(int B, int L, int32_t* widths)
+{
+    if (B < L || L < 1) return OR_EINVAL;
+    for (int d = 0; d < L; ++d) widths[d] = B / L + (d < B % L ? 1 : 0);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* SABA: state-aware budget allocation.                                        */
+/* [GRAFT] "State-aware budget allocation": the state s_t = [conf, degen,      */
+/* hist] with conf = mean over the D positions of the drafter's probability of */
+/* its top candidate, hist = mean acceptance over the last w rounds, degen =   */
+/* mean of the adjacent-position cosine similarities r_d = cos(h_d, h_{d+1})   */
+/* of the drafter's hidden states plus their growth r_{D-1} - r_1; gain        */
+/* G(B) = a * B^beta with beta = 0.5 and a = mean of (l + 1) over the last w   */
+/* accepted lengths l; cost C(B) = B * c_verify + c_fixed; B_t = argmax G / C. */
+/* As printed, a scales G and cancels in the argmax, which is therefore        */
+/* c_fixed / c_verify for every state (beta = 0.5; flagged, not repaired).     */
+/* Readings: hist and a use the rounds recorded so far when fewer than w       */
+/* (hist = 0, a = 1 with none); the argmax runs over the integers              */
+/* [B_min, B_max], the smallest B on ties, with U(B) evaluated in fp32 as      */
+/* (a * sqrtf(B)) / (B * c_verify + c_fixed), one rounding per operation.      */
+/* The history ring: before the state is read, prev_len (if >= 0) is stored at */
+/* ring[count % w] and count is incremented.  conf, degen in double.           */
+/* Pinned: argmax = c_fixed / c_verify when that is an integer in range, the    */
+/* clamps, independence from the history, hand-computed conf / degen / hist /  */
+/* a (tests).                                                                  */
+/* ------------------------------------------------------------------------- */
+int or_saba(const float* top_lp /* [D] lp of each position's top candidate */, int D,
+            const float* hidden /* nullable [D][Hd] */, int Hd,
+            int32_t* ring /* [w] */, int32_t* count, int w, int prev_len,
+            float c_verify, float c_fixed, int B_min, int B_max,
+            float* state /* [4]: conf, degen, hist, a */, int32_t* budget)
+{
+    if (D < 1 || w < 1 || B_min < 1 || B_max < B_min || !(c_verify > 0.0f) || !(c_fixed >= 0.0f)) return OR_EINVAL;
+    if (prev_len >= 0) { ring[*count % w] = prev_len; *count += 1; }
+    int n = *count < w ? *count : w;
+    int64_t sum = 0;
+    for (int i = 0; i < n; ++i) sum += ring[(*count - 1 - i) % w];
+    float hist = n ? (float)sum / (float)n : 0.0f;
+    float a = n ? (float)(sum + n) / (float)n : 1.0f;
+    double conf = 0.0;
+    for (int d = 0; d < D; ++d) conf += exp((double)top_lp[d]);
+    conf /= D;
+    double degen = 0.0;
+    if (hidden && D >= 2) {
+        double r0 = 0.0, rl = 0.0, rs = 0.0;
+        for (int d = 0; d + 1 < D; ++d) {
+            double dot = 0.0, n1 = 0.0, n2 = 0.0;
+            for (int k = 0; k < Hd; ++k) {
+                double x = hidden[(int64_t)d * Hd + k], y = hidden[(int64_t)(d + 1) * Hd + k];
+                dot += x * y; n1 += x * x; n2 += y * y;
+            }
+            double r = (n1 > 0.0 && n2 > 0.0) ? dot / sqrt(n1 * n2) : 0.0;
+            if (d == 0) r0 = r;
+            rl = r;
+            rs += r;
+        }
+        degen = rs / (D - 1) + (rl - r0);
+    }
+    int best = B_min;
+    float bu = -1.0f;
+    for (int B = B_min; B <= B_max; ++B) {
+        float u = (a * sqrtf((float)B)) / ((float)B * c_verify + c_fixed);
+        if (u > bu) { bu = u; best = B; }
+    }
+    state[0] = (float)conf; state[1] = (float)degen; state[2] = hist; state[3] = a;
+    *budget = best;
+    return OR_OK;
 }
 
 /* ------------------------------------------------------------------------- */
