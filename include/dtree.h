@@ -129,7 +129,17 @@ typedef struct {
                            aligned U, Vt.  0 = the unnormalised term. */
     const dt_tdes* tdes; /* DT_MODE_HEAP: TDES edge scorer, or NULL (then the
                            Markov term when R > 0, else no edge term) */
+    int32_t budget_policy; /* DT_BUDGET_*.  DARTree only: DT_BUDGET_UNIFORM is
+                           DARTree (fixed) ([DARTree] experimental setup):
+                           depth d keeps B/L children (one more for the first
+                           B%L depths), W is ignored, B >= L. */
+    const int32_t* budget; /* DDTree and HEAP: [batch] per-request node budgets
+                           (e.g. from dt_saba_budget), each clamped to [1, B];
+                           NULL: B for every request.  B still sizes the
+                           kernels and max_nodes. */
 } dt_build_params;
+#define DT_BUDGET_TOPB 0
+#define DT_BUDGET_UNIFORM 1
 
 /* Tree buffers (caller-owned device memory).  Node 0 of each request is the
  * root (token -1, parent -1, depth 0, rank -1, score 0); nodes 1..n-1 follow
@@ -337,6 +347,38 @@ dt_status dt_verify_rule(const dt_tree* tree, int32_t batch, int32_t V, int32_t 
                          const void* draft_logits, int32_t rule, const float* uniforms,
                          int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
                          float* visited_lse, dt_stream_t stream);
+
+/* SABA: state-aware per-request budgets ([GRAFT] "State-aware budget
+ * allocation").  For every request b, from the candidate tables in `tree`
+ * (dt_candidates), optional drafter hidden states and the acceptance history:
+ *   1. if prev_acc_len is given and prev_acc_len[b] >= 0, store it in the
+ *      ring: ring[b][count[b] % window] = prev_acc_len[b], count[b] += 1;
+ *   2. over the last n = min(count[b], window) rounds: hist = (sum l) / n,
+ *      a = (sum (l + 1)) / n (fp32; hist = 0, a = 1 with no history);
+ *   3. conf = mean over the L positions of exp(lp of the top candidate);
+ *      degen = mean of r_d = cos(h_d, h_{d+1}) plus r_{L-2} - r_0 (0 without
+ *      hidden states or with L = 1);
+ *   4. budget[b] = argmax over the integers B in [B_min, B_max] of
+ *      (a * sqrt(B)) / (B * c_verify + c_fixed) in fp32, one rounding per
+ *      operation, the smallest B on ties.  As the page prints the model, a
+ *      cancels and the optimum is c_fixed / c_verify for every state.
+ *   state[b] = (conf, degen, hist, a), fp32.
+ * hidden: NULL or [batch][L][Hd] fp32.  ring [batch][window] and count
+ * [batch] int32 are caller-owned, zeroed before the first round, updated in
+ * place.  budget [batch] int32 feeds dt_build_params.budget.  Returns
+ * DT_ERR_INVALID_ARG for window < 1, c_verify <= 0, c_fixed < 0, or B_min,
+ * B_max outside 1 <= B_min <= B_max <= 1024. */
+typedef struct {
+    int32_t window;     /* w: rounds of acceptance history */
+    float c_verify;     /* per-node verification cost */
+    float c_fixed;      /* fixed per-round cost */
+    int32_t B_min;
+    int32_t B_max;
+} dt_saba_params;
+dt_status dt_saba_budget(const dt_saba_params* q, const dt_tree* tree, int32_t batch,
+                         const float* hidden, int32_t Hd, const int32_t* prev_acc_len,
+                         int32_t* ring, int32_t* count, float* state, int32_t* budget,
+                         dt_stream_t stream);
 
 /* Allocation-free DARTree selection.  The pages have no counterpart: this is
  * a service to callers that cannot allocate device memory -- e.g. a serving

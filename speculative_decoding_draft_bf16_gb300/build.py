@@ -18,7 +18,8 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libdtree.so")
 
 SOURCES = ["dt_abi.cu", "kn1_candidates.cu", "kn1b_rows.cu", "kn2_ddtree.cu", "kn3_dartree.cu", "kn3n_norm.cu", "kn4_talon.cu",
-           "kn5_mask.cu", "kn6_verify.cu", "kn7_heap.cu"]
+           "kn5_mask.cu", "kn6_verify.cu", "kn7_heap.cu",
+           "kn9_saba.cu"]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off", "--fmad=false",

@@ -115,6 +115,11 @@ bool markov_on(const dt_build_params* p) {
     return (p->mode == DT_MODE_DARTREE || (p->mode == DT_MODE_HEAP && !p->tdes)) && p->R > 0 && p->U;
 }
 
+// DARTree layer width: W, or the largest per-depth width of the uniform budget.
+int dartree_w(const dt_build_params* p) {
+    return p->budget_policy == DT_BUDGET_UNIFORM ? (p->B + p->L - 1) / p->L : p->W;
+}
+
 // A per-request edge table lives in the workspace.
 bool table_on(const dt_build_params* p) { return markov_on(p) || (p->mode == DT_MODE_HEAP && p->tdes); }
 
@@ -134,8 +139,12 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
         if (p->K < 1 || p->K > p->V || p->K > DT_MAX_KC) return DT_ERR_INVALID_ARG;
         if (p->B < 1 || p->B > DT_MAX_NODES - 1) return DT_ERR_INVALID_ARG;
     }
+    if (p->budget_policy != DT_BUDGET_TOPB && p->budget_policy != DT_BUDGET_UNIFORM) return DT_ERR_INVALID_ARG;
+    if (p->budget_policy == DT_BUDGET_UNIFORM && (p->mode != DT_MODE_DARTREE || p->B < p->L)) return DT_ERR_INVALID_ARG;
+    if (p->budget && p->mode != DT_MODE_DDTREE && p->mode != DT_MODE_HEAP) return DT_ERR_INVALID_ARG;
     if (p->mode == DT_MODE_DARTREE) {
-        if (p->W < 1 || (long long)p->W * p->K > 4096 || (long long)p->W * p->L > 4096) return DT_ERR_INVALID_ARG;
+        const int W = dartree_w(p);
+        if (W < 1 || (long long)W * p->K > 4096 || (long long)W * p->L > 4096) return DT_ERR_INVALID_ARG;
         if (!(p->beta <= 0.f)) return DT_ERR_INVALID_ARG;  // Lemma 1 needs beta <= 0
         if (p->R < 0 || p->R > 1024) return DT_ERR_INVALID_ARG;
         if (p->R > 0 && (!p->U || !p->Vt)) return DT_ERR_INVALID_ARG;
@@ -144,7 +153,7 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
         if (p->markov_norm && (p->R == 0 || !p->U)) return DT_ERR_INVALID_ARG;  // nothing to normalise
         if (p->markov_norm && p->R != 64) return DT_ERR_UNSUPPORTED;           // tensor-core tile: R = 64
         if (p->markov_norm && ((((uintptr_t)p->U) | ((uintptr_t)p->Vt)) & 15u)) return DT_ERR_INVALID_ARG;
-        if (dt_kn3_select_smem_bytes(p->L, p->K, p->W, p->R > 0 && p->U) > kSmemMax) return DT_ERR_UNSUPPORTED;
+        if (dt_kn3_select_smem_bytes(p->L, p->K, W, p->R > 0 && p->U) > kSmemMax) return DT_ERR_UNSUPPORTED;
     }
     if (p->mode == DT_MODE_HEAP) {
         if (p->K > 256) return DT_ERR_UNSUPPORTED;
@@ -167,7 +176,8 @@ dt_status check_build(const dt_build_params* p, const dt_tree* t) {
     if (t->L != p->L) return DT_ERR_INVALID_ARG;
     if (t->max_nodes < budget_of(p) + 1 || t->max_nodes > DT_MAX_NODES) {
         // DARTree needs room for min(B, |S|) nodes; DDTree and TALON for their budget
-        if (!(p->mode == DT_MODE_DARTREE && t->max_nodes >= 1 + ((p->B < p->W * p->L) ? p->B : p->W * p->L) &&
+        if (!(p->mode == DT_MODE_DARTREE &&
+              t->max_nodes >= 1 + ((p->B < dartree_w(p) * p->L) ? p->B : dartree_w(p) * p->L) &&
               t->max_nodes <= DT_MAX_NODES))
             return DT_ERR_INVALID_ARG;
     }
@@ -274,7 +284,7 @@ static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspa
     switch (p->mode) {
         case DT_MODE_DDTREE:
             if (dt_kn2_smem_bytes(p->L, p->K, p->B) > kSmemMax) return DT_ERR_UNSUPPORTED;
-            e = dt_kn2_launch(p->batch, p->L, p->K, p->B, Mmax, t->cand_lp, t->cand_id, t->lse, t->node_tok,
+            e = dt_kn2_launch(p->batch, p->L, p->K, p->B, p->budget, Mmax, t->cand_lp, t->cand_id, t->lse, t->node_tok,
                               t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, mask, pos, pos_offset, st);
             break;
         case DT_MODE_DARTREE: {
@@ -283,7 +293,8 @@ static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspa
             const bool term = p->R > 0 && p->U;
             const float* znorm =
                 (term && p->markov_norm) ? (const float*)((const unsigned char*)workspace + DT_ZNORM_OFFSET(p)) : nullptr;
-            e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt, p->root_tok,
+            e = dt_kn3_launch(p->batch, p->L, p->V, p->K, dartree_w(p), p->budget_policy == DT_BUDGET_UNIFORM, p->B,
+                              p->beta, term ? p->R : 0, p->U, p->Vt, p->root_tok,
                               Mmax, t->cand_lp, t->cand_id, t->lse, term ? (float*)workspace : nullptr, znorm,
                               t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, mask, pos,
                               pos_offset, st);
@@ -306,7 +317,8 @@ static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspa
                                      ? (const float*)((const unsigned char*)workspace + DT_ZNORM_OFFSET(p))
                                      : nullptr;
             if (e == cudaSuccess)
-                e = dt_kn7_launch(p->batch, p->L, p->V, p->K, p->B, Mmax, t->cand_lp, t->cand_id, table, p->root_tok,
+                e = dt_kn7_launch(p->batch, p->L, p->V, p->K, p->B, p->budget, Mmax, t->cand_lp, t->cand_id, table,
+                                  p->root_tok,
                                   znorm, t->node_tok, t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status,
                                   st);
             break;
@@ -442,6 +454,19 @@ dt_status dt_verify_rule(const dt_tree* t, int32_t batch, int32_t V, int32_t dty
     return cuda_status(e);
 }
 
+dt_status dt_saba_budget(const dt_saba_params* q, const dt_tree* t, int32_t batch, const float* hidden, int32_t Hd,
+                         const int32_t* prev_acc_len, int32_t* ring, int32_t* count, float* state, int32_t* budget,
+                         dt_stream_t stream) {
+    if (!q || !t || batch < 1 || !ring || !count || !state || !budget || !t->cand_lp) return DT_ERR_INVALID_ARG;
+    if (t->L < 1 || t->L > DT_MAX_L || t->Kc < 1) return DT_ERR_INVALID_ARG;
+    if (q->window < 1 || !(q->c_verify > 0.f) || !(q->c_fixed >= 0.f)) return DT_ERR_INVALID_ARG;
+    if (q->B_min < 1 || q->B_max < q->B_min || q->B_max > DT_MAX_NODES - 1) return DT_ERR_INVALID_ARG;
+    if (hidden && Hd < 1) return DT_ERR_INVALID_ARG;
+    cudaError_t e = dt_kn9_launch(batch, t->L, t->Kc, t->cand_lp, hidden, Hd, prev_acc_len, ring, count, q->window,
+                                  q->c_verify, q->c_fixed, q->B_min, q->B_max, state, budget, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
 const char* dt_status_str(dt_status s) {
     switch (s) {
         case DT_OK: return "ok";
@@ -514,7 +539,8 @@ extern "C" dt_status dt_select_dartree_noalloc(const dt_build_params* p, dt_tree
         s = noalloc_table(&table);
         if (s != DT_OK) return s;
     }
-    cudaError_t e = dt_kn3_launch(p->batch, p->L, p->V, p->K, p->W, p->B, p->beta, term ? p->R : 0, p->U, p->Vt,
+    cudaError_t e = dt_kn3_launch(p->batch, p->L, p->V, p->K, dartree_w(p), p->budget_policy == DT_BUDGET_UNIFORM,
+                                  p->B, p->beta, term ? p->R : 0, p->U, p->Vt,
                                   p->root_tok, t->max_nodes, t->cand_lp, t->cand_id, t->lse, table, nullptr, t->node_tok,
                                   t->parent, t->depth, t->rank, t->score, t->n_nodes, t->status, nullptr, nullptr, 0,
                                   (cudaStream_t)stream);

@@ -71,7 +71,9 @@ cudaError_t dt_kn1b_launch(const void* logits, int dtype, int rows, int V, int K
 
 // DDTree selection (kn2_ddtree.cu).
 size_t dt_kn2_smem_bytes(int L, int K, int B);
-cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
+// budget: NULL, or [batch] per-request budgets clamped to [1, B] (B sizes the buffers).
+cudaError_t dt_kn2_launch(int batch, int L, int K, int B, const int32_t* budget, int Mmax, const float* cand_lp,
+                          const int32_t* cand_id,
                           const float* lse, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
                           float* score, int32_t* n_nodes, int32_t* status, uint32_t* mask, int32_t* pos,
                           int pos_offset, cudaStream_t st);
@@ -79,7 +81,8 @@ cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float*
 // DARTree Markov table + selection (kn3_dartree.cu).
 size_t dt_kn3_table_smem_bytes(int K, int R);
 size_t dt_kn3_select_smem_bytes(int L, int K, int W, int use_table);
-cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
+// wfix = 1: per-depth widths B/L (+1 for the first B%L depths), W their maximum.
+cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int wfix, int B, float beta, int R, const float* U,
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* lse, float* table, const float* znorm, int32_t* tok,
                           int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
@@ -95,7 +98,7 @@ cudaError_t dt_kn3_table_launch(int batch, int L, int V, int K, int R, const flo
 // the depth-1 term only when root_tok names a token.  Returns
 // cudaErrorInvalidValue when the shapes do not fit shared memory.
 size_t dt_kn7_smem_bytes(int L, int K, int B, int Mmax);
-cudaError_t dt_kn7_launch(int batch, int L, int V, int K, int B, int Mmax, const float* cand_lp,
+cudaError_t dt_kn7_launch(int batch, int L, int V, int K, int B, const int32_t* budget, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* table, const int32_t* root_tok, const float* znorm,
                           int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
                           int32_t* n_nodes, int32_t* status, cudaStream_t st);
@@ -105,6 +108,11 @@ size_t dt_kn8_smem_bytes(int K, int H);
 cudaError_t dt_kn8_launch(int batch, int L, int V, int K, int H, const float* Ap, const float* Ac, const float* Dd,
                           const float* w, float b0, float s, const int32_t* root_tok, const int32_t* cand_id,
                           float* table, cudaStream_t st);
+
+// SABA state and per-request budgets (kn9_saba.cu).
+cudaError_t dt_kn9_launch(int batch, int L, int Kc, const float* cand_lp, const float* hidden, int Hd,
+                          const int32_t* prev_len, int32_t* ring, int32_t* count, int w, float c_verify,
+                          float c_fixed, int B_min, int B_max, float* state, int32_t* budget, cudaStream_t st);
 
 // TALON selection (kn4_talon.cu).
 size_t dt_kn4_smem_bytes(int Kc, int N);

@@ -80,7 +80,8 @@ DT_DI bool c_before_cand(int i, unsigned long long y, int d, const float* cs, co
 
 __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_lp,
                                                  const int32_t* __restrict__ cand_id,
-                                                 const float* __restrict__ lse, int L, int K, int B, int Mmax,
+                                                 const float* __restrict__ lse, int L, int K, int Bcap,
+                                                 const int32_t* __restrict__ budget, int Mmax,
                                                  int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,
                                                  int32_t* __restrict__ o_dep, int32_t* __restrict__ o_rank,
                                                  float* __restrict__ o_score, int32_t* __restrict__ o_n,
@@ -92,9 +93,11 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
     __shared__ float chain[DT_MAX_L + 1];  // score of the rank-0 chain to each depth
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
-    Kn2Smem S = carve(smem, L, K, B);
+    Kn2Smem S = carve(smem, L, K, Bcap);
     dt_pdl_trigger();
     dt_pdl_wait();
+    // this request's budget (buffers are sized for Bcap)
+    const int B = budget ? min(Bcap, max(1, budget[b])) : Bcap;
     const float* lpb = cand_lp + (size_t)b * L * K;
     const bool lp_all = (size_t)L * K * 4 <= LP_ALL_BYTES;
     if (lp_all)
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
 
     for (int d = 2; d <= L; ++d) {
         const bool full0 = (nC == B);
-        const float tau0 = full0 ? (S.cs + cur * B)[B - 1] : 0.f;
+        const float tau0 = full0 ? (S.cs + cur * Bcap)[B - 1] : 0.f;
         // nothing at this depth or below can reach the current B-th score
         if (full0 && chain[d] < tau0) break;
         const float* lpd = S.lp;
@@ -141,15 +144,15 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
             const float lp0 = lpd[0];
             int cnt_local = 0;
             for (int i = tid; i < nC; i += NT)
-                cnt_local += ((S.cdep + cur * B)[i] == d - 1) &&
-                             (!full0 || __fadd_rn((S.cs + cur * B)[i], lp0) >= tau0);
+                cnt_local += ((S.cdep + cur * Bcap)[i] == d - 1) &&
+                             (!full0 || __fadd_rn((S.cs + cur * Bcap)[i], lp0) >= tau0);
             // compact with a scan over a per-thread strided layout
             int tot;
             int ex = dt_block_excl_scan<NT>(cnt_local, red, &tot);
             int w = ex;
             for (int i = tid; i < nC; i += NT)
-                if ((S.cdep + cur * B)[i] == d - 1 && (!full0 || __fadd_rn((S.cs + cur * B)[i], lp0) >= tau0))
-                    S.cand[w++] = ((unsigned long long)(S.clex + cur * B)[i] << 32) | (unsigned)i;
+                if ((S.cdep + cur * Bcap)[i] == d - 1 && (!full0 || __fadd_rn((S.cs + cur * Bcap)[i], lp0) >= tau0))
+                    S.cand[w++] = ((unsigned long long)(S.clex + cur * Bcap)[i] << 32) | (unsigned)i;
             if (tid == 0) { sh_nP = tot; sh_any = 0; }
             __syncthreads();
             // already in lexicographic order (e.g. the depth-1 nodes)? then no sort
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
         int lr_lo = 0;
         while (lr_lo < nP) {
             const bool full = (nC == B);
-            const float tau = full ? (S.cs + cur * B)[B - 1] : 0.f;
+            const float tau = full ? (S.cs + cur * Bcap)[B - 1] : 0.f;
             // children of each remaining parent that can still enter
             for (int j = tid; j < nP; j += NT) {
                 int cnt = 0;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     if (!full) {
                         cnt = K;
                     } else {
-                        const float sp = (S.cs + cur * B)[p];
+                        const float sp = (S.cs + cur * Bcap)[p];
                         int lo = 0, hi = K;
                         while (lo < hi) {
                             int mid = (lo + hi) >> 1;
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     }
                     const int j = lo;
                     const int r = g - S.pn[j];
-                    const float s = __fadd_rn((S.cs + cur * B)[S.pidx[j]], lpd[r]);
+                    const float s = __fadd_rn((S.cs + cur * Bcap)[S.pidx[j]], lpd[r]);
                     const uint32_t lex = ((uint32_t)j << 16) | (uint32_t)r;
                     S.cand[idx] = ((unsigned long long)dt_fkey(s) << 32) | (unsigned long long)(0xFFFFFFFFu - lex);
                 }
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     int lo = 0, hi = mm;
                     while (lo < hi) {
                         int mid = (lo + hi) >> 1;
-                        if (c_before_cand(i, S.cand[mid], d, (S.cs + cur * B), (S.cdep + cur * B), (S.cpar + cur * B), (S.clex + cur * B), S.pidx))
+                        if (c_before_cand(i, S.cand[mid], d, (S.cs + cur * Bcap), (S.cdep + cur * Bcap), (S.cpar + cur * Bcap), (S.clex + cur * Bcap), S.pidx))
                             hi = mid;
                         else
                             lo = mid + 1;
@@ -251,12 +254,12 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                 for (int i = tid; i < nC; i += NT) {
                     const int np = S.newpos[i];
                     if (np >= 0) {
-                        const int pp = (S.cpar + cur * B)[i];
-                        (S.cs + nx * B)[np] = (S.cs + cur * B)[i];
-                        (S.cpar + nx * B)[np] = pp < 0 ? -1 : S.newpos[pp];
-                        (S.crank + nx * B)[np] = (S.crank + cur * B)[i];
-                        (S.cdep + nx * B)[np] = (S.cdep + cur * B)[i];
-                        (S.clex + nx * B)[np] = (S.clex + cur * B)[i];
+                        const int pp = (S.cpar + cur * Bcap)[i];
+                        (S.cs + nx * Bcap)[np] = (S.cs + cur * Bcap)[i];
+                        (S.cpar + nx * Bcap)[np] = pp < 0 ? -1 : S.newpos[pp];
+                        (S.crank + nx * Bcap)[np] = (S.crank + cur * Bcap)[i];
+                        (S.cdep + nx * Bcap)[np] = (S.cdep + cur * Bcap)[i];
+                        (S.clex + nx * Bcap)[np] = (S.clex + cur * Bcap)[i];
                     }
                 }
                 // ... and of every candidate
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     int lo = 0, hi = nC;
                     while (lo < hi) {
                         int mid = (lo + hi) >> 1;
-                        if (c_before_cand(mid, y, d, (S.cs + cur * B), (S.cdep + cur * B), (S.cpar + cur * B), (S.clex + cur * B), S.pidx))
+                        if (c_before_cand(mid, y, d, (S.cs + cur * Bcap), (S.cdep + cur * Bcap), (S.cpar + cur * Bcap), (S.clex + cur * Bcap), S.pidx))
                             lo = mid + 1;
                         else
                             hi = mid;
@@ -274,11 +277,11 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     if (nr < B) {
                         const uint32_t lex = 0xFFFFFFFFu - (uint32_t)y;
                         const int j = (int)(lex >> 16);
-                        (S.cs + nx * B)[nr] = dt_fkey_val((uint32_t)(y >> 32));
-                        (S.cpar + nx * B)[nr] = S.newpos[S.pidx[j]];
-                        (S.crank + nx * B)[nr] = (int)(lex & 0xFFFFu);
-                        (S.cdep + nx * B)[nr] = d;
-                        (S.clex + nx * B)[nr] = lex;
+                        (S.cs + nx * Bcap)[nr] = dt_fkey_val((uint32_t)(y >> 32));
+                        (S.cpar + nx * Bcap)[nr] = S.newpos[S.pidx[j]];
+                        (S.crank + nx * Bcap)[nr] = (int)(lex & 0xFFFFu);
+                        (S.cdep + nx * Bcap)[nr] = d;
+                        (S.clex + nx * Bcap)[nr] = lex;
                     }
                 }
                 __syncthreads();
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
         if (tid == 0) sh_any = 0;
         __syncthreads();
         for (int i = tid; i < nC; i += NT)
-            if ((S.cdep + cur * B)[i] == d) sh_any = 1;
+            if ((S.cdep + cur * Bcap)[i] == d) sh_any = 1;
         __syncthreads();
         if (!sh_any) break;
     }
@@ -304,13 +307,13 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
     // ---- output: root, then C in order -----------------------------------
     const size_t ob = (size_t)b * Mmax;
     for (int i = tid; i < nC; i += NT) {
-        const int dd = (S.cdep + cur * B)[i];
-        const int rr = (S.crank + cur * B)[i];
+        const int dd = (S.cdep + cur * Bcap)[i];
+        const int rr = (S.crank + cur * Bcap)[i];
         o_tok[ob + i + 1] = cand_id[((size_t)b * L + dd - 1) * K + rr];
-        o_par[ob + i + 1] = (S.cpar + cur * B)[i] + 1;
+        o_par[ob + i + 1] = (S.cpar + cur * Bcap)[i] + 1;
         o_dep[ob + i + 1] = dd;
         o_rank[ob + i + 1] = rr;
-        o_score[ob + i + 1] = (S.cs + cur * B)[i];
+        o_score[ob + i + 1] = (S.cs + cur * Bcap)[i];
     }
     if (tid == 0) {
         o_tok[ob] = -1;
@@ -341,7 +344,8 @@ size_t dt_kn2_smem_bytes(int L, int K, int B) {
            (size_t)(B + 1) * 4 + 16;
 }
 
-cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float* cand_lp, const int32_t* cand_id,
+cudaError_t dt_kn2_launch(int batch, int L, int K, int B, const int32_t* budget, int Mmax, const float* cand_lp,
+                          const int32_t* cand_id,
                           const float* lse, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank,
                           float* score, int32_t* n_nodes, int32_t* status, uint32_t* mask, int32_t* pos,
                           int pos_offset, cudaStream_t st) {
@@ -349,6 +353,6 @@ cudaError_t dt_kn2_launch(int batch, int L, int K, int B, int Mmax, const float*
     cudaError_t e = cudaFuncSetAttribute(kn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     DtLaunch lc(dim3(batch), dim3(NT), smem, st);
-    return cudaLaunchKernelEx(&lc.cfg, kn2_kernel, cand_lp, cand_id, lse, L, K, B, Mmax, tok, parent, depth, rank,
+    return cudaLaunchKernelEx(&lc.cfg, kn2_kernel, cand_lp, cand_id, lse, L, K, B, budget, Mmax, tok, parent, depth, rank,
                               score, n_nodes, status, mask, pos, pos_offset);
 }

@@ -126,7 +126,7 @@ DT_DI Kn3Smem kn3_carve(unsigned char* p, int L, int K, int W, bool stage_tab) {
     return m;
 }
 
-__global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int B, float beta, int use_table,
+__global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int wfix, int B, float beta, int use_table,
                                                         const int32_t* __restrict__ root_tok, int V,
                                                         int Mmax, const float* __restrict__ cand_lp,
                                                         const int32_t* __restrict__ cand_id,
@@ -187,7 +187,9 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
             const uint32_t lx = ((uint32_t)j << 16) | (uint32_t)r;
             return ((unsigned long long)dt_fkey(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - lx);
         };
-        const int keep = min(W, m);
+        // layer width: W, or (DARTree fixed) B spread over the depths, the
+        // remainder to the shallowest ones (W is then the largest of them)
+        const int keep = min(wfix ? B / L + (d - 1 < B % L ? 1 : 0) : W, m);
         if (W <= 32) {
             // top-W: warp sorts merged in a tree; the layer's lexicographic
             // order by warp 0 alone
@@ -393,7 +395,7 @@ cudaError_t dt_kn3_table_launch(int batch, int L, int V, int K, int R, const flo
     return cudaLaunchKernelEx(&lt.cfg, kn3_table_kernel, L, K, R, V, U, Vt, root_tok, cand_id, table);
 }
 
-cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float beta, int R, const float* U,
+cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int wfix, int B, float beta, int R, const float* U,
                           const float* Vt, const int32_t* root_tok, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* lse, float* table, const float* znorm, int32_t* tok,
                           int32_t* parent, int32_t* depth, int32_t* rank, float* score, int32_t* n_nodes,
@@ -415,7 +417,7 @@ cudaError_t dt_kn3_launch(int batch, int L, int V, int K, int W, int B, float be
         cudaSuccess)
         return e;
     DtLaunch ls(dim3(batch), dim3(NT), sm, st);
-    return cudaLaunchKernelEx(&ls.cfg, kn3_select_kernel, L, K, W, B, beta, use_table, root_tok, V, Mmax, cand_lp,
+    return cudaLaunchKernelEx(&ls.cfg, kn3_select_kernel, L, K, W, wfix, B, beta, use_table, root_tok, V, Mmax, cand_lp,
                               cand_id, lse, (const float*)table, znorm, tok, parent, depth, rank, score, n_nodes,
                               status, mask, pos, pos_offset);
 }

@@ -157,7 +157,8 @@ DT_DI bool entry_before(const Kn7Smem& S, int a, float sa, int b, float sb) {
     return desc_less(S, S.fp[a], S.fj[a], S.fp[b], S.fj[b]);
 }
 
-__global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, int Mmax,
+__global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, const int32_t* __restrict__ budget,
+                                                  int Mmax,
                                                   const float* __restrict__ cand_lp,
                                                   const int32_t* __restrict__ cand_id,
                                                   const float* __restrict__ table,
@@ -221,7 +222,8 @@ __global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, in
         };
         int nf = 1, n = 0;
         refresh(0, nf);
-        while (n < B && nf > 0) {
+        const int Bq = budget ? min(B, max(1, budget[b])) : B;  // this request's budget
+        while (n < Bq && nf > 0) {
             if (n + 1 >= Mmax) break;  // the host checks max_nodes > B; never taken
             const uint32_t g = __reduce_max_sync(0xffffffffu, bk0 > bk1 ? bk0 : bk1);
             const unsigned h0 = __ballot_sync(0xffffffffu, bk0 == g), h1 = __ballot_sync(0xffffffffu, bk1 == g);
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(NT8) kn8_kernel(int L, int K, int H, int V, co
 
 size_t dt_kn7_smem_bytes(int L, int K, int B, int Mmax) { return kn7_layout(L, K, B, Mmax, nullptr, nullptr); }
 
-cudaError_t dt_kn7_launch(int batch, int L, int V, int K, int B, int Mmax, const float* cand_lp,
+cudaError_t dt_kn7_launch(int batch, int L, int V, int K, int B, const int32_t* budget, int Mmax, const float* cand_lp,
                           const int32_t* cand_id, const float* table, const int32_t* root_tok, const float* znorm,
                           int32_t* tok, int32_t* parent, int32_t* depth, int32_t* rank, float* score,
                           int32_t* n_nodes, int32_t* status, cudaStream_t st) {
@@ -376,7 +378,7 @@ cudaError_t dt_kn7_launch(int batch, int L, int V, int K, int B, int Mmax, const
     cudaError_t e = cudaFuncSetAttribute(kn7_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     DtLaunch lc(dim3(batch), dim3(NT7), sm, st);
-    return cudaLaunchKernelEx(&lc.cfg, kn7_kernel, L, V, K, B, Mmax, cand_lp, cand_id, table, root_tok, znorm, tok,
+    return cudaLaunchKernelEx(&lc.cfg, kn7_kernel, L, V, K, B, budget, Mmax, cand_lp, cand_id, table, root_tok, znorm, tok,
                               parent, depth, rank, score, n_nodes, status);
 }
 

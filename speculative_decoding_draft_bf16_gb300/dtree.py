@@ -16,6 +16,7 @@ import torch
 from . import build as _build
 
 DT_MODE = {"ddtree": 0, "dartree": 1, "talon": 2, "heap": 3}
+BUDGET_POLICY = {"topb": 0, "uniform": 1}
 DT_BF16, DT_F32 = 0, 1
 DT_DEV_BAD_TREE, DT_DEV_TIMEOUT, DT_DEV_BESTFIRST = 0x1, 0x2, 0x4
 DT_DEV_VIOLATION_SHIFT = 8
@@ -39,7 +40,12 @@ class BuildParams(ctypes.Structure):
                 ("K", _i32), ("B", _i32), ("W", _i32), ("beta", ctypes.c_float), ("R", _i32),
                 ("U", _vp), ("Vt", _vp), ("root_tok", _vp), ("talon_k", _i32),
                 ("log_mu", ctypes.c_float), ("N", _i32), ("markov_norm", _i32),
-                ("tdes", ctypes.POINTER(TdesStruct))]
+                ("tdes", ctypes.POINTER(TdesStruct)), ("budget_policy", _i32), ("budget", _vp)]
+
+
+class SabaStruct(ctypes.Structure):
+    _fields_ = [("window", _i32), ("c_verify", ctypes.c_float), ("c_fixed", ctypes.c_float), ("B_min", _i32),
+                ("B_max", _i32)]
 
 
 class TreeStruct(ctypes.Structure):
@@ -76,6 +82,8 @@ def lib():
         L.dt_tree_mask.restype = _i32
         L.dt_tree_mask.argtypes = [tp, _i32, _i32, _vp, _vp, _vp]
         L.dt_verify.restype = _i32
+        L.dt_saba_budget.restype = _i32
+        L.dt_saba_budget.argtypes = [ctypes.POINTER(SabaStruct), tp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
         L.dt_verify_rule.restype = _i32
         L.dt_verify_rule.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
         L.dt_verify.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
@@ -146,6 +154,8 @@ class Params:
     N: int = 0
     markov_norm: bool = False  # DARTree: full-vocabulary normalised correction
     tdes: "Tdes" = None        # heap mode: TDES edge scorer
+    budget_policy: str = "topb"  # DARTree: "uniform" = DARTree (fixed), per-depth widths from B
+    budgets: torch.Tensor = None  # DDTree / heap: [batch] int32 per-request budgets (dt_build_params.budget)
 
     @property
     def Kc(self):
@@ -166,6 +176,10 @@ class Params:
         if self.tdes is not None:
             bp._tdes = self.tdes.struct()  # kept alive with the parameter block
             bp.tdes = ctypes.pointer(bp._tdes)
+        bp.budget_policy = BUDGET_POLICY[self.budget_policy]
+        if self.budgets is not None:
+            _need(self.budgets, torch.int32, "budgets")
+            bp.budget = _ptr(self.budgets)
         return bp
 
 
@@ -349,3 +363,31 @@ def alloc_verify_out(tree, device="cuda"):
     return (torch.full((tree.batch, tree.L + 1), -1, dtype=torch.int32, device=device),
             torch.zeros((tree.batch,), dtype=torch.int32, device=device),
             torch.zeros((tree.batch,), dtype=torch.int32, device=device))
+
+
+class SabaState:
+    """Device SABA history for a batch: ring [batch, window] and count [batch] (int32, zeroed)."""
+
+    def __init__(self, batch, window, device="cuda"):
+        self.window = window
+        self.ring = torch.zeros((batch, window), dtype=torch.int32, device=device)
+        self.count = torch.zeros((batch,), dtype=torch.int32, device=device)
+
+
+def saba_budget(tree, st, c_verify, c_fixed, B_min, B_max, budget, state, hidden=None, prev_acc_len=None,
+                batch=None, stream=None):
+    """dt_saba_budget: per-request budgets [batch] int32 and state [batch, 4] fp32 (conf, degen, hist, a);
+    hidden: optional [batch, L, Hd] fp32 drafter hidden states; prev_acc_len: last round's acc_len."""
+    batch = batch or tree.batch
+    _need(budget, torch.int32, "budget")
+    _need(state, torch.float32, "state")
+    Hd = 0
+    if hidden is not None:
+        _need(hidden, torch.float32, "hidden")
+        Hd = int(hidden.shape[-1])
+    if prev_acc_len is not None:
+        _need(prev_acc_len, torch.int32, "prev_acc_len")
+    q = SabaStruct(st.window, float(c_verify), float(c_fixed), int(B_min), int(B_max))
+    _check(lib().dt_saba_budget(ctypes.byref(q), ctypes.byref(tree.struct()), batch, _ptr(hidden), Hd,
+                                _ptr(prev_acc_len), _ptr(st.ring), _ptr(st.count), _ptr(state), _ptr(budget),
+                                _stream(stream)), "dt_saba_budget")

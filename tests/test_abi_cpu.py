@@ -213,3 +213,29 @@ def test_heap_mode_rejects_invalid_arguments():
     big = dtree.Params(mode="heap", batch=1, L=4, V=1000, dtype="bf16", K=300, B=8)
     assert L.dt_select(ctypes.byref(big.struct()), ctypes.byref(_FakeTree(1, 4, 300, 9).struct()), None, 0,
                        None) == -2
+
+
+def test_budget_policies_reject_invalid_arguments():
+    L = dtree.lib()
+    fake = ctypes.c_void_p(0x3000)
+    t = _FakeTree(2, 4, 4, 9).struct()
+    # uniform per-depth budgets are DARTree's; per-request budgets are DDTree's and the heap's
+    bad = [dtree.Params(mode="ddtree", batch=2, L=4, V=32, dtype="bf16", K=4, B=8, budget_policy="uniform")]
+    st = dtree.Params(mode="dartree", batch=2, L=4, V=32, dtype="bf16", K=4, W=2, B=8).struct()
+    st.budget = fake
+    st2 = dtree.Params(mode="dartree", batch=2, L=4, V=32, dtype="bf16", K=4, W=2, B=3,
+                       budget_policy="uniform").struct()  # B < L
+    st3 = dtree.Params(mode="ddtree", batch=2, L=4, V=32, dtype="bf16", K=4, B=8).struct()
+    st3.budget_policy = 7
+    for s in [b.struct() for b in bad] + [st, st2, st3]:
+        assert L.dt_select(ctypes.byref(s), ctypes.byref(t), None, 0, None) == -1
+    # SABA parameters
+    tr = _FakeTree(2, 4, 4, 9).struct()
+    for q in (dtree.SabaStruct(0, 1.0, 1.0, 1, 8), dtree.SabaStruct(4, 0.0, 1.0, 1, 8),
+              dtree.SabaStruct(4, 1.0, -1.0, 1, 8), dtree.SabaStruct(4, 1.0, 1.0, 0, 8),
+              dtree.SabaStruct(4, 1.0, 1.0, 9, 8), dtree.SabaStruct(4, 1.0, 1.0, 1, 2000)):
+        assert L.dt_saba_budget(ctypes.byref(q), ctypes.byref(tr), 2, None, 0, None, fake, fake, fake, fake,
+                                None) == -1
+    ok = dtree.SabaStruct(4, 1.0, 1.0, 1, 8)
+    assert L.dt_saba_budget(ctypes.byref(ok), ctypes.byref(tr), 2, None, 0, None, None, fake, fake, fake, None) == -1
+    assert L.dt_saba_budget(ctypes.byref(ok), ctypes.byref(tr), 2, fake, 0, None, fake, fake, fake, fake, None) == -1
