@@ -74,6 +74,8 @@ def workloads():
         "dartree_beta0": wk.dartree_supertree(0.0),
         "dartree_beta-0.5": wk.dartree_supertree(-0.5),
         "dartree_norm_beta0": wk.dartree_normalised(0.0),
+        "dartree_fixed": wk.dartree_fixed(),
+        "ddtree_saba_b16": wk.ddtree_saba(16),
         "heap_markov": wk.heap_markov(False),
         "heap_markov_norm": wk.heap_markov(True),
         "heap_tdes": wk.heap_tdes(256),
@@ -129,7 +131,7 @@ def normaliser_roofline(wl, stage_us, peaks):
         "note": "one exp per (row, token) in the epilogue: %.0f M per launch" % (rows * wl.V / 1e6)}}
 
 
-def params_for(wl, U=None, Vt=None, tdes=None):
+def params_for(wl, U=None, Vt=None, tdes=None, budgets=None):
     from speculative_decoding_draft_bf16_gb300 import dtree
     td = None
     if tdes is not None:
@@ -137,7 +139,7 @@ def params_for(wl, U=None, Vt=None, tdes=None):
         td = dtree.Tdes(Ap, Ac, Dd, w, b0=b0, s=s)
     return dtree.Params(mode=wl.mode, batch=wl.batch, L=wl.L, V=wl.V, dtype=wl.dtype, K=wl.K, B=wl.B, W=wl.W,
                         beta=wl.beta, R=wl.R, U=U, Vt=Vt, talon_k=wl.talon_k, mu=wl.mu, N=wl.N,
-                        markov_norm=wl.markov_norm, tdes=td)
+                        markov_norm=wl.markov_norm, tdes=td, budget_policy=wl.budget_policy, budgets=budgets)
 
 
 def max_nodes_of(wl):
@@ -215,7 +217,12 @@ def run_ours(args, wl, rank, world, local):
         U, Vt = wk.markov_tables(wl.V, wl.R, device=dev)
     if wl.H > 0:
         tdes = wk.tdes_weights(wl.V, wl.L, wl.H, device=dev)
-    p = params_for(wl, U, Vt, tdes)
+    saba = None
+    if wl.saba_cv > 0:  # one history for the batch rows; the budgets feed the selection
+        saba = dict(st=dtree.SabaState(wl.batch, 8, device=dev),
+                    budget=torch.full((wl.batch,), wl.B, dtype=torch.int32, device=dev),
+                    state=torch.zeros((wl.batch, 4), device=dev))
+    p = params_for(wl, U, Vt, tdes, saba["budget"] if saba else None)
     Mmax = max_nodes_of(wl)
     esize = 2 if wl.dtype == "bf16" else 4
     draft_bytes = wl.batch * wl.L * wl.V * esize
@@ -242,6 +249,10 @@ def run_ours(args, wl, rank, world, local):
         copies.append(dict(x=x, tree=tree, ws=ws, tgt=tgt, uni=uni, mask=mask, pos=pos, out=out))
 
     def step(c, stages=("buildmask", "verify")):
+        if saba is not None and ("buildmask" in stages or "saba" in stages):
+            # SABA from this copy's previous round: its stage-1 tables and accepted lengths
+            dtree.saba_budget(c["tree"], saba["st"], wl.saba_cv, wl.saba_cf, 1, wl.B, saba["budget"],
+                              saba["state"], prev_acc_len=c["out"][1])
         if "buildmask" in stages:  # stage 1, selection, and the mask written by the selection kernel
             dtree.build_tree_mask(p, c["x"], c["tree"], c["mask"], c["pos"], workspace=c["ws"])
         if "build" in stages:
@@ -328,6 +339,8 @@ def run_ours(args, wl, rank, world, local):
                   ("mask", ("mask",)), ("verify", ("verify",))]
     if wl.markov_norm:
         stage_list.insert(1, ("normalise", ("norm",)))
+    if saba is not None:
+        stage_list.insert(1, ("saba", ("saba",)))
     for name, stages in stage_list:
         n = max(R, (args.steps // R) * R)
         stage_us[name] = timed(stages, n, R) * 1000.0 / n
@@ -379,7 +392,7 @@ def run_ours(args, wl, rank, world, local):
     # edge table; the normalised correction's table conversion, normaliser and merge
     edge_table = wl.mode in ("dartree", "heap") and (wl.R > 0 or wl.H > 0)
     launches_per_step = (3 + (1 if wl.mode == "heap" else 0) + (1 if edge_table else 0) +
-                         (3 if wl.markov_norm else 0))
+                         (3 if wl.markov_norm else 0) + (1 if saba is not None else 0))
     kn1_s = stage_us["candidates"] / 1e6
     achieved = draft_bytes / kn1_s / 1e9
     peaks = {}
@@ -409,7 +422,9 @@ def run_ours(args, wl, rank, world, local):
         "data": "synthetic (seeded Gaussian logits with confident-token spikes; Qwen3 vocabulary)",
         "config": {"workload": wl.name, "mode": wl.mode, "batch_per_gpu": wl.batch, "L": wl.L, "V": wl.V,
                    "K": wl.K, "B": wl.B, "W": wl.W, "beta": wl.beta, "N": wl.N, "R": wl.R, "H": wl.H,
-                   "markov_norm": wl.markov_norm, "temperature": temperature,
+                   "markov_norm": wl.markov_norm, "budget_policy": wl.budget_policy,
+                   "saba": {"c_verify": wl.saba_cv, "c_fixed": wl.saba_cf} if saba is not None else None,
+                   "temperature": temperature,
                    "verify_rule": wl.verify_rule or ("ratio" if temperature else "greedy"),
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d input copies (drafter logits %.0f MB > 2x L2)" % (R, R * draft_bytes / 1e6)},
@@ -438,10 +453,15 @@ def oracle_round(wl, x, tgt, uni, M):
     Mmax = max_nodes_of(wl)
     U, Vt = M["U"], M["Vt"]
     if wl.mode == "ddtree":
-        t = oracle.ddtree(lps, ids, wl.B, Mmax=Mmax)
+        B = wl.B
+        if wl.saba_cv > 0:  # SABA budget from this tree's state (no history yet)
+            B, _ = oracle.saba(lps[:, 0], None, oracle.SabaState(8), -1, wl.saba_cv, wl.saba_cf, 1, wl.B)
+        t = oracle.ddtree(lps, ids, B, Mmax=Mmax)
     elif wl.mode == "dartree":
         z = oracle.markov_norm(x, ids, U, Vt, -1) if wl.markov_norm else None
-        t, _, _ = oracle.dartree(lps, ids, U, Vt, -1, wl.W, wl.beta, wl.B, Mmax=Mmax, znorm=z)
+        widths = oracle.uniform_widths(wl.B, wl.L) if wl.budget_policy == "uniform" else None
+        W = int(widths.max()) if widths is not None else wl.W
+        t, _, _ = oracle.dartree(lps, ids, U, Vt, -1, W, wl.beta, wl.B, Mmax=Mmax, znorm=z, widths=widths)
     elif wl.mode == "heap":
         z = E = None
         if M["tdes"] is not None:

@@ -51,6 +51,9 @@ class Workload:
     markov_norm: bool = False  # DARTree: full-vocabulary normalised correction
     verify_rule: str = ""      # acceptance rule at T=1 ("" = "ratio"; "iter_residual", "target_match")
     H: int = 0                 # heap mode: TDES hidden units (0: the Markov term when R > 0)
+    budget_policy: str = "topb"  # DARTree: "uniform" = DARTree (fixed)
+    saba_cv: float = 0.0       # SABA per-node verification cost (0: no SABA)
+    saba_cf: float = 0.0       # SABA fixed per-round cost
 
     @property
     def Kc(self):
@@ -104,6 +107,18 @@ def dartree_normalised(beta):
     """The DARTree workload with the full-vocabulary normalised correction."""
     return dataclasses.replace(dartree_supertree(beta), markov_norm=True,
                                name="dartree_norm_b8_L16_V151936_W32_K16_B512_beta%g" % beta)
+
+
+def dartree_fixed():
+    """DARTree (fixed) at the pages' default: b=8, L=16, K=64, B=64 spread as 4 nodes per depth, R=64."""
+    return Workload("dartree_fixed_b8_L16_V151936_K64_B64", "dartree", 8, 16, V_QWEN3, "bf16", 3.0, 0.7, 0.0,
+                    K=64, B=64, W=4, R=64, budget_policy="uniform", cfg=3)
+
+
+def ddtree_saba(batch=16):
+    """DDTree with SABA budgets (c_verify 0.5, c_fixed 64: B_t = 128 of at most 256), greedy."""
+    return Workload("ddtree_saba_b%d_L16_V151936_K256_Bmax256" % batch, "ddtree", batch, 16, V_QWEN3, "bf16",
+                    3.0, 0.7, 0.0, K=256, B=256, saba_cv=0.5, saba_cf=64.0, cfg=2)
 
 
 def heap_markov(norm=False):
