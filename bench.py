@@ -40,11 +40,18 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel, keyed by (kernel, workload, sha1 of the kernel's sources when the
 # capture was taken); a changed kernel reports null until it is captured again.
 KN1_TRAFFIC = {
-    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', 'e191525f2920d993c087cc777a01718198052a7c'): 4932000,
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 38962500,
-    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 78785500,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 315424500,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', 'b009f141508188da5ce1a39c55a797fde3d29c8f'): 346304500,
+    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', 'e472a2dfd8ec0ad0ca4c3125948646905931dcf0'): 4932779,
+    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962261,
+    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 78582613,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 315160235,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 346956800,
+    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38963200,
+    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,
+    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 78582613,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 78582613,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
 }
 STAGE1_SOURCES = {
     "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),
