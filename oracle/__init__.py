@@ -58,6 +58,9 @@ def lib():
                                     ctypes.c_int, _f32p, _f32p, _f32p, ctypes.c_int, _f32p,
                                     _f32p, _i32p, _i32p, _i32p, _f32p])
         L.or_verify_iter_residual.argtypes = L.or_verify_t1.argtypes
+        L.or_verify_t1_markov.argtypes = ([_i32p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           _f32p, _f32p, _f32p, ctypes.c_int, _f32p, _f32p, ctypes.c_int,
+                                           ctypes.c_int, _f32p, ctypes.c_int, _f32p, _f32p, _i32p, _i32p, _i32p])
         L.or_verify_target_match.argtypes = ([_i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               _f32p, ctypes.c_int, _f32p, _f32p, _i32p, _i32p, _i32p, _f32p])
         L.or_spec_scalar.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_double,
@@ -363,6 +366,31 @@ def verify_t1(tree, target, draft, draft_lse, uniforms, L, Mmax, lse_in=None, ru
                             _p(nxt, ctypes.c_int32), _p(lse_out, ctypes.c_float))
     _check(rc, "verify_t1 " + rule)
     return acc, int(alen[0]), int(nxt[0]), lse_out
+
+
+def verify_t1_markov(tree, target, draft, draft_lse, U, Vt, root_tok, znorm, uniforms, L, Mmax, lse_in=None):
+    """T=1 walk against the normalised DARTree proposal q~(. | parent token);
+    znorm: [L, K] log-normalisers (markov_norm).  Returns (acc_nodes, acc_len, next_tok)."""
+    target, draft, draft_lse = _f32(target), _f32(draft), _f32(draft_lse)
+    U, Vt, z, u = _f32(U), _f32(Vt), _f32(znorm), _f32(uniforms)
+    assert u.shape == (2, Mmax)
+    V = target.shape[-1]
+    acc = np.empty(L + 1, np.int32)
+    alen = np.zeros(1, np.int32)
+    nxt = np.zeros(1, np.int32)
+    tok, par, dep, rnk = _i32(tree.tok), _i32(tree.parent), _i32(tree.depth), _i32(tree.rank)
+    lin = None
+    if lse_in is not None:
+        lse_in = _f32(lse_in)
+        lin = _p(lse_in, ctypes.c_float)
+    rc = lib().or_verify_t1_markov(_p(tok, ctypes.c_int32), _p(par, ctypes.c_int32), _p(dep, ctypes.c_int32),
+                                   _p(rnk, ctypes.c_int32), tree.n, L, Mmax, _p(target, ctypes.c_float),
+                                   _p(draft, ctypes.c_float), _p(draft_lse, ctypes.c_float), V,
+                                   _p(U, ctypes.c_float), _p(Vt, ctypes.c_float), U.shape[1], int(root_tok),
+                                   _p(z, ctypes.c_float), z.shape[-1], _p(u, ctypes.c_float), lin,
+                                   _p(acc, ctypes.c_int32), _p(alen, ctypes.c_int32), _p(nxt, ctypes.c_int32))
+    _check(rc, "verify_t1_markov")
+    return acc, int(alen[0]), int(nxt[0])
 
 
 def verify_target_match(tree, target, uniforms, L, Mmax, lse_in=None):

@@ -1042,6 +1042,95 @@ int or_verify_t1(const int32_t* tok, const int32_t* parent, const int32_t* depth
 }
 
 /* ------------------------------------------------------------------------- */
+/* T=1 tree verification against the normalised DARTree proposal.             */
+/* [DARTree] "Causal correction" (with the full-vocabulary normaliser the       */
+/* corrected distribution q~(. | u) is a probability, which is what lets the   */
+/* speculative-sampling test of "Speculative sampling" use it): at node n, the */
+/* drafter proposes n's children from                                          */
+/*   log q~(v | u) = ((d_pos[v] - lse_pos) + <U[u], Vt[v]>) - z,               */
+/* u = tok(n) (the root: root_tok), pos = depth(n) (the children's position),  */
+/* z = znorm[pos][rank(n)] (the root: znorm[0][0]), each step rounded to fp32, */
+/* the dot product the serial fmaf chain of or_markov.  Without a parent token */
+/* (the root and root_tok < 0) q~ is the plain marginal.  Otherwise the rule   */
+/* of or_verify_t1: children in rank order, u[0][c] < exp_canon(lpt - log q~), */
+/* first acceptance descends, the replacement from max(0, P - Q~), Q~ the 2^32 */
+/* fixed-point masses of q~, or from P when that is empty or n has no          */
+/* children.                                                                   */
+/* Pinned: U = 0 and z = 0 give or_verify_t1; the proposal sums to 1 with the  */
+/* exact normaliser; a chain whose child is drawn from q~ emits p (tests).     */
+/* ------------------------------------------------------------------------- */
+int or_verify_t1_markov(const int32_t* tok, const int32_t* parent, const int32_t* depth,
+                        const int32_t* rank, int M, int L, int Mmax,
+                        const float* target, const float* draft, const float* draft_lse,
+                        int V, const float* U, const float* Vt, int R, int root_tok,
+                        const float* znorm /* [L][K] */, int K,
+                        const float* u, const float* lse_in,
+                        int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok)
+{
+    if (!or_tree_valid(parent, depth, M, L)) return OR_EBADTREE;
+    if (!U || !Vt || R < 1 || !znorm || K < 1) return OR_EINVAL;
+    uint64_t* w = (uint64_t*)malloc((size_t)V * sizeof(uint64_t));
+    int* kids = (int*)malloc((size_t)M * sizeof(int));
+    if (!w || !kids) { free(w); free(kids); return OR_ENOMEM; }
+    for (int i = 0; i <= L; ++i) acc_nodes[i] = -1;
+    int n = 0, len = 0, out = -1;
+    acc_nodes[0] = 0;
+    for (;;) {
+        const float* trow = target + (int64_t)n * V;
+        float lse_t = lse_in ? lse_in[n] : or_row_lse(trow, V);
+        int ptok = n == 0 ? root_tok : tok[n];
+        int pos = depth[n];
+        float z = 0.0f;
+        if (ptok >= 0 && pos < L) z = znorm[pos * K + (n == 0 ? 0 : rank[n])];
+        int nk = 0;
+        for (int c = 1; c < M; ++c)
+            if (parent[c] == n) {
+                int j = nk++;
+                while (j > 0 && rank[kids[j - 1]] > rank[c]) { kids[j] = kids[j - 1]; --j; }
+                kids[j] = c;
+            }
+        const float* drow = pos < L ? draft + (int64_t)pos * V : NULL;
+        float lsed = pos < L ? draft_lse[pos] : 0.0f;
+        int acc = -1;
+        for (int i = 0; i < nk && acc < 0; ++i) {
+            int c = kids[i];
+            float lpt = trow[tok[c]] - lse_t;
+            float lpq = drow[tok[c]] - lsed;
+            if (ptok >= 0) { lpq = lpq + or_markov(U, Vt, R, ptok, tok[c]); lpq = lpq - z; }
+            if (u[c] < or_exp_canon(lpt - lpq)) acc = c;
+        }
+        if (acc >= 0 && len < L) {
+            acc_nodes[++len] = acc;
+            n = acc;
+            continue;
+        }
+        uint64_t S = 0;
+        if (nk > 0) {
+            for (int v = 0; v < V; ++v) {
+                float lpq = drow[v] - lsed;
+                if (ptok >= 0) { lpq = lpq + or_markov(U, Vt, R, ptok, v); lpq = lpq - z; }
+                uint64_t P = or_fixed32(or_exp_canon(trow[v] - lse_t));
+                uint64_t Q = or_fixed32(or_exp_canon(lpq));
+                w[v] = P > Q ? P - Q : 0;
+                S += w[v];
+            }
+        }
+        if (S == 0) {
+            for (int v = 0; v < V; ++v) {
+                w[v] = or_fixed32(or_exp_canon(trow[v] - lse_t));
+                S += w[v];
+            }
+        }
+        out = or_draw(w, V, S, u[Mmax + n]);
+        break;
+    }
+    *acc_len = len;
+    *next_tok = out;
+    free(w); free(kids);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Tree verification at T=1 with one residual per rejected sibling.            */
 /* [Unit11] residual formula: after drafting y ~ q is rejected, the output is   */
 /* drawn from r = [p - q]_+ / sum [p - q]_+; [DARTree] "Speculative sampling"  */

@@ -215,3 +215,62 @@ def test_target_match_emits_target_samples_along_the_path():
         freq = cnt / tot
         sigma = np.sqrt(pr * (1 - pr) / tot)
         assert np.all(np.abs(freq - pr) <= 3.5 * sigma), (freq, pr)
+
+
+# ---------------------------------------------------------------------------
+# T=1 against the normalised DARTree proposal q~(. | parent token)
+# ---------------------------------------------------------------------------
+def test_markov_walk_without_term_is_the_plain_walk():
+    rng = np.random.default_rng(21)
+    V, L, K = 30, 4, 3
+    for trial in range(25):
+        x = (rng.standard_normal((L, V)) * 1.5).astype(np.float32)
+        l32, _, ids, lps = oracle.candidates(x, K)
+        t = oracle.ddtree(lps, ids, 12).trimmed()
+        tgt = (rng.standard_normal((t.n, V)) * 1.5).astype(np.float32)
+        u = rng.random((2, t.n)).astype(np.float32)
+        zero_U = np.zeros((V, 2), np.float32)
+        a = oracle.verify_t1(t, tgt, x, l32, u, L, t.n)
+        b = oracle.verify_t1_markov(t, tgt, x, l32, zero_U, zero_U, 5, np.zeros((L, K), np.float32), u, L, t.n)
+        assert a[0].tolist() == b[0].tolist() and a[1:3] == b[1:3], trial
+
+
+def _qtilde(x_row, U, Vt, u, z):
+    lp = x_row.astype(np.float64) - np.logaddexp.reduce(x_row.astype(np.float64))
+    return np.exp(lp + Vt.astype(np.float64) @ U[u].astype(np.float64) - z)
+
+
+@pytest.mark.parametrize("proposal,lossless", [("markov", True), ("plain", False)])
+def test_markov_walk_preserves_p_when_the_child_is_drawn_from_q_tilde(proposal, lossless):
+    # one child under the root, its token drawn from q~(. | root token); the
+    # walk with the corrected proposal emits p; the plain marginal does not
+    V, R, root = 6, 2, 4
+    rng = np.random.default_rng(5)
+    x = np.array([[1.0, 0.5, 0.0, -0.5, 0.2, 0.8]], np.float32)
+    U = (rng.standard_normal((V, R)) * 1.5).astype(np.float32)
+    Vt = (rng.standard_normal((V, R)) * 1.5).astype(np.float32)
+    ids = np.arange(V, dtype=np.int32)[None, :1]
+    z = oracle.markov_norm(x, ids, U, Vt, root)
+    qt = _qtilde(x[0], U, Vt, root, float(z[0, 0]))
+    assert abs(qt.sum() - 1) < 1e-5  # the exact normaliser makes q~ a probability
+    p = np.array([0.05, 0.3, 0.1, 0.25, 0.2, 0.1])
+    rows = np.stack([np.log(p).astype(np.float32)] * 2)
+    l32 = np.array([np.logaddexp.reduce(x[0].astype(np.float64))], np.float32)
+    n = 30_000
+    counts = np.zeros(V, np.int64)
+    cq = np.cumsum(qt)
+    Uw = U if proposal == "markov" else np.zeros_like(U)
+    zw = z if proposal == "markov" else np.zeros_like(z)
+    for _ in range(n):
+        tok = int(min(np.searchsorted(cq, rng.random(), side="right"), V - 1))
+        t = oracle.Tree(np.array([-1, tok], np.int32), np.array([-1, 0], np.int32), np.array([0, 1], np.int32),
+                        np.array([-1, 0], np.int32), np.zeros(2, np.float32), 2)
+        u = rng.random((2, 2)).astype(np.float32)
+        acc, alen, nxt = oracle.verify_t1_markov(t, rows, x, l32, Uw, Vt, root, zw, u, 1, 2,
+                                                 lse_in=np.zeros(2, np.float32))
+        counts[tok if alen == 1 else nxt] += 1
+    dev = np.abs(counts / n - p) / np.sqrt(p * (1 - p) / n)
+    if lossless:
+        assert np.all(dev <= 3.5), (counts / n, p)
+    else:
+        assert np.max(dev) > 10, (counts / n, p)
