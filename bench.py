@@ -81,6 +81,7 @@ def workloads():
         "dartree_beta0": wk.dartree_supertree(0.0),
         "dartree_beta-0.5": wk.dartree_supertree(-0.5),
         "dartree_norm_beta0": wk.dartree_normalised(0.0),
+        "dartree_norm_t1": wk.dartree_normalised_t1(0.0),
         "dartree_fixed": wk.dartree_fixed(),
         "ddtree_saba_b16": wk.ddtree_saba(16),
         "heap_markov": wk.heap_markov(False),
@@ -255,6 +256,8 @@ def run_ours(args, wl, rank, world, local):
         out = dtree.alloc_verify_out(tree, device=dev)
         copies.append(dict(x=x, tree=tree, ws=ws, tgt=tgt, uni=uni, mask=mask, pos=pos, out=out))
 
+    markov_t1 = wl.mode == "dartree" and wl.markov_norm and temperature == 1.0
+
     def step(c, stages=("buildmask", "verify")):
         if saba is not None and ("buildmask" in stages or "saba" in stages):
             # SABA from this copy's previous round: its stage-1 tables and accepted lengths
@@ -274,7 +277,10 @@ def run_ours(args, wl, rank, world, local):
             dtree.select_mask(p, c["tree"], c["mask"], c["pos"], workspace=c["ws"])
         if "mask" in stages:
             dtree.tree_mask(c["tree"], c["mask"], c["pos"])
-        if "verify" in stages:
+        if "verify" in stages and markov_t1:  # T=1 against the normalised proposal q~
+            dtree.verify_markov(p, c["tree"], c["tgt"], c["x"], dtree.znorm_view(p, c["ws"]), c["uni"],
+                                out=c["out"])
+        elif "verify" in stages:
             dtree.verify(c["tree"], c["tgt"], temperature=temperature,
                          draft=c["x"] if temperature and wl.verify_rule != "target_match" else None,
                          uniforms=c["uni"], out=c["out"], rule=wl.verify_rule or None)
@@ -483,7 +489,9 @@ def oracle_round(wl, x, tgt, uni, M):
     oracle.tree_mask(t, Mmax, wl.L)
     if tgt is None:
         return t
-    if wl.temperature == 1.0:
+    if wl.temperature == 1.0 and wl.mode == "dartree" and wl.markov_norm:
+        oracle.verify_t1_markov(t, tgt, x, l32, U, Vt, -1, z, uni, wl.L, Mmax)
+    elif wl.temperature == 1.0:
         oracle.verify_t1(t, tgt, x, l32, uni, wl.L, Mmax, rule=wl.verify_rule or "ratio")
     else:
         oracle.verify_greedy(t, tgt, wl.L)

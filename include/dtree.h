@@ -338,6 +338,25 @@ dt_status dt_verify(const dt_tree* tree, int32_t batch, int32_t V, int32_t dtype
  *   may be NULL).
  * Other arguments and outputs as for dt_verify; target_lse and uniforms apply
  * to every T=1 rule.  Returns DT_ERR_INVALID_ARG for an unknown rule. */
+/* T=1 walk of a tree built with the normalised DARTree correction
+ * ([DARTree] "Causal correction": with the full-vocabulary normaliser the
+ * corrected distribution is a probability, so speculative sampling ([DARTree]
+ * "Speculative sampling") can test against it).  DT_VERIFY_RATIO's rule with
+ * the drafter's proposal of node n's children replaced by
+ *   log q~(v | u) = ((d_pos[v] - lse_pos) + <U[u], Vt[v]>) - z,
+ * u = tok(n) (the root: p->root_tok[b]), pos = depth(n), z =
+ * znorm[b][pos][rank(n)] (the root: znorm[b][0][0]), each step in fp32, the dot
+ * product a serial fma chain over R; without a parent token q~ is the plain
+ * marginal.  Both the acceptance ratios and the residual max(0, P - Q~) use it.
+ * p supplies U, Vt (fp32 [V][R], Vt 16-byte aligned, 4 <= R <= 64, R % 4 == 0),
+ * R, root_tok, batch, V, K and dtype; znorm: [batch][L][K] fp32, e.g. the
+ * table dt_markov_norm wrote at DT_ZNORM_OFFSET(p).  Other arguments as for
+ * dt_verify at temperature 1. */
+dt_status dt_verify_markov(const dt_build_params* p, const dt_tree* tree, const void* target_logits,
+                           const float* target_lse, const void* draft_logits, const float* znorm,
+                           const float* uniforms, int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                           float* visited_lse, dt_stream_t stream);
+
 #define DT_VERIFY_GREEDY 0
 #define DT_VERIFY_RATIO 1
 #define DT_VERIFY_ITER_RESIDUAL 2

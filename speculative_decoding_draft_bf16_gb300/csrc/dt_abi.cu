@@ -26,7 +26,7 @@ int chunk_of(int V, int S, int dtype) {
 }
 
 // Clusters of S CTAs that the device holds at once for stage 1 (kind 1,
-// extra = Kc) or the verification walk (kind 6, extra = 4 * max_nodes + rule)
+// extra = Kc) or the verification walk (kind 6, extra = 8 * max_nodes + rule)
 // with these sizes; cached per device.
 int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
     struct Fit {
@@ -47,7 +47,7 @@ int max_clusters(int kind, int dtype, int S, int chunk, int extra) {
             return f.n;
     }
     const int n = kind == 1 ? dt_kn1_max_clusters(dtype, S, chunk, extra)
-                            : dt_kn6_max_clusters(dtype, S, chunk, extra >> 2, extra & 3);
+                            : dt_kn6_max_clusters(dtype, S, chunk, extra >> 3, extra & 7);
     if (n > 0 && nfit < 128) fits[nfit++] = Fit{dev, kind, dtype, S, chunk, extra, n};
     return n;
 }
@@ -417,18 +417,22 @@ dt_status dt_verify(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, c
                           next_tok, visited_lse, stream);
 }
 
-dt_status dt_verify_rule(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, const void* target_logits,
-                         const float* target_lse, const void* draft_logits, int32_t rule, const float* uniforms,
-                         int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
-                         dt_stream_t stream) {
+}  // extern "C"
+
+// The walk for every rule; prop (rule DT_KN6_RATIO_MARKOV only) describes the
+// normalised DARTree proposal.
+static dt_status verify_impl(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, const void* target_logits,
+                             const float* target_lse, const void* draft_logits, int32_t rule, const float* uniforms,
+                             int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
+                             const DtKn6Proposal* prop, cudaStream_t stream) {
     if (!t || batch < 1 || V < 1 || !target_logits || !acc_nodes || !acc_len || !next_tok) return DT_ERR_INVALID_ARG;
     if (V > DT_MAX_V) return DT_ERR_UNSUPPORTED;
     if (dtype != DT_BF16 && dtype != DT_F32) return DT_ERR_INVALID_ARG;
     if (t->max_nodes < 1 || t->max_nodes > DT_MAX_NODES || t->L < 1 || t->L > DT_MAX_L) return DT_ERR_INVALID_ARG;
     if (!t->node_tok || !t->parent || !t->depth || !t->rank || !t->n_nodes || !t->status) return DT_ERR_INVALID_ARG;
-    if (rule < DT_VERIFY_GREEDY || rule > DT_VERIFY_TARGET_MATCH) return DT_ERR_INVALID_ARG;
+    if (rule < DT_VERIFY_GREEDY || rule > DT_KN6_RATIO_MARKOV) return DT_ERR_INVALID_ARG;
     const bool t1 = rule != DT_VERIFY_GREEDY;
-    const bool uses_q = rule == DT_VERIFY_RATIO || rule == DT_VERIFY_ITER_RESIDUAL;
+    const bool uses_q = rule == DT_VERIFY_RATIO || rule == DT_VERIFY_ITER_RESIDUAL || rule == DT_KN6_RATIO_MARKOV;
     if (t1 && !uniforms) return DT_ERR_INVALID_ARG;
     if (uses_q && (!draft_logits || !t->lse)) return DT_ERR_INVALID_ARG;
     // the walk is sequential per request: spread each row over a cluster as
@@ -443,15 +447,38 @@ dt_status dt_verify_rule(const dt_tree* t, int32_t batch, int32_t V, int32_t dty
             return dt_kn6_smem_bytes(chunk, esize, Mmax, rule) + 1024 <= kSmemMax &&
                    (rule != DT_VERIFY_ITER_RESIDUAL || dt_kn6_pq_cache(chunk, esize, Mmax, rule));
         },
-        [&](int q, int chunk) { return max_clusters(6, dtype, q, chunk, Mmax * 4 + rule); });
+        [&](int q, int chunk) { return max_clusters(6, dtype, q, chunk, Mmax * 8 + rule); });
     const int chunk = chunk_of(V, s, dtype);
     if (chunk > kChunkMax || dt_kn6_smem_bytes(chunk, esize, Mmax, rule) + 1024 > kSmemMax) return DT_ERR_UNSUPPORTED;
     cudaError_t e = dt_kn6_launch(batch, t->L, V, dtype, t->max_nodes, s, chunk, rule, t->node_tok, t->parent,
                                   t->depth, t->rank, t->n_nodes, t->lse, target_logits, t1 ? target_lse : nullptr,
-                                  uses_q ? draft_logits : nullptr,
-                                  uniforms, acc_nodes,
-                                  acc_len, next_tok, visited_lse, t->status, (cudaStream_t)stream);
+                                  uses_q ? draft_logits : nullptr, uniforms, acc_nodes, acc_len, next_tok, visited_lse,
+                                  t->status, prop, stream);
     return cuda_status(e);
+}
+
+extern "C" {
+
+dt_status dt_verify_rule(const dt_tree* t, int32_t batch, int32_t V, int32_t dtype, const void* target_logits,
+                         const float* target_lse, const void* draft_logits, int32_t rule, const float* uniforms,
+                         int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
+                         dt_stream_t stream) {
+    if (rule < DT_VERIFY_GREEDY || rule > DT_VERIFY_TARGET_MATCH) return DT_ERR_INVALID_ARG;
+    return verify_impl(t, batch, V, dtype, target_logits, target_lse, draft_logits, rule, uniforms, acc_nodes,
+                       acc_len, next_tok, visited_lse, nullptr, (cudaStream_t)stream);
+}
+
+dt_status dt_verify_markov(const dt_build_params* p, const dt_tree* t, const void* target_logits,
+                           const float* target_lse, const void* draft_logits, const float* znorm,
+                           const float* uniforms, int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                           float* visited_lse, dt_stream_t stream) {
+    if (!p || !t || !znorm) return DT_ERR_INVALID_ARG;
+    if (p->R < 4 || p->R > 64 || (p->R & 3) || !p->U || !p->Vt) return DT_ERR_INVALID_ARG;
+    if (((uintptr_t)p->Vt) & 15u) return DT_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->K < 1 || t->Kc != p->K || t->L != p->L) return DT_ERR_INVALID_ARG;
+    const DtKn6Proposal prop{p->U, p->Vt, p->R, znorm, p->K, p->root_tok};
+    return verify_impl(t, p->batch, p->V, p->dtype, target_logits, target_lse, draft_logits, DT_KN6_RATIO_MARKOV,
+                       uniforms, acc_nodes, acc_len, next_tok, visited_lse, &prop, (cudaStream_t)stream);
 }
 
 dt_status dt_saba_budget(const dt_saba_params* q, const dt_tree* t, int32_t batch, const float* hidden, int32_t Hd,

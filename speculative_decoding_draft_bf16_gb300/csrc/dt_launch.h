@@ -135,7 +135,17 @@ size_t dt_kn5_smem_bytes(int Mmax);
 cudaError_t dt_kn5_launch(int batch, int L, int Mmax, int pos_offset, const int32_t* parent, const int32_t* depth,
                           const int32_t* n_nodes, uint32_t* mask, int32_t* pos, int32_t* status, cudaStream_t st);
 
-// Verification walk (kn6_verify.cu); rule: DT_VERIFY_*.
+// Verification walk (kn6_verify.cu); rule: DT_VERIFY_*, or DT_KN6_RATIO_MARKOV:
+// the ratio rule against the normalised DARTree proposal described by `prop`.
+#define DT_KN6_RATIO_MARKOV 4
+struct DtKn6Proposal {
+    const float* U;           // [V][R] fp32
+    const float* Vt;          // [V][R] fp32, 16-byte aligned
+    int R;                    // 4..64, a multiple of 4
+    const float* z;           // [batch][L][K] log-normalisers
+    int K;
+    const int32_t* root_tok;  // [batch] or NULL
+};
 int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax, int rule);
 size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax, int rule);
 int dt_kn6_pq_cache(int chunk, int esize, int Mmax, int rule);  // 1: the residual passes cache (P, Q)
@@ -144,4 +154,4 @@ cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, i
                           const int32_t* n_nodes, const float* draft_lse, const void* target,
                           const float* target_lse, const void* draft,
                           const float* uniforms, int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
-                          float* visited_lse, int32_t* status, cudaStream_t st);
+                          float* visited_lse, int32_t* status, const DtKn6Proposal* prop, cudaStream_t st);

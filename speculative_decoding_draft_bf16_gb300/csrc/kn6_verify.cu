@@ -174,10 +174,21 @@ struct Rows {
     }
 };
 
+// The normalised DARTree proposal q~(v | u) = exp(((d[v] - lse) + <U[u], Vt[v]>) - z)
+// of a node's children (u: the node's token, z: its log-normaliser row).
+struct Kn6Corr {
+    const float* U;         // [V][R] fp32
+    const float* Vt;        // [V][R] fp32, 16-byte aligned, R % 4 == 0
+    int R;                  // <= 64
+    const float* z;         // [batch][L][K] log-normalisers
+    int K;
+    const int32_t* root_tok;  // [batch] or NULL
+};
+
 // One instantiation per acceptance rule (RULE = DT_VERIFY_*), so that each
-// walk carries only its own code.
-template <typename T, int RULE>
-__global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int chunk, int nbt, int pq_on,
+// walk carries only its own code; CORR: the ratio rule against q~.
+template <typename T, int RULE, bool CORR>
+__global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, int Mmax, int chunk, int nbt, int pq_on,
                                                  const int32_t* __restrict__ g_tok,
                                                  const int32_t* __restrict__ g_par,
                                                  const int32_t* __restrict__ g_dep,
@@ -191,6 +202,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
                                                  int32_t* __restrict__ status) {
     using E = DtElem<T>;
     constexpr int EPV = 16 / sizeof(T);
+    __shared__ __align__(16) float s_ur[CORR ? 64 : 4];  // U row of the proposing node's token
     const float NEG_INF = -__int_as_float(0x7F800000);
     extern __shared__ __align__(128) unsigned char smem[];
     cg::cluster_group cluster = cg::this_cluster();
@@ -442,6 +454,43 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
             ++k;
             lse_t = M_ + logf(ssum);
         }
+        // the proposal of n's children: q~ needs n's token (the root: root_tok)
+        // and log-normaliser, and the U row staged for the dot products
+        int qu = -1;
+        float qz = 0.f;
+        if constexpr (CORR) {
+            qu = n == 0 ? (corr.root_tok ? corr.root_tok[b] : -1) : s_tok[n];
+            if (qu >= V || s_dep[n] >= L) qu = -1;
+            if (qu >= 0) {
+                qz = corr.z[((size_t)b * L + s_dep[n]) * corr.K + (n == 0 ? 0 : s_rank[n])];
+                if (tid < corr.R) s_ur[tid] = corr.U[(size_t)qu * corr.R + tid];
+            }
+            __syncthreads();
+        }
+        // <U[qu], Vt[v]>: serial fp32 fma from 0 over the R columns
+        auto markov_dot = [&](int v) {
+            float acc = 0.f;
+            const float4* vr = (const float4*)(corr.Vt + (size_t)v * corr.R);
+            for (int k4 = 0; k4 < (corr.R >> 2); ++k4) {
+                const float4 q = vr[k4];
+                acc = __fmaf_rn(s_ur[4 * k4 + 0], q.x, acc);
+                acc = __fmaf_rn(s_ur[4 * k4 + 1], q.y, acc);
+                acc = __fmaf_rn(s_ur[4 * k4 + 2], q.z, acc);
+                acc = __fmaf_rn(s_ur[4 * k4 + 3], q.w, acc);
+            }
+            return acc;
+        };
+        // log q of token v at n's children's position from its drafter value dv
+        auto proposal_lp = [&](float dv, float dlse, int v) {
+            float l = __fsub_rn(dv, dlse);
+            if constexpr (CORR) {
+                if (qu >= 0) {
+                    l = __fadd_rn(l, markov_dot(v));
+                    l = __fsub_rn(l, qz);
+                }
+            }
+            return l;
+        };
         // single-residual test of child i against p (fp32, exp_canon ratio)
         auto ratio_accepts = [&](int i) {
             const int tk = s_tok[i];
@@ -449,7 +498,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
             const float tv = E::val(trow_of(n)[tk]);
             const float dv = E::val(drow_of(pos)[tk]);
             const float lpt = __fsub_rn(tv, lse_t);
-            const float lpq = __fsub_rn(dv, draft_lse[(size_t)b * L + pos]);
+            const float lpq = proposal_lp(dv, draft_lse[(size_t)b * L + pos], tk);
             return u0[i] < dt_exp_canon(__fsub_rn(lpt, lpq));
         };
         unsigned long long prev_key = 0;  // one residual per sibling: the last child tested
@@ -514,7 +563,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
             const unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
             rP += P;
             if (resid) {
-                const unsigned long long Q = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(y[e]), lse_d)));
+                const unsigned long long Q = dt_fixed32(dt_exp_canon(proposal_lp(E::val(y[e]), lse_d, lo + e)));
                 const unsigned long long w = P > Q ? P - Q : 0ull;
                 rR += w;
                 if (cache) {
@@ -639,7 +688,11 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(int L, int V, int Mmax, int 
                     for (int g0 = a0; g0 < a1; g0 += 32) {
                         const int e = g0 + lane;
                         unsigned long long P = 0;
-                        if (e < a1) P = mass(E::val(x[e]), lse_t, use_r, use_r ? E::val(y[e]) : 0.f, lse_d, Tq);
+                        if (e < a1) {
+                            P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
+                            if (use_r)
+                                P = resid_w(P, dt_fixed32(dt_exp_canon(proposal_lp(E::val(y[e]), lse_d, lo + e))), Tq);
+                        }
                         const unsigned long long ci = warp_incl_scan_u64(P);
                         const unsigned found = __ballot_sync(0xffffffffu, P > 0 && base + ci > local);
                         if (found) {
@@ -729,41 +782,63 @@ int dt_kn6_pq_cache(int chunk, int esize, int Mmax, int rule) {
 }
 
 // Sets the kernel's shared-memory and cluster-size attributes for a launch.
-template <typename T, int RULE>
+template <typename T, int RULE, bool CORR>
 cudaError_t kn6_prepare(int S, size_t smem) {
-    cudaError_t e = cudaFuncSetAttribute(kn6_kernel<T, RULE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(kn6_kernel<T, RULE, CORR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess && S > 8)
-        e = cudaFuncSetAttribute(kn6_kernel<T, RULE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(kn6_kernel<T, RULE, CORR>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
 
-template <typename T, int RULE>
+template <typename T, int RULE, bool CORR>
 int kn6_max_clusters(int S, size_t smem) {
-    if (kn6_prepare<T, RULE>(S, smem) != cudaSuccess) return 0;
-    return dt_max_active_clusters(kn6_kernel<T, RULE>, S, NT, smem);
+    if (kn6_prepare<T, RULE, CORR>(S, smem) != cudaSuccess) return 0;
+    return dt_max_active_clusters(kn6_kernel<T, RULE, CORR>, S, NT, smem);
 }
 
 template <typename T>
 int kn6_max_clusters_rule(int rule, int S, size_t smem) {
     switch (rule) {
-        case DT_VERIFY_GREEDY: return kn6_max_clusters<T, DT_VERIFY_GREEDY>(S, smem);
-        case DT_VERIFY_RATIO: return kn6_max_clusters<T, DT_VERIFY_RATIO>(S, smem);
-        case DT_VERIFY_ITER_RESIDUAL: return kn6_max_clusters<T, DT_VERIFY_ITER_RESIDUAL>(S, smem);
-        default: return kn6_max_clusters<T, DT_VERIFY_TARGET_MATCH>(S, smem);
+        case DT_VERIFY_GREEDY: return kn6_max_clusters<T, DT_VERIFY_GREEDY, false>(S, smem);
+        case DT_VERIFY_RATIO: return kn6_max_clusters<T, DT_VERIFY_RATIO, false>(S, smem);
+        case DT_VERIFY_ITER_RESIDUAL: return kn6_max_clusters<T, DT_VERIFY_ITER_RESIDUAL, false>(S, smem);
+        case DT_VERIFY_TARGET_MATCH: return kn6_max_clusters<T, DT_VERIFY_TARGET_MATCH, false>(S, smem);
+        default: return kn6_max_clusters<T, DT_VERIFY_RATIO, true>(S, smem);  // DT_KN6_RATIO_MARKOV
     }
 }
 
-template <typename T, int RULE>
-cudaError_t kn6_launch_t(const DtLaunch& lc, size_t smem, int S, int L, int V, int Mmax, int chunk, int nbt,
-                         int pq_on, const int32_t* tok, const int32_t* parent, const int32_t* depth,
-                         const int32_t* rank, const int32_t* n_nodes, const float* draft_lse, const void* target,
-                         const float* target_lse, const void* draft, const float* uniforms, int32_t* acc_nodes,
-                         int32_t* acc_len, int32_t* next_tok, float* visited_lse, int32_t* status) {
-    cudaError_t e = kn6_prepare<T, RULE>(S, smem);
+template <typename T, int RULE, bool CORR>
+cudaError_t kn6_launch_t(const DtLaunch& lc, size_t smem, int S, const Kn6Corr& corr, int L, int V, int Mmax,
+                         int chunk, int nbt, int pq_on, const int32_t* tok, const int32_t* parent,
+                         const int32_t* depth, const int32_t* rank, const int32_t* n_nodes, const float* draft_lse,
+                         const void* target, const float* target_lse, const void* draft, const float* uniforms,
+                         int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
+                         int32_t* status) {
+    cudaError_t e = kn6_prepare<T, RULE, CORR>(S, smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<T, RULE>, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank,
-                              n_nodes, draft_lse, (const T*)target, target_lse, (const T*)draft, uniforms, acc_nodes,
-                              acc_len, next_tok, visited_lse, status);
+    return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<T, RULE, CORR>, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent,
+                              depth, rank, n_nodes, draft_lse, (const T*)target, target_lse, (const T*)draft,
+                              uniforms, acc_nodes, acc_len, next_tok, visited_lse, status);
+}
+
+template <typename T>
+cudaError_t kn6_launch_rule(int rule, const DtLaunch& lc, size_t smem, int S, const Kn6Corr& corr, int L, int V,
+                            int Mmax, int chunk, int nbt, int pq_on, const int32_t* tok, const int32_t* parent,
+                            const int32_t* depth, const int32_t* rank, const int32_t* n_nodes,
+                            const float* draft_lse, const void* target, const float* target_lse, const void* draft,
+                            const float* uniforms, int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
+                            float* visited_lse, int32_t* status) {
+#define DT_KN6_ARGS lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank, n_nodes, draft_lse, \
+                    target, target_lse, draft, uniforms, acc_nodes, acc_len, next_tok, visited_lse, status
+    switch (rule) {
+        case DT_VERIFY_GREEDY: return kn6_launch_t<T, DT_VERIFY_GREEDY, false>(DT_KN6_ARGS);
+        case DT_VERIFY_RATIO: return kn6_launch_t<T, DT_VERIFY_RATIO, false>(DT_KN6_ARGS);
+        case DT_VERIFY_ITER_RESIDUAL: return kn6_launch_t<T, DT_VERIFY_ITER_RESIDUAL, false>(DT_KN6_ARGS);
+        case DT_VERIFY_TARGET_MATCH: return kn6_launch_t<T, DT_VERIFY_TARGET_MATCH, false>(DT_KN6_ARGS);
+        default: return kn6_launch_t<T, DT_VERIFY_RATIO, true>(DT_KN6_ARGS);
+    }
+#undef DT_KN6_ARGS
 }
 
 int dt_kn6_max_clusters(int dtype, int S, int chunk, int Mmax, int rule) {
@@ -778,27 +853,23 @@ cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, i
                           const int32_t* n_nodes, const float* draft_lse, const void* target,
                           const float* target_lse, const void* draft, const float* uniforms, int32_t* acc_nodes,
                           int32_t* acc_len, int32_t* next_tok, float* visited_lse, int32_t* status,
-                          cudaStream_t st) {
+                          const DtKn6Proposal* prop, cudaStream_t st) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
     const Kn6Layout lay = kn6_layout(chunk, esize, Mmax, rule);
     const size_t smem = lay.total;
     const int nbt = lay.nbt, pq_on = lay.pq > 0;
     DtLaunch lc(dim3(S, batch, 1), dim3(NT, 1, 1), smem, st, S);
-#define DT_KN6_ARGS lc, smem, S, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank, n_nodes, draft_lse, target, \
-                    target_lse, draft, uniforms, acc_nodes, acc_len, next_tok, visited_lse, status
-    if (dtype == DT_BF16) {
-        switch (rule) {
-            case DT_VERIFY_GREEDY: return kn6_launch_t<uint16_t, DT_VERIFY_GREEDY>(DT_KN6_ARGS);
-            case DT_VERIFY_RATIO: return kn6_launch_t<uint16_t, DT_VERIFY_RATIO>(DT_KN6_ARGS);
-            case DT_VERIFY_ITER_RESIDUAL: return kn6_launch_t<uint16_t, DT_VERIFY_ITER_RESIDUAL>(DT_KN6_ARGS);
-            default: return kn6_launch_t<uint16_t, DT_VERIFY_TARGET_MATCH>(DT_KN6_ARGS);
-        }
+    Kn6Corr corr{nullptr, nullptr, 0, nullptr, 0, nullptr};
+    if (rule == DT_KN6_RATIO_MARKOV) {
+        if (!prop || !prop->U || !prop->Vt || prop->R < 4 || prop->R > 64 || (prop->R & 3) || !prop->z)
+            return cudaErrorInvalidValue;
+        corr = Kn6Corr{prop->U, prop->Vt, prop->R, prop->z, prop->K, prop->root_tok};
     }
-    switch (rule) {
-        case DT_VERIFY_GREEDY: return kn6_launch_t<float, DT_VERIFY_GREEDY>(DT_KN6_ARGS);
-        case DT_VERIFY_RATIO: return kn6_launch_t<float, DT_VERIFY_RATIO>(DT_KN6_ARGS);
-        case DT_VERIFY_ITER_RESIDUAL: return kn6_launch_t<float, DT_VERIFY_ITER_RESIDUAL>(DT_KN6_ARGS);
-        default: return kn6_launch_t<float, DT_VERIFY_TARGET_MATCH>(DT_KN6_ARGS);
-    }
-#undef DT_KN6_ARGS
+    if (dtype == DT_BF16)
+        return kn6_launch_rule<uint16_t>(rule, lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth,
+                                         rank, n_nodes, draft_lse, target, target_lse, draft, uniforms, acc_nodes,
+                                         acc_len, next_tok, visited_lse, status);
+    return kn6_launch_rule<float>(rule, lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank,
+                                  n_nodes, draft_lse, target, target_lse, draft, uniforms, acc_nodes, acc_len,
+                                  next_tok, visited_lse, status);
 }

@@ -84,6 +84,8 @@ def lib():
         L.dt_verify.restype = _i32
         L.dt_saba_budget.restype = _i32
         L.dt_saba_budget.argtypes = [ctypes.POINTER(SabaStruct), tp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.dt_verify_markov.restype = _i32
+        L.dt_verify_markov.argtypes = [bp, tp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.dt_verify_rule.restype = _i32
         L.dt_verify_rule.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
         L.dt_verify.argtypes = [tp, _i32, _i32, _i32, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
@@ -356,6 +358,24 @@ def verify(tree, target, temperature=0.0, draft=None, uniforms=None, out=None, v
     _check(lib().dt_verify(ctypes.byref(tree.struct()), batch, V, _dtype_code(target), _ptr(target),
                            _ptr(target_lse), _ptr(draft), float(temperature), _ptr(uniforms), _ptr(acc_nodes),
                            _ptr(acc_len), _ptr(next_tok), _ptr(visited_lse), _stream(stream)), "dt_verify")
+    return out
+
+
+def verify_markov(p, tree, target, draft, znorm, uniforms, out=None, visited_lse=None, target_lse=None,
+                  stream=None):
+    """T=1 walk against the normalised DARTree proposal (dt_verify_markov); znorm [b, L, K] fp32,
+    e.g. znorm_view(p, workspace) after markov_norm."""
+    _need(target, name="target")
+    _need(draft, name="draft")
+    _need(znorm, torch.float32, "znorm")
+    _need(uniforms, torch.float32, "uniforms")
+    if out is None:
+        out = alloc_verify_out(tree)
+    acc_nodes, acc_len, next_tok = out
+    _check(lib().dt_verify_markov(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _ptr(target),
+                                  _ptr(target_lse), _ptr(draft), _ptr(znorm), _ptr(uniforms), _ptr(acc_nodes),
+                                  _ptr(acc_len), _ptr(next_tok), _ptr(visited_lse), _stream(stream)),
+           "dt_verify_markov")
     return out
 
 

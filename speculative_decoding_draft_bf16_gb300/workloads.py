@@ -109,6 +109,12 @@ def dartree_normalised(beta):
                                name="dartree_norm_b8_L16_V151936_W32_K16_B512_beta%g" % beta)
 
 
+def dartree_normalised_t1(beta=0.0):
+    """The normalised DARTree workload verified at T=1 against its own proposal q~."""
+    return dataclasses.replace(dartree_normalised(beta), temperature=1.0,
+                               name="dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta%g" % beta)
+
+
 def dartree_fixed():
     """DARTree (fixed) at the pages' default: b=8, L=16, K=64, B=64 spread as 4 nodes per depth, R=64."""
     return Workload("dartree_fixed_b8_L16_V151936_K64_B64", "dartree", 8, 16, V_QWEN3, "bf16", 3.0, 0.7, 0.0,

@@ -239,3 +239,21 @@ def test_budget_policies_reject_invalid_arguments():
     ok = dtree.SabaStruct(4, 1.0, 1.0, 1, 8)
     assert L.dt_saba_budget(ctypes.byref(ok), ctypes.byref(tr), 2, None, 0, None, None, fake, fake, fake, None) == -1
     assert L.dt_saba_budget(ctypes.byref(ok), ctypes.byref(tr), 2, fake, 0, None, fake, fake, fake, fake, None) == -1
+
+
+def test_verify_markov_rejects_invalid_arguments():
+    L = dtree.lib()
+    fake = ctypes.c_void_p(0x3000)
+    t = _FakeTree(1, 4, 4, 9).struct()
+
+    def params(R=64, vt=0x10000, K=4):
+        q = dtree.Params(mode="dartree", batch=1, L=4, V=32, dtype="bf16", K=K, W=4, B=8).struct()
+        q.R, q.U, q.Vt = R, ctypes.c_void_p(0x20000), ctypes.c_void_p(vt)
+        return q
+    call = lambda q, z=fake: L.dt_verify_markov(ctypes.byref(q), ctypes.byref(t), fake, None, fake, z, fake, fake,
+                                                fake, fake, None, None)
+    assert call(params(), z=None) == -1        # no normalisers
+    assert call(params(R=66)) == -1            # more than 64 columns
+    assert call(params(R=62)) == -1            # not a multiple of 4
+    assert call(params(vt=0x10004)) == -1      # Vt not 16-byte aligned
+    assert call(params(K=5)) == -1             # tree lists of another length
