@@ -162,6 +162,8 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
             if (sh_any) {
                 if (tot <= 32) {
                     dt_warp_sort_u64(S.cand, tot, false);
+                } else if (tot <= NT) {
+                    dt_block_sort_u64<NT>(S.cand, tot, false, S.cand + NT);
                 } else {
                     const int P2 = dt_pow2_ceil(tot);
                     for (int i = tot + tid; i < P2; i += NT) S.cand[i] = ~0ull;
@@ -229,6 +231,8 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                 __syncthreads();
                 if (m <= 32) {
                     dt_warp_sort_u64(S.cand, m, true);
+                } else if (m <= NT) {
+                    dt_block_sort_u64<NT>(S.cand, m, true, S.cand + NT);
                 } else {
                     const int P2 = dt_pow2_ceil(m);
                     for (int i = m + tid; i < P2; i += NT) S.cand[i] = 0ull;
