@@ -224,25 +224,26 @@ DT_DI unsigned long long dt_warp_merge_reg(unsigned long long x, bool desc) {
     }
     return x;
 }
-// Sort n <= NT distinct 64-bit keys in shared memory (descending when desc)
-// with two block barriers: every warp sorts one 32-key segment in registers;
-// a key's place is then its place in its segment plus, for each other
-// segment, how many keys there come before it (a binary search over 32).
-// scratch: 32 * ceil(n / 32) keys, not overlapping a[0, n).  Pads (0 when
-// desc, all ones otherwise) must not be valid keys.  Ends with __syncthreads.
+// Sort n <= 512 distinct 64-bit keys in shared memory (descending when desc)
+// with two block barriers: warps sort 32-key segments in registers; a key's
+// place is then its place in its segment plus, for each other segment, how
+// many keys there come before it (a binary search over 32).  scratch:
+// 32 * ceil(n / 32) keys, not overlapping a[0, n).  Pads (0 when desc, all
+// ones otherwise) must not be valid keys.  Ends with __syncthreads.
 template <int NT>
 DT_DI void dt_block_sort_u64(unsigned long long* a, int n, bool desc, unsigned long long* scratch) {
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nseg = (n + 31) >> 5;
-    if (tid < nseg * 32) {  // whole warps
-        const unsigned long long x = tid < n ? a[tid] : (desc ? 0ull : ~0ull);
-        scratch[tid] = dt_warp_sort_reg(x, desc);
+    for (int sg = wid; sg < nseg; sg += NT / 32) {
+        const int i = sg * 32 + lane;
+        const unsigned long long x = i < n ? a[i] : (desc ? 0ull : ~0ull);
+        scratch[i] = dt_warp_sort_reg(x, desc);
     }
     __syncthreads();
-    if (tid < n) {  // the pads sort to the end of the last segment: [0, n) holds the keys
-        const unsigned long long x = scratch[tid];
-        const int own = tid >> 5;
-        int rank = lane;
+    for (int i = tid; i < n; i += NT) {  // the pads sort to the end of the last segment
+        const unsigned long long x = scratch[i];
+        const int own = i >> 5;
+        int rank = i & 31;
         for (int t = 0; t < nseg; ++t) {
             if (t == own) continue;
             const unsigned long long* seg = scratch + 32 * t;
