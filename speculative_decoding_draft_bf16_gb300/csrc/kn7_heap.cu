@@ -54,12 +54,11 @@ struct Kn7Smem {
     float* ts;        // [cap_rows][K] their edge scores
     unsigned long long* keys;  // [NW7][K] sort scratch, one slice per warp
     float* fs;        // [B+1] frontier: path score
-    int* fp;          // [B+1]           parent node
-    int* fj;          // [B+1]           order position under the parent
+    int4* fe;         // [B+1] frontier: parent node, (depth << 16) | order position, parent's order
+                      //       row, parent's score (bits)
     int* npar;        // [Mmax] emitted nodes
     int* nord;
     int* ndep;
-    int* nrow;        // order row of the node's children (-1: depth L)
     int* nrank;
     int* ntok;
     float* nsc;
@@ -83,9 +82,9 @@ __host__ __device__ inline size_t kn7_layout(int L, int K, int B, int Mmax, Kn7S
     const size_t o_lp = take((size_t)L * K * 4), o_id = take((size_t)L * K * 4), o_rm = take((size_t)L * K * 4);
     const size_t o_ord = take((size_t)cap * K * 2), o_ts = take((size_t)cap * K * 4);
     const size_t o_keys = take((size_t)NW7 * K * 8);
-    const size_t o_fs = take((size_t)(B + 1) * 4), o_fp = take((size_t)(B + 1) * 4), o_fj = take((size_t)(B + 1) * 4);
+    const size_t o_fs = take((size_t)(B + 1) * 4), o_fe = take((size_t)(B + 1) * 16);
     const size_t o_np = take((size_t)Mmax * 4), o_no = take((size_t)Mmax * 4), o_nd = take((size_t)Mmax * 4);
-    const size_t o_nr = take((size_t)Mmax * 4), o_nk = take((size_t)Mmax * 4), o_nt = take((size_t)Mmax * 4);
+    const size_t o_nk = take((size_t)Mmax * 4), o_nt = take((size_t)Mmax * 4);
     const size_t o_ns = take((size_t)Mmax * 4), o_misc = take(16);
     if (S) {
         S->lp = (float*)(base + o_lp);
@@ -95,12 +94,10 @@ __host__ __device__ inline size_t kn7_layout(int L, int K, int B, int Mmax, Kn7S
         S->ts = (float*)(base + o_ts);
         S->keys = (unsigned long long*)(base + o_keys);
         S->fs = (float*)(base + o_fs);
-        S->fp = (int*)(base + o_fp);
-        S->fj = (int*)(base + o_fj);
+        S->fe = (int4*)(base + o_fe);
         S->npar = (int*)(base + o_np);
         S->nord = (int*)(base + o_no);
         S->ndep = (int*)(base + o_nd);
-        S->nrow = (int*)(base + o_nr);
         S->nrank = (int*)(base + o_nk);
         S->ntok = (int*)(base + o_nt);
         S->nsc = (float*)(base + o_ns);
@@ -154,7 +151,7 @@ DT_DI bool desc_less(const Kn7Smem& S, int pa, int ja, int pb, int jb) {
 // Frontier entry a before entry b?
 DT_DI bool entry_before(const Kn7Smem& S, int a, float sa, int b, float sb) {
     if (sa != sb) return sa > sb;
-    return desc_less(S, S.fp[a], S.fj[a], S.fp[b], S.fj[b]);
+    return desc_less(S, S.fe[a].x, S.fe[a].y & 0xFFFF, S.fe[b].x, S.fe[b].y & 0xFFFF);
 }
 
 __global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, const int32_t* __restrict__ budget,
@@ -198,11 +195,10 @@ __global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, co
         int nrows = pre;
         // the root and its first child
         if (lane == 0) {
-            S.npar[0] = -1; S.nord[0] = 0; S.ndep[0] = 0; S.nrow[0] = 0; S.nrank[0] = -1; S.ntok[0] = -1;
+            S.npar[0] = -1; S.nord[0] = 0; S.ndep[0] = 0; S.nrank[0] = -1; S.ntok[0] = -1;
             S.nsc[0] = 0.f;
             S.fs[0] = __fadd_rn(0.f, S.ts[0]);
-            S.fp[0] = 0;
-            S.fj[0] = 0;
+            S.fe[0] = make_int4(0, 1 << 16, 0, __float_as_int(0.f));  // first child of the root, order row 0
         }
         __syncwarp();
         // Block maxima: the frontier is cut into blocks of 32 slots; lane l keeps
@@ -223,6 +219,7 @@ __global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, co
         int nf = 1, n = 0;
         refresh(0, nf);
         const int Bq = budget ? min(B, max(1, budget[b])) : B;  // this request's budget
+        const bool all_rows = pre == total;  // row of (position d + 1, parent rank c): 1 + (d - 1) * K + c
         while (n < Bq && nf > 0) {
             if (n + 1 >= Mmax) break;  // the host checks max_nodes > B; never taken
             const uint32_t g = __reduce_max_sync(0xffffffffu, bk0 > bk1 ? bk0 : bk1);
@@ -247,48 +244,53 @@ __global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, co
                     if (ob >= 0 && (best < 0 || entry_before(S, ob, os, best, bs))) { best = ob; bs = os; }
                 }
             }
-            const int x = best, p = S.fp[x], j = S.fj[x];
+            const int x = best;
             const float bs = S.fs[x];
-            const int d = S.ndep[p] + 1, rowp = S.nrow[p];
-            const int c = S.ord[(size_t)rowp * K + j];
+            const int4 ent = S.fe[x];
+            const int p = ent.x, j = ent.y & 0xFFFF, d = ent.y >> 16, rowp = ent.z;
+            const int c = S.ord[rowp * K + j];
             const int m = ++n;
+            int r = -1;  // order row of m's children
+            if (d < L) {
+                if (all_rows) {
+                    r = 1 + (d - 1) * K + c;
+                } else {
+                    r = S.rowmap[d * K + c];
+                    if (r < 0) {
+                        r = nrows++;
+                        make_row(S, r, d + 1, c, K, tab, true, z, S.keys);
+                        if (lane == 0) S.rowmap[d * K + c] = r;
+                    }
+                }
+            }
+            const bool sib = j + 1 < K, kid = r >= 0;
             __syncwarp();
+            // the popped slot takes the sibling, else the first child; the other is appended
             const int last = nf - 1;
+            const int kid_slot = sib ? nf : x;
             if (lane == 0) {
                 S.npar[m] = p; S.nord[m] = j; S.ndep[m] = d; S.nrank[m] = c; S.ntok[m] = S.id[(d - 1) * K + c];
                 S.nsc[m] = bs;
-                if (x != last) { S.fs[x] = S.fs[last]; S.fp[x] = S.fp[last]; S.fj[x] = S.fj[last]; }
-                if (j + 1 < K) {  // next sibling under p
-                    S.fs[last] = __fadd_rn(S.nsc[p], S.ts[(size_t)rowp * K + j + 1]);
-                    S.fp[last] = p;
-                    S.fj[last] = j + 1;
+                if (sib) {
+                    S.fs[x] = __fadd_rn(__int_as_float(ent.w), S.ts[rowp * K + j + 1]);
+                    S.fe[x] = make_int4(p, ent.y + 1, rowp, ent.w);
+                }
+                if (kid) {
+                    S.fs[kid_slot] = __fadd_rn(bs, S.ts[r * K]);
+                    S.fe[kid_slot] = make_int4(m, (d + 1) << 16, r, __float_as_int(bs));
+                }
+                if (!sib && !kid && x != last) {  // nothing to push: the last entry fills the slot
+                    S.fs[x] = S.fs[last];
+                    S.fe[x] = S.fe[last];
                 }
             }
-            nf = last + (j + 1 < K ? 1 : 0);
-            int r = -1;
-            if (d < L) {
-                r = S.rowmap[d * K + c];
-                if (r < 0) {
-                    r = nrows++;
-                    make_row(S, r, d + 1, c, K, tab, true, z, S.keys);
-                    if (lane == 0) S.rowmap[d * K + c] = r;
-                }
-            }
-            if (lane == 0) {
-                S.nrow[m] = r;
-                if (r >= 0) {  // first child
-                    S.fs[nf] = __fadd_rn(bs, S.ts[(size_t)r * K]);
-                    S.fp[nf] = m;
-                    S.fj[nf] = 0;
-                }
-            }
-            if (r >= 0) ++nf;
+            nf = (sib && kid) ? nf + 1 : ((sib || kid) ? nf : last);
             __syncwarp();
-            // blocks touched: the popped slot's, the old last slot's, the new last slot's
-            const int bx = x >> 5, bl = last >> 5, bn = nf > 0 ? (nf - 1) >> 5 : bl;
+            // blocks touched: the popped slot's, and the appended or vacated slot's
+            const int bx = x >> 5;
+            const int bo = (sib && kid) ? (nf - 1) >> 5 : ((!sib && !kid) ? last >> 5 : bx);
             refresh(bx, nf);
-            if (bl != bx) refresh(bl, nf);
-            if (bn != bx && bn != bl) refresh(bn, nf);
+            if (bo != bx) refresh(bo, nf);
         }
         if (lane == 0) S.misc[0] = n;
     }
