@@ -40,18 +40,20 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel, keyed by (kernel, workload, sha1 of the kernel's sources when the
 # capture was taken); a changed kernel reports null until it is captured again.
 KN1_TRAFFIC = {
-    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', 'e472a2dfd8ec0ad0ca4c3125948646905931dcf0'): 4932779,
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962261,
-    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 78582613,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 315160235,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 346956800,
-    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38963200,
-    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,
-    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 78582613,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 78582613,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', 'aa7c7432c9dbd36fa151c1e4b54b2f3e4366b852'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', '5357a3e39a57741ee6f50845876507318bf214c8'): 4933376,
+    ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', '5357a3e39a57741ee6f50845876507318bf214c8'): 4932267,
+    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 38962347,
+    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 78719403,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 315172864,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 347023019,
+    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 38962517,
+    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 38962261,
+    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 78719403,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 78719403,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 38962261,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 38962261,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 38962261,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta0', '2e50065f504d2d97bf0a774d40e1b56aab6a143a'): 38962261,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
 }
 STAGE1_SOURCES = {
     "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),
