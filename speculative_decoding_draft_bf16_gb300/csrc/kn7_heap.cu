@@ -19,13 +19,14 @@
 // first), push its first child and its next sibling.  Nodes are written in pop
 // order (parents before children).
 //
-// One CTA per request.  All warps first compute the order rows that fit in
-// shared memory (all of them for the usual sizes); warp 0 then runs the B pops
-// alone: the frontier (at most B + 1 entries) lives in shared memory, cut into
-// blocks of 32 slots whose maxima the lanes keep in registers, so a pop is a
-// warp max and one ballot; ties on the score go to the smaller descriptor,
-// found by walking both parent chains.  Rows that did not fit are computed by
-// warp 0 when a node needing them is popped.
+// One CTA per request.  All warps first compute every order row when they all
+// fit in shared memory (the usual sizes), else only the root's; warp 0 then
+// runs the B pops alone, computing a missing row when a node needing it is
+// popped.  The frontier (at most B + 1 entries, each carrying its parent's
+// order row and score) lives in shared memory, cut into blocks of 32 slots
+// whose maxima the lanes keep in registers, so a pop is a warp max and one
+// ballot; ties on the score go to the smaller descriptor, found by walking
+// both parent chains.  The popped slot takes one of the pushes.
 //
 // TDES table (kn8): the projections depend only on the token, so the inputs
 // are the per-token first-layer rows Ap = W_p g_p(e), Ac = W_c g_c(e) and the
