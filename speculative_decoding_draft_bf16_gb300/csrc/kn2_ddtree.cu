@@ -20,7 +20,9 @@
 // sort, and merge with C (merge path: one binary search per element).  Ties
 // across depths are resolved by walking the candidate's ancestors.  Stops at
 // the first depth that adds nothing.  Work per depth is O((|C| + m) log) plus
-// the sorts; everything lives in shared memory.
+// the sorts (up to 512 keys: warp-register sorts of 32-key segments ranked
+// against each other by binary search, two block barriers); everything lives
+// in shared memory.
 #include "dt_device.cuh"
 #include "dt_launch.h"
 
