@@ -31,7 +31,8 @@ namespace {
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int UNR = 4;      // maximum slots per thread; loads in flight per thread in pass 2
-constexpr int RING = 8;     // per-thread ring of 16-byte vectors in pass 1
+constexpr int RING = 8;     // per-thread ring of 16-byte vectors in pass 1 (two CTAs per SM)
+constexpr int RING_DEEP = 16;  // the same when every row has an SM to itself: more bytes in flight
 constexpr int CAP = 2048;   // candidates of a row
 
 struct Kn1bMisc {
@@ -56,7 +57,11 @@ constexpr size_t OFF_RS = OFF_HIST + 1024;
 constexpr size_t OFF_CAND = OFF_RS + 4096;
 constexpr size_t OFF_WORK = OFF_CAND + (size_t)CAP * 8;
 constexpr size_t OFF_RING = OFF_WORK + (size_t)CAP * 8;
-constexpr size_t SMEM = OFF_RING + (size_t)RING * NT * 16;
+template <int R>
+constexpr size_t smem_of() { return OFF_RING + (size_t)R * NT * 16; }
+constexpr size_t SMEM = smem_of<RING>();
+static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM with the shallow ring");
+static_assert(smem_of<RING_DEEP>() + 1024 <= 233472, "one CTA per SM with the deep ring");
 static_assert(sizeof(Kn1bMisc) <= OFF_HIST, "misc block overflows its slot");
 static_assert(sizeof(DtRankScratch) <= 4096, "rank scratch overflows its slot");
 static_assert((size_t)CAP * 8 >= (size_t)NW * 1024, "per-warp histograms must fit the work area");
@@ -227,8 +232,8 @@ __device__ __noinline__ void fallback_row(const T* __restrict__ rp, int V, int n
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(NT, 2) kn1b_kernel(const T* __restrict__ logits, int V, int Kc, int rows,
+template <typename T, int RING>
+__global__ void __launch_bounds__(NT, RING > 8 ? 1 : 2) kn1b_kernel(const T* __restrict__ logits, int V, int Kc, int rows,
                                                      float* __restrict__ lse_out, int32_t* __restrict__ cand_id,
                                                      float* __restrict__ cand_lp) {
     using E = DtElem<T>;
@@ -243,7 +248,8 @@ __global__ void __launch_bounds__(NT, 2) kn1b_kernel(const T* __restrict__ logit
     unsigned long long* bucket = (unsigned long long*)(smem + OFF_WORK);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
-    dt_pdl_trigger();
+    // No early trigger: the rows fill the SMs' shared memory and the bandwidth, and blocks of the next
+    // kernels parked beside them (waiting on this grid) only slowed the whole step down.
     dt_pdl_wait();  // the logits may come from the kernel just before us
 
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -277,7 +283,7 @@ __global__ void __launch_bounds__(NT, 2) kn1b_kernel(const T* __restrict__ logit
                 if (k % G == G - 1) dt_cp_commit();
             }
             for (int m0 = 0; m0 < nmine; m0 += UNR) {
-                const int rbase = m0 % RING;  // 0 or UNR
+                const int rbase = m0 % RING;  // a multiple of UNR
 #pragma unroll
                 for (int h = 0; h < UNR / G; ++h) {
                     if (m0 + h * G < nmine) {
@@ -444,19 +450,32 @@ __global__ void __launch_bounds__(NT, 2) kn1b_kernel(const T* __restrict__ logit
 
 size_t dt_kn1b_smem_bytes() { return SMEM; }
 
+template <typename T, int R>
+cudaError_t kn1b_launch_t(const void* logits, int rows, int V, int Kc, float* lse, int32_t* cand_id, float* cand_lp,
+                          cudaStream_t st) {
+    constexpr size_t sm = smem_of<R>();
+    cudaError_t e = cudaFuncSetAttribute(kn1b_kernel<T, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    DtLaunch lc(dim3(rows, 1, 1), dim3(NT, 1, 1), sm, st);
+    return cudaLaunchKernelEx(&lc.cfg, kn1b_kernel<T, R>, (const T*)logits, V, Kc, rows, lse, cand_id, cand_lp);
+}
+
 cudaError_t dt_kn1b_launch(const void* logits, int dtype, int rows, int V, int Kc, float* lse, int32_t* cand_id,
                            float* cand_lp, cudaStream_t st) {
-    DtLaunch lc(dim3(rows, 1, 1), dim3(NT, 1, 1), SMEM, st);
-    cudaError_t e;
-    if (dtype == DT_BF16) {
-        if ((e = cudaFuncSetAttribute(kn1b_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
-            cudaSuccess)
-            return e;
-        return cudaLaunchKernelEx(&lc.cfg, kn1b_kernel<uint16_t>, (const uint16_t*)logits, V, Kc, rows, lse, cand_id,
-                                  cand_lp);
+    // rows that each get an SM to themselves stream with the deep ring
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess) {
+            (void)cudaGetLastError();
+            sms = -1;
+        }
     }
-    if ((e = cudaFuncSetAttribute(kn1b_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
-        cudaSuccess)
-        return e;
-    return cudaLaunchKernelEx(&lc.cfg, kn1b_kernel<float>, (const float*)logits, V, Kc, rows, lse, cand_id, cand_lp);
+    const bool deep = sms > 0 && rows <= sms;
+    if (dtype == DT_BF16)
+        return deep ? kn1b_launch_t<uint16_t, RING_DEEP>(logits, rows, V, Kc, lse, cand_id, cand_lp, st)
+                    : kn1b_launch_t<uint16_t, RING>(logits, rows, V, Kc, lse, cand_id, cand_lp, st);
+    return deep ? kn1b_launch_t<float, RING_DEEP>(logits, rows, V, Kc, lse, cand_id, cand_lp, st)
+                : kn1b_launch_t<float, RING>(logits, rows, V, Kc, lse, cand_id, cand_lp, st);
 }
