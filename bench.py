@@ -42,19 +42,19 @@ L2_BYTES = 129 * 1024 * 1024
 KN1_TRAFFIC = {
     ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', '5357a3e39a57741ee6f50845876507318bf214c8'): 4933376,
     ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', '5357a3e39a57741ee6f50845876507318bf214c8'): 4932267,
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 38962688,
-    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 78445141,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 315046741,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 346472875,
-    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 38962091,
-    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 38962176,
-    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 78445141,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 78445141,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta0', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 38962176,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'ddtree_saba_b16_L16_V151936_K256_Bmax256', 'ac53148d6dad917bbcabd3f4a50b7181f126f01b'): 78517163,
+    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38965589,
+    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78574336,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 314991445,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 342579712,
+    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962176,
+    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,
+    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta0', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'ddtree_saba_b16_L16_V151936_K256_Bmax256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78566571,
 }
 STAGE1_SOURCES = {
     "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),

@@ -8,7 +8,8 @@
 //   pass 1  streams the row from HBM: each thread copies its 16-byte
 //           vectors (every NT-th) asynchronously into its own ring of RING
 //           shared-memory slots, RING - 1 copies in flight, and keeps a running
-//           maximum and sum exp(x - max) (rescaled whenever the maximum grows)
+//           maximum and sum exp(x - max) (rescaled whenever the maximum grows;
+//           the two vectors of each landed copy group are folded in together)
 //           and the maximum of its vectors m = u (mod 4) for u = 0..3 -- 4 x 512
 //           = 2048 maxima of distinct elements;
 //   the CTA merges the (max, sum) pairs into the row's log-normaliser and
@@ -86,23 +87,25 @@ DT_DI void online_add(const float (&x)[EPV], float vm, float& M, float& S) {
         S = (M == NEG_INF) ? 0.f : __fmul_rn(S, dt_ex2_approx(__fmul_rn(__fsub_rn(M, vm), log2e)));
         M = vm;
     }
-    if (M == NEG_INF) return;  // every element so far is -inf
     if (fabsf(M) < 64.f) {
-        // two lanes per packed f32x2 instruction
+        // two lanes per packed f32x2 instruction; with 8 or more elements two
+        // independent accumulators shorten the dependent chain
         const float c = __fmul_rn(M, log2e);
         const unsigned long long l2 = dt_f2_pack(log2e, log2e), c2 = dt_f2_pack(-c, -c);
-        unsigned long long acc = dt_f2_pack(0.f, 0.f);
+        unsigned long long acc[2] = {dt_f2_pack(0.f, 0.f), dt_f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int s = 0; s < EPV; s += 2) {
             float d0, d1;
             dt_f2_unpack(dt_f2_fma(dt_f2_pack(x[s], x[s + 1]), l2, c2), d0, d1);
-            acc = dt_f2_add(acc, dt_f2_pack(dt_ex2_approx(d0), dt_ex2_approx(d1)));
+            unsigned long long& a = acc[EPV >= 8 ? (s >> 1) & 1 : 0];
+            a = dt_f2_add(a, dt_f2_pack(dt_ex2_approx(d0), dt_ex2_approx(d1)));
         }
         float a0, a1;
-        dt_f2_unpack(acc, a0, a1);
+        dt_f2_unpack(EPV >= 8 ? dt_f2_add(acc[0], acc[1]) : acc[0], a0, a1);
         S = __fadd_rn(S, __fadd_rn(a0, a1));
         return;
     }
+    if (M == NEG_INF) return;  // every element so far is -inf
     float e[EPV];
 #pragma unroll
     for (int s = 0; s < EPV; ++s) e[s] = dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], M), log2e));
@@ -294,17 +297,26 @@ __global__ void __launch_bounds__(NT, RING > 8 ? 1 : 2) kn1b_kernel(const T* __r
                                 dt_cp_async16(ring + ((rbase + (h + PRE) * G + j) % RING) * NT, src + (size_t)(mi + j) * NT);
                         dt_cp_commit();
                         dt_cp_wait<PRE>();  // this group has landed
-#pragma unroll
-                        for (int j = 0; j < G; ++j) {
-                            const int u = h * G + j;
-                            if (m0 + u < nmine) {
-                                const uint4 q = ring[(rbase + u) * NT];
-                                const float vm = dt_vec_max<T>(q);
-                                gm[u] = fmaxf(gm[u], vm);
-                                float x[EPV];
-                                dt_vec_vals<T>(q, x);
-                                online_add<EPV>(x, vm, M, S);
-                            }
+                        // the group's two vectors fold into (M, S) together: one
+                        // rescale check and two chains of packed adds per pair
+                        static_assert(G == 2, "vectors are folded in pairs");
+                        const int u = h * G;
+                        if (m0 + u + 1 < nmine) {
+                            const uint4 qa = ring[(rbase + u) * NT], qb = ring[(rbase + u + 1) * NT];
+                            const float va = dt_vec_max<T>(qa), vb = dt_vec_max<T>(qb);
+                            gm[u] = fmaxf(gm[u], va);
+                            gm[u + 1] = fmaxf(gm[u + 1], vb);
+                            float x[2 * EPV];
+                            dt_vec_vals<T>(qa, *reinterpret_cast<float(*)[EPV]>(x));
+                            dt_vec_vals<T>(qb, *reinterpret_cast<float(*)[EPV]>(x + EPV));
+                            online_add<2 * EPV>(x, fmaxf(va, vb), M, S);
+                        } else {  // the thread's last vector, on its own
+                            const uint4 q = ring[(rbase + u) * NT];
+                            const float vm = dt_vec_max<T>(q);
+                            gm[u] = fmaxf(gm[u], vm);
+                            float x[EPV];
+                            dt_vec_vals<T>(q, x);
+                            online_add<EPV>(x, vm, M, S);
                         }
                     }
                 }
