@@ -8,6 +8,7 @@ for what pins it.
 """
 import ctypes
 import dataclasses
+import os
 
 import numpy as np
 
@@ -25,7 +26,9 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 def lib():
     global _LIB
     if _LIB is None:
-        path = _build.build()
+        # DT_ORACLE_LIB: another build of the oracle source (the mutation tests
+        # load deliberately broken copies this way, one per process)
+        path = os.environ.get("DT_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         L.or_exp_canon.restype = ctypes.c_float
         L.or_exp_canon.argtypes = [ctypes.c_float]

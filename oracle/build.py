@@ -17,17 +17,21 @@ CFLAGS = ["-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off",
           "-fno-fast-math", "-fexcess-precision=standard", "-Wall"]
 
 
+def compile_to(src: str, out: str) -> str:
+    """Compile an oracle source file into the shared library `out` (same flags)."""
+    tmp = out + ".tmp%d" % os.getpid()
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle if its library is missing or older than its source."""
     if (not force and os.path.exists(LIB)
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = ["gcc", *CFLAGS, "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    return compile_to(SRC, LIB)
 
 
 if __name__ == "__main__":

@@ -140,6 +140,8 @@ int or_candidates(const float* x, int64_t rows, int32_t V, int32_t Kc,
 /* (0-based per-position ranks), a proper prefix before its extensions.        */
 /* [DARTree] Lemma 1 ("ancestors first on ties"); [DDTree] section 3.3 (heap   */
 /* of (-score, rho) tuples orders equal scores by the descriptor tuple).       */
+/* Pinned: a parent and child of equal score (lp = 0) stay in that order in    */
+/* TALON's output and in DARTree's TopB(S) (tests).                            */
 /* ------------------------------------------------------------------------- */
 typedef struct {
     float s;               /* path score */
@@ -481,7 +483,7 @@ int or_uniform_widths(int B, int L, int32_t* widths)
 /* ring[count % w] and count is incremented.  conf, degen in double.           */
 /* Pinned: argmax = c_fixed / c_verify when that is an integer in range, the    */
 /* clamps, independence from the history, hand-computed conf / degen / hist /  */
-/* a (tests).                                                                  */
+/* a, the smallest of budgets whose fp32 scores tie (tests).                   */
 /* ------------------------------------------------------------------------- */
 int or_saba(const float* top_lp /* [D] lp of each position's top candidate */, int D,
             const float* hidden /* nullable [D][Hd] */, int Hd,
@@ -890,7 +892,8 @@ int or_tree_mask(const int32_t* parent, const int32_t* depth, int M, int Mmax,
 /* acc_nodes[0] = 0 (root), acc_nodes[1..acc_len] the accepted nodes, the rest */
 /* -1.  visited rows only.                                                     */
 /* Pinned: chain tree = sequential greedy decoding; hash-defined target (the   */
-/* accepted path equals greedy decoding until it leaves the tree) (tests).     */
+/* accepted path equals greedy decoding until it leaves the tree); a tie of    */
+/* two tokens goes to the smaller id (tests).                                  */
 /* ------------------------------------------------------------------------- */
 int or_verify_greedy(const int32_t* tok, const int32_t* parent, const int32_t* depth,
                      int M, int L, const float* target, int V,
@@ -939,7 +942,8 @@ int or_verify_greedy(const int32_t* tok, const int32_t* parent, const int32_t* d
 /* lse_in supplies it per node ([Mmax], row n's normaliser); lse_out receives  */
 /* the values used, per step of the walk.                                      */
 /* Pinned: worked example through a one-child chain, output frequencies equal  */
-/* p within 3 sigma, R = 0 and p = 0 edge cases (tests).                       */
+/* p within 3 sigma, R = 0 and p = 0 edge cases, a uniform of exactly 1/2 over */
+/* two equal masses draws the second token (tests).                            */
 /* ------------------------------------------------------------------------- */
 static uint64_t or_fixed32(float p)
 {

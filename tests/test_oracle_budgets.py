@@ -84,6 +84,16 @@ def test_saba_budget_clamps_to_the_range():
     assert oracle.saba(np.zeros(2, np.float32), None, st, -1, 10.0, 1.0, 16, 256)[0] == 16
 
 
+def test_saba_takes_the_smallest_budget_on_ties():
+    # The reading: the smallest B among equal scores.  With c_fixed = 0 the
+    # objective a sqrt(B) / (B c_verify) falls with B, so the range's first
+    # budget is the maximum; evaluated in fp32, budgets past 2^24 share float
+    # values (2^25, 2^25 + 1 and 2^25 + 2 all become 2^25) and tie with it.
+    st = oracle.SabaState(2)
+    lo = 1 << 25
+    assert oracle.saba(np.zeros(2, np.float32), None, st, -1, 1.0, 0.0, lo, lo + 3)[0] == lo
+
+
 def test_saba_state_by_hand():
     # conf: top probabilities 0.5 and 0.25 -> 0.375
     # degen: h = (1,0), (1,0), (0,1): r = (1, 0), mean 0.5, growth 0 - 1 -> -0.5

@@ -396,6 +396,29 @@ def test_talon_mu_one_is_a_chain_and_flat_fills_first_layer():
     assert set(t.depth[1:t.n].tolist()) == {1, 2}
 
 
+def test_equal_scores_put_ancestors_first():
+    # [DARTree] Lemma 1: on equal scores ancestors come first.  A drafter that is
+    # certain at position 2 (lp = 0 for its top token) gives every depth-2 child
+    # of rank 0 its parent's score; the node order must still put the parent
+    # first, so the output stays topological, and DARTree's TopB(S) still equals
+    # the best-first heap (beta = 0, every log-probability <= 0).
+    lp = np.array([[-0.5, -1.0, -2.0, -3.0],
+                   [0.0, -100.0, -100.0, -100.0],
+                   [-0.25, -1.5, -2.5, -3.5]], np.float32)
+    ids = np.tile(np.arange(4, dtype=np.int32), (3, 1))
+    t = oracle.talon(lp, ids, 2, np.float32(math.log(0.3)), 8)
+    ties = 0
+    for n in range(1, t.n):
+        assert t.parent[n] < n, (n, t.parent[:t.n])
+        ties += int(t.score[n] == t.score[t.parent[n]])
+    assert ties >= 2  # both depth-1 nodes have an equal-score child
+    U = np.zeros((4, 8), np.float32)
+    tree, info, _ = oracle.dartree(lp, ids, U, U, -1, 4, 0.0, 10, Mmax=11)
+    assert info["topb_equals_bestfirst"]
+    assert all(tree.parent[n] < n for n in range(1, tree.n))
+    assert sum(int(tree.score[n] == tree.score[tree.parent[n]]) for n in range(1, tree.n)) >= 2
+
+
 # --------------------------------------------------------------------------
 # Tree mask
 # --------------------------------------------------------------------------
@@ -468,6 +491,38 @@ def test_verify_greedy_chain_rule():
         assert alen == expect_len
         assert acc[:alen + 1].tolist() == list(range(alen + 1))
         assert nxt == int(np.argmax(tgt[alen]))
+
+
+def test_verify_greedy_ties_go_to_the_smallest_token_id():
+    # [Unit11] temperature section: a greedy tie goes to the smallest vocabulary
+    # index.  Row 0 peaks at tokens 2 and 5 alike; the root's children carry 5
+    # (rank 0) and 2 (rank 1): the walk must take token 2's child.
+    V, L = 8, 3
+    t = oracle.Tree(np.array([-1, 5, 2], np.int32), np.array([-1, 0, 0], np.int32), np.array([0, 1, 1], np.int32),
+                    np.array([-1, 0, 1], np.int32), np.zeros(3, np.float32), 3)
+    tgt = np.zeros((3, V), np.float32)
+    tgt[0, [2, 5]] = 4.0
+    tgt[2, 7] = 3.0
+    tgt[1, 6] = 3.0
+    acc, alen, nxt = oracle.verify_greedy(t, tgt, L)
+    assert alen == 1 and acc[1] == 2 and nxt == 7
+
+
+def test_draw_at_a_mass_boundary_takes_the_next_token():
+    # The draw is an inverse CDF over half-open intervals: with two equal masses
+    # a uniform of exactly 1/2 lies at the start of the second token's interval.
+    # A root without children draws its token from the target row alone.
+    V, L, Mmax = 4, 2, 1
+    root = oracle.Tree(np.array([-1], np.int32), np.array([-1], np.int32), np.array([0], np.int32),
+                       np.array([-1], np.int32), np.zeros(1, np.float32), 1)
+    tgt = np.array([[1.5, 1.5, -np.inf, -np.inf]], np.float32)
+    draft = np.zeros((L, V), np.float32)
+    dl = np.full(L, np.log(V), np.float32)
+    for u1, want in ((0.5, 1), (0.4999999, 0), (0.0, 0), (0.9999999, 1)):
+        u = np.array([[0.0], [u1]], np.float32)
+        for rule in ("ratio", "target_match"):
+            _, alen, nxt, _ = oracle.verify_t1(root, tgt, draft, dl, u, L, Mmax, rule=rule)
+            assert alen == 0 and nxt == want, (u1, rule, nxt)
 
 
 def test_verify_greedy_equals_sequential_greedy_with_hash_target():
