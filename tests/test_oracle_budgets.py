@@ -105,6 +105,8 @@ def test_saba_state_by_hand():
     assert s0[2] == 0.0 and s0[3] == 1.0  # no history yet
     for prev in (3, 5, 7):
         _, s = oracle.saba(top, hid, st, prev, 1.0, 10.0, 1, 64)
+        if prev == 3:  # one round recorded, fewer than w: hist 3, a = 3 + 1
+            assert s[2] == 3.0 and s[3] == 4.0
     assert abs(s[0] - (0.5 + 0.25 + 0.375) / 3) < 1e-6
     assert abs(s[1] - (-0.5)) < 1e-6
     assert s[2] == 6.0 and s[3] == 7.0

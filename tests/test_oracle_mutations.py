@@ -94,6 +94,41 @@ MUTANTS = [
      "lpq = lpq - z; }", [VARIANTS]),
     ("target_match_wrong_uniform", "y = or_draw(w, V, S, u[Mmax + n]);", "y = or_draw(w, V, S, u[n]);", [VARIANTS]),
     ("scalar_residual_not_clipped", "residual[i] = z > 0.0 ? z : 0.0;", "residual[i] = z;", [PINS]),
+    ("t1_drafter_row_off_by_one", "int pos = depth[c] - 1;", "int pos = depth[c];", [PINS]),
+    ("t1_accept_wrong_uniform_row", "if (u[c] < ratio) acc = c;", "if (u[Mmax + c] < ratio) acc = c;", [PINS]),
+    ("iter_accept_scale_halved", "unsigned __int128 rhs = (unsigned __int128)W << 56;",
+     "unsigned __int128 rhs = (unsigned __int128)W << 55;", [VARIANTS]),
+    ("t1_markov_every_parent_takes_rank0_norm",
+     "if (ptok >= 0 && pos < L) z = znorm[pos * K + (n == 0 ? 0 : rank[n])];",
+     "if (ptok >= 0 && pos < L) z = znorm[pos * K];", [VARIANTS]),
+    # more of stage 1, the selections and the tables
+    ("exp_underflows_early", "if (x < -86.0f) return 0.0f;", "if (x < -80.0f) return 0.0f;", [PINS]),
+    ("markov_dot_drops_last_term", "for (int k = 0; k < R; ++k)\n        acc = fmaf(",
+     "for (int k = 0; k < R - 1; ++k)\n        acc = fmaf(", [PINS, HEAP, NORM, VARIANTS]),
+    ("dartree_depth1_skips_root_term", "if (U != NULL && ptok >= 0) {", "if (U != NULL && ptok >= 0 && d > 1) {",
+     [PINS, NORM]),
+    ("ddtree_budget_plus_one",
+     "while (rc == OR_OK && n < B && h.n > 0) {\n        or_node x = or_heap_pop(&h);\n        /* the parent",
+     "while (rc == OR_OK && n <= B && h.n > 0) {\n        or_node x = or_heap_pop(&h);\n        /* the parent",
+     [PINS]),
+    ("talon_truncates_one_short", "npass = room;", "npass = room - 1;", [PINS]),
+    ("talon_root_scores_zero", "x->d = 1; x->r[0] = r; x->s = lp[r];", "x->d = 1; x->r[0] = r; x->s = 0.0f;",
+     [PINS]),
+    ("heap_child_ties_by_larger_rank", "return a < b ? -1 : (a > b ? 1 : 0);", "return a > b ? -1 : (a < b ? 1 : 0);",
+     [HEAP]),
+    ("heap_first_child_wrong_row", "ch.s = x.s + or_hs_edge(ch.d, c, ord[(size_t)n * K]);",
+     "ch.s = x.s + or_hs_edge(ch.d, jpos, ord[(size_t)n * K]);", [HEAP]),
+    ("norm_parent_row_off_by_one", "const int u = (d == 0) ? (i == 0 ? root_tok : -1) : id[(d - 1) * K + i];",
+     "const int u = (d == 0) ? (i == 0 ? root_tok : -1) : id[d * K + i];", [NORM, HEAP]),
+    ("tdes_wrong_depth_row", "a = a + Dd[(int64_t)d * H + h];", "a = a + Dd[(int64_t)(d > 0 ? d - 1 : 0) * H + h];",
+     [HEAP]),
+    ("saba_hist_over_window", "float hist = n ? (float)sum / (float)n : 0.0f;",
+     "float hist = n ? (float)sum / (float)w : 0.0f;", [BUDGETS]),
+    ("saba_gain_drops_the_bonus_token", "float a = n ? (float)(sum + n) / (float)n : 1.0f;",
+     "float a = n ? (float)sum / (float)n : 1.0f;", [BUDGETS]),
+    ("saba_conf_without_exp", "conf += exp((double)top_lp[d]);", "conf += (double)top_lp[d];", [BUDGETS]),
+    ("tree_check_skips_depth", "if (depth[n] != depth[p] + 1) return 0;", "", [PINS]),
+    ("mask_bit_modulo_31", "row[a / 32] |= 1u << (a % 32);", "row[a / 32] |= 1u << (a % 31);", [PINS]),
 ]
 
 

@@ -274,3 +274,40 @@ def test_markov_walk_preserves_p_when_the_child_is_drawn_from_q_tilde(proposal, 
         assert np.all(dev <= 3.5), (counts / n, p)
     else:
         assert np.max(dev) > 10, (counts / n, p)
+
+
+def test_markov_walk_uses_the_parents_own_normaliser():
+    # The proposal below a node u is q~(. | tok(u)) normalised by u's own row of
+    # the normalisers (its position, its candidate rank).  Root -> u (token 1, the
+    # rank-1 candidate of position 1, accepted with certainty) -> one child drawn
+    # from q~(. | 1): the token at position 2 must follow p.  The rank-0
+    # candidate (token 3) has another normaliser, which would bias it.
+    V, R, L, root = 6, 2, 2, 4
+    rng = np.random.default_rng(9)
+    x = np.array([[0.3, 0.9, -0.2, 1.1, 0.0, -0.4],
+                  [1.0, 0.5, 0.0, -0.5, 0.2, 0.8]], np.float32)
+    U = (rng.standard_normal((V, R)) * 1.5).astype(np.float32)
+    Vt = (rng.standard_normal((V, R)) * 1.5).astype(np.float32)
+    ids = np.array([[3, 1], [0, 1]], np.int32)
+    z = oracle.markov_norm(x, ids, U, Vt, root)
+    assert abs(float(z[1, 0]) - float(z[1, 1])) > 0.2  # the two parents' normalisers differ
+    qt = _qtilde(x[1], U, Vt, 1, float(z[1, 1]))
+    assert abs(qt.sum() - 1) < 1e-5
+    p = np.array([0.05, 0.3, 0.1, 0.25, 0.2, 0.1])
+    sure = np.full(V, -30.0, np.float32)
+    sure[1] = 0.0  # the root's target takes token 1: u is always accepted
+    rows = np.stack([sure, np.log(p).astype(np.float32), np.log(np.full(V, 1 / V)).astype(np.float32)])
+    l32 = np.array([np.logaddexp.reduce(r.astype(np.float64)) for r in x], np.float32)
+    n = 30_000
+    counts = np.zeros(V, np.int64)
+    cq = np.cumsum(qt)
+    for _ in range(n):
+        tok = int(min(np.searchsorted(cq, rng.random(), side="right"), V - 1))
+        t = _tree([-1, 1, tok], [-1, 0, 1], [-1, 1, 0])
+        u = rng.random((2, 3)).astype(np.float32)
+        acc, alen, nxt = oracle.verify_t1_markov(t, rows, x, l32, U, Vt, root, z, u, L, 3,
+                                                 lse_in=np.zeros(3, np.float32))
+        assert alen >= 1
+        counts[tok if alen == 2 else nxt] += 1
+    dev = np.abs(counts / n - p) / np.sqrt(p * (1 - p) / n)
+    assert np.all(dev <= 3.5), (counts / n, p)
