@@ -92,6 +92,12 @@ def test_saba_takes_the_smallest_budget_on_ties():
     st = oracle.SabaState(2)
     lo = 1 << 25
     assert oracle.saba(np.zeros(2, np.float32), None, st, -1, 1.0, 0.0, lo, lo + 3)[0] == lo
+    # c_fixed / c_verify = 1000.5 puts the optimum between 1000 and 1001, whose
+    # fp32 scores are equal (checked here with numpy's float32 arithmetic)
+    f = np.float32
+    u = [f(f(1.0) * np.sqrt(f(b))) / f(f(b) * f(1.0) + f(1000.5)) for b in (1000, 1001)]
+    assert u[0] == u[1]
+    assert oracle.saba(np.zeros(2, np.float32), None, st, -1, 1.0, 1000.5, 1, 1024)[0] == 1000
 
 
 def test_saba_state_by_hand():
