@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -37,24 +38,25 @@ METRIC = "draft trees built+verified/sec and logit-read HBM GB/s (% of GB300 pea
 L2_BYTES = 129 * 1024 * 1024
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the stage-1
-# kernel, keyed by (kernel, workload, sha1 of the kernel's sources when the
-# capture was taken); a changed kernel reports null until it is captured again.
+# kernel, keyed by (kernel, workload, sha1 of the kernel's sources -- code only,
+# comments and whitespace dropped -- when the capture was taken); a changed
+# kernel reports null until it is captured again.
 KN1_TRAFFIC = {
-    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', '5357a3e39a57741ee6f50845876507318bf214c8'): 4933376,
-    ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', '5357a3e39a57741ee6f50845876507318bf214c8'): 4932267,
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38965589,
-    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78574336,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 314991445,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 342579712,
-    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962176,
-    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,
-    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta0', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'ddtree_saba_b16_L16_V151936_K256_Bmax256', '0bba34c2b5066a6ddef519c7bb17b18aab51f22c'): 78566571,
+    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', 'b98ce52d59fa86e838199b13597ff315854b0179'): 4933376,
+    ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', 'b98ce52d59fa86e838199b13597ff315854b0179'): 4932267,
+    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38965589,
+    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78574336,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', '941c75344dafb22507da4ed1256971f75afc3e9e'): 314991445,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', '941c75344dafb22507da4ed1256971f75afc3e9e'): 342579712,
+    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962176,
+    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,
+    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
+    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta0', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
+    ('kn1b_kernel', 'ddtree_saba_b16_L16_V151936_K256_Bmax256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78566571,
 }
 STAGE1_SOURCES = {
     "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),
@@ -62,11 +64,19 @@ STAGE1_SOURCES = {
 }
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace runs collapsed: what the compiler sees,
+    so that a comment edit does not void counters taken on unchanged code."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def stage1_source_hash(kernel):
     h = hashlib.sha1()
     for f in STAGE1_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "speculative_decoding_draft_bf16_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "speculative_decoding_draft_bf16_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

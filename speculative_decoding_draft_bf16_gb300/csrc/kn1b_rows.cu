@@ -7,9 +7,11 @@
 // CTA needs no cross-CTA exchange at all:
 //   pass 1  streams the row from HBM: each thread copies its 16-byte
 //           vectors (every NT-th) asynchronously into its own ring of RING
-//           shared-memory slots, RING - 1 copies in flight, and keeps a running
-//           maximum and sum exp(x - max) (rescaled whenever the maximum grows;
-//           the two vectors of each landed copy group are folded in together)
+//           shared-memory slots (16 at one CTA per SM when every row has an SM
+//           to itself, else 8 at two per SM), in pairs, RING - 2 copies in
+//           flight, and keeps a running maximum and sum exp(x - max) (rescaled
+//           whenever the maximum grows; the two vectors of each landed pair are
+//           folded in together)
 //           and the maximum of its vectors m = u (mod 4) for u = 0..3 -- 4 x 512
 //           = 2048 maxima of distinct elements;
 //   the CTA merges the (max, sum) pairs into the row's log-normaliser and
