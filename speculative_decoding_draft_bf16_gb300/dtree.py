@@ -125,14 +125,47 @@ def _dtype_code(t):
     raise TypeError("logits must be bfloat16 or float32, got %s" % t.dtype)
 
 
-def _need(t, dtype=None, name="tensor"):
+def _need(t, dtype=None, name="tensor", numel=None):
+    """A contiguous CUDA tensor (of dtype), holding at least numel elements: the
+    C ABI takes bare pointers, so sizes are checked here, before any launch."""
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     if dtype is not None and t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    _need_numel(t, numel, name)
     return t
+
+
+def _need_numel(t, numel, name):
+    if numel is not None and t.numel() < numel:
+        raise ValueError("%s holds %d elements, the call reads or writes %d" % (name, t.numel(), numel))
+
+
+def _need_batch(tree, batch):
+    """The tree buffers (dt_tree carries no batch size) must hold `batch` requests."""
+    if batch > tree.batch:
+        raise ValueError("the tree buffers hold %d requests, the call covers %d" % (tree.batch, batch))
+
+
+def _need_logits(t, p, name="draft_logits"):
+    """[batch, L, V] drafter logits of Params p's dtype."""
+    _need(t, name=name, numel=p.batch * p.L * p.V)
+    if _dtype_code(t) != (DT_BF16 if p.dtype == "bf16" else DT_F32):
+        raise TypeError("%s must be %s for dtype=%r, got %s" % (name, "bfloat16" if p.dtype == "bf16" else "float32",
+                                                                p.dtype, t.dtype))
+    if t.shape[-1] != p.V:
+        raise ValueError("%s rows must hold V = %d logits, got %d" % (name, p.V, t.shape[-1]))
+
+
+def _need_workspace(workspace):
+    ws, n = (workspace if workspace is not None else (None, 0))
+    if ws is not None:
+        _need(ws, name="workspace")
+        if ws.numel() * ws.element_size() < n:
+            raise ValueError("workspace holds %d bytes, %d were declared" % (ws.numel() * ws.element_size(), n))
+    return ws, n
 
 
 @dataclasses.dataclass
@@ -167,7 +200,9 @@ class Params:
     def budget(self):
         return self.N if self.mode == "talon" else self.B
 
-    def struct(self):
+    def struct(self, for_launch=True):
+        """The dt_build_params block.  for_launch: check the device tensors it points
+        to (the host-only queries, workspace_size and stage1_plan, read no tensor)."""
         log_mu = 0.0
         if self.mode == "talon":
             log_mu = float(torch.tensor(math.log(self.mu), dtype=torch.float64).float())
@@ -175,12 +210,24 @@ class Params:
                          DT_BF16 if self.dtype == "bf16" else DT_F32, self.K, self.B, self.W,
                          self.beta, self.R if self.U is not None else 0, _ptr(self.U), _ptr(self.Vt),
                          _ptr(self.root_tok), self.talon_k, log_mu, self.N, int(bool(self.markov_norm)))
+        if for_launch:
+            if self.U is not None:
+                _need(self.U, torch.float32, "U", numel=self.V * self.R)
+                _need(self.Vt, torch.float32, "Vt", numel=self.V * self.R)
+            if self.root_tok is not None:
+                _need(self.root_tok, torch.int32, "root_tok", numel=self.batch)
+            if self.budgets is not None:
+                _need(self.budgets, torch.int32, "budgets", numel=self.batch)
         if self.tdes is not None:
+            if for_launch:
+                H = int(self.tdes.w.shape[0])
+                _need_numel(self.tdes.Ap, self.V * H, "Ap")
+                _need_numel(self.tdes.Ac, self.V * H, "Ac")
+                _need_numel(self.tdes.Dd, self.L * H, "Dd")
             bp._tdes = self.tdes.struct()  # kept alive with the parameter block
             bp.tdes = ctypes.pointer(bp._tdes)
         bp.budget_policy = BUDGET_POLICY[self.budget_policy]
         if self.budgets is not None:
-            _need(self.budgets, torch.int32, "budgets")
             bp.budget = _ptr(self.budgets)
         return bp
 
@@ -233,7 +280,7 @@ class TreeBuffers:
 
 def workspace_size(p):
     ok = ctypes.c_int(0)
-    n = lib().dt_workspace_size(ctypes.byref(p.struct()), ctypes.byref(ok))
+    n = lib().dt_workspace_size(ctypes.byref(p.struct(for_launch=False)), ctypes.byref(ok))
     if not ok.value:
         raise DtError("invalid parameters for dt_workspace_size")
     return int(n)
@@ -245,8 +292,8 @@ def make_workspace(p, device="cuda"):
 
 
 def candidates(p, draft_logits, tree, stream=None):
-    _need(draft_logits, name="draft_logits")
-    assert _dtype_code(draft_logits) == (DT_BF16 if p.dtype == "bf16" else DT_F32)
+    _need_logits(draft_logits, p)
+    _need_batch(tree, p.batch)
     _check(lib().dt_candidates(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()),
                                _stream(stream)), "dt_candidates")
 
@@ -256,12 +303,15 @@ def stage1_plan(p):
     """(kernel, cluster) that candidates() launches for Params p: kernel is
     "cluster" (each row over a cluster of `cluster` CTAs) or "rows" (a CTA per row)."""
     k, c = _i32(0), _i32(0)
-    _check(lib().dt_stage1_plan(ctypes.byref(p.struct()), ctypes.byref(k), ctypes.byref(c)), "dt_stage1_plan")
+    _check(lib().dt_stage1_plan(ctypes.byref(p.struct(for_launch=False)), ctypes.byref(k), ctypes.byref(c)),
+           "dt_stage1_plan")
     return ({DT_STAGE1_CLUSTER: "cluster", DT_STAGE1_ROWS: "rows"}[k.value], c.value)
 
 def markov_norm(p, draft_logits, tree, workspace, stream=None):
     """Full-vocabulary DARTree log-normalisers into the workspace (dt_markov_norm)."""
-    ws, n = workspace
+    _need_logits(draft_logits, p)
+    _need_batch(tree, p.batch)
+    ws, n = _need_workspace(workspace)
     _check(lib().dt_markov_norm(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()), _ptr(ws),
                                 n, _stream(stream)), "dt_markov_norm")
 
@@ -275,7 +325,8 @@ def znorm_view(p, workspace):
 
 
 def select(p, tree, workspace=None, stream=None):
-    ws, n = (workspace if workspace is not None else (None, 0))
+    _need_batch(tree, p.batch)
+    ws, n = _need_workspace(workspace)
     _check(lib().dt_select(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _ptr(ws), n, _stream(stream)),
            "dt_select")
 
@@ -283,15 +334,16 @@ def select(p, tree, workspace=None, stream=None):
 def select_dartree_noalloc(p, tree, stream=None):
     """DARTree selection with the library's own fixed table (no workspace);
     see dt_select_dartree_noalloc in include/dtree.h."""
+    _need_batch(tree, p.batch)
     _check(lib().dt_select_dartree_noalloc(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _stream(stream)),
            "dt_select_dartree_noalloc")
 
 
 def build_tree(p, draft_logits, tree, workspace=None, stream=None):
     """Stage 1 + selection.  workspace: (tensor, bytes) from make_workspace (DARTree)."""
-    _need(draft_logits, name="draft_logits")
-    assert _dtype_code(draft_logits) == (DT_BF16 if p.dtype == "bf16" else DT_F32)
-    ws, n = (workspace if workspace is not None else (None, 0))
+    _need_logits(draft_logits, p)
+    _need_batch(tree, p.batch)
+    ws, n = _need_workspace(workspace)
     _check(lib().dt_build_tree(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()),
                                _ptr(ws), n, _stream(stream)), "dt_build_tree")
 
@@ -299,9 +351,9 @@ def build_tree(p, draft_logits, tree, workspace=None, stream=None):
 
 def select_mask(p, tree, mask, pos, workspace=None, pos_offset=0, stream=None):
     """select + tree_mask with the mask written by the selection kernel (dt_select_mask)."""
-    _need(mask, torch.int32, "mask")
-    _need(pos, torch.int32, "pos")
-    ws, n = (workspace if workspace is not None else (None, 0))
+    _need_batch(tree, p.batch)
+    _need_mask(tree, p.batch, mask, pos)
+    ws, n = _need_workspace(workspace)
     _check(lib().dt_select_mask(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _ptr(ws), n, int(pos_offset),
                                 _ptr(mask), _ptr(pos), _stream(stream)), "dt_select_mask")
 
@@ -309,20 +361,43 @@ def select_mask(p, tree, mask, pos, workspace=None, pos_offset=0, stream=None):
 def build_tree_mask(p, draft_logits, tree, mask, pos, workspace=None, pos_offset=0, stream=None):
     """build_tree + tree_mask with the mask written by the selection kernel
     (dt_build_tree_mask); mask, pos from alloc_mask(tree)."""
-    _need(draft_logits, name="draft_logits")
-    assert _dtype_code(draft_logits) == (DT_BF16 if p.dtype == "bf16" else DT_F32)
-    _need(mask, torch.int32, "mask")
-    _need(pos, torch.int32, "pos")
-    ws, n = (workspace if workspace is not None else (None, 0))
+    _need_logits(draft_logits, p)
+    _need_batch(tree, p.batch)
+    _need_mask(tree, p.batch, mask, pos)
+    ws, n = _need_workspace(workspace)
     _check(lib().dt_build_tree_mask(ctypes.byref(p.struct()), _ptr(draft_logits), ctypes.byref(tree.struct()),
                                     _ptr(ws), n, int(pos_offset), _ptr(mask), _ptr(pos), _stream(stream)),
            "dt_build_tree_mask")
 
 def tree_mask(tree, mask, pos, pos_offset=0, batch=None, stream=None):
-    _need(mask, torch.int32, "mask")
-    _need(pos, torch.int32, "pos")
-    _check(lib().dt_tree_mask(ctypes.byref(tree.struct()), batch or tree.batch, pos_offset, _ptr(mask), _ptr(pos),
+    batch = batch or tree.batch
+    _need_batch(tree, batch)
+    _need_mask(tree, batch, mask, pos)
+    _check(lib().dt_tree_mask(ctypes.byref(tree.struct()), batch, pos_offset, _ptr(mask), _ptr(pos),
                               _stream(stream)), "dt_tree_mask")
+
+
+def _need_mask(tree, batch, mask, pos):
+    words = (tree.max_nodes + 31) // 32
+    _need(mask, torch.int32, "mask", numel=batch * tree.max_nodes * words)
+    _need(pos, torch.int32, "pos", numel=batch * tree.max_nodes)
+
+
+def _need_verify_io(tree, batch, V, draft, uniforms, target_lse, out, visited_lse):
+    if draft is not None:
+        _need(draft, name="draft", numel=batch * tree.L * V)
+        if draft.shape[-1] != V:
+            raise ValueError("draft rows must hold V = %d logits, got %d" % (V, draft.shape[-1]))
+    if uniforms is not None:
+        _need(uniforms, torch.float32, "uniforms", numel=batch * 2 * tree.max_nodes)
+    if target_lse is not None:
+        _need(target_lse, torch.float32, "target_lse", numel=batch * tree.max_nodes)
+    acc_nodes, acc_len, next_tok = out
+    _need(acc_nodes, torch.int32, "acc_nodes", numel=batch * (tree.L + 1))
+    _need(acc_len, torch.int32, "acc_len", numel=batch)
+    _need(next_tok, torch.int32, "next_tok", numel=batch)
+    if visited_lse is not None:
+        _need(visited_lse, torch.float32, "visited_lse", numel=batch * (tree.L + 1))
 
 
 def alloc_mask(tree, device="cuda"):
@@ -337,18 +412,14 @@ def verify(tree, target, temperature=0.0, draft=None, uniforms=None, out=None, v
     """Acceptance walk.  out = (acc_nodes [b, L+1], acc_len [b], next_tok [b]) int32 tensors;
     target_lse: optional [b, max_nodes] fp32 normalisers of the target rows (T=1);
     rule: None (greedy at temperature 0, "ratio" at 1) or one of VERIFY_RULES."""
-    _need(target, name="target")
     batch = batch or tree.batch
+    _need_batch(tree, batch)
     V = target.shape[-1]
+    _need(target, name="target", numel=batch * tree.max_nodes * V)
     if out is None:
         out = alloc_verify_out(tree)
     acc_nodes, acc_len, next_tok = out
-    if draft is not None:
-        _need(draft, name="draft")
-    if uniforms is not None:
-        _need(uniforms, torch.float32, "uniforms")
-    if target_lse is not None:
-        _need(target_lse, torch.float32, "target_lse")
+    _need_verify_io(tree, batch, V, draft, uniforms, target_lse, out, visited_lse)
     if rule is not None:
         _check(lib().dt_verify_rule(ctypes.byref(tree.struct()), batch, V, _dtype_code(target), _ptr(target),
                                     _ptr(target_lse), _ptr(draft), VERIFY_RULES[rule], _ptr(uniforms),
@@ -365,13 +436,16 @@ def verify_markov(p, tree, target, draft, znorm, uniforms, out=None, visited_lse
                   stream=None):
     """T=1 walk against the normalised DARTree proposal (dt_verify_markov); znorm [b, L, K] fp32,
     e.g. znorm_view(p, workspace) after markov_norm."""
-    _need(target, name="target")
-    _need(draft, name="draft")
-    _need(znorm, torch.float32, "znorm")
-    _need(uniforms, torch.float32, "uniforms")
+    _need_batch(tree, p.batch)
+    _need(target, name="target", numel=p.batch * tree.max_nodes * p.V)
+    _need_logits(draft, p, "draft")
+    _need(znorm, torch.float32, "znorm", numel=p.batch * p.L * p.K)
     if out is None:
         out = alloc_verify_out(tree)
     acc_nodes, acc_len, next_tok = out
+    _need_verify_io(tree, p.batch, p.V, None, uniforms, target_lse, out, visited_lse)
+    if uniforms is None:
+        raise ValueError("verify_markov needs uniforms")
     _check(lib().dt_verify_markov(ctypes.byref(p.struct()), ctypes.byref(tree.struct()), _ptr(target),
                                   _ptr(target_lse), _ptr(draft), _ptr(znorm), _ptr(uniforms), _ptr(acc_nodes),
                                   _ptr(acc_len), _ptr(next_tok), _ptr(visited_lse), _stream(stream)),
@@ -399,14 +473,17 @@ def saba_budget(tree, st, c_verify, c_fixed, B_min, B_max, budget, state, hidden
     """dt_saba_budget: per-request budgets [batch] int32 and state [batch, 4] fp32 (conf, degen, hist, a);
     hidden: optional [batch, L, Hd] fp32 drafter hidden states; prev_acc_len: last round's acc_len."""
     batch = batch or tree.batch
-    _need(budget, torch.int32, "budget")
-    _need(state, torch.float32, "state")
+    _need_batch(tree, batch)
+    _need(budget, torch.int32, "budget", numel=batch)
+    _need(state, torch.float32, "state", numel=batch * 4)
+    _need(st.ring, torch.int32, "ring", numel=batch * st.window)
+    _need(st.count, torch.int32, "count", numel=batch)
     Hd = 0
     if hidden is not None:
-        _need(hidden, torch.float32, "hidden")
         Hd = int(hidden.shape[-1])
+        _need(hidden, torch.float32, "hidden", numel=batch * tree.L * Hd)
     if prev_acc_len is not None:
-        _need(prev_acc_len, torch.int32, "prev_acc_len")
+        _need(prev_acc_len, torch.int32, "prev_acc_len", numel=batch)
     q = SabaStruct(st.window, float(c_verify), float(c_fixed), int(B_min), int(B_max))
     _check(lib().dt_saba_budget(ctypes.byref(q), ctypes.byref(tree.struct()), batch, _ptr(hidden), Hd,
                                 _ptr(prev_acc_len), _ptr(st.ring), _ptr(st.count), _ptr(state), _ptr(budget),

@@ -257,3 +257,17 @@ def test_verify_markov_rejects_invalid_arguments():
     assert call(params(R=62)) == -1            # not a multiple of 4
     assert call(params(vt=0x10004)) == -1      # Vt not 16-byte aligned
     assert call(params(K=5)) == -1             # tree lists of another length
+
+
+def test_binding_size_checks_reject_short_buffers_and_small_trees():
+    # the C ABI takes bare pointers: the binding compares sizes before any launch
+    import torch
+    dtree._need_numel(torch.zeros(12), 12, "x")
+    with pytest.raises(ValueError):
+        dtree._need_numel(torch.zeros(11), 12, "x")
+    t = _FakeTree(2, 4, 4, 9)
+    dtree._need_batch(t, 2)
+    with pytest.raises(ValueError):
+        dtree._need_batch(t, 3)
+    with pytest.raises(ValueError):
+        dtree._need(torch.zeros(4), name="cpu tensor")  # a host tensor never reaches a kernel
