@@ -129,6 +129,32 @@ MUTANTS = [
     ("saba_conf_without_exp", "conf += exp((double)top_lp[d]);", "conf += (double)top_lp[d];", [BUDGETS]),
     ("tree_check_skips_depth", "if (depth[n] != depth[p] + 1) return 0;", "", [PINS]),
     ("mask_bit_modulo_31", "row[a / 32] |= 1u << (a % 32);", "row[a / 32] |= 1u << (a % 31);", [PINS]),
+    # output assembly: ids, parent indices, ranks, emitted tokens
+    ("candidates_write_rank_not_id", "ids[r * Kc + k] = buf[k].id;", "ids[r * Kc + k] = k;", [PINS]),
+    ("ddtree_parent_off_by_one", "par = j + 1;", "par = j;", [PINS]),
+    ("talon_parent_in_build_order", "parent[i + 1] = x->parent < 0 ? 0 : out_of[x->parent];",
+     "parent[i + 1] = x->parent < 0 ? 0 : x->parent + 1;", [PINS]),
+    ("talon_score_drops_parent", "x->s = T[v].s + lp[(d - 1) * Kc + w];", "x->s = lp[(d - 1) * Kc + w];", [PINS]),
+    ("dartree_parent_supertree_index", "parent[i + 1] = out_of[x->parent];", "parent[i + 1] = x->parent;",
+     [PINS, NORM, BUDGETS]),
+    ("dartree_rank_of_first_position", "rank[i + 1] = x->r[x->d - 1];\n            score[i + 1] = x->s;\n        }\n"
+     "        *n_nodes = n + 1;", "rank[i + 1] = x->r[0];\n            score[i + 1] = x->s;\n        }\n"
+     "        *n_nodes = n + 1;", [PINS, NORM, BUDGETS]),
+    ("heap_parent_off_by_one", "        parent[n] = p;\n        depth[n] = x.d;\n        rank[n] = c;",
+     "        parent[n] = p > 0 ? p - 1 : p;\n        depth[n] = x.d;\n        rank[n] = c;", [HEAP]),
+    ("norm_root_token_on_every_row", "const int u = (d == 0) ? (i == 0 ? root_tok : -1) : id[(d - 1) * K + i];",
+     "const int u = (d == 0) ? root_tok : id[(d - 1) * K + i];", [NORM, HEAP]),
+    ("saba_range_excludes_the_top", "for (int B = B_min; B <= B_max; ++B) {", "for (int B = B_min; B < B_max; ++B) {",
+     [BUDGETS]),
+    ("positions_from_the_parent", "pos[n] = depth[n] + pos_offset;", "pos[n] = (n ? depth[parent[n]] : 0) + pos_offset;",
+     [PINS]),
+    ("greedy_emits_last_accepted_token", "*next_tok = a;", "*next_tok = n > 0 ? tok[n] : a;", [PINS]),
+    ("t1_no_fallback_to_p_below_children",
+     "(drow[v] - lsed));\n                w[v] = P > Q ? P - Q : 0;\n                S += w[v];\n            }\n"
+     "        }\n        if (S == 0) {",
+     "(drow[v] - lsed));\n                w[v] = P > Q ? P - Q : 0;\n                S += w[v];\n            }\n"
+     "        }\n        if (S == 0 && nk == 0) {",
+     [PINS]),
 ]
 
 

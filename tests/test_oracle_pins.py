@@ -646,3 +646,22 @@ def test_t1_edge_cases_r_zero_and_p_zero():
         _, alen, nxt, _ = oracle.verify_t1(t, np.stack([tgt, tgt]), lq, np.zeros(1, np.float32), u, 1, 2,
                                            lse_in=np.zeros(2, np.float32))
         assert alen == 0 and nxt == 0
+
+
+def test_t1_rejection_with_an_empty_residual_draws_from_p():
+    # A rejected child whose residual is empty: the replacement comes from p.
+    # Target and drafter rows are the same logits, but the drafter's supplied
+    # normaliser sits 0.001 below the true one, so every drafter mass is at
+    # least the target's (the residual [p - q]_+ is empty) while the child's
+    # ratio is exp(-0.001) ~ 0.999 < u.  Row: two equal masses, so a draw
+    # uniform of 1/2 lies at the start of the second token's interval.
+    V = 6
+    row = np.full(V, -30.0, np.float32)
+    row[[0, 4]] = 1.5
+    lse = np.float32(np.logaddexp.reduce(row.astype(np.float64)))
+    t = _chain_tree([0])
+    t.rank[1] = 0
+    u = np.array([[0.0, 0.9999], [0.5, 0.5]], np.float32)
+    acc, alen, nxt, _ = oracle.verify_t1(t, np.stack([row, row]), row[None, :], np.array([lse - 0.001], np.float32),
+                                         u, 1, 2)
+    assert alen == 0 and nxt == 4
