@@ -5,9 +5,14 @@
  * One speculative round on the pages: a block drafter scores all L future
  * positions in one pass; per position the library keeps the Top-K tokens and
  * their log-probabilities, selects a budget-B prefix tree (DDTree Top-B,
- * DARTree supertree + deferred Top-B, or TALON gating), builds the tree
- * attention mask and position ids, and, once the target model has scored every
- * tree node, walks the longest accepted path.  Sources (by page title):
+ * DARTree supertree + deferred Top-B with the Markov correction, plain or
+ * normalised over the vocabulary, DARTree's fixed per-depth widths, the
+ * best-first heap with Markov or TDES edge scores, or TALON gating; per-request
+ * budgets from the caller or from SABA), builds the tree attention mask and
+ * position ids, and, once the target model has scored every tree node, walks
+ * the longest accepted path (greedy, the T=1 ratio rule, one residual per
+ * rejected sibling, target-sample matching, or T=1 against the normalised
+ * DARTree proposal).  Sources (by page title):
  *   [DARTree] "DARTree: Speculative Diffusion Decoding With Autoregressive
  *             Draft Trees" -- "Speculative sampling", "Tree verification and
  *             DDTree", Algorithm 1, "Deferred best-first pruning", Lemma 1.
@@ -20,6 +25,9 @@
  *   [DDTree]  "DDTree algorithm: efficient inference-tree construction"
  *             (CSDN explainer) -- Prop 1, Prop 2, Lemma (S_K), Algorithm 1
  *             (heap over rank descriptors), section 4.2 (tree attention mask).
+ *   [GRAFT]   "GRAFT: adaptive DLM draft-tree construction with
+ *             target-distilled edge scoring" -- "Target-distilled edge
+ *             scoring", "Inference", "State-aware budget allocation".
  *
  * Conventions for every call:
  *  - All array pointers are DEVICE pointers owned by the caller; the library
