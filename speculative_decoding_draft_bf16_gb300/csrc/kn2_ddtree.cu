@@ -22,7 +22,8 @@
 // the first depth that adds nothing.  Work per depth is O((|C| + m) log) plus
 // the sorts (up to 512 keys: warp-register sorts of 32-key segments ranked
 // against each other by binary search, two block barriers); everything lives
-// in shared memory.
+// in shared memory.  A per-request budget (budget[b], clamped to [1, B], e.g.
+// from SABA) replaces B for that request; the buffers keep B's stride.
 #include "dt_device.cuh"
 #include "dt_launch.h"
 

@@ -19,6 +19,9 @@
 // shared node order by merging the per-depth sorted layers, and emits TopB(S)
 // when it is topologically ordered; otherwise (some edge raised the score) it
 // runs the best-first heap over S and sets DT_DEV_BESTFIRST.
+// DARTree (fixed) (wfix): depth d keeps B / L children, one more for each of the
+// first B mod L depths (the shallowest), instead of W; the widths sum to B, so
+// the final pruning keeps all of S.
 #include "dt_device.cuh"
 #include "dt_launch.h"
 

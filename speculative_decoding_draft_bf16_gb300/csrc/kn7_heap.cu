@@ -26,7 +26,8 @@
 // order row and score) lives in shared memory, cut into blocks of 32 slots
 // whose maxima the lanes keep in registers, so a pop is a warp max and one
 // ballot; ties on the score go to the smaller descriptor, found by walking
-// both parent chains.  The popped slot takes one of the pushes.
+// both parent chains.  The popped slot takes one of the pushes.  A per-request
+// budget (budget[b], clamped to [1, B]) bounds the pops of that request.
 //
 // TDES table (kn8): the projections depend only on the token, so the inputs
 // are the per-token first-layer rows Ap = W_p g_p(e), Ac = W_c g_c(e) and the
