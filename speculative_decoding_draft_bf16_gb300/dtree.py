@@ -75,6 +75,8 @@ def lib():
         L.dt_markov_norm.argtypes = [bp, _vp, tp, _vp, ctypes.c_size_t, _vp]
         L.dt_stage1_plan.restype = _i32
         L.dt_stage1_plan.argtypes = [bp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
+        L.dt_stage1_ceiling.restype = _i32
+        L.dt_stage1_ceiling.argtypes = [bp, _vp, _vp, _vp, _vp]
         L.dt_select.restype = _i32
         L.dt_select.argtypes = [bp, tp, _vp, ctypes.c_size_t, _vp]
         L.dt_build_tree.restype = _i32
@@ -307,6 +309,20 @@ def stage1_plan(p):
            "dt_stage1_plan")
     return ({DT_STAGE1_CLUSTER: "cluster", DT_STAGE1_ROWS: "rows"}[k.value], c.value)
 
+def stage1_ceiling(p, draft_logits, chunk_max, status=None, stream=None):
+    """The read floor of the cluster stage-1 launch (dt_stage1_ceiling): every
+    CTA's chunk maximum into chunk_max [batch * L, S] fp32, S from stage1_plan."""
+    kind, S = stage1_plan(p)
+    if kind != "cluster":
+        raise DtError("dt_stage1_ceiling: the stage-1 plan for these parameters is one CTA per row")
+    _need_logits(draft_logits, p)
+    _need(chunk_max, torch.float32, "chunk_max", numel=p.batch * p.L * S)
+    if status is not None:
+        _need(status, torch.int32, "status", numel=1)
+    _check(lib().dt_stage1_ceiling(ctypes.byref(p.struct()), _ptr(draft_logits), _ptr(chunk_max), _ptr(status),
+                                   _stream(stream)), "dt_stage1_ceiling")
+
+
 def markov_norm(p, draft_logits, tree, workspace, stream=None):
     """Full-vocabulary DARTree log-normalisers into the workspace (dt_markov_norm)."""
     _need_logits(draft_logits, p)
@@ -416,6 +432,9 @@ def verify(tree, target, temperature=0.0, draft=None, uniforms=None, out=None, v
     _need_batch(tree, batch)
     V = target.shape[-1]
     _need(target, name="target", numel=batch * tree.max_nodes * V)
+    if draft is not None and draft.dtype != target.dtype:
+        # the walk reads both row sets with the target's element type
+        raise TypeError("draft logits (%s) and target logits (%s) must share one dtype" % (draft.dtype, target.dtype))
     if out is None:
         out = alloc_verify_out(tree)
     acc_nodes, acc_len, next_tok = out
@@ -439,6 +458,9 @@ def verify_markov(p, tree, target, draft, znorm, uniforms, out=None, visited_lse
     _need_batch(tree, p.batch)
     _need(target, name="target", numel=p.batch * tree.max_nodes * p.V)
     _need_logits(draft, p, "draft")
+    if _dtype_code(target) != _dtype_code(draft):
+        # the walk reads the target rows with the parameter block's element type
+        raise TypeError("target logits must be %s for dtype=%r, got %s" % (draft.dtype, p.dtype, target.dtype))
     _need(znorm, torch.float32, "znorm", numel=p.batch * p.L * p.K)
     if out is None:
         out = alloc_verify_out(tree)

@@ -32,6 +32,18 @@ def test_short_or_mismatched_buffers_are_refused():
     with pytest.raises(ValueError):  # uniforms for one request
         dtree.verify(tree, torch.zeros((2, 9, 64), device="cuda"), temperature=1.0, draft=x,
                      uniforms=torch.zeros((1, 2, 9), device="cuda"))
+    with pytest.raises(TypeError):  # bf16 drafter rows beside fp32 target rows: one element type is read
+        dtree.verify(tree, torch.zeros((2, 9, 64), device="cuda"), temperature=1.0, draft=x,
+                     uniforms=torch.zeros((2, 2, 9), device="cuda"))
+    with pytest.raises(TypeError):  # the reverse: fp32 drafter rows beside bf16 target rows
+        dtree.verify(tree, torch.zeros((2, 9, 64), dtype=torch.bfloat16, device="cuda"), temperature=1.0,
+                     draft=x.float(), uniforms=torch.zeros((2, 2, 9), device="cuda"))
+    pm = dtree.Params(mode="dartree", batch=2, L=4, V=64, dtype="bf16", K=4, W=4, B=8, R=2,
+                      U=torch.zeros((64, 2), device="cuda"), Vt=torch.zeros((64, 2), device="cuda"),
+                      markov_norm=True)
+    with pytest.raises(TypeError):  # fp32 target rows for a bf16 parameter block (normalised DARTree walk)
+        dtree.verify_markov(pm, tree, torch.zeros((2, 9, 64), device="cuda"), x,
+                            torch.zeros((2, 4, 4), device="cuda"), torch.zeros((2, 2, 9), device="cuda"))
     mask, pos = dtree.alloc_mask(small)
     with pytest.raises(ValueError):  # a mask for one request
         dtree.select_mask(p, tree, mask, pos)
