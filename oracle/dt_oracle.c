@@ -44,7 +44,10 @@ enum { OR_OK = 0, OR_EINVAL = -1, OR_ENOMEM = -2, OR_EBADTREE = -5 };
 /* exact and a tail, then e^r by its Taylor series to degree 7 in Horner form, */
 /* then scaling by 2^k.  Every step is one correctly rounded fp32 operation,   */
 /* so any IEEE machine with a true fma produces the same bits.                 */
-/* Range: returns 0 for x < -86 (results below 2^-124) and +inf for x > 88.5.  */
+/* Range: returns 0 for x < -86 (results below 2^-124) and +inf for x > 88.5;  */
+/* every x <= 88.5 gives a finite value (e^88.5 < FLT_MAX).  Near the top k    */
+/* reaches 128, whose 2^k is not a float, so 2^k is applied as 2^127 * 2:      */
+/* both are exact scalings, so the product is rounded once, as for smaller k.  */
 /* Pinned: ulp error against double exp, monotonicity (tests).                 */
 /* ------------------------------------------------------------------------- */
 static float or_pow2i(int k) /* 2^k for -126 <= k <= 127, built from its bits */
@@ -75,6 +78,7 @@ float or_exp_canon(float x)
     p = fmaf(p, r, 0.5f);
     p = fmaf(p, r, 1.0f);
     p = fmaf(p, r, 1.0f);
+    if (k > 127) return (p * or_pow2i(127)) * 2.0f;
     return p * or_pow2i(k);
 }
 

@@ -39,6 +39,7 @@
 // residual draw computes each thread's run of masses once; the CTA holding the
 // draw scans the run sums, and one warp re-walks the single run that holds it.
 #include "dt_device.cuh"
+#include "dt_exp.cuh"
 #include "dt_launch.h"
 
 namespace {

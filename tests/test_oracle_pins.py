@@ -39,6 +39,19 @@ def test_exp_canon_ulp_error_and_monotone():
     assert np.isinf(oracle.exp_canon(np.array([89.0]))[0])
 
 
+def test_exp_canon_top_of_range_is_finite():
+    # e^x stays below FLT_MAX up to ln(FLT_MAX) = 88.72; the range the function
+    # states ends at 88.5.  Above 127.5 ln 2 = 88.376 the reduction picks k = 128,
+    # whose power of two is not a float, and the value must still be finite.
+    xs = np.array([88.3, 88.376, 88.38, 88.4, 88.45, 88.5], dtype=np.float32)
+    y = oracle.exp_canon(xs)
+    assert np.all(np.isfinite(y)), y
+    ref = np.exp(xs.astype(np.float64))
+    ulps = np.abs(y.astype(np.float64) - ref) / np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert ulps.max() <= 2.0, ulps
+    assert np.all(np.diff(y) > 0)
+
+
 # --------------------------------------------------------------------------
 # Stage 1: log-normaliser and Top-Kc list.
 # --------------------------------------------------------------------------
