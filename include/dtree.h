@@ -205,6 +205,21 @@ dt_status dt_candidates(const dt_build_params* p, const void* draft_logits,
 #define DT_STAGE1_ROWS 2
 dt_status dt_stage1_plan(const dt_build_params* p, int32_t* kernel, int32_t* cluster);
 
+/* Measurement kernel, not a step of the method: the read floor of the cluster
+ * stage-1 launch.  Reads draft_logits [batch][L][V] with exactly the launch
+ * dt_candidates uses when dt_stage1_plan answers DT_STAGE1_CLUSTER (the same
+ * clusters, chunks, shared memory and programmatic dependent launch) and does
+ * the least work that consumes every byte: each CTA writes its chunk's
+ * maximum to chunk_max[row][S] (S = *cluster of dt_stage1_plan; the row
+ * maximum is the maximum of a row's S entries).  Its device time is the floor
+ * that stage 1's own exchanges and passes add to.  status: NULL, or one int32
+ * that gets bit DT_DEV_TIMEOUT (OR-ed) when a staging wait ran out of its bound.
+ * Returns DT_ERR_UNSUPPORTED when the plan is DT_STAGE1_ROWS (there the
+ * measured HBM copy bandwidth is the floor), DT_ERR_INVALID_ARG as
+ * dt_stage1_plan or for a NULL pointer. */
+dt_status dt_stage1_ceiling(const dt_build_params* p, const void* draft_logits, float* chunk_max,
+                            int32_t* status, dt_stream_t stream);
+
 /* Stages 2-3: tree selection from the candidate lists already in `tree`
  * (written by dt_candidates, or by the caller), writing node_tok, parent,
  * depth, rank, score, n_nodes and a fresh status word per request.
@@ -414,17 +429,21 @@ dt_status dt_saba_budget(const dt_saba_params* q, const dt_tree* tree, int32_t b
  * banned because they can synchronise the device.
  * Same result as dt_select with p->mode == DT_MODE_DARTREE, but the Markov
  * table that dt_select keeps in the caller's workspace lives in a fixed array
- * inside the library (DT_NOALLOC_TABLE_BYTES, resident on every GPU that
- * loads the library until the process exits).  The caller still owns and
- * passes the tree buffers.  Nothing is allocated, by the library or by CUDA on
- * its behalf.
+ * inside the library (DT_NOALLOC_TABLE_BYTES).  CUDA reserves that array on a
+ * device when it loads the library's device code there -- under lazy module
+ * loading, at the first library call on that device -- and it stays reserved
+ * for the life of the device's context.  The caller still owns and passes the
+ * tree buffers.  A call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
  *   - Returns DT_ERR_UNSUPPORTED when batch * L * K * K * 4 exceeds
  *     DT_NOALLOC_TABLE_BYTES or p->markov_norm is set (its normaliser table
  *     needs caller workspace), DT_ERR_INVALID_ARG for a mode other than
  *     DT_MODE_DARTREE, and the usual errors otherwise.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  The lookup is repeated when the device's context has
+ *     changed since (after cudaDeviceReset, for instance); make the first call
+ *     after such a change outside stream capture as well.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; each call writes every entry it reads, so none needs clearing.
  *     Calls whose kernels overlap on the GPU (different streams, or

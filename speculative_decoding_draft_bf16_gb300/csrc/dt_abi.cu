@@ -249,6 +249,19 @@ dt_status dt_stage1_plan(const dt_build_params* p, int32_t* kernel, int32_t* clu
     return DT_OK;
 }
 
+dt_status dt_stage1_ceiling(const dt_build_params* p, const void* draft_logits, float* chunk_max, int32_t* status,
+                            dt_stream_t stream) {
+    int32_t kernel = 0, S = 0;
+    dt_status s = dt_stage1_plan(p, &kernel, &S);
+    if (s != DT_OK) return s;
+    if (!draft_logits || !chunk_max) return DT_ERR_INVALID_ARG;
+    if (kernel != DT_STAGE1_CLUSTER) return DT_ERR_UNSUPPORTED;
+    Stage1Plan plan;
+    if ((s = plan_stage1(p, &plan)) != DT_OK) return s;
+    return cuda_status(dt_kn0_launch(draft_logits, p->dtype, p->batch * p->L, p->V, kc_of(p), plan.S, plan.chunk,
+                                     chunk_max, status, (cudaStream_t)stream));
+}
+
 dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_tree* t, dt_stream_t stream) {
     dt_status s = check_build(p, t);
     if (s != DT_OK) return s;
@@ -517,8 +530,10 @@ int32_t dt_version(void) { return 100; }
 // latency-critical path where cudaMalloc/cudaFree are not allowed because they
 // can synchronise the device.  For them the DARTree Markov table lives in a
 // fixed file-scope device array instead of caller memory.  Limits: at most
-// DT_NOALLOC_TABLE_BYTES of table (batch * L * K * K floats); the array is
-// resident on every GPU that loads this library, for the life of the process.
+// DT_NOALLOC_TABLE_BYTES of table (batch * L * K * K floats); CUDA places the
+// array on a device when it loads this library's device code there (under
+// lazy module loading: at the first library call on that device), and it
+// stays there for the life of that device context.
 // ---------------------------------------------------------------------------
 
 namespace {
@@ -531,23 +546,55 @@ static __device__ __align__(256) float g_noalloc_table[kNoallocTableFloats];
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-float* g_noalloc_addr[kNoallocMaxDevices];  // device address of the array, per device
+struct NoallocSlot {
+    float* addr;               // device address of the array in that context
+    unsigned long long ctx;    // the context it was looked up in (0: unknown)
+};
+NoallocSlot g_noalloc_slot[kNoallocMaxDevices];
 
-// Device address of g_noalloc_table on the current device, looked up once per
-// device (with that device current) and cached.
+// The driver's cuCtxGetId, fetched through the runtime (no link against the
+// driver library); null when the driver does not offer it.
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+CtxGetIdFn ctx_get_id_fn() {
+    static CtxGetIdFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return (CtxGetIdFn)f;
+    }();
+    return fn;
+}
+
+// Id of the calling thread's current context; false if there is none yet.
+bool current_ctx_id(unsigned long long* id) {
+    CtxGetIdFn fn = ctx_get_id_fn();
+    return fn && fn(nullptr, id) == 0 && *id != 0;
+}
+
+// Device address of g_noalloc_table on the current device.  Looked up with
+// cudaGetSymbolAddress (which also makes the device's primary context current
+// on this thread) on the first call on a device and again whenever the
+// device's context has changed since (a cudaDeviceReset ends a context, and
+// the address of the array in the next one may differ); otherwise cached.
 dt_status noalloc_table(float** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_status(e);
     if (dev < 0 || dev >= kNoallocMaxDevices) return DT_ERR_UNSUPPORTED;
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_ctx_id(&ctx);
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    NoallocSlot& slot = g_noalloc_slot[dev];
+    if (!slot.addr || !have_ctx || slot.ctx != ctx) {
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_table);
         if (e != cudaSuccess || !ptr) return cuda_status(e == cudaSuccess ? cudaErrorInvalidSymbol : e);
-        g_noalloc_addr[dev] = (float*)ptr;
+        slot.addr = (float*)ptr;
+        slot.ctx = current_ctx_id(&ctx) ? ctx : 0;
     }
-    *out = g_noalloc_addr[dev];
+    *out = slot.addr;
     return DT_OK;
 }
 

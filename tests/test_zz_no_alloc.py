@@ -5,8 +5,12 @@ the whole device budget, or a latency-critical loop where cudaMalloc is not
 allowed because it can synchronise the device -- so they cannot pass the
 DARTree workspace.  The allocation-free entry point keeps that table in a fixed
 array inside the library instead.  Its trees must equal the workspace entry
-point's, bit for bit, on two calls in a row (the second call finds the first
-call's table contents in the shared array).  This file is collected last."""
+point's, bit for bit, on two calls in a row on one shape with different
+inputs: the second call finds the first call's table in the shared array at
+the same offsets.  With a root token a call also uses the depth-1 entries,
+without one it skips them, so both orders are run: a call with root tokens
+after one without (it must write what it reads), and the reverse (it must not
+read the stale depth-1 entries).  This file is collected last."""
 import ctypes
 
 import pytest
@@ -30,24 +34,31 @@ def _case(seed, batch, L, V, K, W, B, R, root):
     return x.cuda(), p, min(B, W * L) + 1
 
 
+def _check_one(seed, shape, root):
+    batch, L, V, K, W, B, R = shape
+    x, p, max_nodes = _case(seed, batch, L, V, K, W, B, R, root)
+    ref = dtree.TreeBuffers.for_params(p, max_nodes=max_nodes)
+    got = dtree.TreeBuffers.for_params(p, max_nodes=max_nodes)
+    dtree.candidates(p, x, ref)
+    for f in ("lse", "cand_id", "cand_lp"):
+        getattr(got, f).copy_(getattr(ref, f))
+    dtree.select(p, ref, workspace=dtree.make_workspace(p))
+    dtree.select_dartree_noalloc(p, got)
+    torch.cuda.synchronize()
+    for f in FIELDS:
+        assert torch.equal(getattr(ref, f), getattr(got, f)), (seed, root, f)
+    assert torch.equal(ref.score.view(torch.int32), got.score.view(torch.int32)), (seed, root)
+
+
 def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_lib):
-    cases = [
-        (11, 3, 6, 2000, 8, 6, 20, 16, True),       # small, with root tokens
-        (12, 8, 16, 151936, 16, 32, 512, 64, False),  # the batch-8 supertree workload shape
+    shapes = [
+        (3, 6, 2000, 8, 6, 20, 16),          # small
+        (8, 16, 151936, 16, 32, 512, 64),    # the batch-8 supertree workload shape
     ]
-    for seed, batch, L, V, K, W, B, R, root in cases:
-        x, p, max_nodes = _case(seed, batch, L, V, K, W, B, R, root)
-        ref = dtree.TreeBuffers.for_params(p, max_nodes=max_nodes)
-        got = dtree.TreeBuffers.for_params(p, max_nodes=max_nodes)
-        dtree.candidates(p, x, ref)
-        for f in ("lse", "cand_id", "cand_lp"):
-            getattr(got, f).copy_(getattr(ref, f))
-        dtree.select(p, ref, workspace=dtree.make_workspace(p))
-        dtree.select_dartree_noalloc(p, got)
-        torch.cuda.synchronize()
-        for f in FIELDS:
-            assert torch.equal(getattr(ref, f), getattr(got, f)), (seed, f)
-        assert torch.equal(ref.score.view(torch.int32), got.score.view(torch.int32)), seed
+    for i, shape in enumerate(shapes):
+        first_root = i % 2 == 0               # small: root tokens first; large: none first
+        _check_one(11 + 2 * i, shape, first_root)
+        _check_one(12 + 2 * i, shape, not first_root)
 
 
 def test_noalloc_rejects_tables_beyond_the_fixed_size(cuda_lib):
