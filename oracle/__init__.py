@@ -13,6 +13,7 @@ import os
 import numpy as np
 
 from . import build as _build
+from .endtoend import path_scores, selection_check  # noqa: F401  (end-to-end selection check)
 
 _LIB = None
 

@@ -219,7 +219,7 @@ def _has_equal_score_edges(t):
 
 def test_equal_parent_and_child_scores_keep_the_parent_first():
     x = _certain_second_position(2, 6, 3000, seed=41)
-    tree, p, want = talon_case(x, 40, 0.2, talon_k=4)
+    tree, p, want, _ = talon_case(x, 40, 0.2, talon_k=4)
     for b in range(2):
         g = gpu_tree(tree, b)
         assert _has_equal_score_edges(g) >= 1

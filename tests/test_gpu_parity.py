@@ -61,27 +61,35 @@ def assert_same_tree(g, o, what=""):
     assert np.array_equal(g.score[:n].view(np.uint32), o.score[:n].view(np.uint32)), what
 
 
-def near_tie_diff(g, o):
-    """Trees may differ only through selections whose scores lie within TOL of
-    the last selected score; returns the number of differing nodes."""
-    def paths(t):
-        out = {}
-        for n in range(1, t.n):
-            p, a = [], n
-            while a != 0:
-                p.append(int(t.tok[a]))
-                a = int(t.parent[a])
-            out[tuple(reversed(p))] = float(t.score[n])
-        return out
-    pg, po = paths(g), paths(o)
-    diff = set(pg) ^ set(po)
-    if not diff:
-        return 0
-    last = min(min(pg.values()), min(po.values()))
-    for d in diff:
-        s = pg.get(d, po.get(d))
-        assert abs(s - last) <= 10 * TOL, ("selection differs beyond a near-tie", d, s, last)
-    return len(diff)
+# End to end, the GPU's own stage-1 tables carry the oracle's ids and log-probs
+# within TOL, and every tree score is a path sum of them: a selection may differ
+# from the oracle's only by near-ties, within the per-node tolerance
+# oracle.selection_check derives from TOL (it grows with depth, up to about
+# 1.6e-4 plus rounding at depth 16).  Each end-to-end case states how many
+# near-tie nodes it accepts per request: one exchange across a cut is two
+# nodes (one kept by each side).  Spiky rows have scores far apart, and
+# allow one exchange; rows with massive ties allow more (stated per case).
+NEAR_TIES_PER_REQUEST = 2
+NEAR_TIE_TALLY = {"requests": 0, "near_ties": 0, "consequences": 0, "order_swaps": 0, "score_err_max": 0.0}
+
+
+def check_end_to_end(g, o, lps, mode, max_near_ties=NEAR_TIES_PER_REQUEST, what="", **kw):
+    """GPU tree g (from its own stage 1) against the oracle tree o (from the
+    oracle's table lps): every difference a near-tie, the count within
+    max_near_ties, every GPU score within its tolerance of the oracle's
+    arithmetic on the same path."""
+    rep = oracle.selection_check(g, o, lps, mode, eps_lp=TOL, got_scores=g.score, **kw)
+    assert rep["mismatches"] == [], ("selection differs beyond a near-tie", what, rep["mismatches"][:3])
+    assert rep["order_mismatches"] == 0, ("node order differs beyond a near-tie", what)
+    assert rep["score_err_viol"] == 0, ("a score beyond its tolerance", what, rep["score_err_max"])
+    assert rep["near_ties"] <= max_near_ties, ("more near-ties than the case allows", what, rep["near_ties"])
+    NEAR_TIE_TALLY["requests"] += 1
+    for k in ("near_ties", "consequences", "order_swaps"):
+        NEAR_TIE_TALLY[k] += rep[k]
+    NEAR_TIE_TALLY["score_err_max"] = max(NEAR_TIE_TALLY["score_err_max"], rep["score_err_max"])
+    print("end to end %s: near-ties %d, consequences %d, order swaps %d, max score error %.2e (tolerance up to %.2e)"
+          % (what, rep["near_ties"], rep["consequences"], rep["order_swaps"], rep["score_err_max"], rep["tau_max"]))
+    return rep
 
 
 def oracle_tables(x_b, Kc):
@@ -151,6 +159,23 @@ def test_candidates_parity(batch, L, V, dtype, Kc, scale, p_spike):
     want = (np.take_along_axis(xs, g_ids, 1) - g_lse[:, None]).astype(np.float32)
     assert np.array_equal(g_lp.view(np.uint32), want.view(np.uint32))
     assert int(tree.status.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("batch,L,V,dtype,Kc", [(1, 16, 151936, "bf16", 256), (2, 3, 1001, "bf16", 64),
+                                                 (1, 2, 5000, "f32", 100)])
+def test_stage1_ceiling_reads_every_element(batch, L, V, dtype, Kc):
+    # the measurement kernel with the cluster stage-1 launch: the maximum of each
+    # row's chunk maxima is the row maximum (every element was read)
+    x = gen_logits(batch, L, V, dtype, 3.0, 0.7, seed=V).cuda()
+    p = dtree.Params(mode="ddtree", batch=batch, L=L, V=V, dtype=dtype, K=Kc, B=Kc)
+    kind, S = dtree.stage1_plan(p)
+    assert kind == "cluster"
+    out = torch.full((batch * L, S), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dtree.stage1_ceiling(p, x, out, st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+    assert torch.equal(out.max(dim=1).values, x.float().reshape(batch * L, V).max(dim=1).values)
 
 
 def test_candidates_edge_rows():
@@ -238,27 +263,32 @@ def ddtree_case(batch, L, V, dtype, K, B, scale, p_spike, seed):
     x = gen_logits(batch, L, V, dtype, scale, p_spike, seed=seed)
     p = dtree.Params(mode="ddtree", batch=batch, L=L, V=V, dtype=dtype, K=K, B=B)
     tree = dtree.TreeBuffers.for_params(p)
-    otrees = []
+    otrees, tables = [], []
     for b in range(batch):
         l32, ids, lps = oracle_tables(x[b], K)
         upload_tables(tree, b, l32, ids, lps)
         otrees.append(oracle.ddtree(lps, ids, B).trimmed())
+        tables.append(lps)
     dtree.select(p, tree)
     torch.cuda.synchronize()
     for b in range(batch):
         assert_same_tree(gpu_tree(tree, b), otrees[b], "b=%d" % b)
-    return tree, otrees, x, p
+    return tree, otrees, x, p, tables
 
 
 @pytest.mark.parametrize("batch,L,V,dtype,K,B,scale,p_spike", DD_CASES)
 def test_ddtree_parity(batch, L, V, dtype, K, B, scale, p_spike):
-    _, otrees, x, p = ddtree_case(batch, L, V, dtype, K, B, scale, p_spike, seed=K * 7 + B)
+    _, otrees, x, p, tables = ddtree_case(batch, L, V, dtype, K, B, scale, p_spike, seed=K * 7 + B)
     # end to end: the GPU alone from raw logits
     tree = dtree.TreeBuffers.for_params(p)
     dtree.build_tree(p, x.cuda(), tree)
     torch.cuda.synchronize()
-    ties = sum(near_tie_diff(gpu_tree(tree, b), otrees[b]) for b in range(batch))
-    print("near-tie differences end to end:", ties)
+    # flat rows (scale <= 1) pack many exactly tied scores at the cut, whose
+    # order a rounding difference can flip: up to B/16 near-tie nodes there
+    allow = NEAR_TIES_PER_REQUEST if scale > 1.0 else max(NEAR_TIES_PER_REQUEST, B // 16)
+    for b in range(batch):
+        check_end_to_end(gpu_tree(tree, b), otrees[b], tables[b], "ddtree", allow, "ddtree %s b=%d" % (
+            (batch, L, V, dtype, K, B, scale), b))
 
 
 def test_ddtree_single_request_full_size_all_budgets():
@@ -276,7 +306,7 @@ def test_ddtree_single_request_full_size_all_budgets():
         tree2 = dtree.TreeBuffers.for_params(p)
         dtree.build_tree(p, x.cuda(), tree2)
         torch.cuda.synchronize()
-        near_tie_diff(gpu_tree(tree2, 0), o)
+        check_end_to_end(gpu_tree(tree2, 0), o, lps, "ddtree", what="single request B=%d" % B)
 
 
 # ---------------------------------------------------------------------------
@@ -316,7 +346,7 @@ def test_mask_hand_drawn_depth3_on_gpu():
 @pytest.mark.parametrize("case", [1, 3, 7, 8])
 def test_mask_parity_on_oracle_trees(case):
     batch, L, V, dtype, K, B, scale, p_spike = DD_CASES[case]
-    tree, otrees, _, _ = ddtree_case(batch, L, V, dtype, K, B, scale, p_spike, seed=11)
+    tree, otrees, _, _, _ = ddtree_case(batch, L, V, dtype, K, B, scale, p_spike, seed=11)
     t2 = dtree.TreeBuffers(batch, L, K, B + 1)
     for b in range(batch):
         upload_tree(t2, b, otrees[b])
@@ -550,7 +580,9 @@ def test_dartree_full_size(beta):
     for b in (0, 5):
         _, ids, lps = oracle_tables(x[b], wl.K)
         ot, _, _ = oracle.dartree(lps, ids, U.numpy(), Vt.numpy(), -1, wl.W, beta, wl.B, Mmax=tree.max_nodes)
-        near_tie_diff(gpu_tree(t2, b), ot.trimmed())
+        E = oracle.markov_table(ids, U.numpy(), Vt.numpy(), -1)
+        check_end_to_end(gpu_tree(t2, b), ot.trimmed(), lps, "dartree", E=E, beta=beta,
+                         what="dartree beta=%g b=%d" % (beta, b))
 
 
 # ---------------------------------------------------------------------------
@@ -563,17 +595,18 @@ def talon_case(x, N, mu, talon_k=10, sample=None):
     tree = dtree.TreeBuffers.for_params(p)
     dtree.candidates(p, x.cuda(), tree)
     sample = list(range(batch)) if sample is None else sample
-    want = {}
+    want, tables = {}, {}
     log_mu = p.struct().log_mu
     for b in sample:
         l32, ids, lps = oracle_tables(x[b], p.Kc)
         upload_tables(tree, b, l32, ids, lps)
         want[b] = oracle.talon(lps, ids, p.talon_k, log_mu, N).trimmed()
+        tables[b] = lps
     dtree.select(p, tree)
     torch.cuda.synchronize()
     for b in sample:
         assert_same_tree(gpu_tree(tree, b), want[b], "talon b=%d" % b)
-    return tree, p, want
+    return tree, p, want, tables
 
 
 @pytest.mark.parametrize("N,mu,scale", [(7, 0.25, 3.0), (60, 0.03, 3.0), (200, 0.01, 0.5), (1024, 0.03, 0.7),
@@ -597,7 +630,7 @@ def test_talon_full_size(N):
     wl = wk.talon_gated(N)
     x, spikes = wk.draft_logits(wl)
     sample = [0, 17, 40, 63]
-    tree, p, want = talon_case(x, N, 0.03, sample=sample)
+    tree, p, want, tables = talon_case(x, N, 0.03, sample=sample)
     # mask of the sampled oracle trees through the GPU, and greedy verify
     t2 = dtree.TreeBuffers(len(sample), wl.L, wl.Kc, wl.max_nodes)
     for i, b in enumerate(sample):
@@ -621,8 +654,9 @@ def test_talon_full_size(N):
     t3 = dtree.TreeBuffers.for_params(p)
     dtree.build_tree(p, x.cuda(), t3)
     torch.cuda.synchronize()
+    log_mu = p.struct().log_mu
     for b in sample:
-        near_tie_diff(gpu_tree(t3, b), want[b])
+        check_end_to_end(gpu_tree(t3, b), want[b], tables[b], "talon", log_mu=log_mu, what="talon N=%d b=%d" % (N, b))
 
 
 # ---------------------------------------------------------------------------
@@ -677,7 +711,14 @@ def test_fused_mask_single_request_against_oracle():
     dtree.build_tree_mask(p, x.cuda(), t, m, pp, pos_offset=5)
     torch.cuda.synchronize()
     g = gpu_tree(t, 0)
-    if near_tie_diff(g, ot.trimmed()) == 0 and np.array_equal(g.parent[:g.n], ot.trimmed().parent[:g.n]):
-        n = g.n
+    n = g.n
+    # the mask of the GPU's own tree, always (the oracle's mask builder on the GPU's parents and depths)
+    rc, gmask, gpos = oracle.tree_mask(g, 257, 16, pos_offset=5)
+    assert rc == 0
+    assert np.array_equal(m[0, :n].cpu().numpy().view(np.uint32), gmask[:n])
+    assert np.array_equal(pp[0, :n].cpu().numpy(), gpos[:n])
+    # and the tree against the oracle's: near-ties only; where the two agree node for node, the masks too
+    check_end_to_end(g, ot.trimmed(), lps, "ddtree", what="fused mask single request")
+    if g.n == ot.n and np.array_equal(g.tok, ot.tok[:n]) and np.array_equal(g.parent, ot.parent[:n]):
         assert np.array_equal(m[0, :n].cpu().numpy().view(np.uint32), omask[:n])
         assert np.array_equal(pp[0, :n].cpu().numpy(), opos[:n])
