@@ -36,27 +36,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "draft trees built+verified/sec and logit-read HBM GB/s (% of GB300 peak) at V=151936"
 L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the stage-1
 # kernel, keyed by (kernel, workload, sha1 of the kernel's sources -- code only,
 # comments and whitespace dropped -- when the capture was taken); a changed
 # kernel reports null until it is captured again.
 KN1_TRAFFIC = {
-    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', 'b98ce52d59fa86e838199b13597ff315854b0179'): 4933376,
-    ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', 'b98ce52d59fa86e838199b13597ff315854b0179'): 4932267,
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38965589,
-    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78574336,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', '941c75344dafb22507da4ed1256971f75afc3e9e'): 314991445,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', '941c75344dafb22507da4ed1256971f75afc3e9e'): 342579712,
-    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962176,
-    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,
-    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78574336,  # same drafter logits and launch as ddtree_t1_b16_L16_V151936_K256_B256
-    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta0', '941c75344dafb22507da4ed1256971f75afc3e9e'): 38962432,  # same drafter logits and launch as heap_markov_b8_L16_V151936_K16_B512
-    ('kn1b_kernel', 'ddtree_saba_b16_L16_V151936_K256_Bmax256', '941c75344dafb22507da4ed1256971f75afc3e9e'): 78566571,
 }
 STAGE1_SOURCES = {
     "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),
@@ -154,6 +140,19 @@ def normaliser_roofline(wl, stage_us, peaks):
         "note": "one exp per (row, token) in the epilogue: %.0f M per launch" % (rows * wl.V / 1e6)}}
 
 
+def ceiling_fields(stage_us, draft_bytes, achieved, peak):
+    """The read floor of the same launch (cluster stage 1 only): the same bytes
+    read by a kernel with stage 1's grid, chunks, shared memory and launch mode
+    that does nothing but take each chunk's maximum."""
+    if "stage1_ceiling" not in stage_us:
+        return {"ceiling": None}
+    us = stage_us["stage1_ceiling"]
+    gbs = draft_bytes / (us * 1e-6) / 1e9
+    return {"ceiling": {"kernel": "kn0_kernel (stage 1's cluster launch; bulk copy + chunk max only)",
+                        "us": us, "gbs": gbs, "frac_of_peak": gbs / peak},
+            "frac_of_ceiling": achieved / gbs}
+
+
 def params_for(wl, U=None, Vt=None, tdes=None, budgets=None):
     from speculative_decoding_draft_bf16_gb300 import dtree
     td = None
@@ -246,6 +245,7 @@ def run_ours(args, wl, rank, world, local):
                     budget=torch.full((wl.batch,), wl.B, dtype=torch.int32, device=dev),
                     state=torch.zeros((wl.batch, 4), device=dev))
     p = params_for(wl, U, Vt, tdes, saba["budget"] if saba else None)
+    plan_kind, plan_cluster = dtree.stage1_plan(p)
     Mmax = max_nodes_of(wl)
     esize = 2 if wl.dtype == "bf16" else 4
     draft_bytes = wl.batch * wl.L * wl.V * esize
@@ -269,7 +269,8 @@ def run_ours(args, wl, rank, world, local):
         uni = wk.uniforms(wl, device=dev, first_req=first) if temperature == 1.0 else None
         mask, pos = dtree.alloc_mask(tree, device=dev)
         out = dtree.alloc_verify_out(tree, device=dev)
-        copies.append(dict(x=x, tree=tree, ws=ws, tgt=tgt, uni=uni, mask=mask, pos=pos, out=out))
+        cmax = (torch.empty((wl.batch * wl.L, plan_cluster), device=dev) if plan_kind == "cluster" else None)
+        copies.append(dict(x=x, tree=tree, ws=ws, tgt=tgt, uni=uni, mask=mask, pos=pos, out=out, cmax=cmax))
 
     markov_t1 = wl.mode == "dartree" and wl.markov_norm and temperature == 1.0
 
@@ -284,6 +285,8 @@ def run_ours(args, wl, rank, world, local):
             dtree.build_tree(p, c["x"], c["tree"], workspace=c["ws"])
         if "cand" in stages:
             dtree.candidates(p, c["x"], c["tree"])
+        if "ceil" in stages:  # the read floor of the cluster stage-1 launch
+            dtree.stage1_ceiling(p, c["x"], c["cmax"])
         if "norm" in stages:
             dtree.markov_norm(p, c["x"], c["tree"], c["ws"])
         if "select" in stages:
@@ -369,6 +372,8 @@ def run_ours(args, wl, rank, world, local):
         stage_list.insert(1, ("normalise", ("norm",)))
     if saba is not None:
         stage_list.insert(1, ("saba", ("saba",)))
+    if plan_kind == "cluster":
+        stage_list.insert(1, ("stage1_ceiling", ("ceil",)))
     for name, stages in stage_list:
         n = max(R, (args.steps // R) * R)
         stage_us[name] = timed(stages, n, R) * 1000.0 / n
@@ -432,7 +437,6 @@ def run_ours(args, wl, rank, world, local):
     peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_source = ("measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks
                    else "fallback (6.8 TB/s, an earlier GB300 copy measurement; no MEASURED_PEAKS.json value)")
-    plan_kind, plan_cluster = dtree.stage1_plan(p)
     kn1_name = "kn1_kernel" if plan_kind == "cluster" else "kn1b_kernel"
     kn1_desc = ("%s (log-softmax + Top-K, a cluster of %d CTAs per row)" % (kn1_name, plan_cluster)
                 if plan_kind == "cluster" else "%s (log-softmax + Top-K, one CTA per row)" % kn1_name)
@@ -460,7 +464,9 @@ def run_ours(args, wl, rank, world, local):
                    "l2": "rotating %d input copies (drafter logits %.0f MB > 2x L2)" % (R, R * draft_bytes / 1e6)},
         "roofline": {"bound": "hbm", "kernel": kn1_desc, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_source,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": draft_bytes},
+                     "peak_nominal": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": draft_bytes,
+                     **ceiling_fields(stage_us, draft_bytes, achieved, peak)},
         "stages_us": stage_us,
         **(normaliser_roofline(wl, stage_us, peaks) if wl.markov_norm else {}),
         "gpu_launches": launches_per_step * args.steps,
@@ -476,12 +482,16 @@ def run_ours(args, wl, rank, world, local):
 # ---------------------------------------------------------------------------
 def oracle_round(wl, x, tgt, uni, M):
     """One tree through the oracle: stage 1, selection, mask, walk.  M: the
-    edge-term weights (U, Vt: Markov; tdes: TDES) as host arrays."""
+    edge-term weights (U, Vt: Markov; tdes: TDES) as host arrays.  Returns a
+    dict: tree, lps (the stage-1 table), check (selection_check arguments for
+    this mode), walk ((acc_nodes, acc_len, next_tok), or None without targets)."""
     import numpy as np
     import oracle
     _, l32, ids, lps = oracle.candidates(x, wl.Kc)
     Mmax = max_nodes_of(wl)
     U, Vt = M["U"], M["Vt"]
+    check = {"mode": wl.mode}
+    z = None
     if wl.mode == "ddtree":
         B = wl.B
         if wl.saba_cv > 0:  # SABA budget from this tree's state (no history yet)
@@ -492,8 +502,10 @@ def oracle_round(wl, x, tgt, uni, M):
         widths = oracle.uniform_widths(wl.B, wl.L) if wl.budget_policy == "uniform" else None
         W = int(widths.max()) if widths is not None else wl.W
         t, _, _ = oracle.dartree(lps, ids, U, Vt, -1, W, wl.beta, wl.B, Mmax=Mmax, znorm=z, widths=widths)
+        if U is not None:
+            check.update(E=oracle.markov_table(ids, U, Vt, -1), znorm=z, beta=wl.beta)
     elif wl.mode == "heap":
-        z = E = None
+        E = None
         if M["tdes"] is not None:
             Ap, Ac, Dd, w, b0, s = M["tdes"]
             E = oracle.tdes_table(ids, Ap, Ac, Dd, w, b0, s, -1)
@@ -501,18 +513,20 @@ def oracle_round(wl, x, tgt, uni, M):
             E = oracle.markov_table(ids, U, Vt, -1)
             z = oracle.markov_norm(x, ids, U, Vt, -1) if wl.markov_norm else None
         t = oracle.heap_select(lps, ids, wl.B, E=E, znorm=z, Mmax=Mmax)
+        check.update(E=E, znorm=z)
     else:
         t = oracle.talon(lps, ids, wl.talon_k, wl.log_mu, wl.N, Mmax=Mmax)
+        check.update(log_mu=wl.log_mu)
     oracle.tree_mask(t, Mmax, wl.L)
-    if tgt is None:
-        return t
-    if wl.temperature == 1.0 and wl.mode == "dartree" and wl.markov_norm:
-        oracle.verify_t1_markov(t, tgt, x, l32, U, Vt, -1, z, uni, wl.L, Mmax)
-    elif wl.temperature == 1.0:
-        oracle.verify_t1(t, tgt, x, l32, uni, wl.L, Mmax, rule=wl.verify_rule or "ratio")
-    else:
-        oracle.verify_greedy(t, tgt, wl.L)
-    return t
+    walk = None
+    if tgt is not None:
+        if wl.temperature == 1.0 and wl.mode == "dartree" and wl.markov_norm:
+            walk = oracle.verify_t1_markov(t, tgt, x, l32, U, Vt, -1, z, uni, wl.L, Mmax)[:3]
+        elif wl.temperature == 1.0:
+            walk = oracle.verify_t1(t, tgt, x, l32, uni, wl.L, Mmax, rule=wl.verify_rule or "ratio")[:3]
+        else:
+            walk = oracle.verify_greedy(t, tgt, wl.L)
+    return {"tree": t, "lps": lps, "check": check, "walk": walk}
 
 
 def oracle_inputs(wl, n_trees, seed_base=10_000):
@@ -530,7 +544,7 @@ def oracle_inputs(wl, n_trees, seed_base=10_000):
     for i in range(n_trees):
         x, spikes = wk.draft_logits(one, first_req=seed_base + i)
         xf = x[0].float().numpy()
-        t = oracle_round(wl, xf, None, None, M)
+        t = oracle_round(wl, xf, None, None, M)["tree"]
         Mmax = max_nodes_of(wl)
         depth = np.zeros((1, Mmax), np.int32)
         depth[0, :t.n] = t.depth[:t.n]
@@ -541,27 +555,100 @@ def oracle_inputs(wl, n_trees, seed_base=10_000):
 
 
 def time_oracle(wl, items, M, threads):
+    """Seconds for the oracle rounds of `items` on `threads` host threads, and their results."""
     t0 = time.perf_counter()
     with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(lambda it: oracle_round(wl, it[0], it[1], it[2], M), items))
-    return time.perf_counter() - t0
+        res = list(ex.map(lambda it: oracle_round(wl, it[0], it[1], it[2], M), items))
+    return time.perf_counter() - t0, res
+
+
+# Tolerance of the normaliser table of the normalised DARTree correction,
+# added to the per-log-prob 1e-5 for the edge terms that subtract it.
+ZNORM_TOL = 1e-5
+
+
+def parity_sample(wl, items, results, n_max=16):
+    """The GPU's trees and walks against the oracle's on the first n_max
+    requests of the CPU sample (untimed): every selection difference must be a
+    near-tie (oracle.selection_check, the per-log-prob tolerance 1e-5 summed
+    along each path); the count is reported.  Walks are compared on requests
+    whose trees agree node for node.  SABA budgets depend on each request's
+    history, which the sample does not carry: not compared."""
+    import numpy as np
+    import torch
+    import oracle
+    from speculative_decoding_draft_bf16_gb300 import dtree
+    from speculative_decoding_draft_bf16_gb300 import workloads as wk
+    if wl.saba_cv > 0:
+        return {"compared": 0, "reason": "SABA budgets depend on per-request history"}
+    dev = torch.device("cuda", torch.cuda.current_device())
+    one = wl.with_(batch=1)
+    U = Vt = tdes = None
+    if wl.R > 0 and wl.mode in ("dartree", "heap"):
+        U, Vt = wk.markov_tables(wl.V, wl.R, device=dev)
+    if wl.H > 0:
+        tdes = wk.tdes_weights(wl.V, wl.L, wl.H, device=dev)
+    p = params_for(one, U, Vt, tdes)
+    tot = {"requests": 0, "near_ties": 0, "consequences": 0, "order_swaps": 0, "mismatches": 0,
+           "order_mismatches": 0, "score_err_viol": 0, "score_err_max": 0.0, "tolerance_max": 0.0,
+           "walks_compared": 0, "walk_mismatches": 0}
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    Mmax = max_nodes_of(wl)
+    for (xf, tgt, uni), res in list(zip(items, results))[:n_max]:
+        x = torch.from_numpy(xf).to(dt).reshape(1, wl.L, wl.V).to(dev)
+        tree = dtree.TreeBuffers(1, wl.L, p.Kc, Mmax, device=dev)
+        ws = dtree.make_workspace(p, device=dev)
+        dtree.build_tree(p, x, tree, workspace=ws)
+        t_dev = torch.from_numpy(tgt).to(dt).reshape(1, Mmax, wl.V).to(dev)
+        u_dev = torch.from_numpy(uni).reshape(1, 2, Mmax).to(dev) if uni is not None else None
+        if wl.temperature == 1.0 and wl.mode == "dartree" and wl.markov_norm:
+            out = dtree.verify_markov(p, tree, t_dev, x, dtree.znorm_view(p, ws), u_dev)
+        else:
+            out = dtree.verify(tree, t_dev, temperature=wl.temperature,
+                               draft=x if wl.temperature and wl.verify_rule != "target_match" else None,
+                               uniforms=u_dev, rule=wl.verify_rule or None)
+        torch.cuda.synchronize()
+        n = int(tree.n_nodes[0])
+        g = oracle.Tree(*(getattr(tree, f)[0].cpu().numpy()[:n].copy() for f in
+                          ("node_tok", "parent", "depth", "rank", "score")), n)
+        kw = dict(res["check"])
+        mode = kw.pop("mode")
+        eps_z = ZNORM_TOL if kw.get("znorm") is not None else 0.0
+        rep = oracle.selection_check(g, res["tree"].trimmed(), res["lps"], mode, eps_z=eps_z, got_scores=g.score,
+                                     **kw)
+        tot["requests"] += 1
+        for k in ("near_ties", "consequences", "order_swaps", "order_mismatches", "score_err_viol"):
+            tot[k] += rep[k]
+        tot["mismatches"] += len(rep["mismatches"])
+        tot["score_err_max"] = max(tot["score_err_max"], rep["score_err_max"])
+        tot["tolerance_max"] = max(tot["tolerance_max"], rep["tau_max"])
+        o = res["tree"]
+        if g.n == o.n and np.array_equal(g.tok, o.tok[:n]) and np.array_equal(g.parent, o.parent[:n]):
+            acc, alen, nxt = res["walk"]
+            tot["walks_compared"] += 1
+            same = (out[0][0].cpu().tolist() == list(acc) and int(out[1][0]) == alen and int(out[2][0]) == nxt)
+            tot["walk_mismatches"] += 0 if same else 1
+    return tot
 
 
 def cpu_baseline(wl, cpu_seconds=20.0):
     """The oracle on the host cores, one tree per thread, on a sample sized to
-    about `cpu_seconds` of CPU work (one tree is timed first to size it)."""
+    about `cpu_seconds` of CPU work (one tree is timed first to size it); then
+    the GPU's trees on the first requests of the same sample against the
+    oracle's (untimed)."""
     from oracle import build as ob
     ob.build()
     cores = os.cpu_count() or 1
     probe, M = oracle_inputs(wl, 1, seed_base=20_000)
-    t1 = time_oracle(wl, probe, M, 1)
+    t1, _ = time_oracle(wl, probe, M, 1)
     trees = int(max(cores, min(4 * cores, cpu_seconds / max(t1, 1e-3))))
     items, M = oracle_inputs(wl, trees)
-    sec = time_oracle(wl, items, M, cores)
-    return {"value": trees / sec, "unit": "trees/s", "cores": cores, "kind": "oracle",
+    sec, results = time_oracle(wl, items, M, cores)
+    base = {"value": trees / sec, "unit": "trees/s", "cores": cores, "kind": "oracle",
             "sample": "%d single-request trees of the %s workload (stage 1, selection, mask, walk; "
                       "%.2f s per tree on one core), one thread per tree over %d host cores"
                       % (trees, wl.name, t1, cores)}
+    return base, parity_sample(wl, items, results)
 
 
 def run_reference(args, wl, rank, world, budget_s=150.0, warm_budget_s=30.0):
@@ -577,14 +664,14 @@ def run_reference(args, wl, rank, world, budget_s=150.0, warm_budget_s=30.0):
     cores = os.cpu_count() or 1
     per_step = cores
     items, M = oracle_inputs(wl, per_step)
-    warm = time_oracle(wl, items, M, cores)  # the first untimed warm-up step, which also sizes the rest
+    warm, _ = time_oracle(wl, items, M, cores)  # the first untimed warm-up step, which also sizes the rest
     warmup = max(1, min(args.warmup, max(3, int(warm_budget_s / max(warm, 1e-3)))))
     for _ in range(warmup - 1):
         time_oracle(wl, items, M, cores)
     steps = max(1, min(args.steps, int(budget_s / max(warm, 1e-3))))
     total = 0.0
     for _ in range(steps):
-        total += time_oracle(wl, items, M, cores)
+        total += time_oracle(wl, items, M, cores)[0]
     value = steps * per_step / total
     sample = "%d single-request trees per step (one per host core), %d of %d requested steps timed after %d " \
              "of %d requested warm-up steps" % (per_step, steps, args.steps, warmup, args.warmup)
@@ -619,7 +706,11 @@ def main():
     del copies
     if rank == 0:
         if not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(wl)
+            result["cpu_baseline"], par = cpu_baseline(wl)
+            result["parity_sample"] = par
+            result["near_ties"] = par.get("near_ties")
+            result["mismatches"] = (par["mismatches"] + par["order_mismatches"] + par["score_err_viol"] +
+                                    par["walk_mismatches"]) if par.get("requests") else None
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.barrier()

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libdtree.so")
 
-SOURCES = ["dt_abi.cu", "kn1_candidates.cu", "kn1b_rows.cu", "kn2_ddtree.cu", "kn3_dartree.cu", "kn3n_norm.cu", "kn4_talon.cu",
+SOURCES = ["dt_abi.cu", "kn0_ceiling.cu", "kn1_candidates.cu", "kn1b_rows.cu", "kn2_ddtree.cu", "kn3_dartree.cu", "kn3n_norm.cu", "kn4_talon.cu",
            "kn5_mask.cu", "kn6_verify.cu", "kn7_heap.cu",
            "kn9_saba.cu"]
 

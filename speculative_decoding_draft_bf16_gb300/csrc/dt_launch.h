@@ -64,6 +64,11 @@ size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize);
 cudaError_t dt_kn1_launch(const void* logits, int dtype, int rows, int grid_rows, int V, int Kc, int S, int chunk,
                           float* lse, int32_t* cand_id, float* cand_lp, cudaStream_t st);
 
+// The read floor of the cluster stage-1 launch (kn0_ceiling.cu): the same
+// grid, chunks and shared memory, each CTA's chunk maximum to out[row][S].
+cudaError_t dt_kn0_launch(const void* logits, int dtype, int rows, int V, int Kc, int S, int chunk, float* out,
+                          int32_t* timed_out, cudaStream_t st);
+
 // Stage 1 for many rows, one CTA per row (kn1b_rows.cu).
 size_t dt_kn1b_smem_bytes();
 cudaError_t dt_kn1b_launch(const void* logits, int dtype, int rows, int V, int Kc, float* lse, int32_t* cand_id,

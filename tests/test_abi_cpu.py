@@ -145,6 +145,7 @@ def test_stage1_plan_picks_the_kernel_by_rows_and_list_length():
     L = dtree.lib()
     k = ctypes.c_int32()
     assert L.dt_stage1_plan(None, ctypes.byref(k), ctypes.byref(k)) == -1
+    assert L.dt_stage1_ceiling(None, None, None, None, None) == -1
 
 
 def test_fused_entry_points_and_normalisation_reject_invalid_arguments():
