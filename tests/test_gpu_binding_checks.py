@@ -30,7 +30,7 @@ def test_short_or_mismatched_buffers_are_refused():
     with pytest.raises(ValueError):  # target rows for fewer nodes than max_nodes
         dtree.verify(tree, torch.zeros((2, 4, 64), device="cuda"))
     with pytest.raises(ValueError):  # uniforms for one request
-        dtree.verify(tree, torch.zeros((2, 9, 64), device="cuda"), temperature=1.0, draft=x,
+        dtree.verify(tree, torch.zeros((2, 9, 64), dtype=torch.bfloat16, device="cuda"), temperature=1.0, draft=x,
                      uniforms=torch.zeros((1, 2, 9), device="cuda"))
     with pytest.raises(TypeError):  # bf16 drafter rows beside fp32 target rows: one element type is read
         dtree.verify(tree, torch.zeros((2, 9, 64), device="cuda"), temperature=1.0, draft=x,
