@@ -108,6 +108,13 @@ def job_throughput(steps, batch_per_rank, world, max_ms):
     return steps * batch_per_rank * world / (max_ms / 1000.0)
 
 
+def headline(steps, batch_per_rank, world, max_ms):
+    """The line's throughput keys for `steps` steps of `batch_per_rank` trees on
+    each of `world` replicas, the slowest taking max_ms."""
+    return {"value": job_throughput(steps, batch_per_rank, world, max_ms), "unit": "trees/s", "n_gpus": world,
+            "steps": steps, "ms_per_step": max_ms / steps, "scaling": "weak"}
+
+
 def parse():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,14 +450,9 @@ def run_ours(args, wl, rank, world, local):
     traffic = KN1_TRAFFIC.get((kn1_name, wl.name, stage1_source_hash(kn1_name)))
     result = {
         "metric": METRIC,
-        "value": job_throughput(args.steps, wl.batch, world, ms),
-        "unit": "trees/s",
-        "n_gpus": world,
-        "steps": args.steps,
+        **headline(args.steps, wl.batch, world, ms),
         "warmup": args.warmup,
-        "ms_per_step": ms / args.steps,
         "higher_is_better": True,
-        "scaling": "weak",
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded Gaussian logits with confident-token spikes; Qwen3 vocabulary)",
@@ -583,11 +585,12 @@ def parity_sample(wl, items, results, n_max=16):
         return {"compared": 0, "reason": "SABA budgets depend on per-request history"}
     dev = torch.device("cuda", torch.cuda.current_device())
     one = wl.with_(batch=1)
+    # the oracle's tables are drawn on the host (a device generator draws other values): the same here
     U = Vt = tdes = None
     if wl.R > 0 and wl.mode in ("dartree", "heap"):
-        U, Vt = wk.markov_tables(wl.V, wl.R, device=dev)
+        U, Vt = (t.to(dev) for t in wk.markov_tables(wl.V, wl.R))
     if wl.H > 0:
-        tdes = wk.tdes_weights(wl.V, wl.L, wl.H, device=dev)
+        tdes = tuple(v.to(dev) if torch.is_tensor(v) else v for v in wk.tdes_weights(wl.V, wl.L, wl.H))
     p = params_for(one, U, Vt, tdes)
     tot = {"requests": 0, "near_ties": 0, "consequences": 0, "order_swaps": 0, "mismatches": 0,
            "order_mismatches": 0, "score_err_viol": 0, "score_err_max": 0.0, "tolerance_max": 0.0,
@@ -688,8 +691,35 @@ def run_reference(args, wl, rank, world, budget_s=150.0, warm_budget_s=30.0):
     }
 
 
+def launch_plan(gpus, env, argv, port=None):
+    """How `bench.py --gpus N` runs.  Under a launcher that set WORLD_SIZE (the
+    driver's torchrun) each process is one rank and WORLD_SIZE must equal N:
+    ("ranks", None), or ("single", None) for N = 1.  Without one, N = 1 runs
+    here and N > 1 re-launches this script as N local ranks, one per GPU,
+    through torch.distributed.run on 127.0.0.1: ("spawn", command).  Requests
+    are independent, so the ranks are replicas that share only the final
+    max-over-ranks time reduction."""
+    world = env.get("WORLD_SIZE")
+    if world is not None:
+        if int(world) != gpus:
+            raise SystemExit("bench.py: --gpus %d does not match WORLD_SIZE=%s" % (gpus, world))
+        return ("ranks", None) if gpus > 1 else ("single", None)
+    if gpus <= 1:
+        return ("single", None)
+    if port is None:
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+    return ("spawn", [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(gpus),
+                      "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv])
+
+
 def main():
     args = parse()
+    mode, cmd = launch_plan(args.gpus, os.environ, sys.argv[1:])
+    if mode == "spawn":
+        sys.exit(subprocess.call(cmd))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -261,11 +261,15 @@ dt_status dt_select(const dt_build_params* p, dt_tree* tree, void* workspace,
  *   log Z = log sum over every v of exp(lp_d(v) + <U[u], Vt[v]>)
  * written as fp32 to the workspace at DT_ZNORM_OFFSET(p), [b][L][K] (rows
  * without a parent token get 0).  The [b*L*K x 64] x [64 x V] contraction
- * runs on the tensor cores with U and Vt rounded to bf16 (fp32
- * accumulation), so each value differs from the exact one by at most about
- * 2^-8 * max_v sum_k |U[u][k] * Vt[v][k]| plus 1e-5.  Reads draft_logits and
- * tree->cand_id, tree->lse (from dt_candidates).  A row whose bounded wait
- * ran out gets NaN, which dt_select reports as DT_DEV_TIMEOUT. */
+ * runs on the tensor cores: U and Vt are each split into a bf16 head and a
+ * bf16 tail (the rounded remainder) and all four products are accumulated in
+ * fp32, so each dot product is within about 2^-17 * sum_k |U[u][k] * Vt[v][k]|
+ * of the fp32 tables' and each value within that (at its largest over v) plus
+ * the fp32 log-sum-exp's own error (below 1e-5) of the exact one.  Reads
+ * draft_logits and tree->cand_id, tree->lse (from dt_candidates).  The
+ * workspace must be 16-byte aligned (DT_ERR_INVALID_ARG otherwise).  A row
+ * whose bounded wait ran out gets NaN, which dt_select reports as
+ * DT_DEV_TIMEOUT. */
 #define DT_ZNORM_OFFSET(p) ((((size_t)(p)->batch * (p)->L * (p)->K * (p)->K * 4) + 255) & ~(size_t)255)
 dt_status dt_markov_norm(const dt_build_params* p, const void* draft_logits, dt_tree* tree, void* workspace,
                          size_t workspace_bytes, dt_stream_t stream);
@@ -451,6 +455,25 @@ dt_status dt_saba_budget(const dt_saba_params* q, const dt_tree* tree, int32_t b
  *     them. */
 #define DT_NOALLOC_TABLE_BYTES (4u << 20)
 dt_status dt_select_dartree_noalloc(const dt_build_params* p, dt_tree* tree, dt_stream_t stream);
+
+/* Test hook of the timeout path (failure detection without a GPU fault).
+ * Every mbarrier wait in the library is bounded; when a bound runs out the
+ * kernel records it and carries on (stage 1: the row's lse becomes NaN and the
+ * selection sets DT_DEV_TIMEOUT; the walk sets DT_DEV_TIMEOUT in the status
+ * word; the normaliser writes NaN, which the selection reports the same way).
+ * For the kernels named in `kernels` (DT_PROBE_* bits, 0 = off) this makes
+ * the staging wait first wait on a barrier that nothing ever completes, bounded
+ * by budget_cycles SM clock cycles (1 .. DT_PROBE_MAX_BUDGET), so that path
+ * runs; the real wait follows unchanged, so every copy lands before its data
+ * is read and outputs other than the flags are the usual ones.  Applies to the
+ * current device; synchronous (a copy to device symbols): call it outside
+ * stream capture and with no library kernel running.  Not for production use.
+ * Returns DT_ERR_INVALID_ARG for unknown bits or a budget out of range. */
+#define DT_PROBE_STAGE1 0x1      /* the cluster stage-1 kernel (dt_candidates, few rows) */
+#define DT_PROBE_WALK 0x2        /* the acceptance walk (dt_verify, dt_verify_rule, dt_verify_markov) */
+#define DT_PROBE_NORMALISER 0x4  /* the tensor-core normaliser (dt_markov_norm) */
+#define DT_PROBE_MAX_BUDGET (1ll << 28)
+dt_status dt_test_wait_fault(int32_t kernels, int64_t budget_cycles);
 
 /* Static string for a dt_status value. */
 const char* dt_status_str(dt_status s);

@@ -385,6 +385,7 @@ dt_status dt_markov_norm(const dt_build_params* p, const void* draft_logits, dt_
     if (s != DT_OK) return s;
     if (!markov_on(p) || !p->markov_norm || !draft_logits) return DT_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < dt_workspace_size(p, nullptr)) return DT_ERR_INVALID_ARG;
+    if ((uintptr_t)workspace & 15u) return DT_ERR_INVALID_ARG;  // the scratch tiles are bulk-copied
     unsigned char* ws = (unsigned char*)workspace;
     float* z = (float*)(ws + DT_ZNORM_OFFSET(p));
     void* scratch = ws + DT_ZNORM_OFFSET(p) + znorm_bytes(p);
@@ -504,6 +505,16 @@ dt_status dt_saba_budget(const dt_saba_params* q, const dt_tree* t, int32_t batc
     if (hidden && Hd < 1) return DT_ERR_INVALID_ARG;
     cudaError_t e = dt_kn9_launch(batch, t->L, t->Kc, t->cand_lp, hidden, Hd, prev_acc_len, ring, count, q->window,
                                   q->c_verify, q->c_fixed, q->B_min, q->B_max, state, budget, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+dt_status dt_test_wait_fault(int32_t kernels, int64_t budget_cycles) {
+    if (kernels & ~(DT_PROBE_STAGE1 | DT_PROBE_WALK | DT_PROBE_NORMALISER)) return DT_ERR_INVALID_ARG;
+    if (kernels && (budget_cycles < 1 || budget_cycles > DT_PROBE_MAX_BUDGET)) return DT_ERR_INVALID_ARG;
+    const long long on = kernels ? (long long)budget_cycles : 0;
+    cudaError_t e = dt_kn1_set_probe((kernels & DT_PROBE_STAGE1) ? on : 0);
+    if (e == cudaSuccess) e = dt_kn6_set_probe((kernels & DT_PROBE_WALK) ? on : 0);
+    if (e == cudaSuccess) e = dt_kn3n_set_probe((kernels & DT_PROBE_NORMALISER) ? on : 0);
     return cuda_status(e);
 }
 

@@ -292,8 +292,9 @@ DT_DI void dt_bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar
         "l"(src), "r"(bytes), "r"(dt_smem_addr(bar))
         : "memory");
 }
-// Wait for the phase with parity `phase` to complete; false if the budget ran out.
-DT_DI bool dt_mbar_wait(uint64_t* bar, uint32_t phase) {
+// Wait for the phase with parity `phase` to complete; false once `budget`
+// SM clock cycles have passed without it.
+DT_DI bool dt_mbar_wait_budget(uint64_t* bar, uint32_t phase, long long budget) {
     const uint32_t a = dt_smem_addr(bar);
     const long long t0 = clock64();
     for (;;) {
@@ -307,8 +308,19 @@ DT_DI bool dt_mbar_wait(uint64_t* bar, uint32_t phase) {
             : "r"(a), "r"(phase), "r"(10000000u)
             : "memory");
         if (done) return true;
-        if (clock64() - t0 > DT_WAIT_BUDGET) return false;
+        if (clock64() - t0 > budget) return false;
     }
+}
+DT_DI bool dt_mbar_wait(uint64_t* bar, uint32_t phase) { return dt_mbar_wait_budget(bar, phase, DT_WAIT_BUDGET); }
+
+// Test hook of the timeout path (dt_test_wait_fault): a kernel whose probe
+// budget is positive first waits, with that budget, on `probe` -- a barrier
+// initialised with one expected arrival that nothing ever arrives on -- so the
+// wait runs out and the kernel takes its timeout path; the real wait follows
+// unchanged, so every copy still lands before the data is read.  Returns false
+// when the probe ran out.
+DT_DI bool dt_probe_wait(uint64_t* probe, long long budget) {
+    return budget <= 0 || dt_mbar_wait_budget(probe, 0, budget);
 }
 
 // Programmatic dependent launch: every kernel of the library is launched so

@@ -57,6 +57,12 @@ inline int dt_max_active_clusters(K kernel, int cluster_x, int block, size_t sme
     return n;
 }
 
+// Timeout-path test hook: probe budgets (SM clock cycles, 0 = off) of the
+// kernels with bounded mbarrier waits (see dt_probe_wait); synchronous.
+cudaError_t dt_kn1_set_probe(long long budget);
+cudaError_t dt_kn6_set_probe(long long budget);
+cudaError_t dt_kn3n_set_probe(long long budget);
+
 // Stage 1 (kn1_candidates.cu).
 // grid_rows clusters share the rows round-robin.
 int dt_kn1_max_clusters(int dtype, int S, int chunk, int Kc);

@@ -57,6 +57,7 @@ struct RowPub {
 
 struct Kn1Misc {
     uint64_t bar;      // the chunk copy
+    uint64_t probe;    // the timeout-path test hook's barrier (never completes)
     float m;           // this row: chunk max value
     uint32_t mk16;     // this row: chunk max key, top 16 bits
     RowPub pub[2];
@@ -155,6 +156,9 @@ DT_DI void merge_plain(cg::cluster_group& cluster, const uint32_t* h, int S, uin
     __syncthreads();
 }
 
+// Probe budget of the timeout-path test hook (0: off), set by dt_kn1_set_probe.
+__device__ long long g_kn1_probe;
+
 template <typename T>
 __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits, int V, int chunk, int Kc, int rows,
                                                  float* __restrict__ lse_out,
@@ -179,6 +183,7 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
 
     if (tid == 0) {
         dt_mbar_init(&misc->bar, 1);
+        dt_mbar_init(&misc->probe, 1);
         dt_fence_mbar_init();
     }
     dt_pdl_trigger();
@@ -211,6 +216,7 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
         // one thread waits on this row's copy; the others block in the barrier
         // below (blocked warps take no issue slots)
         if (pend) {
+            if (tid == 0 && !dt_probe_wait(&misc->probe, g_kn1_probe)) mp->timeout = 1;
             if (tid == 0 && !dt_mbar_wait(&misc->bar, phase)) {
                 mp->timeout = 1;
                 dt_mbar_wait(&misc->bar, phase);
@@ -597,6 +603,10 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
 }
 
 }  // namespace
+
+cudaError_t dt_kn1_set_probe(long long budget) {
+    return cudaMemcpyToSymbol(g_kn1_probe, &budget, sizeof(budget));
+}
 
 size_t dt_kn1_smem_bytes(int chunk, int Kc, int esize) {
     (void)Kc;  // the fixed candidate buffers also hold the fallback's Kc <= 1024 selections

@@ -10,14 +10,21 @@
 //
 // log Z_d(u) = logsumexp_v (x_d(v) + <U[u], Vt[v]>) - lse_d.  The [rows x R]
 // x [R x V] contraction (R = 64) is the one dense contraction of the method:
-// it runs on the fifth-generation tensor cores (tcgen05.mma, kind::f16, bf16
-// operands rounded to nearest from the fp32 tables, fp32 accumulation in
-// tensor memory).  Each CTA takes a tile of 128 rows and a slice of the
-// vocabulary: it stages the rows' U vectors once and, per 128-token step, the
-// tokens' Vt vectors (both as 128-byte-swizzled K-major bf16 tiles), issues
-// four 128x128x16 MMAs from one thread, and its four warps read the 128x128
-// fp32 accumulator back (one row per thread), add the drafter logits and fold
-// exp into a running (max, sum) per row.  A second kernel merges the slices.
+// it runs on the fifth-generation tensor cores (tcgen05.mma, kind::f16, fp32
+// accumulation in tensor memory).  The tables are fp32; each is split into a
+// bf16 head and a bf16 tail (U = Uh + Ul + e with |e| <= 2^-18 |U|, the tail
+// being the rounded remainder), and the accumulator takes all four products
+// Uh.Vh + Uh.Vl + Ul.Vh + Ul.Vl (products of bf16 values are exact in fp32),
+// so each dot product is within about 2^-17 * sum_k |U_k Vt_k| of the fp32
+// tables' -- the bf16 rounding of a single product would leave 2^-8.
+// Each CTA takes a tile of 128 rows and a slice of the vocabulary: it stages
+// the rows' U vectors once (head and tail, 128-byte-swizzled K-major bf16
+// tiles) and, per 128-token step, the tokens' Vt tiles -- laid out in global
+// memory by the conversion kernel exactly as the tensor cores read them, so
+// one 32 KB bulk copy brings a step's head and tail -- issues sixteen
+// 128x128x16 MMAs from one thread, and its eight epilogue warps read the
+// 128x128 fp32 accumulator back, add the drafter logits and fold exp into a
+// running (max, sum) per row.  A second kernel merges the slices.
 #include <cuda_bf16.h>
 
 #include "dt_launch.h"
@@ -27,28 +34,31 @@ namespace {
 
 constexpr int NT = 320;       // warps 0-7: epilogue; warp 8: copies; warp 9: MMA issue
 constexpr int NEPI = 256;     // epilogue threads: TMEM lane quarter (warp % 4) x column half (warp / 4)
-constexpr int STAGES = 3;     // ring of Vt / logit tiles
+constexpr int STAGES = 2;     // ring of Vt / logit tiles
 constexpr int TM = 128;       // rows per tile
 constexpr int TN = 128;       // tokens per MMA step
 constexpr int RK = 64;        // contraction length R (64 bf16 = one 128-byte row)
 constexpr int XG = 16;        // (request, position) logit rows staged per step, at most
 constexpr uint32_t IDESC = dt_idesc_bf16_f32(TM, TN);
-constexpr size_t A_BYTES = 16384, B_BYTES = 16384, X_BYTES = (size_t)XG * TN * 4;
+constexpr size_t HALF = 16384;                            // one 128 x 64 bf16 tile
+constexpr size_t A_BYTES = 2 * HALF, B_BYTES = 2 * HALF;  // head tile, then tail tile
+constexpr size_t X_BYTES = (size_t)XG * TN * 2;           // bf16 logit rows (fp32 logits are read in place)
 constexpr size_t OFF_B = A_BYTES;
 constexpr size_t OFF_X = OFF_B + STAGES * B_BYTES;
 constexpr size_t OFF_BAR = OFF_X + STAGES * X_BYTES;
 
 struct Kn3nShared {
-    uint64_t full[STAGES];   // tile landed (32 copy-thread arrivals)
+    uint64_t full[STAGES];   // tile landed (the Vt bulk copy + 32 logit-copy arrivals)
     uint64_t empty[STAGES];  // tile consumed (MMA commit + NEPI logit readers)
     uint64_t accf[2];        // accumulator written (MMA commit)
     uint64_t acce[2];        // accumulator read (NEPI arrivals)
+    uint64_t probe;          // the timeout-path test hook's barrier (never completes)
     uint32_t tmem;
     int fail;
     float pm[TM], ps[TM];    // second column half's partial (max, sum) per row
 };
-// A tile, three B tiles and three logit tiles from a 1024-byte aligned base; at
-// most two CTAs fit an SM, so their 2 x 256 TMEM columns always fit its 512
+// The A tiles, two B stages and two logit tiles from a 1024-byte aligned base;
+// at most two CTAs fit an SM, so their 2 x 256 TMEM columns always fit its 512
 constexpr size_t SMEM = 1024 + OFF_BAR + sizeof(Kn3nShared);
 static_assert(2 * (SMEM + 1024) <= 233472 && 3 * (SMEM + 1024) > 233472, "two CTAs per SM, not three");
 
@@ -63,18 +73,27 @@ DT_DI int row_parent(int r, int L, int K, int V, const int32_t* root_tok, const 
     return (u >= 0 && u < V) ? u : -1;
 }
 
-// Columns [k0, k0 + 32) of an fp32 [*, 64] table row into a swizzled bf16
-// tile row (zeros when src is null).
-DT_DI void stage_half_row_bf16(unsigned char* tile, int row, int k0, const float* src) {
+// bf16 head and tail of two fp32 values (round to nearest; the tail is the
+// rounded remainder, which fp32 holds exactly).
+DT_DI void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(__fsub_rn(a, hf.x), __fsub_rn(b, hf.y));
+    hi = *(const uint32_t*)&h;
+    lo = *(const uint32_t*)&l;
+}
+
+// Columns [k0, k0 + 32) of an fp32 [*, 64] table row into the swizzled bf16
+// head tile and tail tile (HALF bytes after it); zeros when src is null.
+DT_DI void stage_half_row_split(unsigned char* tile, int row, int k0, const float* src) {
 #pragma unroll
     for (int k = k0; k < k0 + 32; k += 4) {
         float4 f = src ? *(const float4*)(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(f.x, f.y);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(f.z, f.w);
-        uint2 w;
-        w.x = *(const uint32_t*)&lo;
-        w.y = *(const uint32_t*)&hi;
-        *(uint2*)(tile + dt_sw128_offset(row, k)) = w;
+        uint2 wh, wl;
+        split2(f.x, f.y, wh.x, wl.x);
+        split2(f.z, f.w, wh.y, wl.y);
+        *(uint2*)(tile + dt_sw128_offset(row, k)) = wh;
+        *(uint2*)(tile + HALF + dt_sw128_offset(row, k)) = wl;
     }
 }
 
@@ -83,21 +102,30 @@ DT_DI void wait_or_fail(uint64_t* bar, uint32_t parity, int* fail) {
     if (!dt_mbar_wait(bar, parity)) *fail = 1;
 }
 
-// Fp32 table -> bf16 table (round to nearest), 8 values per thread step.
-__global__ void __launch_bounds__(256) kn3n_convert_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
-                                                           size_t n8) {
+// Fp32 Vt [V][64] -> per 128-token tile a 32 KB block [head | tail], each
+// half the K-major 128-byte-swizzled bf16 layout the MMA reads (row r's
+// 16-byte chunk c at r * 128 + ((c ^ (r % 8)) << 4)); rows past V are zero.
+// One thread per (token, chunk of 8 values).
+__global__ void __launch_bounds__(256) kn3n_convert_kernel(const float* __restrict__ src, unsigned char* __restrict__ dst,
+                                                           int V, int ntiles) {
     dt_pdl_trigger();
     dt_pdl_wait();
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 a = ((const float4*)src)[2 * i], c = ((const float4*)src)[2 * i + 1];
-        const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
-        const __nv_bfloat162 p2 = __floats2bfloat162_rn(c.x, c.y), p3 = __floats2bfloat162_rn(c.z, c.w);
-        uint4 w;
-        w.x = *(const uint32_t*)&p0;
-        w.y = *(const uint32_t*)&p1;
-        w.z = *(const uint32_t*)&p2;
-        w.w = *(const uint32_t*)&p3;
-        ((uint4*)dst)[i] = w;
+    const size_t n = (size_t)ntiles * TN * 8;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int v = (int)(i >> 3), c = (int)(i & 7);
+        const int t = v / TN, r = v % TN;
+        uint4 wh = make_uint4(0u, 0u, 0u, 0u), wl = wh;
+        if (v < V) {
+            const float4 a = ((const float4*)(src + (size_t)v * RK + c * 8))[0];
+            const float4 b = ((const float4*)(src + (size_t)v * RK + c * 8))[1];
+            split2(a.x, a.y, wh.x, wl.x);
+            split2(a.z, a.w, wh.y, wl.y);
+            split2(b.x, b.y, wh.z, wl.z);
+            split2(b.z, b.w, wh.w, wl.w);
+        }
+        unsigned char* base = dst + (size_t)t * B_BYTES + (size_t)r * 128 + ((c ^ (r & 7)) << 4);
+        *(uint4*)base = wh;
+        *(uint4*)(base + HALF) = wl;
     }
 }
 
@@ -163,11 +191,14 @@ DT_DI void fold32(float (&v)[32], int nvalid, float& M, float& S) {
     }
 }
 
+// Probe budget of the timeout-path test hook (0: off), set by dt_kn3n_set_probe.
+__device__ long long g_kn3n_probe;
+
 template <typename T>
 __global__ void __launch_bounds__(NT, 2) kn3n_kernel(const T* __restrict__ x, int V, int L, int K, int rows,
                                                      const int32_t* __restrict__ root_tok,
                                                      const int32_t* __restrict__ cand_id,
-                                                     const float* __restrict__ U, const uint16_t* __restrict__ Vt16,
+                                                     const float* __restrict__ U, const unsigned char* __restrict__ Vtt,
                                                      int vs, float2* __restrict__ part) {
     using E = DtElem<T>;
     extern __shared__ unsigned char smem_raw[];
@@ -182,29 +213,30 @@ __global__ void __launch_bounds__(NT, 2) kn3n_kernel(const T* __restrict__ x, in
     // logit rows of this tile: flat (request, position) indices g0 .. g0 + ng - 1
     const int g0 = (tile * TM) / K;
     const int ng = (min(rows, tile * TM + TM) - 1) / K - g0 + 1;
-    const bool xs = ng <= XG && (((uintptr_t)x) & 15u) == 0 && ((size_t)V * sizeof(T)) % 16 == 0;
+    const bool xs = sizeof(T) == 2 && ng <= XG && (((uintptr_t)x) & 15u) == 0 && ((size_t)V * sizeof(T)) % 16 == 0;
 
     if (wid == 0) dt_tmem_alloc(&sh->tmem, 2 * TN);
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            dt_mbar_init(&sh->full[i], 32);
+            dt_mbar_init(&sh->full[i], 33);
             dt_mbar_init(&sh->empty[i], 1 + NEPI);
         }
         for (int i = 0; i < 2; ++i) {
             dt_mbar_init(&sh->accf[i], 1);
             dt_mbar_init(&sh->acce[i], NEPI);
         }
+        dt_mbar_init(&sh->probe, 1);
         dt_fence_mbar_init();
         sh->fail = 0;
     }
     dt_pdl_trigger();
     dt_pdl_wait();  // candidate ids, logits and the bf16 table come from earlier kernels
 
-    if (tid < NEPI) {  // A tile: the rows' U vectors, two threads per row
+    if (tid < NEPI) {  // A tiles: the rows' U vectors (head, tail), two threads per row
         const int row = tid & (TM - 1), r = tile * TM + row;
         int b, d;
         const int u = r < rows ? row_parent(r, L, K, V, root_tok, cand_id, &b, &d) : -1;
-        stage_half_row_bf16(sm, row, 32 * (tid >> 7), u >= 0 ? U + (size_t)u * RK : nullptr);
+        stage_half_row_split(sm, row, 32 * (tid >> 7), u >= 0 ? U + (size_t)u * RK : nullptr);
     }
     dt_fence_proxy_async_smem();
     dt_tc_fence_before();
@@ -213,19 +245,17 @@ __global__ void __launch_bounds__(NT, 2) kn3n_kernel(const T* __restrict__ x, in
     const uint32_t tmem = sh->tmem;
 
     if (wid == 8) {
-        // ---- copies: Vt rows (swizzled) and logit rows of each step ---------
+        // ---- copies: the step's Vt tile pair (one bulk copy) and logit rows
         for (int j = 0; j < nsteps; ++j) {
             const int s = j % STAGES;
             if (j >= STAGES) wait_or_fail(&sh->empty[s], ((j / STAGES) - 1) & 1, &sh->fail);
             const int v0 = vbeg + j * TN;
-            unsigned char* bt = sm + OFF_B + s * B_BYTES;
-            for (int q = lane; q < TN * 8; q += 32) {
-                const int row = q >> 3, c = q & 7, v = v0 + row;
-                const bool ok = v < vend;
-                dt_cp_async16_zfill(bt + row * 128 + ((c ^ (row & 7)) << 4), Vt16 + (size_t)(ok ? v : 0) * RK + c * 8,
-                                    ok ? 16u : 0u);
+            if (lane == 0) {
+                dt_mbar_arrive_expect_tx(&sh->full[s], (uint32_t)B_BYTES);
+                dt_bulk_g2s(sm + OFF_B + s * B_BYTES, Vtt + (size_t)(v0 / TN) * B_BYTES, (uint32_t)B_BYTES,
+                            &sh->full[s]);
             }
-            if (xs) {
+            if constexpr (sizeof(T) == 2) if (xs) {
                 constexpr int EPC = 16 / sizeof(T);   // elements per 16-byte chunk
                 constexpr int CPR = TN / EPC;         // chunks per logit row
                 unsigned char* xt = sm + OFF_X + s * X_BYTES;
@@ -244,6 +274,7 @@ __global__ void __launch_bounds__(NT, 2) kn3n_kernel(const T* __restrict__ x, in
         // ---- MMA issue: 128 x 128 x 64 per step into alternating accumulators
         if (lane == 0) {
             const uint32_t ab = dt_smem_addr(sm);
+            if (!dt_probe_wait(&sh->probe, g_kn3n_probe)) sh->fail = 1;
             for (int j = 0; j < nsteps; ++j) {
                 const int s = j % STAGES, a = j & 1;
                 wait_or_fail(&sh->full[s], (j / STAGES) & 1, &sh->fail);
@@ -251,10 +282,15 @@ __global__ void __launch_bounds__(NT, 2) kn3n_kernel(const T* __restrict__ x, in
                 dt_tc_fence_after();
                 dt_fence_proxy_async_smem();
                 const uint32_t bb = dt_smem_addr(sm + OFF_B + s * B_BYTES);
+                // head x head, then the three products with a tail
 #pragma unroll
-                for (int kk = 0; kk < RK / 16; ++kk)
-                    dt_mma_bf16(tmem + a * TN, dt_desc_kmajor_sw128(ab + 32 * kk), dt_desc_kmajor_sw128(bb + 32 * kk),
-                                IDESC, kk > 0);
+                for (int pr = 0; pr < 4; ++pr) {
+                    const uint32_t ao = ab + (pr >> 1) * (uint32_t)HALF, bo = bb + (pr & 1) * (uint32_t)HALF;
+#pragma unroll
+                    for (int kk = 0; kk < RK / 16; ++kk)
+                        dt_mma_bf16(tmem + a * TN, dt_desc_kmajor_sw128(ao + 32 * kk),
+                                    dt_desc_kmajor_sw128(bo + 32 * kk), IDESC, pr > 0 || kk > 0);
+                }
                 dt_mma_commit(&sh->empty[s]);
                 dt_mma_commit(&sh->accf[a]);
             }
@@ -367,9 +403,13 @@ __global__ void __launch_bounds__(256) kn3n_reduce_kernel(const float2* __restri
 
 }  // namespace
 
+cudaError_t dt_kn3n_set_probe(long long budget) {
+    return cudaMemcpyToSymbol(g_kn3n_probe, &budget, sizeof(budget));
+}
+
 size_t dt_kn3n_scratch_bytes(int rows, int V) {
     const size_t part = (((size_t)rows * DT_KN3N_MAX_SPLIT * sizeof(float2)) + 255) & ~(size_t)255;
-    return part + (size_t)V * RK * sizeof(uint16_t);
+    return part + (size_t)((V + TN - 1) / TN) * B_BYTES;
 }
 
 cudaError_t dt_kn3n_launch(const void* x, int dtype, int batch, int L, int K, int V, const int32_t* root_tok,
@@ -378,20 +418,21 @@ cudaError_t dt_kn3n_launch(const void* x, int dtype, int batch, int L, int K, in
     const int rows = batch * L * K;
     const int mtiles = (rows + TM - 1) / TM;
     float2* part = (float2*)scratch;
-    uint16_t* Vt16 = (uint16_t*)((unsigned char*)scratch +
-                                 ((((size_t)rows * DT_KN3N_MAX_SPLIT * sizeof(float2)) + 255) & ~(size_t)255));
+    unsigned char* Vtt = (unsigned char*)scratch +
+                         ((((size_t)rows * DT_KN3N_MAX_SPLIT * sizeof(float2)) + 255) & ~(size_t)255);
+    const int ntiles = (V + TN - 1) / TN;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess || sms < 1) {
         (void)cudaGetLastError();
         sms = 148;
     }
     cudaError_t e;
-    // the child-token table in bf16, once per call
-    const size_t n8 = (size_t)V * RK / 8;
+    // the child-token table as bf16 head and tail tiles, once per call
+    const size_t n8 = (size_t)ntiles * TN * 8;
     size_t cblocks = (n8 + 255) / 256;
     if (cblocks > (size_t)sms * 8) cblocks = (size_t)sms * 8;
     DtLaunch lcv(dim3((unsigned)cblocks), dim3(256), 0, st);
-    if ((e = cudaLaunchKernelEx(&lcv.cfg, kn3n_convert_kernel, Vt, Vt16, n8)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&lcv.cfg, kn3n_convert_kernel, Vt, Vtt, V, ntiles)) != cudaSuccess) return e;
     // two CTAs per SM, vocabulary slices of whole 128-token steps
     int nsplit = (2 * sms + mtiles - 1) / mtiles;
     const int steps = (V + TN - 1) / TN;
@@ -404,13 +445,13 @@ cudaError_t dt_kn3n_launch(const void* x, int dtype, int batch, int L, int K, in
             cudaSuccess)
             return e;
         e = cudaLaunchKernelEx(&lc.cfg, kn3n_kernel<uint16_t>, (const uint16_t*)x, V, L, K, rows, root_tok, cand_id, U,
-                               (const uint16_t*)Vt16, vs, part);
+                               (const unsigned char*)Vtt, vs, part);
     } else {
         if ((e = cudaFuncSetAttribute(kn3n_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
             cudaSuccess)
             return e;
         e = cudaLaunchKernelEx(&lc.cfg, kn3n_kernel<float>, (const float*)x, V, L, K, rows, root_tok, cand_id, U,
-                               (const uint16_t*)Vt16, vs, part);
+                               (const unsigned char*)Vtt, vs, part);
     }
     if (e != cudaSuccess) return e;
     DtLaunch lr(dim3((rows + 255) / 256), dim3(256), 0, st);

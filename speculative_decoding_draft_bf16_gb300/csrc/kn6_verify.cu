@@ -56,6 +56,7 @@ struct Pub {
 
 struct Kn6Misc {
     uint64_t bar[NBMAX];
+    uint64_t probe;               // the timeout-path test hook's barrier (never completes)
     int timeout;
     int bad;
     Pub pub[2];
@@ -125,11 +126,15 @@ struct Rows {
     uint32_t pend;        // bit i: a bulk copy into buffer i has not been waited for
     uint32_t ph;          // bit i: mbarrier phase parity of buffer i
     DtStager<T> s0, s1, s2;  // ragged chunk ends of each buffer's latest copy, in registers
+    uint64_t* probe;      // the timeout-path test hook's barrier, and its budget (0: off)
+    long long probe_budget;
 
-    DT_DI void init(unsigned char* b, int s, uint64_t* bars) {
+    DT_DI void init(unsigned char* b, int s, uint64_t* bars, uint64_t* probe_bar, long long pb) {
         base = b;
         stride = s;
         bar = bars;
+        probe = probe_bar;
+        probe_budget = pb;
         h0 = h1 = h2 = 0;
         t0 = t1 = t2 = -1;
         pend = ph = 0;
@@ -150,6 +155,7 @@ struct Rows {
         else if (i == 1) s1.held_off = -1;
         else s2.held_off = -1;
         if (!((pend >> i) & 1u)) return;
+        if (threadIdx.x == 0 && !dt_probe_wait(probe, probe_budget)) *timeout = 1;
         if (threadIdx.x == 0 && !dt_mbar_wait(&bar[i], (ph >> i) & 1u)) {
             *timeout = 1;
             dt_mbar_wait(&bar[i], (ph >> i) & 1u);
@@ -185,6 +191,9 @@ struct Kn6Corr {
     int K;
     const int32_t* root_tok;  // [batch] or NULL
 };
+
+// Probe budget of the timeout-path test hook (0: off), set by dt_kn6_set_probe.
+__device__ long long g_kn6_probe;
 
 // One instantiation per acceptance rule (RULE = DT_VERIFY_*), so that each
 // walk carries only its own code; CORR: the ratio rule against q~.
@@ -225,10 +234,12 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
     const int DB = nbt;           // index of the drafter buffer
 
     Rows<T> rows;
-    rows.init(smem + 1024 + tree_bytes, (int)(((size_t)chunk * sizeof(T) + 16 + 127) & ~(size_t)127), misc->bar);
+    rows.init(smem + 1024 + tree_bytes, (int)(((size_t)chunk * sizeof(T) + 16 + 127) & ~(size_t)127), misc->bar,
+              &misc->probe, g_kn6_probe);
 
     if (tid == 0) {
         for (int i = 0; i < NBMAX; ++i) dt_mbar_init(&misc->bar[i], 1);
+        dt_mbar_init(&misc->probe, 1);
         dt_fence_mbar_init();
         misc->timeout = 0;
     }
@@ -773,6 +784,10 @@ Kn6Layout kn6_layout(int chunk, int esize, int Mmax, int rule) {
 }
 
 }  // namespace
+
+cudaError_t dt_kn6_set_probe(long long budget) {
+    return cudaMemcpyToSymbol(g_kn6_probe, &budget, sizeof(budget));
+}
 
 size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax, int rule) {
     return kn6_layout(chunk, esize, Mmax, rule).total;

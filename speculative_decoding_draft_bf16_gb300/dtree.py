@@ -94,11 +94,25 @@ def lib():
                                 _vp]
         L.dt_select_dartree_noalloc.restype = _i32
         L.dt_select_dartree_noalloc.argtypes = [bp, tp, _vp]
+        L.dt_test_wait_fault.restype = _i32
+        L.dt_test_wait_fault.argtypes = [_i32, ctypes.c_int64]
         L.dt_status_str.restype = ctypes.c_char_p
         L.dt_status_str.argtypes = [_i32]
         L.dt_version.restype = _i32
         _LIB = L
     return _LIB
+
+
+PROBE = {"stage1": 0x1, "walk": 0x2, "normaliser": 0x4}
+
+
+def set_test_wait_fault(kernels=(), budget_cycles=2_000_000):
+    """dt_test_wait_fault: make the named kernels' bounded waits run out once per
+    staging step (a test of the timeout path); kernels=() turns it off."""
+    mask = 0
+    for k in kernels:
+        mask |= PROBE[k]
+    _check(lib().dt_test_wait_fault(mask, int(budget_cycles) if mask else 0), "dt_test_wait_fault")
 
 
 class DtError(RuntimeError):
