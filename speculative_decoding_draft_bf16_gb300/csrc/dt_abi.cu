@@ -68,21 +68,27 @@ constexpr int kRowsPerCtaKc = 512;
 constexpr long long kFixedElems = 12288;
 
 // Cluster size for a row-parallel vocabulary pass over `rows` rows (one
-// cluster per row): the power of two in [s_min, 16] -- chunks of at most
-// kChunkMax elements, and of at least ~1K unless that is s_min -- that
-// minimises the estimated time, waves x (chunk + kFixedElems), where a wave is
-// as many clusters as the device holds at once.  smem_ok(S) says whether a
-// cluster size fits in shared memory; fits(S) gives the resident clusters.
+// cluster per row): the size in [s_min, 16] -- a power of two unless any_size
+// -- with chunks of at most kChunkMax elements, and of at least ~1K unless that
+// is s_min, that minimises the estimated time, waves x (chunk + kFixedElems),
+// where a wave is as many clusters as the device holds at once.  smem_ok(S)
+// says whether a cluster size fits in shared memory; fits(S) gives the
+// resident clusters.  (Clusters are placed within a GPC, so how many fit
+// depends on the size in ways only the occupancy query knows: on a GB300 at
+// one CTA per SM, 15 clusters of 8 but more of 7.)
 template <typename SmemOk, typename Fits>
-int cluster_for(int V, long long rows, int dtype, SmemOk smem_ok, Fits fits) {
-    int s_min = pow2_ceil(((long long)V + kChunkMax - 1) / kChunkMax);
+int cluster_for(int V, long long rows, int dtype, SmemOk smem_ok, Fits fits, bool any_size = false) {
+    // any size: the kernel has an SM to itself, so only its shared memory
+    // (smem_ok) bounds the chunk; powers of two: chunks of at most kChunkMax
+    int s_min = any_size ? (int)(((long long)V + 65535) / 65536)
+                         : pow2_ceil(((long long)V + kChunkMax - 1) / kChunkMax);
     int s_cap = pow2_ceil(((long long)V + 1023) / 1024);  // chunks of at least ~1K elements
     if (s_cap > 16) s_cap = 16;
     if (s_min < 1) s_min = 1;
     if (s_cap < s_min) s_cap = s_min;
     int best = s_min;
     long long best_cost = -1;
-    for (int s = s_min; s <= s_cap; s <<= 1) {
+    for (int s = s_min; s <= s_cap; s = any_size ? s + 1 : s << 1) {
         if (!smem_ok(s)) continue;
         const int chunk = chunk_of(V, s, dtype);
         int n = fits(s, chunk);
@@ -209,7 +215,7 @@ dt_status plan_stage1(const dt_build_params* p, Stage1Plan* plan) {
     }
     const int S = cluster_for(
         V, rows, dtype, [&](int q) { return dt_kn1_smem_bytes(chunk_of(V, q, dtype), Kc, esize) + 4096 <= kSmemMax; },
-        [&](int q, int chunk) { return max_clusters(1, dtype, q, chunk, Kc); });
+        [&](int q, int chunk) { return max_clusters(1, dtype, q, chunk, Kc); }, true);
     const int chunk = chunk_of(V, S, dtype);
     if (dt_kn1_smem_bytes(chunk, Kc, esize) + 4096 > kSmemMax) return DT_ERR_UNSUPPORTED;
     *plan = Stage1Plan{DT_STAGE1_CLUSTER, S, chunk};

@@ -3,8 +3,8 @@
 // A measurement kernel, not a step of the method: it reads the drafter rows
 // with exactly the launch that the cluster stage-1 kernel (kn1_candidates.cu)
 // gets -- the same grid of S-CTA clusters, one per row, the same chunk per
-// CTA, the same dynamic shared memory (so the same residency), programmatic
-// dependent launch -- and does the least work that still consumes every
+// CTA, the same residency (one CTA per SM), programmatic dependent launch --
+// and does the least work that still consumes every
 // byte: each CTA bulk-copies its chunk into shared memory, takes the chunk's
 // maximum in one pass and writes it.  No exchange between the CTAs.  Its
 // device time bounds from below what any kernel of that launch shape can
@@ -17,9 +17,10 @@ namespace {
 
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
+constexpr size_t kOneCtaSmem = 120 * 1024;  // above half of an SM's shared memory
 
 template <typename T>
-__global__ void __launch_bounds__(NT, 2) kn0_kernel(const T* __restrict__ logits, int V, int chunk, int S,
+__global__ void __launch_bounds__(NT, 1) kn0_kernel(const T* __restrict__ logits, int V, int chunk, int S,
                                                      size_t data_off, float* __restrict__ out,
                                                      int32_t* __restrict__ timed_out) {
     constexpr int EPV = 16 / sizeof(T);
@@ -85,9 +86,12 @@ __global__ void __launch_bounds__(NT, 2) kn0_kernel(const T* __restrict__ logits
 cudaError_t dt_kn0_launch(const void* logits, int dtype, int rows, int V, int Kc, int S, int chunk, float* out,
                           int32_t* timed_out, cudaStream_t st) {
     const int esize = dtype == DT_BF16 ? 2 : 4;
-    // the stage-1 kernel's dynamic shared memory: its data area sits at the end
-    const size_t smem = dt_kn1_smem_bytes(chunk, Kc, esize);
-    const size_t data_off = smem - (size_t)chunk * esize - 32;
+    // the stage-1 kernel's dynamic shared memory (its data area sits at the
+    // end), and at least half an SM's, so that -- like the stage-1 kernel,
+    // whose registers allow one CTA per SM -- no two CTAs share an SM
+    const size_t need = dt_kn1_smem_bytes(chunk, Kc, esize);
+    const size_t smem = need > kOneCtaSmem ? need : kOneCtaSmem;
+    const size_t data_off = need - (size_t)chunk * esize - 32;
     DtLaunch lc(dim3(S, rows, 1), dim3(NT, 1, 1), smem, st, S);
     cudaError_t e;
     if (dtype == DT_BF16) {

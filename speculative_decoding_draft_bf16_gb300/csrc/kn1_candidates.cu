@@ -7,24 +7,30 @@
 // owns a contiguous vocabulary chunk, staged once from HBM into shared memory
 // by a 1-D bulk async copy and then read 16 bytes per lane at a time.
 //
-// Fast path (no per-element atomics):
-//   pass 1   each lane's maximum over its elements (packed compares) and the
-//            chunk maximum; the lane maxima (one per thread) go into a 256-bin
-//            histogram of order keys below the chunk maximum;
+// Fast path (two cluster barriers per row):
+//   pass 1   each lane's running maximum and sum exp(x - max) over its
+//            elements (rescaled whenever the maximum grows); the lane maxima
+//            (one per thread) go into a 256-bin histogram of order keys below
+//            the chunk maximum; the lanes' (max, sum) pairs merge into the
+//            chunk's;
+//   barrier  1;
 //   exchange every lane maximum is a distinct element of the row, so the
 //            Kc-th largest lane maximum of the row is a lower bound for its
-//            Kc-th largest logit.  The CTAs merge their histograms in the
-//            frame of the row maximum through DSMEM (entries that fall outside
-//            the frame are dropped, which can only lower the bound) and read
-//            the bound off the top;
-//   pass 2   sum exp(x - max) for the normaliser (packed f32x2 arithmetic) and
-//            collect every element at or above the bound as a candidate
-//            (a vector is looked into only when its maximum reaches the bound);
-//   exchange normaliser and candidate counts; every CTA gathers the row's
-//            candidates and ranks its own (logit descending, token id
-//            ascending), writing those of rank < Kc.
-// The candidates hold the true Top-Kc and everything ranked above any of its
-// members, so their ranks among themselves are the exact ranks.
+//            Kc-th largest logit.  Every CTA merges the cluster's histograms
+//            in the frame of the row maximum through DSMEM (entries that fall
+//            outside the frame are dropped, which can only lower the bound)
+//            and reads the bound off the top, and merges the chunks' (max,
+//            sum) pairs into the row's normaliser;
+//   pass 2   collect every element at or above the bound as a candidate (a
+//            vector is looked into only when its maximum reaches the bound);
+//            then every CTA appends its candidates to every CTA's row list
+//            (one remote atomic per destination for the offset, then plain
+//            remote stores);
+//   barrier  2;
+//   rank     each CTA now holds the row's whole candidate list locally and
+//            ranks its own candidates in it (logit descending, token id
+//            ascending), writing those of rank < Kc.  No shared memory of
+//            another CTA is touched after the second barrier.
 // Rows whose candidates overflow the buffers (a row of many equal logits, a
 // tiny vocabulary) take the fallback, the same for the whole cluster: a 256-bin
 // window histogram of all keys below the chunk maximum, the exact threshold
@@ -45,29 +51,35 @@ constexpr int SMAX = 16;
 constexpr int CCAP = 1024;  // candidates one CTA keeps (>= the largest Kc)
 constexpr int ACAP = 2048;  // candidates of one row
 
-// Per-row values that partners read after the row's second cluster barrier,
-// kept per row parity: a CTA may start its next row while a partner still
-// reads them.
+// Per-row values of the fallback that partners read after its cluster
+// barriers, kept per row parity: a CTA may start its next row while a partner
+// still reads them.
 struct RowPub {
-    float s;      // chunk sum exp(x - m)
     int ncand;    // candidates found in this CTA (may exceed CCAP)
     int nsel;     // fallback: selected entries in this CTA
-    int timeout;  // the chunk's staging wait ran out
+};
+
+// Values partners read between a row's two barriers are written before the
+// first and not again before the second has passed, so they need no parity.
+// A CTA's per-row statistics, pushed into every CTA of the cluster.
+struct Kn1Stat {
+    float m;        // chunk max value
+    float s;        // chunk sum exp(x - m)
+    uint32_t mk16;  // chunk max key, top 16 bits
+    int timeout;    // the chunk's staging wait ran out
 };
 
 struct Kn1Misc {
     uint64_t bar;      // the chunk copy
     uint64_t probe;    // the timeout-path test hook's barrier (never completes)
-    float m;           // this row: chunk max value
-    uint32_t mk16;     // this row: chunk max key, top 16 bits
+    int timeout;       // this row: this CTA's staging wait ran out
+    int nrecv;         // this row: candidates the cluster has appended to `all`
     RowPub pub[2];
-    float cm[SMAX];    // partners' values, copied through DSMEM
-    float cs[SMAX];
+    Kn1Stat pin[SMAX]; // this row: every CTA's statistics, pushed by each before the first barrier
     uint32_t cmk[SMAX];
-    int cnc[SMAX];
+    int pbase[SMAX];   // this CTA's offset in each partner's list
     int ceq[SMAX];
     int cnsel[SMAX];
-    int cto[SMAX];
     float lse;
     DtBinSearch bs;
     int weq[NW];       // fallback: threshold ties per warp slice
@@ -76,12 +88,14 @@ struct Kn1Misc {
 };
 
 // Dynamic shared memory: [misc 1 KB][chist 2 KB][cand CCAP*8][all ACAP*8]
-// [chunk data + 32].  The fallback's per-warp histograms (NW*1 KB) live in
-// `all`, which it fills only after its last histogram read.
+// [hin SMAX*1 KB][chunk data + 32].  The fallback's per-warp histograms
+// (NW*1 KB) live in `all`, which it fills only after its last histogram read.
+// hin[j] receives CTA j's lane-maximum histogram (its own frame) each row.
 constexpr size_t OFF_CHIST = 1024;
 constexpr size_t OFF_CAND = OFF_CHIST + 2048;
 constexpr size_t OFF_ALL = OFF_CAND + (size_t)CCAP * 8;
-constexpr size_t OFF_DATA = OFF_ALL + (size_t)ACAP * 8;
+constexpr size_t OFF_HIN = OFF_ALL + (size_t)ACAP * 8;
+constexpr size_t OFF_DATA = OFF_HIN + (size_t)SMAX * 1024;
 static_assert((size_t)ACAP * 8 >= (size_t)NW * 1024, "per-warp histograms must fit in the gather buffer");
 static_assert(sizeof(Kn1Misc) <= OFF_CHIST, "misc block overflows its slot");
 static_assert(OFF_DATA % 128 == 0, "chunk data must stay 128-byte aligned");
@@ -141,6 +155,20 @@ DT_DI void merge_framed(cg::cluster_group& cluster, const uint32_t* h, int S, co
     __syncthreads();
 }
 
+// The same from histograms already copied into this CTA (hin[j]: CTA j's).
+DT_DI void merge_framed_local(const uint32_t* hin, int S, const uint32_t* refs, uint32_t top, uint32_t* g) {
+    const int t = threadIdx.x;
+    if (t < 256) {
+        uint32_t a = 0;
+        for (int j = 0; j < S; ++j) {
+            const int wj = t - (int)(top - refs[j]);
+            if (wj >= 0 && wj < 256) a += hin[j * 256 + wj];
+        }
+        g[t] = a;
+    }
+    __syncthreads();
+}
+
 // Sum over the cluster of bin-aligned histograms (buffer `h` of every CTA).
 DT_DI void merge_plain(cg::cluster_group& cluster, const uint32_t* h, int S, uint32_t* g) {
     const int t = threadIdx.x;
@@ -159,8 +187,11 @@ DT_DI void merge_plain(cg::cluster_group& cluster, const uint32_t* h, int S, uin
 // Probe budget of the timeout-path test hook (0: off), set by dt_kn1_set_probe.
 __device__ long long g_kn1_probe;
 
+// One CTA per SM: the registers this allows keep the fast path free of
+// spills, and a CTA never shares its SM with a partner of the same row pass
+// (the cluster size is chosen so that every row's cluster fits at once).
 template <typename T>
-__global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits, int V, int chunk, int Kc, int rows,
+__global__ void __launch_bounds__(NT, 1) kn1_kernel(const T* __restrict__ logits, int V, int chunk, int Kc, int rows,
                                                  float* __restrict__ lse_out,
                                                  int32_t* __restrict__ cand_id,
                                                  float* __restrict__ cand_lp) {
@@ -180,6 +211,7 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
     uint32_t* chist = (uint32_t*)(smem + OFF_CHIST);
     unsigned long long* cand = (unsigned long long*)(smem + OFF_CAND);
     unsigned long long* all = (unsigned long long*)(smem + OFF_ALL);
+    uint32_t* hin = (uint32_t*)(smem + OFF_HIN);
 
     if (tid == 0) {
         dt_mbar_init(&misc->bar, 1);
@@ -202,23 +234,27 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
     int row = blockIdx.y;
     if (row < rows) issue(row);
 
+    bool fallback_taken = false;
     for (int it = 0; row < rows; ++it, row += G) {
         const int par = it & 1;
         const int nxt = row + G;
         RowPub* mp = &misc->pub[par];
+        // partners stopped reading this CTA's per-row values at the previous
+        // row's second barrier, and append to `all` only after the first
         if (tid == 0) {
             mp->ncand = 0;
             mp->nsel = 0;
-            mp->timeout = 0;
+            misc->timeout = 0;
+            misc->nrecv = 0;
         }
         if (tid < 256) chist[tid] = 0;
         stg.finish(smem + OFF_DATA);  // this row's ragged ends
         // one thread waits on this row's copy; the others block in the barrier
         // below (blocked warps take no issue slots)
         if (pend) {
-            if (tid == 0 && !dt_probe_wait(&misc->probe, g_kn1_probe)) mp->timeout = 1;
+            if (tid == 0 && !dt_probe_wait(&misc->probe, g_kn1_probe)) misc->timeout = 1;
             if (tid == 0 && !dt_mbar_wait(&misc->bar, phase)) {
-                mp->timeout = 1;
+                misc->timeout = 1;
                 dt_mbar_wait(&misc->bar, phase);
             }
             phase ^= 1u;
@@ -239,53 +275,82 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
         const int full_lo = (ch.h > 0) ? 1 : 0;
         const int full_hi = ((ch.h + ch.n) % EPV == 0) ? ch.nv : ch.nv - 1;
 
-        // ---- pass 1: lane maxima and the chunk maximum ----------------------
-        float lmax = NEG_INF;
-        for (int j = v0 + lane; j < v1; j += 32) {
+        // ---- pass 1: lane maxima and running (max, sum exp) -----------------
+        // two full vectors per step fold in together (one rescale check, two
+        // chains of packed adds); partial vectors and a lone last one singly
+        float lm = NEG_INF, ls = 0.f;
+        auto fold1 = [&](int j) {
             const uint4 q = ch.v[j];
+            float x[EPV];
+            dt_vec_vals<T>(q, x);
             if (j >= full_lo && j < full_hi) {
-                lmax = fmaxf(lmax, dt_vec_max<T>(q));
+                dt_online_add<EPV>(x, dt_vec_max<T>(q), lm, ls);
             } else {
-                T e[EPV];
-                ch.unpack(q, e);
+                float vm = NEG_INF;
 #pragma unroll
                 for (int s = 0; s < EPV; ++s) {
                     const int idx = j * EPV + s - ch.h;
-                    if (idx >= 0 && idx < ch.n) lmax = fmaxf(lmax, E::val(e[s]));
+                    if (idx >= 0 && idx < ch.n) vm = fmaxf(vm, x[s]);
+                    else x[s] = NEG_INF;
+                }
+                dt_online_add<EPV>(x, vm, lm, ls);
+            }
+        };
+        {
+            int j = v0 + lane;
+            for (; j + 32 < v1; j += 64) {
+                if (j >= full_lo && j + 32 < full_hi) {
+                    const uint4 qa = ch.v[j], qb = ch.v[j + 32];
+                    float x[2 * EPV];
+                    dt_vec_vals<T>(qa, *reinterpret_cast<float(*)[EPV]>(x));
+                    dt_vec_vals<T>(qb, *reinterpret_cast<float(*)[EPV]>(x + EPV));
+                    dt_online_add<2 * EPV>(x, fmaxf(dt_vec_max<T>(qa), dt_vec_max<T>(qb)), lm, ls);
+                } else {
+                    fold1(j);
+                    fold1(j + 32);
                 }
             }
+            if (j < v1) fold1(j);
         }
         const bool has = v0 + lane < v1;  // every vector holds at least one element
-        const float wmax = dt_warp_max(lmax);
+        // the chunk maximum first; then every lane scales its sum to it (one
+        // exponential per lane, all in parallel) and the sums are plain adds
+        const float wmax = dt_warp_max(lm);
         if (lane == 0) misc->red_f[wid] = wmax;
         __syncthreads();
         float m_c = NEG_INF;
 #pragma unroll
         for (int w = 0; w < NW; ++w) m_c = fmaxf(m_c, misc->red_f[w]);
+        const float log2e = 1.44269504088896340736f;
+        const float scaled = (lm == NEG_INF) ? 0.f : __fmul_rn(ls, dt_ex2_approx(__fmul_rn(__fsub_rn(lm, m_c), log2e)));
+        const float wsum = dt_warp_sum(scaled);
+        if (lane == 0) misc->red_s[wid] = wsum;
         const bool any = ch.n > 0;
         const uint32_t mk16 = any ? (E::key(dt_to_elem<T>(m_c)) >> (E::KB - 16)) : 0u;
-        const bool finite_max = (m_c != NEG_INF);
-        if (has) {
-            const uint32_t bn = mk16 - (E::key(dt_to_elem<T>(lmax)) >> (E::KB - 16));
-            if (bn < 256u) atomicAdd(&chist[bn], 1u);
+        {
+            // lane maxima into the histogram: one atomic per distinct bin of a warp
+            const uint32_t bn = has ? mk16 - (E::key(dt_to_elem<T>(lm)) >> (E::KB - 16)) : 0xFFFFFFFFu;
+            const uint32_t same = __match_any_sync(0xffffffffu, bn);
+            if (bn < 256u && lane == __ffs(same) - 1) atomicAdd(&chist[bn], (uint32_t)__popc(same));
         }
-        if (tid == 0) {
-            misc->m = m_c;
-            misc->mk16 = mk16;
-        }
-        __syncthreads();
-        cluster.sync();
-
-        // ---- exchange 1: a lower bound for the Kc-th logit from the lane maxima
+        __syncthreads();  // red_s and the histogram are complete
         if (tid < S) {
-            const Kn1Misc* r = cluster.map_shared_rank(misc, tid);
-            misc->cm[tid] = r->m;
-            misc->cmk[tid] = r->mk16;
+            // the chunk's (max, sum) with the timeout flag, pushed to every CTA
+            float cs = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) cs += misc->red_s[w];
+            *cluster.map_shared_rank(&misc->pin[c], tid) = Kn1Stat{m_c, cs, mk16, misc->timeout};
         }
+        // push the histogram into slot c of every CTA's hin
+        for (int i = tid; i < S * 256; i += NT) cluster.map_shared_rank(hin, i >> 8)[c * 256 + (i & 255)] = chist[i & 255];
+        cluster.sync();  // barrier 1: every CTA holds every CTA's statistics and histogram
+
+        // ---- exchange (local): the bound from the lane maxima; the row's normaliser
+        if (tid < S) misc->cmk[tid] = misc->pin[tid].mk16;
         __syncthreads();
         uint32_t Mk16 = 0;
         for (int j = 0; j < S; ++j) Mk16 = max(Mk16, misc->cmk[j]);
-        merge_framed(cluster, chist, S, misc->cmk, Mk16, g);
+        merge_framed_local(hin, S, misc->cmk, Mk16, g);
         dt_find_bin<false>(g, Kc, &misc->bs);
         float bound = NEG_INF;
         if (misc->bs.digit >= 0) {
@@ -293,17 +358,20 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
             // smallest value whose key has these top bits (keys <= 127 are -inf or NaN)
             if (b16 > 127u) bound = E::key_val(b16 << (E::KB - 16));
         }
+        if (tid == 0) {
+            float M = misc->pin[0].m;
+            for (int j = 1; j < S; ++j) M = fmaxf(M, misc->pin[j].m);
+            float ssum = 0.f;
+            for (int j = 0; j < S; ++j)
+                if (misc->pin[j].m != NEG_INF) ssum += misc->pin[j].s * __expf(misc->pin[j].m - M);
+            misc->lse = M + logf(ssum);
+        }
 
-        // ---- pass 2: sum exp(x - max); candidates at or above the bound ----
-        const float log2e = 1.44269504088896340736f;
-        const unsigned long long m2 = dt_f2_pack(m_c, m_c), l2 = dt_f2_pack(log2e, log2e);
-        unsigned long long acc = dt_f2_pack(0.f, 0.f);
-        float sum = 0.f;
+        // ---- pass 2: candidates at or above the bound -----------------------
         for (int j = v0 + lane; j < v1; j += 32) {
             const uint4 q = ch.v[j];
             float x[EPV];
             if (j >= full_lo && j < full_hi) {
-                if (finite_max) acc = dt_vec_expsum<T>(q, m2, l2, acc);
                 if (dt_vec_max<T>(q) >= bound) {
                     dt_vec_vals<T>(q, x);
 #pragma unroll
@@ -321,75 +389,38 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
 #pragma unroll
                 for (int s = 0; s < EPV; ++s) {
                     const int idx = j * EPV + s - ch.h;
-                    if (idx >= 0 && idx < ch.n) {
-                        if (finite_max) sum += dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], m_c), log2e));
-                        if (x[s] >= bound) {
-                            const int slot = atomicAdd(&mp->ncand, 1);
-                            if (slot < CCAP)
-                                cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
-                                             (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
-                        }
+                    if (idx >= 0 && idx < ch.n && x[s] >= bound) {
+                        const int slot = atomicAdd(&mp->ncand, 1);
+                        if (slot < CCAP)
+                            cand[slot] = ((unsigned long long)E::key(dt_to_elem<T>(x[s])) << 32) |
+                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(lo + idx));
                     }
                 }
             }
         }
-        {
-            float a0, a1;
-            dt_f2_unpack(acc, a0, a1);
-            sum += a0 + a1;
-        }
-        sum = dt_warp_sum(sum);
-        if (lane == 0) misc->red_s[wid] = sum;
         __syncthreads();
-        if (tid == 0) {
-            float a = 0.f;
-            for (int i = 0; i < NW; ++i) a += misc->red_s[i];
-            mp->s = a;
-        }
+        // append this CTA's candidates to every CTA's row list; a CTA that found
+        // more than it keeps adds a count that marks every list as overflowing
+        const int nloc = mp->ncand;
+        const int npush = nloc > CCAP ? 0 : nloc;
+        if (tid < S) misc->pbase[tid] = atomicAdd(cluster.map_shared_rank(&misc->nrecv, tid), nloc > CCAP ? ACAP + 1 : nloc);
         __syncthreads();
-        cluster.sync();
+        for (int i = tid; i < S * npush; i += NT) {
+            const int d = i / npush, k = i - d * npush;
+            const int at = misc->pbase[d] + k;
+            if (at < ACAP) cluster.map_shared_rank(all, d)[at] = cand[k];
+        }
+        cluster.sync();  // barrier 2: every list complete
 
-        // ---- exchange 2: normaliser and candidate counts --------------------
-        if (tid < S) {
-            const RowPub* r = &cluster.map_shared_rank(misc, tid)->pub[par];
-            misc->cs[tid] = r->s;
-            misc->cnc[tid] = r->ncand;
-            misc->cto[tid] = r->timeout;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            float M = misc->cm[0];
-            for (int j = 1; j < S; ++j) M = fmaxf(M, misc->cm[j]);
-            float ssum = 0.f;
-            for (int j = 0; j < S; ++j)
-                if (misc->cm[j] != NEG_INF) ssum += misc->cs[j] * __expf(misc->cm[j] - M);
-            misc->lse = M + logf(ssum);
-        }
-        // every CTA sees the same counts, so the branch below is uniform across
-        // the cluster (it holds cluster barriers)
-        int total = 0;
-        bool overflow = false;
-        for (int j = 0; j < S; ++j) {
-            total += misc->cnc[j];
-            overflow |= misc->cnc[j] > CCAP;
-        }
-        overflow |= total > ACAP;
-        __syncthreads();
+        // every CTA received every CTA's count, so the branch below is uniform
+        // across the cluster (the fallback holds cluster barriers)
+        const int total = misc->nrecv;
         const float lse = misc->lse;
-
-        if (!overflow) {
-            // ---- gather every CTA's candidates (one warp per partner) -------
-            for (int j = wid; j < S; j += NW) {
-                int off = 0;
-                for (int q = 0; q < j; ++q) off += misc->cnc[q];
-                const unsigned long long* rs = cluster.map_shared_rank(cand, j);
-                const int cnt = misc->cnc[j];
-                for (int i = lane; i < cnt; i += 32) all[off + i] = rs[i];
-            }
-            __syncthreads();
+        if (total <= ACAP) {
             if (total > DT_SORT_MIN) dt_sort_and_write<T, NT>(all, total, Kc, c, S, lse, row, cand_id, cand_lp);
-            else dt_rank_and_write<T, NT>(cand, misc->cnc[c], all, total, Kc, lse, row, cand_id, cand_lp);
+            else dt_rank16_and_write<T, NT>(cand, nloc, all, total, Kc, lse, row, cand_id, cand_lp);
         } else {
+            fallback_taken = true;
             // ---- fallback: window histogram over all keys, exact radix select
             uint32_t* whist = (uint32_t*)all;  // per-warp histograms
             uint32_t* myh = whist + wid * 256;
@@ -587,7 +618,7 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
         }
         if (c == 0 && tid == 0) {
             int to = 0;
-            for (int j = 0; j < S; ++j) to |= misc->cto[j];
+            for (int j = 0; j < S; ++j) to |= misc->pin[j].timeout;
             lse_out[row] = to ? __int_as_float(0x7FC00000) : lse;
         }
         // the next row's copy starts once every read of this one is done
@@ -597,9 +628,12 @@ __global__ void __launch_bounds__(NT, 2) kn1_kernel(const T* __restrict__ logits
             issue(nxt);
         }
     }
-    // partners may still be gathering from this CTA's shared memory
-    __syncthreads();
-    cluster.sync();
+    // after a fallback, partners may still be gathering from this CTA's
+    // shared memory (every CTA took the same rows down the same branches)
+    if (fallback_taken) {
+        __syncthreads();
+        cluster.sync();
+    }
 }
 
 }  // namespace

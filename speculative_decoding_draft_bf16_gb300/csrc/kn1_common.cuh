@@ -3,6 +3,67 @@
 
 #include "dt_device.cuh"
 
+// Folds a vector (values x, maximum vm) into a running (max M, sum S of
+// exp(x - M)).  For |M| < 64 each term is exp2(x * log2e - c) with c = M *
+// log2e rounded, one fused multiply-add: c's rounding error (<= 2^-18) is a
+// factor common to all terms, shifting the log-normaliser by < 3e-6.  Larger
+// maxima round x - M first, so that an element equal to M adds exactly 1 at
+// any magnitude.
+template <int EPV>
+DT_DI void dt_online_add(const float (&x)[EPV], float vm, float& M, float& S) {
+    const float NEG_INF = -__int_as_float(0x7F800000);
+    const float log2e = 1.44269504088896340736f;
+    if (vm > M) {
+        S = (M == NEG_INF) ? 0.f : __fmul_rn(S, dt_ex2_approx(__fmul_rn(__fsub_rn(M, vm), log2e)));
+        M = vm;
+    }
+    if (fabsf(M) < 64.f) {
+        // two lanes per packed f32x2 instruction; with 8 or more elements two
+        // independent accumulators shorten the dependent chain
+        const float c = __fmul_rn(M, log2e);
+        const unsigned long long l2 = dt_f2_pack(log2e, log2e), c2 = dt_f2_pack(-c, -c);
+        unsigned long long acc[2] = {dt_f2_pack(0.f, 0.f), dt_f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int s = 0; s < EPV; s += 2) {
+            float d0, d1;
+            dt_f2_unpack(dt_f2_fma(dt_f2_pack(x[s], x[s + 1]), l2, c2), d0, d1);
+            unsigned long long& a = acc[EPV >= 8 ? (s >> 1) & 1 : 0];
+            a = dt_f2_add(a, dt_f2_pack(dt_ex2_approx(d0), dt_ex2_approx(d1)));
+        }
+        float a0, a1;
+        dt_f2_unpack(EPV >= 8 ? dt_f2_add(acc[0], acc[1]) : acc[0], a0, a1);
+        S = __fadd_rn(S, __fadd_rn(a0, a1));
+        return;
+    }
+    if (M == NEG_INF) return;  // every element so far is -inf
+    float e[EPV];
+#pragma unroll
+    for (int s = 0; s < EPV; ++s) e[s] = dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], M), log2e));
+#pragma unroll
+    for (int w = EPV / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int s = 0; s < w; ++s) e[s] = __fadd_rn(e[s], e[s + w]);
+    S = __fadd_rn(S, e[0]);
+}
+
+// Merges a running (max M2, sum S2 of exp(x - M2)) into (M, S).
+DT_DI void dt_online_merge(float& M, float& S, float M2, float S2) {
+    const float NEG_INF = -__int_as_float(0x7F800000);
+    const float log2e = 1.44269504088896340736f;
+    if (M2 == NEG_INF) return;
+    if (M == NEG_INF) {
+        M = M2;
+        S = S2;
+        return;
+    }
+    if (M2 > M) {
+        S = __fadd_rn(__fmul_rn(S, dt_ex2_approx(__fmul_rn(__fsub_rn(M, M2), log2e))), S2);
+        M = M2;
+    } else {
+        S = __fadd_rn(S, __fmul_rn(S2, dt_ex2_approx(__fmul_rn(__fsub_rn(M2, M), log2e))));
+    }
+}
+
 // Shared-memory scratch of dt_find_bin.
 struct DtBinSearch {
     int wsum[8];
@@ -59,6 +120,27 @@ DT_DI void dt_rank_and_write(const unsigned long long* own, int mine, const unsi
         for (int q = lane; q < total; q += 32) rank += (all[q] > key);
         rank = dt_warp_sum_i(rank);
         if (lane == 0 && rank < Kc) dt_write_cand<T>(key, rank, Kc, lse, row, cand_id, cand_lp);
+    }
+}
+
+// The same with sixteen threads per entry (each counts a stride-16 slice of
+// `all`, then a 4-step reduction within the half-warp): more entries in flight
+// than one warp per entry when the lists are short.
+template <typename T, int NT>
+DT_DI void dt_rank16_and_write(const unsigned long long* own, int mine, const unsigned long long* all, int total,
+                               int Kc, float lse, int row, int32_t* cand_id, float* cand_lp) {
+    const int sub = threadIdx.x & 15, grp = threadIdx.x >> 4;
+    const int rounds = (mine + NT / 16 - 1) / (NT / 16);
+    for (int rd = 0; rd < rounds; ++rd) {  // uniform trip count: every lane reaches the shuffles
+        const int i = grp + rd * (NT / 16);
+        const bool live = i < mine;
+        const unsigned long long key = live ? own[i] : ~0ull;
+        int rank = 0;
+        if (live)
+            for (int q = sub; q < total; q += 16) rank += (all[q] > key);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (live && sub == 0 && rank < Kc) dt_write_cand<T>(key, rank, Kc, lse, row, cand_id, cand_lp);
     }
 }
 

@@ -75,48 +75,6 @@ DT_DI uint4 ldv(const T* row, int v) {
     return __ldg(reinterpret_cast<const uint4*>(row) + v);
 }
 
-// Folds a vector (values x, maximum vm) into a running (max M, sum S of
-// exp(x - M)).  For |M| < 64 each term is exp2(x * log2e - c) with c = M *
-// log2e rounded, one fused multiply-add: c's rounding error (<= 2^-18) is a
-// factor common to all terms, shifting the log-normaliser by < 3e-6.  Larger
-// maxima round x - M first, so that an element equal to M adds exactly 1 at
-// any magnitude.
-template <int EPV>
-DT_DI void online_add(const float (&x)[EPV], float vm, float& M, float& S) {
-    const float NEG_INF = -__int_as_float(0x7F800000);
-    const float log2e = 1.44269504088896340736f;
-    if (vm > M) {
-        S = (M == NEG_INF) ? 0.f : __fmul_rn(S, dt_ex2_approx(__fmul_rn(__fsub_rn(M, vm), log2e)));
-        M = vm;
-    }
-    if (fabsf(M) < 64.f) {
-        // two lanes per packed f32x2 instruction; with 8 or more elements two
-        // independent accumulators shorten the dependent chain
-        const float c = __fmul_rn(M, log2e);
-        const unsigned long long l2 = dt_f2_pack(log2e, log2e), c2 = dt_f2_pack(-c, -c);
-        unsigned long long acc[2] = {dt_f2_pack(0.f, 0.f), dt_f2_pack(0.f, 0.f)};
-#pragma unroll
-        for (int s = 0; s < EPV; s += 2) {
-            float d0, d1;
-            dt_f2_unpack(dt_f2_fma(dt_f2_pack(x[s], x[s + 1]), l2, c2), d0, d1);
-            unsigned long long& a = acc[EPV >= 8 ? (s >> 1) & 1 : 0];
-            a = dt_f2_add(a, dt_f2_pack(dt_ex2_approx(d0), dt_ex2_approx(d1)));
-        }
-        float a0, a1;
-        dt_f2_unpack(EPV >= 8 ? dt_f2_add(acc[0], acc[1]) : acc[0], a0, a1);
-        S = __fadd_rn(S, __fadd_rn(a0, a1));
-        return;
-    }
-    if (M == NEG_INF) return;  // every element so far is -inf
-    float e[EPV];
-#pragma unroll
-    for (int s = 0; s < EPV; ++s) e[s] = dt_ex2_approx(__fmul_rn(__fsub_rn(x[s], M), log2e));
-#pragma unroll
-    for (int w = EPV / 2; w > 0; w >>= 1)
-#pragma unroll
-        for (int s = 0; s < w; ++s) e[s] = __fadd_rn(e[s], e[s + w]);
-    S = __fadd_rn(S, e[0]);
-}
 
 // (M, S) <- the merge of two running (max, sum) pairs.
 DT_DI void merge_pair(float& M, float& S, float M2, float S2) {
@@ -311,14 +269,14 @@ __global__ void __launch_bounds__(NT, RING > 8 ? 1 : 2) kn1b_kernel(const T* __r
                             float x[2 * EPV];
                             dt_vec_vals<T>(qa, *reinterpret_cast<float(*)[EPV]>(x));
                             dt_vec_vals<T>(qb, *reinterpret_cast<float(*)[EPV]>(x + EPV));
-                            online_add<2 * EPV>(x, fmaxf(va, vb), M, S);
+                            dt_online_add<2 * EPV>(x, fmaxf(va, vb), M, S);
                         } else {  // the thread's last vector, on its own
                             const uint4 q = ring[(rbase + u) * NT];
                             const float vm = dt_vec_max<T>(q);
                             gm[u] = fmaxf(gm[u], vm);
                             float x[EPV];
                             dt_vec_vals<T>(q, x);
-                            online_add<EPV>(x, vm, M, S);
+                            dt_online_add<EPV>(x, vm, M, S);
                         }
                     }
                 }
@@ -338,7 +296,7 @@ __global__ void __launch_bounds__(NT, RING > 8 ? 1 : 2) kn1b_kernel(const T* __r
             }
             gm[0] = fmaxf(gm[0], vm);
             gv |= 1u;
-            online_add<EPV>(x, vm, M, S);
+            dt_online_add<EPV>(x, vm, M, S);
         }
         for (int o = 16; o > 0; o >>= 1) {
             const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
