@@ -464,10 +464,11 @@ static dt_status verify_impl(const dt_tree* t, int32_t batch, int32_t V, int32_t
         [&](int q) {
             // the residual-per-sibling rule wants clusters whose chunks leave room for its cache
             const int chunk = chunk_of(V, q, dtype);
-            return dt_kn6_smem_bytes(chunk, esize, Mmax, rule) + 1024 <= kSmemMax &&
+            return chunk <= kChunkMax && dt_kn6_smem_bytes(chunk, esize, Mmax, rule) + 1024 <= kSmemMax &&
                    (rule != DT_VERIFY_ITER_RESIDUAL || dt_kn6_pq_cache(chunk, esize, Mmax, rule));
         },
-        [&](int q, int chunk) { return max_clusters(6, dtype, q, chunk, Mmax * 8 + rule); });
+        [&](int q, int chunk) { return max_clusters(6, dtype, q, chunk, Mmax * 8 + rule); },
+        rule == DT_VERIFY_ITER_RESIDUAL);  // its cache leaves one CTA per SM: any cluster size that fits
     const int chunk = chunk_of(V, s, dtype);
     if (chunk > kChunkMax || dt_kn6_smem_bytes(chunk, esize, Mmax, rule) + 1024 > kSmemMax) return DT_ERR_UNSUPPORTED;
     cudaError_t e = dt_kn6_launch(batch, t->L, V, dtype, t->max_nodes, s, chunk, rule, t->node_tok, t->parent,

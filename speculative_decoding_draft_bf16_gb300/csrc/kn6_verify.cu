@@ -68,9 +68,16 @@ struct Kn6Misc {
     unsigned long long best_kid;
     float xm[SMAX];               // partners' published values, copied through DSMEM
     float xs[SMAX];
-    unsigned long long xu[SMAX];
-    unsigned long long xw[SMAX];
+    unsigned long long xu[SMAX];  // greedy: partners' argmax keys
+    // residual and mass sums of every CTA of the cluster, pushed by each into
+    // slot c of every CTA before a cluster barrier; two buffers by exchange parity
+    unsigned long long su[2][SMAX];
+    unsigned long long sw[2][SMAX];
+    int nkid;                     // children of the node whose residual loop runs
+    int scan[NW];                 // per-warp totals of a block scan
 };
+constexpr size_t MISC_BYTES = 2048;
+static_assert(sizeof(Kn6Misc) <= MISC_BYTES, "misc block overflows its slot");
 
 DT_DI unsigned long long warp_max_u64(unsigned long long v) {
     for (int o = 16; o > 0; o >>= 1) {
@@ -93,6 +100,12 @@ DT_DI unsigned long long warp_incl_scan_u64(unsigned long long v) {
 DT_DI unsigned long long resid_w(unsigned long long P, unsigned long long Q, unsigned long long T) {
     const unsigned long long s = ((Q * T) >> 32) | (__umul64hi(Q, T) << 32);
     return P > s ? P - s : 0ull;
+}
+// The same for 32-bit P and Q (Q < 2^32), T split as Th * 2^32 + Tl:
+// floor(Q * T / 2^32) = Q * Th + floor(Q * Tl / 2^32), two 32 x 32 -> 64-bit products.
+DT_DI unsigned long long resid_w32(uint32_t P, uint32_t Q, uint32_t Th, uint32_t Tl) {
+    const unsigned long long s = (unsigned long long)Q * Th + (((unsigned long long)Q * Tl) >> 32);
+    return (unsigned long long)P > s ? (unsigned long long)P - s : 0ull;
 }
 
 // Test of a child against the residual with weights W (sum S):
@@ -198,7 +211,7 @@ __device__ long long g_kn6_probe;
 // One instantiation per acceptance rule (RULE = DT_VERIFY_*), so that each
 // walk carries only its own code; CORR: the ratio rule against q~.
 template <typename T, int RULE, bool CORR>
-__global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, int Mmax, int chunk, int nbt, int pq_on,
+__global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, int Mmax, int chunk, int nbt, int pq_cap,
                                                  const int32_t* __restrict__ g_tok,
                                                  const int32_t* __restrict__ g_par,
                                                  const int32_t* __restrict__ g_dep,
@@ -224,7 +237,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
     const int nch = hi - lo;
 
     Kn6Misc* misc = (Kn6Misc*)smem;
-    int* s_tok = (int*)(smem + 1024);
+    int* s_tok = (int*)(smem + MISC_BYTES);
     int* s_par = s_tok + Mmax;
     int* s_dep = s_par + Mmax;
     int* s_rank = s_dep + Mmax;
@@ -234,8 +247,11 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
     const int DB = nbt;           // index of the drafter buffer
 
     Rows<T> rows;
-    rows.init(smem + 1024 + tree_bytes, (int)(((size_t)chunk * sizeof(T) + 16 + 127) & ~(size_t)127), misc->bar,
-              &misc->probe, g_kn6_probe);
+    // the residual-per-sibling rule keeps its ordered children before the row
+    // buffers, so that its pair cache may take the buffers' place
+    const size_t kids_bytes = RULE == DT_VERIFY_ITER_RESIDUAL ? (((size_t)Mmax * 24) + 127) & ~(size_t)127 : 0;
+    rows.init(smem + MISC_BYTES + tree_bytes + kids_bytes,
+              (int)(((size_t)chunk * sizeof(T) + 16 + 127) & ~(size_t)127), misc->bar, &misc->probe, g_kn6_probe);
 
     if (tid == 0) {
         for (int i = 0; i < NBMAX; ++i) dt_mbar_init(&misc->bar[i], 1);
@@ -513,7 +529,6 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
             const float lpq = proposal_lp(dv, draft_lse[(size_t)b * L + pos], tk);
             return u0[i] < dt_exp_canon(__fsub_rn(lpt, lpq));
         };
-        unsigned long long prev_key = 0;  // one residual per sibling: the last child tested
         if (!greedy) {
             if (c == 0 && tid == 0 && visited_lse) visited_lse[(size_t)b * (L + 1) + len] = lse_t;
             if (uses_q) {
@@ -531,8 +546,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
                 const unsigned long long bk = misc->best_kid;
                 if (rule == DT_VERIFY_RATIO) {
                     child = (bk == ~0ull) ? -1 : (int)(bk & 0xFFFFFFFFull);
-                } else if (bk != ~0ull) {
-                    prev_key = bk;
+                } else if (bk != ~0ull) {  // the first child in test order
                     if (ratio_accepts((int)(bk & 0xFFFFFFFFull))) child = (int)(bk & 0xFFFFFFFFull);
                 }
             }
@@ -563,13 +577,17 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
         const int e0 = min(nch, tid * run), e1 = min(nch, e0 + run);
         unsigned long long Tq = 1ull << 32;  // residual weights max(0, P - floor(Q * Tq / 2^32))
         unsigned long long rR = 0, rP = 0, totR = 0;
-        // one residual per sibling: the run's (P, Q) are kept in shared memory
-        // (32 bits each; a 2^32 mass -- a one-hot row -- sends the CTA back to
-        // recomputing them) and a bit mask marks the elements whose weight is
-        // still positive, which is all a later pass visits (weights only fall)
-        const bool cache = pq_on && rule == DT_VERIFY_ITER_RESIDUAL && resid && run <= 64;
-        uint2* pq = (uint2*)(smem + 1024 + tree_bytes + (size_t)(nbt + 1) * rows.stride);
-        unsigned long long alive = 0;
+        // one residual per sibling: the CTA keeps the (P, Q) pairs whose weight
+        // is still positive, 32 bits each, every thread its own in a segment
+        // of pq (sized by a scan of the threads' counts), and drops a pair once
+        // its weight reaches 0 (weights only fall as T grows).  The cache takes
+        // the place of the staged rows, which from then on are read from
+        // global memory (the fill, a recompute, the draw).  When the pairs do
+        // not fit (pq_cap pairs), or the CTA holds a 2^32 mass (a one-hot row),
+        // every step recomputes the runs instead.
+        const bool iter = rule == DT_VERIFY_ITER_RESIDUAL && resid;
+        uint2* pq = (uint2*)(smem + MISC_BYTES + tree_bytes + kids_bytes);  // over the row buffers
+        int na = 0;
         bool sat = false;
         for (int e = e0; e < e1; ++e) {
             const unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
@@ -578,73 +596,145 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
                 const unsigned long long Q = dt_fixed32(dt_exp_canon(proposal_lp(E::val(y[e]), lse_d, lo + e)));
                 const unsigned long long w = P > Q ? P - Q : 0ull;
                 rR += w;
-                if (cache) {
-                    pq[e] = make_uint2((uint32_t)P, (uint32_t)Q);
+                if (iter && w) {
                     sat |= ((P | Q) >> 32) != 0;
-                    if (w) alive |= 1ull << (e - e0);
+                    na += Q != 0;  // Q = 0: the weight stays P at every T (summed once, below)
                 }
             }
         }
-        const bool use_pq = cache && !__syncthreads_or(sat);
+        bool use_pq = false;
+        int seg = 0;                   // this thread's first pair in pq
+        unsigned long long rconst = 0;  // cached mode: the weights of the run's Q = 0 elements
+        if (iter && pq_cap > 0 && !__syncthreads_or(sat)) {
+            // exclusive scan of the pair counts; cache only if the CTA's fit
+            const int inc = dt_warp_incl_scan(na);
+            if (lane == 31) misc->scan[wid] = inc;
+            __syncthreads();
+            int before = 0, total = 0;
+            for (int w = 0; w < NW; ++w) {
+                if (w < wid) before += misc->scan[w];
+                total += misc->scan[w];
+            }
+            seg = before + inc - na;
+            use_pq = total <= pq_cap;
+            __syncthreads();  // every thread has read scan and is done with the staged rows
+            if (use_pq) {
+                x = trow_of(n) + lo;  // the rows again, from global memory
+                y = drow_of(s_dep[n]) + lo;
+                int j = seg;
+                for (int e = e0; e < e1; ++e) {
+                    const unsigned long long P = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(x[e]), lse_t)));
+                    const unsigned long long Q = dt_fixed32(dt_exp_canon(proposal_lp(E::val(y[e]), lse_d, lo + e)));
+                    if (P > Q) {
+                        if (Q) pq[j++] = make_uint2((uint32_t)P, (uint32_t)Q);
+                        else rconst += P;
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        // the node's children in test order (rank, then index), with the masses
+        // and uniforms of their tests, once per node
+        unsigned long long* kidP = (unsigned long long*)(smem + MISC_BYTES + tree_bytes);
+        unsigned long long* kidQ = kidP + Mmax;
+        int* kidI = (int*)(kidQ + Mmax);
+        float* kidU = (float*)(kidI + Mmax);
+        int nk = 0;
+        if (iter) {
+            int* unord = (int*)kidQ;  // the children gathered in any order (kidQ is filled after)
+            if (tid == 0) misc->nkid = 0;
+            __syncthreads();
+            for (int i = 1 + tid; i < M; i += NT)
+                if (s_par[i] == n) unord[atomicAdd(&misc->nkid, 1)] = i;
+            __syncthreads();
+            nk = misc->nkid;
+            for (int q = tid; q < nk; q += NT) {
+                const int i = unord[q];
+                const unsigned long long ki = kid_key(i);
+                int pos = 0;
+                for (int r = 0; r < nk; ++r) pos += kid_key(unord[r]) < ki;
+                kidI[pos] = i;
+            }
+            __syncthreads();  // the order is complete and the gathered list no longer read
+            const float dl = draft_lse[(size_t)b * L + s_dep[n]];
+            for (int q = tid; q < nk; q += NT) {
+                const int i = kidI[q], tk = s_tok[i];
+                kidP[q] = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(trow_of(n)[tk]), lse_t)));
+                kidQ[q] = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(drow_of(s_dep[n])[tk]), dl)));
+                kidU[q] = u0[i];
+            }
+            __syncthreads();
+        }
+        // cluster-wide sums of the threads' run sums: each CTA pushes its sum
+        // into slot c of every CTA (parity k & 1), one barrier, local adds
+        auto cluster_sum = [&](unsigned long long v, unsigned long long w, bool with_w) {
+            const unsigned long long sv = dt_warp_sum_u64(v), sw = with_w ? dt_warp_sum_u64(w) : 0ull;
+            if (lane == 0) {
+                misc->red_u[wid] = sv;
+                misc->red_w[wid] = sw;
+            }
+            __syncthreads();
+            if (wid == 0) {
+                unsigned long long av = lane < NW ? misc->red_u[lane] : 0ull;
+                unsigned long long aw = (with_w && lane < NW) ? misc->red_w[lane] : 0ull;
+                av = dt_warp_sum_u64(av);
+                aw = dt_warp_sum_u64(aw);
+                if (lane < S) {
+                    Kn6Misc* r = cluster.map_shared_rank(misc, lane);
+                    r->su[k & 1][c] = av;
+                    if (with_w) r->sw[k & 1][c] = aw;
+                }
+            }
+            cluster.sync();
+            ++k;
+        };
         child = -1;
+        int kpos = 1;  // the first child was tested against p above
+        const unsigned long long* swp = nullptr;  // the CTAs' P sums (first exchange)
         for (bool first = true;; first = false) {
             if (!first) {  // a later residual: T has grown
                 rR = 0;
                 if (use_pq) {
-                    for (unsigned long long m = alive; m; m &= m - 1) {
-                        const int j = __ffsll((long long)m) - 1;
-                        const uint2 v = pq[e0 + j];
-                        const unsigned long long w = resid_w(v.x, v.y, Tq);
-                        rR += w;
-                        if (!w) alive &= ~(1ull << j);
+                    // four pairs per step (independent loads and products); the
+                    // survivors are written back in order to the segment's front
+                    const uint32_t Th = (uint32_t)(Tq >> 32), Tl = (uint32_t)Tq;
+                    rR = rconst;
+                    int keep = 0, j = 0;
+                    for (; j + 4 <= na; j += 4) {
+                        const uint2 v0 = pq[seg + j], v1 = pq[seg + j + 1], v2 = pq[seg + j + 2], v3 = pq[seg + j + 3];
+                        const unsigned long long w0 = resid_w32(v0.x, v0.y, Th, Tl), w1 = resid_w32(v1.x, v1.y, Th, Tl);
+                        const unsigned long long w2 = resid_w32(v2.x, v2.y, Th, Tl), w3 = resid_w32(v3.x, v3.y, Th, Tl);
+                        rR += (w0 + w1) + (w2 + w3);
+                        if (w0) pq[seg + keep++] = v0;
+                        if (w1) pq[seg + keep++] = v1;
+                        if (w2) pq[seg + keep++] = v2;
+                        if (w3) pq[seg + keep++] = v3;
                     }
+                    for (; j < na; ++j) {
+                        const uint2 v = pq[seg + j];
+                        const unsigned long long w = resid_w32(v.x, v.y, Th, Tl);
+                        rR += w;
+                        if (w) pq[seg + keep++] = v;
+                    }
+                    na = keep;
                 } else {
                     for (int e = e0; e < e1; ++e)
                         rR += mass(E::val(x[e]), lse_t, true, E::val(y[e]), lse_d, Tq);
                 }
             }
-            {
-                const unsigned long long sR = dt_warp_sum_u64(rR), sP = dt_warp_sum_u64(rP);
-                if (lane == 0) { misc->red_u[wid] = sR; misc->red_w[wid] = sP; }
-            }
-            __syncthreads();
-            if (tid == 0) {
-                unsigned long long aR = 0, aP = 0;
-                for (int w = 0; w < NW; ++w) { aR += misc->red_u[w]; aP += misc->red_w[w]; }
-                misc->pub[k & 1].u = aR;
-                misc->pub[k & 1].w = aP;
-            }
-            __syncthreads();
-            cluster.sync();
-            if (tid < S) {
-                const Pub* r = &cluster.map_shared_rank(misc, tid)->pub[k & 1];
-                misc->xu[tid] = r->u;
-                misc->xw[tid] = r->w;
-            }
-            __syncthreads();
-            ++k;
-            totR = 0;
-            for (int j = 0; j < S; ++j) totR += misc->xu[j];
-            if (rule != DT_VERIFY_ITER_RESIDUAL || !resid || totR == 0) break;
+            cluster_sum(rR, rP, first);
+            const unsigned long long* su = misc->su[(k - 1) & 1];
+            if (first) swp = misc->sw[(k - 1) & 1];
+            totR = dt_warp_sum_u64(lane < S ? su[lane] : 0ull);  // the S partials, loaded in parallel
+            if (!iter || totR == 0 || kpos >= nk) break;
             // the next child in test order, against the residual just summed
-            if (tid == 0) misc->best_kid = ~0ull;
-            __syncthreads();
-            for (int i = 1 + tid; i < M; i += NT)
-                if (s_par[i] == n && kid_key(i) > prev_key) atomicMin(&misc->best_kid, kid_key(i));
-            __syncthreads();
-            const unsigned long long bk = misc->best_kid;
-            if (bk == ~0ull) break;  // every child rejected: draw from this residual
-            prev_key = bk;
-            const int ci = (int)(bk & 0xFFFFFFFFull);
-            const int tk = s_tok[ci];
-            const unsigned long long Pc = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(trow_of(n)[tk]), lse_t)));
-            const unsigned long long Qc = dt_fixed32(dt_exp_canon(__fsub_rn(E::val(drow_of(s_dep[n])[tk]), lse_d)));
-            if (resid_accepts(u0[ci], Qc, totR, resid_w(Pc, Qc, Tq))) {
-                child = ci;
+            // (every thread takes the same decision from the same values)
+            if (resid_accepts(kidU[kpos], kidQ[kpos], totR, resid_w(kidP[kpos], kidQ[kpos], Tq))) {
+                child = kidI[kpos];
                 break;
             }
+            ++kpos;
             Tq += totR;
-            __syncthreads();  // every thread has read best_kid and xu
         }
         if (child >= 0) {
             descend(child);
@@ -654,7 +744,7 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
         // the residual, or P where the residual is empty (or the node has no
         // children, or the rule draws from the target)
         const bool use_r = resid && totR > 0;
-        const unsigned long long* sums = use_r ? misc->xu : misc->xw;
+        const unsigned long long* sums = use_r ? misc->su[(k - 1) & 1] : swp;
         unsigned long long tot = 0, before = 0, mine = 0;
         for (int j = 0; j < S; ++j) {
             const unsigned long long v = sums[j];
@@ -763,24 +853,34 @@ __global__ void __launch_bounds__(NT, 2) kn6_kernel(Kn6Corr corr, int L, int V, 
     cluster.sync();  // keep shared memory alive until every CTA finished its remote reads
 }
 
-// Shared-memory layout: misc (1 KB), tree, nbt target-row buffers and one
-// drafter-row buffer, and for the residual-per-sibling rule the (P, Q) cache
-// (8 bytes per chunk element) when it fits.  Two target buffers (prefetch of
-// the favourite child) when they fit, but the cache comes first.
+// Shared-memory layout: misc (2 KB), tree, nbt target-row buffers and one
+// drafter-row buffer.  For the residual-per-sibling rule: misc, tree, the
+// ordered children of a node with their test values (24 bytes per node), one
+// target-row and one drafter-row buffer, and over those buffers a cache of
+// `cap` (P, Q) pairs (8 bytes each) for the CTA's alive elements, up to the
+// chunk, within the shared memory.  Two target buffers (prefetch of the
+// favourite child) when they fit, for the other rules.
 struct Kn6Layout {
-    int nbt;
-    size_t pq, total;
+    int nbt, cap;
+    size_t total;
 };
 Kn6Layout kn6_layout(int chunk, int esize, int Mmax, int rule) {
     const size_t tree = (((size_t)Mmax * 24) + 127) & ~(size_t)127;
     const size_t buf = (((size_t)chunk * esize + 16 + 127) & ~(size_t)127);
-    const size_t pq = rule == DT_VERIFY_ITER_RESIDUAL ? (((size_t)chunk * 8 + 127) & ~(size_t)127) : 0;
-    const size_t cap = (size_t)226 * 1024;
-    auto total = [&](int nbt, size_t p) { return 1024 + tree + (size_t)(nbt + 1) * buf + p; };
-    if (pq && total(2, pq) <= cap) return Kn6Layout{2, pq, total(2, pq)};
-    if (pq && total(1, pq) <= cap) return Kn6Layout{1, pq, total(1, pq)};
-    const int nbt = total(2, 0) <= cap ? 2 : 1;
-    return Kn6Layout{nbt, 0, total(nbt, 0)};
+    const size_t room = (size_t)226 * 1024;
+    auto base = [&](int nbt) { return MISC_BYTES + tree + (size_t)(nbt + 1) * buf; };
+    if (rule != DT_VERIFY_ITER_RESIDUAL) {
+        const int nbt = base(2) <= room ? 2 : 1;
+        return Kn6Layout{nbt, 0, base(nbt)};
+    }
+    const size_t kids = (((size_t)Mmax * 24) + 127) & ~(size_t)127;
+    const size_t pre = MISC_BYTES + tree + kids;
+    const long long left = (long long)room - (long long)pre;
+    long long cap = left > 0 ? left / 8 : 0;
+    if (cap > chunk) cap = chunk;
+    if (cap < NT) cap = 0;  // too few to help: recompute
+    const size_t body = 2 * buf > (size_t)cap * 8 ? 2 * buf : (size_t)cap * 8;
+    return Kn6Layout{1, (int)cap, pre + body};
 }
 
 }  // namespace
@@ -794,7 +894,7 @@ size_t dt_kn6_smem_bytes(int chunk, int esize, int Mmax, int rule) {
 }
 
 int dt_kn6_pq_cache(int chunk, int esize, int Mmax, int rule) {
-    return kn6_layout(chunk, esize, Mmax, rule).pq > 0;
+    return kn6_layout(chunk, esize, Mmax, rule).cap;
 }
 
 // Sets the kernel's shared-memory and cluster-size attributes for a launch.
@@ -826,26 +926,26 @@ int kn6_max_clusters_rule(int rule, int S, size_t smem) {
 
 template <typename T, int RULE, bool CORR>
 cudaError_t kn6_launch_t(const DtLaunch& lc, size_t smem, int S, const Kn6Corr& corr, int L, int V, int Mmax,
-                         int chunk, int nbt, int pq_on, const int32_t* tok, const int32_t* parent,
+                         int chunk, int nbt, int pq_cap, const int32_t* tok, const int32_t* parent,
                          const int32_t* depth, const int32_t* rank, const int32_t* n_nodes, const float* draft_lse,
                          const void* target, const float* target_lse, const void* draft, const float* uniforms,
                          int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok, float* visited_lse,
                          int32_t* status) {
     cudaError_t e = kn6_prepare<T, RULE, CORR>(S, smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<T, RULE, CORR>, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent,
+    return cudaLaunchKernelEx(&lc.cfg, kn6_kernel<T, RULE, CORR>, corr, L, V, Mmax, chunk, nbt, pq_cap, tok, parent,
                               depth, rank, n_nodes, draft_lse, (const T*)target, target_lse, (const T*)draft,
                               uniforms, acc_nodes, acc_len, next_tok, visited_lse, status);
 }
 
 template <typename T>
 cudaError_t kn6_launch_rule(int rule, const DtLaunch& lc, size_t smem, int S, const Kn6Corr& corr, int L, int V,
-                            int Mmax, int chunk, int nbt, int pq_on, const int32_t* tok, const int32_t* parent,
+                            int Mmax, int chunk, int nbt, int pq_cap, const int32_t* tok, const int32_t* parent,
                             const int32_t* depth, const int32_t* rank, const int32_t* n_nodes,
                             const float* draft_lse, const void* target, const float* target_lse, const void* draft,
                             const float* uniforms, int32_t* acc_nodes, int32_t* acc_len, int32_t* next_tok,
                             float* visited_lse, int32_t* status) {
-#define DT_KN6_ARGS lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank, n_nodes, draft_lse, \
+#define DT_KN6_ARGS lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_cap, tok, parent, depth, rank, n_nodes, draft_lse, \
                     target, target_lse, draft, uniforms, acc_nodes, acc_len, next_tok, visited_lse, status
     switch (rule) {
         case DT_VERIFY_GREEDY: return kn6_launch_t<T, DT_VERIFY_GREEDY, false>(DT_KN6_ARGS);
@@ -873,7 +973,7 @@ cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, i
     const int esize = dtype == DT_BF16 ? 2 : 4;
     const Kn6Layout lay = kn6_layout(chunk, esize, Mmax, rule);
     const size_t smem = lay.total;
-    const int nbt = lay.nbt, pq_on = lay.pq > 0;
+    const int nbt = lay.nbt, pq_cap = lay.cap;
     DtLaunch lc(dim3(S, batch, 1), dim3(NT, 1, 1), smem, st, S);
     Kn6Corr corr{nullptr, nullptr, 0, nullptr, 0, nullptr};
     if (rule == DT_KN6_RATIO_MARKOV) {
@@ -882,10 +982,10 @@ cudaError_t dt_kn6_launch(int batch, int L, int V, int dtype, int Mmax, int S, i
         corr = Kn6Corr{prop->U, prop->Vt, prop->R, prop->z, prop->K, prop->root_tok};
     }
     if (dtype == DT_BF16)
-        return kn6_launch_rule<uint16_t>(rule, lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth,
+        return kn6_launch_rule<uint16_t>(rule, lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_cap, tok, parent, depth,
                                          rank, n_nodes, draft_lse, target, target_lse, draft, uniforms, acc_nodes,
                                          acc_len, next_tok, visited_lse, status);
-    return kn6_launch_rule<float>(rule, lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_on, tok, parent, depth, rank,
+    return kn6_launch_rule<float>(rule, lc, smem, S, corr, L, V, Mmax, chunk, nbt, pq_cap, tok, parent, depth, rank,
                                   n_nodes, draft_lse, target, target_lse, draft, uniforms, acc_nodes, acc_len,
                                   next_tok, visited_lse, status);
 }
