@@ -667,10 +667,12 @@ int or_tdes_table(const int32_t* id, int L, int K, const float* Ap, const float*
 /* lattices with non-positive edge scores, the best-first invariant with       */
 /* arbitrary signs, and DARTree without width pruning (tests).                 */
 /* ------------------------------------------------------------------------- */
-static const float* or_hs_lp;
-static const float* or_hs_E;
-static const float* or_hs_z;
-static int or_hs_K, or_hs_i, or_hs_d;
+/* The comparator's context, one copy per thread: callers may run several
+ * heaps at once on host threads. */
+static _Thread_local const float* or_hs_lp;
+static _Thread_local const float* or_hs_E;
+static _Thread_local const float* or_hs_z;
+static _Thread_local int or_hs_K, or_hs_i, or_hs_d;
 
 static float or_hs_edge(int d, int i, int j) /* d: 1-based position of the child */
 {
