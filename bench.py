@@ -43,25 +43,10 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 # comments and whitespace dropped -- when the capture was taken); a changed
 # kernel reports null until it is captured again.
 KN1_TRAFFIC = {
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta-0.5', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38962347,
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38962347,
-    ('kn1b_kernel', 'dartree_fixed_b8_L16_V151936_K64_B64', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38962432,
-    ('kn1b_kernel', 'dartree_norm_b8_L16_V151936_W32_K16_B512_beta0', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38962603,
-    ('kn1b_kernel', 'dartree_norm_t1_b8_L16_V151936_W32_K16_B512_beta0', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38969429,
-    ('kn1b_kernel', 'ddtree_saba_b16_L16_V151936_K256_Bmax256', '4a1b419d3fa04901f8af7fc5764326969e456062'): 78596864,
-    ('kn1b_kernel', 'heap_markov_b8_L16_V151936_K16_B512', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38962432,
-    ('kn1b_kernel', 'heap_markov_norm_b8_L16_V151936_K16_B512', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38962688,
-    ('kn1b_kernel', 'heap_tdes_H256_b8_L16_V151936_K16_B512', '4a1b419d3fa04901f8af7fc5764326969e456062'): 38962603,
     ('kn1_kernel', 'ddtree_b1_L16_V151936_K128_B128', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4933803,
     ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4932352,
     ('kn1_kernel', 'ddtree_b1_L16_V151936_K64_B64', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4932437,
     ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4932437,
-    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', '4a1b419d3fa04901f8af7fc5764326969e456062'): 78578176,
-    ('kn1b_kernel', 'ddtree_t1_b4_L16_V151936_K256_B256', '4a1b419d3fa04901f8af7fc5764326969e456062'): 19515051,
-    ('kn1b_kernel', 'ddtree_t1_iter_residual_b16_L16_V151936_K256_B256', '4a1b419d3fa04901f8af7fc5764326969e456062'): 78621696,
-    ('kn1b_kernel', 'ddtree_t1_target_match_b16_L16_V151936_K256_B256', '4a1b419d3fa04901f8af7fc5764326969e456062'): 78534656,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', '4a1b419d3fa04901f8af7fc5764326969e456062'): 341855744,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', '4a1b419d3fa04901f8af7fc5764326969e456062'): 314968576,
 }
 STAGE1_SOURCES = {
     "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),

@@ -136,6 +136,9 @@ CAND_CASES = [
     (6, 16, 151936, "f32", 256, 3.0, 0.7),    # many fp32 rows
     (4, 16, 300000, "f32", 64, 3.0, 0.7),     # long fp32 rows: > 32 vectors per maximum slot
     (4, 16, 10001, "bf16", 32, 3.0, 0.7),     # many rows, odd V: rows not 16-byte aligned
+    (4, 16, 10001, "bf16", 200, 3.0, 0.7),    # long lists (per-vector words), rows not 16-byte aligned
+    (5, 16, 20000, "bf16", 129, 3.0, 0.7),    # the shortest list on the per-vector words: counting rank
+    (4, 16, 300000, "bf16", 256, 3.0, 0.7),   # long bf16 rows: two vectors per word, unordered ranking
 ]
 
 
@@ -203,13 +206,14 @@ def test_candidates_edge_rows():
         assert abs(float(tree.lse[0, 3]) - math.log(2.0)) < TOL
 
 
-@pytest.mark.parametrize("batch", [6, 16])
-def test_candidates_edge_rows_among_many(batch):
+@pytest.mark.parametrize("batch,Kc", [(6, 40), (16, 40), (6, 200)])
+def test_candidates_edge_rows_among_many(batch, Kc):
     # many rows, so that CTAs or clusters run through several rows in turn;
     # edge rows (equal logits, an outlier, -inf runs) between Gaussian rows
     # switch between the candidate path and the exact fallback from one row to
-    # the next
-    L, V, Kc = 16, 20000, 40
+    # the next (Kc = 200: on the per-vector words, whose bound can list every
+    # vector of a row and overflow into several staged rounds)
+    L, V = 16, 20000
     g = torch.Generator().manual_seed(99)
     x = torch.randn((batch * L, V), generator=g) * 2
     for r in range(0, batch * L, 5):
