@@ -43,15 +43,15 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 # comments and whitespace dropped -- when the capture was taken); a changed
 # kernel reports null until it is captured again.
 KN1_TRAFFIC = {
-    ('kn1_kernel', 'ddtree_b1_L16_V151936_K128_B128', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4933803,
-    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4932352,
-    ('kn1_kernel', 'ddtree_b1_L16_V151936_K64_B64', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4932437,
-    ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', '1537b2ec13e7cd69fa895181e886d46273dce956'): 4932437,
-    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', '01e86095f055d594fe16bb9b9f3c89d13b1d17f5'): 38963456,
-    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', '01e86095f055d594fe16bb9b9f3c89d13b1d17f5'): 78302805,
-    ('kn1b_kernel', 'ddtree_t1_b4_L16_V151936_K256_B256', '01e86095f055d594fe16bb9b9f3c89d13b1d17f5'): 19515221,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', '01e86095f055d594fe16bb9b9f3c89d13b1d17f5'): 325609557,
-    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', '01e86095f055d594fe16bb9b9f3c89d13b1d17f5'): 315134293,
+    ('kn1_kernel', 'ddtree_b1_L16_V151936_K128_B128', 'cbcf81db6862727ca848226199f3ec3a09787490'): 4932437,
+    ('kn1_kernel', 'ddtree_b1_L16_V151936_K256_B256', 'cbcf81db6862727ca848226199f3ec3a09787490'): 4932523,
+    ('kn1_kernel', 'ddtree_b1_L16_V151936_K64_B64', 'cbcf81db6862727ca848226199f3ec3a09787490'): 4932608,
+    ('kn1_kernel', 'ddtree_t1_b1_L16_V151936_K256_B256', 'cbcf81db6862727ca848226199f3ec3a09787490'): 4932267,
+    ('kn1b_kernel', 'dartree_b8_L16_V151936_W32_K16_B512_beta0', 'f17fce87448e4d8e01b396ff5ed69d6396ca1699'): 38964139,
+    ('kn1b_kernel', 'ddtree_t1_b16_L16_V151936_K256_B256', 'f17fce87448e4d8e01b396ff5ed69d6396ca1699'): 78302464,
+    ('kn1b_kernel', 'ddtree_t1_b4_L16_V151936_K256_B256', 'f17fce87448e4d8e01b396ff5ed69d6396ca1699'): 19515136,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N1024', 'f17fce87448e4d8e01b396ff5ed69d6396ca1699'): 325276075,
+    ('kn1b_kernel', 'talon_b64_L16_V151936_k10_mu0.03_N60', 'f17fce87448e4d8e01b396ff5ed69d6396ca1699'): 315164501,
 }
 STAGE1_SOURCES = {
     "kn1_kernel": ("kn1_candidates.cu", "kn1_common.cuh", "dt_device.cuh"),

@@ -285,11 +285,6 @@ dt_status dt_candidates(const dt_build_params* p, const void* draft_logits, dt_t
     return cuda_status(e);
 }
 
-// Largest tree (rows) whose mask the selection kernel writes itself; larger
-// trees get the level-by-level mask kernel after the selection (measured on a
-// GB300: fused is faster for 61, 257 and 497 rows, slower for 1025).
-constexpr int kFusedMaskMaxNodes = 512;
-
 // Selection kernels, optionally also writing the tree mask and positions.
 static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspace, size_t workspace_bytes,
                              uint32_t* mask_out, int32_t* pos_out, int pos_offset, cudaStream_t st) {
@@ -297,7 +292,10 @@ static dt_status select_impl(const dt_build_params* p, dt_tree* t, void* workspa
     if (s != DT_OK) return s;
     cudaError_t e = cudaSuccess;
     const int Mmax = t->max_nodes;
-    const bool fuse = mask_out && Mmax <= kFusedMaskMaxNodes && p->mode != DT_MODE_HEAP;
+    // The DDTree, DARTree and TALON kernels write the mask rows themselves,
+    // walking parents in shared memory (dt_mask.cuh); the heap selection is
+    // followed by the level-by-level mask kernel.
+    const bool fuse = mask_out && p->mode != DT_MODE_HEAP;
     uint32_t* mask = fuse ? mask_out : nullptr;
     int32_t* pos = fuse ? pos_out : nullptr;
     switch (p->mode) {

@@ -546,51 +546,6 @@ struct DtStager {
     }
 };
 
-// Tree-attention mask rows and position ids of one request's tree, written by
-// the CTA that has just written its arrays (call after a __syncthreads): bit
-// m % 32 of word m / 32 of row n is set iff node m is n or one of its
-// ancestors; pos[n] = depth[n] + pos_offset.  Parents must precede their
-// children (true of every tree the selection kernels write), so a node's
-// ancestor chain visits words in non-increasing order: the row is zeroed, then
-// each word on the chain is written once.  A parent index that does not
-// precede its child falls back to one chain walk per word.
-template <int NT>
-DT_DI void dt_write_mask_rows(int M, int Mmax, const int32_t* par, const int32_t* dep, int pos_offset,
-                              uint32_t* mask, int32_t* pos) {
-    const int Wd = (Mmax + 31) >> 5;
-    for (int n = threadIdx.x; n < M; n += NT) {
-        uint32_t* row = mask + (size_t)n * Wd;
-        for (int w = 0; w < Wd; ++w) row[w] = 0u;
-        int w = n >> 5;
-        uint32_t bits = 1u << (n & 31);
-        bool ordered = true;
-        for (int a = par[n], prev = n; a >= 0; prev = a, a = par[a]) {
-            if (a >= prev) {
-                ordered = false;
-                break;
-            }
-            if ((a >> 5) != w) {
-                row[w] = bits;
-                w = a >> 5;
-                bits = 0u;
-            }
-            bits |= 1u << (a & 31);
-        }
-        if (ordered) {
-            row[w] = bits;
-        } else {
-            for (int q = 0; q < Wd; ++q) {
-                uint32_t word = 0u;
-                int steps = 0;
-                for (int a = n; a >= 0 && steps <= DT_MAX_L; a = par[a], ++steps)
-                    if ((a >> 5) == q) word |= 1u << (a & 31);
-                row[q] = word;
-            }
-        }
-        pos[n] = dep[n] + pos_offset;
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Shared node order on explicit node arrays (score s, depth dep, parent par,
 // lex = (lexicographic rank of the parent among its depth << 16) | own rank):

@@ -25,6 +25,7 @@
 // in shared memory.  A per-request budget (budget[b], clamped to [1, B], e.g.
 // from SABA) replaces B for that request; the buffers keep B's stride.
 #include "dt_device.cuh"
+#include "dt_mask.cuh"
 #include "dt_launch.h"
 
 namespace {
@@ -36,6 +37,8 @@ namespace {
 #endif
 constexpr int NT = DT_KN2_NT;
 constexpr int CAP = 2048;  // candidates materialised per merge
+constexpr int SMALL_M = 256;  // merges of at most this many candidates rank them without a sort
+static_assert(SMALL_M * 8 + SMALL_M * 4 * 2 <= CAP * 8, "the small-merge arrays must fit after its keys");
 
 struct Kn2Smem {
     float* lp;       // [K]
@@ -163,10 +166,14 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     S.cand[w++] = ((unsigned long long)(S.clex + cur * Bcap)[i] << 32) | (unsigned)i;
             if (tid == 0) { sh_nP = tot; sh_any = 0; }
             __syncthreads();
-            // already in lexicographic order (e.g. the depth-1 nodes)? then no sort
-            for (int i = tid; i + 1 < tot; i += NT)
-                if (S.cand[i] > S.cand[i + 1]) sh_any = 1;
-            __syncthreads();
+            // already in lexicographic order? then no sort.  The depth-1 nodes
+            // always are when each thread compacted at most one of them: their
+            // scores fall with their rank, so C holds them in rank order.
+            if (d > 2 || nC > NT) {
+                for (int i = tid; i + 1 < tot; i += NT)
+                    if (S.cand[i] > S.cand[i + 1]) sh_any = 1;
+                __syncthreads();
+            }
             if (sh_any) {
                 if (tot <= 32) {
                     dt_warp_sort_u64(S.cand, tot, false);
@@ -212,12 +219,15 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
             }
             __syncthreads();
             dt_block_scan_array<NT>(S.pn, S.pn, nP, red);
-            if (tid == 0) sh_lrhi = lr_lo + 1;
-            __syncthreads();
-            for (int j = lr_lo + 1 + tid; j <= nP; j += NT)
-                if (S.pn[j] - S.pn[lr_lo] <= CAP) atomicMax(&sh_lrhi, j);
-            __syncthreads();
-            const int lr_hi = sh_lrhi;
+            int lr_hi = nP;  // the rest of the parents, when their children fit CAP
+            if (S.pn[nP] - S.pn[lr_lo] > CAP) {  // block-uniform
+                if (tid == 0) sh_lrhi = lr_lo + 1;
+                __syncthreads();
+                for (int j = lr_lo + 1 + tid; j <= nP; j += NT)
+                    if (S.pn[j] - S.pn[lr_lo] <= CAP) atomicMax(&sh_lrhi, j);
+                __syncthreads();
+                lr_hi = sh_lrhi;
+            }
             const int base = S.pn[lr_lo];
             const int m = S.pn[lr_hi] - base;
             if (m > 0) {
@@ -237,55 +247,85 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     S.cand[idx] = ((unsigned long long)dt_fkey(s) << 32) | (unsigned long long)(0xFFFFFFFFu - lex);
                 }
                 __syncthreads();
-                if (m <= 32) {
-                    dt_warp_sort_u64(S.cand, m, true);
-                } else if (m <= 512) {
-                    dt_block_sort_u64<NT>(S.cand, m, true, S.cand + 512);
-                } else {
-                    const int P2 = dt_pow2_ceil(m);
-                    for (int i = m + tid; i < P2; i += NT) S.cand[i] = 0ull;
-                    __syncthreads();
-                    dt_bitonic_u64<NT>(S.cand, P2, true);
-                }
-                const int mm = min(m, B);
-                // merge path: new position of every C member ...
-                for (int i = tid; i < nC; i += NT) {
-                    int lo = 0, hi = mm;
+                const int nx = cur ^ 1;
+                const float* ccs = S.cs + cur * Bcap;
+                const int* ccdep = S.cdep + cur * Bcap;
+                const int* ccpar = S.cpar + cur * Bcap;
+                const uint32_t* cclex = S.clex + cur * Bcap;
+                // C members before candidate y (C is sorted, the predicate monotone)
+                auto c_before = [&](unsigned long long y) {
+                    int lo = 0, hi = nC;
                     while (lo < hi) {
-                        int mid = (lo + hi) >> 1;
-                        if (c_before_cand(i, S.cand[mid], d, (S.cs + cur * Bcap), (S.cdep + cur * Bcap), (S.cpar + cur * Bcap), (S.clex + cur * Bcap), S.pidx))
-                            hi = mid;
-                        else
-                            lo = mid + 1;
+                        const int mid = (lo + hi) >> 1;
+                        if (c_before_cand(mid, y, d, ccs, ccdep, ccpar, cclex, S.pidx)) lo = mid + 1;
+                        else hi = mid;
                     }
-                    const int nr = i + lo;
-                    S.newpos[i] = nr < B ? nr : -1;
+                    return lo;
+                };
+                // a candidate's new position: its rank among the candidates plus
+                // the C members before it
+                int* cpos = (int*)(S.cand + SMALL_M);  // [SMALL_M] C members before candidate q
+                int* cfin = cpos + SMALL_M;           // [SMALL_M] its position in the merged order
+                if (m <= SMALL_M) {
+                    // no sort: rank each candidate against all (keys are
+                    // distinct), and move C member i by the candidates placed
+                    // before it
+                    for (int q = tid; q < m; q += NT) {
+                        const unsigned long long y = S.cand[q];
+                        int r = 0;
+                        for (int q2 = 0; q2 < m; ++q2) r += (S.cand[q2] > y);
+                        const int lo = c_before(y);
+                        cpos[q] = lo;
+                        cfin[q] = r + lo;
+                    }
+                    __syncthreads();
+                    for (int i = tid; i < nC; i += NT) {
+                        int before = 0;
+                        for (int q = 0; q < m; ++q) before += (cpos[q] <= i);
+                        const int nr = i + before;
+                        S.newpos[i] = nr < B ? nr : -1;
+                    }
+                } else {
+                    if (m <= 512) {
+                        dt_block_sort_u64<NT>(S.cand, m, true, S.cand + 512);
+                    } else {
+                        const int P2 = dt_pow2_ceil(m);
+                        for (int i = m + tid; i < P2; i += NT) S.cand[i] = 0ull;
+                        __syncthreads();
+                        dt_bitonic_u64<NT>(S.cand, P2, true);
+                    }
+                    const int mm = min(m, B);
+                    // merge path: new position of every C member ...
+                    for (int i = tid; i < nC; i += NT) {
+                        int lo = 0, hi = mm;
+                        while (lo < hi) {
+                            int mid = (lo + hi) >> 1;
+                            if (c_before_cand(i, S.cand[mid], d, ccs, ccdep, ccpar, cclex, S.pidx))
+                                hi = mid;
+                            else
+                                lo = mid + 1;
+                        }
+                        const int nr = i + lo;
+                        S.newpos[i] = nr < B ? nr : -1;
+                    }
                 }
                 __syncthreads();
-                const int nx = cur ^ 1;
                 for (int i = tid; i < nC; i += NT) {
                     const int np = S.newpos[i];
                     if (np >= 0) {
-                        const int pp = (S.cpar + cur * Bcap)[i];
-                        (S.cs + nx * Bcap)[np] = (S.cs + cur * Bcap)[i];
+                        const int pp = ccpar[i];
+                        (S.cs + nx * Bcap)[np] = ccs[i];
                         (S.cpar + nx * Bcap)[np] = pp < 0 ? -1 : S.newpos[pp];
                         (S.crank + nx * Bcap)[np] = (S.crank + cur * Bcap)[i];
-                        (S.cdep + nx * Bcap)[np] = (S.cdep + cur * Bcap)[i];
-                        (S.clex + nx * Bcap)[np] = (S.clex + cur * Bcap)[i];
+                        (S.cdep + nx * Bcap)[np] = ccdep[i];
+                        (S.clex + nx * Bcap)[np] = cclex[i];
                     }
                 }
-                // ... and of every candidate
-                for (int q = tid; q < mm; q += NT) {
+                // ... and of every candidate that still enters
+                const int mq = m <= SMALL_M ? m : min(m, B);
+                for (int q = tid; q < mq; q += NT) {
                     const unsigned long long y = S.cand[q];
-                    int lo = 0, hi = nC;
-                    while (lo < hi) {
-                        int mid = (lo + hi) >> 1;
-                        if (c_before_cand(mid, y, d, (S.cs + cur * Bcap), (S.cdep + cur * Bcap), (S.cpar + cur * Bcap), (S.clex + cur * Bcap), S.pidx))
-                            lo = mid + 1;
-                        else
-                            hi = mid;
-                    }
-                    const int nr = q + lo;
+                    const int nr = m <= SMALL_M ? cfin[q] : q + c_before(y);
                     if (nr < B) {
                         const uint32_t lex = 0xFFFFFFFFu - (uint32_t)y;
                         const int j = (int)(lex >> 16);
@@ -301,7 +341,7 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
                     const int p = S.pidx[j];
                     if (p >= 0) S.pidx[j] = S.newpos[p];
                 }
-                nC = min(B, nC + mm);
+                nC = min(B, nC + m);
                 cur = nx;
                 __syncthreads();
             }
@@ -326,8 +366,10 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
         o_dep[ob + i + 1] = dd;
         o_rank[ob + i + 1] = rr;
         o_score[ob + i + 1] = (S.cs + cur * Bcap)[i];
+        if (o_mask) o_pos[ob + i + 1] = dd + pos_offset;
     }
     if (tid == 0) {
+        if (o_mask) o_pos[ob] = pos_offset;
         o_tok[ob] = -1;
         o_par[ob] = -1;
         o_dep[ob] = 0;
@@ -341,10 +383,10 @@ __global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_
         }
         status[b] = bits;
     }
-    if (o_mask) {  // fused tree mask and positions
-        __syncthreads();
-        dt_write_mask_rows<NT>(nC + 1, Mmax, o_par + ob, o_dep + ob, pos_offset,
-                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5), o_pos + ob);
+    if (o_mask) {  // fused tree mask (positions above): parents from C in shared memory
+        const int* cpar = S.cpar + cur * Bcap;
+        dt_write_mask_rows<NT>(nC + 1, Mmax, [&](int a) { return a == 0 ? -1 : cpar[a - 1] + 1; },
+                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5));
     }
 }
 

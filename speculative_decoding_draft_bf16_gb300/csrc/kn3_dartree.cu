@@ -23,6 +23,7 @@
 // first B mod L depths (the shallowest), instead of W; the widths sum to B, so
 // the final pruning keeps all of S.
 #include "dt_device.cuh"
+#include "dt_mask.cuh"
 #include "dt_launch.h"
 
 namespace {
@@ -349,8 +350,10 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
         o_dep[ob + q + 1] = dd;
         o_rank[ob + q + 1] = rr;
         o_score[ob + q + 1] = S.s[x];
+        if (o_mask) o_pos[ob + q + 1] = dd + pos_offset;
     }
     if (tid == 0) {
+        if (o_mask) o_pos[ob] = pos_offset;
         o_tok[ob] = -1;
         o_par[ob] = -1;
         o_dep[ob] = 0;
@@ -369,10 +372,14 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
                 if (S.zs[i] != S.zs[i]) bits |= DT_DEV_TIMEOUT;  // the normaliser kernel flagged this row
         status[b] = bits;
     }
-    if (o_mask) {  // fused tree mask and positions
-        __syncthreads();
-        dt_write_mask_rows<NT>(nOut + 1, Mmax, o_par + ob, o_dep + ob, pos_offset,
-                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5), o_pos + ob);
+    if (o_mask) {  // fused tree mask (positions above): parents through the output map in shared memory
+        dt_write_mask_rows<NT>(nOut + 1, Mmax,
+                               [&](int a) {
+                                   if (a == 0) return -1;
+                                   const int p = S.par[S.order[a - 1]];
+                                   return p < 0 ? 0 : S.cstart[p];
+                               },
+                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5));
     }
 }
 

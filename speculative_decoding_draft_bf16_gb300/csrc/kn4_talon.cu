@@ -20,6 +20,7 @@
 // top list + group, bitonic sort), pruning later groups by the running cutoff.
 // The finished tree is sorted once in the shared node order.
 #include "dt_device.cuh"
+#include "dt_mask.cuh"
 #include "dt_launch.h"
 
 namespace {
@@ -223,8 +224,10 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
         o_dep[ob + q + 1] = dd;
         o_rank[ob + q + 1] = rr;
         o_score[ob + q + 1] = S.s[x];
+        if (o_mask) o_pos[ob + q + 1] = dd + pos_offset;
     }
     if (tid == 0) {
+        if (o_mask) o_pos[ob] = pos_offset;
         o_tok[ob] = -1;
         o_par[ob] = -1;
         o_dep[ob] = 0;
@@ -238,10 +241,14 @@ __global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, flo
         }
         status[b] = bits;
     }
-    if (o_mask) {  // fused tree mask and positions
-        __syncthreads();
-        dt_write_mask_rows<NT>(nT + 1, Mmax, o_par + ob, o_dep + ob, pos_offset,
-                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5), o_pos + ob);
+    if (o_mask) {  // fused tree mask (positions above): parents through the output map in shared memory
+        dt_write_mask_rows<NT>(nT + 1, Mmax,
+                               [&](int a) {
+                                   if (a == 0) return -1;
+                                   const int p = S.par[S.ord[a - 1]];
+                                   return p < 0 ? 0 : S.pn[p];
+                               },
+                               o_mask + (size_t)b * Mmax * ((Mmax + 31) >> 5));
     }
 }
 

@@ -259,6 +259,7 @@ DD_CASES = [
     (2, 2, 400, "bf16", 8, 1024, 3.0, 0.7),    # B far above |S_K|
     (1, 6, 4000, "bf16", 256, 1024, 0.3, 0.0),  # largest budget, many candidates per depth
     (2, 16, 2000, "bf16", 16, 300, 0.05, 0.0),  # nearly uniform rows: massive score ties
+    (1, 4, 3000, "bf16", 512, 600, 0.3, 0.0),   # more depth-1 nodes than threads: parents re-sorted
 ]
 
 
@@ -680,7 +681,7 @@ def test_fused_mask_equals_mask_kernel(mode):
                          U=U, Vt=Vt)
     elif mode == "talon":
         p = dtree.Params(mode="talon", batch=batch, L=L, V=V, dtype="bf16", talon_k=6, mu=0.05, N=90)
-    else:  # more than 512 rows: the mask kernel runs after the selection
+    else:  # more than 512 rows: mask rows of 22 words
         p = dtree.Params(mode="talon", batch=batch, L=L, V=V, dtype="bf16", talon_k=10, mu=0.01, N=700)
     max_nodes = min(p.B, p.W * L) + 1 if mode == "dartree" else p.budget + 1
     ws = dtree.make_workspace(p)
