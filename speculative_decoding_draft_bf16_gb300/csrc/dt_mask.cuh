@@ -10,11 +10,12 @@
 // index (-1 for the root, node 0) from shared memory, so walking a chain costs
 // shared-memory latency only.  The M rows are zeroed first with coalesced
 // stores; after a barrier each thread walks its rows' chains.  Parents precede
-// their children (true of every tree the selection kernels write), so a
-// chain visits words in non-increasing order and each nonzero word is stored
-// once; a parent index that does not precede its child switches that row to
-// atomic ORs.  Chains are cut after DT_MAX_L + 1 nodes.  Block-uniform;
-// contains one __syncthreads.
+// their children in every tree the selection kernels write, so a chain visits
+// words in non-increasing order and each nonzero word is stored once; a
+// parent index that does not precede its child (a tree built from non-finite
+// scores, which the status reports) ends the chain there, so that no index
+// outside the tree is ever followed.  Block-uniform; contains one
+// __syncthreads.
 template <int NT, typename ParentOf>
 DT_DI void dt_write_mask_rows(int M, int Mmax, ParentOf parent_of, uint32_t* mask) {
     const int Wd = (Mmax + 31) >> 5;
@@ -24,13 +25,7 @@ DT_DI void dt_write_mask_rows(int M, int Mmax, ParentOf parent_of, uint32_t* mas
         uint32_t* row = mask + (size_t)n * Wd;
         int w = n >> 5;
         uint32_t bits = 1u << (n & 31);
-        bool ordered = true;
-        int a = parent_of(n);
-        for (int prev = n, steps = 1; a >= 0 && steps <= DT_MAX_L; prev = a, a = parent_of(a), ++steps) {
-            if (a >= prev) {
-                ordered = false;
-                break;
-            }
+        for (int prev = n, a = parent_of(n); a >= 0 && a < prev; prev = a, a = parent_of(a)) {
             if ((a >> 5) != w) {
                 row[w] = bits;
                 w = a >> 5;
@@ -38,12 +33,6 @@ DT_DI void dt_write_mask_rows(int M, int Mmax, ParentOf parent_of, uint32_t* mas
             }
             bits |= 1u << (a & 31);
         }
-        if (ordered) {
-            row[w] = bits;
-        } else {
-            atomicOr(&row[w], bits);
-            for (int steps = 0; a >= 0 && steps <= DT_MAX_L; a = parent_of(a), ++steps)
-                atomicOr(&row[a >> 5], 1u << (a & 31));
-        }
+        row[w] = bits;
     }
 }

@@ -77,9 +77,9 @@ DT_DI Kn2Smem carve(unsigned char* s, int L, int K, int B) {
 // Does C node i precede the depth-d candidate with key y?
 DT_DI bool c_before_cand(int i, unsigned long long y, int d, const float* cs, const int* cdep, const int* cpar,
                          const uint32_t* clex, const int* pidx) {
-    const float sy = dt_fkey_val((uint32_t)(y >> 32));
-    const float si = cs[i];
-    if (si != sy) return si > sy;
+    // score keys, not floats: a strict total order even for NaN scores
+    const uint32_t ky = (uint32_t)(y >> 32), ki = dt_fkey(cs[i]);
+    if (ki != ky) return ki > ky;
     const uint32_t ly = 0xFFFFFFFFu - (uint32_t)y;
     const int e = cdep[i];
     if (e == d) return clex[i] < ly;
@@ -89,7 +89,7 @@ DT_DI bool c_before_cand(int i, unsigned long long y, int d, const float* cs, co
     return clex[i] < clex[a];
 }
 
-__global__ void __launch_bounds__(NT) kn2_kernel(const float* __restrict__ cand_lp,
+__global__ void __launch_bounds__(NT, 1) kn2_kernel(const float* __restrict__ cand_lp,
                                                  const int32_t* __restrict__ cand_id,
                                                  const float* __restrict__ lse, int L, int K, int Bcap,
                                                  const int32_t* __restrict__ budget, int Mmax,

@@ -130,7 +130,19 @@ DT_DI Kn3Smem kn3_carve(unsigned char* p, int L, int K, int W, bool stage_tab) {
     return m;
 }
 
-__global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int wfix, int B, float beta, int use_table,
+// The node order made total for any scores: scores compare by their order
+// keys (so a NaN has a place), equal keys by dt_node_before, and a pair that
+// neither precedes (only NaN scores do that) by node index.  For finite
+// scores it is dt_node_before.
+DT_DI bool node_before_total(int y, int x, const float* s, const int* dep, const int* par, const uint32_t* lex) {
+    const uint32_t ky = dt_fkey(s[y]), kx = dt_fkey(s[x]);
+    if (ky != kx) return ky > kx;
+    if (dt_node_before(y, x, s, dep, par, lex)) return true;
+    if (dt_node_before(x, y, s, dep, par, lex)) return false;
+    return y < x;
+}
+
+__global__ void __launch_bounds__(NT, 1) kn3_select_kernel(int L, int K, int W, int wfix, int B, float beta, int use_table,
                                                         const int32_t* __restrict__ root_tok, int V,
                                                         int Mmax, const float* __restrict__ cand_lp,
                                                         const int32_t* __restrict__ cand_id,
@@ -249,29 +261,74 @@ __global__ void __launch_bounds__(NT) kn3_select_kernel(int L, int K, int W, int
     }
     __syncthreads();
 
-    // edges whose child outscores its parent (Lemma 1 needs none)
-    for (int x = tid; x < nS; x += NT) {
-        const int p = S.par[x];
-        const float sp = p < 0 ? 0.f : S.s[p];
-        if (S.s[x] > sp) atomicAdd(&sh_viol, 1);
-    }
-    // rank of every node in the shared order: merge of the per-depth sorted layers
-    for (int x = tid; x < nS; x += NT) {
-        const int dx = S.dep[x];
-        int g = x - lay_start[dx - 1];
-        for (int e = 1; e <= L; ++e) {
-            if (e == dx) continue;
-            int lo = lay_start[e - 1], hi = lay_start[e];
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (dt_node_before(mid, x, S.s, S.dep, S.par, S.lex)) lo = mid + 1;
-                else hi = mid;
-            }
-            g += lo - lay_start[e - 1];
+    // edges whose child outscores its parent (Lemma 1 needs none); counted
+    // per warp first -- hundreds of atomics on one word would serialise
+    {
+        int nv = 0;
+        for (int x = tid; x < nS; x += NT) {
+            const int p = S.par[x];
+            const float sp = p < 0 ? 0.f : S.s[p];
+            nv += S.s[x] > sp;
         }
-        S.grank[x] = g;
+        nv = dt_warp_sum_i(nv);
+        if ((tid & 31) == 0 && nv) atomicAdd(&sh_viol, nv);
     }
-    __syncthreads();
+    // rank of every node in the shared order: a merge tree over the per-depth
+    // layers, each sorted in that order and stored contiguously.  At level l
+    // lists of 2^l layers merge pairwise: an element's place in the merged
+    // list is its place in its own list plus the partner list's elements
+    // before it (one binary search; score keys decide unless equal, then the
+    // full node order).  cur[p] is the node at position p; the merged lists
+    // keep the layers' position ranges.
+    {
+        int* cur = S.order;
+        int* nxt = S.clist;
+        for (int x = tid; x < nS; x += NT) cur[x] = x;
+        __syncthreads();
+        // a strict total order whatever the scores (NaN included): positions
+        // of the merged lists are then a permutation
+        auto before = [&](int y, int x, uint32_t kx) {
+            const uint32_t ky = dt_fkey(S.s[y]);
+            if (ky != kx) return ky > kx;
+            return node_before_total(y, x, S.s, S.dep, S.par, S.lex);
+        };
+        // (an entry is read clamped into [0, nS): a defence that keeps every
+        // index inside the tree should the order ever not be total)
+        auto node_at = [&](int q) { const int v = cur[q]; return (unsigned)v < (unsigned)nS ? v : 0; };
+        for (int w = 1; w < L; w <<= 1) {  // list width in layers
+            for (int p = tid; p < nS; p += NT) {
+                const int x = node_at(p);
+                const uint32_t kx = dt_fkey(S.s[x]);
+                const int li = (S.dep[x] - 1) / w;  // list index
+                const int A = li & ~1;              // the pair's first list
+                const int a0 = lay_start[min(A * w, L)], b0 = lay_start[min((A + 1) * w, L)];
+                const int b1 = lay_start[min((A + 2) * w, L)];
+                int lo, hi;
+                if (li == A) {
+                    lo = b0;
+                    hi = b1;
+                } else {
+                    lo = a0;
+                    hi = b0;
+                }
+                const int base = lo;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (before(node_at(mid), x, kx)) lo = mid + 1;
+                    else hi = mid;
+                }
+                const int j = lo - base;
+                const int np = li == A ? p + j : p - (b0 - a0) + j;
+                if ((unsigned)np < (unsigned)nS) nxt[np] = x;
+            }
+            __syncthreads();
+            int* t = cur;
+            cur = nxt;
+            nxt = t;
+        }
+        for (int p = tid; p < nS; p += NT) S.grank[node_at(p)] = p;
+        __syncthreads();
+    }
     const int nT = min(B, nS);
     for (int x = tid; x < nS; x += NT) {
         const int g = S.grank[x];

@@ -73,7 +73,7 @@ DT_DI int find_parent(const int* pn, int lo, int hi, int g) {
     return lo;
 }
 
-__global__ void __launch_bounds__(NT) kn4_kernel(int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
+__global__ void __launch_bounds__(NT, 1) kn4_kernel(int L, int Kc, int talon_k, float log_mu, int N, int Mmax,
                                                  const float* __restrict__ cand_lp,
                                                  const int32_t* __restrict__ cand_id, const float* __restrict__ lse,
                                                  int32_t* __restrict__ o_tok, int32_t* __restrict__ o_par,

@@ -156,7 +156,7 @@ DT_DI bool entry_before(const Kn7Smem& S, int a, float sa, int b, float sb) {
     return desc_less(S, S.fe[a].x, S.fe[a].y & 0xFFFF, S.fe[b].x, S.fe[b].y & 0xFFFF);
 }
 
-__global__ void __launch_bounds__(NT7) kn7_kernel(int L, int V, int K, int B, const int32_t* __restrict__ budget,
+__global__ void __launch_bounds__(NT7, 1) kn7_kernel(int L, int V, int K, int B, const int32_t* __restrict__ budget,
                                                   int Mmax,
                                                   const float* __restrict__ cand_lp,
                                                   const int32_t* __restrict__ cand_id,
