@@ -19,3 +19,12 @@ def test_every_traffic_entry_matches_the_current_sources():
     for (kernel, workload, h), v in bench.KN1_TRAFFIC.items():
         assert h == hashes[kernel], (kernel, workload)
         assert v > 0 and workload in names, (kernel, workload)
+
+
+def test_the_default_bench_line_carries_stage1_traffic():
+    # the default workload (one request, 16 rows) runs the cluster stage-1
+    # kernel; its DRAM counters must be on record for the current sources, or
+    # the bench line's roofline.traffic would be null
+    wl = bench.workloads()["single_request_B256"]
+    key = ("kn1_kernel", wl.name, bench.stage1_source_hash("kn1_kernel"))
+    assert bench.KN1_TRAFFIC.get(key, 0) > 0
