@@ -43,6 +43,16 @@
  *    per-request status word (dt_tree.status), readable after the stream
  *    synchronises; see DT_DEV_*.
  *  - A launch failure returns DT_ERR_CUDA (cudaGetLastError is consumed).
+ *  - So there are three host error codes: a missing or short workspace is
+ *    DT_ERR_INVALID_ARG like any other bad argument, while an invalid tree and
+ *    a wait that ran out, which only the device sees, are the status bits
+ *    DT_DEV_BAD_TREE and DT_DEV_TIMEOUT rather than return codes.
+ *  - dt_tree.rank holds each node's own candidate rank; its full rank
+ *    descriptor is the ranks along its parent chain.
+ *  - The walk's rules are split over three calls: dt_verify (greedy, or the
+ *    T=1 ratio rule with one normalised residual), dt_verify_rule (one
+ *    residual per rejected sibling, or target-sample matching) and
+ *    dt_verify_markov (T=1 against the normalised DARTree proposal).
  * Limits: L <= 32, V <= DT_MAX_V, candidate list Kc <= 1024, nodes per
  * request (incl. the root) <= 1025.
  */
